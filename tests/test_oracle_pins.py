@@ -1,0 +1,360 @@
+"""Pins of the CPU oracle to things other than itself (CPU only).
+
+Each pin is chosen so that a plausible mistake in the oracle fails it:
+  * hand-derived integer fixtures (tests/golden/ring_window_cases.json) for the
+    key list, the window bounds, the prep and commit ring slots and the meta
+    update (off-by-one in the window, wrong modulus, wrong head advance);
+  * closed forms of the rotation (sign, pairing e <-> e + hd/2, frequency of the
+    first pair and of pair hd/4), of the unit norm (eps inside the root of the
+    sum), of a two-key softmax, of a one-key window and of uniform scores;
+  * a library attention routine (torch scaled_dot_product_attention in float64
+    with an explicit sliding-window mask) on a materialised logical sequence;
+  * invariants: softmax weights sum to 1, ring-rotation invariance, a t-row
+    chunk equals t single-row steps with commits, the RoPE relative-position
+    identity.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import expit
+
+import oracle
+import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "ring_window_cases.json")
+
+
+def _cases():
+    with open(GOLDEN) as f:
+        return json.load(f)["cases"]
+
+
+# ---------------------------------------------------------------------------
+# integer fixtures
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c["name"])
+def test_key_lists_and_windows_match_hand_derivation(case):
+    meta_b = np.array(case["meta"])
+    for row in case["rows"]:
+        lo, hi = oracle.row_window(meta_b, row["i"], case["cap"])
+        assert (lo, hi) == (row["lo"], row["hi"])
+        keys = oracle.row_key_list(meta_b, row["i"], case["ns"], case["cap"])
+        assert [[k, int(v)] for k, v in keys] == row["keys"]
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c["name"])
+def test_commit_slots_ring_and_meta_match_hand_derivation(case):
+    meta_b = np.array(case["meta"])
+    t, cap = case["t"], case["cap"]
+    slots = [oracle.commit_slot(meta_b, j, cap) for j in range(t)]
+    assert slots == case["commit_slots"]
+    # Tag each chunk row's key with its row index to read back the final ring.
+    ring = np.full((1, 1, cap, 1), -1.0)
+    kc = np.arange(t, dtype=np.float64).reshape(1, t, 1, 1)
+    rk, rv, new_meta = oracle.commit(meta_b.reshape(1, 4), ring, ring, kc, kc)
+    expect = np.full(cap, -1.0)
+    for slot, row in case["final_ring"].items():
+        expect[int(slot)] = row
+    np.testing.assert_array_equal(rk[0, 0, :, 0], expect)
+    np.testing.assert_array_equal(rv[0, 0, :, 0], expect)
+    assert new_meta[0].tolist() == case["meta_after"]
+
+
+@pytest.mark.parametrize("case", _cases(), ids=lambda c: c["name"])
+def test_prep_slots_match_hand_derivation(case):
+    slots = [oracle.prep_ring_slot(case["pos0"], j, case["cap"]) for j in range(case["t"])]
+    assert slots == case["prep_slots"]
+
+
+# ---------------------------------------------------------------------------
+# rotation and unit heads
+# ---------------------------------------------------------------------------
+def test_rope_table_closed_forms():
+    hd, theta = 64, 10000.0
+    pos0 = np.array([0, 7, 12345])
+    tab = oracle.rope_table(pos0, 3, hd, theta)
+    half = hd // 2
+    # position 0: the identity rotation
+    np.testing.assert_array_equal(tab[0, 0, :half], np.ones(half))
+    np.testing.assert_array_equal(tab[0, 0, half:], np.zeros(half))
+    for b, p0 in enumerate(pos0):
+        for j in range(3):
+            pos = int(p0) + j
+            # pair 0 turns by pos radians; pair hd/4 by pos / sqrt(theta) = pos / 100
+            assert tab[b, j, 0] == pytest.approx(math.cos(pos), abs=1e-12)
+            assert tab[b, j, half] == pytest.approx(math.sin(pos), abs=1e-12)
+            assert tab[b, j, hd // 4] == pytest.approx(math.cos(pos / 100.0), abs=1e-12)
+            assert tab[b, j, half + hd // 4] == pytest.approx(math.sin(pos / 100.0), abs=1e-12)
+    # frequencies fall with the pair index
+    ang = np.arctan2(oracle.rope_table(np.array([1]), 1, hd, theta)[0, 0, half:],
+                     oracle.rope_table(np.array([1]), 1, hd, theta)[0, 0, :half])
+    assert np.all(np.diff(ang) < 0)
+
+
+def test_rotation_sign_and_pairing():
+    hd = 8
+    c = np.cos(np.array([0.3, 0.5, 0.7, 0.9]))
+    s = np.sin(np.array([0.3, 0.5, 0.7, 0.9]))
+    x = np.zeros(hd)
+    x[1] = 1.0            # first half, pair 1
+    r = oracle.rotate_head(x, c, s)
+    expect = np.zeros(hd)
+    expect[1] = c[1]
+    expect[1 + hd // 2] = s[1]   # a rotation by +angle of (1, 0)
+    np.testing.assert_allclose(r, expect, atol=1e-15)
+    y = np.zeros(hd)
+    y[1 + hd // 2] = 1.0  # second half of pair 1
+    r = oracle.rotate_head(y, c, s)
+    expect = np.zeros(hd)
+    expect[1] = -s[1]
+    expect[1 + hd // 2] = c[1]
+    np.testing.assert_allclose(r, expect, atol=1e-15)
+
+
+def test_rope_relative_position_identity():
+    rng = np.random.default_rng(5)
+    hd = 32
+    a = rng.standard_normal(hd)
+    k = rng.standard_normal(hd)
+    tab = oracle.rope_table(np.array([0]), 40, hd)
+    half = hd // 2
+
+    def rot(v, p):
+        return oracle.rotate_head(v, tab[0, p, :half], tab[0, p, half:])
+
+    for p, q in [(9, 4), (30, 25), (17, 12)]:
+        assert np.dot(rot(a, p), rot(k, q)) == pytest.approx(np.dot(rot(a, p - q), k), rel=1e-12)
+    # rotation preserves the norm
+    assert np.linalg.norm(rot(a, 33)) == pytest.approx(np.linalg.norm(a), rel=1e-12)
+
+
+def test_unit_norm_puts_eps_inside_root_of_sum():
+    rng = np.random.default_rng(1)
+    v = rng.standard_normal(64)
+    S = float(np.sum(v * v))
+    # eps == S halves the squared norm: |v|^2 / (S + eps) = 1/2
+    assert np.sum(oracle.unit_head(v, S) ** 2) == pytest.approx(0.5, rel=1e-12)
+    assert np.sum(oracle.unit_head(v, 1e-6) ** 2) == pytest.approx(S / (S + 1e-6), rel=1e-12)
+
+
+def test_prep_norms_scale_and_value_copy():
+    w = workloads.custom(B=2, t=3, nh=4, nk=2, hd=32, window=8, cap=8, pos_lo=5)
+    inp = workloads.make_inputs(w)
+    rope = oracle.rope_table(inp["pos0"].numpy(), w.t, w.hd)
+    eps = 1e-6
+    q, k, v = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope,
+                          inp["q_scale"].numpy(), eps)
+    S_k = np.sum(inp["yk"].numpy().astype(np.float64) ** 2, axis=-1)
+    np.testing.assert_allclose(np.sum(k * k, axis=-1), S_k / (S_k + eps), rtol=1e-12)
+    S_q = np.sum(inp["yq"].numpy().astype(np.float64) ** 2, axis=-1)
+    q_unscaled = q / inp["q_scale"].numpy().astype(np.float64)[None, None]
+    np.testing.assert_allclose(np.sum(q_unscaled ** 2, axis=-1), S_q / (S_q + eps), rtol=1e-12)
+    np.testing.assert_array_equal(v, inp["yv"].numpy().astype(np.float64))
+    # a one-hot query scale keeps exactly that feature
+    sq = np.zeros((w.nh, w.hd))
+    sq[:, 3] = 2.0
+    q1, _, _ = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope, sq, eps)
+    assert np.count_nonzero(q1[..., np.arange(w.hd) != 3]) == 0
+    np.testing.assert_allclose(q1[..., 3], 2.0 * q_unscaled[..., 3], rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# attention: closed forms
+# ---------------------------------------------------------------------------
+def _attend_inputs(w, inp, q=None):
+    """Oracle attend inputs from the generator's tensors (q from prep unless given)."""
+    rope = oracle.rope_table(inp["pos0"].numpy(), w.t, w.hd, w.theta)
+    qh, kh, vv = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope,
+                             inp["q_scale"].numpy(), w.eps)
+    return {
+        "meta": inp["meta"].numpy(),
+        "q": qh if q is None else q,
+        "k_chunk": kh, "v_chunk": vv,
+        "ring_k": inp["ring_k"].numpy().astype(np.float64),
+        "ring_v": inp["ring_v"].numpy().astype(np.float64),
+        "sink_k": inp["sink_k"].numpy().astype(np.float64),
+        "sink_v": inp["sink_v"].numpy().astype(np.float64),
+        "gate": inp["gate"].numpy().astype(np.float64),
+        "gate_scale": inp["gate_scale"].numpy().astype(np.float64),
+    }
+
+
+def test_two_key_softmax_closed_form():
+    hd = 4
+    inp = {
+        "meta": np.array([[0, 0, 0, 1]]),
+        "q": np.array([[[[math.log(3.0), 0, 0, 0]]]]),
+        "k_chunk": np.zeros((1, 1, 1, hd)),
+        "v_chunk": np.array([[[[0.0, 4.0, 0.0, 8.0]]]]),
+        "ring_k": np.zeros((1, 1, 1, hd)), "ring_v": np.zeros((1, 1, 1, hd)),
+        "sink_k": np.array([[[[1.0, 0, 0, 0]]]]),
+        "sink_v": np.array([[[[4.0, 0.0, 8.0, 0.0]]]]),
+        "gate": np.array([[[[0.0, 0.0, 1.0, -1.0]]]]),
+        "gate_scale": np.array([[1.0, 2.0, 2.0, 2.0]]),
+    }
+    out = oracle.attend(inp, scale=1.0, hpg=1)
+    # weights 3/4 (sink, score ln 3) and 1/4 (chunk row, score 0)
+    o = np.array([3.0, 1.0, 6.0, 2.0])
+    gate = np.array([0.5, 0.5, expit(2.0), expit(-2.0)])
+    np.testing.assert_allclose(out[0, 0, 0], o * gate, rtol=1e-14)
+
+
+def test_one_key_window_returns_gated_value():
+    w = workloads.custom(B=2, t=3, nh=8, nk=2, hd=16, window=1, cap=1, ns=0, pos_lo=9)
+    inp = workloads.make_inputs(w)
+    a = _attend_inputs(w, inp)
+    out = oracle.attend(a, w.score_scale, w.hpg)
+    for b in range(w.B):
+        for i in range(w.t):
+            for h in range(w.nh):
+                expect = a["v_chunk"][b, i, h // w.hpg] * expit(a["gate"][b, i, h] * a["gate_scale"][h])
+                np.testing.assert_allclose(out[b, i, h], expect, rtol=1e-13, atol=1e-15)
+
+
+def _textbook_masked_attention(w, a):
+    """Materialise each sequence's logical keys (ring un-rotated, then the chunk),
+    build the sliding-window causal mask position-wise, and run torch's
+    scaled_dot_product_attention in float64."""
+    B, t, nh, hd = a["q"].shape
+    out = np.zeros_like(a["q"])
+    for b in range(B):
+        len0, head0, _, wf = (int(x) for x in a["meta"][b])
+        W = wf if wf else a["ring_k"].shape[2]
+        ring_k = np.stack([a["ring_k"][b, :, (head0 + x) % W] for x in range(len0)], 1) \
+            if len0 else np.zeros((w.nk, 0, hd))
+        ring_v = np.stack([a["ring_v"][b, :, (head0 + x) % W] for x in range(len0)], 1) \
+            if len0 else np.zeros((w.nk, 0, hd))
+        seq_k = np.concatenate([a["sink_k"][b], ring_k, a["k_chunk"][b].transpose(1, 0, 2)], 1)
+        seq_v = np.concatenate([a["sink_v"][b], ring_v, a["v_chunk"][b].transpose(1, 0, 2)], 1)
+        n = seq_k.shape[1]
+        mask = np.zeros((t, n), dtype=bool)
+        for i in range(t):
+            qpos = len0 + i          # logical position of row i
+            for col in range(n):
+                if col < w.ns:
+                    mask[i, col] = True
+                else:
+                    kpos = col - w.ns
+                    mask[i, col] = kpos <= qpos and qpos - kpos < W
+        for h in range(nh):
+            g = h // w.hpg
+            q = torch.tensor(a["q"][b, :, h][None, None])           # [1,1,t,hd]
+            k = torch.tensor(seq_k[g][None, None])
+            v = torch.tensor(seq_v[g][None, None])
+            o = torch.nn.functional.scaled_dot_product_attention(
+                q, k, v, attn_mask=torch.tensor(mask)[None, None], scale=w.score_scale)
+            gate = expit(a["gate"][b, :, h] * a["gate_scale"][h][None])
+            out[b, :, h] = o[0, 0].numpy() * gate
+    return out
+
+
+SDPA_CASES = [
+    dict(B=2, t=1, nh=8, nk=2, hd=16, window=12, cap=12, ns=0, pos_mode="fixed", pos_lo=29),
+    dict(B=3, t=4, nh=6, nk=2, hd=8, window=10, cap=10, ns=2, pos_mode="partial", pos_lo=1, pos_hi=10),
+    dict(B=2, t=7, nh=4, nk=1, hd=8, window=5, cap=5, ns=1, pos_mode="prompt", pos_lo=0, pos_hi=9),
+    dict(B=2, t=9, nh=4, nk=2, hd=8, window=3, cap=3, ns=3, pos_mode="full", pos_lo=3, pos_hi=40),
+    dict(B=1, t=5, nh=2, nk=2, hd=4, window=16, cap=16, ns=0, pos_mode="fixed", pos_lo=0),
+]
+
+
+@pytest.mark.parametrize("kw", SDPA_CASES)
+@pytest.mark.parametrize("sharp", [False, True])
+def test_attend_matches_library_attention_on_materialised_sequence(kw, sharp):
+    w = workloads.custom(scale=3.0 if sharp else None, **kw)
+    inp = workloads.make_inputs(w)
+    a = _attend_inputs(w, inp)
+    out = oracle.attend(a, w.score_scale, w.hpg)
+    ref = _textbook_masked_attention(w, a)
+    np.testing.assert_allclose(out, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_softmax_weights_sum_to_one_and_follow_scores():
+    w = workloads.custom(B=1, t=3, nh=4, nk=1, hd=16, window=9, cap=9, ns=2, pos_mode="full",
+                         pos_lo=9, pos_hi=30, scale=2.0)
+    a = _attend_inputs(w, workloads.make_inputs(w))
+    for i in range(w.t):
+        for h in range(w.nh):
+            _, p, keys = oracle.attend_row(0, i, h, a, w.score_scale, w.hpg, return_weights=True)
+            assert p.sum() == pytest.approx(1.0, abs=1e-14)
+            assert len(p) == w.ns + min(9, int(a["meta"][0][0]) + i + 1)
+
+
+def test_uniform_scores_return_window_mean():
+    w = workloads.custom(B=2, t=4, nh=4, nk=2, hd=8, window=6, cap=6, ns=1, pos_mode="full",
+                         pos_lo=6, pos_hi=50)
+    inp = workloads.make_inputs(w)
+    a = _attend_inputs(w, inp, q=np.zeros((w.B, w.t, w.nh, w.hd)))
+    out = oracle.attend(a, w.score_scale, w.hpg)
+    for b in range(w.B):
+        len0, head0 = int(a["meta"][b][0]), int(a["meta"][b][1])
+        for i in range(w.t):
+            for h in range(w.nh):
+                g = h // w.hpg
+                vals = [a["sink_v"][b, g, 0]]
+                qpos = len0 + i
+                for kpos in range(qpos - 6 + 1, qpos + 1):   # the 6 newest positions
+                    vals.append(a["ring_v"][b, g, (head0 + kpos) % 6] if kpos < len0
+                                else a["v_chunk"][b, kpos - len0, g])
+                expect = np.mean(vals, axis=0) * expit(a["gate"][b, i, h] * a["gate_scale"][h])
+                np.testing.assert_allclose(out[b, i, h], expect, rtol=1e-12, atol=1e-15)
+
+
+# ---------------------------------------------------------------------------
+# invariants
+# ---------------------------------------------------------------------------
+def test_ring_rotation_invariance():
+    w = workloads.custom(B=2, t=3, nh=4, nk=2, hd=8, window=7, cap=7, ns=2, pos_mode="full",
+                         pos_lo=7, pos_hi=60, scale=2.0)
+    a = _attend_inputs(w, workloads.make_inputs(w))
+    base = oracle.attend(a, w.score_scale, w.hpg)
+    for r in (1, 3, 6):
+        b2 = dict(a)
+        b2["ring_k"] = np.roll(a["ring_k"], r, axis=2)
+        b2["ring_v"] = np.roll(a["ring_v"], r, axis=2)
+        m = a["meta"].copy()
+        m[:, 1] = (m[:, 1] + r) % 7
+        b2["meta"] = m
+        np.testing.assert_allclose(oracle.attend(b2, w.score_scale, w.hpg), base, rtol=1e-13,
+                                   atol=1e-15)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=2, t=5, nh=4, nk=2, hd=8, window=4, cap=4, ns=1, pos_mode="full", pos_lo=4, pos_hi=30),
+    dict(B=2, t=6, nh=2, nk=1, hd=8, window=8, cap=8, ns=0, pos_mode="partial", pos_lo=1, pos_hi=8),
+])
+def test_chunk_equals_sequential_single_row_steps(kw):
+    w = workloads.custom(scale=2.0, **kw)
+    a = _attend_inputs(w, workloads.make_inputs(w))
+    out_chunk = oracle.attend(a, w.score_scale, w.hpg)
+    rk_c, rv_c, meta_c = oracle.commit(a["meta"], a["ring_k"], a["ring_v"], a["k_chunk"], a["v_chunk"])
+    meta = a["meta"].copy()
+    rk, rv = a["ring_k"].copy(), a["ring_v"].copy()
+    for i in range(w.t):
+        step = {
+            "meta": meta, "q": a["q"][:, i:i + 1], "k_chunk": a["k_chunk"][:, i:i + 1],
+            "v_chunk": a["v_chunk"][:, i:i + 1], "ring_k": rk, "ring_v": rv,
+            "sink_k": a["sink_k"], "sink_v": a["sink_v"], "gate": a["gate"][:, i:i + 1],
+            "gate_scale": a["gate_scale"],
+        }
+        o = oracle.attend(step, w.score_scale, w.hpg)
+        np.testing.assert_allclose(o[:, 0], out_chunk[:, i], rtol=1e-13, atol=1e-15)
+        rk, rv, meta = oracle.commit(meta, rk, rv, step["k_chunk"], step["v_chunk"])
+    np.testing.assert_array_equal(rk, rk_c)
+    np.testing.assert_array_equal(rv, rv_c)
+    np.testing.assert_array_equal(meta, meta_c)
+
+
+def test_commit_after_prep_grown_ring_matches_prep_slots():
+    """For a ring grown from position 0 (win_head = (pos0 - win_len) % W, W = cap),
+    the commit slot equals the prep slot (pos0 + j) % cap."""
+    for name in ("tiny_decode", "batched_decode", "spec_verify", "prompt_chunk", "long_decode"):
+        w = workloads.WORKLOADS[name]
+        pos0, meta = workloads.make_meta(w, torch.Generator().manual_seed(w.seed))
+        for b in range(meta.shape[0]):
+            for j in (0, w.t - 1):
+                assert oracle.commit_slot(meta[b].numpy(), j, w.cap) == \
+                    oracle.prep_ring_slot(int(pos0[b]), j, w.cap)
