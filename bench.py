@@ -1,0 +1,391 @@
+#!/usr/bin/env python
+"""Throughput of the sliding-window GQA token path on GB300: one JSON line.
+
+A step is one pass of the whole path over one batch resident in HBM: the RoPE
+table, prep (rotation, unit heads, query scale, ring write for t == 1), the
+split-KV attention, the merge with the sigmoid gate, and the commit of the
+chunk into the ring with the advanced meta written to a second meta buffer (so
+every step repeats the same work on the same state).
+
+Metric: attended KV-keys/s = sum over (sequence, row, KV head) of
+ns + min(window, win_len + row + 1), per second, over all GPUs. Also reported:
+the algorithmic KV-read bandwidth (each distinct K/V byte of a
+(sequence, KV head) once per step) and its fraction of the measured HBM peak.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+       [--impl reference]
+Under torchrun every rank runs the full workload on its own GPU (sequence
+shards, no collective on the data path) and rank 0 prints the line.
+"""
+from __future__ import annotations
+
+import os
+
+# The CPU oracle is timed single-threaded (reported as cores = 1).
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+    os.environ.setdefault(_v, "1")
+
+import argparse  # noqa: E402
+import hashlib  # noqa: E402
+import json  # noqa: E402
+import re  # noqa: E402
+import statistics  # noqa: E402
+import subprocess  # noqa: E402
+import sys  # noqa: E402
+import tempfile  # noqa: E402
+import time  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+DEFAULT_WORKLOAD = "batched_decode"
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+ATTEND_SRC = os.path.join(ROOT, "sliding_window_gqa_prep_gb300", "csrc", "swa_attend.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="swa", choices=["swa", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="CPU time budget of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# measurement definitions
+# ---------------------------------------------------------------------------
+def keys_and_bytes(w, meta):
+    return workloads.kv_keys_and_bytes(w, meta)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def attend_source_hash():
+    with open(ATTEND_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(PROFILE_DIR, f"attend_partial_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch\s*[:=]\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256_16\s*[:=]\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != attend_source_hash():
+        return None
+    return float(m.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.index = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", self.index], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        self.file.close()
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names[1:], r[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline / reference arm)
+# ---------------------------------------------------------------------------
+def oracle_units(w, inp, units):
+    """Run the oracle (rope table, prep of the sequence's rows, attention of
+    every query head of the sampled (sequence, row, KV head) units). Returns
+    the attended KV-keys of the units."""
+    import oracle
+    keys = 0
+    by_seq = {}
+    for b, i, g in units:
+        by_seq.setdefault(b, []).append((i, g))
+    for b, lst in by_seq.items():
+        rope = oracle.rope_table(inp["pos0"].numpy()[b:b + 1], w.t, w.hd, w.theta)
+        q, k, v = oracle.prep(inp["yq"].numpy()[b:b + 1], inp["yk"].numpy()[b:b + 1],
+                              inp["yv"].numpy()[b:b + 1], rope, inp["q_scale"].numpy(), w.eps)
+        a = {"meta": inp["meta"].numpy()[b:b + 1], "q": q, "k_chunk": k, "v_chunk": v,
+             "ring_k": inp["ring_k"].numpy()[b:b + 1], "ring_v": inp["ring_v"].numpy()[b:b + 1],
+             "sink_k": inp["sink_k"].numpy()[b:b + 1], "sink_v": inp["sink_v"].numpy()[b:b + 1],
+             "gate": inp["gate"].numpy()[b:b + 1], "gate_scale": inp["gate_scale"].numpy()}
+        for i, g in lst:
+            for h in range(g * w.hpg, (g + 1) * w.hpg):
+                oracle.attend_row(0, i, h, a, w.score_scale, w.hpg)
+            L, W = int(a["meta"][0][0]), int(a["meta"][0][3])
+            keys += w.ns + min(W, L + i + 1)
+    return keys
+
+
+def sample_inputs(w, nseq=2):
+    return workloads.make_inputs(w, batch=min(w.B, nseq))
+
+
+def cpu_baseline(w, budget_s):
+    inp = sample_inputs(w)
+    B = inp["meta"].shape[0]
+    all_units = [(b, i, g) for b in range(B) for i in range(w.t) for g in range(w.nk)]
+    rng = np.random.default_rng(0)
+    rng.shuffle(all_units)
+    t0 = time.perf_counter()
+    keys, n = 0, 0
+    while n < len(all_units) and time.perf_counter() - t0 < budget_s:
+        keys += oracle_units(w, inp, [all_units[n]])
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": keys / dt, "unit": "keys/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} (sequence, row, KV head) units of {w.name} with all their query heads "
+                      f"({keys} attended KV-keys, {dt:.1f} s, numpy float64, one thread)"}
+
+
+def run_reference(args, w, rank):
+    """Reference arm: the CPU oracle as it stands, on a bounded sample per step."""
+    if rank != 0:
+        return
+    inp = sample_inputs(w)
+    B = inp["meta"].shape[0]
+    all_units = [(b, i, g) for b in range(B) for i in range(w.t) for g in range(w.nk)]
+    rng = np.random.default_rng(1)
+    rng.shuffle(all_units)
+    t_unit0 = time.perf_counter()
+    oracle_units(w, inp, [all_units[0]])
+    t_unit = max(time.perf_counter() - t_unit0, 1e-4)
+    budget_per_step = 150.0 / max(1, args.steps + args.warmup)
+    per_step = max(1, min(len(all_units), int(budget_per_step / t_unit)))
+    cursor = 0
+
+    def step():
+        nonlocal cursor
+        units = [all_units[(cursor + k) % len(all_units)] for k in range(per_step)]
+        cursor += per_step
+        return oracle_units(w, inp, units)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    keys = 0
+    for _ in range(args.steps):
+        keys += step()
+    dt = time.perf_counter() - t0
+    value = keys / dt
+    sample = (f"{per_step} (sequence, row, KV head) units of {w.name} per step with all their "
+              f"query heads, numpy float64, one thread")
+    line = {"impl": "reference", "metric": "attended KV-keys/s", "value": value, "unit": "keys/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(w, n):
+    return {"workload": w.name, "B": w.B, "t": w.t, "nh": w.nh, "nk": w.nk, "hd": w.hd,
+            "window": w.window, "cap": w.cap, "ns": w.ns, "seed": w.seed,
+            "parallelism": f"sequence shards x{n} (no collective)" if n > 1 else "1 GPU",
+            "l2": "inputs larger than L2: the K/V rings read each step exceed 129 MB"
+            if w.B * w.nk * w.cap * w.hd * 8 > 129e6 else
+            "inputs smaller than L2 (reported as is)"}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def make_events(n):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:          # materialise the CUDA events before handing them to C
+        e.record()
+    torch.cuda.synchronize()
+    return evs
+
+
+def run_gpu(args, w, rank, world, local_rank):
+    import sliding_window_gqa_prep_gb300 as swa
+
+    dev = torch.device("cuda", local_rank)
+    inp = workloads.make_inputs(w, seed=w.seed + 1000 * rank)
+    keys, kv_bytes = keys_and_bytes(w, inp["meta"])
+    tp = swa.TokenPath(B=w.B, t=w.t, nh=w.nh, nk=w.nk, hd=w.hd, cap=w.cap, ns=w.ns,
+                       q_scale=inp["q_scale"], gate_scale=inp["gate_scale"],
+                       ring_k=inp["ring_k"], ring_v=inp["ring_v"], sink_k=inp["sink_k"],
+                       sink_v=inp["sink_v"], meta=inp["meta"], pos0=inp["pos0"],
+                       scale=w.score_scale, eps=w.eps, theta=w.theta, device=dev)
+    d_in = {k: inp[k].to(dev).contiguous() for k in ("yq", "yk", "yv", "gate")}
+    del inp["ring_k"], inp["ring_v"]
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # warm-up
+    for _ in range(args.warmup):
+        tp.step(d_in["yq"], d_in["yk"], d_in["yv"], d_in["gate"])
+    torch.cuda.synchronize()
+
+    K = args.steps
+    kev = make_events(2 * K)
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    barrier()
+    l0 = swa.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for s in range(K):
+        tp.step(d_in["yq"], d_in["yk"], d_in["yv"], d_in["gate"], ev_start=kev[2 * s],
+                ev_stop=kev[2 * s + 1])
+    e1.record()
+    barrier()
+    launches = swa.launch_count() - l0
+    clk = clocks.stop() if clocks else None
+    ms = e0.elapsed_time(e1)
+    kern_ms = [kev[2 * s].elapsed_time(kev[2 * s + 1]) for s in range(K)]
+    err = int(tp.err.item())
+    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+    ms = float(t_max.item())
+
+    # end to end: pinned host inputs in, gated output back, every step
+    e2e = None
+    if not args.no_e2e:
+        h_in = {k: v.cpu().pin_memory() for k, v in d_in.items()}
+        h_out = torch.empty(w.B, w.t, w.nh, w.hd).pin_memory()
+        for _ in range(max(args.warmup, 1)):
+            tp.step(h_in["yq"], h_in["yk"], h_in["yv"], h_in["gate"], out_host=h_out)
+        K2 = K
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(K2):
+            tp.step(h_in["yq"], h_in["yk"], h_in["yv"], h_in["gate"], out_host=h_out)
+        barrier()
+        e2e_s = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
+        if world > 1:
+            torch.distributed.all_reduce(e2e_s, op=torch.distributed.ReduceOp.MAX)
+        e2e = {"value": keys * K2 * world / float(e2e_s.item()), "unit": "keys/s",
+               "h2d_bytes_per_step": sum(v.numel() * 4 for v in h_in.values()),
+               "d2h_bytes_per_step": h_out.numel() * 4,
+               "ms_per_step": float(e2e_s.item()) * 1e3 / K2}
+
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peaks()
+    step_s = ms / 1e3 / K
+    kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
+    achieved = kv_bytes / kern_avg_s / 1e9
+    traffic = recorded_traffic(w.name)
+    line = {
+        "metric": "attended KV-keys/s",
+        "value": keys * world / step_s,
+        "unit": "keys/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded generator, shapes of the named workload)",
+        "config": workload_config(w, world),
+        "kv_read_gbs_step": kv_bytes * world / step_s / 1e9,
+        "kv_read_frac_of_peak_step": kv_bytes / step_s / 1e9 / peak,
+        "roofline": {"bound": "hbm", "kernel": "attend_partial_kernel",
+                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
+                     "launch_ms_avg": kern_avg_s * 1e3},
+        "gpu_launches": launches,
+        "launches_per_step": launches / K,
+        "device_errors": err,
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    w = workloads.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_gpu(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

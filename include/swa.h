@@ -1,0 +1,201 @@
+/*
+ * swa.h — C ABI of the sliding-window GQA token path on GB300 (sm_103a).
+ *
+ * Two stages of a sealed sliding-window attention layer, as defined on the
+ * Metal shader pages of the cortiq-engine crate:
+ *   prep   — "dory_msl.metal" (cortiq-engine 0.8.57), kernel dory_prep:
+ *            rotate-half RoPE of every q/k head, unit heads with eps, the
+ *            per-feature query scale, K/V into the ring at slot (pos0+j) % cap.
+ *   attend — "o1c_msl.metal" (cortiq-engine 0.8.79), kernels o1c_score,
+ *            o1c_max, o1c_soft, o1c_sum, o1c_add, o1c_tok_near, o1c_tok_merge,
+ *            o1c_ring_commit, o1c_meta; "dory_msl.metal" dory_gate:
+ *            each chunk row attends the sinks plus its causal window over the
+ *            ring and the chunk's own earlier rows, all query heads of a KV
+ *            head together (GQA), max-subtracted f32 softmax, value sums split
+ *            across key ranges and reduced, then out = o * sigmoid(g * s_g).
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller, f32 unless
+ *     stated, densely packed in the row-major layout given beside each field,
+ *     and 16-byte aligned (SWA_E_ALIGN otherwise).
+ *   - Work is enqueued on `stream` (0 = legacy default stream). No entry point
+ *     synchronises the device, allocates device memory or keeps state between
+ *     calls besides cached device attributes.
+ *   - Arguments are checked on the host before anything is enqueued; a
+ *     negative status means nothing was enqueued, except SWA_E_CUDA, which
+ *     reports a failed launch (the CUDA error text is kept for
+ *     swa_status_string / swa_last_cuda_error).
+ *   - Sizes are ints; hd must be 64, 128 or 256; nh must be a multiple of nk
+ *     with nh / nk <= 32.
+ */
+#ifndef SWA_H
+#define SWA_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every int entry point. */
+#define SWA_OK            0
+#define SWA_E_NULL       -1  /* a required pointer is NULL */
+#define SWA_E_SHAPE      -2  /* unsupported or inconsistent sizes */
+#define SWA_E_ALIGN      -3  /* a tensor pointer is not 16-byte aligned */
+#define SWA_E_WORKSPACE  -4  /* workspace missing or smaller than swa_attend_workspace_size */
+#define SWA_E_HAZARD     -5  /* prep ring write requested for t > 1 (see swa_prep) */
+#define SWA_E_CUDA       -6  /* a CUDA launch or query failed */
+
+/* Bits a kernel ORs into the optional device error word (`err`). The kernels
+ * never trap: on such an event they clamp or stop and report it here. */
+#define SWA_DERR_META     1u /* meta out of range: window > cap, win_len > window
+                                or win_head >= window (values were clamped) */
+#define SWA_DERR_TIMEOUT  2u /* a bounded wait on a copy into shared memory
+                                expired; the kernel stopped without output */
+
+/* Per-sequence ring state, as the per-group meta of o1c_msl.metal:
+ *   win_len  — keys held in the ring (<= window)
+ *   win_head — slot of the oldest held key (< window)
+ *   far_len  — keys that have left the window (advanced by the commit, read
+ *              by nothing on this path)
+ *   window   — the window W, which is also the ring modulus; 0 means cap. */
+typedef struct swa_meta {
+  uint32_t win_len, win_head, far_len, window;
+} swa_meta;
+
+/* Human-readable text of a status code (static storage). */
+const char* swa_status_string(int status);
+/* Text of the last CUDA error seen by this library in this thread ("" if none). */
+const char* swa_last_cuda_error(void);
+/* Library version string (static storage). */
+const char* swa_version(void);
+/* Number of kernels this library has launched in this process. */
+uint64_t swa_launch_count(void);
+
+/*
+ * swa_rope_table — fill the RoPE table that swa_prep consumes.
+ *   rope [B][t][hd]: row (b, j) holds cos(a_e) for e < hd/2, then sin(a_e),
+ *   a_e = (pos0[b] + j) * theta^(-2e/hd), angles and cos/sin in f64, stored
+ *   rounded to f32. The pages consume such a table (dory_prep reads cos at e
+ *   and sin at hd/2 + e; eg_qkv_prep in "egemma2_msl.metal" the same pairing)
+ *   but do not show how it is built: this is the standard rotate-half
+ *   schedule.
+ *   pos0 [B] (device, uint32): absolute position of chunk row 0.
+ * Errors: SWA_E_NULL, SWA_E_SHAPE (B, t < 1 or hd unsupported, theta <= 0),
+ *         SWA_E_ALIGN, SWA_E_CUDA.
+ */
+int swa_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd,
+                   double theta, cudaStream_t stream);
+
+/*
+ * swa_prep — rotation, unit heads, query scale and ring write of a chunk
+ * ("dory_msl.metal", dory_prep). For every sequence b, row j, head:
+ *   x = head[0:hd/2], y = head[hd/2:hd], c/s = rope[b][j] halves
+ *   u = x*c - y*s, v = y*c + x*s, inv = 1 / sqrt(sum(u^2 + v^2) + eps)
+ *   q_out[b][j][h] = (u, v) * inv * q_scale[h]          (h < nh)
+ *   k_out[b][j][g] = (u, v) * inv                       (g < nk)
+ *   v_out[b][j][g] = yv[b][j][g]                        (unchanged)
+ * and, when ring_k/ring_v are non-NULL, k_out/v_out rows also go to ring
+ * slot (pos0[b] + j) % cap.
+ *
+ * The ring write is only accepted for t == 1 (SWA_E_HAZARD otherwise): with a
+ * full ring a chunk's later rows land on slots that its earlier rows still
+ * read. For t > 1 pass NULL rings here and let swa_attend commit the chunk
+ * after its reads (commit = 1). For t == 1 the written slot is the evicted
+ * one, which the row does not read. The ring slot (pos0 + j) % cap agrees
+ * with swa_attend's slot map when the sequence's window equals cap and
+ * win_head == (pos0 - win_len) % cap (a ring grown from position 0).
+ */
+typedef struct swa_prep_args {
+  int B, t, nh, nk, hd, cap;     /* cap only read when rings are given      */
+  float eps;                     /* added to the sum of squares             */
+  const float* yq;               /* [B][t][nh][hd]                          */
+  const float* yk;               /* [B][t][nk][hd]                          */
+  const float* yv;               /* [B][t][nk][hd]                          */
+  const float* rope;             /* [B][t][hd] (swa_rope_table)             */
+  const float* q_scale;          /* [nh][hd]                                */
+  const uint32_t* pos0;          /* [B]; required when rings are given      */
+  float* q_out;                  /* [B][t][nh][hd]                          */
+  float* k_out;                  /* [B][t][nk][hd]                          */
+  float* v_out;                  /* [B][t][nk][hd] or NULL (no copy)        */
+  float* ring_k;                 /* [B][nk][cap][hd] or NULL                */
+  float* ring_v;                 /* [B][nk][cap][hd] or NULL (with ring_k)  */
+} swa_prep_args;
+
+int swa_prep(const swa_prep_args* args, cudaStream_t stream);
+
+/*
+ * swa_attend — attention of a chunk of t rows of a sealed sliding-window
+ * layer; a decode token (t = 1), a speculative verify and a prompt chunk take
+ * the same call ("o1c_msl.metal" o1c_score ... o1c_add and o1c_tok_*;
+ * "dory_msl.metal" dory_gate).
+ *
+ * Row i of sequence b (len0 = win_len, head0 = win_head, W = window before
+ * the chunk) attends, for each query head h of KV head g = h / (nh/nk):
+ *   the ns sinks sink_k/v[b][g][0..ns), always, and
+ *   logical keys x in [lo_i, len0 + i], win_i = min(W, len0 + i + 1),
+ *   lo_i = len0 + i + 1 - win_i; x < len0 reads ring slot (head0 + x) % W,
+ *   x >= len0 reads chunk row x - len0 from k_chunk/v_chunk.
+ *   s = scale * <q, key>, p = exp(s - max s), o = sum p v / sum p,
+ *   out[b][i][h] = o * 1 / (1 + exp(-gate[b][i][h] * gate_scale[h])).
+ * The ring is read per the meta BEFORE the chunk; chunk rows always come
+ * from k_chunk / v_chunk.
+ *
+ * commit = 1 additionally, after every read of the call: writes chunk row j
+ * (the last min(t, W) rows) into ring slot (head0 + len0 + j) % W
+ * (o1c_ring_commit) and writes the advanced meta to meta_out (o1c_meta):
+ * win_len = min(len0 + t, W); on an overflow by ev keys win_head advances by
+ * ev (mod W) and far_len grows by ev. meta_out may alias meta.
+ *
+ * The value sums run split across key ranges (split-KV) with partial
+ * (max, sum, numerator) records in `workspace`, reduced by a second kernel
+ * that also applies the gate and the commit. num_splits = 0 lets the library
+ * choose; a positive value caps the splits per (sequence, KV head, row block)
+ * (results agree within f32 rounding for any split count).
+ *
+ * Workspace: `workspace_bytes` >= swa_attend_workspace_size(args), device
+ * memory, 256-byte aligned, no initial contents needed; overlapping calls
+ * must not share it. ev_start / ev_stop, when non-NULL, are recorded on the
+ * stream right before and after the main attention kernel (for timing it).
+ * err, when non-NULL, is a device word the kernels OR SWA_DERR_* bits into.
+ *
+ * Errors: SWA_E_NULL, SWA_E_SHAPE, SWA_E_ALIGN, SWA_E_WORKSPACE, SWA_E_CUDA.
+ */
+typedef struct swa_attend_args {
+  int B, t, nh, nk, hd, cap, ns;
+  float scale;                   /* score scale (e.g. 1/sqrt(hd))           */
+  const swa_meta* meta;          /* [B], state before the chunk             */
+  const float* q;                /* [B][t][nh][hd] (q_out of swa_prep)      */
+  const float* k_chunk;          /* [B][t][nk][hd]                          */
+  const float* v_chunk;          /* [B][t][nk][hd]                          */
+  float* ring_k;                 /* [B][nk][cap][hd]; written iff commit    */
+  float* ring_v;                 /* [B][nk][cap][hd]; written iff commit    */
+  const float* sink_k;           /* [B][nk][ns][hd]; NULL allowed if ns = 0 */
+  const float* sink_v;           /* [B][nk][ns][hd]; NULL allowed if ns = 0 */
+  const float* gate;             /* [B][t][nh][hd]                          */
+  const float* gate_scale;       /* [nh][hd]                                */
+  float* out;                    /* [B][t][nh][hd]                          */
+  void* workspace;               /* split-KV partials                       */
+  size_t workspace_bytes;
+  int commit;                    /* 1: ring + meta commit after the reads   */
+  swa_meta* meta_out;            /* [B]; required when commit = 1           */
+  int num_splits;                /* 0: automatic                            */
+  uint32_t* err;                 /* optional device error word              */
+  cudaEvent_t ev_start;          /* optional                                */
+  cudaEvent_t ev_stop;           /* optional                                */
+} swa_attend_args;
+
+/* Bytes of workspace swa_attend needs for these sizes (reads B, t, nh, nk,
+ * hd, cap, ns, num_splits; 0 if the sizes are invalid). Queries the current
+ * device's SM count on first use. */
+size_t swa_attend_workspace_size(const swa_attend_args* args);
+
+int swa_attend(const swa_attend_args* args, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SWA_H */

@@ -1,0 +1,228 @@
+"""Sliding-window GQA token path on GB300: Python binding of libswa_gb300.so.
+
+The binding only checks tensors and passes their device addresses to the C ABI
+(include/swa.h); every step of the path runs in the library's CUDA kernels.
+PyTorch provides device memory and streams. There is no CPU fallback: on a
+machine without the built library or without a GPU the calls raise.
+
+Public calls (same names as the C ABI):
+  rope_table(pos0, t, hd, theta)                 -> rope [B][t][hd]
+  prep(yq, yk, yv, rope, q_scale, eps, ...)      -> (q, k, v) chunk tensors
+  attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v,
+         gate, gate_scale, scale, ...)           -> out [B][t][nh][hd]
+  attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits=0)
+  TokenPath: holds a batch's ring state and runs whole steps
+Meta tensors are int32 [B][4] = (win_len, win_head, far_len, window), read by
+the kernels as uint32; pos0 tensors are int32 [B].
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _abi
+from ._abi import SwaError, SWA_DERR_META, SWA_DERR_TIMEOUT  # noqa: F401
+
+__all__ = ["rope_table", "prep", "attend", "attend_workspace_size", "launch_count",
+           "TokenPath", "SwaError", "library"]
+
+
+def library() -> ctypes.CDLL:
+    return _abi.load()
+
+
+def launch_count() -> int:
+    """Kernels the library has launched in this process."""
+    return int(library().swa_launch_count())
+
+
+def _stream(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(x: Optional[torch.Tensor], name: str, shape=None, dtype=torch.float32,
+         required: bool = True) -> int:
+    if x is None:
+        if required:
+            raise ValueError(f"{name} is required")
+        return 0
+    if not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {x.dtype}")
+    if not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(x.shape)}, expected {tuple(shape)}")
+    return x.data_ptr()
+
+
+def rope_table(pos0: torch.Tensor, t: int, hd: int, theta: float = 10000.0,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """RoPE table [B][t][hd] (cos | sin of (pos0[b] + j) * theta^(-2e/hd))."""
+    B = pos0.shape[0]
+    if out is None:
+        out = torch.empty(B, t, hd, device=pos0.device, dtype=torch.float32)
+    lib = library()
+    rc = lib.swa_rope_table(_ptr(out, "out", (B, t, hd)), _ptr(pos0, "pos0", (B,), torch.int32),
+                            B, t, hd, float(theta), _stream(stream))
+    _abi.check(rc, "swa_rope_table")
+    return out
+
+
+def prep(yq, yk, yv, rope, q_scale, eps: float = 1e-6, *, pos0=None, ring_k=None,
+         ring_v=None, q_out=None, k_out=None, v_out=None, copy_v: bool = True, stream=None):
+    """Rotation, unit heads, query scale and (t == 1 only) the ring write.
+
+    Returns (q_out, k_out, v) where v is v_out when copy_v, else yv itself."""
+    B, t, nh, hd = yq.shape
+    nk = yk.shape[2]
+    if q_out is None:
+        q_out = torch.empty_like(yq)
+    if k_out is None:
+        k_out = torch.empty_like(yk)
+    if copy_v and v_out is None:
+        v_out = torch.empty_like(yv)
+    cap = ring_k.shape[2] if ring_k is not None else 0
+    a = _abi.PrepArgs()
+    a.B, a.t, a.nh, a.nk, a.hd, a.cap = B, t, nh, nk, hd, cap
+    a.eps = float(eps)
+    a.yq = _ptr(yq, "yq", (B, t, nh, hd))
+    a.yk = _ptr(yk, "yk", (B, t, nk, hd))
+    a.yv = _ptr(yv, "yv", (B, t, nk, hd))
+    a.rope = _ptr(rope, "rope", (B, t, hd))
+    a.q_scale = _ptr(q_scale, "q_scale", (nh, hd))
+    a.pos0 = _ptr(pos0, "pos0", (B,), torch.int32, required=ring_k is not None)
+    a.q_out = _ptr(q_out, "q_out", (B, t, nh, hd))
+    a.k_out = _ptr(k_out, "k_out", (B, t, nk, hd))
+    a.v_out = _ptr(v_out, "v_out", (B, t, nk, hd), required=False) if copy_v else 0
+    a.ring_k = _ptr(ring_k, "ring_k", (B, nk, cap, hd), required=False)
+    a.ring_v = _ptr(ring_v, "ring_v", (B, nk, cap, hd), required=ring_k is not None)
+    rc = library().swa_prep(ctypes.byref(a), _stream(stream))
+    _abi.check(rc, "swa_prep")
+    return q_out, k_out, (v_out if copy_v else yv)
+
+
+def _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits=0) -> _abi.AttendArgs:
+    a = _abi.AttendArgs()
+    a.B, a.t, a.nh, a.nk, a.hd, a.cap, a.ns = B, t, nh, nk, hd, cap, ns
+    a.num_splits = int(num_splits)
+    return a
+
+
+def attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits: int = 0) -> int:
+    a = _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits)
+    n = int(library().swa_attend_workspace_size(ctypes.byref(a)))
+    if n == 0:
+        raise SwaError(_abi.SWA_E_SHAPE, "swa_attend_workspace_size")
+    return n
+
+
+def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate_scale,
+           scale: float, *, out=None, workspace=None, commit: bool = False, meta_out=None,
+           num_splits: int = 0, err=None, ev_start=None, ev_stop=None, stream=None):
+    """Attention of a chunk (decode, verify or prompt); see include/swa.h."""
+    B, t, nh, hd = q.shape
+    nk = k_chunk.shape[2]
+    cap = ring_k.shape[2]
+    ns = sink_k.shape[2] if sink_k is not None else 0
+    if out is None:
+        out = torch.empty_like(q)
+    need = attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits)
+    if workspace is None:
+        workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
+    a = _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits)
+    a.scale = float(scale)
+    a.meta = _ptr(meta, "meta", (B, 4), torch.int32)
+    a.q = _ptr(q, "q", (B, t, nh, hd))
+    a.k_chunk = _ptr(k_chunk, "k_chunk", (B, t, nk, hd))
+    a.v_chunk = _ptr(v_chunk, "v_chunk", (B, t, nk, hd))
+    a.ring_k = _ptr(ring_k, "ring_k", (B, nk, cap, hd))
+    a.ring_v = _ptr(ring_v, "ring_v", (B, nk, cap, hd))
+    a.sink_k = _ptr(sink_k, "sink_k", (B, nk, ns, hd), required=ns > 0) if ns else 0
+    a.sink_v = _ptr(sink_v, "sink_v", (B, nk, ns, hd), required=ns > 0) if ns else 0
+    a.gate = _ptr(gate, "gate", (B, t, nh, hd))
+    a.gate_scale = _ptr(gate_scale, "gate_scale", (nh, hd))
+    a.out = _ptr(out, "out", (B, t, nh, hd))
+    a.workspace = _ptr(workspace, "workspace", None, torch.uint8)
+    a.workspace_bytes = workspace.numel()
+    a.commit = 1 if commit else 0
+    a.meta_out = _ptr(meta_out, "meta_out", (B, 4), torch.int32, required=commit)
+    a.err = _ptr(err, "err", (1,), torch.int32, required=False)
+    a.ev_start = ctypes.c_void_p(ev_start.cuda_event) if ev_start is not None else None
+    a.ev_stop = ctypes.c_void_p(ev_stop.cuda_event) if ev_stop is not None else None
+    rc = library().swa_attend(ctypes.byref(a), _stream(stream))
+    _abi.check(rc, "swa_attend")
+    return out
+
+
+class TokenPath:
+    """One batch of sequences of a sealed sliding-window layer, resident on the GPU.
+
+    Holds the ring K/V, sinks, meta, the per-head scales and the workspace;
+    ``step`` runs prep + attend (+ commit) for a chunk of t rows. With host
+    (CPU, ideally pinned) inputs, ``step`` copies them in, runs the kernels and
+    copies the gated output back (the end-to-end call); with device inputs it
+    returns the device output.
+    """
+
+    def __init__(self, *, B, t, nh, nk, hd, cap, ns, window=None, q_scale, gate_scale,
+                 ring_k, ring_v, sink_k, sink_v, meta, pos0, scale=None, eps=1e-6,
+                 theta=10000.0, device="cuda", num_splits=0):
+        self.B, self.t, self.nh, self.nk, self.hd, self.cap, self.ns = B, t, nh, nk, hd, cap, ns
+        self.scale = float(scale) if scale is not None else hd ** -0.5
+        self.eps, self.theta = float(eps), float(theta)
+        dev = torch.device(device)
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.q_scale = q_scale.to(**f32).contiguous()
+        self.gate_scale = gate_scale.to(**f32).contiguous()
+        self.ring_k = ring_k.to(**f32).contiguous()
+        self.ring_v = ring_v.to(**f32).contiguous()
+        self.sink_k = sink_k.to(**f32).contiguous()
+        self.sink_v = sink_v.to(**f32).contiguous()
+        self.meta = meta.to(device=dev, dtype=torch.int32).contiguous()
+        self.meta_next = self.meta.clone()
+        self.pos0 = pos0.to(device=dev, dtype=torch.int32).contiguous()
+        self.num_splits = num_splits
+        self.rope = torch.empty(B, t, hd, **f32)
+        self.q = torch.empty(B, t, nh, hd, **f32)
+        self.k = torch.empty(B, t, nk, hd, **f32)
+        self.out = torch.empty(B, t, nh, hd, **f32)
+        self.workspace = torch.empty(attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits),
+                                     device=dev, dtype=torch.uint8)
+        self.err = torch.zeros(1, device=dev, dtype=torch.int32)
+        self.in_bufs = {
+            "yq": torch.empty(B, t, nh, hd, **f32), "yk": torch.empty(B, t, nk, hd, **f32),
+            "yv": torch.empty(B, t, nk, hd, **f32), "gate": torch.empty(B, t, nh, hd, **f32),
+        }
+
+    def step(self, yq, yk, yv, gate, *, commit: bool = True, out_host=None,
+             ev_start=None, ev_stop=None, stream=None):
+        """One pass of the path. commit = True writes the chunk into the ring and
+        the advanced meta into ``meta_next`` (the current ``meta`` is kept, so
+        repeating a step repeats the same work). Host inputs are copied in and
+        the output is copied back (into ``out_host`` when given, e.g. pinned)."""
+        host = not yq.is_cuda
+        if host:
+            for name, x in (("yq", yq), ("yk", yk), ("yv", yv), ("gate", gate)):
+                self.in_bufs[name].copy_(x, non_blocking=True)
+            yq, yk, yv, gate = (self.in_bufs[n] for n in ("yq", "yk", "yv", "gate"))
+        rope_table(self.pos0, self.t, self.hd, self.theta, out=self.rope, stream=stream)
+        ring = self.t == 1
+        q, k, v = prep(yq, yk, yv, self.rope, self.q_scale, self.eps, pos0=self.pos0,
+                       ring_k=self.ring_k if ring else None, ring_v=self.ring_v if ring else None,
+                       q_out=self.q, k_out=self.k, copy_v=False, stream=stream)
+        attend(self.meta, q, k, v, self.ring_k, self.ring_v, self.sink_k, self.sink_v, gate,
+               self.gate_scale, self.scale, out=self.out, workspace=self.workspace,
+               commit=commit, meta_out=self.meta_next, num_splits=self.num_splits, err=self.err,
+               ev_start=ev_start, ev_stop=ev_stop, stream=stream)
+        if host:
+            if out_host is None:
+                return self.out.to("cpu")
+            out_host.copy_(self.out, non_blocking=True)
+            (stream if stream is not None else torch.cuda.current_stream()).synchronize()
+            return out_host
+        return self.out

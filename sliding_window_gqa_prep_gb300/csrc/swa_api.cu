@@ -1,0 +1,213 @@
+// C ABI of the sliding-window GQA token path: argument checks, the split
+// planner and the kernel launches (declarations and contracts in swa.h).
+#include "swa_internal.cuh"
+
+#include <atomic>
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+
+namespace swa {
+
+static std::atomic<uint64_t> g_launches{0};
+static thread_local char g_cuda_err[256] = "";
+
+void note_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return SWA_OK;
+  std::snprintf(g_cuda_err, sizeof g_cuda_err, "%s: %s", cudaGetErrorName(e), cudaGetErrorString(e));
+  return SWA_E_CUDA;
+}
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64) cached[dev] = sms;
+  return sms;
+}
+
+static bool hd_ok(int hd) { return hd == 64 || hd == 128 || hd == 256; }
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int attend_shape_ok(const swa_attend_args* a) {
+  if (a->B < 1 || a->t < 1 || a->nh < 1 || a->nk < 1 || a->cap < 1 || a->ns < 0) return 0;
+  if (!hd_ok(a->hd)) return 0;
+  if (a->nh % a->nk != 0) return 0;
+  if (a->nh / a->nk > 32) return 0;
+  if (a->num_splits < 0) return 0;
+  return 1;
+}
+
+// Cut a call into CTAs. A row block holds `rows` chunk rows so that its
+// rows * hpg query vectors fit one CTA (<= 32); the split count balances the
+// CTAs over the SMs: it minimises (waves of resident CTAs) x (keys per CTA +
+// a fixed per-CTA cost), with the keys of a row block bounded by
+// ns + cap + rows - 1 (the window never exceeds cap).
+bool make_plan(const swa_attend_args* a, AttendPlan* p) {
+  if (!attend_shape_ok(a)) return false;
+  const int hpg = a->nh / a->nk;
+  int rows = 32 / hpg;
+  if (rows < 1) rows = 1;
+  if (rows > a->t) rows = a->t;
+  const int used = rows * hpg;
+  int nq = 4;
+  while (nq < used) nq *= 2;
+  p->nq = nq;
+  p->rows = rows;
+  p->n_rb = (a->t + rows - 1) / rows;
+  const long long keys_max = (long long)a->ns + a->cap + rows - 1;
+  if (keys_max > (1LL << 30)) return false;
+  p->keys_max = (int)keys_max;
+  const int max_splits = (int)((keys_max + TK - 1) / TK);
+  const long long units = (long long)a->B * a->nk * p->n_rb;
+  int best_s = 1;
+  if (a->num_splits > 0) {
+    best_s = a->num_splits < max_splits ? a->num_splits : max_splits;
+  } else {
+    const int sms = num_sms();
+    const int occ = attend_partial_occupancy(a->hd, nq);
+    const long long slots = (long long)(sms > 0 ? sms : 148) * (occ > 0 ? occ : 1);
+    double best = 1e300;
+    for (int s = 1; s <= max_splits; ++s) {
+      const long long chunk = ((keys_max + s - 1) / s + TK - 1) / TK * TK;
+      const long long s_eff = (keys_max + chunk - 1) / chunk;
+      if (s_eff != s) continue;
+      const long long ctas = units * s_eff;
+      const long long waves = (ctas + slots - 1) / slots;
+      const double cost = (double)waves * (double)(chunk + 2 * TK);
+      if (cost < best * 0.999) {
+        best = cost;
+        best_s = s;
+      }
+    }
+  }
+  long long chunk = ((keys_max + best_s - 1) / best_s + TK - 1) / TK * TK;
+  p->chunk = (int)chunk;
+  p->splits = (int)((keys_max + chunk - 1) / chunk);
+  p->items = (size_t)units * p->splits;
+  const size_t acc_bytes = p->items * nq * (size_t)a->hd * sizeof(float);
+  const size_t ml_bytes = p->items * nq * sizeof(float2);
+  const size_t ns_bytes = (size_t)a->B * p->n_rb * sizeof(int);
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  p->off_ml = up(acc_bytes);
+  p->off_nsplit = p->off_ml + up(ml_bytes);
+  p->ws_bytes = p->off_nsplit + up(ns_bytes);
+  return true;
+}
+
+}  // namespace swa
+
+using namespace swa;
+
+extern "C" {
+
+const char* swa_status_string(int status) {
+  switch (status) {
+    case SWA_OK: return "ok";
+    case SWA_E_NULL: return "a required pointer is NULL";
+    case SWA_E_SHAPE: return "unsupported or inconsistent sizes";
+    case SWA_E_ALIGN: return "a tensor pointer is not 16-byte aligned";
+    case SWA_E_WORKSPACE: return "workspace missing or too small";
+    case SWA_E_HAZARD: return "prep ring write needs t == 1 (commit chunks through swa_attend)";
+    case SWA_E_CUDA: return "a CUDA launch or query failed";
+  }
+  return "unknown status";
+}
+
+const char* swa_last_cuda_error(void) { return g_cuda_err; }
+
+const char* swa_version(void) { return "swa-gb300 0.1 (sm_103a)"; }
+
+uint64_t swa_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int swa_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd, double theta,
+                   cudaStream_t stream) {
+  if (!rope || !pos0) return SWA_E_NULL;
+  if (B < 1 || t < 1 || !hd_ok(hd) || !(theta > 0.0)) return SWA_E_SHAPE;
+  if (!aligned16(rope)) return SWA_E_ALIGN;
+  double inv_freq[128];
+  for (int e = 0; e < hd / 2; ++e) inv_freq[e] = std::pow(theta, -2.0 * e / hd);
+  return launch_rope_table(rope, pos0, B, t, hd, inv_freq, stream);
+}
+
+int swa_prep(const swa_prep_args* a, cudaStream_t stream) {
+  if (!a) return SWA_E_NULL;
+  if (!a->yq || !a->yk || !a->yv || !a->rope || !a->q_scale || !a->q_out || !a->k_out)
+    return SWA_E_NULL;
+  if (a->B < 1 || a->t < 1 || a->nh < 1 || a->nk < 1 || !hd_ok(a->hd)) return SWA_E_SHAPE;
+  if (!(a->eps >= 0.0f)) return SWA_E_SHAPE;
+  const bool ring = a->ring_k || a->ring_v;
+  if (ring) {
+    if (!a->ring_k || !a->ring_v || !a->pos0) return SWA_E_NULL;
+    if (a->cap < 1) return SWA_E_SHAPE;
+    if (a->t > 1) return SWA_E_HAZARD;
+  }
+  const void* ptrs[] = {a->yq, a->yk, a->yv, a->rope, a->q_scale, a->q_out, a->k_out,
+                        a->v_out, a->ring_k, a->ring_v};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return SWA_E_ALIGN;
+  PrepParams p;
+  p.B = a->B; p.t = a->t; p.nh = a->nh; p.nk = a->nk; p.hd = a->hd; p.cap = a->cap;
+  p.eps = a->eps;
+  p.yq = a->yq; p.yk = a->yk; p.yv = a->yv; p.rope = a->rope; p.q_scale = a->q_scale;
+  p.pos0 = a->pos0;
+  p.q_out = a->q_out; p.k_out = a->k_out; p.v_out = a->v_out;
+  p.ring_k = ring ? a->ring_k : nullptr;
+  p.ring_v = ring ? a->ring_v : nullptr;
+  return launch_prep(p, stream);
+}
+
+size_t swa_attend_workspace_size(const swa_attend_args* a) {
+  if (!a) return 0;
+  AttendPlan plan;
+  if (!make_plan(a, &plan)) return 0;
+  return plan.ws_bytes;
+}
+
+int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
+  if (!a) return SWA_E_NULL;
+  if (!a->meta || !a->q || !a->k_chunk || !a->v_chunk || !a->ring_k || !a->ring_v || !a->gate ||
+      !a->gate_scale || !a->out)
+    return SWA_E_NULL;
+  if (a->ns > 0 && (!a->sink_k || !a->sink_v)) return SWA_E_NULL;
+  if (a->commit && !a->meta_out) return SWA_E_NULL;
+  if (!attend_shape_ok(a)) return SWA_E_SHAPE;
+  if (!(a->scale == a->scale) || std::isinf(a->scale)) return SWA_E_SHAPE;
+  const void* ptrs[] = {a->q, a->k_chunk, a->v_chunk, a->ring_k, a->ring_v, a->sink_k,
+                        a->sink_v, a->gate, a->gate_scale, a->out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return SWA_E_ALIGN;
+  AttendPlan plan;
+  if (!make_plan(a, &plan)) return SWA_E_SHAPE;
+  if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return SWA_E_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return SWA_E_ALIGN;
+
+  AttendParams p;
+  p.B = a->B; p.t = a->t; p.nh = a->nh; p.nk = a->nk; p.hd = a->hd; p.cap = a->cap;
+  p.ns = a->ns; p.hpg = a->nh / a->nk;
+  p.qmul = a->scale * 1.4426950408889634f;
+  p.meta = a->meta;
+  p.q = a->q; p.k_chunk = a->k_chunk; p.v_chunk = a->v_chunk;
+  p.ring_k = a->ring_k; p.ring_v = a->ring_v;
+  p.sink_k = a->sink_k; p.sink_v = a->sink_v;
+  p.gate = a->gate; p.gate_scale = a->gate_scale; p.out = a->out;
+  char* ws = static_cast<char*>(a->workspace);
+  p.ws_acc = reinterpret_cast<float*>(ws);
+  p.ws_ml = reinterpret_cast<float2*>(ws + plan.off_ml);
+  p.ws_nsplit = reinterpret_cast<int*>(ws + plan.off_nsplit);
+  p.commit = a->commit ? 1 : 0;
+  p.meta_out = a->meta_out;
+  p.err = a->err;
+  p.nq = plan.nq; p.rows = plan.rows; p.n_rb = plan.n_rb; p.chunk = plan.chunk;
+  p.splits = plan.splits;
+  int rc = launch_attend_partial(p, stream, a->ev_start, a->ev_stop);
+  if (rc != SWA_OK) return rc;
+  return launch_attend_merge(p, stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,158 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cstdint>
+#include <cstddef>
+#include <cuda_runtime.h>
+
+#include "swa.h"
+
+namespace swa {
+
+// ---------------------------------------------------------------------------
+// Launch bookkeeping (swa_api.cu)
+// ---------------------------------------------------------------------------
+void note_launch(int n = 1);
+int cuda_status(cudaError_t e);   // records the error text, returns SWA_E_CUDA / SWA_OK
+int num_sms();                    // SM count of the current device (cached per device)
+
+// ---------------------------------------------------------------------------
+// Attention plan: how a call is cut into CTAs (host side, swa_api.cu).
+// ---------------------------------------------------------------------------
+constexpr int TK = 32;            // keys per shared-memory tile
+struct AttendPlan {
+  int nq;          // query vectors per CTA: 4, 8, 16 or 32 (rows_per_block * hpg, rounded up)
+  int rows;        // chunk rows per CTA (row block)
+  int n_rb;        // row blocks per sequence
+  int keys_max;    // upper bound of keys a row block reads (sinks + window + rows - 1)
+  int chunk;       // keys per split (multiple of TK)
+  int splits;      // splits per (sequence, KV head, row block)
+  size_t items;    // B * nk * n_rb * splits partial records
+  size_t ws_bytes; // workspace bytes
+  size_t off_ml;   // byte offset of the (m, l) records
+  size_t off_nsplit; // byte offset of the per-(b, rb) valid-split counts
+};
+bool make_plan(const swa_attend_args* a, AttendPlan* p);
+
+// Kernel parameters of the attention (one struct, passed by value).
+struct AttendParams {
+  int B, t, nh, nk, hd, cap, ns, hpg;
+  float qmul;                 // scale * log2(e): scores are kept in log2 units
+  const swa_meta* meta;
+  const float* q;
+  const float* k_chunk;
+  const float* v_chunk;
+  float* ring_k;
+  float* ring_v;
+  const float* sink_k;
+  const float* sink_v;
+  const float* gate;
+  const float* gate_scale;
+  float* out;
+  float* ws_acc;              // [items][nq][hd]
+  float2* ws_ml;              // [items][nq] (m in log2 units, l)
+  int* ws_nsplit;             // [B][n_rb]
+  int commit;
+  swa_meta* meta_out;
+  uint32_t* err;
+  int nq, rows, n_rb, chunk, splits;
+};
+
+int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+int launch_attend_merge(const AttendParams& p, cudaStream_t s);
+int attend_partial_occupancy(int hd, int nq);   // resident CTAs per SM
+
+struct PrepParams {
+  int B, t, nh, nk, hd, cap;
+  float eps;
+  const float* yq;
+  const float* yk;
+  const float* yv;
+  const float* rope;
+  const float* q_scale;
+  const uint32_t* pos0;
+  float* q_out;
+  float* k_out;
+  float* v_out;
+  float* ring_k;
+  float* ring_v;
+};
+int launch_prep(const PrepParams& p, cudaStream_t s);
+int launch_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd,
+                      const double* inv_freq, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
+// Device helpers: mbarrier, bulk copies into shared memory, bounded waits.
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+               :: "r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the barrier's phase `parity` to complete, for at most `limit_ns`
+// nanoseconds of wall time. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Order this thread's earlier shared-memory accesses (generic proxy) before
+// later bulk copies (async proxy) that overwrite the same bytes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy (TMA, non-tensor) of `bytes` (multiple of 16, both addresses
+// 16-byte aligned) from global memory into this CTA's shared memory; the
+// transaction count of `bar` is decremented by `bytes` when it lands.
+__device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(smem_u32(dst_smem)), "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void set_err(uint32_t* err, uint32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+#endif  // __CUDACC__
+
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per bounded wait
+
+}  // namespace swa

@@ -1,0 +1,165 @@
+// Prep stage: rotation, unit heads, query scale, ring write ("dory_msl.metal",
+// cortiq-engine 0.8.57, kernel dory_prep), and the RoPE table it consumes.
+//
+// One warp per (row, head): the q heads of a row come first, then its k heads
+// (the same split of the head index as dory_prep). Lane l owns the hd/64
+// rotated pairs (e, e + hd/2) with e in [l*hd/64, (l+1)*hd/64), so both halves
+// of a head are read and written as contiguous, coalesced vectors. The sum of
+// squares is a butterfly over the warp. Every byte moves once: the kernel is
+// bandwidth-bound and tiny next to the attention.
+#include "swa_internal.cuh"
+
+namespace swa {
+namespace {
+
+template <int P> struct VecT;
+template <> struct VecT<1> { using T = float; };
+template <> struct VecT<2> { using T = float2; };
+template <> struct VecT<4> { using T = float4; };
+
+template <int P>
+__device__ __forceinline__ void ldv(const float* p, float (&r)[P]) {
+  typename VecT<P>::T v = *reinterpret_cast<const typename VecT<P>::T*>(p);
+  const float* f = reinterpret_cast<const float*>(&v);
+#pragma unroll
+  for (int i = 0; i < P; ++i) r[i] = f[i];
+}
+
+template <int P>
+__device__ __forceinline__ void stv(float* p, const float (&r)[P]) {
+  typename VecT<P>::T v;
+  float* f = reinterpret_cast<float*>(&v);
+#pragma unroll
+  for (int i = 0; i < P; ++i) f[i] = r[i];
+  *reinterpret_cast<typename VecT<P>::T*>(p) = v;
+}
+
+constexpr int kPrepWarps = 8;
+
+template <int HD>
+__global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
+  constexpr int P = HD / 64;       // pairs per lane
+  constexpr int HALF = HD / 2;
+  const int row = blockIdx.x;      // b * t + j
+  const int a = blockIdx.y * kPrepWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (a >= p.nh + p.nk) return;
+  const int e = lane * P;
+
+  float c[P], s[P];
+  const float* rope = p.rope + (size_t)row * HD;
+  ldv<P>(rope + e, c);
+  ldv<P>(rope + HALF + e, s);
+
+  const bool is_q = a < p.nh;
+  const int kh = a - p.nh;
+  const float* src = is_q ? p.yq + ((size_t)row * p.nh + a) * HD
+                          : p.yk + ((size_t)row * p.nk + kh) * HD;
+  float x[P], y[P], u[P], v[P];
+  ldv<P>(src + e, x);
+  ldv<P>(src + HALF + e, y);
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    u[i] = x[i] * c[i] - y[i] * s[i];
+    v[i] = y[i] * c[i] + x[i] * s[i];
+    ss += u[i] * u[i] + v[i] * v[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = 1.0f / sqrtf(ss + p.eps);
+
+  if (is_q) {
+    float sa[P], sb[P];
+    ldv<P>(p.q_scale + (size_t)a * HD + e, sa);
+    ldv<P>(p.q_scale + (size_t)a * HD + HALF + e, sb);
+#pragma unroll
+    for (int i = 0; i < P; ++i) {
+      u[i] = u[i] * inv * sa[i];
+      v[i] = v[i] * inv * sb[i];
+    }
+    float* dst = p.q_out + ((size_t)row * p.nh + a) * HD;
+    stv<P>(dst + e, u);
+    stv<P>(dst + HALF + e, v);
+    return;
+  }
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    u[i] *= inv;
+    v[i] *= inv;
+  }
+  float* kd = p.k_out + ((size_t)row * p.nk + kh) * HD;
+  stv<P>(kd + e, u);
+  stv<P>(kd + HALF + e, v);
+  const float* vs = p.yv + ((size_t)row * p.nk + kh) * HD;
+  float va[P], vb[P];
+  ldv<P>(vs + e, va);
+  ldv<P>(vs + HALF + e, vb);
+  if (p.v_out) {
+    float* vd = p.v_out + ((size_t)row * p.nk + kh) * HD;
+    stv<P>(vd + e, va);
+    stv<P>(vd + HALF + e, vb);
+  }
+  if (p.ring_k) {
+    const int b = row / p.t, j = row % p.t;
+    const uint32_t slot = (uint32_t)(((uint64_t)p.pos0[b] + (uint64_t)j) % (uint64_t)p.cap);
+    const size_t at = (((size_t)b * p.nk + kh) * p.cap + slot) * HD;
+    stv<P>(p.ring_k + at + e, u);
+    stv<P>(p.ring_k + at + HALF + e, v);
+    stv<P>(p.ring_v + at + e, va);
+    stv<P>(p.ring_v + at + HALF + e, vb);
+  }
+}
+
+struct RopeFreq {
+  double inv_freq[128];
+};
+
+// One thread per (row, pair e): angle in f64 from the absolute position and the
+// host-computed frequency theta^(-2e/hd); cos/sin in f64, stored as f32.
+__global__ void rope_table_kernel(float* rope, const uint32_t* pos0, int B, int t, int hd,
+                                  RopeFreq f) {
+  const int half = hd / 2;
+  const size_t n = (size_t)B * t * half;
+  for (size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n;
+       idx += (size_t)gridDim.x * blockDim.x) {
+    const int e = (int)(idx % half);
+    const size_t r = idx / half;
+    const int b = (int)(r / t), j = (int)(r % t);
+    const double pos = (double)pos0[b] + (double)j;
+    double sn, cs;
+    sincos(pos * f.inv_freq[e], &sn, &cs);
+    rope[r * hd + e] = (float)cs;
+    rope[r * hd + half + e] = (float)sn;
+  }
+}
+
+}  // namespace
+
+int launch_prep(const PrepParams& p, cudaStream_t s) {
+  dim3 grid((unsigned)(p.B * p.t), (unsigned)((p.nh + p.nk + kPrepWarps - 1) / kPrepWarps));
+  dim3 block(kPrepWarps * 32);
+  switch (p.hd) {
+    case 64: prep_kernel<64><<<grid, block, 0, s>>>(p); break;
+    case 128: prep_kernel<128><<<grid, block, 0, s>>>(p); break;
+    case 256: prep_kernel<256><<<grid, block, 0, s>>>(p); break;
+    default: return SWA_E_SHAPE;
+  }
+  note_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+int launch_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd,
+                      const double* inv_freq, cudaStream_t s) {
+  RopeFreq f;
+  for (int e = 0; e < 128; ++e) f.inv_freq[e] = e < hd / 2 ? inv_freq[e] : 0.0;
+  const size_t n = (size_t)B * t * (hd / 2);
+  const int block = 256;
+  const size_t want = (n + block - 1) / block;
+  const unsigned grid = (unsigned)(want < 4096 ? (want ? want : 1) : 4096);
+  rope_table_kernel<<<grid, block, 0, s>>>(rope, pos0, B, t, hd, f);
+  note_launch();
+  return cuda_status(cudaGetLastError());
+}
+
+}  // namespace swa

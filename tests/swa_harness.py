@@ -1,0 +1,106 @@
+"""Shared helpers of the parity tests: run the CUDA path and the CPU oracle on
+the same seeded inputs and compare them.
+
+Tolerance (floating point outputs, per tensor): max |gpu - oracle| <= 2e-5 and
+max |gpu - oracle| / max |oracle| <= 1e-4. Integer results (ring slots, meta)
+are compared exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import workloads
+import sliding_window_gqa_prep_gb300 as swa
+
+MAX_ABS = 2e-5
+MAX_REL = 1e-4
+
+
+def assert_close(gpu, ref, what, max_abs=MAX_ABS, max_rel=MAX_REL):
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert gpu.shape == ref.shape, (what, gpu.shape, ref.shape)
+    assert np.all(np.isfinite(gpu)), f"{what}: non-finite GPU values"
+    err = np.max(np.abs(gpu - ref)) if gpu.size else 0.0
+    scale = np.max(np.abs(ref)) if ref.size else 0.0
+    rel = err / scale if scale > 0 else err
+    assert err <= max_abs and rel <= max_rel, f"{what}: max_abs {err:.3e}, rel {rel:.3e}"
+    return err, rel
+
+
+def to_dev(inp, dev="cuda"):
+    out = {}
+    for k, v in inp.items():
+        if k in ("meta", "pos0"):
+            out[k] = v.to(torch.int32).to(dev).contiguous()
+        else:
+            out[k] = v.to(dev).contiguous()
+    return out
+
+
+def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_alias=False):
+    """rope table -> prep -> attend (+ commit) on the GPU. The prep writes the
+    ring only for t == 1 with window == cap (prep's slot map); otherwise the
+    attend's commit does."""
+    d = to_dev(inp)
+    if prep_ring is None:
+        prep_ring = w.t == 1 and w.window == w.cap
+    rope = swa.rope_table(d["pos0"], w.t, w.hd, w.theta)
+    ring_k, ring_v = d["ring_k"].clone(), d["ring_v"].clone()
+    q, k, v = swa.prep(d["yq"], d["yk"], d["yv"], rope, d["q_scale"], w.eps, pos0=d["pos0"],
+                       ring_k=ring_k if prep_ring else None,
+                       ring_v=ring_v if prep_ring else None)
+    ring_after_prep_k = ring_k.clone() if prep_ring else None
+    meta = d["meta"].clone()
+    meta_out = meta if meta_alias else torch.full_like(meta, -1)
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = swa.attend(meta, q, k, v, ring_k, ring_v, d["sink_k"] if w.ns else None,
+                     d["sink_v"] if w.ns else None, d["gate"], d["gate_scale"], w.score_scale,
+                     commit=commit, meta_out=meta_out, num_splits=num_splits, err=err)
+    torch.cuda.synchronize()
+    return {
+        "rope": rope.cpu().numpy(), "q": q.cpu().numpy(), "k": k.cpu().numpy(),
+        "v": v.cpu().numpy(), "out": out.cpu().numpy(), "ring_k": ring_k.cpu().numpy(),
+        "ring_v": ring_v.cpu().numpy(), "meta_out": meta_out.cpu().numpy(),
+        "err": int(err.item()),
+        "ring_after_prep_k": None if ring_after_prep_k is None else ring_after_prep_k.cpu().numpy(),
+    }
+
+
+def oracle_inputs(w, inp, q=None, k=None, v=None):
+    """The oracle's attend inputs: its own prep unless q/k/v are given."""
+    if q is None:
+        rope = oracle.rope_table(inp["pos0"].numpy(), w.t, w.hd, w.theta)
+        q, k, v = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope,
+                              inp["q_scale"].numpy(), w.eps)
+    return {
+        "meta": inp["meta"].numpy(), "q": q, "k_chunk": k, "v_chunk": v,
+        "ring_k": inp["ring_k"].numpy(), "ring_v": inp["ring_v"].numpy(),
+        "sink_k": inp["sink_k"].numpy(), "sink_v": inp["sink_v"].numpy(),
+        "gate": inp["gate"].numpy(), "gate_scale": inp["gate_scale"].numpy(),
+    }
+
+
+def check_commit_placement(w, inp, res):
+    """Ring after the commit: each slot the oracle's slot map assigns to chunk
+    row j holds the GPU's own k/v row j bit for bit; every other slot is
+    unchanged (bit for bit). Meta after the commit equals the oracle's."""
+    meta = inp["meta"].numpy()
+    ring0_k = inp["ring_k"].numpy()
+    ring0_v = inp["ring_v"].numpy()
+    for b in range(w.B):
+        final = {}
+        for j in range(w.t):
+            final[oracle.commit_slot(meta[b], j, w.cap)] = j
+        for slot in range(w.cap):
+            if slot in final:
+                j = final[slot]
+                np.testing.assert_array_equal(res["ring_k"][b, :, slot], res["k"][b, j])
+                np.testing.assert_array_equal(res["ring_v"][b, :, slot], res["v"][b, j])
+            else:
+                np.testing.assert_array_equal(res["ring_k"][b, :, slot], ring0_k[b, :, slot])
+                np.testing.assert_array_equal(res["ring_v"][b, :, slot], ring0_v[b, :, slot])
+        expect = oracle.commit_meta(meta[b], w.t, w.cap)
+        assert res["meta_out"][b].astype(np.int64).tolist() == expect.tolist(), (b, res["meta_out"][b], expect)

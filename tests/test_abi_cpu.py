@@ -1,0 +1,119 @@
+"""The C ABI without a GPU: the library builds, loads, exports every entry
+point include/swa.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run on a machine with no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from sliding_window_gqa_prep_gb300 import _abi
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w\s\*]*?\b(swa_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return _abi.load()
+
+
+def test_header_declares_the_path(lib):
+    names = declared_functions()
+    for n in ("swa_prep", "swa_attend", "swa_attend_workspace_size", "swa_rope_table",
+              "swa_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert lib.swa_status_string(code)
+    assert b"unknown" in lib.swa_status_string(-99)
+    assert b"sm_103a" in lib.swa_version()
+
+
+FAKE = 0x10000  # an aligned address that is never dereferenced: checks fail first
+
+
+def _prep(**kw):
+    a = _abi.PrepArgs()
+    a.B, a.t, a.nh, a.nk, a.hd, a.cap, a.eps = 2, 1, 8, 2, 128, 16, 1e-6
+    for f in ("yq", "yk", "yv", "rope", "q_scale", "q_out", "k_out"):
+        setattr(a, f, FAKE)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_prep_rejects_bad_arguments(lib):
+    call = lambda a: lib.swa_prep(ctypes.byref(a), None)
+    assert lib.swa_prep(None, None) == _abi.SWA_E_NULL
+    assert call(_prep(yq=None)) == _abi.SWA_E_NULL
+    assert call(_prep(hd=96)) == _abi.SWA_E_SHAPE
+    assert call(_prep(B=0)) == _abi.SWA_E_SHAPE
+    assert call(_prep(eps=-1.0)) == _abi.SWA_E_SHAPE
+    assert call(_prep(yq=FAKE + 4)) == _abi.SWA_E_ALIGN
+    # ring write: both rings and pos0 needed, and only for t == 1
+    assert call(_prep(ring_k=FAKE)) == _abi.SWA_E_NULL
+    assert call(_prep(ring_k=FAKE, ring_v=FAKE)) == _abi.SWA_E_NULL
+    assert call(_prep(t=4, ring_k=FAKE, ring_v=FAKE, pos0=FAKE)) == _abi.SWA_E_HAZARD
+    assert call(_prep(cap=0, ring_k=FAKE, ring_v=FAKE, pos0=FAKE)) == _abi.SWA_E_SHAPE
+
+
+def _attend(**kw):
+    a = _abi.AttendArgs()
+    a.B, a.t, a.nh, a.nk, a.hd, a.cap, a.ns = 2, 1, 8, 2, 128, 64, 2
+    a.scale = 0.1
+    for f in ("meta", "q", "k_chunk", "v_chunk", "ring_k", "ring_v", "sink_k", "sink_v", "gate",
+              "gate_scale", "out", "workspace"):
+        setattr(a, f, FAKE)
+    a.workspace_bytes = 1 << 40
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_attend_rejects_bad_arguments(lib):
+    call = lambda a: lib.swa_attend(ctypes.byref(a), None)
+    assert lib.swa_attend(None, None) == _abi.SWA_E_NULL
+    assert call(_attend(q=None)) == _abi.SWA_E_NULL
+    assert call(_attend(sink_k=None)) == _abi.SWA_E_NULL          # ns > 0 needs sinks
+    assert call(_attend(commit=1)) == _abi.SWA_E_NULL             # commit needs meta_out
+    assert call(_attend(hd=100)) == _abi.SWA_E_SHAPE
+    assert call(_attend(nh=9)) == _abi.SWA_E_SHAPE                # nh % nk
+    assert call(_attend(nh=66)) == _abi.SWA_E_SHAPE               # 33 q heads per KV head
+    assert call(_attend(cap=0)) == _abi.SWA_E_SHAPE
+    assert call(_attend(ns=-1)) == _abi.SWA_E_SHAPE
+    assert call(_attend(scale=float("nan"))) == _abi.SWA_E_SHAPE
+    assert call(_attend(out=FAKE + 8)) == _abi.SWA_E_ALIGN
+    assert call(_attend(workspace_bytes=16)) == _abi.SWA_E_WORKSPACE
+    assert call(_attend(workspace=None)) == _abi.SWA_E_WORKSPACE
+    assert call(_attend(workspace=FAKE + 16)) == _abi.SWA_E_ALIGN  # workspace wants 256 B
+
+
+def test_workspace_size_rejects_bad_sizes(lib):
+    assert lib.swa_attend_workspace_size(None) == 0
+    a = _attend(hd=100)
+    assert lib.swa_attend_workspace_size(ctypes.byref(a)) == 0
+
+
+def test_rope_table_rejects_bad_arguments(lib):
+    assert lib.swa_rope_table(None, FAKE, 1, 1, 64, 1e4, None) == _abi.SWA_E_NULL
+    assert lib.swa_rope_table(FAKE, FAKE, 1, 1, 48, 1e4, None) == _abi.SWA_E_SHAPE
+    assert lib.swa_rope_table(FAKE, FAKE, 1, 1, 64, -1.0, None) == _abi.SWA_E_SHAPE
+    assert lib.swa_rope_table(FAKE + 4, FAKE, 1, 1, 64, 1e4, None) == _abi.SWA_E_ALIGN

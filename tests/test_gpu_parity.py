@@ -1,0 +1,310 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle on the GPU.
+
+Floating point: max_abs <= 2e-5 and max_abs / max|oracle| <= 1e-4 per tensor.
+Ring slots, window bounds and meta: exact.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import sliding_window_gqa_prep_gb300 as swa
+from swa_harness import (assert_close, check_commit_placement, gpu_full_path, oracle_inputs,
+                         to_dev)
+
+pytestmark = pytest.mark.gpu
+
+requires_gpu = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without a GPU")
+    yield
+
+
+# ---------------------------------------------------------------------------
+# rope table and prep
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_rope_table_matches_oracle_to_one_ulp(hd):
+    pos0 = np.array([0, 1, 99, 4095, 20000, 131071, 262143], dtype=np.int64)
+    t = 3
+    gpu = swa.rope_table(torch.tensor(pos0, dtype=torch.int32, device="cuda"), t, hd).cpu().numpy()
+    ref = oracle.rope_table(pos0, t, hd)
+    ulp = np.spacing(np.abs(ref).astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(gpu.astype(np.float64) - ref) <= ulp + 1e-30)
+
+
+PREP_CASES = [
+    dict(B=3, t=1, nh=8, nk=2, hd=64, window=32, cap=32, pos_mode="full", pos_lo=32, pos_hi=500),
+    dict(B=2, t=5, nh=16, nk=4, hd=128, window=64, cap=64, pos_mode="full", pos_lo=64, pos_hi=9000),
+    dict(B=2, t=1, nh=8, nk=2, hd=256, window=16, cap=16, pos_mode="full", pos_lo=16, pos_hi=130000),
+    dict(B=1, t=7, nh=6, nk=3, hd=64, window=16, cap=16, pos_mode="prompt", pos_lo=0, pos_hi=40),
+]
+
+
+@pytest.mark.parametrize("kw", PREP_CASES)
+def test_prep_matches_oracle_and_writes_ring_slots_exactly(kw):
+    w = workloads.custom(seed=11, **kw)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=False)
+    rope = oracle.rope_table(inp["pos0"].numpy(), w.t, w.hd, w.theta)
+    q, k, v = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope,
+                          inp["q_scale"].numpy(), w.eps)
+    assert_close(res["q"], q, "q_hat")
+    assert_close(res["k"], k, "k_hat")
+    np.testing.assert_array_equal(res["v"], inp["yv"].numpy())
+    if w.t == 1:
+        # prep's ring write: slot (pos0 + j) % cap holds the GPU's k row bit for bit,
+        # every other slot is untouched
+        ring = res["ring_after_prep_k"]
+        for b in range(w.B):
+            slot = oracle.prep_ring_slot(int(inp["pos0"][b]), 0, w.cap)
+            for s in range(w.cap):
+                want = res["k"][b, 0] if s == slot else inp["ring_k"].numpy()[b, :, s]
+                np.testing.assert_array_equal(ring[b, :, s], want)
+
+
+# ---------------------------------------------------------------------------
+# attend: full path (generator -> rope -> prep -> attend -> commit) vs oracle
+# ---------------------------------------------------------------------------
+ATTEND_CASES = [
+    # decode, wrapped ring, several tiles + ragged tail, sinks
+    dict(B=3, t=1, nh=8, nk=2, hd=128, window=200, cap=200, ns=3, pos_mode="full", pos_lo=200, pos_hi=5000),
+    # tiny decode shape
+    dict(B=1, t=1, nh=8, nk=2, hd=64, window=32, cap=32, ns=0, pos_mode="fixed", pos_lo=100),
+    # long head dim, one KV head
+    dict(B=2, t=1, nh=4, nk=1, hd=256, window=300, cap=300, ns=8, pos_mode="full", pos_lo=300, pos_hi=99999),
+    # verify: partially filled rings, causal chunk
+    dict(B=4, t=8, nh=16, nk=4, hd=128, window=150, cap=150, ns=4, pos_mode="partial", pos_lo=1, pos_hi=150),
+    # prompt chunk longer than the window, empty ring in sequence 0
+    dict(B=2, t=40, nh=8, nk=2, hd=64, window=24, cap=24, ns=2, pos_mode="prompt", pos_lo=0, pos_hi=60),
+    # one key window
+    dict(B=2, t=3, nh=4, nk=1, hd=64, window=1, cap=1, ns=0, pos_mode="full", pos_lo=1, pos_hi=50),
+    # ragged query block (t * hpg not a power of two), hpg = 6
+    dict(B=2, t=3, nh=12, nk=2, hd=128, window=70, cap=70, ns=1, pos_mode="full", pos_lo=70, pos_hi=999),
+    # hpg = 1 and hpg = 32
+    dict(B=2, t=2, nh=2, nk=2, hd=64, window=40, cap=40, ns=0, pos_mode="partial", pos_lo=1, pos_hi=40),
+    dict(B=1, t=1, nh=32, nk=1, hd=128, window=90, cap=90, ns=2, pos_mode="full", pos_lo=90, pos_hi=400),
+    # hd 256, verify-sized block
+    dict(B=2, t=8, nh=8, nk=2, hd=256, window=64, cap=64, ns=4, pos_mode="full", pos_lo=64, pos_hi=700),
+]
+
+
+@pytest.mark.parametrize("kw", ATTEND_CASES)
+@pytest.mark.parametrize("sharp", [False, True])
+def test_full_path_matches_oracle(kw, sharp):
+    w = workloads.custom(seed=5, scale=4.0 if sharp else None, **kw)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=True)
+    assert res["err"] == 0
+    a = oracle_inputs(w, inp)
+    ref = oracle.attend(a, w.score_scale, w.hpg)
+    assert_close(res["out"], ref, "out")
+    check_commit_placement(w, inp, res)
+
+
+def test_attend_only_matches_oracle_on_shared_q_k():
+    """Attend fed the same (generator-drawn) q and chunk k/v on both sides."""
+    w = workloads.custom(B=3, t=8, nh=16, nk=4, hd=128, window=100, cap=100, ns=4,
+                         pos_mode="partial", pos_lo=1, pos_hi=100, seed=21, scale=1.0)
+    inp = workloads.make_inputs(w)
+    g = torch.Generator().manual_seed(99)
+    q = torch.randn(w.B, w.t, w.nh, w.hd, generator=g)
+    k = torch.randn(w.B, w.t, w.nk, w.hd, generator=g)
+    v = torch.randn(w.B, w.t, w.nk, w.hd, generator=g)
+    d = to_dev(inp)
+    meta_out = torch.empty_like(d["meta"])
+    out = swa.attend(d["meta"], q.cuda(), k.cuda(), v.cuda(), d["ring_k"], d["ring_v"],
+                     d["sink_k"], d["sink_v"], d["gate"], d["gate_scale"], w.score_scale,
+                     commit=False, meta_out=meta_out)
+    ref = oracle.attend(oracle_inputs(w, inp, q.numpy(), k.numpy(), v.numpy()), w.score_scale, w.hpg)
+    assert_close(out.cpu().numpy(), ref, "out")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+def test_split_count_invariance(splits):
+    w = workloads.custom(B=2, t=4, nh=8, nk=2, hd=128, window=500, cap=500, ns=4,
+                         pos_mode="full", pos_lo=500, pos_hi=9000, seed=3, scale=3.0)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=False, num_splits=splits)
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, f"out (splits={splits})")
+
+
+def test_window_bounds_exact_via_one_hot_values():
+    """Uniform scores (q = 0) and one-hot values that name each key: the set of
+    keys each row attends is read back exactly and compared with the oracle's
+    key list (sinks, ring slots, chunk rows)."""
+    B, t, nh, nk, hd, cap, ns = 3, 8, 4, 1, 128, 100, 4
+    w = workloads.custom(B=B, t=t, nh=nh, nk=nk, hd=hd, window=cap, cap=cap, ns=ns,
+                         pos_mode="partial", pos_lo=1, pos_hi=cap, seed=8)
+    inp = workloads.make_inputs(w)
+    ring_v = torch.zeros(B, nk, cap, hd)
+    for s in range(cap):
+        ring_v[:, :, s, s] = 1.0
+    sink_v = torch.zeros(B, nk, ns, hd)
+    for s in range(ns):
+        sink_v[:, :, s, cap + s] = 1.0
+    v_chunk = torch.zeros(B, t, nk, hd)
+    for j in range(t):
+        v_chunk[:, j, :, cap + ns + j] = 1.0
+    d = to_dev(inp)
+    q = torch.zeros(B, t, nh, hd, device="cuda")
+    k = torch.randn(B, t, nk, hd, device="cuda")
+    gate = torch.zeros(B, t, nh, hd, device="cuda")          # sigmoid(0) = 1/2
+    meta_out = torch.empty_like(d["meta"])
+    out = swa.attend(d["meta"], q, k, v_chunk.cuda(), d["ring_k"], ring_v.cuda(), d["sink_k"],
+                     sink_v.cuda(), gate, d["gate_scale"], w.score_scale, meta_out=meta_out)
+    out = out.cpu().numpy() * 2.0
+    meta = inp["meta"].numpy()
+    for b in range(B):
+        for i in range(t):
+            keys = oracle.row_key_list(meta[b], i, ns, cap)
+            want = set()
+            for kind, idx in keys:
+                want.add(idx if kind == "ring" else (cap + idx if kind == "sink" else cap + ns + idx))
+            for h in range(nh):
+                got = set(np.nonzero(out[b, i, h] > 0.5 / len(keys))[0].tolist())
+                assert got == want, (b, i, h)
+                np.testing.assert_allclose(out[b, i, h][sorted(want)], 1.0 / len(keys), rtol=1e-5)
+
+
+def test_out_of_window_ring_slots_are_never_read():
+    """NaN in every ring slot outside the pre-chunk window (and in the slots the
+    chunk will overwrite): outputs stay finite, so no such slot is loaded."""
+    w = workloads.custom(B=4, t=8, nh=8, nk=2, hd=128, window=64, cap=96, ns=2,
+                         pos_mode="partial", pos_lo=1, pos_hi=64, seed=4)
+    inp = workloads.make_inputs(w)
+    meta = inp["meta"].numpy()
+    for b in range(w.B):
+        len0, head0 = int(meta[b][0]), int(meta[b][1])
+        live = {(head0 + x) % 64 for x in range(len0)}
+        for s in range(w.cap):
+            if s not in live:
+                inp["ring_k"][b, :, s] = float("nan")
+                inp["ring_v"][b, :, s] = float("nan")
+    res = gpu_full_path(w, inp, commit=False)
+    assert np.all(np.isfinite(res["out"]))
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, "out")
+
+
+def test_window_smaller_than_cap_and_zero_window_field():
+    w = workloads.custom(B=2, t=4, nh=8, nk=2, hd=64, window=40, cap=64, ns=1,
+                         pos_mode="full", pos_lo=40, pos_hi=3000, seed=12)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=True)
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, "out")
+    check_commit_placement(w, inp, res)
+    # window field 0 means cap
+    w0 = workloads.custom(B=2, t=2, nh=4, nk=1, hd=64, window=48, cap=48, ns=0,
+                          pos_mode="full", pos_lo=48, pos_hi=3000, seed=13)
+    inp0 = workloads.make_inputs(w0)
+    inp0["meta"][:, 3] = 0
+    res0 = gpu_full_path(w0, inp0, commit=True)
+    ref0 = oracle.attend(oracle_inputs(w0, inp0), w0.score_scale, w0.hpg)
+    assert_close(res0["out"], ref0, "out")
+    check_commit_placement(w0, inp0, res0)
+
+
+def test_commit_with_meta_out_aliasing_meta():
+    w = workloads.custom(B=3, t=5, nh=8, nk=2, hd=128, window=32, cap=32, ns=0,
+                         pos_mode="full", pos_lo=32, pos_hi=900, seed=14)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=True, meta_alias=True)
+    check_commit_placement(w, inp, res)
+
+
+def test_chunk_equals_sequential_decode_steps_on_gpu():
+    """A t-row chunk with commit == t single-row steps, each committing and
+    advancing the meta: outputs within tolerance, final ring and meta exact."""
+    w = workloads.custom(B=2, t=6, nh=8, nk=2, hd=128, window=48, cap=48, ns=2,
+                         pos_mode="full", pos_lo=48, pos_hi=2000, seed=15)
+    inp = workloads.make_inputs(w)
+    chunk = gpu_full_path(w, inp, commit=True)
+    d = to_dev(inp)
+    rope = swa.rope_table(d["pos0"], w.t, w.hd, w.theta)
+    q, k, v = swa.prep(d["yq"], d["yk"], d["yv"], rope, d["q_scale"], w.eps)
+    ring_k, ring_v = d["ring_k"].clone(), d["ring_v"].clone()
+    meta = d["meta"].clone()
+    outs = []
+    for i in range(w.t):
+        meta_next = torch.empty_like(meta)
+        o = swa.attend(meta, q[:, i:i + 1].contiguous(), k[:, i:i + 1].contiguous(),
+                       v[:, i:i + 1].contiguous(), ring_k, ring_v, d["sink_k"], d["sink_v"],
+                       d["gate"][:, i:i + 1].contiguous(), d["gate_scale"], w.score_scale,
+                       commit=True, meta_out=meta_next)
+        outs.append(o.clone())
+        meta = meta_next
+    seq_out = torch.cat(outs, dim=1).cpu().numpy()
+    assert_close(seq_out, chunk["out"], "sequential vs chunk")
+    np.testing.assert_array_equal(ring_k.cpu().numpy(), chunk["ring_k"])
+    np.testing.assert_array_equal(ring_v.cpu().numpy(), chunk["ring_v"])
+    np.testing.assert_array_equal(meta.cpu().numpy(), chunk["meta_out"])
+
+
+def test_bad_meta_sets_error_word_without_fault():
+    w = workloads.custom(B=2, t=1, nh=4, nk=1, hd=64, window=16, cap=16, ns=0,
+                         pos_mode="full", pos_lo=16, pos_hi=100, seed=16)
+    inp = workloads.make_inputs(w)
+    inp["meta"][0, 0] = 50       # win_len > window
+    inp["meta"][1, 3] = 1000     # window > cap
+    res = gpu_full_path(w, inp, commit=False)
+    assert res["err"] & swa.SWA_DERR_META
+    assert np.all(np.isfinite(res["out"]))
+
+
+def test_token_path_host_step_matches_device_step():
+    w = workloads.custom(B=2, t=1, nh=8, nk=2, hd=128, window=64, cap=64, ns=2,
+                         pos_mode="full", pos_lo=64, pos_hi=900, seed=17)
+    inp = workloads.make_inputs(w)
+    mk = lambda: swa.TokenPath(B=w.B, t=w.t, nh=w.nh, nk=w.nk, hd=w.hd, cap=w.cap, ns=w.ns,
+                               q_scale=inp["q_scale"], gate_scale=inp["gate_scale"],
+                               ring_k=inp["ring_k"], ring_v=inp["ring_v"], sink_k=inp["sink_k"],
+                               sink_v=inp["sink_v"], meta=inp["meta"], pos0=inp["pos0"])
+    host = mk().step(inp["yq"].pin_memory(), inp["yk"].pin_memory(), inp["yv"].pin_memory(),
+                     inp["gate"].pin_memory(), out_host=torch.empty(w.B, w.t, w.nh, w.hd).pin_memory())
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(host.numpy(), ref, "out")
+
+
+# ---------------------------------------------------------------------------
+# the five named workloads at full size, in the launch configuration the bench
+# times (automatic splits): every prep output, sampled attention outputs
+# ---------------------------------------------------------------------------
+SAMPLES = {"tiny_decode": 16, "batched_decode": 24, "spec_verify": 24, "prompt_chunk": 24,
+           "long_decode": 10}
+
+
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_named_workload_full_size(name):
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=True)
+    assert res["err"] == 0
+    rope = oracle.rope_table(inp["pos0"].numpy(), w.t, w.hd, w.theta)
+    q, k, v = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope,
+                          inp["q_scale"].numpy(), w.eps)
+    assert_close(res["q"], q, "q_hat")
+    assert_close(res["k"], k, "k_hat")
+    a = oracle_inputs(w, inp, q, k, v)
+    rng = np.random.default_rng(7)
+    picks = [(0, 0, 0), (w.B - 1, w.t - 1, w.nh - 1)]
+    while len(picks) < SAMPLES[name]:
+        picks.append((int(rng.integers(w.B)), int(rng.integers(w.t)), int(rng.integers(w.nh))))
+    got = np.stack([res["out"][b, i, h] for b, i, h in picks])
+    ref = np.stack([oracle.attend_row(b, i, h, a, w.score_scale, w.hpg) for b, i, h in picks])
+    assert_close(got, ref, f"{name} sampled out")
+    # every output is finite and the meta after the commit is exact for all sequences
+    assert np.all(np.isfinite(res["out"]))
+    meta = inp["meta"].numpy()
+    for b in range(w.B):
+        assert res["meta_out"][b].astype(np.int64).tolist() == \
+            oracle.commit_meta(meta[b], w.t, w.cap).tolist()
