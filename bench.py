@@ -59,6 +59,8 @@ def parse_args():
                     help="CPU time budget of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's sequence count (small profiling cases)")
     return ap.parse_args()
 
 
@@ -154,73 +156,83 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # CPU oracle timing (baseline / reference arm)
 # ---------------------------------------------------------------------------
-def oracle_units(w, inp, units):
-    """Run the oracle (rope table, prep of the sequence's rows, attention of
-    every query head of the sampled (sequence, row, KV head) units). Returns
-    the attended KV-keys of the units."""
+def oracle_prep_seq(w, inp, b):
+    """The oracle's rope table and prep of sequence b; returns its attend inputs."""
     import oracle
-    keys = 0
-    by_seq = {}
-    for b, i, g in units:
-        by_seq.setdefault(b, []).append((i, g))
-    for b, lst in by_seq.items():
-        rope = oracle.rope_table(inp["pos0"].numpy()[b:b + 1], w.t, w.hd, w.theta)
-        q, k, v = oracle.prep(inp["yq"].numpy()[b:b + 1], inp["yk"].numpy()[b:b + 1],
-                              inp["yv"].numpy()[b:b + 1], rope, inp["q_scale"].numpy(), w.eps)
-        a = {"meta": inp["meta"].numpy()[b:b + 1], "q": q, "k_chunk": k, "v_chunk": v,
-             "ring_k": inp["ring_k"].numpy()[b:b + 1], "ring_v": inp["ring_v"].numpy()[b:b + 1],
-             "sink_k": inp["sink_k"].numpy()[b:b + 1], "sink_v": inp["sink_v"].numpy()[b:b + 1],
-             "gate": inp["gate"].numpy()[b:b + 1], "gate_scale": inp["gate_scale"].numpy()}
-        for i, g in lst:
-            for h in range(g * w.hpg, (g + 1) * w.hpg):
-                oracle.attend_row(0, i, h, a, w.score_scale, w.hpg)
-            L, W = int(a["meta"][0][0]), int(a["meta"][0][3])
-            keys += w.ns + min(W, L + i + 1)
-    return keys
+    rope = oracle.rope_table(inp["pos0"].numpy()[b:b + 1], w.t, w.hd, w.theta)
+    q, k, v = oracle.prep(inp["yq"].numpy()[b:b + 1], inp["yk"].numpy()[b:b + 1],
+                          inp["yv"].numpy()[b:b + 1], rope, inp["q_scale"].numpy(), w.eps)
+    return {"meta": inp["meta"].numpy()[b:b + 1], "q": q, "k_chunk": k, "v_chunk": v,
+            "ring_k": inp["ring_k"].numpy()[b:b + 1], "ring_v": inp["ring_v"].numpy()[b:b + 1],
+            "sink_k": inp["sink_k"].numpy()[b:b + 1], "sink_v": inp["sink_v"].numpy()[b:b + 1],
+            "gate": inp["gate"].numpy()[b:b + 1], "gate_scale": inp["gate_scale"].numpy()}
 
 
-def sample_inputs(w, nseq=2):
+def oracle_unit(w, a, i, g):
+    """The oracle's attention of every query head of KV head g in row i;
+    returns the attended KV-keys of the unit."""
+    import oracle
+    for h in range(g * w.hpg, (g + 1) * w.hpg):
+        oracle.attend_row(0, i, h, a, w.score_scale, w.hpg)
+    L, W = int(a["meta"][0][0]), int(a["meta"][0][3])
+    return w.ns + min(W, L + i + 1)
+
+
+def sample_inputs(w, nseq=4):
     return workloads.make_inputs(w, batch=min(w.B, nseq))
 
 
+def _units_of(w, b, seed):
+    units = [(i, g) for i in range(w.t) for g in range(w.nk)]
+    np.random.default_rng(seed + b).shuffle(units)
+    return units
+
+
 def cpu_baseline(w, budget_s):
+    """The oracle on a time-bounded sample: sequences in turn, each prepped
+    (rope table + prep of all its rows) and then attended unit by unit."""
     inp = sample_inputs(w)
     B = inp["meta"].shape[0]
-    all_units = [(b, i, g) for b in range(B) for i in range(w.t) for g in range(w.nk)]
-    rng = np.random.default_rng(0)
-    rng.shuffle(all_units)
     t0 = time.perf_counter()
-    keys, n = 0, 0
-    while n < len(all_units) and time.perf_counter() - t0 < budget_s:
-        keys += oracle_units(w, inp, [all_units[n]])
-        n += 1
+    keys, n, seqs, b = 0, 0, 0, 0
+    while time.perf_counter() - t0 < budget_s:
+        a = oracle_prep_seq(w, inp, b % B)
+        seqs += 1
+        for i, g in _units_of(w, b % B, 0):
+            keys += oracle_unit(w, a, i, g)
+            n += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        b += 1
     dt = time.perf_counter() - t0
     return {"value": keys / dt, "unit": "keys/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} (sequence, row, KV head) units of {w.name} with all their query heads "
-                      f"({keys} attended KV-keys, {dt:.1f} s, numpy float64, one thread)"}
+            "sample": f"{n} (sequence, row, KV head) units of {w.name} over {seqs} prepped sequences, "
+                      f"all query heads of each unit ({keys} attended KV-keys, {dt:.1f} s, "
+                      f"numpy float64, one thread)"}
 
 
 def run_reference(args, w, rank):
-    """Reference arm: the CPU oracle as it stands, on a bounded sample per step."""
+    """Reference arm: the CPU oracle as it stands; each step preps one sequence
+    of the workload and attends a bounded number of its units."""
     if rank != 0:
         return
     inp = sample_inputs(w)
     B = inp["meta"].shape[0]
-    all_units = [(b, i, g) for b in range(B) for i in range(w.t) for g in range(w.nk)]
-    rng = np.random.default_rng(1)
-    rng.shuffle(all_units)
-    t_unit0 = time.perf_counter()
-    oracle_units(w, inp, [all_units[0]])
-    t_unit = max(time.perf_counter() - t_unit0, 1e-4)
+    t_a = time.perf_counter()
+    a0 = oracle_prep_seq(w, inp, 0)
+    t_prep = time.perf_counter() - t_a
+    t_a = time.perf_counter()
+    oracle_unit(w, a0, *_units_of(w, 0, 1)[0])
+    t_unit = max(time.perf_counter() - t_a, 1e-5)
     budget_per_step = 150.0 / max(1, args.steps + args.warmup)
-    per_step = max(1, min(len(all_units), int(budget_per_step / t_unit)))
-    cursor = 0
+    per_step = int(max(1, min(w.t * w.nk, (budget_per_step - t_prep) / t_unit)))
+    state = {"b": 0}
 
     def step():
-        nonlocal cursor
-        units = [all_units[(cursor + k) % len(all_units)] for k in range(per_step)]
-        cursor += per_step
-        return oracle_units(w, inp, units)
+        b = state["b"] % B
+        state["b"] += 1
+        a = oracle_prep_seq(w, inp, b)
+        return sum(oracle_unit(w, a, i, g) for i, g in _units_of(w, b, 1)[:per_step])
 
     for _ in range(args.warmup):
         step()
@@ -230,8 +242,8 @@ def run_reference(args, w, rank):
         keys += step()
     dt = time.perf_counter() - t0
     value = keys / dt
-    sample = (f"{per_step} (sequence, row, KV head) units of {w.name} per step with all their "
-              f"query heads, numpy float64, one thread")
+    sample = (f"per step: rope table + prep of one sequence of {w.name} and {per_step} of its "
+              f"(row, KV head) units with all their query heads; numpy float64, one thread")
     line = {"impl": "reference", "metric": "attended KV-keys/s", "value": value, "unit": "keys/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
@@ -371,6 +383,9 @@ def run_gpu(args, w, rank, world, local_rank):
 def main():
     args = parse_args()
     w = workloads.WORKLOADS[args.workload]
+    if args.batch:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
