@@ -194,6 +194,41 @@ size_t swa_attend_workspace_size(const swa_attend_args* args);
 
 int swa_attend(const swa_attend_args* args, cudaStream_t stream);
 
+/*
+ * swa_attend_noalloc — swa_attend for callers that cannot allocate device
+ * memory. The pages have no counterpart: it is a deployment convenience of
+ * this library, not part of the method.
+ *
+ * Some callers cannot call cudaMalloc at all: a plugin that its host program
+ * hands only the input and output buffers, a serving engine whose device
+ * memory is reserved up front by its own allocator, or a latency-critical loop
+ * that must not take the device-wide synchronisation an allocation can cause.
+ * This entry point runs exactly what swa_attend runs, with the split-KV
+ * scratch (per-split partial records and valid-split counts) taken from a
+ * fixed array of SWA_NOALLOC_SCRATCH_BYTES that the library owns; every GPU
+ * that loads the library holds that array until the process exits.
+ *
+ * args->workspace and args->workspace_bytes are ignored; every other field
+ * means what it means for swa_attend, and the caller still passes all inputs
+ * and outputs. Nothing is allocated: no cudaMalloc, cudaFree or allocating
+ * library call.
+ *   - Sizes whose scratch need (swa_attend_workspace_size) exceeds
+ *     SWA_NOALLOC_SCRATCH_BYTES are refused with SWA_E_WORKSPACE before
+ *     anything is enqueued; use swa_attend with your own workspace for them.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array, which keeps the last call's contents.
+ *     Nothing in it needs to start at zero (every record is written before it
+ *     is read within a call), but calls that overlap on the GPU (different
+ *     streams, or different host threads, without ordering between them)
+ *     race on it and corrupt each other's results: order them.
+ * Errors: those of swa_attend, SWA_E_WORKSPACE for oversized calls, SWA_E_CUDA
+ * if the address lookup fails.
+ */
+#define SWA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,63 @@
+// swa_attend_noalloc: the attention of swa_attend, with its split-KV scratch in
+// a fixed array that the library owns, so that the caller never allocates.
+//
+// Some callers cannot call cudaMalloc: a plugin that a host program hands only
+// its input and output buffers, a serving engine whose device memory is all
+// reserved up front by its own allocator, or a latency-critical loop that must
+// not take the device-wide synchronisation an allocation can cause. For them
+// the scratch (the per-split partial records and the valid-split counts) lives
+// in the file-scope array below, which every GPU that loads this library holds
+// until the process exits.
+#include "swa_internal.cuh"
+
+#include <mutex>
+
+namespace swa {
+namespace {
+
+constexpr size_t kScratchBytes = SWA_NOALLOC_SCRATCH_BYTES;
+
+// The scratch itself. In host code this name is only a stand-in for the
+// device symbol; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_scratch on the current device, looked up once per device
+// (with that device current) and cached.
+int scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kMaxDevices) return SWA_E_SHAPE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_scratch);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (!p) return SWA_E_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return SWA_OK;
+}
+
+}  // namespace
+}  // namespace swa
+
+extern "C" int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream) {
+  if (!args) return SWA_E_NULL;
+  // Sizes whose partial records would not fit the fixed scratch are refused
+  // before anything is enqueued.
+  const size_t need = swa_attend_workspace_size(args);
+  if (need > swa::kScratchBytes) return SWA_E_WORKSPACE;
+  void* scratch = nullptr;
+  const int rc = swa::scratch_address(&scratch);
+  if (rc != SWA_OK) return rc;
+  swa_attend_args a = *args;
+  a.workspace = scratch;
+  a.workspace_bytes = swa::kScratchBytes;
+  return swa_attend(&a, stream);
+}
