@@ -69,22 +69,16 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   if (a->num_splits > 0) {
     best_s = a->num_splits < max_splits ? a->num_splits : max_splits;
   } else {
+    // About 8 waves of resident CTAs (a short tail and enough key streams in
+    // flight to cover HBM latency), but at least 4 tiles of keys per split.
     const int sms = num_sms();
     const int occ = attend_partial_occupancy(a->hd, nq);
     const long long slots = (long long)(sms > 0 ? sms : 148) * (occ > 0 ? occ : 1);
-    double best = 1e300;
-    for (int s = 1; s <= max_splits; ++s) {
-      const long long chunk = ((keys_max + s - 1) / s + TK - 1) / TK * TK;
-      const long long s_eff = (keys_max + chunk - 1) / chunk;
-      if (s_eff != s) continue;
-      const long long ctas = units * s_eff;
-      const long long waves = (ctas + slots - 1) / slots;
-      const double cost = (double)waves * (double)(chunk + 2 * TK);
-      if (cost < best * 0.999) {
-        best = cost;
-        best_s = s;
-      }
-    }
+    long long want = (8 * slots + units - 1) / units;
+    const long long cap_s = (keys_max + 4 * TK - 1) / (4 * TK);
+    if (want > cap_s) want = cap_s;
+    if (want < 1) want = 1;
+    best_s = (int)want;
   }
   long long chunk = ((keys_max + best_s - 1) / best_s + TK - 1) / TK * TK;
   p->chunk = (int)chunk;

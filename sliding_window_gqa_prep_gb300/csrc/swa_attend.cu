@@ -67,23 +67,6 @@ struct Cfg {
   static_assert(KS * NQ * HD <= 2 * STAGES * TK * HDP, "split reduction fits the stage buffers");
 };
 
-struct SeqState {
-  int W, len0, head0;
-};
-
-__device__ __forceinline__ SeqState load_state(const AttendParams& p, int b, bool report) {
-  const swa_meta m = p.meta[b];
-  int W = m.window ? (int)m.window : p.cap;
-  bool bad = false;
-  if (W > p.cap) { W = p.cap; bad = true; }
-  int len0 = (int)m.win_len;
-  if (len0 > W) { len0 = W; bad = true; }
-  int head0 = (int)m.win_head;
-  if (head0 >= W) { head0 %= W; bad = true; }
-  if (bad && report) set_err(p.err, SWA_DERR_META);
-  return {W, len0, head0};
-}
-
 template <int HD, int NQ>
 __global__ void __launch_bounds__(kNT) attend_partial_kernel(AttendParams p) {
   using C = Cfg<HD, NQ>;
@@ -502,6 +485,7 @@ int occupancy_hd(int nq) {
 }  // namespace
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  if (p.nq <= 8) return launch_attend_decode(p, s, e0, e1);
   switch (p.hd) {
     case 64: return launch_partial_hd<64>(p, s, e0, e1);
     case 128: return launch_partial_hd<128>(p, s, e0, e1);
@@ -511,6 +495,7 @@ int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0,
 }
 
 int attend_partial_occupancy(int hd, int nq) {
+  if (nq <= 8) return attend_decode_occupancy(hd, nq);
   switch (hd) {
     case 64: return occupancy_hd<64>(nq);
     case 128: return occupancy_hd<128>(nq);

@@ -61,6 +61,9 @@ struct AttendParams {
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int launch_attend_merge(const AttendParams& p, cudaStream_t s);
 int attend_partial_occupancy(int hd, int nq);   // resident CTAs per SM
+// decode kernel (nq <= 8 query vectors per CTA), swa_decode.cu
+int launch_attend_decode(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+int attend_decode_occupancy(int hd, int nq);
 
 struct PrepParams {
   int B, t, nh, nk, hd, cap;
@@ -149,6 +152,36 @@ __device__ __forceinline__ void bulk_g2s(void* dst_smem, const void* src_gmem, u
 
 __device__ __forceinline__ void set_err(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
+}
+
+// Plain arrival (no transaction bytes) on a barrier.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier among `nthreads` threads (whole warps) of the CTA on hardware barrier `id`.
+__device__ __forceinline__ void named_barrier(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" :: "r"(id), "r"(nthreads) : "memory");
+}
+
+// A sequence's ring state with the window, length and head clamped into range
+// (window <= cap, win_len <= window, win_head < window); out-of-range meta is
+// reported through the error word when `report` is set.
+struct SeqState {
+  int W, len0, head0;
+};
+
+__device__ __forceinline__ SeqState load_state(const AttendParams& p, int b, bool report) {
+  const swa_meta m = p.meta[b];
+  int W = m.window ? (int)m.window : p.cap;
+  bool bad = false;
+  if (W > p.cap) { W = p.cap; bad = true; }
+  int len0 = (int)m.win_len;
+  if (len0 > W) { len0 = W; bad = true; }
+  int head0 = (int)m.win_head;
+  if (head0 >= W) { head0 %= W; bad = true; }
+  if (bad && report) set_err(p.err, SWA_DERR_META);
+  return {W, len0, head0};
 }
 
 #endif  // __CUDACC__
