@@ -45,7 +45,7 @@ import workloads  # noqa: E402
 
 DEFAULT_WORKLOAD = "batched_decode"
 PROFILE_DIR = os.path.join(ROOT, "profiles")
-ATTEND_SRC = os.path.join(ROOT, "sliding_window_gqa_prep_gb300", "csrc", "swa_attend.cu")
+CSRC = os.path.join(ROOT, "sliding_window_gqa_prep_gb300", "csrc")
 
 
 def parse_args():
@@ -80,21 +80,35 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def attend_source_hash():
-    with open(ATTEND_SRC, "rb") as f:
+def dominant_kernel(w):
+    """The attention kernel a workload runs and its source file: row blocks of
+    at most 8 query vectors (rows x query heads per KV head) take the decode
+    kernel, larger ones the block kernel."""
+    rows = max(1, min(w.t, 32 // w.hpg))
+    nq = 4
+    while nq < rows * w.hpg:
+        nq *= 2
+    if nq <= 8:
+        return "attend_decode_kernel", os.path.join(CSRC, "swa_decode.cu")
+    return "attend_partial_kernel", os.path.join(CSRC, "swa_attend.cu")
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(workload):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(PROFILE_DIR, f"attend_partial_{workload}.md")
+def recorded_traffic(w):
+    """DRAM bytes per launch of the workload's attention kernel from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    kernel, src = dominant_kernel(w)
+    path = os.path.join(PROFILE_DIR, f"{kernel}_{w.name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch\s*[:=]\s*([0-9.eE+]+)", text)
     h = re.search(r"kernel_source_sha256_16\s*[:=]\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != attend_source_hash():
+    if not m or not h or h.group(1) != source_hash(src):
         return None
     return float(m.group(1))
 
@@ -351,7 +365,8 @@ def run_gpu(args, w, rank, world, local_rank):
     step_s = ms / 1e3 / K
     kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
     achieved = kv_bytes / kern_avg_s / 1e9
-    traffic = recorded_traffic(w.name)
+    traffic = recorded_traffic(w)
+    kernel_name = dominant_kernel(w)[0]
     line = {
         "metric": "attended KV-keys/s",
         "value": keys * world / step_s,
@@ -363,7 +378,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "config": workload_config(w, world),
         "kv_read_gbs_step": kv_bytes * world / step_s / 1e9,
         "kv_read_frac_of_peak_step": kv_bytes / step_s / 1e9 / peak,
-        "roofline": {"bound": "hbm", "kernel": "attend_partial_kernel",
+        "roofline": {"bound": "hbm", "kernel": kernel_name,
                      "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,

@@ -51,6 +51,28 @@ static int attend_shape_ok(const swa_attend_args* a) {
 bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   if (!attend_shape_ok(a)) return false;
   const int hpg = a->nh / a->nk;
+  // Prompt-sized chunks (at least 64 query vectors per KV head, hd <= 128) run
+  // the tensor-core kernel on blocks of 64 query vectors, one split each.
+  if (a->hd <= 128 && (long long)a->t * hpg >= 64) {
+    const int rows = 64 / hpg;
+    p->nq = 64;
+    p->rows = rows;
+    p->n_rb = (a->t + rows - 1) / rows;
+    const long long keys_max = (long long)a->ns + a->cap + rows - 1;
+    if (keys_max > (1LL << 30)) return false;
+    p->keys_max = (int)keys_max;
+    p->chunk = (int)((keys_max + TK - 1) / TK * TK);
+    p->splits = 1;
+    p->items = (size_t)a->B * a->nk * p->n_rb;
+    const size_t acc_bytes = p->items * p->nq * (size_t)a->hd * sizeof(float);
+    const size_t ml_bytes = p->items * p->nq * sizeof(float2);
+    const size_t ns_bytes = (size_t)a->B * p->n_rb * sizeof(int);
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    p->off_ml = up(acc_bytes);
+    p->off_nsplit = p->off_ml + up(ml_bytes);
+    p->ws_bytes = p->off_nsplit + up(ns_bytes);
+    return true;
+  }
   int rows = 32 / hpg;
   if (rows < 1) rows = 1;
   if (rows > a->t) rows = a->t;

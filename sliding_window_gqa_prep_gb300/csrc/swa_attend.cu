@@ -486,6 +486,7 @@ int occupancy_hd(int nq) {
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   if (p.nq <= 8) return launch_attend_decode(p, s, e0, e1);
+  if (p.nq == 64) return launch_attend_prompt(p, s, e0, e1);
   switch (p.hd) {
     case 64: return launch_partial_hd<64>(p, s, e0, e1);
     case 128: return launch_partial_hd<128>(p, s, e0, e1);

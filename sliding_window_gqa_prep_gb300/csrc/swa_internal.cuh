@@ -64,6 +64,8 @@ int attend_partial_occupancy(int hd, int nq);   // resident CTAs per SM
 // decode kernel (nq <= 8 query vectors per CTA), swa_decode.cu
 int launch_attend_decode(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int attend_decode_occupancy(int hd, int nq);
+// prompt-chunk kernel (64 query vectors per CTA, tensor cores), swa_prompt.cu
+int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 
 struct PrepParams {
   int B, t, nh, nk, hd, cap;

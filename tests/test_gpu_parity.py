@@ -93,6 +93,12 @@ ATTEND_CASES = [
     dict(B=1, t=1, nh=32, nk=1, hd=128, window=90, cap=90, ns=2, pos_mode="full", pos_lo=90, pos_hi=400),
     # hd 256, verify-sized block
     dict(B=2, t=8, nh=8, nk=2, hd=256, window=64, cap=64, ns=4, pos_mode="full", pos_lo=64, pos_hi=700),
+    # tensor-core prompt path: hpg 8 (8 rows per block, ragged last block), partial rings
+    dict(B=3, t=37, nh=16, nk=2, hd=128, window=100, cap=100, ns=3, pos_mode="partial", pos_lo=1, pos_hi=100),
+    # tensor-core prompt path: hpg 6 (10 rows = 60 of 64 query slots), wrapped rings, window < t
+    dict(B=2, t=33, nh=12, nk=2, hd=64, window=20, cap=20, ns=1, pos_mode="full", pos_lo=20, pos_hi=900),
+    # tensor-core prompt path: empty ring, hpg 4, several key tiles
+    dict(B=2, t=70, nh=8, nk=2, hd=128, window=64, cap=64, ns=0, pos_mode="prompt", pos_lo=0, pos_hi=200),
 ]
 
 
