@@ -71,26 +71,45 @@ def keys_and_bytes(w, meta):
     return workloads.kv_keys_and_bytes(w, meta)
 
 
-def measured_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
-        with open(path) as f:
-            d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
-
-
-def dominant_kernel(w):
-    """The attention kernel a workload runs and its source file: row blocks of
-    at most 8 query vectors (rows x query heads per KV head) take the decode
-    kernel, larger ones the block kernel."""
+def attention_path(w):
+    """Which attention kernel a workload's row blocks take (the library's
+    planner rule): >= 64 query vectors per KV head with hd <= 128 -> tensor-core
+    prompt kernel; <= 8 query vectors per row block -> decode kernel; else the
+    verify kernel."""
+    if w.hd <= 128 and w.t * w.hpg >= 64:
+        return "prompt"
     rows = max(1, min(w.t, 32 // w.hpg))
     nq = 4
     while nq < rows * w.hpg:
         nq *= 2
-    if nq <= 8:
-        return "attend_decode_kernel", os.path.join(CSRC, "swa_decode.cu")
-    return "attend_partial_kernel", os.path.join(CSRC, "swa_attend.cu")
+    return "decode" if nq <= 8 else "verify"
+
+
+def dominant_kernel(w):
+    """The attention kernel a workload runs and its source file."""
+    path = attention_path(w)
+    name = {"decode": "attend_decode_kernel", "verify": "attend_verify_kernel",
+            "prompt": "attend_prompt_kernel"}[path]
+    src = {"decode": "swa_decode.cu", "verify": "swa_verify.cu", "prompt": "swa_prompt.cu"}[path]
+    return name, os.path.join(CSRC, src)
+
+
+def peaks():
+    """Roofline denominators: measured HBM copy GB/s and bf16 TFLOP/s (or the
+    fallback), the FP32 CUDA-core peak derived from unit counts and the max SM
+    clock (152 SMs x 128 FMA/clk x 2 flop), and the TF32 tensor peak as the
+    measured bf16 peak x the nominal TF32/bf16 ratio (1.1 / 2.25)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        hbm, bf16, kind = float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+        mhz = float(d.get("sm_max_mhz", 2070.0))
+    else:
+        hbm, bf16, kind, mhz = 6800.0, 1900.0, "fallback", 2070.0
+    fp32 = 152 * 128 * 2 * mhz * 1e6 / 1e12
+    return {"hbm_gbs": hbm, "bf16_tflops": bf16, "tf32_tflops": bf16 * 1.1 / 2.25,
+            "fp32_tflops": fp32, "kind": kind}
 
 
 def source_hash(path):
@@ -292,6 +311,7 @@ def make_events(n):
 
 def run_gpu(args, w, rank, world, local_rank):
     import sliding_window_gqa_prep_gb300 as swa
+    from sliding_window_gqa_prep_gb300.dist import max_over_ranks
 
     dev = torch.device("cuda", local_rank)
     inp = workloads.make_inputs(w, seed=w.seed + 1000 * rank)
@@ -333,10 +353,7 @@ def run_gpu(args, w, rank, world, local_rank):
     ms = e0.elapsed_time(e1)
     kern_ms = [kev[2 * s].elapsed_time(kev[2 * s + 1]) for s in range(K)]
     err = int(tp.err.item())
-    t_max = torch.tensor([ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
-    ms = float(t_max.item())
+    ms = max_over_ranks(ms, dev)
 
     # end to end: pinned host inputs in, gated output back, every step
     e2e = None
@@ -351,22 +368,38 @@ def run_gpu(args, w, rank, world, local_rank):
         for _ in range(K2):
             tp.step(h_in["yq"], h_in["yk"], h_in["yv"], h_in["gate"], out_host=h_out)
         barrier()
-        e2e_s = torch.tensor([time.perf_counter() - t0], dtype=torch.float64, device=dev)
-        if world > 1:
-            torch.distributed.all_reduce(e2e_s, op=torch.distributed.ReduceOp.MAX)
-        e2e = {"value": keys * K2 * world / float(e2e_s.item()), "unit": "keys/s",
+        e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": keys * K2 * world / e2e_s, "unit": "keys/s",
                "h2d_bytes_per_step": sum(v.numel() * 4 for v in h_in.values()),
                "d2h_bytes_per_step": h_out.numel() * 4,
-               "ms_per_step": float(e2e_s.item()) * 1e3 / K2}
+               "ms_per_step": e2e_s * 1e3 / K2}
 
     if rank != 0:
         return
-    peak, peak_kind = measured_peaks()
+    pk = peaks()
+    peak = pk["hbm_gbs"]
     step_s = ms / 1e3 / K
     kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
-    achieved = kv_bytes / kern_avg_s / 1e9
     traffic = recorded_traffic(w)
     kernel_name = dominant_kernel(w)[0]
+    path = attention_path(w)
+    useful_flop = keys * w.hpg * w.hd * 4          # Q K^T and P V, 2 flop per multiply-add
+    if path == "decode":
+        roof = {"bound": "hbm", "achieved": kv_bytes / kern_avg_s / 1e9, "peak": peak,
+                "unit": "GB/s", "peak_kind": pk["kind"]}
+    elif path == "verify":
+        roof = {"bound": "alu", "achieved": useful_flop / kern_avg_s / 1e12,
+                "peak": pk["fp32_tflops"], "unit": "TFLOP/s",
+                "peak_kind": "derived: 152 SMs x 128 FP32 FMA/clk x 2 x max SM clock",
+                "kv_gbs": kv_bytes / kern_avg_s / 1e9, "kv_frac_of_hbm": kv_bytes / kern_avg_s / 1e9 / peak}
+    else:
+        roof = {"bound": "tensor", "achieved": 3 * useful_flop / kern_avg_s / 1e12,
+                "peak": pk["tf32_tflops"], "unit": "TFLOP/s",
+                "peak_kind": f"{pk['kind']} bf16 x 1.1/2.25 (nominal TF32/bf16); achieved counts the 3 TF32 products of each multiply-add",
+                "useful_tflops": useful_flop / kern_avg_s / 1e12}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": kernel_name,
+                 "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
+                 "launch_ms_avg": kern_avg_s * 1e3})
     line = {
         "metric": "attended KV-keys/s",
         "value": keys * world / step_s,
@@ -378,11 +411,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "config": workload_config(w, world),
         "kv_read_gbs_step": kv_bytes * world / step_s / 1e9,
         "kv_read_frac_of_peak_step": kv_bytes / step_s / 1e9 / peak,
-        "roofline": {"bound": "hbm", "kernel": kernel_name,
-                     "achieved": achieved, "peak": peak, "peak_kind": peak_kind,
-                     "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
-                     "launch_ms_avg": kern_avg_s * 1e3},
+        "roofline": roof,
         "gpu_launches": launches,
         "launches_per_step": launches / K,
         "device_errors": err,

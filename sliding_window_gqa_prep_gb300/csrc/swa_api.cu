@@ -70,7 +70,8 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     p->off_ml = up(acc_bytes);
     p->off_nsplit = p->off_ml + up(ml_bytes);
-    p->ws_bytes = p->off_nsplit + up(ns_bytes);
+    p->off_meta = p->off_nsplit + up(ns_bytes);
+    p->ws_bytes = p->off_meta + up((size_t)a->B * sizeof(swa_meta));
     return true;
   }
   int rows = 32 / hpg;
@@ -112,7 +113,8 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
   p->off_ml = up(acc_bytes);
   p->off_nsplit = p->off_ml + up(ml_bytes);
-  p->ws_bytes = p->off_nsplit + up(ns_bytes);
+  p->off_meta = p->off_nsplit + up(ns_bytes);
+  p->ws_bytes = p->off_meta + up((size_t)a->B * sizeof(swa_meta));
   return true;
 }
 
@@ -216,6 +218,14 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   p.ws_acc = reinterpret_cast<float*>(ws);
   p.ws_ml = reinterpret_cast<float2*>(ws + plan.off_ml);
   p.ws_nsplit = reinterpret_cast<int*>(ws + plan.off_nsplit);
+  p.ws_meta = reinterpret_cast<swa_meta*>(ws + plan.off_meta);
+  {
+    // commit CTAs per sequence: about 4 float4 pairs per thread of 256
+    const long long rows = a->t < a->cap ? a->t : a->cap;
+    const long long work = rows * a->nk * (a->hd / 4);
+    long long cb = (work + 1023) / 1024;
+    p.commit_blocks = (int)(cb < 1 ? 1 : (cb > 4096 ? 4096 : cb));
+  }
   p.commit = a->commit ? 1 : 0;
   p.meta_out = a->meta_out;
   p.err = a->err;

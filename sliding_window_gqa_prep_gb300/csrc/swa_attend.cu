@@ -97,6 +97,7 @@ __global__ void __launch_bounds__(kNT) attend_partial_kernel(AttendParams p) {
   const int xlo = st.len0 + r0 + 1 - win0;       // first logical key of the block
   const int n = p.ns + (st.len0 + r_last - xlo + 1);
   if (g == 0 && s == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = (n + p.chunk - 1) / p.chunk;
+  if (g == 0 && s == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
   const int jb = s * p.chunk;
   if (jb >= n) return;
   const int je = min(n, jb + p.chunk);
@@ -357,24 +358,29 @@ __global__ void __launch_bounds__(kNT) attend_partial_kernel(AttendParams p) {
 template <int HD>
 __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int out_blocks) {
   if ((int)blockIdx.x >= out_blocks) {
-    // ---- commit of sequence b: ring rows, then the meta (o1c_ring_commit, o1c_meta)
-    const int b = blockIdx.x - out_blocks;
-    const SeqState st = load_state(p, b, false);
+    // ---- commit of sequence b, spread over commit_blocks CTAs: the last
+    // min(t, W) chunk rows into their ring slots (o1c_ring_commit), then the
+    // meta (o1c_meta). The ring map comes from the copy of the meta the
+    // attention kernel saved, so meta_out may alias meta.
+    const int cb = (blockIdx.x - out_blocks) % p.commit_blocks;
+    const int b = (blockIdx.x - out_blocks) / p.commit_blocks;
+    const swa_meta m0 = p.ws_meta[b];
+    const SeqState st = sanitize_state(m0, p.cap, nullptr);
     const int first = max(0, p.t - st.W);      // only the last W rows survive
     const int nrow = p.t - first;
     const int per_row = p.nk * (HD / 4);
-    for (int idx = threadIdx.x; idx < nrow * per_row; idx += blockDim.x) {
+    const int stride = p.commit_blocks * blockDim.x;
+    for (int idx = cb * blockDim.x + threadIdx.x; idx < nrow * per_row; idx += stride) {
       const int j = first + idx / per_row;
       const int g = (idx % per_row) / (HD / 4);
       const int d4 = idx % (HD / 4);
-      const int slot = (int)(((long long)st.head0 + st.len0 + j) % st.W);
+      int slot = (int)(((long long)st.head0 + st.len0 + j) % st.W);
       const size_t src = (((size_t)b * p.t + j) * p.nk + g) * HD + d4 * 4;
       const size_t dst = (((size_t)b * p.nk + g) * p.cap + slot) * HD + d4 * 4;
       *reinterpret_cast<float4*>(p.ring_k + dst) = *reinterpret_cast<const float4*>(p.k_chunk + src);
       *reinterpret_cast<float4*>(p.ring_v + dst) = *reinterpret_cast<const float4*>(p.v_chunk + src);
     }
-    if (threadIdx.x == 0) {
-      const swa_meta m0 = p.meta[b];
+    if (cb == 0 && threadIdx.x == 0) {
       swa_meta m1 = m0;
       const long long tot = (long long)st.len0 + p.t;
       if (tot <= st.W) {
@@ -487,6 +493,7 @@ int occupancy_hd(int nq) {
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   if (p.nq <= 8) return launch_attend_decode(p, s, e0, e1);
   if (p.nq == 64) return launch_attend_prompt(p, s, e0, e1);
+  if (p.nq == 16 || p.nq == 32) return launch_attend_verify(p, s, e0, e1);
   switch (p.hd) {
     case 64: return launch_partial_hd<64>(p, s, e0, e1);
     case 128: return launch_partial_hd<128>(p, s, e0, e1);
@@ -497,6 +504,7 @@ int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0,
 
 int attend_partial_occupancy(int hd, int nq) {
   if (nq <= 8) return attend_decode_occupancy(hd, nq);
+  if (nq == 16 || nq == 32) return attend_verify_occupancy(hd, nq);
   switch (hd) {
     case 64: return occupancy_hd<64>(nq);
     case 128: return occupancy_hd<128>(nq);
@@ -509,7 +517,7 @@ int launch_attend_merge(const AttendParams& p, cudaStream_t s) {
   const size_t total = (size_t)p.B * p.t * p.nh * (p.hd / 4);
   const int block = 256;
   const int out_blocks = (int)((total + block - 1) / block);
-  const int grid = out_blocks + (p.commit ? p.B : 0);
+  const int grid = out_blocks + (p.commit ? p.B * p.commit_blocks : 0);
   switch (p.hd) {
     case 64: attend_merge_kernel<64><<<grid, block, 0, s>>>(p, out_blocks); break;
     case 128: attend_merge_kernel<128><<<grid, block, 0, s>>>(p, out_blocks); break;

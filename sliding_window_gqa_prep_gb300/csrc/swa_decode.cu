@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kDecThreads) attend_decode_kernel(AttendParams
   const int xlo = st.len0 + r0 + 1 - win0;       // first logical key of the block
   const int n = p.ns + (st.len0 + r_last - xlo + 1);
   if (g == 0 && s == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = (n + p.chunk - 1) / p.chunk;
+  if (g == 0 && s == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
   const int jb = s * p.chunk;
   if (jb >= n) return;
   const int je = min(n, jb + p.chunk);

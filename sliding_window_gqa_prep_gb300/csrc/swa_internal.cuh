@@ -31,6 +31,7 @@ struct AttendPlan {
   size_t ws_bytes; // workspace bytes
   size_t off_ml;   // byte offset of the (m, l) records
   size_t off_nsplit; // byte offset of the per-(b, rb) valid-split counts
+  size_t off_meta;   // byte offset of the per-sequence copy of the meta before the chunk
 };
 bool make_plan(const swa_attend_args* a, AttendPlan* p);
 
@@ -52,7 +53,9 @@ struct AttendParams {
   float* ws_acc;              // [items][nq][hd]
   float2* ws_ml;              // [items][nq] (m in log2 units, l)
   int* ws_nsplit;             // [B][n_rb]
+  swa_meta* ws_meta;          // [B]: meta before the chunk, saved by the attention kernel
   int commit;
+  int commit_blocks;          // CTAs per sequence of the commit
   swa_meta* meta_out;
   uint32_t* err;
   int nq, rows, n_rb, chunk, splits;
@@ -66,6 +69,9 @@ int launch_attend_decode(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, 
 int attend_decode_occupancy(int hd, int nq);
 // prompt-chunk kernel (64 query vectors per CTA, tensor cores), swa_prompt.cu
 int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+// verify kernel (16 or 32 query vectors per CTA, CUDA cores), swa_verify.cu
+int launch_attend_verify(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+int attend_verify_occupancy(int hd, int nq);
 
 struct PrepParams {
   int B, t, nh, nk, hd, cap;
@@ -173,17 +179,23 @@ struct SeqState {
   int W, len0, head0;
 };
 
-__device__ __forceinline__ SeqState load_state(const AttendParams& p, int b, bool report) {
-  const swa_meta m = p.meta[b];
-  int W = m.window ? (int)m.window : p.cap;
+__device__ __forceinline__ SeqState sanitize_state(const swa_meta m, int cap, bool* bad_out) {
+  int W = m.window ? (int)m.window : cap;
   bool bad = false;
-  if (W > p.cap) { W = p.cap; bad = true; }
+  if (W > cap) { W = cap; bad = true; }
   int len0 = (int)m.win_len;
   if (len0 > W) { len0 = W; bad = true; }
   int head0 = (int)m.win_head;
   if (head0 >= W) { head0 %= W; bad = true; }
-  if (bad && report) set_err(p.err, SWA_DERR_META);
+  if (bad_out) *bad_out = bad;
   return {W, len0, head0};
+}
+
+__device__ __forceinline__ SeqState load_state(const AttendParams& p, int b, bool report) {
+  bool bad = false;
+  const SeqState st = sanitize_state(p.meta[b], p.cap, &bad);
+  if (bad && report) set_err(p.err, SWA_DERR_META);
+  return st;
 }
 
 #endif  // __CUDACC__

@@ -100,6 +100,7 @@ __global__ void __launch_bounds__(kPThreads, 2) attend_prompt_kernel(AttendParam
   const int xlo = st.len0 + r0 + 1 - win0;
   const int n = p.ns + (st.len0 + r_last - xlo + 1);
   if (g == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = 1;
+  if (g == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
   const int ntiles = (n + kPTK - 1) / kPTK;
   const size_t kv_head = (size_t)b * p.nk + g;
 
