@@ -162,6 +162,20 @@ __device__ __forceinline__ void set_err(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }
 
+// 16-byte asynchronous copy global -> shared (L2 only), tracked by cp.async groups
+// or, after cp_async_arrive_noinc, by an mbarrier.
+__device__ __forceinline__ void cp_async16_cg(void* dst_smem, const void* src_gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+               :: "r"(smem_u32(dst_smem)), "l"(src_gmem) : "memory");
+}
+
+// The barrier receives one arrival from this thread once all of the thread's
+// earlier cp.async copies have landed (the arrival is counted in the barrier's
+// expected count: no pending-count increment).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" :: "r"(smem_u32(bar)) : "memory");
+}
+
 // Plain arrival (no transaction bytes) on a barrier.
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(smem_u32(bar)) : "memory");

@@ -209,9 +209,11 @@ __global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p
     const int cnt = min(TK, je - j0);
 
     // ---- scores of key `lane` against the warp's query vectors
-    u64 sacc[C::QW];
+    // two independent accumulator chains per query vector (features 4i..4i+1
+    // and 4i+2..4i+3) keep consecutive packed FMAs from waiting on each other
+    u64 sacc[C::QW], sacc2[C::QW];
 #pragma unroll
-    for (int k = 0; k < C::QW; ++k) sacc[k] = 0ull;
+    for (int k = 0; k < C::QW; ++k) sacc[k] = sacc2[k] = 0ull;
     const float* krow = Ks + ((size_t)stage * TK + lane) * C::KP;
     const float* qrow = Qs + (size_t)q0 * HD;
 #pragma unroll 8
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p
       for (int k = 0; k < C::QW; ++k) {
         const ulonglong2 qv = *reinterpret_cast<const ulonglong2*>(qrow + k * HD + d4 * 4);
         sacc[k] = ffma2(qv.x, kv.x, sacc[k]);
-        sacc[k] = ffma2(qv.y, kv.y, sacc[k]);
+        sacc2[k] = ffma2(qv.y, kv.y, sacc2[k]);
       }
     }
     const int j = j0 + lane;
@@ -231,9 +233,10 @@ __global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p
 #pragma unroll
     for (int k = 0; k < C::QW; ++k) {
       const float2 sp = unpack2(sacc[k]);
+      const float2 sp2 = unpack2(sacc2[k]);
       bool v = key_in && q_ok[k];
       if (v && j >= p.ns) v = x >= q_lo[k] && x <= q_hi[k];
-      const float sv = v ? sp.x + sp.y : -INFINITY;
+      const float sv = v ? (sp.x + sp.y) + (sp2.x + sp2.y) : -INFINITY;
       float tmax = sv;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kVFull, tmax, o));
@@ -255,6 +258,7 @@ __global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p
     for (int k = 0; k < C::QW; ++k)
 #pragma unroll
       for (int d = 0; d < C::DPL / 2; ++d) acc[k][d] = ffma2(acc[k][d], cc[k], zero2);
+#pragma unroll 4
     for (int kk = 0; kk < cnt; ++kk) {
       u64 pk[C::QW];
 #pragma unroll
