@@ -73,9 +73,11 @@ def keys_and_bytes(w, meta):
 
 def attention_path(w):
     """Which attention kernel a workload's row blocks take (the library's
-    planner rule): >= 64 query vectors per KV head with hd <= 128 -> tensor-core
-    prompt kernel; <= 8 query vectors per row block -> decode kernel; else the
-    verify kernel."""
+    planner rule, hd <= 128 for the tensor-core paths): >= 128 query vectors per
+    KV head -> tcgen05 prompt kernel; >= 64 -> mma.sync prompt kernel; <= 8
+    query vectors per row block -> decode kernel; else the verify kernel."""
+    if w.hd <= 128 and w.t * w.hpg >= 128:
+        return "prompt_tc"
     if w.hd <= 128 and w.t * w.hpg >= 64:
         return "prompt"
     rows = max(1, min(w.t, 32 // w.hpg))
@@ -89,8 +91,9 @@ def dominant_kernel(w):
     """The attention kernel a workload runs and its source file."""
     path = attention_path(w)
     name = {"decode": "attend_decode_kernel", "verify": "attend_verify_kernel",
-            "prompt": "attend_prompt_kernel"}[path]
-    src = {"decode": "swa_decode.cu", "verify": "swa_verify.cu", "prompt": "swa_prompt.cu"}[path]
+            "prompt": "attend_prompt_kernel", "prompt_tc": "attend_prompt_tc_kernel"}[path]
+    src = {"decode": "swa_decode.cu", "verify": "swa_verify.cu", "prompt": "swa_prompt.cu",
+           "prompt_tc": "swa_prompt_tc.cu"}[path]
     return name, os.path.join(CSRC, src)
 
 

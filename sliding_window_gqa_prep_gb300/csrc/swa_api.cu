@@ -51,11 +51,13 @@ static int attend_shape_ok(const swa_attend_args* a) {
 bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   if (!attend_shape_ok(a)) return false;
   const int hpg = a->nh / a->nk;
-  // Prompt-sized chunks (at least 64 query vectors per KV head, hd <= 128) run
-  // the tensor-core kernel on blocks of 64 query vectors, one split each.
+  // Prompt-sized chunks run on tensor cores, one split per row block: blocks of
+  // 128 query vectors on tcgen05 when a chunk has at least 128 query vectors
+  // per KV head, else blocks of 64 on mma.sync (hd <= 128 in both).
   if (a->hd <= 128 && (long long)a->t * hpg >= 64) {
-    const int rows = 64 / hpg;
-    p->nq = 64;
+    const int block = (long long)a->t * hpg >= 128 ? 128 : 64;
+    const int rows = block / hpg;
+    p->nq = block;
     p->rows = rows;
     p->n_rb = (a->t + rows - 1) / rows;
     const long long keys_max = (long long)a->ns + a->cap + rows - 1;

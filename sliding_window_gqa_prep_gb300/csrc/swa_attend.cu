@@ -7,7 +7,8 @@
 // number of query vectors (rows x query heads of a KV head) a CTA serves:
 //   <= 8       attend_decode_kernel (swa_decode.cu), HBM-bound;
 //   16 or 32   attend_verify_kernel (swa_verify.cu), FP32-bound;
-//   64         attend_prompt_kernel (swa_prompt.cu), tensor cores (3xTF32).
+//   64         attend_prompt_kernel (swa_prompt.cu), mma.sync TF32 (3xTF32);
+//   128        attend_prompt_tc_kernel (swa_prompt_tc.cu), tcgen05 + TMEM (3xTF32).
 // Each writes, per (sequence, KV head, row block, split) and query vector, a
 // record (m in log2 units, l, unnormalised numerator). attend_merge_kernel
 // then takes, per output (b, row, head, 4 features), the max over the valid
@@ -107,6 +108,7 @@ int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0,
   if (p.nq <= 8) return launch_attend_decode(p, s, e0, e1);
   if (p.nq == 16 || p.nq == 32) return launch_attend_verify(p, s, e0, e1);
   if (p.nq == 64) return launch_attend_prompt(p, s, e0, e1);
+  if (p.nq == 128) return launch_attend_prompt_tc(p, s, e0, e1);
   return SWA_E_SHAPE;
 }
 

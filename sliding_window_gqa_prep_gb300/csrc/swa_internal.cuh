@@ -69,6 +69,8 @@ int launch_attend_decode(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, 
 int attend_decode_occupancy(int hd, int nq);
 // prompt-chunk kernel (64 query vectors per CTA, tensor cores), swa_prompt.cu
 int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+// prompt-chunk kernel on tcgen05 / TMEM (128 query vectors per CTA), swa_prompt_tc.cu
+int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // verify kernel (16 or 32 query vectors per CTA, CUDA cores), swa_verify.cu
 int launch_attend_verify(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int attend_verify_occupancy(int hd, int nq);

@@ -1,0 +1,484 @@
+// Prompt-chunk attention on the 5th-generation tensor cores (tcgen05, TMEM):
+// the GEMM path of "o1c_msl.metal" (cortiq-engine 0.8.79: o1c_gather, o1c_cols,
+// o1c_gmax, o1c_gsoft, o1c_gadd and the engine GEMMs Q K^T and P V they feed)
+// as one flash-style kernel per block of 128 query vectors.
+//
+// Precision: every operand is split a = a_hi + a_lo with a_hi = a rounded to
+// TF32 and a_lo = (a - a_hi) rounded to TF32; each product is
+// a_hi b_hi + a_hi b_lo + a_lo b_hi accumulated in f32 (three tcgen05.mma
+// kind::tf32), which keeps f32 accuracy (the dropped a_lo b_lo is ~2^-22 of
+// the product).
+//
+// CTA = 6 warps:
+//   warps 0-3  one thread per query vector = per TMEM lane (the 128-row MMA
+//              accumulator rows): split of the K/V tiles into TF32 hi/lo
+//              shared-memory operands, softmax of the thread's own score row
+//              (read from TMEM), P into TMEM, rescale of O, final record;
+//   warp 4     producer: keys with contiguous sources (ring runs, sinks) as one
+//              cp.async.bulk per run into fp32 landing tiles of 32 keys;
+//   warp 5     one elected lane issues every tcgen05.mma and tcgen05.commit.
+// Tensor memory (512 columns): Q_hi, Q_lo (A operands of S = Q K^T), S,
+// O (the P V accumulator), P_hi, P_lo (A operands of P V).
+// Shared memory: two fp32 landing stages, K_hi/K_lo (32 keys x hd, K-major
+// canonical core-matrix layout: 8 rows x 16 bytes per core matrix) and
+// V^T_hi/V^T_lo (hd x 32 keys, K-major): TF32 operands must be K-major, so V
+// is transposed while it is split.
+// Every hand-off is an mbarrier; all waits are bounded (1 s) and report
+// SWA_DERR_TIMEOUT; tensor memory is released on every path.
+#include "swa_internal.cuh"
+
+namespace swa {
+namespace {
+
+constexpr int kTM = 128;               // query vectors per CTA (MMA M)
+constexpr int kTN = 32;                // keys per tile
+constexpr int kTThreads = 6 * 32;
+constexpr int kSoftThreads = 128;
+constexpr unsigned kTF = 0xffffffffu;
+
+template <int HD>
+struct TCfg {
+  // TMEM columns
+  static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S = 2 * HD, C_O = 2 * HD + kTN;
+  static constexpr uint32_t C_PHI = 3 * HD + kTN, C_PLO = 3 * HD + 2 * kTN;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(3 * HD + 3 * kTN <= 512, "tensor memory budget");
+  // shared memory (bytes)
+  static constexpr int LAND = kTN * HD * 4;                 // one fp32 tile of K or V
+  static constexpr int OFF_LK = 0;                          // [2 stages] K landing
+  static constexpr int OFF_LV = 2 * LAND;                   // [2 stages] V landing
+  static constexpr int OFF_KHI = 4 * LAND;
+  static constexpr int OFF_KLO = OFF_KHI + LAND;
+  static constexpr int OFF_VHI = OFF_KLO + LAND;
+  static constexpr int OFF_VLO = OFF_VHI + LAND;
+  static constexpr int OFF_BAR = OFF_VLO + LAND;            // mbarriers
+  static constexpr int NBAR = 9;
+  // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
+  static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
+  static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
+  // K-major core-matrix layouts: LBO = next core matrix along K, SBO = next 8 rows
+  static constexpr uint32_t K_LBO = 128, K_SBO = (HD / 4) * 128;   // K_hi: rows = keys, K = features
+  static constexpr uint32_t V_LBO = 128, V_SBO = (kTN / 4) * 128;  // V^T: rows = features, K = keys
+};
+
+// ---- tcgen05 / TMEM wrappers -------------------------------------------------
+__device__ __forceinline__ void tc_alloc(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+               :: "r"(smem_u32(dst_smem)), "r"(ncols) : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] x B[smem]^T, kind::tf32, A in TMEM, B K-major in shared memory
+__device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
+               :: "r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(acc ? 1 : 0) : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+               :: "r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ uint64_t smem_desc(const void* base, uint32_t lbo, uint32_t sbo) {
+  const uint32_t a = smem_u32(base);
+  return (uint64_t)((a >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
+}
+// instruction descriptor: D f32, A/B TF32, both K-major, M x N
+__host__ __device__ constexpr uint32_t tc_idesc(int m, int n) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+
+#define SWA_R32(r) "=r"(r[0]),"=r"(r[1]),"=r"(r[2]),"=r"(r[3]),"=r"(r[4]),"=r"(r[5]),"=r"(r[6]),"=r"(r[7]), \
+  "=r"(r[8]),"=r"(r[9]),"=r"(r[10]),"=r"(r[11]),"=r"(r[12]),"=r"(r[13]),"=r"(r[14]),"=r"(r[15]), \
+  "=r"(r[16]),"=r"(r[17]),"=r"(r[18]),"=r"(r[19]),"=r"(r[20]),"=r"(r[21]),"=r"(r[22]),"=r"(r[23]), \
+  "=r"(r[24]),"=r"(r[25]),"=r"(r[26]),"=r"(r[27]),"=r"(r[28]),"=r"(r[29]),"=r"(r[30]),"=r"(r[31])
+#define SWA_W32(r) "r"(r[0]),"r"(r[1]),"r"(r[2]),"r"(r[3]),"r"(r[4]),"r"(r[5]),"r"(r[6]),"r"(r[7]), \
+  "r"(r[8]),"r"(r[9]),"r"(r[10]),"r"(r[11]),"r"(r[12]),"r"(r[13]),"r"(r[14]),"r"(r[15]), \
+  "r"(r[16]),"r"(r[17]),"r"(r[18]),"r"(r[19]),"r"(r[20]),"r"(r[21]),"r"(r[22]),"r"(r[23]), \
+  "r"(r[24]),"r"(r[25]),"r"(r[26]),"r"(r[27]),"r"(r[28]),"r"(r[29]),"r"(r[30]),"r"(r[31])
+#define SWA_LIST32 "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}"
+#define SWA_LIST32_1 "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32}"
+
+// 32 consecutive 32-bit columns of this warp's 32 TMEM lanes (one lane per thread)
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 " SWA_LIST32 ", [%32];" : SWA_R32(r) : "r"(taddr));
+}
+__device__ __forceinline__ void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], " SWA_LIST32_1 ";" :: "r"(taddr), SWA_W32(r) : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t tf32_hi(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
+  using C = TCfg<HD>;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  float* landK = reinterpret_cast<float*>(sm + C::OFF_LK);
+  float* landV = reinterpret_cast<float*>(sm + C::OFF_LV);
+  uint32_t* khi = reinterpret_cast<uint32_t*>(sm + C::OFF_KHI);
+  uint32_t* klo = reinterpret_cast<uint32_t*>(sm + C::OFF_KLO);
+  uint32_t* vhi = reinterpret_cast<uint32_t*>(sm + C::OFF_VHI);
+  uint32_t* vlo = reinterpret_cast<uint32_t*>(sm + C::OFF_VLO);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  uint64_t* land_full = bars + 0;    // [2] producer -> softmax warps (bytes)
+  uint64_t* land_empty = bars + 2;   // [2] softmax warps -> producer (4 arrivals)
+  uint64_t* split_done = bars + 4;   // softmax warps -> MMA (4 arrivals)
+  uint64_t* s_full = bars + 5;       // MMA commit -> softmax warps
+  uint64_t* p_ready = bars + 6;      // softmax warps -> MMA (4 arrivals)
+  uint64_t* pv_done = bars + 7;      // MMA commit -> softmax warps
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 8);
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + 8) + 1);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rb = blockIdx.y, bg = blockIdx.z;
+  const int b = bg / p.nk, g = bg % p.nk;
+  const SeqState st = load_state(p, b, tid == 0 && g == 0 && rb == 0);
+  const int r0 = rb * p.rows;
+  const int r_last = min(r0 + p.rows, p.t) - 1;
+  const int rows_eff = r_last - r0 + 1;
+  const int win0 = min(st.W, st.len0 + r0 + 1);
+  const int xlo = st.len0 + r0 + 1 - win0;
+  const int n = p.ns + (st.len0 + r_last - xlo + 1);
+  if (g == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = 1;
+  if (g == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
+  const int ntiles = (n + kTN - 1) / kTN;
+  const size_t kv_head = (size_t)b * p.nk + g;
+
+  if (tid == 0) {
+    mbar_init(&land_full[0], 1);
+    mbar_init(&land_full[1], 1);
+    mbar_init(&land_empty[0], 4);
+    mbar_init(&land_empty[1], 4);
+    mbar_init(split_done, 4);
+    mbar_init(s_full, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(pv_done, 1);
+    mbar_fence_init();
+    *s_abort = 0;
+  }
+  if (warp == 0) tc_alloc(const_cast<uint32_t*>(s_tmem), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  // ------------------------------------------------------------------ producer
+  if (warp == 4) {
+    for (int i = 0; i < ntiles; ++i) {
+      const int stage = i & 1;
+      const int use = i >> 1;
+      bool ok = use == 0 || mbar_wait_bounded(&land_empty[stage], (uint32_t)((use - 1) & 1), kWaitLimitNs);
+      ok = __all_sync(kTF, ok);
+      if (!ok) {
+        if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
+        break;
+      }
+      if (__shfl_sync(kTF, *s_abort, 0)) break;
+      fence_proxy_async_smem();
+      const int j0 = i * kTN;
+      const int cnt = min(kTN, n - j0);
+      if (lane == 0) mbar_arrive_expect_tx(&land_full[stage], (uint32_t)(cnt * HD * 4 * 2));
+      __syncwarp();
+      const float* sk = nullptr;
+      const float* sv = nullptr;
+      if (lane < cnt) {
+        const int j = j0 + lane;
+        if (j < p.ns) {
+          const size_t at = (kv_head * p.ns + j) * HD;
+          sk = p.sink_k + at;
+          sv = p.sink_v + at;
+        } else {
+          const int x = xlo + (j - p.ns);
+          if (x < st.len0) {
+            int slot = st.head0 + x;
+            if (slot >= st.W) slot -= st.W;
+            const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
+            sk = p.ring_k + at;
+            sv = p.ring_v + at;
+          } else {
+            const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
+            sk = p.k_chunk + at;
+            sv = p.v_chunk + at;
+          }
+        }
+      }
+      const unsigned long long pk = __shfl_up_sync(kTF, reinterpret_cast<unsigned long long>(sk), 1);
+      const unsigned long long pv = __shfl_up_sync(kTF, reinterpret_cast<unsigned long long>(sv), 1);
+      const bool start = lane < cnt && (lane == 0 || reinterpret_cast<unsigned long long>(sk) != pk + HD * 4 ||
+                                        reinterpret_cast<unsigned long long>(sv) != pv + HD * 4);
+      const unsigned starts = __ballot_sync(kTF, start);
+      if (start) {
+        const unsigned later = starts & ~((2u << lane) - 1u);
+        const int end = later ? __ffs(later) - 1 : cnt;
+        const uint32_t bytes = (uint32_t)((end - lane) * HD * 4);
+        bulk_g2s(landK + ((size_t)stage * kTN + lane) * HD, sk, bytes, &land_full[stage]);
+        bulk_g2s(landV + ((size_t)stage * kTN + lane) * HD, sv, bytes, &land_full[stage]);
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ MMA issuer
+  if (warp == 5 && lane == 0) {
+    const uint32_t id_s = tc_idesc(kTM, kTN);
+    const uint32_t id_o = tc_idesc(kTM, HD);
+    for (int i = 0; i < ntiles; ++i) {
+      if (!mbar_wait_bounded(split_done, (uint32_t)(i & 1), kWaitLimitNs) || *s_abort) {
+        *s_abort = 1;
+        set_err(p.err, SWA_DERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      // S = Q_lo K_hi + Q_hi K_lo + Q_hi K_hi over hd / 8 steps of K = 8
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t qcol = term == 0 ? C::C_QLO : C::C_QHI;
+        const uint32_t* kb = term == 1 ? klo : khi;
+        for (int ks = 0; ks < HD / 8; ++ks) {
+          const uint64_t bd = smem_desc(kb + ks * 64, C::K_LBO, C::K_SBO);   // 2 core matrices along K
+          tc_mma(tmem + C::C_S, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
+        }
+      }
+      tc_commit(s_full);
+      if (!mbar_wait_bounded(p_ready, (uint32_t)(i & 1), kWaitLimitNs) || *s_abort) {
+        *s_abort = 1;
+        set_err(p.err, SWA_DERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      // O += P_lo V_hi + P_hi V_lo + P_hi V_hi over 32 / 8 steps of K = 8
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t pcol = term == 0 ? C::C_PLO : C::C_PHI;
+        const uint32_t* vb = term == 1 ? vlo : vhi;
+        for (int ks = 0; ks < kTN / 8; ++ks) {
+          const uint64_t bd = smem_desc(vb + ks * 64, C::V_LBO, C::V_SBO);
+          tc_mma(tmem + C::C_O, tmem + pcol + ks * 8, bd, id_o, i > 0 || term > 0 || ks > 0);
+        }
+      }
+      tc_commit(pv_done);
+    }
+  }
+
+  // ------------------------------------------------------------------ softmax warps
+  if (warp < 4) {
+    const int q = tid;                                   // query vector = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int rr = q / p.hpg, h = q % p.hpg;
+    const bool q_ok = rr < rows_eff && q < p.rows * p.hpg;
+    const int r = r0 + rr;
+    const int q_lo = st.len0 + r + 1 - min(st.W, st.len0 + r + 1);
+    const int q_hi = st.len0 + r;
+    // Q row -> TMEM (hi and lo parts), times scale * log2 e
+    {
+      const float* src = p.q + (((size_t)b * p.t + r) * p.nh + (size_t)g * p.hpg + h) * HD;
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (q_ok) v = *reinterpret_cast<const float4*>(src + c0 + c);
+          const float x[4] = {v.x * p.qmul, v.y * p.qmul, v.z * p.qmul, v.w * p.qmul};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[c + e] = tf32_hi(x[e]);
+            lo[c + e] = tf32_hi(x[e] - __uint_as_float(hi[c + e]));
+          }
+        }
+        tc_st32(tmem + lane_off + C::C_QHI + c0, hi);
+        tc_st32(tmem + lane_off + C::C_QLO + c0, lo);
+      }
+      tc_wait_st();
+    }
+    float m_run = -INFINITY, l_run = 0.f;
+    bool dead = false;
+    for (int i = 0; i < ntiles; ++i) {
+      const int stage = i & 1;
+      bool ok = mbar_wait_bounded(&land_full[stage], (uint32_t)((i >> 1) & 1), kWaitLimitNs);
+      if (i > 0) ok = ok && mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), kWaitLimitNs);
+      ok = __all_sync(kTF, ok);
+      if (!ok || *s_abort) {
+        if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
+        dead = true;
+        break;
+      }
+      tc_fence_after();
+      const int cnt = min(kTN, n - i * kTN);
+      // ---- split the fp32 tiles into TF32 hi/lo operands (K-major core matrices)
+      const float* lk = landK + (size_t)stage * kTN * HD;
+      const float* lv = landV + (size_t)stage * kTN * HD;
+      // K: element (key, f) -> (key/8)*K_SBO + (f/4)*128 + (key%8)*16 + (f%4)*4 bytes
+      for (int idx = tid; idx < kTN * HD / 4; idx += kSoftThreads) {
+        const int key = idx % kTN, f4 = idx / kTN;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (key < cnt) v = *reinterpret_cast<const float4*>(lk + key * HD + f4 * 4);
+        const float x[4] = {v.x, v.y, v.z, v.w};
+        uint4 hv, lv4;
+        uint32_t* hp = &hv.x;
+        uint32_t* lp = &lv4.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          hp[e] = tf32_hi(x[e]);
+          lp[e] = tf32_hi(x[e] - __uint_as_float(hp[e]));
+        }
+        const int off = ((key >> 3) * (int)C::K_SBO + f4 * 128 + (key & 7) * 16) / 4;
+        *reinterpret_cast<uint4*>(khi + off) = hv;
+        *reinterpret_cast<uint4*>(klo + off) = lv4;
+      }
+      // V^T: element (f, key) -> (f/8)*V_SBO + (key/4)*128 + (f%8)*16 + (key%4)*4 bytes
+      for (int idx = tid; idx < HD * kTN / 4; idx += kSoftThreads) {
+        const int f = idx % HD, k4 = idx / HD;
+        uint4 hv, lv4;
+        uint32_t* hp = &hv.x;
+        uint32_t* lp = &lv4.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int key = k4 * 4 + e;
+          const float x = key < cnt ? lv[key * HD + f] : 0.f;
+          hp[e] = tf32_hi(x);
+          lp[e] = tf32_hi(x - __uint_as_float(hp[e]));
+        }
+        const int off = ((f >> 3) * (int)C::V_SBO + k4 * 128 + (f & 7) * 16) / 4;
+        *reinterpret_cast<uint4*>(vhi + off) = hv;
+        *reinterpret_cast<uint4*>(vlo + off) = lv4;
+      }
+      fence_proxy_async_smem();               // generic writes -> tensor-core reads
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&land_empty[stage]);
+        mbar_arrive(split_done);
+      }
+      // ---- scores of this query vector against the tile's 32 keys
+      if (!__all_sync(kTF, mbar_wait_bounded(s_full, (uint32_t)(i & 1), kWaitLimitNs))) {
+        if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
+        dead = true;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[32];
+      tc_ld32(tmem + lane_off + C::C_S, sr);
+      tc_wait_ld();
+      float tmax = -INFINITY;
+      float s[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const int j = i * kTN + k;
+        bool v = q_ok && k < cnt;
+        if (v && j >= p.ns) {
+          const int x = xlo + (j - p.ns);
+          v = x >= q_lo && x <= q_hi;
+        }
+        s[k] = v ? __uint_as_float(sr[k]) : -INFINITY;
+        tmax = fmaxf(tmax, s[k]);
+      }
+      const float m_new = fmaxf(m_run, tmax);
+      const float c = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+      uint32_t phi[32], plo[32];
+      float psum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) {
+        const float pv = m_new == -INFINITY ? 0.f : exp2f(s[k] - m_new);
+        psum += pv;
+        phi[k] = tf32_hi(pv);
+        plo[k] = tf32_hi(pv - __uint_as_float(phi[k]));
+      }
+      l_run = l_run * c + psum;
+      m_run = m_new;
+      tc_st32(tmem + lane_off + C::C_PHI, phi);
+      tc_st32(tmem + lane_off + C::C_PLO, plo);
+      // rescale this row of O when its max moved (warp-uniform decision)
+      if (i > 0 && __any_sync(kTF, c != 1.f)) {
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(tmem + lane_off + C::C_O + c0, o);
+          tc_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * c);
+          tc_st32(tmem + lane_off + C::C_O + c0, o);
+        }
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(p_ready);
+    }
+    // ---- the block's record: m, l, O (unnormalised)
+    if (!dead && !*s_abort) {
+      const bool ok = __all_sync(kTF, ntiles == 0 ||
+                                          mbar_wait_bounded(pv_done, (uint32_t)((ntiles - 1) & 1), kWaitLimitNs));
+      if (ok) {
+        tc_fence_after();
+        const size_t item = ((size_t)bg * p.n_rb + rb) * p.splits;
+        float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(tmem + lane_off + C::C_O + c0, o);
+          tc_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(dst + c0 + k) =
+                make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]), __uint_as_float(o[k + 2]),
+                            __uint_as_float(o[k + 3]));
+        }
+        p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run);
+      } else if (lane == 0) {
+        *s_abort = 1;
+        set_err(p.err, SWA_DERR_TIMEOUT);
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  // Outstanding MMAs of an aborted run finish on their own; wait (bounded) for
+  // the last commit before the tensor memory is released.
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    if (*s_abort && ntiles > 0) mbar_wait_bounded(pv_done, (uint32_t)((ntiles - 1) & 1), kWaitLimitNs);
+    tc_fence_after();
+    tc_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int HD>
+int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  using C = TCfg<HD>;
+  auto kern = attend_prompt_tc_kernel<HD>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  dim3 grid(1u, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
+  if (e0) cudaEventRecord(e0, s);
+  kern<<<grid, kTThreads, C::BYTES, s>>>(p);
+  note_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e1) cudaEventRecord(e1, s);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  switch (p.hd) {
+    case 64: return launch_tc<64>(p, s, e0, e1);
+    case 128: return launch_tc<128>(p, s, e0, e1);
+  }
+  return SWA_E_SHAPE;
+}
+
+}  // namespace swa

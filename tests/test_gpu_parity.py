@@ -99,6 +99,9 @@ ATTEND_CASES = [
     dict(B=2, t=33, nh=12, nk=2, hd=64, window=20, cap=20, ns=1, pos_mode="full", pos_lo=20, pos_hi=900),
     # tensor-core prompt path: empty ring, hpg 4, several key tiles
     dict(B=2, t=70, nh=8, nk=2, hd=128, window=64, cap=64, ns=0, pos_mode="prompt", pos_lo=0, pos_hi=200),
+    # mid-size chunks (64 <= rows x heads < 128): the 64-vector mma.sync path
+    dict(B=2, t=20, nh=8, nk=2, hd=128, window=90, cap=90, ns=2, pos_mode="full", pos_lo=90, pos_hi=900),
+    dict(B=2, t=12, nh=16, nk=2, hd=64, window=30, cap=30, ns=1, pos_mode="partial", pos_lo=1, pos_hi=30),
 ]
 
 
