@@ -23,6 +23,11 @@
 // canonical core-matrix layout: 8 rows x 16 bytes per core matrix) and
 // V^T_hi/V^T_lo (hd x 32 keys, K-major): TF32 operands must be K-major, so V
 // is transposed while it is split.
+// Pipelining: the hi/lo operand sets and the S accumulator are double
+// buffered, so the MMA lane issues S of tile i+1 before P V of tile i and the
+// tensor cores compute the next scores while the softmax warps work on the
+// current ones; the K half of the next split needs no wait (its buffer was
+// last read by S of tile i-1), only its V half waits for P V of tile i-1.
 // Every hand-off is an mbarrier; all waits are bounded (1 s) and report
 // SWA_DERR_TIMEOUT; tensor memory is released on every path.
 #include "swa_internal.cuh"
@@ -39,20 +44,18 @@ constexpr unsigned kTF = 0xffffffffu;
 template <int HD>
 struct TCfg {
   // TMEM columns
-  static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S = 2 * HD, C_O = 2 * HD + kTN;
-  static constexpr uint32_t C_PHI = 3 * HD + kTN, C_PLO = 3 * HD + 2 * kTN;
+  static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S0 = 2 * HD, C_S1 = 2 * HD + kTN;
+  static constexpr uint32_t C_O = 2 * HD + 2 * kTN, C_PHI = 3 * HD + 2 * kTN, C_PLO = 3 * HD + 3 * kTN;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(3 * HD + 3 * kTN <= 512, "tensor memory budget");
+  static_assert(3 * HD + 4 * kTN <= 512, "tensor memory budget");
   // shared memory (bytes)
   static constexpr int LAND = kTN * HD * 4;                 // one fp32 tile of K or V
   static constexpr int OFF_LK = 0;                          // [2 stages] K landing
   static constexpr int OFF_LV = 2 * LAND;                   // [2 stages] V landing
-  static constexpr int OFF_KHI = 4 * LAND;
-  static constexpr int OFF_KLO = OFF_KHI + LAND;
-  static constexpr int OFF_VHI = OFF_KLO + LAND;
-  static constexpr int OFF_VLO = OFF_VHI + LAND;
-  static constexpr int OFF_BAR = OFF_VLO + LAND;            // mbarriers
-  static constexpr int NBAR = 9;
+  static constexpr int OFF_OPS = 4 * LAND;                  // [2 sets] K_hi, K_lo, V^T_hi, V^T_lo
+  static constexpr int SET = 4 * LAND;
+  static constexpr int OFF_BAR = OFF_OPS + 2 * SET;         // mbarriers
+  static constexpr int NBAR = 12;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
@@ -126,19 +129,19 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   extern __shared__ __align__(1024) unsigned char sm[];
   float* landK = reinterpret_cast<float*>(sm + C::OFF_LK);
   float* landV = reinterpret_cast<float*>(sm + C::OFF_LV);
-  uint32_t* khi = reinterpret_cast<uint32_t*>(sm + C::OFF_KHI);
-  uint32_t* klo = reinterpret_cast<uint32_t*>(sm + C::OFF_KLO);
-  uint32_t* vhi = reinterpret_cast<uint32_t*>(sm + C::OFF_VHI);
-  uint32_t* vlo = reinterpret_cast<uint32_t*>(sm + C::OFF_VLO);
+  // operand set k (k = tile % 2): K_hi, K_lo, V^T_hi, V^T_lo
+  auto op = [&](int set, int which) {
+    return reinterpret_cast<uint32_t*>(sm + C::OFF_OPS + set * C::SET + which * C::LAND);
+  };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint64_t* land_full = bars + 0;    // [2] producer -> softmax warps (bytes)
   uint64_t* land_empty = bars + 2;   // [2] softmax warps -> producer (4 arrivals)
-  uint64_t* split_done = bars + 4;   // softmax warps -> MMA (4 arrivals)
-  uint64_t* s_full = bars + 5;       // MMA commit -> softmax warps
-  uint64_t* p_ready = bars + 6;      // softmax warps -> MMA (4 arrivals)
-  uint64_t* pv_done = bars + 7;      // MMA commit -> softmax warps
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 8);
-  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + 8) + 1);
+  uint64_t* split_done = bars + 4;   // [2 sets] softmax warps -> MMA (4 arrivals)
+  uint64_t* s_full = bars + 6;       // [2 S buffers] MMA commit -> softmax warps
+  uint64_t* p_ready = bars + 8;      // softmax warps -> MMA (4 arrivals)
+  uint64_t* pv_done = bars + 9;      // MMA commit -> softmax warps
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 10);
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + 10) + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rb = blockIdx.y, bg = blockIdx.z;
@@ -160,8 +163,10 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     mbar_init(&land_full[1], 1);
     mbar_init(&land_empty[0], 4);
     mbar_init(&land_empty[1], 4);
-    mbar_init(split_done, 4);
-    mbar_init(s_full, 1);
+    mbar_init(&split_done[0], 4);
+    mbar_init(&split_done[1], 4);
+    mbar_init(&s_full[0], 1);
+    mbar_init(&s_full[1], 1);
     mbar_init(p_ready, 4);
     mbar_init(pv_done, 1);
     mbar_fence_init();
@@ -232,41 +237,46 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   if (warp == 5 && lane == 0) {
     const uint32_t id_s = tc_idesc(kTM, kTN);
     const uint32_t id_o = tc_idesc(kTM, HD);
-    for (int i = 0; i < ntiles; ++i) {
-      if (!mbar_wait_bounded(split_done, (uint32_t)(i & 1), kWaitLimitNs) || *s_abort) {
-        *s_abort = 1;
-        set_err(p.err, SWA_DERR_TIMEOUT);
-        break;
-      }
+    // S(j) = Q_lo K_hi + Q_hi K_lo + Q_hi K_hi of tile j into S buffer j % 2
+    auto issue_s = [&](int j) -> bool {
+      const int set = j & 1;
+      if (!mbar_wait_bounded(&split_done[set], (uint32_t)((j >> 1) & 1), kWaitLimitNs) || *s_abort)
+        return false;
       tc_fence_after();
-      // S = Q_lo K_hi + Q_hi K_lo + Q_hi K_hi over hd / 8 steps of K = 8
+      const uint32_t dcol = set ? C::C_S1 : C::C_S0;
 #pragma unroll 1
       for (int term = 0; term < 3; ++term) {
         const uint32_t qcol = term == 0 ? C::C_QLO : C::C_QHI;
-        const uint32_t* kb = term == 1 ? klo : khi;
+        const uint32_t* kb = op(set, term == 1 ? 1 : 0);
         for (int ks = 0; ks < HD / 8; ++ks) {
           const uint64_t bd = smem_desc(kb + ks * 64, C::K_LBO, C::K_SBO);   // 2 core matrices along K
-          tc_mma(tmem + C::C_S, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
+          tc_mma(tmem + dcol, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
         }
       }
-      tc_commit(s_full);
-      if (!mbar_wait_bounded(p_ready, (uint32_t)(i & 1), kWaitLimitNs) || *s_abort) {
-        *s_abort = 1;
-        set_err(p.err, SWA_DERR_TIMEOUT);
-        break;
-      }
+      tc_commit(&s_full[set]);
+      return true;
+    };
+    bool ok = ntiles == 0 || issue_s(0);
+    for (int i = 0; ok && i < ntiles; ++i) {
+      if (i + 1 < ntiles && !issue_s(i + 1)) { ok = false; break; }
+      if (!mbar_wait_bounded(p_ready, (uint32_t)(i & 1), kWaitLimitNs) || *s_abort) { ok = false; break; }
       tc_fence_after();
       // O += P_lo V_hi + P_hi V_lo + P_hi V_hi over 32 / 8 steps of K = 8
+      const int set = i & 1;
 #pragma unroll 1
       for (int term = 0; term < 3; ++term) {
         const uint32_t pcol = term == 0 ? C::C_PLO : C::C_PHI;
-        const uint32_t* vb = term == 1 ? vlo : vhi;
+        const uint32_t* vb = op(set, term == 1 ? 3 : 2);
         for (int ks = 0; ks < kTN / 8; ++ks) {
           const uint64_t bd = smem_desc(vb + ks * 64, C::V_LBO, C::V_SBO);
           tc_mma(tmem + C::C_O, tmem + pcol + ks * 8, bd, id_o, i > 0 || term > 0 || ks > 0);
         }
       }
       tc_commit(pv_done);
+    }
+    if (!ok) {
+      *s_abort = 1;
+      set_err(p.err, SWA_DERR_TIMEOUT);
     }
   }
 
@@ -302,24 +312,24 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     }
     float m_run = -INFINITY, l_run = 0.f;
     bool dead = false;
-    for (int i = 0; i < ntiles; ++i) {
-      const int stage = i & 1;
-      bool ok = mbar_wait_bounded(&land_full[stage], (uint32_t)((i >> 1) & 1), kWaitLimitNs);
-      if (i > 0) ok = ok && mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), kWaitLimitNs);
-      ok = __all_sync(kTF, ok);
-      if (!ok || *s_abort) {
-        if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
-        dead = true;
-        break;
-      }
-      tc_fence_after();
-      const int cnt = min(kTN, n - i * kTN);
-      // ---- split the fp32 tiles into TF32 hi/lo operands (K-major core matrices)
-      const float* lk = landK + (size_t)stage * kTN * HD;
-      const float* lv = landV + (size_t)stage * kTN * HD;
-      // K: element (key, f) -> (key/8)*K_SBO + (f/4)*128 + (key%8)*16 + (f%4)*4 bytes
-      for (int idx = tid; idx < kTN * HD / 4; idx += kSoftThreads) {
-        const int key = idx % kTN, f4 = idx / kTN;
+    auto fail = [&]() {
+      if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
+      dead = true;
+    };
+    // fp32 landing tile j -> TF32 hi/lo operands of set j % 2.
+    // K: element (key, f) -> (key/8)*K_SBO + (f/4)*128 + (key%8)*16 + (f%4)*4 bytes. Lane t of an
+    // 8-lane phase takes key 8kg + t and feature chunk (fb + t) mod hd/4, so the 8 reads hit 8
+    // different chunks of 8 rows and the 8 writes 8 consecutive 16-byte slots: no bank conflicts.
+    auto split_k = [&](int j) {
+      const float* lk = landK + (size_t)(j & 1) * kTN * HD;
+      uint32_t* kh = op(j & 1, 0);
+      uint32_t* kl = op(j & 1, 1);
+      const int cnt = min(kTN, n - j * kTN);
+      constexpr int D4 = HD / 4;
+      for (int idx = tid; idx < kTN * D4; idx += kSoftThreads) {
+        const int t8 = idx & 7, rest = idx >> 3;
+        const int kg = rest % (kTN / 8), fb = rest / (kTN / 8);
+        const int key = kg * 8 + t8, f4 = (fb + t8) % D4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (key < cnt) v = *reinterpret_cast<const float4*>(lk + key * HD + f4 * 4);
         const float x[4] = {v.x, v.y, v.z, v.w};
@@ -332,10 +342,16 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
           lp[e] = tf32_hi(x[e] - __uint_as_float(hp[e]));
         }
         const int off = ((key >> 3) * (int)C::K_SBO + f4 * 128 + (key & 7) * 16) / 4;
-        *reinterpret_cast<uint4*>(khi + off) = hv;
-        *reinterpret_cast<uint4*>(klo + off) = lv4;
+        *reinterpret_cast<uint4*>(kh + off) = hv;
+        *reinterpret_cast<uint4*>(kl + off) = lv4;
       }
-      // V^T: element (f, key) -> (f/8)*V_SBO + (key/4)*128 + (f%8)*16 + (key%4)*4 bytes
+    };
+    // V^T: element (f, key) -> (f/8)*V_SBO + (key/4)*128 + (f%8)*16 + (key%4)*4 bytes
+    auto split_v = [&](int j) {
+      const float* lv = landV + (size_t)(j & 1) * kTN * HD;
+      uint32_t* vh = op(j & 1, 2);
+      uint32_t* vl = op(j & 1, 3);
+      const int cnt = min(kTN, n - j * kTN);
       for (int idx = tid; idx < HD * kTN / 4; idx += kSoftThreads) {
         const int f = idx % HD, k4 = idx / HD;
         uint4 hv, lv4;
@@ -349,24 +365,46 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
           lp[e] = tf32_hi(x - __uint_as_float(hp[e]));
         }
         const int off = ((f >> 3) * (int)C::V_SBO + k4 * 128 + (f & 7) * 16) / 4;
-        *reinterpret_cast<uint4*>(vhi + off) = hv;
-        *reinterpret_cast<uint4*>(vlo + off) = lv4;
+        *reinterpret_cast<uint4*>(vh + off) = hv;
+        *reinterpret_cast<uint4*>(vl + off) = lv4;
       }
+    };
+    // Split of tile j: K half, then (after P V of tile j - 2 freed the V half) V half.
+    auto split = [&](int j) -> bool {
+      if (!__all_sync(kTF, mbar_wait_bounded(&land_full[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitNs)))
+        return false;
+      split_k(j);
+      if (j >= 2 && !__all_sync(kTF, mbar_wait_bounded(pv_done, (uint32_t)((j - 2) & 1), kWaitLimitNs)))
+        return false;
+      split_v(j);
       fence_proxy_async_smem();               // generic writes -> tensor-core reads
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&land_empty[stage]);
-        mbar_arrive(split_done);
+        mbar_arrive(&land_empty[j & 1]);
+        mbar_arrive(&split_done[j & 1]);
       }
-      // ---- scores of this query vector against the tile's 32 keys
-      if (!__all_sync(kTF, mbar_wait_bounded(s_full, (uint32_t)(i & 1), kWaitLimitNs))) {
-        if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
-        dead = true;
+      return true;
+    };
+    if (ntiles > 0 && !split(0)) fail();
+    for (int i = 0; !dead && i < ntiles; ++i) {
+      if (*s_abort) { fail(); break; }
+      if (i + 1 < ntiles) {
+        if (!split(i + 1)) { fail(); break; }     // waits P V of tile i - 1 for its V half
+      } else if (i >= 1) {
+        if (!__all_sync(kTF, mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), kWaitLimitNs))) {
+          fail();
+          break;
+        }
+      }
+      // P V of tile i - 1 is complete here: P and O may be rewritten
+      const int cnt = min(kTN, n - i * kTN);
+      if (!__all_sync(kTF, mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1), kWaitLimitNs))) {
+        fail();
         break;
       }
       tc_fence_after();
       uint32_t sr[32];
-      tc_ld32(tmem + lane_off + C::C_S, sr);
+      tc_ld32(tmem + lane_off + ((i & 1) ? C::C_S1 : C::C_S0), sr);
       tc_wait_ld();
       float tmax = -INFINITY;
       float s[32];
