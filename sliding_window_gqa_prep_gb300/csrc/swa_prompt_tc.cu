@@ -9,14 +9,15 @@
 // kind::tf32), which keeps f32 accuracy (the dropped a_lo b_lo is ~2^-22 of
 // the product).
 //
-// CTA = 6 warps:
+// CTA = 10 warps:
 //   warps 0-3  one thread per query vector = per TMEM lane (the 128-row MMA
-//              accumulator rows): split of the K/V tiles into TF32 hi/lo
-//              shared-memory operands, softmax of the thread's own score row
-//              (read from TMEM), P into TMEM, rescale of O, final record;
+//              accumulator rows): softmax of the thread's own score row (read
+//              from TMEM), P into TMEM, rescale of O, final record;
 //   warp 4     producer: keys with contiguous sources (ring runs, sinks) as one
 //              cp.async.bulk per run into fp32 landing tiles of 32 keys;
-//   warp 5     one elected lane issues every tcgen05.mma and tcgen05.commit.
+//   warp 5     one elected lane issues every tcgen05.mma and tcgen05.commit;
+//   warps 6-9  split of the landed K/V tiles into TF32 hi/lo shared-memory
+//              operands, in parallel with the softmax warps.
 // Tensor memory (512 columns): Q_hi, Q_lo (A operands of S = Q K^T), S,
 // O (the P V accumulator), P_hi, P_lo (A operands of P V).
 // Shared memory: two fp32 landing stages, K_hi/K_lo (32 keys x hd, K-major
@@ -37,7 +38,7 @@ namespace {
 
 constexpr int kTM = 128;               // query vectors per CTA (MMA M)
 constexpr int kTN = 32;                // keys per tile
-constexpr int kTThreads = 6 * 32;
+constexpr int kTThreads = 10 * 32;
 constexpr int kSoftThreads = 128;
 constexpr unsigned kTF = 0xffffffffu;
 
@@ -55,7 +56,7 @@ struct TCfg {
   static constexpr int OFF_OPS = 4 * LAND;                  // [2 sets] K_hi, K_lo, V^T_hi, V^T_lo
   static constexpr int SET = 4 * LAND;
   static constexpr int OFF_BAR = OFF_OPS + 2 * SET;         // mbarriers
-  static constexpr int NBAR = 12;
+  static constexpr int NBAR = 14;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
@@ -140,8 +141,9 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   uint64_t* s_full = bars + 6;       // [2 S buffers] MMA commit -> softmax warps
   uint64_t* p_ready = bars + 8;      // softmax warps -> MMA (4 arrivals)
   uint64_t* pv_done = bars + 9;      // MMA commit -> softmax warps
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 10);
-  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + 10) + 1);
+  uint64_t* v_free = bars + 10;      // [2 sets] MMA commit (P V of the set done) -> split warps
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 12);
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + 12) + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rb = blockIdx.y, bg = blockIdx.z;
@@ -169,6 +171,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     mbar_init(&s_full[1], 1);
     mbar_init(p_ready, 4);
     mbar_init(pv_done, 1);
+    mbar_init(&v_free[0], 1);
+    mbar_init(&v_free[1], 1);
     mbar_fence_init();
     *s_abort = 0;
   }
@@ -177,6 +181,39 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
+
+  // Q rows of the block -> TMEM (hi and lo parts), times scale * log2 e; done by
+  // the softmax warps before any role starts, so the first S finds Q in place.
+  if (warp < 4) {
+    const int q = tid;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int rr = q / p.hpg, h = q % p.hpg;
+    const bool q_ok = rr < rows_eff && q < p.rows * p.hpg;
+    const int r = r0 + rr;
+    {
+      const float* src = p.q + (((size_t)b * p.t + r) * p.nh + (size_t)g * p.hpg + h) * HD;
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int c = 0; c < 32; c += 4) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (q_ok) v = *reinterpret_cast<const float4*>(src + c0 + c);
+          const float x[4] = {v.x * p.qmul, v.y * p.qmul, v.z * p.qmul, v.w * p.qmul};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            hi[c + e] = tf32_hi(x[e]);
+            lo[c + e] = tf32_hi(x[e] - __uint_as_float(hi[c + e]));
+          }
+        }
+        tc_st32(tmem + lane_off + C::C_QHI + c0, hi);
+        tc_st32(tmem + lane_off + C::C_QLO + c0, lo);
+      }
+      tc_wait_st();
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
   // ------------------------------------------------------------------ producer
   if (warp == 4) {
@@ -273,6 +310,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
         }
       }
       tc_commit(pv_done);
+      tc_commit(&v_free[set]);
     }
     if (!ok) {
       *s_abort = 1;
@@ -280,42 +318,9 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     }
   }
 
-  // ------------------------------------------------------------------ softmax warps
-  if (warp < 4) {
-    const int q = tid;                                   // query vector = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const int rr = q / p.hpg, h = q % p.hpg;
-    const bool q_ok = rr < rows_eff && q < p.rows * p.hpg;
-    const int r = r0 + rr;
-    const int q_lo = st.len0 + r + 1 - min(st.W, st.len0 + r + 1);
-    const int q_hi = st.len0 + r;
-    // Q row -> TMEM (hi and lo parts), times scale * log2 e
-    {
-      const float* src = p.q + (((size_t)b * p.t + r) * p.nh + (size_t)g * p.hpg + h) * HD;
-      for (int c0 = 0; c0 < HD; c0 += 32) {
-        uint32_t hi[32], lo[32];
-#pragma unroll
-        for (int c = 0; c < 32; c += 4) {
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (q_ok) v = *reinterpret_cast<const float4*>(src + c0 + c);
-          const float x[4] = {v.x * p.qmul, v.y * p.qmul, v.z * p.qmul, v.w * p.qmul};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            hi[c + e] = tf32_hi(x[e]);
-            lo[c + e] = tf32_hi(x[e] - __uint_as_float(hi[c + e]));
-          }
-        }
-        tc_st32(tmem + lane_off + C::C_QHI + c0, hi);
-        tc_st32(tmem + lane_off + C::C_QLO + c0, lo);
-      }
-      tc_wait_st();
-    }
-    float m_run = -INFINITY, l_run = 0.f;
-    bool dead = false;
-    auto fail = [&]() {
-      if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
-      dead = true;
-    };
+  // ------------------------------------------------------------------ split warps
+  if (warp >= 6) {
+    const int sidx = tid - 6 * 32;                     // 0 .. 127
     // fp32 landing tile j -> TF32 hi/lo operands of set j % 2.
     // K: element (key, f) -> (key/8)*K_SBO + (f/4)*128 + (key%8)*16 + (f%4)*4 bytes. Lane t of an
     // 8-lane phase takes key 8kg + t and feature chunk (fb + t) mod hd/4, so the 8 reads hit 8
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       uint32_t* kl = op(j & 1, 1);
       const int cnt = min(kTN, n - j * kTN);
       constexpr int D4 = HD / 4;
-      for (int idx = tid; idx < kTN * D4; idx += kSoftThreads) {
+      for (int idx = sidx; idx < kTN * D4; idx += kSoftThreads) {
         const int t8 = idx & 7, rest = idx >> 3;
         const int kg = rest % (kTN / 8), fb = rest / (kTN / 8);
         const int key = kg * 8 + t8, f4 = (fb + t8) % D4;
@@ -352,7 +357,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       uint32_t* vh = op(j & 1, 2);
       uint32_t* vl = op(j & 1, 3);
       const int cnt = min(kTN, n - j * kTN);
-      for (int idx = tid; idx < HD * kTN / 4; idx += kSoftThreads) {
+      for (int idx = sidx; idx < HD * kTN / 4; idx += kSoftThreads) {
         const int f = idx % HD, k4 = idx / HD;
         uint4 hv, lv4;
         uint32_t* hp = &hv.x;
@@ -369,13 +374,17 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
         *reinterpret_cast<uint4*>(vl + off) = lv4;
       }
     };
-    // Split of tile j: K half, then (after P V of tile j - 2 freed the V half) V half.
-    auto split = [&](int j) -> bool {
-      if (!__all_sync(kTF, mbar_wait_bounded(&land_full[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitNs)))
-        return false;
-      split_k(j);
-      if (j >= 2 && !__all_sync(kTF, mbar_wait_bounded(pv_done, (uint32_t)((j - 2) & 1), kWaitLimitNs)))
-        return false;
+    // tile j: K half, then (once P V of tile j - 2 has freed the set) V half
+    for (int j = 0; j < ntiles; ++j) {
+      bool ok = mbar_wait_bounded(&land_full[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitNs);
+      ok = __all_sync(kTF, ok) && !*s_abort;
+      if (ok) split_k(j);
+      if (ok && j >= 2)
+        ok = __all_sync(kTF, mbar_wait_bounded(&v_free[j & 1], (uint32_t)(((j - 2) >> 1) & 1), kWaitLimitNs));
+      if (!ok) {
+        if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
+        break;
+      }
       split_v(j);
       fence_proxy_async_smem();               // generic writes -> tensor-core reads
       __syncwarp();
@@ -383,18 +392,29 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
         mbar_arrive(&land_empty[j & 1]);
         mbar_arrive(&split_done[j & 1]);
       }
-      return true;
+    }
+  }
+
+  // ------------------------------------------------------------------ softmax warps
+  if (warp < 4) {
+    const int q = tid;                                   // query vector = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int rr = q / p.hpg;
+    const bool q_ok = rr < rows_eff && q < p.rows * p.hpg;
+    const int r = r0 + rr;
+    const int q_lo = st.len0 + r + 1 - min(st.W, st.len0 + r + 1);
+    const int q_hi = st.len0 + r;
+    float m_run = -INFINITY, l_run = 0.f;
+    bool dead = false;
+    auto fail = [&]() {
+      if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
+      dead = true;
     };
-    if (ntiles > 0 && !split(0)) fail();
     for (int i = 0; !dead && i < ntiles; ++i) {
       if (*s_abort) { fail(); break; }
-      if (i + 1 < ntiles) {
-        if (!split(i + 1)) { fail(); break; }     // waits P V of tile i - 1 for its V half
-      } else if (i >= 1) {
-        if (!__all_sync(kTF, mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), kWaitLimitNs))) {
-          fail();
-          break;
-        }
+      if (i >= 1 && !__all_sync(kTF, mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), kWaitLimitNs))) {
+        fail();
+        break;
       }
       // P V of tile i - 1 is complete here: P and O may be rewritten
       const int cnt = min(kTN, n - i * kTN);
