@@ -100,6 +100,10 @@ int swa_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd,
  * and, when ring_k/ring_v are non-NULL, k_out/v_out rows also go to ring
  * slot (pos0[b] + j) % cap.
  *
+ * rope may be NULL: the kernel then computes each row's cos/sin itself from
+ * pos0 and theta exactly as swa_rope_table does (same f64 angles, same f32
+ * rounding, bit-identical values) and no table is read or written.
+ *
  * The ring write is only accepted for t == 1 (SWA_E_HAZARD otherwise): with a
  * full ring a chunk's later rows land on slots that its earlier rows still
  * read. For t > 1 pass NULL rings here and let swa_attend commit the chunk
@@ -114,14 +118,15 @@ typedef struct swa_prep_args {
   const float* yq;               /* [B][t][nh][hd]                          */
   const float* yk;               /* [B][t][nk][hd]                          */
   const float* yv;               /* [B][t][nk][hd]                          */
-  const float* rope;             /* [B][t][hd] (swa_rope_table)             */
+  const float* rope;             /* [B][t][hd] (swa_rope_table) or NULL     */
   const float* q_scale;          /* [nh][hd]                                */
-  const uint32_t* pos0;          /* [B]; required when rings are given      */
+  const uint32_t* pos0;          /* [B]; required with rings or rope NULL   */
   float* q_out;                  /* [B][t][nh][hd]                          */
   float* k_out;                  /* [B][t][nk][hd]                          */
   float* v_out;                  /* [B][t][nk][hd] or NULL (no copy)        */
   float* ring_k;                 /* [B][nk][cap][hd] or NULL                */
   float* ring_v;                 /* [B][nk][cap][hd] or NULL (with ring_k)  */
+  double theta;                  /* RoPE base, read only when rope is NULL  */
 } swa_prep_args;
 
 int swa_prep(const swa_prep_args* args, cudaStream_t stream);

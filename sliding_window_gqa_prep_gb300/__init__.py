@@ -74,10 +74,13 @@ def rope_table(pos0: torch.Tensor, t: int, hd: int, theta: float = 10000.0,
 
 
 def prep(yq, yk, yv, rope, q_scale, eps: float = 1e-6, *, pos0=None, ring_k=None,
-         ring_v=None, q_out=None, k_out=None, v_out=None, copy_v: bool = True, stream=None):
+         ring_v=None, q_out=None, k_out=None, v_out=None, copy_v: bool = True,
+         theta: float = 10000.0, stream=None):
     """Rotation, unit heads, query scale and (t == 1 only) the ring write.
 
-    Returns (q_out, k_out, v) where v is v_out when copy_v, else yv itself."""
+    rope=None computes the RoPE angles in the kernel from pos0 and theta
+    (bit-identical to rope_table). Returns (q_out, k_out, v) where v is v_out
+    when copy_v, else yv itself."""
     B, t, nh, hd = yq.shape
     nk = yk.shape[2]
     if q_out is None:
@@ -93,9 +96,10 @@ def prep(yq, yk, yv, rope, q_scale, eps: float = 1e-6, *, pos0=None, ring_k=None
     a.yq = _ptr(yq, "yq", (B, t, nh, hd))
     a.yk = _ptr(yk, "yk", (B, t, nk, hd))
     a.yv = _ptr(yv, "yv", (B, t, nk, hd))
-    a.rope = _ptr(rope, "rope", (B, t, hd))
+    a.rope = _ptr(rope, "rope", (B, t, hd), required=False)
+    a.theta = float(theta)
     a.q_scale = _ptr(q_scale, "q_scale", (nh, hd))
-    a.pos0 = _ptr(pos0, "pos0", (B,), torch.int32, required=ring_k is not None)
+    a.pos0 = _ptr(pos0, "pos0", (B,), torch.int32, required=ring_k is not None or rope is None)
     a.q_out = _ptr(q_out, "q_out", (B, t, nh, hd))
     a.k_out = _ptr(k_out, "k_out", (B, t, nk, hd))
     a.v_out = _ptr(v_out, "v_out", (B, t, nk, hd), required=False) if copy_v else 0
@@ -187,7 +191,6 @@ class TokenPath:
         self.meta_next = self.meta.clone()
         self.pos0 = pos0.to(device=dev, dtype=torch.int32).contiguous()
         self.num_splits = num_splits
-        self.rope = torch.empty(B, t, hd, **f32)
         self.q = torch.empty(B, t, nh, hd, **f32)
         self.k = torch.empty(B, t, nk, hd, **f32)
         self.out = torch.empty(B, t, nh, hd, **f32)
@@ -210,9 +213,8 @@ class TokenPath:
             for name, x in (("yq", yq), ("yk", yk), ("yv", yv), ("gate", gate)):
                 self.in_bufs[name].copy_(x, non_blocking=True)
             yq, yk, yv, gate = (self.in_bufs[n] for n in ("yq", "yk", "yv", "gate"))
-        rope_table(self.pos0, self.t, self.hd, self.theta, out=self.rope, stream=stream)
         ring = self.t == 1
-        q, k, v = prep(yq, yk, yv, self.rope, self.q_scale, self.eps, pos0=self.pos0,
+        q, k, v = prep(yq, yk, yv, None, self.q_scale, self.eps, pos0=self.pos0, theta=self.theta,
                        ring_k=self.ring_k if ring else None, ring_v=self.ring_v if ring else None,
                        q_out=self.q, k_out=self.k, copy_v=False, stream=stream)
         attend(self.meta, q, k, v, self.ring_k, self.ring_v, self.sink_k, self.sink_v, gate,
@@ -226,3 +228,35 @@ class TokenPath:
             (stream if stream is not None else torch.cuda.current_stream()).synchronize()
             return out_host
         return self.out
+
+    def capture(self):
+        """Record one host-to-host step as a CUDA graph: the copies of the
+        pinned inputs ``h_in`` to the device, prep, attention, merge/gate/
+        commit and the copy of the output into the pinned ``h_out``. Write a
+        step's inputs into ``h_in`` and call ``replay``."""
+        self.h_in = {n: torch.empty(tuple(b.shape), dtype=b.dtype).pin_memory()
+                     for n, b in self.in_bufs.items()}
+        self.h_out = torch.empty(tuple(self.out.shape), dtype=self.out.dtype).pin_memory()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):           # warm-up: attributes, plans, allocations
+            self._graph_body()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self._graph_body()
+        self.graph = g
+        return g
+
+    def _graph_body(self):
+        for name, buf in self.in_bufs.items():
+            buf.copy_(self.h_in[name], non_blocking=True)
+        self.step(self.in_bufs["yq"], self.in_bufs["yk"], self.in_bufs["yv"], self.in_bufs["gate"])
+        self.h_out.copy_(self.out, non_blocking=True)
+
+    def replay(self):
+        """One captured step; returns the pinned host output."""
+        self.graph.replay()
+        torch.cuda.current_stream().synchronize()
+        return self.h_out

@@ -29,6 +29,7 @@ class PrepArgs(ctypes.Structure):
         ("q_scale", c_float_p), ("pos0", c_float_p),
         ("q_out", c_float_p), ("k_out", c_float_p), ("v_out", c_float_p),
         ("ring_k", c_float_p), ("ring_v", c_float_p),
+        ("theta", ctypes.c_double),
     ]
 
 

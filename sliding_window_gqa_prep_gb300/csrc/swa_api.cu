@@ -32,6 +32,10 @@ int num_sms() {
 }
 
 static bool hd_ok(int hd) { return hd == 64 || hd == 128 || hd == 256; }
+
+void fill_inv_freq(double theta, int hd, double* inv_freq) {
+  for (int e = 0; e < 128; ++e) inv_freq[e] = e < hd / 2 ? std::pow(theta, -2.0 * e / hd) : 0.0;
+}
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static int attend_shape_ok(const swa_attend_args* a) {
@@ -41,6 +45,20 @@ static int attend_shape_ok(const swa_attend_args* a) {
   if (a->nh / a->nk > 32) return 0;
   if (a->num_splits < 0) return 0;
   return 1;
+}
+
+// Resident attention CTAs per SM for (hd, nq) on the current device, queried
+// once and cached (the first call per device should precede any stream capture).
+static int cached_occupancy(int hd, int nq) {
+  static int cache[64][3][8] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return attend_partial_occupancy(hd, nq);
+  const int hi = hd == 64 ? 0 : (hd == 128 ? 1 : 2);
+  int qi = 0;
+  while ((4 << qi) < nq && qi < 7) ++qi;
+  int& c = cache[dev][hi][qi];
+  if (c == 0) c = attend_partial_occupancy(hd, nq);
+  return c;
 }
 
 // Cut a call into CTAs. A row block holds `rows` chunk rows so that its
@@ -97,7 +115,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
     // About 8 waves of resident CTAs (a short tail and enough key streams in
     // flight to cover HBM latency), but at least 4 tiles of keys per split.
     const int sms = num_sms();
-    const int occ = attend_partial_occupancy(a->hd, nq);
+    const int occ = cached_occupancy(a->hd, nq);
     const long long slots = (long long)(sms > 0 ? sms : 148) * (occ > 0 ? occ : 1);
     long long want = (8 * slots + units - 1) / units;
     const long long cap_s = (keys_max + 4 * TK - 1) / (4 * TK);
@@ -151,14 +169,17 @@ int swa_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd, doub
   if (B < 1 || t < 1 || !hd_ok(hd) || !(theta > 0.0)) return SWA_E_SHAPE;
   if (!aligned16(rope)) return SWA_E_ALIGN;
   double inv_freq[128];
-  for (int e = 0; e < hd / 2; ++e) inv_freq[e] = std::pow(theta, -2.0 * e / hd);
+  fill_inv_freq(theta, hd, inv_freq);
   return launch_rope_table(rope, pos0, B, t, hd, inv_freq, stream);
 }
 
 int swa_prep(const swa_prep_args* a, cudaStream_t stream) {
   if (!a) return SWA_E_NULL;
-  if (!a->yq || !a->yk || !a->yv || !a->rope || !a->q_scale || !a->q_out || !a->k_out)
-    return SWA_E_NULL;
+  if (!a->yq || !a->yk || !a->yv || !a->q_scale || !a->q_out || !a->k_out) return SWA_E_NULL;
+  if (!a->rope) {
+    if (!a->pos0) return SWA_E_NULL;
+    if (!(a->theta > 0.0)) return SWA_E_SHAPE;
+  }
   if (a->B < 1 || a->t < 1 || a->nh < 1 || a->nk < 1 || !hd_ok(a->hd)) return SWA_E_SHAPE;
   if (!(a->eps >= 0.0f)) return SWA_E_SHAPE;
   const bool ring = a->ring_k || a->ring_v;
@@ -179,6 +200,7 @@ int swa_prep(const swa_prep_args* a, cudaStream_t stream) {
   p.q_out = a->q_out; p.k_out = a->k_out; p.v_out = a->v_out;
   p.ring_k = ring ? a->ring_k : nullptr;
   p.ring_v = ring ? a->ring_v : nullptr;
+  fill_inv_freq(a->rope ? 10000.0 : a->theta, a->hd, p.inv_freq);
   return launch_prep(p, stream);
 }
 

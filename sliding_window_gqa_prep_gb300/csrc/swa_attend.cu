@@ -63,12 +63,14 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
     }
     return;
   }
+  // ---- one warp per output row (b, r, h): lane s of each group of 32 splits
+  // takes that split's (m, l); the weights exp2(m_s - M) are broadcast and each
+  // lane adds its features of every split's numerator (independent loads).
   constexpr int D4 = HD / 4;
-  const size_t total = (size_t)p.B * p.t * p.nh * D4;
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= total) return;
-  const int d4 = (int)(idx % D4);
-  const size_t row = idx / D4;                 // (b * t + r) * nh + h
+  constexpr int PER = (D4 + 31) / 32;          // float4 chunks per lane
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = (size_t)blockIdx.x * (blockDim.x / 32) + warp;   // (b * t + r) * nh + h
+  if (row >= (size_t)p.B * p.t * p.nh) return;
   const int h = (int)(row % p.nh);
   const size_t br = row / p.nh;
   const int r = (int)(br % p.t);
@@ -79,27 +81,55 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
   const size_t item0 = (((size_t)b * p.nk + g) * p.n_rb + rb) * p.splits;
   const int nval = p.ws_nsplit[b * p.n_rb + rb];
   float M = -INFINITY;
-  for (int sidx = 0; sidx < nval; ++sidx) M = fmaxf(M, p.ws_ml[(item0 + sidx) * p.nq + q].x);
+  for (int s0 = 0; s0 < nval; s0 += 32)
+    if (s0 + lane < nval) M = fmaxf(M, p.ws_ml[(item0 + s0 + lane) * p.nq + q].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   float den = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int sidx = 0; sidx < nval; ++sidx) {
-    const float2 ml = p.ws_ml[(item0 + sidx) * p.nq + q];
-    if (ml.x == -INFINITY) continue;           // a split with no key of this row
-    const float w = exp2f(ml.x - M);
-    den += ml.y * w;
-    const float4 a = *reinterpret_cast<const float4*>(
-        p.ws_acc + ((item0 + sidx) * p.nq + q) * (size_t)HD + d4 * 4);
-    acc.x += a.x * w; acc.y += a.y * w; acc.z += a.z * w; acc.w += a.w * w;
+  float4 acc[PER];
+#pragma unroll
+  for (int c = 0; c < PER; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < nval; s0 += 32) {
+    float w = 0.f;
+    if (s0 + lane < nval) {
+      const float2 ml = p.ws_ml[(item0 + s0 + lane) * p.nq + q];
+      if (ml.x != -INFINITY) {                 // a split with no key of this row weighs 0
+        w = exp2f(ml.x - M);
+        den += ml.y * w;
+      }
+    }
+    const int cnt = min(32, nval - s0);
+#pragma unroll 4
+    for (int k = 0; k < cnt; ++k) {
+      const float wk = __shfl_sync(0xffffffffu, w, k);
+      if (wk == 0.f) continue;
+      const float* src = p.ws_acc + ((item0 + s0 + k) * p.nq + q) * (size_t)HD;
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = c * 32 + lane;
+        if (d4 < D4) {
+          const float4 a = *reinterpret_cast<const float4*>(src + d4 * 4);
+          acc[c].x += a.x * wk; acc[c].y += a.y * wk; acc[c].z += a.z * wk; acc[c].w += a.w * wk;
+        }
+      }
+    }
   }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
   const float inv = 1.0f / den;
-  const float4 gt = *reinterpret_cast<const float4*>(p.gate + row * HD + d4 * 4);
-  const float4 gs = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * HD + d4 * 4);
-  float4 o;
-  o.x = acc.x * inv / (1.0f + expf(-(gt.x * gs.x)));
-  o.y = acc.y * inv / (1.0f + expf(-(gt.y * gs.y)));
-  o.z = acc.z * inv / (1.0f + expf(-(gt.z * gs.z)));
-  o.w = acc.w * inv / (1.0f + expf(-(gt.w * gs.w)));
-  *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) = o;
+#pragma unroll
+  for (int c = 0; c < PER; ++c) {
+    const int d4 = c * 32 + lane;
+    if (d4 >= D4) continue;
+    const float4 gt = *reinterpret_cast<const float4*>(p.gate + row * HD + d4 * 4);
+    const float4 gs = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * HD + d4 * 4);
+    float4 o;
+    o.x = acc[c].x * inv / (1.0f + expf(-(gt.x * gs.x)));
+    o.y = acc[c].y * inv / (1.0f + expf(-(gt.y * gs.y)));
+    o.z = acc[c].z * inv / (1.0f + expf(-(gt.z * gs.z)));
+    o.w = acc[c].w * inv / (1.0f + expf(-(gt.w * gs.w)));
+    *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) = o;
+  }
 }
 
 }  // namespace
@@ -119,9 +149,9 @@ int attend_partial_occupancy(int hd, int nq) {
 }
 
 int launch_attend_merge(const AttendParams& p, cudaStream_t s) {
-  const size_t total = (size_t)p.B * p.t * p.nh * (p.hd / 4);
+  const size_t rows = (size_t)p.B * p.t * p.nh;   // one warp per output row
   const int block = 256;
-  const int out_blocks = (int)((total + block - 1) / block);
+  const int out_blocks = (int)((rows + block / 32 - 1) / (block / 32));
   const int grid = out_blocks + (p.commit ? p.B * p.commit_blocks : 0);
   switch (p.hd) {
     case 64: attend_merge_kernel<64><<<grid, block, 0, s>>>(p, out_blocks); break;

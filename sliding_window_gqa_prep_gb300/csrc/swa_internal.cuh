@@ -89,8 +89,10 @@ struct PrepParams {
   float* v_out;
   float* ring_k;
   float* ring_v;
+  double inv_freq[128];       // theta^(-2e/hd), used when rope == nullptr
 };
 int launch_prep(const PrepParams& p, cudaStream_t s);
+void fill_inv_freq(double theta, int hd, double* inv_freq);   // theta^(-2e/hd), e < hd/2
 int launch_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd,
                       const double* inv_freq, cudaStream_t s);
 

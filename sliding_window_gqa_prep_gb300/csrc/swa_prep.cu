@@ -43,11 +43,25 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
   const int row = blockIdx.x;      // b * t + j
   const int a = blockIdx.y * kPrepWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
+  // Without a table, the row's cos/sin are computed once per CTA, with the
+  // same f64 expression as rope_table_kernel (bit-identical f32 values).
+  __shared__ __align__(16) float s_cs[HD];
+  if (p.rope == nullptr) {
+    const int b = row / p.t, j = row % p.t;
+    const double pos = (double)p.pos0[b] + (double)j;
+    for (int e2 = threadIdx.x; e2 < HALF; e2 += blockDim.x) {
+      double sn, cs;
+      sincos(pos * p.inv_freq[e2], &sn, &cs);
+      s_cs[e2] = (float)cs;
+      s_cs[HALF + e2] = (float)sn;
+    }
+    __syncthreads();
+  }
   if (a >= p.nh + p.nk) return;
   const int e = lane * P;
 
   float c[P], s[P];
-  const float* rope = p.rope + (size_t)row * HD;
+  const float* rope = p.rope ? p.rope + (size_t)row * HD : s_cs;
   ldv<P>(rope + e, c);
   ldv<P>(rope + HALF + e, s);
 

@@ -68,6 +68,9 @@ def test_prep_rejects_bad_arguments(lib):
     assert call(_prep(B=0)) == _abi.SWA_E_SHAPE
     assert call(_prep(eps=-1.0)) == _abi.SWA_E_SHAPE
     assert call(_prep(yq=FAKE + 4)) == _abi.SWA_E_ALIGN
+    # no table: the angles need pos0 and a positive theta
+    assert call(_prep(rope=None, theta=1e4)) == _abi.SWA_E_NULL
+    assert call(_prep(rope=None, pos0=FAKE, theta=0.0)) == _abi.SWA_E_SHAPE
     # ring write: both rings and pos0 needed, and only for t == 1
     assert call(_prep(ring_k=FAKE)) == _abi.SWA_E_NULL
     assert call(_prep(ring_k=FAKE, ring_v=FAKE)) == _abi.SWA_E_NULL

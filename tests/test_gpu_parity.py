@@ -70,6 +70,19 @@ def test_prep_matches_oracle_and_writes_ring_slots_exactly(kw):
                 np.testing.assert_array_equal(ring[b, :, s], want)
 
 
+@pytest.mark.parametrize("hd", [64, 128, 256])
+def test_prep_with_in_kernel_angles_equals_table_prep_bit_for_bit(hd):
+    w = workloads.custom(B=3, t=4, nh=8, nk=2, hd=hd, window=64, cap=64, pos_mode="full",
+                         pos_lo=64, pos_hi=131000, seed=19)
+    d = to_dev(workloads.make_inputs(w))
+    rope = swa.rope_table(d["pos0"], w.t, w.hd, w.theta)
+    q1, k1, _ = swa.prep(d["yq"], d["yk"], d["yv"], rope, d["q_scale"], w.eps)
+    q2, k2, _ = swa.prep(d["yq"], d["yk"], d["yv"], None, d["q_scale"], w.eps, pos0=d["pos0"],
+                         theta=w.theta)
+    torch.cuda.synchronize()
+    assert torch.equal(q1, q2) and torch.equal(k1, k2)
+
+
 # ---------------------------------------------------------------------------
 # attend: full path (generator -> rope -> prep -> attend -> commit) vs oracle
 # ---------------------------------------------------------------------------
@@ -282,6 +295,23 @@ def test_token_path_host_step_matches_device_step():
                      inp["gate"].pin_memory(), out_host=torch.empty(w.B, w.t, w.nh, w.hd).pin_memory())
     ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
     assert_close(host.numpy(), ref, "out")
+
+
+def test_token_path_captured_graph_matches_oracle_twice():
+    w = workloads.custom(B=3, t=1, nh=8, nk=2, hd=128, window=96, cap=96, ns=2,
+                         pos_mode="full", pos_lo=96, pos_hi=5000, seed=23)
+    inp = workloads.make_inputs(w)
+    tp = swa.TokenPath(B=w.B, t=w.t, nh=w.nh, nk=w.nk, hd=w.hd, cap=w.cap, ns=w.ns,
+                       q_scale=inp["q_scale"], gate_scale=inp["gate_scale"],
+                       ring_k=inp["ring_k"], ring_v=inp["ring_v"], sink_k=inp["sink_k"],
+                       sink_v=inp["sink_v"], meta=inp["meta"], pos0=inp["pos0"])
+    tp.capture()
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    for _ in range(2):
+        for k in ("yq", "yk", "yv", "gate"):
+            tp.h_in[k].copy_(inp[k])
+        out = tp.replay()
+        assert_close(out.numpy(), ref, "graph replay out")
 
 
 # ---------------------------------------------------------------------------
