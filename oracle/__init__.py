@@ -7,5 +7,5 @@ from .swa_oracle import (  # noqa: F401
     WIN_LEN, WIN_HEAD, FAR_LEN, WINDOW,
     ring_modulus, rope_table, rotate_head, unit_head, prep, prep_ring_slot,
     prep_ring_write, row_window, row_key_list, sigmoid_gate, attend_row, attend,
-    commit_slot, commit_meta, commit,
+    commit_slot, commit_meta, commit, rollback_meta, rollback,
 )

@@ -275,3 +275,43 @@ def commit(meta, ring_k, ring_v, k_chunk, v_chunk):
                 rv[b, g, slot] = v_chunk[b, j, g]
         new_meta[b] = commit_meta(meta[b], t, cap)
     return rk, rv, new_meta
+
+
+# ---------------------------------------------------------------------------
+# Speculative rollback (dory_msl.metal, dory_o1_back)
+# ---------------------------------------------------------------------------
+def rollback_meta(meta_b, n, cap):
+    """Meta after rejecting the last ``n`` pushed tokens, one token at a time
+    as dory_o1_back does: while the window is full (win_len equals the ring
+    modulus) the head steps back one slot (mod W) and far_len drops by one in
+    32-bit unsigned arithmetic; otherwise win_len drops by one. A full window
+    therefore stays full. Returns None when a non-full window would have to
+    drop below zero keys (an invalid request)."""
+    W = ring_modulus(meta_b, cap)
+    length = int(meta_b[WIN_LEN])
+    head = int(meta_b[WIN_HEAD])
+    far = int(meta_b[FAR_LEN])
+    for _ in range(int(n)):
+        if length == W:
+            head = (head + W - 1) % W
+            far = (far - 1) % (1 << 32)
+        else:
+            if length == 0:
+                return None
+            length -= 1
+    return np.array([length, head, far, int(meta_b[WINDOW])], dtype=np.int64)
+
+
+def rollback(meta, n_back, cap):
+    """rollback_meta over a batch; a sequence whose request is invalid keeps
+    its meta and is flagged. Returns (new_meta, bad[B])."""
+    meta = np.asarray(meta, dtype=np.int64)
+    out = meta.copy()
+    bad = np.zeros(meta.shape[0], dtype=bool)
+    for b in range(meta.shape[0]):
+        r = rollback_meta(meta[b], n_back[b], cap)
+        if r is None:
+            bad[b] = True
+        else:
+            out[b] = r
+    return out, bad

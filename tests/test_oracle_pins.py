@@ -358,3 +358,49 @@ def test_commit_after_prep_grown_ring_matches_prep_slots():
             for j in (0, w.t - 1):
                 assert oracle.commit_slot(meta[b].numpy(), j, w.cap) == \
                     oracle.prep_ring_slot(int(pos0[b]), j, w.cap)
+
+
+# ---------------------------------------------------------------------------
+# speculative rollback (dory_msl.metal, dory_o1_back)
+# ---------------------------------------------------------------------------
+ROLLBACK_GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "rollback_cases.json")
+with open(ROLLBACK_GOLDEN) as _f:
+    ROLLBACK_CASES = json.load(_f)["cases"]
+
+
+@pytest.mark.parametrize("case", ROLLBACK_CASES, ids=[c["name"] for c in ROLLBACK_CASES])
+def test_rollback_matches_hand_derivation(case):
+    got = oracle.rollback_meta(np.array(case["meta"]), case["n"], case["cap"])
+    if case["after"] is None:
+        assert got is None
+    else:
+        assert got is not None and got.tolist() == case["after"]
+
+
+@pytest.mark.parametrize("len0,t,W", [(0, 5, 16), (3, 12, 16), (16, 5, 16), (16, 40, 16), (6, 1, 8)])
+def test_rollback_undoes_a_commit_that_never_changes_fullness(len0, t, W):
+    # a window that stays below W, or is full throughout, returns exactly to
+    # the meta before the commit (o1c_meta forward, dory_o1_back backward)
+    meta = np.array([len0, 5 % W, 11, W])
+    fwd = oracle.commit_meta(meta, t, W)
+    back = oracle.rollback_meta(fwd, t, W)
+    assert back.tolist() == meta.tolist()
+
+
+def test_rollback_after_a_commit_that_fills_the_window_stays_full():
+    # len0 + t crosses W: the forward commit evicts ev keys; rewinding t tokens
+    # keeps the window full and moves the head back t slots from where the
+    # commit left it, so it ends t - ev slots before the original head
+    W, len0, t, head0 = 16, 12, 7, 3
+    fwd = oracle.commit_meta(np.array([len0, head0, 0, W]), t, W)
+    ev = len0 + t - W
+    assert fwd.tolist() == [W, (head0 + ev) % W, ev, W]
+    back = oracle.rollback_meta(fwd, t, W)
+    assert back.tolist() == [W, (head0 + ev - t) % W, (ev - t) % (1 << 32), W]
+
+
+def test_rollback_batch_flags_only_invalid_sequences():
+    meta = np.array([[5, 0, 0, 8], [8, 3, 2, 8], [2, 1, 0, 8]])
+    out, bad = oracle.rollback(meta, [2, 1, 3], 8)
+    assert bad.tolist() == [False, False, True]
+    assert out.tolist() == [[3, 0, 0, 8], [8, 2, 1, 8], [2, 1, 0, 8]]
