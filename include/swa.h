@@ -199,6 +199,30 @@ size_t swa_attend_workspace_size(const swa_attend_args* args);
 
 int swa_attend(const swa_attend_args* args, cudaStream_t stream);
 
+/* Speculative rollback of the ring meta ("dory_msl.metal", cortiq-engine
+ * 0.8.57, kernel dory_o1_back). After a verify step committed t draft rows
+ * (swa_attend with commit = 1) and only the first a were accepted, pass
+ * n_back[b] = t - a to rewind sequence b's meta by that many tokens, one
+ * token at a time as the page does:
+ *   - window full (win_len == W, W = window or cap when window is 0): the
+ *     length stays W, win_head steps back one slot mod W and far_len drops
+ *     by one (modulo 2^32). A full window stays full, and its oldest slots
+ *     keep the rejected rows' keys: the keys those rows evicted are gone.
+ *   - otherwise: win_len drops by one. Exact: the rejected rows' slots fall
+ *     outside the window again.
+ * The ring contents are not touched.
+ *   meta    [B] device, updated in place (state after the verify's commit)
+ *   n_back  [B] int32 device, >= 0
+ *   cap     ring capacity the meta refers to
+ *   err     optional device error word: SWA_DERR_META when a meta is out of
+ *           range, n_back is negative, or a window that is not full would
+ *           drop below zero keys; that sequence's meta is left unchanged.
+ * Errors: SWA_E_NULL (meta or n_back NULL), SWA_E_SHAPE (B < 1 or cap < 1),
+ * SWA_E_ALIGN (meta not 16-byte aligned), SWA_E_CUDA. One launch, no
+ * synchronisation. */
+int swa_rollback(swa_meta* meta, const int32_t* n_back, int B, int cap, uint32_t* err,
+                 cudaStream_t stream);
+
 /*
  * swa_attend_noalloc — swa_attend for callers that cannot allocate device
  * memory. The pages have no counterpart: it is a deployment convenience of

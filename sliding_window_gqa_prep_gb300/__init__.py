@@ -25,7 +25,7 @@ import torch
 from . import _abi
 from ._abi import SwaError, SWA_DERR_META, SWA_DERR_TIMEOUT  # noqa: F401
 
-__all__ = ["rope_table", "prep", "attend", "attend_workspace_size", "launch_count",
+__all__ = ["rope_table", "prep", "attend", "attend_workspace_size", "rollback", "launch_count",
            "TokenPath", "SwaError", "library"]
 
 
@@ -161,6 +161,18 @@ def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate
     rc = library().swa_attend(ctypes.byref(a), _stream(stream))
     _abi.check(rc, "swa_attend")
     return out
+
+
+def rollback(meta: torch.Tensor, n_back: torch.Tensor, cap: int, err=None, stream=None):
+    """Rewind each sequence's meta (in place) by n_back[b] rejected draft
+    tokens, one token at a time as dory_o1_back does. Returns meta."""
+    B = meta.shape[0]
+    rc = library().swa_rollback(_ptr(meta, "meta", (B, 4), torch.int32),
+                                _ptr(n_back, "n_back", (B,), torch.int32), B, int(cap),
+                                _ptr(err, "err", (1,), torch.int32, required=False),
+                                _stream(stream))
+    _abi.check(rc, "swa_rollback")
+    return meta
 
 
 class TokenPath:

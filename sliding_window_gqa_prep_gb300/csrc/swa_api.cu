@@ -173,6 +173,14 @@ int swa_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd, doub
   return launch_rope_table(rope, pos0, B, t, hd, inv_freq, stream);
 }
 
+int swa_rollback(swa_meta* meta, const int32_t* n_back, int B, int cap, uint32_t* err,
+                 cudaStream_t stream) {
+  if (!meta || !n_back) return SWA_E_NULL;
+  if (B < 1 || cap < 1) return SWA_E_SHAPE;
+  if (!aligned16(meta)) return SWA_E_ALIGN;
+  return launch_rollback(meta, n_back, B, cap, err, stream);
+}
+
 int swa_prep(const swa_prep_args* a, cudaStream_t stream) {
   if (!a) return SWA_E_NULL;
   if (!a->yq || !a->yk || !a->yv || !a->q_scale || !a->q_out || !a->k_out) return SWA_E_NULL;

@@ -63,6 +63,8 @@ struct AttendParams {
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int launch_attend_merge(const AttendParams& p, cudaStream_t s);
+int launch_rollback(swa_meta* meta, const int32_t* n_back, int B, int cap, uint32_t* err,
+                    cudaStream_t s);
 int attend_partial_occupancy(int hd, int nq);   // resident CTAs per SM
 // decode kernel (nq <= 8 query vectors per CTA), swa_decode.cu
 int launch_attend_decode(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);

@@ -120,3 +120,11 @@ def test_rope_table_rejects_bad_arguments(lib):
     assert lib.swa_rope_table(FAKE, FAKE, 1, 1, 48, 1e4, None) == _abi.SWA_E_SHAPE
     assert lib.swa_rope_table(FAKE, FAKE, 1, 1, 64, -1.0, None) == _abi.SWA_E_SHAPE
     assert lib.swa_rope_table(FAKE + 4, FAKE, 1, 1, 64, 1e4, None) == _abi.SWA_E_ALIGN
+
+
+def test_rollback_rejects_bad_arguments(lib):
+    assert lib.swa_rollback(None, FAKE, 1, 8, None, None) == _abi.SWA_E_NULL
+    assert lib.swa_rollback(FAKE, None, 1, 8, None, None) == _abi.SWA_E_NULL
+    assert lib.swa_rollback(FAKE, FAKE, 0, 8, None, None) == _abi.SWA_E_SHAPE
+    assert lib.swa_rollback(FAKE, FAKE, 1, 0, None, None) == _abi.SWA_E_SHAPE
+    assert lib.swa_rollback(FAKE + 4, FAKE, 1, 8, None, None) == _abi.SWA_E_ALIGN

@@ -314,6 +314,59 @@ def test_token_path_captured_graph_matches_oracle_twice():
         assert_close(out.numpy(), ref, "graph replay out")
 
 
+def test_rollback_matches_oracle_bit_for_bit():
+    g = torch.Generator().manual_seed(31)
+    B, cap = 300, 64
+    W = torch.randint(1, cap + 1, (B,), generator=g)
+    W[::7] = 0                                            # window 0 means cap
+    Wm = torch.where(W == 0, torch.full_like(W, cap), W)
+    full = torch.rand(B, generator=g) < 0.5
+    length = torch.where(full, Wm, (torch.rand(B, generator=g) * Wm.double()).long())
+    head = (torch.rand(B, generator=g) * Wm.double()).long()
+    far = torch.randint(0, 50, (B,), generator=g)
+    meta = torch.stack([length, head, far, W], 1).to(torch.int32)
+    n_back = torch.randint(0, 3 * cap, (B,), generator=g).to(torch.int32)
+    n_back[:20] = length[:20].to(torch.int32)             # exactly to empty (or full: any)
+    ref, bad = oracle.rollback(meta.numpy().astype(np.int64) % (1 << 32), n_back.numpy(), cap)
+    d_meta, err = meta.cuda(), torch.zeros(1, dtype=torch.int32, device="cuda")
+    swa.rollback(d_meta, n_back.cuda(), cap, err=err)
+    got = d_meta.cpu().numpy().astype(np.int64) % (1 << 32)
+    assert (got == ref % (1 << 32)).all()
+    assert bad.any() and (int(err.item()) & 1) == 1
+
+
+def test_rollback_after_verify_commit_equals_committing_the_accepted_prefix():
+    # a window that does not fill: verify t rows with commit, reject t - a,
+    # then the meta and the logical window's ring rows equal those of a
+    # commit of only the first a rows
+    w = workloads.custom(B=4, t=6, nh=8, nk=2, hd=64, window=64, cap=64, ns=0,
+                         pos_mode="partial", pos_lo=1, pos_hi=40, seed=37)
+    inp = workloads.make_inputs(w)
+    acc = torch.tensor([0, 2, 5, 6], dtype=torch.int32)
+    d = to_dev(inp)
+    meta_out = torch.empty_like(d["meta"])
+    q, k, v = swa.prep(d["yq"], d["yk"], d["yv"], None, d["q_scale"], w.eps, pos0=d["pos0"])
+    swa.attend(d["meta"], q, k, v, d["ring_k"], d["ring_v"], None, None, d["gate"],
+               d["gate_scale"], w.score_scale, commit=True, meta_out=meta_out)
+    swa.rollback(meta_out, (w.t - acc).cuda(), w.cap)
+    got_meta = meta_out.cpu().numpy()
+    rk = d["ring_k"].cpu().numpy()
+    for b in range(w.B):
+        a = int(acc[b])
+        len0, head0 = int(inp["meta"][b][0]), int(inp["meta"][b][1])
+        W = int(inp["meta"][b][3]) or w.cap
+        ref_meta = oracle.commit_meta(inp["meta"][b].numpy(), a, w.cap)
+        assert got_meta[b].tolist() == ref_meta.tolist()
+        written = {(head0 + len0 + j) % W for j in range(w.t)}
+        L, H = int(ref_meta[0]), int(ref_meta[1])
+        for x in range(L):
+            slot = (H + x) % W
+            if x < len0 and slot not in written:          # untouched key of the old window
+                np.testing.assert_array_equal(rk[b, :, slot], inp["ring_k"][b, :, slot].numpy())
+            elif len0 + w.t <= W and x >= len0:           # an accepted row (window never filled)
+                np.testing.assert_array_equal(rk[b, :, slot], k[b, x - len0].cpu().numpy())
+
+
 # ---------------------------------------------------------------------------
 # the five named workloads at full size, in the launch configuration the bench
 # times (automatic splits): every prep output, sampled attention outputs
