@@ -3,27 +3,41 @@
 // "o1c_msl.metal" (cortiq-engine 0.8.79) for several rows at once, as one
 // warp-specialised split-KV kernel writing the shared partial-record format.
 //
-// With 32 query vectors per key the path does 16 flops per K/V byte, so FP32
-// FMA throughput, not HBM, bounds it. The layout is chosen to keep the FMA
-// pipe fed:
-//  - a producer warp streams 32-key tiles into shared memory (one
-//    cp.async.bulk per K row into rows padded to hd + 4 floats, and per V row)
-//    through full/empty mbarriers;
-//  - consumer warp w owns query vectors [w * nq/4, (w + 1) * nq/4) and runs
-//    their complete softmax rows over every key, so warps never combine
-//    states and no CTA barrier runs in the key loop;
-//  - scores: lane = key; each lane reads its K row (the padding puts the 8
-//    lanes of a shared-memory phase on distinct banks) and the query rows by
-//    broadcast, accumulating with packed fma.rn.f32x2 over feature pairs;
-//  - P V: lane = a slice of hd/32 features; P goes through a per-warp shared
-//    slice stored as (p, p) pairs so the packed FMA needs no shuffles.
+// With 32 query vectors per key the path does 16 flops per K/V byte, so the
+// FP32 FMA pipe, not HBM, bounds it, and the design is about feeding that
+// pipe: every FMA is a packed fma.rn.f32x2 and shared-memory wavefronts stay
+// near half the FMA cycles in both products.
+//  - 32-key tiles stream through STAGES shared-memory stages. Keys whose
+//    sources are contiguous (a run of ring slots up to the wrap, the sinks,
+//    the chunk rows) travel as ONE cp.async.bulk per run for K and one for V
+//    into consecutive unpadded rows (4-16 KB copies run at the HBM read rate;
+//    one 512-byte copy per row would cap the stream far below it). Warp 0
+//    issues them: the first STAGES tiles up front, then each stage again as
+//    soon as all four warps have released it. There is no separate producer
+//    warp, so two CTAs put exactly two warps on each SM sub-partition and
+//    every thread may hold the 128 accumulator registers the tiles need.
+//  - Consumer warp w owns a group of QW query vectors and a range of KW keys of
+//    every tile, with its own online softmax state for them; warps that share
+//    query vectors combine their states once, after the key loop, so no CTA
+//    barrier runs inside it.
+//  - Scores: lane (kq, e) = (lane / 8, lane % 8) takes keys kq + 4j of the
+//    warp's range and the float4 feature chunks e, e + 8, ...: each 8-lane
+//    shared-memory phase reads one contiguous 128-byte piece of a K row. The
+//    query vectors sit transposed ([feature][query], chunk-rotated by feature
+//    so the 8 chunk lanes hit distinct banks) and are read as pairs of query
+//    vectors, so one packed FMA updates the scores of two query vectors.
+//    Transposed shuffles over the 8 chunk lanes leave each lane the full
+//    scores of QW / 8 query vectors for its keys.
+//  - P V: lane = (query group of 8, feature group); P is handed over through a
+//    per-warp shared slice as (p, p) pairs, and each lane accumulates an
+//    8 x FPL tile of the numerator in registers.
 #include "swa_internal.cuh"
 
 namespace swa {
 namespace {
 
-constexpr int kVCW = 4;                        // consumer warps
-constexpr int kVThreads = (kVCW + 1) * 32;     // + one producer warp
+constexpr int kVCW = 4;                        // warps (all consume; warp 0 also issues copies)
+constexpr int kVThreads = kVCW * 32;
 constexpr unsigned kVFull = 0xffffffffu;
 
 typedef unsigned long long u64;
@@ -43,31 +57,48 @@ __device__ __forceinline__ float2 unpack2(u64 v) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
   return r;
 }
+__device__ __forceinline__ float comp(const float4& v, int i) {
+  return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
 
 template <int HD, int NQ>
 struct VCfg {
-  static constexpr int KP = HD + 4;            // padded K row (floats)
-  static constexpr int QW = NQ / kVCW;         // query vectors per consumer warp
-  static constexpr int D4 = HD / 4;
-  static constexpr int DPL = HD / 32;          // features per lane in P V (2, 4 or 8)
-  static constexpr int STAGES = 2;
-  static constexpr int OFF_K = 0;                              // [STAGES][TK][KP]
-  static constexpr int OFF_V = STAGES * TK * KP;               // [STAGES][TK][HD]
-  static constexpr int OFF_Q = OFF_V + STAGES * TK * HD;       // [NQ][HD]
-  static constexpr int OFF_P = OFF_Q + NQ * HD;                // [kVCW][TK][QW] x (p, p)
-  static constexpr int OFF_FLAG = OFF_P + kVCW * TK * QW * 2;
+  static constexpr int QW = HD == 256 ? 8 : 16;   // query vectors per consumer warp
+  static constexpr int QG = NQ / QW;              // query groups
+  static constexpr int KG = kVCW / QG;            // key groups (warps per query group)
+  static constexpr int KW = TK / KG;              // keys per warp per tile
+  static constexpr int KPL = KW / 4;              // keys per lane in the scores
+  static constexpr int CH = HD / 32;              // float4 chunks per lane in the scores
+  static constexpr int QO = QW / 8;               // query vectors a lane owns after the reduction
+  static constexpr int FG = QW == 16 ? 16 : 32;   // feature lanes in P V
+  static constexpr int QGL = 32 / FG;             // query lanes in P V
+  static constexpr int QPL = QW / QGL;            // query vectors per lane in P V
+  static constexpr int FPL = HD / FG;             // features per lane in P V
+  static constexpr int FCH = FPL / 4;
+  static constexpr int STAGES = HD == 64 ? 4 : 2;
+  static constexpr int OFF_K = 0;                             // [STAGES][TK][HD]
+  static constexpr int OFF_V = STAGES * TK * HD;              // [STAGES][TK][HD]
+  static constexpr int OFF_QT = 2 * STAGES * TK * HD;         // [HD][32] rotated chunks
+  static constexpr int OFF_P = OFF_QT + HD * 32;              // [kVCW][KW][QW] (p, p)
+  static constexpr int OFF_C = OFF_P + kVCW * KW * QW * 2;    // [kVCW][QW] (c, c)
+  static constexpr int OFF_ML = OFF_C + kVCW * QW * 2;        // [kVCW][QW] (m, l)
+  static constexpr int OFF_FLAG = OFF_ML + kVCW * QW * 2;
   static constexpr int FLOATS = ((OFF_FLAG + 4 + 1) / 2) * 2;
   static constexpr size_t BYTES = (size_t)FLOATS * 4 + 2 * STAGES * sizeof(uint64_t);
-  static_assert(QW == 4 || QW == 8, "4 or 8 query vectors per warp");
+  static constexpr int MIN_BLOCKS = HD == 256 ? 1 : 2;
+  static_assert(NQ == 16 || NQ == 32, "16 or 32 query vectors");
+  static_assert(QG * KG == kVCW && KPL >= 1 && QPL == 8 && FCH >= 1, "warp arrangement");
+  static_assert(kVCW * QW * HD <= 2 * STAGES * TK * HD, "warp states fit the stage buffers");
 };
 
 template <int HD, int NQ>
-__global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p) {
+__global__ void __launch_bounds__(kVThreads, VCfg<HD, NQ>::MIN_BLOCKS)
+attend_verify_kernel(AttendParams p) {
   using C = VCfg<HD, NQ>;
   extern __shared__ __align__(128) float smem[];
   float* Ks = smem + C::OFF_K;
   float* Vs = smem + C::OFF_V;
-  float* Qs = smem + C::OFF_Q;
+  float* QT = smem + C::OFF_QT;
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + C::OFF_FLAG);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::FLOATS);
   uint64_t* empty = full + C::STAGES;
@@ -82,7 +113,7 @@ __global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p
   const int r_last = min(r0 + p.rows, p.t) - 1;
   const int rows_eff = r_last - r0 + 1;
   const int win0 = min(st.W, st.len0 + r0 + 1);
-  const int xlo = st.len0 + r0 + 1 - win0;
+  const int xlo = st.len0 + r0 + 1 - win0;       // first logical key of the block
   const int n = p.ns + (st.len0 + r_last - xlo + 1);
   if (g == 0 && s == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = (n + p.chunk - 1) / p.chunk;
   if (g == 0 && s == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
@@ -99,100 +130,120 @@ __global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p
     mbar_fence_init();
     *s_abort = 0;
   }
-  for (int idx = tid; idx < NQ * C::D4; idx += kVThreads) {
-    const int q = idx / C::D4, d4 = idx % C::D4;
+  // Query vectors of the block (rows then heads) times scale * log2 e, stored
+  // transposed: feature f holds the 32 query slots as 8 float4 chunks, chunk
+  // c at position c ^ ((f / 4) mod 8).
+  for (int idx = tid; idx < 32 * (HD / 4); idx += kVThreads) {
+    const int q = idx % 32, d4 = idx / 32;        // a warp covers the 32 query slots of a chunk
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     const int rr = q / p.hpg, h = q % p.hpg;
-    if (rr < rows_eff && q < p.rows * p.hpg) {
+    if (q < NQ && rr < rows_eff && q < p.rows * p.hpg) {
       v = *reinterpret_cast<const float4*>(
           p.q + (((size_t)b * p.t + r0 + rr) * p.nh + (size_t)g * p.hpg + h) * HD + d4 * 4);
       v.x *= p.qmul; v.y *= p.qmul; v.z *= p.qmul; v.w *= p.qmul;
     }
-    *reinterpret_cast<float4*>(Qs + q * HD + d4 * 4) = v;
+    const int pos = (((q >> 2) ^ d4) & 7) * 4 + (q & 3);
+    QT[(d4 * 4 + 0) * 32 + pos] = v.x;
+    QT[(d4 * 4 + 1) * 32 + pos] = v.y;
+    QT[(d4 * 4 + 2) * 32 + pos] = v.z;
+    QT[(d4 * 4 + 3) * 32 + pos] = v.w;
   }
   __syncthreads();
   const size_t kv_head = (size_t)b * p.nk + g;
 
-  // ------------------------------------------------------------------ producer
-  if (warp == kVCW) {
-    int last = -1;
-    for (int i = 0; i < ntiles; ++i) {
-      const int stage = i % C::STAGES;
-      const int use = i / C::STAGES;
-      bool ok = use == 0 || mbar_wait_bounded(&empty[stage], (uint32_t)((use - 1) & 1), kWaitLimitNs);
-      ok = __all_sync(kVFull, ok);
-      if (!ok) {
-        if (lane == 0) {
-          *s_abort = 1;
-          set_err(p.err, SWA_DERR_TIMEOUT);
-        }
-        break;
-      }
-      if (__shfl_sync(kVFull, *s_abort, 0)) break;
-      fence_proxy_async_smem();
-      const int j0 = jb + i * TK;
-      const int cnt = min(TK, je - j0);
-      if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(cnt * HD * 4 * 2));
-      __syncwarp();
-      if (lane < cnt) {
-        const int j = j0 + lane;
-        const float* sk;
-        const float* sv;
-        if (j < p.ns) {
-          const size_t at = (kv_head * p.ns + j) * HD;
-          sk = p.sink_k + at;
-          sv = p.sink_v + at;
+  // ------------------------------------------------------------ copy issue
+  // Warp 0 copies tile `it` into its stage: the source row of key `lane`; a
+  // lane whose row does not follow its left neighbour's starts a run and
+  // issues one copy of the whole run.
+  auto issue_tile = [&](int it) {
+    const int stage = it % C::STAGES;
+    const int j0 = jb + it * TK;
+    const int cnt = min(TK, je - j0);
+    if (lane == 0) mbar_arrive_expect_tx(&full[stage], (uint32_t)(cnt * HD * 4 * 2));
+    __syncwarp();
+    const float* sk = nullptr;
+    const float* sv = nullptr;
+    if (lane < cnt) {
+      const int j = j0 + lane;
+      if (j < p.ns) {
+        const size_t at = (kv_head * p.ns + j) * HD;
+        sk = p.sink_k + at;
+        sv = p.sink_v + at;
+      } else {
+        const int x = xlo + (j - p.ns);
+        if (x < st.len0) {
+          int slot = st.head0 + x;
+          if (slot >= st.W) slot -= st.W;        // head0 < W and x < W
+          const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
+          sk = p.ring_k + at;
+          sv = p.ring_v + at;
         } else {
-          const int x = xlo + (j - p.ns);
-          if (x < st.len0) {
-            int slot = st.head0 + x;
-            if (slot >= st.W) slot -= st.W;
-            const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
-            sk = p.ring_k + at;
-            sv = p.ring_v + at;
-          } else {
-            const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
-            sk = p.k_chunk + at;
-            sv = p.v_chunk + at;
-          }
+          const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
+          sk = p.k_chunk + at;
+          sv = p.v_chunk + at;
         }
-        bulk_g2s(Ks + ((size_t)stage * TK + lane) * C::KP, sk, HD * 4, &full[stage]);
-        bulk_g2s(Vs + ((size_t)stage * TK + lane) * HD, sv, HD * 4, &full[stage]);
       }
-      last = i;
     }
-    for (int st_i = 0; st_i < C::STAGES && st_i <= last; ++st_i) {
-      const int lt = last - ((last - st_i) % C::STAGES);
-      mbar_wait_bounded(&full[st_i], (uint32_t)((lt / C::STAGES) & 1), kWaitLimitNs);
+    const u64 prev_k = __shfl_up_sync(kVFull, reinterpret_cast<u64>(sk), 1);
+    const u64 prev_v = __shfl_up_sync(kVFull, reinterpret_cast<u64>(sv), 1);
+    const bool start = lane < cnt &&
+                       (lane == 0 || reinterpret_cast<u64>(sk) != prev_k + HD * 4 ||
+                        reinterpret_cast<u64>(sv) != prev_v + HD * 4);
+    const unsigned starts = __ballot_sync(kVFull, start);
+    if (start) {
+      const unsigned later = starts & ~((2u << lane) - 1u);
+      const int end = later ? __ffs(later) - 1 : cnt;
+      const uint32_t bytes = (uint32_t)((end - lane) * HD * 4);
+      bulk_g2s(Ks + ((size_t)stage * TK + lane) * HD, sk, bytes, &full[stage]);
+      bulk_g2s(Vs + ((size_t)stage * TK + lane) * HD, sv, bytes, &full[stage]);
     }
-    return;
+  };
+  int issued = 0;                                 // tiles warp 0 has issued
+  if (warp == 0) {
+    for (; issued < C::STAGES && issued < ntiles; ++issued) issue_tile(issued);
   }
 
   // ------------------------------------------------------------------ consumers
-  const int q0 = warp * C::QW;                     // this warp's first query vector
-  int q_lo[C::QW], q_hi[C::QW];
-  bool q_ok[C::QW];
+  const int e = lane & 7, kq = lane >> 3;
+  const int qgrp = warp % C::QG, kgrp = warp / C::QG;
+  const int kbase = kgrp * C::KW;                 // the warp's first key of every tile
+  // query vectors this lane owns after the score reduction: qgrp*QW + e*QO + o
+  int q_lo[C::QO], q_hi[C::QO];
+  bool q_ok[C::QO];
 #pragma unroll
-  for (int k = 0; k < C::QW; ++k) {
-    const int q = q0 + k;
+  for (int o = 0; o < C::QO; ++o) {
+    const int q = qgrp * C::QW + e * C::QO + o;
     const int rr = q / p.hpg;
     const int r = r0 + rr;
-    q_ok[k] = rr < rows_eff && q < p.rows * p.hpg;
-    q_lo[k] = st.len0 + r + 1 - min(st.W, st.len0 + r + 1);
-    q_hi[k] = st.len0 + r;
+    q_ok[o] = rr < rows_eff && q < p.rows * p.hpg;
+    q_lo[o] = st.len0 + r + 1 - min(st.W, st.len0 + r + 1);
+    q_hi[o] = st.len0 + r;
   }
-  float m[C::QW], l[C::QW];
-  u64 acc[C::QW][C::DPL / 2];
+  float m[C::QO], l[C::QO];
 #pragma unroll
-  for (int k = 0; k < C::QW; ++k) {
-    m[k] = -INFINITY;
-    l[k] = 0.f;
-#pragma unroll
-    for (int d = 0; d < C::DPL / 2; ++d) acc[k][d] = 0ull;
+  for (int o = 0; o < C::QO; ++o) {
+    m[o] = -INFINITY;
+    l[o] = 0.f;
   }
-  u64* Pw = reinterpret_cast<u64*>(smem + C::OFF_P) + warp * TK * C::QW;
-  const u64 zero2 = 0ull;
+  // P V lane arrangement
+  const int fg = lane % C::FG, qgl = lane / C::FG;
+  u64 acc[C::QPL][C::FPL / 2];
+#pragma unroll
+  for (int k = 0; k < C::QPL; ++k)
+#pragma unroll
+    for (int d = 0; d < C::FPL / 2; ++d) acc[k][d] = 0ull;
 
+  u64* Pw = reinterpret_cast<u64*>(smem + C::OFF_P) + warp * C::KW * C::QW;
+  u64* Cw = reinterpret_cast<u64*>(smem + C::OFF_C) + warp * C::QW;
+  const u64 one2 = pack2(1.f, 1.f);
+  const u64 zero2 = 0ull;
+  const bool b1 = (e & 2) != 0, b0 = (e & 1) != 0;
+  // Visit order of the warp's query chunks: after the chunk-level reduction
+  // rounds (lane bits 2 and 1 when QW = 16, bit 2 when QW = 8) a lane keeps
+  // the chunk whose index bits equal those lane bits.
+  const int uperm = C::QW == 16 ? (e >> 1) : (e >> 2);
+
+  int consumed = 0;                               // tiles whose copies have landed
   for (int i = 0; i < ntiles; ++i) {
     const int stage = i % C::STAGES;
     const bool ok = __all_sync(kVFull, mbar_wait_bounded(&full[stage], (uint32_t)((i / C::STAGES) & 1),
@@ -204,103 +255,275 @@ __global__ void __launch_bounds__(kVThreads) attend_verify_kernel(AttendParams p
       }
       break;
     }
+    consumed = i + 1;
     if (__shfl_sync(kVFull, *s_abort, 0)) break;
     const int j0 = jb + i * TK;
     const int cnt = min(TK, je - j0);
+    const float* Kt = Ks + (size_t)stage * TK * HD;
+    const float* Vt = Vs + (size_t)stage * TK * HD;
 
-    // ---- scores of key `lane` against the warp's query vectors
-    // two independent accumulator chains per query vector (features 4i..4i+1
-    // and 4i+2..4i+3) keep consecutive packed FMAs from waiting on each other
-    u64 sacc[C::QW], sacc2[C::QW];
+    // ---- partial scores: keys kbase + kq + 4j, query pairs of the warp's group
+    u64 sp[C::KPL][C::QW / 2];
 #pragma unroll
-    for (int k = 0; k < C::QW; ++k) sacc[k] = sacc2[k] = 0ull;
-    const float* krow = Ks + ((size_t)stage * TK + lane) * C::KP;
-    const float* qrow = Qs + (size_t)q0 * HD;
-#pragma unroll 8
-    for (int d4 = 0; d4 < C::D4; ++d4) {
-      const ulonglong2 kv = *reinterpret_cast<const ulonglong2*>(krow + d4 * 4);
+    for (int j = 0; j < C::KPL; ++j)
 #pragma unroll
-      for (int k = 0; k < C::QW; ++k) {
-        const ulonglong2 qv = *reinterpret_cast<const ulonglong2*>(qrow + k * HD + d4 * 4);
-        sacc[k] = ffma2(qv.x, kv.x, sacc[k]);
-        sacc2[k] = ffma2(qv.y, kv.y, sacc2[k]);
+      for (int u = 0; u < C::QW / 2; ++u) sp[j][u] = 0ull;
+#pragma unroll
+    for (int c = 0; c < C::CH; ++c) {
+      const int ch = e + 8 * c;
+      float4 kv[C::KPL];
+#pragma unroll
+      for (int j = 0; j < C::KPL; ++j)
+        kv[j] = *reinterpret_cast<const float4*>(Kt + (size_t)(kbase + kq + 4 * j) * HD + ch * 4);
+#pragma unroll
+      for (int f = 0; f < 4; ++f) {
+        const float* qrow = QT + (ch * 4 + f) * 32;
+        u64 kd[C::KPL];
+#pragma unroll
+        for (int j = 0; j < C::KPL; ++j) {
+          const float kf = comp(kv[j], f);
+          kd[j] = pack2(kf, kf);
+        }
+#pragma unroll
+        for (int u = 0; u < C::QW / 4; ++u) {
+          const int lc = qgrp * (C::QW / 4) + (u ^ uperm);
+          const ulonglong2 qv = *reinterpret_cast<const ulonglong2*>(qrow + ((lc ^ e) & 7) * 4);
+#pragma unroll
+          for (int j = 0; j < C::KPL; ++j) {
+            sp[j][2 * u] = ffma2(qv.x, kd[j], sp[j][2 * u]);
+            sp[j][2 * u + 1] = ffma2(qv.y, kd[j], sp[j][2 * u + 1]);
+          }
+        }
       }
     }
-    const int j = j0 + lane;
-    const bool key_in = lane < cnt;
-    const int x = xlo + (j - p.ns);
-    u64 cc[C::QW];
+    // ---- transposed reduction over the 8 chunk lanes (lane bits 2, 1, 0).
+    // The lane's query chunks were visited in the order u ^ uperm, so at the
+    // chunk-level rounds the half a lane keeps is always its first half: no
+    // selects there.
+    constexpr int P0 = C::QW / 2;                 // query pairs before the reduction
+    u64 r1[C::KPL][P0 / 2];
 #pragma unroll
-    for (int k = 0; k < C::QW; ++k) {
-      const float2 sp = unpack2(sacc[k]);
-      const float2 sp2 = unpack2(sacc2[k]);
-      bool v = key_in && q_ok[k];
-      if (v && j >= p.ns) v = x >= q_lo[k] && x <= q_hi[k];
-      const float sv = v ? (sp.x + sp.y) + (sp2.x + sp2.y) : -INFINITY;
-      float tmax = sv;
+    for (int j = 0; j < C::KPL; ++j)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) tmax = fmaxf(tmax, __shfl_xor_sync(kVFull, tmax, o));
-      const float m_new = fmaxf(m[k], tmax);
-      float c = 1.f, pv = 0.f;
-      if (m_new != -INFINITY) {
-        c = exp2f(m[k] - m_new);
-        pv = exp2f(sv - m_new);
+      for (int k = 0; k < P0 / 2; ++k)
+        r1[j][k] = ffma2(sp[j][k], one2, __shfl_xor_sync(kVFull, sp[j][P0 / 2 + k], 4));
+    u64 r2[C::KPL][P0 / 4];
+#pragma unroll
+    for (int j = 0; j < C::KPL; ++j)
+#pragma unroll
+      for (int k = 0; k < P0 / 4; ++k) {
+        if constexpr (C::QW == 16) {
+          r2[j][k] = ffma2(r1[j][k], one2, __shfl_xor_sync(kVFull, r1[j][P0 / 4 + k], 2));
+        } else {
+          const u64 send = b1 ? r1[j][k] : r1[j][P0 / 4 + k];
+          const u64 keep = b1 ? r1[j][P0 / 4 + k] : r1[j][k];
+          r2[j][k] = ffma2(keep, one2, __shfl_xor_sync(kVFull, send, 2));
+        }
       }
-      l[k] = l[k] * c + pv;
-      m[k] = m_new;
-      cc[k] = pack2(c, c);
-      Pw[lane * C::QW + k] = pack2(pv, pv);
+    float sc[C::KPL][C::QO];
+#pragma unroll
+    for (int j = 0; j < C::KPL; ++j) {
+      if constexpr (C::QO == 2) {                 // one pair left per lane: queries 2e, 2e + 1
+        const u64 send = b0 ? r2[j][0] : r2[j][1];
+        const u64 keep = b0 ? r2[j][1] : r2[j][0];
+        const float2 v = unpack2(ffma2(keep, one2, __shfl_xor_sync(kVFull, send, 1)));
+        sc[j][0] = v.x;
+        sc[j][1] = v.y;
+      } else {                                    // split the last pair: query e
+        const float2 v = unpack2(r2[j][0]);
+        const float send = b0 ? v.x : v.y;
+        const float keep = b0 ? v.y : v.x;
+        sc[j][0] = keep + __shfl_xor_sync(kVFull, send, 1);
+      }
+    }
+    // ---- window mask, online softmax of the owned query vectors over the
+    // warp's keys of this tile, P and the rescale factors to shared memory
+    float cq[C::QO];
+#pragma unroll
+    for (int o = 0; o < C::QO; ++o) {
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < C::KPL; ++j) {
+        const int kl = kbase + kq + 4 * j;
+        const int jj = j0 + kl;
+        bool v = kl < cnt && q_ok[o];
+        if (v && jj >= p.ns) {
+          const int x = xlo + (jj - p.ns);
+          v = x >= q_lo[o] && x <= q_hi[o];
+        }
+        sc[j][o] = v ? sc[j][o] : -INFINITY;
+        tmax = fmaxf(tmax, sc[j][o]);
+      }
+      tmax = fmaxf(tmax, __shfl_xor_sync(kVFull, tmax, 8));
+      tmax = fmaxf(tmax, __shfl_xor_sync(kVFull, tmax, 16));
+      const float m_new = fmaxf(m[o], tmax);
+      float c = 1.f, lsum = 0.f;
+      if (m_new != -INFINITY) {
+        c = exp2f(m[o] - m_new);
+#pragma unroll
+        for (int j = 0; j < C::KPL; ++j) {
+          sc[j][o] = exp2f(sc[j][o] - m_new);
+          lsum += sc[j][o];
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < C::KPL; ++j) sc[j][o] = 0.f;
+      }
+      l[o] = l[o] * c + lsum;
+      m[o] = m_new;
+      cq[o] = c;
+    }
+#pragma unroll
+    for (int j = 0; j < C::KPL; ++j) {
+      u64* dst = Pw + (size_t)(kq + 4 * j) * C::QW + e * C::QO;
+      if constexpr (C::QO == 2) {
+        ulonglong2 pv;
+        pv.x = pack2(sc[j][0], sc[j][0]);
+        pv.y = pack2(sc[j][1], sc[j][1]);
+        *reinterpret_cast<ulonglong2*>(dst) = pv;
+      } else {
+        *dst = pack2(sc[j][0], sc[j][0]);
+      }
+    }
+    if (kq == 0) {
+#pragma unroll
+      for (int o = 0; o < C::QO; ++o) Cw[e * C::QO + o] = pack2(cq[o], cq[o]);
     }
     __syncwarp();
 
-    // ---- P V: lane = features [lane * DPL, lane * DPL + DPL)
+    // ---- P V: lane = (query group qgl of 8, feature group fg)
+    bool moved = false;
 #pragma unroll
-    for (int k = 0; k < C::QW; ++k)
+    for (int o = 0; o < C::QO; ++o) moved |= cq[o] != 1.f;
+    if (__any_sync(kVFull, moved)) {                // some running max moved: rescale
+      u64 cc[C::QPL];
 #pragma unroll
-      for (int d = 0; d < C::DPL / 2; ++d) acc[k][d] = ffma2(acc[k][d], cc[k], zero2);
-#pragma unroll 4
-    for (int kk = 0; kk < cnt; ++kk) {
-      u64 pk[C::QW];
+      for (int k2 = 0; k2 < C::QPL / 2; ++k2) {
+        const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(Cw + qgl * C::QPL + 2 * k2);
+        cc[2 * k2] = a.x;
+        cc[2 * k2 + 1] = a.y;
+      }
 #pragma unroll
-      for (int k2 = 0; k2 < C::QW / 2; ++k2) {
-        const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(Pw + kk * C::QW + 2 * k2);
+      for (int k = 0; k < C::QPL; ++k)
+#pragma unroll
+        for (int d = 0; d < C::FPL / 2; ++d) acc[k][d] = ffma2(acc[k][d], cc[k], zero2);
+    }
+    const int nkv = min(C::KW, cnt - kbase);
+#pragma unroll 2
+    for (int kk = 0; kk < nkv; ++kk) {
+      u64 pk[C::QPL];
+#pragma unroll
+      for (int k2 = 0; k2 < C::QPL / 2; ++k2) {
+        const ulonglong2 a =
+            *reinterpret_cast<const ulonglong2*>(Pw + (size_t)kk * C::QW + qgl * C::QPL + 2 * k2);
         pk[2 * k2] = a.x;
         pk[2 * k2 + 1] = a.y;
       }
-      const float* vr = Vs + ((size_t)stage * TK + kk) * HD + lane * C::DPL;
-      u64 vv[C::DPL / 2];
-      if constexpr (C::DPL == 2) {
-        vv[0] = *reinterpret_cast<const u64*>(vr);
-      } else {
+      const float* vr = Vt + (size_t)(kbase + kk) * HD;
+      u64 vv[C::FPL / 2];
 #pragma unroll
-        for (int c4 = 0; c4 < C::DPL / 4; ++c4) {
-          const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(vr + 4 * c4);
-          vv[2 * c4] = a.x;
-          vv[2 * c4 + 1] = a.y;
-        }
+      for (int u = 0; u < C::FCH; ++u) {
+        const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(vr + (fg + C::FG * u) * 4);
+        vv[2 * u] = a.x;
+        vv[2 * u + 1] = a.y;
       }
 #pragma unroll
-      for (int k = 0; k < C::QW; ++k)
+      for (int k = 0; k < C::QPL; ++k)
 #pragma unroll
-        for (int d = 0; d < C::DPL / 2; ++d) acc[k][d] = ffma2(pk[k], vv[d], acc[k][d]);
+        for (int d = 0; d < C::FPL / 2; ++d) acc[k][d] = ffma2(pk[k], vv[d], acc[k][d]);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
+    if (warp == 0 && issued < ntiles) {           // refill this stage with tile i + STAGES
+      bool ok2 = mbar_wait_bounded(&empty[stage], (uint32_t)((i / C::STAGES) & 1), kWaitLimitNs);
+      ok2 = __all_sync(kVFull, ok2);
+      if (!ok2) {
+        if (lane == 0) {
+          *s_abort = 1;
+          set_err(p.err, SWA_DERR_TIMEOUT);
+        }
+        break;
+      }
+      fence_proxy_async_smem();
+      issue_tile(issued);
+      ++issued;
+    }
   }
-  if (__shfl_sync(kVFull, *s_abort, 0)) return;
+  // No copy may still be landing in shared memory when the CTA ends: on an
+  // early exit warp 0 waits (bounded) for the tiles it issued beyond the
+  // last one it consumed.
+  if (warp == 0) {
+    for (int it = max(consumed, issued - C::STAGES); it < issued; ++it)
+      mbar_wait_bounded(&full[it % C::STAGES], (uint32_t)((it / C::STAGES) & 1), kWaitLimitNs);
+  }
 
-  // ---- this warp's query vectors of the partial record
+  // ---- combine the states of the warps sharing a query group into the
+  // CTA's partial record
+#pragma unroll
+  for (int o = 0; o < C::QO; ++o) {
+    l[o] += __shfl_xor_sync(kVFull, l[o], 8);
+    l[o] += __shfl_xor_sync(kVFull, l[o], 16);
+  }
+  named_barrier(1, kVCW * 32);                 // every consumer is past its last tile
+  if (*s_abort) return;
+  float* MLs = smem + C::OFF_ML;
+  if (kq == 0) {
+#pragma unroll
+    for (int o = 0; o < C::QO; ++o) {
+      MLs[(warp * C::QW + e * C::QO + o) * 2 + 0] = m[o];
+      MLs[(warp * C::QW + e * C::QO + o) * 2 + 1] = l[o];
+    }
+  }
+  float* red = smem;                           // [kVCW][QW][HD], reuses the stage buffers
+#pragma unroll
+  for (int k = 0; k < C::QPL; ++k) {
+    float* row = red + ((size_t)warp * C::QW + qgl * C::QPL + k) * HD;
+#pragma unroll
+    for (int u = 0; u < C::FCH; ++u) {
+      const float2 a = unpack2(acc[k][2 * u]);
+      const float2 c2 = unpack2(acc[k][2 * u + 1]);
+      *reinterpret_cast<float4*>(row + (fg + C::FG * u) * 4) = make_float4(a.x, a.y, c2.x, c2.y);
+    }
+  }
+  named_barrier(1, kVCW * 32);
+
   const size_t item = (((size_t)bg * p.n_rb + rb) * p.splits + s);
   float* wacc = p.ws_acc + item * (size_t)p.nq * HD;
+  for (int idx = tid; idx < NQ * HD / 4; idx += kVCW * 32) {
+    const int q = idx / (HD / 4), d4 = idx % (HD / 4);
+    const int qg = q / C::QW, ql = q % C::QW;
+    float M = -INFINITY;
 #pragma unroll
-  for (int k = 0; k < C::QW; ++k) {
-    float lt = l[k];
+    for (int kg = 0; kg < C::KG; ++kg) M = fmaxf(M, MLs[((qg + C::QG * kg) * C::QW + ql) * 2]);
+    float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (M != -INFINITY) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) lt += __shfl_xor_sync(kVFull, lt, o);
-    float* dst = wacc + (size_t)(q0 + k) * HD + lane * C::DPL;
+      for (int kg = 0; kg < C::KG; ++kg) {
+        const int w = qg + C::QG * kg;
+        const float mw = MLs[(w * C::QW + ql) * 2];
+        if (mw == -INFINITY) continue;
+        const float f = exp2f(mw - M);
+        const float4 a = *reinterpret_cast<const float4*>(red + ((size_t)w * C::QW + ql) * HD + d4 * 4);
+        sum.x += a.x * f; sum.y += a.y * f; sum.z += a.z * f; sum.w += a.w * f;
+      }
+    }
+    *reinterpret_cast<float4*>(wacc + (size_t)q * HD + d4 * 4) = sum;
+  }
+  if (tid < NQ) {
+    const int qg = tid / C::QW, ql = tid % C::QW;
+    float M = -INFINITY;
 #pragma unroll
-    for (int d = 0; d < C::DPL / 2; ++d) *reinterpret_cast<float2*>(dst + 2 * d) = unpack2(acc[k][d]);
-    if (lane == 0) p.ws_ml[item * p.nq + q0 + k] = make_float2(m[k], lt);
+    for (int kg = 0; kg < C::KG; ++kg) M = fmaxf(M, MLs[((qg + C::QG * kg) * C::QW + ql) * 2]);
+    float L = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int kg = 0; kg < C::KG; ++kg) {
+        const int w = qg + C::QG * kg;
+        const float mw = MLs[(w * C::QW + ql) * 2];
+        if (mw != -INFINITY) L += MLs[(w * C::QW + ql) * 2 + 1] * exp2f(mw - M);
+      }
+    }
+    p.ws_ml[item * p.nq + tid] = make_float2(M, L);
   }
 }
 
