@@ -133,20 +133,27 @@ attend_verify_kernel(AttendParams p) {
   // Query vectors of the block (rows then heads) times scale * log2 e, stored
   // transposed: feature f holds the 32 query slots as 8 float4 chunks, chunk
   // c at position c ^ ((f / 4) mod 8).
-  for (int idx = tid; idx < 32 * (HD / 4); idx += kVThreads) {
-    const int q = idx % 32, d4 = idx / 32;        // a warp covers the 32 query slots of a chunk
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+  {
+    constexpr int PER = 32 * (HD / 4) / kVThreads;   // float4 loads per thread
+    const int q = tid % 32;                           // a warp covers the 32 query slots of a chunk
     const int rr = q / p.hpg, h = q % p.hpg;
-    if (q < NQ && rr < rows_eff && q < p.rows * p.hpg) {
-      v = *reinterpret_cast<const float4*>(
-          p.q + (((size_t)b * p.t + r0 + rr) * p.nh + (size_t)g * p.hpg + h) * HD + d4 * 4);
-      v.x *= p.qmul; v.y *= p.qmul; v.z *= p.qmul; v.w *= p.qmul;
+    const bool live = q < NQ && rr < rows_eff && q < p.rows * p.hpg;
+    const float* qsrc = p.q + (((size_t)b * p.t + r0 + rr) * p.nh + (size_t)g * p.hpg + h) * HD;
+    float4 v[PER];
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {                   // all loads in flight before the stores
+      const int d4 = tid / 32 + k * (kVThreads / 32);
+      v[k] = live ? *reinterpret_cast<const float4*>(qsrc + d4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const int pos = (((q >> 2) ^ d4) & 7) * 4 + (q & 3);
-    QT[(d4 * 4 + 0) * 32 + pos] = v.x;
-    QT[(d4 * 4 + 1) * 32 + pos] = v.y;
-    QT[(d4 * 4 + 2) * 32 + pos] = v.z;
-    QT[(d4 * 4 + 3) * 32 + pos] = v.w;
+#pragma unroll
+    for (int k = 0; k < PER; ++k) {
+      const int d4 = tid / 32 + k * (kVThreads / 32);
+      const int pos = (((q >> 2) ^ d4) & 7) * 4 + (q & 3);
+      QT[(d4 * 4 + 0) * 32 + pos] = v[k].x * p.qmul;
+      QT[(d4 * 4 + 1) * 32 + pos] = v[k].y * p.qmul;
+      QT[(d4 * 4 + 2) * 32 + pos] = v[k].z * p.qmul;
+      QT[(d4 * 4 + 3) * 32 + pos] = v[k].w * p.qmul;
+    }
   }
   __syncthreads();
   const size_t kv_head = (size_t)b * p.nk + g;
@@ -219,6 +226,9 @@ attend_verify_kernel(AttendParams p) {
     q_lo[o] = st.len0 + r + 1 - min(st.W, st.len0 + r + 1);
     q_hi[o] = st.len0 + r;
   }
+  // logical keys inside the window of every row of the block
+  const int x_in_lo = st.len0 + r_last + 1 - min(st.W, st.len0 + r_last + 1);
+  const int x_in_hi = st.len0 + r0;
   float m[C::QO], l[C::QO];
 #pragma unroll
   for (int o = 0; o < C::QO; ++o) {
@@ -338,20 +348,27 @@ attend_verify_kernel(AttendParams p) {
     }
     // ---- window mask, online softmax of the owned query vectors over the
     // warp's keys of this tile, P and the rescale factors to shared memory
+    // A tile whose keys are all present and inside every row's window needs
+    // no mask (warp-uniform test; query slots past the block's rows hold zero
+    // vectors and their records are never read).
+    const bool inside = cnt == TK && xlo + (max(j0, p.ns) - p.ns) >= x_in_lo &&
+                        xlo + (j0 + TK - 1 - p.ns) <= x_in_hi;
     float cq[C::QO];
 #pragma unroll
     for (int o = 0; o < C::QO; ++o) {
       float tmax = -INFINITY;
 #pragma unroll
       for (int j = 0; j < C::KPL; ++j) {
-        const int kl = kbase + kq + 4 * j;
-        const int jj = j0 + kl;
-        bool v = kl < cnt && q_ok[o];
-        if (v && jj >= p.ns) {
-          const int x = xlo + (jj - p.ns);
-          v = x >= q_lo[o] && x <= q_hi[o];
+        if (!inside) {
+          const int kl = kbase + kq + 4 * j;
+          const int jj = j0 + kl;
+          bool v = kl < cnt && q_ok[o];
+          if (v && jj >= p.ns) {
+            const int x = xlo + (jj - p.ns);
+            v = x >= q_lo[o] && x <= q_hi[o];
+          }
+          sc[j][o] = v ? sc[j][o] : -INFINITY;
         }
-        sc[j][o] = v ? sc[j][o] : -INFINITY;
         tmax = fmaxf(tmax, sc[j][o]);
       }
       tmax = fmaxf(tmax, __shfl_xor_sync(kVFull, tmax, 8));
