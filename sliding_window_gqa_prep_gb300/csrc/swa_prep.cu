@@ -1,12 +1,14 @@
 // Prep stage: rotation, unit heads, query scale, ring write ("dory_msl.metal",
 // cortiq-engine 0.8.57, kernel dory_prep), and the RoPE table it consumes.
 //
-// One warp per (row, head): the q heads of a row come first, then its k heads
-// (the same split of the head index as dory_prep). Lane l owns the hd/64
-// rotated pairs (e, e + hd/2) with e in [l*hd/64, (l+1)*hd/64), so both halves
-// of a head are read and written as contiguous, coalesced vectors. The sum of
-// squares is a butterfly over the warp. Every byte moves once: the kernel is
-// bandwidth-bound and tiny next to the attention.
+// One CTA per row, one warp per head at a time: the q heads of a row come
+// first, then its k heads (the same split of the head index as dory_prep).
+// Lane l owns the hd/64 rotated pairs (e, e + hd/2) with e in
+// [l*hd/64, (l+1)*hd/64), so both halves of a head are read and written as
+// contiguous, coalesced vectors. The sum of squares is a butterfly over the
+// warp. Every byte moves once. The row's angles, when the kernel computes
+// them, cost f64 sine/cosine evaluations, which are slow on this GPU: one CTA
+// per row evaluates them once for all of the row's heads.
 #include "swa_internal.cuh"
 
 namespace swa {
@@ -35,43 +37,17 @@ __device__ __forceinline__ void stv(float* p, const float (&r)[P]) {
 }
 
 constexpr int kPrepWarps = 8;
+constexpr int kPrepBatch = 4;      // heads a warp loads before it stores any
 
+// One head of one row: rotation, unit norm, query scale / ring write.
 template <int HD>
-__global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
-  constexpr int P = HD / 64;       // pairs per lane
+__device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, int lane,
+                                          const float (&c)[HD / 64], const float (&s)[HD / 64],
+                                          const float (&x)[HD / 64], const float (&y)[HD / 64]) {
+  constexpr int P = HD / 64;
   constexpr int HALF = HD / 2;
-  const int row = blockIdx.x;      // b * t + j
-  const int a = blockIdx.y * kPrepWarps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  // Without a table, the row's cos/sin are computed once per CTA, with the
-  // same f64 expression as rope_table_kernel (bit-identical f32 values).
-  __shared__ __align__(16) float s_cs[HD];
-  if (p.rope == nullptr) {
-    const int b = row / p.t, j = row % p.t;
-    const double pos = (double)p.pos0[b] + (double)j;
-    for (int e2 = threadIdx.x; e2 < HALF; e2 += blockDim.x) {
-      double sn, cs;
-      sincos(pos * p.inv_freq[e2], &sn, &cs);
-      s_cs[e2] = (float)cs;
-      s_cs[HALF + e2] = (float)sn;
-    }
-    __syncthreads();
-  }
-  if (a >= p.nh + p.nk) return;
   const int e = lane * P;
-
-  float c[P], s[P];
-  const float* rope = p.rope ? p.rope + (size_t)row * HD : s_cs;
-  ldv<P>(rope + e, c);
-  ldv<P>(rope + HALF + e, s);
-
-  const bool is_q = a < p.nh;
-  const int kh = a - p.nh;
-  const float* src = is_q ? p.yq + ((size_t)row * p.nh + a) * HD
-                          : p.yk + ((size_t)row * p.nk + kh) * HD;
-  float x[P], y[P], u[P], v[P];
-  ldv<P>(src + e, x);
-  ldv<P>(src + HALF + e, y);
+  float u[P], v[P];
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
@@ -83,7 +59,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   const float inv = 1.0f / sqrtf(ss + p.eps);
 
-  if (is_q) {
+  if (a < p.nh) {
     float sa[P], sb[P];
     ldv<P>(p.q_scale + (size_t)a * HD + e, sa);
     ldv<P>(p.q_scale + (size_t)a * HD + HALF + e, sb);
@@ -97,6 +73,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
     stv<P>(dst + HALF + e, v);
     return;
   }
+  const int kh = a - p.nh;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
     u[i] *= inv;
@@ -105,6 +82,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
   float* kd = p.k_out + ((size_t)row * p.nk + kh) * HD;
   stv<P>(kd + e, u);
   stv<P>(kd + HALF + e, v);
+  if (!p.v_out && !p.ring_k) return;
   const float* vs = p.yv + ((size_t)row * p.nk + kh) * HD;
   float va[P], vb[P];
   ldv<P>(vs + e, va);
@@ -122,6 +100,57 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
     stv<P>(p.ring_k + at + HALF + e, v);
     stv<P>(p.ring_v + at + e, va);
     stv<P>(p.ring_v + at + HALF + e, vb);
+  }
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
+  constexpr int P = HD / 64;       // pairs per lane
+  constexpr int HALF = HD / 2;
+  const int row = blockIdx.x;      // b * t + j
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  // Without a table, the row's cos/sin are computed once per CTA (the CTA
+  // covers every head of the row), with the same f64 expression as
+  // rope_table_kernel (bit-identical f32 values).
+  __shared__ __align__(16) float s_cs[HD];
+  if (p.rope == nullptr) {
+    const int b = row / p.t, j = row % p.t;
+    const double pos = (double)p.pos0[b] + (double)j;
+    for (int e2 = threadIdx.x; e2 < HALF; e2 += blockDim.x) {
+      double sn, cs;
+      sincos(pos * p.inv_freq[e2], &sn, &cs);
+      s_cs[e2] = (float)cs;
+      s_cs[HALF + e2] = (float)sn;
+    }
+    __syncthreads();
+  }
+  const int e = lane * P;
+  float c[P], s[P];
+  const float* rope = p.rope ? p.rope + (size_t)row * HD : s_cs;
+  ldv<P>(rope + e, c);
+  ldv<P>(rope + HALF + e, s);
+
+  // heads a = warp, warp + kPrepWarps, ...: q heads first, then k heads (the
+  // head split of dory_prep); kPrepBatch heads' inputs are in flight at once
+  const int nheads = p.nh + p.nk;
+  for (int a0 = warp; a0 < nheads; a0 += kPrepWarps * kPrepBatch) {
+    float x[kPrepBatch][P], y[kPrepBatch][P];
+#pragma unroll
+    for (int k = 0; k < kPrepBatch; ++k) {
+      const int a = a0 + k * kPrepWarps;
+      if (a < nheads) {
+        const float* src = a < p.nh ? p.yq + ((size_t)row * p.nh + a) * HD
+                                    : p.yk + ((size_t)row * p.nk + (a - p.nh)) * HD;
+        ldv<P>(src + e, x[k]);
+        ldv<P>(src + HALF + e, y[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kPrepBatch; ++k) {
+      const int a = a0 + k * kPrepWarps;
+      if (a < nheads) prep_head<HD>(p, row, a, lane, c, s, x[k], y[k]);
+    }
   }
 }
 
@@ -151,7 +180,7 @@ __global__ void rope_table_kernel(float* rope, const uint32_t* pos0, int B, int 
 }  // namespace
 
 int launch_prep(const PrepParams& p, cudaStream_t s) {
-  dim3 grid((unsigned)(p.B * p.t), (unsigned)((p.nh + p.nk + kPrepWarps - 1) / kPrepWarps));
+  dim3 grid((unsigned)(p.B * p.t));
   dim3 block(kPrepWarps * 32);
   switch (p.hd) {
     case 64: prep_kernel<64><<<grid, block, 0, s>>>(p); break;
