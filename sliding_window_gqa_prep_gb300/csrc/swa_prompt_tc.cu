@@ -41,6 +41,7 @@ constexpr int kTN = 32;                // keys per tile
 constexpr int kTThreads = 10 * 32;
 constexpr int kSoftThreads = 128;
 constexpr unsigned kTF = 0xffffffffu;
+constexpr float kLazyMax = 8.0f;       // log2 headroom before the running max is raised
 
 template <int HD>
 struct TCfg {
@@ -412,11 +413,6 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     };
     for (int i = 0; !dead && i < ntiles; ++i) {
       if (*s_abort) { fail(); break; }
-      if (i >= 1 && !__all_sync(kTF, mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), kWaitLimitNs))) {
-        fail();
-        break;
-      }
-      // P V of tile i - 1 is complete here: P and O may be rewritten
       const int cnt = min(kTN, n - i * kTN);
       if (!__all_sync(kTF, mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1), kWaitLimitNs))) {
         fail();
@@ -426,21 +422,33 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       uint32_t sr[32];
       tc_ld32(tmem + lane_off + ((i & 1) ? C::C_S1 : C::C_S0), sr);
       tc_wait_ld();
+      // window mask; a tile wholly inside this row's window skips it
+      const int j0 = i * kTN;
+      const bool inside = q_ok && cnt == kTN && j0 >= p.ns && xlo + (j0 - p.ns) >= q_lo &&
+                          xlo + (j0 + kTN - 1 - p.ns) <= q_hi;
       float tmax = -INFINITY;
       float s[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
-        const int j = i * kTN + k;
-        bool v = q_ok && k < cnt;
-        if (v && j >= p.ns) {
-          const int x = xlo + (j - p.ns);
-          v = x >= q_lo && x <= q_hi;
+        bool v = true;
+        if (!inside) {
+          const int j = j0 + k;
+          v = q_ok && k < cnt;
+          if (v && j >= p.ns) {
+            const int x = xlo + (j - p.ns);
+            v = x >= q_lo && x <= q_hi;
+          }
         }
         s[k] = v ? __uint_as_float(sr[k]) : -INFINITY;
         tmax = fmaxf(tmax, s[k]);
       }
-      const float m_new = fmaxf(m_run, tmax);
-      const float c = m_new == -INFINITY ? 1.f : exp2f(m_run - m_new);
+      // The running max m_run moves only when a tile exceeds it by more than
+      // kLazyMax (log2 units): below that, p = 2^(s - m_run) <= 2^kLazyMax and
+      // O and l keep one common scale, so o = O / l is unchanged while the
+      // O rescale in tensor memory is skipped.
+      const bool raise = tmax > m_run + kLazyMax;
+      const float m_new = raise ? tmax : m_run;
+      const float c = raise ? exp2f(m_run - m_new) : 1.f;
       uint32_t phi[32], plo[32];
       float psum = 0.f;
 #pragma unroll
@@ -452,6 +460,13 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       }
       l_run = l_run * c + psum;
       m_run = m_new;
+      // P V of tile i - 1 must be complete before P and O are rewritten; the
+      // work above overlapped it
+      if (i >= 1 && !__all_sync(kTF, mbar_wait_bounded(pv_done, (uint32_t)((i - 1) & 1), kWaitLimitNs))) {
+        fail();
+        break;
+      }
+      tc_fence_after();
       tc_st32(tmem + lane_off + C::C_PHI, phi);
       tc_st32(tmem + lane_off + C::C_PLO, plo);
       // rescale this row of O when its max moved (warp-uniform decision)
