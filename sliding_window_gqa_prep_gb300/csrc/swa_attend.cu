@@ -25,6 +25,8 @@ namespace {
 // Merge of the split records + gate; trailing CTAs commit the chunk.
 template <int HD>
 __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int out_blocks) {
+  pdl_trigger();
+  pdl_wait();
   if ((int)blockIdx.x >= out_blocks) {
     // ---- commit of sequence b, spread over commit_blocks CTAs: the last
     // min(t, W) chunk rows into their ring slots (o1c_ring_commit), then the
@@ -154,13 +156,11 @@ int launch_attend_merge(const AttendParams& p, cudaStream_t s) {
   const int out_blocks = (int)((rows + block / 32 - 1) / (block / 32));
   const int grid = out_blocks + (p.commit ? p.B * p.commit_blocks : 0);
   switch (p.hd) {
-    case 64: attend_merge_kernel<64><<<grid, block, 0, s>>>(p, out_blocks); break;
-    case 128: attend_merge_kernel<128><<<grid, block, 0, s>>>(p, out_blocks); break;
-    case 256: attend_merge_kernel<256><<<grid, block, 0, s>>>(p, out_blocks); break;
+    case 64: return finish_launch(launch_pdl(attend_merge_kernel<64>, dim3(grid), dim3(block), 0, s, p, out_blocks));
+    case 128: return finish_launch(launch_pdl(attend_merge_kernel<128>, dim3(grid), dim3(block), 0, s, p, out_blocks));
+    case 256: return finish_launch(launch_pdl(attend_merge_kernel<256>, dim3(grid), dim3(block), 0, s, p, out_blocks));
     default: return SWA_E_SHAPE;
   }
-  note_launch();
-  return cuda_status(cudaGetLastError());
 }
 
 }  // namespace swa

@@ -81,6 +81,8 @@ __device__ __forceinline__ void store_slice(float* row, int lane, const float (&
 
 template <int HD, int NQ>
 __global__ void __launch_bounds__(kDecThreads) attend_decode_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
   using C = DCfg<HD, NQ>;
   extern __shared__ __align__(128) float smem[];
   float* Ks = smem + C::OFF_K;
@@ -404,9 +406,9 @@ int launch_t(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t 
   }
   dim3 grid((unsigned)p.splits, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
   if (e0) cudaEventRecord(e0, s);
-  kern<<<grid, kDecThreads, C::BYTES, s>>>(p);
+  cudaError_t e = launch_pdl(kern, grid, dim3(kDecThreads), C::BYTES, s, p);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e1) cudaEventRecord(e1, s);
   return cuda_status(e);
 }

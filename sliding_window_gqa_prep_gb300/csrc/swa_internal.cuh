@@ -222,4 +222,39 @@ __device__ __forceinline__ SeqState load_state(const AttendParams& p, int b, boo
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per bounded wait
 
+// Programmatic dependent launch. A kernel started by launch_pdl may be
+// scheduled while the previous kernel of the stream is still running: it calls
+// pdl_wait() before its first global memory access, which returns once that
+// kernel has completed and its writes are visible (so stream order holds for
+// every byte), and pdl_trigger() to let the next kernel's CTAs be scheduled as
+// soon as all of its own CTAs have started. Without a programmatic dependency
+// (an ordinary launch, another preceding operation) both are no-ops.
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
+// Bookkeeping after a launch: count it and fold the launch error into a status.
+inline int finish_launch(cudaError_t e) {
+  note_launch();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return cuda_status(e);
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 }  // namespace swa

@@ -105,6 +105,8 @@ __device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, i
 
 template <int HD>
 __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int P = HD / 64;       // pairs per lane
   constexpr int HALF = HD / 2;
   const int row = blockIdx.x;      // b * t + j
@@ -183,13 +185,11 @@ int launch_prep(const PrepParams& p, cudaStream_t s) {
   dim3 grid((unsigned)(p.B * p.t));
   dim3 block(kPrepWarps * 32);
   switch (p.hd) {
-    case 64: prep_kernel<64><<<grid, block, 0, s>>>(p); break;
-    case 128: prep_kernel<128><<<grid, block, 0, s>>>(p); break;
-    case 256: prep_kernel<256><<<grid, block, 0, s>>>(p); break;
+    case 64: return finish_launch(launch_pdl(prep_kernel<64>, grid, block, 0, s, p));
+    case 128: return finish_launch(launch_pdl(prep_kernel<128>, grid, block, 0, s, p));
+    case 256: return finish_launch(launch_pdl(prep_kernel<256>, grid, block, 0, s, p));
     default: return SWA_E_SHAPE;
   }
-  note_launch();
-  return cuda_status(cudaGetLastError());
 }
 
 int launch_rope_table(float* rope, const uint32_t* pos0, int B, int t, int hd,

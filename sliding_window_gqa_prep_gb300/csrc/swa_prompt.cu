@@ -82,6 +82,8 @@ __device__ __forceinline__ void cp_async_wait_0() { asm volatile("cp.async.wait_
 
 template <int HD>
 __global__ void __launch_bounds__(kPThreads, 2) attend_prompt_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
   using C = PCfg<HD>;
   extern __shared__ __align__(128) float smem[];
   float* Ks = smem + C::OFF_K;
@@ -303,9 +305,9 @@ int launch_prompt_t(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaE
   }
   dim3 grid(1u, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
   if (e0) cudaEventRecord(e0, s);
-  kern<<<grid, kPThreads, C::BYTES, s>>>(p);
+  cudaError_t e = launch_pdl(kern, grid, dim3(kPThreads), C::BYTES, s, p);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e1) cudaEventRecord(e1, s);
   return cuda_status(e);
 }

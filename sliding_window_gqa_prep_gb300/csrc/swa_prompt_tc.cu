@@ -127,6 +127,8 @@ __device__ __forceinline__ uint32_t tf32_hi(float x) {
 
 template <int HD>
 __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
   using C = TCfg<HD>;
   extern __shared__ __align__(1024) unsigned char sm[];
   float* landK = reinterpret_cast<float*>(sm + C::OFF_LK);
@@ -537,9 +539,9 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
   }
   dim3 grid(1u, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
   if (e0) cudaEventRecord(e0, s);
-  kern<<<grid, kTThreads, C::BYTES, s>>>(p);
+  cudaError_t e = launch_pdl(kern, grid, dim3(kTThreads), C::BYTES, s, p);
   note_launch();
-  cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e1) cudaEventRecord(e1, s);
   return cuda_status(e);
 }
