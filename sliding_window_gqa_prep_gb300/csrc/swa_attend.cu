@@ -22,9 +22,90 @@
 namespace swa {
 namespace {
 
-// Merge of the split records + gate; trailing CTAs commit the chunk.
+// Gate of one output row: o = acc * inv, times sigmoid(gate * gate_scale).
+__device__ __forceinline__ float4 gated(const AttendParams& p, size_t row, int h, int d4, int hd,
+                                        float4 acc, float inv) {
+  const float4 gt = *reinterpret_cast<const float4*>(p.gate + row * hd + d4 * 4);
+  const float4 gs = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * hd + d4 * 4);
+  float4 o;
+  o.x = acc.x * inv / (1.0f + expf(-(gt.x * gs.x)));
+  o.y = acc.y * inv / (1.0f + expf(-(gt.y * gs.y)));
+  o.z = acc.z * inv / (1.0f + expf(-(gt.z * gs.z)));
+  o.w = acc.w * inv / (1.0f + expf(-(gt.w * gs.w)));
+  return o;
+}
+
+// One output row (b, r, h) by a whole CTA of 8 warps: every warp finds the
+// max over the valid splits, warp w adds the rescaled records of splits
+// w, w + 8, ... (lanes over features), and the CTA sums the 8 partials.
 template <int HD>
-__global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int out_blocks) {
+__device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
+  constexpr int D4 = HD / 4;
+  constexpr int PER = (D4 + 31) / 32;
+  __shared__ float4 s_acc[8][D4];
+  __shared__ float s_den[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const size_t row = blk;                      // (b * t + r) * nh + h
+  if (row >= (size_t)p.B * p.t * p.nh) return;
+  const int h = (int)(row % p.nh);
+  const size_t br = row / p.nh;
+  const int r = (int)(br % p.t);
+  const int b = (int)(br / p.t);
+  const int g = h / p.hpg;
+  const int rb = r / p.rows;
+  const int q = (r - rb * p.rows) * p.hpg + (h - g * p.hpg);
+  const size_t item0 = (((size_t)b * p.nk + g) * p.n_rb + rb) * p.splits;
+  const int nval = p.ws_nsplit[b * p.n_rb + rb];
+  float M = -INFINITY;
+  for (int s0 = lane; s0 < nval; s0 += 32) M = fmaxf(M, p.ws_ml[(item0 + s0) * p.nq + q].x);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  float4 acc[PER];
+#pragma unroll
+  for (int c = 0; c < PER; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+#pragma unroll 4
+  for (int sp = warp; sp < nval; sp += 8) {
+    const float2 ml = p.ws_ml[(item0 + sp) * p.nq + q];
+    if (ml.x == -INFINITY) continue;            // a split with no key of this row weighs 0
+    const float w = exp2f(ml.x - M);
+    den += ml.y * w;
+    const float* src = p.ws_acc + ((item0 + sp) * p.nq + q) * (size_t)HD;
+#pragma unroll
+    for (int c = 0; c < PER; ++c) {
+      const int d4 = c * 32 + lane;
+      if (d4 < D4) {
+        const float4 a = *reinterpret_cast<const float4*>(src + d4 * 4);
+        acc[c].x += a.x * w; acc[c].y += a.y * w; acc[c].z += a.z * w; acc[c].w += a.w * w;
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < PER; ++c) {
+    const int d4 = c * 32 + lane;
+    if (d4 < D4) s_acc[warp][d4] = acc[c];
+  }
+  if (lane == 0) s_den[warp] = den;
+  __syncthreads();
+  if ((int)threadIdx.x < D4) {
+    const int d4 = threadIdx.x;
+    float4 t = s_acc[0][d4];
+    float dsum = s_den[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) {
+      const float4 a = s_acc[w][d4];
+      t.x += a.x; t.y += a.y; t.z += a.z; t.w += a.w;
+      dsum += s_den[w];
+    }
+    *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) = gated(p, row, h, d4, HD, t, 1.0f / dsum);
+  }
+}
+
+// Merge of the split records + gate; trailing CTAs commit the chunk. With
+// `wide`, one CTA per output row whose 8 warps share the splits (calls with
+// many splits per row); otherwise one warp per output row.
+template <int HD>
+__global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int out_blocks, int wide) {
   pdl_trigger();
   pdl_wait();
   if ((int)blockIdx.x >= out_blocks) {
@@ -63,6 +144,10 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
       }
       p.meta_out[b] = m1;
     }
+    return;
+  }
+  if (wide) {
+    merge_row_wide<HD>(p, blockIdx.x);
     return;
   }
   // ---- one warp per output row (b, r, h): lane s of each group of 32 splits
@@ -151,14 +236,20 @@ int attend_partial_occupancy(int hd, int nq) {
 }
 
 int launch_attend_merge(const AttendParams& p, cudaStream_t s) {
-  const size_t rows = (size_t)p.B * p.t * p.nh;   // one warp per output row
+  const size_t rows = (size_t)p.B * p.t * p.nh;
   const int block = 256;
-  const int out_blocks = (int)((rows + block / 32 - 1) / (block / 32));
+  // many splits per row: a CTA per row (8 warps share the splits); else a warp per row
+  const int wide = p.splits >= 16 ? 1 : 0;
+  // the tcgen05 kernel (128 query vectors per block, one split) writes the
+  // gated output itself: only the commit is left
+  const int out_blocks = p.nq == 128 ? 0
+                         : (wide ? (int)rows : (int)((rows + block / 32 - 1) / (block / 32)));
+  if (out_blocks == 0 && !p.commit) return SWA_OK;
   const int grid = out_blocks + (p.commit ? p.B * p.commit_blocks : 0);
   switch (p.hd) {
-    case 64: return finish_launch(launch_pdl(attend_merge_kernel<64>, dim3(grid), dim3(block), 0, s, p, out_blocks));
-    case 128: return finish_launch(launch_pdl(attend_merge_kernel<128>, dim3(grid), dim3(block), 0, s, p, out_blocks));
-    case 256: return finish_launch(launch_pdl(attend_merge_kernel<256>, dim3(grid), dim3(block), 0, s, p, out_blocks));
+    case 64: return finish_launch(launch_pdl(attend_merge_kernel<64>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
+    case 128: return finish_launch(launch_pdl(attend_merge_kernel<128>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
+    case 256: return finish_launch(launch_pdl(attend_merge_kernel<256>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
     default: return SWA_E_SHAPE;
   }
 }
