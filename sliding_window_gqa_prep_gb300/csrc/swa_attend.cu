@@ -240,11 +240,7 @@ int launch_attend_merge(const AttendParams& p, cudaStream_t s) {
   const int block = 256;
   // many splits per row: a CTA per row (8 warps share the splits); else a warp per row
   const int wide = p.splits >= 16 ? 1 : 0;
-  // the tcgen05 kernel (128 query vectors per block, one split) writes the
-  // gated output itself: only the commit is left
-  const int out_blocks = p.nq == 128 ? 0
-                         : (wide ? (int)rows : (int)((rows + block / 32 - 1) / (block / 32)));
-  if (out_blocks == 0 && !p.commit) return SWA_OK;
+  const int out_blocks = wide ? (int)rows : (int)((rows + block / 32 - 1) / (block / 32));
   const int grid = out_blocks + (p.commit ? p.B * p.commit_blocks : 0);
   switch (p.hd) {
     case 64: return finish_launch(launch_pdl(attend_merge_kernel<64>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));

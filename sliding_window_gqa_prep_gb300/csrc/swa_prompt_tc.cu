@@ -57,7 +57,6 @@ struct TCfg {
   static constexpr int OFF_OPS = 4 * LAND;                  // [2 sets] K_hi, K_lo, V^T_hi, V^T_lo
   static constexpr int SET = 4 * LAND;
   static constexpr int OFF_BAR = OFF_OPS + 2 * SET;         // mbarriers
-  static_assert(kTM * (HD + 4) * 4 <= 2 * SET, "output rows fit the operand buffers");
   static constexpr int NBAR = 14;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
@@ -135,7 +134,6 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   float* landK = reinterpret_cast<float*>(sm + C::OFF_LK);
   float* landV = reinterpret_cast<float*>(sm + C::OFF_LV);
   // operand set k (k = tile % 2): K_hi, K_lo, V^T_hi, V^T_lo
-  float* stage_o = reinterpret_cast<float*>(sm + C::OFF_OPS);   // [128][HD + 4] after the last P V
   auto op = [&](int set, int which) {
     return reinterpret_cast<uint32_t*>(sm + C::OFF_OPS + set * C::SET + which * C::LAND);
   };
@@ -489,54 +487,29 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       __syncwarp();
       if (lane == 0) mbar_arrive(p_ready);
     }
-    // ---- the block has a single split, so o = O / l is final (o1c_tok_merge
-    // with one partial): each thread puts its row into shared memory (the
-    // operand buffers, free once the last P V has completed; rows padded by 4
-    // floats so the lanes' stores hit distinct banks) and the whole CTA
-    // applies the gate below with coalesced accesses
+    // ---- the block's record: m, l, O (unnormalised)
     if (!dead && !*s_abort) {
       const bool ok = __all_sync(kTF, ntiles == 0 ||
                                           mbar_wait_bounded(pv_done, (uint32_t)((ntiles - 1) & 1), kWaitLimitNs));
       if (ok) {
         tc_fence_after();
-        const float inv = q_ok ? 1.0f / l_run : 0.f;
-        float* srow = stage_o + (size_t)q * (HD + 4);
+        const size_t item = ((size_t)bg * p.n_rb + rb) * p.splits;
+        float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD;
         for (int c0 = 0; c0 < HD; c0 += 32) {
           uint32_t o[32];
-          tc_ld32(tmem + lane_off + C::C_O + c0, o);   // warp-collective: every lane takes part
+          tc_ld32(tmem + lane_off + C::C_O + c0, o);
           tc_wait_ld();
 #pragma unroll
           for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(srow + c0 + k) =
-                make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
-                            __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+            *reinterpret_cast<float4*>(dst + c0 + k) =
+                make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]), __uint_as_float(o[k + 2]),
+                            __uint_as_float(o[k + 3]));
         }
+        p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run);
       } else if (lane == 0) {
         *s_abort = 1;
         set_err(p.err, SWA_DERR_TIMEOUT);
       }
-    }
-  }
-
-  // ---- gated output rows, out = o * sigmoid(gate * gate_scale) (dory_gate),
-  // by all warps: consecutive threads take consecutive features of a row
-  __syncthreads();
-  if (!*s_abort) {
-    const int nqv = rows_eff * p.hpg;
-    for (int idx = tid; idx < nqv * (HD / 4); idx += kTThreads) {
-      const int qv = idx / (HD / 4), d4 = idx % (HD / 4);
-      const int rq = r0 + qv / p.hpg;
-      const int hq = g * p.hpg + qv % p.hpg;
-      const size_t orow = (((size_t)b * p.t + rq) * p.nh + hq) * HD;
-      const float4 o = *reinterpret_cast<const float4*>(stage_o + (size_t)qv * (HD + 4) + d4 * 4);
-      const float4 gt = *reinterpret_cast<const float4*>(p.gate + orow + d4 * 4);
-      const float4 gs = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)hq * HD + d4 * 4);
-      float4 v;
-      v.x = o.x / (1.0f + expf(-(gt.x * gs.x)));
-      v.y = o.y / (1.0f + expf(-(gt.y * gs.y)));
-      v.z = o.z / (1.0f + expf(-(gt.z * gs.z)));
-      v.w = o.w / (1.0f + expf(-(gt.w * gs.w)));
-      *reinterpret_cast<float4*>(p.out + orow + d4 * 4) = v;
     }
   }
 
