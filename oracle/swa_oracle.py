@@ -32,6 +32,12 @@ Readings where the pages are silent (each is listed in the design doc):
 * softmax starts from -inf and has no denominator clamp (every row attends at
   least its own key, so the sum is >= 1).
 
+The far field of a decode row (``far_*``, ``attend_far*``) follows
+"o1c_msl.metal" ``o1c_tok_far`` / ``o1c_tok_merge`` / ``o1c_tok_commit`` and the
+optional clip of "dory_msl.metal" ``dory_ofar`` (``rect``). Reading: the state
+(landmark keys and queries, the m x m matrix mu, per-landmark max / mass /
+numerator) is per sequence; the pages hold one sequence and never build it.
+
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, a library attention routine on a materialised sequence,
 invariants, hand-derived integer fixtures under ``tests/golden/``) except the
@@ -40,6 +46,8 @@ default score scale 1/sqrt(hd) for workloads whose scale the pages leave
 open: those two readings are "parity unpinned".
 """
 from __future__ import annotations
+
+import math
 
 import numpy as np
 
@@ -315,3 +323,147 @@ def rollback(meta, n_back, cap):
         else:
             out[b] = r
     return out, bad
+
+
+# ---------------------------------------------------------------------------
+# Far field of a decode row ("o1c_msl.metal": o1c_tok_far, o1c_tok_merge,
+# o1c_tok_commit; "dory_msl.metal": dory_ofar for the optional clip `rect`)
+#
+# far = {"m": landmarks, "rect": 0/1,
+#        "k_tilde": [B][nk][m][hd]  landmark keys of each KV group,
+#        "q_tilde": [B][nh][m][hd]  landmark queries of each query head,
+#        "mu":      [B][nh][m][m]   the landmark weights' matrix,
+#        "mz":      [B][nh][2m]     per landmark: running max, then mass,
+#        "t_hat":   [B][nh][m][hd]  per landmark: far numerator}
+# One decode row (t = 1) of sequence b. Keys leave the window only when it is
+# full (win_len == W): the oldest, ring slot win_head, is evicted by the row.
+# ---------------------------------------------------------------------------
+def far_evict(mx_b, z_b, k_ev, q_tilde_b, scale):
+    """One landmark's running max and mass after an evicted key, as
+    o1c_tok_far does: fe = scale * <q~, k>, mx' = max(mx, fe),
+    rr = exp(mx - mx') (1 when the max stays; an empty field, mx = -inf,
+    gives 0), e = exp(fe - mx'), z' = z * rr + e. Returns (mx', z', rr, e)."""
+    fe = scale * float(np.dot(np.asarray(q_tilde_b, np.float64), np.asarray(k_ev, np.float64)))
+    mx2 = max(mx_b, fe)
+    rr = 1.0 if mx2 == mx_b else math.exp(mx_b - mx2)
+    e = math.exp(fe - mx2)
+    return mx2, z_b * rr + e, rr, e
+
+
+def far_part(q, far, b, h, g, mx2, z2, scale):
+    """The far part of a row for query head h with the far state mx2, z2 (after
+    this row's eviction): landmark scores fs_a = scale * <q, k~_a>, f = max fs;
+    w_b = sum_a exp(fs_a - f) mu[a][b] (clipped at 0 with rect); fm = max_b
+    (f + mx2_b); gain_b = w_b exp(f + mx2_b - fm); far_den = sum_b gain_b z2_b.
+    A negative far_den drops the far part (have = False). Returns
+    (have, fm, far_den, gain[m])."""
+    m = far["m"]
+    kt = np.asarray(far["k_tilde"][b, g], np.float64)
+    mu = np.asarray(far["mu"][b, h], np.float64)
+    fs = scale * (kt @ np.asarray(q, np.float64))
+    f = np.max(fs)
+    w = np.exp(fs - f) @ mu                      # w[b] = sum_a exp(fs_a - f) mu[a][b]
+    if far["rect"]:
+        w = np.maximum(w, 0.0)
+    fb = f + np.asarray(mx2, np.float64)
+    fm = np.max(fb)
+    gain = w * np.exp(fb - fm)
+    far_den = float(np.sum(gain * np.asarray(z2, np.float64)))
+    if not far_den >= 0.0:
+        return False, fm, 0.0, np.zeros(m)
+    return True, fm, far_den, gain
+
+
+def far_row_state(meta_b, far, b, h, g, inp, scale):
+    """This row's eviction against every landmark of head h: the state after
+    it (mx2, z2, t_hat2) and whether a key was evicted."""
+    cap = inp["ring_k"].shape[2]
+    m = far["m"]
+    W = ring_modulus(meta_b, cap)
+    evict = int(meta_b[WIN_LEN]) == W
+    mx = np.asarray(far["mz"][b, h, :m], np.float64)
+    z = np.asarray(far["mz"][b, h, m:], np.float64)
+    th = np.asarray(far["t_hat"][b, h], np.float64)
+    if not evict:
+        return False, mx.copy(), z.copy(), th.copy()
+    slot = int(meta_b[WIN_HEAD]) % W
+    k_ev = inp["ring_k"][b, g, slot]
+    v_ev = np.asarray(inp["ring_v"][b, g, slot], np.float64)
+    mx2, z2, th2 = np.zeros(m), np.zeros(m), np.zeros_like(th)
+    for a in range(m):
+        mx2[a], z2[a], rr, e = far_evict(float(mx[a]), float(z[a]), k_ev, far["q_tilde"][b, h, a], scale)
+        th2[a] = th[a] * rr + e * v_ev
+    return True, mx2, z2, th2
+
+
+def attend_far_row(b, h, inp, far, scale, hpg):
+    """Output of query head h of the decode row of sequence b with the far
+    field (o1c_tok_merge, then dory_gate): with c the larger of the near max
+    and (when the far part is kept) fm,
+    o = (sum_near exp(s - c) v + exp(fm - c) sum_b gain_b t_hat2_b)
+        / (sum_near exp(s - c) + exp(fm - c) far_den)."""
+    meta_b = inp["meta"][b]
+    g = h // hpg
+    cap = inp["ring_k"].shape[2]
+    ns = inp["sink_k"].shape[2]
+    keys = row_key_list(meta_b, 0, ns, cap)
+    q = np.asarray(inp["q"][b, 0, h], np.float64)
+    K, V = [], []
+    for kind, idx in keys:
+        if kind == "sink":
+            K.append(inp["sink_k"][b, g, idx])
+            V.append(inp["sink_v"][b, g, idx])
+        elif kind == "ring":
+            K.append(inp["ring_k"][b, g, idx])
+            V.append(inp["ring_v"][b, g, idx])
+        else:
+            K.append(inp["k_chunk"][b, idx, g])
+            V.append(inp["v_chunk"][b, idx, g])
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    s = scale * (K @ q)
+    evict, mx2, z2, th2 = far_row_state(meta_b, far, b, h, g, inp, scale)
+    farl = int(meta_b[FAR_LEN]) + (1 if evict else 0)
+    have, fm, far_den, gain = (False, -np.inf, 0.0, None)
+    if farl > 0:
+        have, fm, far_den, gain = far_part(q, far, b, h, g, mx2, z2, scale)
+    c = max(np.max(s), fm) if have else np.max(s)
+    p = np.exp(s - c)
+    num = p @ V
+    den = np.sum(p)
+    if have:
+        sf = math.exp(fm - c)
+        num = num + sf * (gain @ th2)
+        den = den + sf * far_den
+    o = num / den
+    return o * sigmoid_gate(np.asarray(inp["gate"][b, 0, h], np.float64),
+                            np.asarray(inp["gate_scale"][h], np.float64))
+
+
+def attend_far(inp, far, scale, hpg):
+    """Every output of a decode step with the far field: out [B][1][nh][hd]."""
+    B, t, nh, hd = inp["q"].shape
+    assert t == 1, "the far field is defined here for decode rows (t = 1)"
+    out = np.zeros((B, 1, nh, hd), np.float64)
+    for b in range(B):
+        for h in range(nh):
+            out[b, 0, h] = attend_far_row(b, h, inp, far, scale, hpg)
+    return out
+
+
+def far_commit(inp, far, scale, hpg):
+    """The far state after the decode row (o1c_tok_commit, far part): for a
+    sequence whose window was full, every landmark of every head takes the
+    evicted key into its max, mass and numerator. Returns (mz, t_hat)."""
+    B, _, nh, _ = inp["q"].shape
+    m = far["m"]
+    mz = np.array(far["mz"], np.float64, copy=True)
+    th = np.array(far["t_hat"], np.float64, copy=True)
+    for b in range(B):
+        for h in range(nh):
+            evict, mx2, z2, th2 = far_row_state(inp["meta"][b], far, b, h, h // hpg, inp, scale)
+            if evict:
+                mz[b, h, :m] = mx2
+                mz[b, h, m:] = z2
+                th[b, h] = th2
+    return mz, th

@@ -404,3 +404,144 @@ def test_rollback_batch_flags_only_invalid_sequences():
     out, bad = oracle.rollback(meta, [2, 1, 3], 8)
     assert bad.tolist() == [False, False, True]
     assert out.tolist() == [[3, 0, 0, 8], [8, 2, 1, 8], [2, 1, 0, 8]]
+
+
+# ---------------------------------------------------------------------------
+# far field of a decode row (o1c_msl.metal: o1c_tok_far, o1c_tok_merge,
+# o1c_tok_commit; dory_msl.metal: dory_ofar)
+# ---------------------------------------------------------------------------
+def test_far_eviction_running_max_and_mass_closed_forms():
+    q = np.array([1.0, 0.0, 0.0, 0.0])
+    k1, k2 = np.array([0.5, 0, 0, 0]), np.array([2.0, 0, 0, 0])
+    mx, z, rr, e = oracle.far_evict(-np.inf, 0.0, k1, q, 1.0)    # empty field
+    assert (mx, z, rr, e) == (0.5, 1.0, 0.0, 1.0)
+    mx, z, rr, e = oracle.far_evict(mx, z, k2, q, 1.0)           # larger score moves the max
+    assert mx == 2.0 and rr == pytest.approx(math.exp(-1.5)) and e == 1.0
+    assert z == pytest.approx(1.0 + math.exp(-1.5))
+    mx, z, rr, e = oracle.far_evict(mx, z, k1, q, 1.0)           # smaller score keeps it
+    assert mx == 2.0 and rr == 1.0 and e == pytest.approx(math.exp(-1.5))
+    assert z == pytest.approx(1.0 + 2 * math.exp(-1.5))
+
+
+def _far_decode_case(seed, W=6, ns=1, hd=16, nh=2, m=4):
+    g = np.random.default_rng(seed)
+    cap = W
+    pos0 = 3 * W + 2
+    meta = np.array([[W, pos0 % W, 0, W]], dtype=np.int64)
+    ring_k, ring_v = g.normal(size=(1, 1, cap, hd)), g.normal(size=(1, 1, cap, hd))
+    inp = {"meta": meta, "ring_k": ring_k, "ring_v": ring_v,
+           "sink_k": g.normal(size=(1, 1, ns, hd)), "sink_v": g.normal(size=(1, 1, ns, hd)),
+           "gate_scale": g.normal(size=(nh, hd))}
+    scale = hd ** -0.5
+    # landmark keys = the first m keys the coming steps evict (slots head0, head0 + 1, ...)
+    head0 = int(meta[0, 1])
+    kt = np.stack([ring_k[0, 0, (head0 + j) % W] for j in range(m)])[None, None]
+    qt = 2.5 * g.normal(size=(1, nh, m, hd))
+    mu = np.zeros((1, nh, m, m))
+    for h in range(nh):
+        Bm = np.exp(scale * qt[0, h] @ kt[0, 0].T)          # Bm[b][j] = exp(s <q~_b, k_j>)
+        assert np.linalg.cond(Bm) < 1e8
+        mu[0, h] = np.linalg.inv(Bm)
+    far = {"m": m, "rect": 0, "k_tilde": kt, "q_tilde": qt, "mu": mu,
+           "mz": np.concatenate([np.full((1, nh, m), -np.inf), np.zeros((1, nh, m))], axis=2),
+           "t_hat": np.zeros((1, nh, m, hd))}
+    return g, inp, far, scale
+
+
+def test_far_field_is_exact_when_the_landmarks_are_the_evicted_keys():
+    """Nystrom reconstruction is exact on its own landmarks: with k~ = the keys
+    the steps evict and mu = [exp(s <q~_b, k_j>)]^-1, every decode step equals
+    full softmax attention over the sinks, every key evicted so far and the
+    window (the far field then loses nothing)."""
+    hd, nh, hpg = 16, 2, 2
+    g, inp, far, scale = _far_decode_case(7, hd=hd, nh=nh)
+    W = 6
+    evicted_k, evicted_v = [], []
+    for step in range(far["m"]):
+        inp["q"] = g.normal(size=(1, 1, nh, hd))
+        inp["k_chunk"] = g.normal(size=(1, 1, 1, hd))
+        inp["v_chunk"] = g.normal(size=(1, 1, 1, hd))
+        inp["gate"] = g.normal(size=(1, 1, nh, hd))
+        got = oracle.attend_far(inp, far, scale, hpg)
+        meta_b = inp["meta"][0]
+        slot = int(meta_b[1]) % W
+        evicted_k.append(inp["ring_k"][0, 0, slot].copy())
+        evicted_v.append(inp["ring_v"][0, 0, slot].copy())
+        for h in range(nh):
+            keys = oracle.row_key_list(meta_b, 0, 1, W)
+            K = [inp["sink_k"][0, 0, 0]] + evicted_k
+            V = [inp["sink_v"][0, 0, 0]] + evicted_v
+            for kind, idx in keys[1:]:
+                src = (inp["ring_k"], inp["ring_v"]) if kind == "ring" else None
+                K.append(src[0][0, 0, idx] if src else inp["k_chunk"][0, idx, 0])
+                V.append(src[1][0, 0, idx] if src else inp["v_chunk"][0, idx, 0])
+            s = scale * (np.asarray(K) @ inp["q"][0, 0, h])
+            p = np.exp(s - s.max())
+            ref = (p @ np.asarray(V)) / p.sum() * oracle.sigmoid_gate(inp["gate"][0, 0, h], inp["gate_scale"][h])
+            np.testing.assert_allclose(got[0, 0, h], ref, rtol=1e-7, atol=1e-9)
+        far["mz"], far["t_hat"] = oracle.far_commit(inp, far, scale, hpg)
+        inp["ring_k"], inp["ring_v"], inp["meta"] = oracle.commit(inp["meta"], inp["ring_k"], inp["ring_v"],
+                                                                 inp["k_chunk"], inp["v_chunk"])
+        assert int(inp["meta"][0, 2]) == step + 1          # far_len counts the evictions
+
+
+def test_far_single_landmark_closed_form():
+    """m = 1: the far part is mu exp(s <q, k~>) * sum_j exp(s <q~, k_j>) (v_j, 1)
+    over the evicted keys, next to the near terms."""
+    hd, nh, hpg = 8, 1, 1
+    g, inp, far, scale = _far_decode_case(11, hd=hd, nh=nh, m=1)
+    far["mu"] = np.full((1, 1, 1, 1), 0.37)
+    inp["q"] = g.normal(size=(1, 1, nh, hd))
+    inp["k_chunk"], inp["v_chunk"] = g.normal(size=(1, 1, 1, hd)), g.normal(size=(1, 1, 1, hd))
+    inp["gate"] = np.zeros((1, 1, nh, hd))                  # sigmoid(0) = 1/2
+    got = oracle.attend_far(inp, far, scale, hpg)[0, 0, 0]
+    W = 6
+    meta_b = inp["meta"][0]
+    slot = int(meta_b[1]) % W
+    kev, vev = inp["ring_k"][0, 0, slot], inp["ring_v"][0, 0, slot]
+    q = inp["q"][0, 0, 0]
+    wfar = 0.37 * math.exp(scale * q @ far["k_tilde"][0, 0, 0]) * math.exp(scale * far["q_tilde"][0, 0, 0] @ kev)
+    num, den = wfar * vev, wfar
+    for kind, idx in oracle.row_key_list(meta_b, 0, 1, W):
+        if kind == "sink":
+            kk, vv = inp["sink_k"][0, 0, idx], inp["sink_v"][0, 0, idx]
+        elif kind == "ring":
+            kk, vv = inp["ring_k"][0, 0, idx], inp["ring_v"][0, 0, idx]
+        else:
+            kk, vv = inp["k_chunk"][0, idx, 0], inp["v_chunk"][0, idx, 0]
+        e = math.exp(scale * q @ kk)
+        num, den = num + e * vv, den + e
+    np.testing.assert_allclose(got, 0.5 * num / den, rtol=1e-10)
+
+
+def test_far_part_with_negative_mass_is_dropped_and_empty_field_adds_nothing():
+    hd, nh, hpg = 8, 2, 2
+    g, inp, far, scale = _far_decode_case(13, hd=hd, nh=nh)
+    inp["q"] = g.normal(size=(1, 1, nh, hd))
+    inp["k_chunk"], inp["v_chunk"] = g.normal(size=(1, 1, 1, hd)), g.normal(size=(1, 1, 1, hd))
+    inp["gate"] = g.normal(size=(1, 1, nh, hd))
+    near = oracle.attend(inp, scale, hpg)
+    far["mu"] = -np.abs(far["mu"]) - 0.1                    # every gain negative: far_den < 0
+    np.testing.assert_allclose(oracle.attend_far(inp, far, scale, hpg), near, rtol=1e-12)
+    inp["meta"] = np.array([[4, 0, 0, 6]])                  # not full: no eviction, far_len 0
+    near = oracle.attend(inp, scale, hpg)
+    far["mu"] = np.abs(far["mu"])
+    np.testing.assert_allclose(oracle.attend_far(inp, far, scale, hpg), near, rtol=1e-12)
+
+
+def test_far_rect_clips_negative_landmark_weights():
+    """rect (dory_ofar): w_b = max(w_b, 0). Two landmarks, mu = diag(2, -1):
+    w = (2 e^{fs_0 - f}, -e^{fs_1 - f}); clipped, only landmark 0 feeds the far
+    part, so the result equals the same state with landmark 1's mu column 0."""
+    hd, nh, hpg = 8, 1, 1
+    g, inp, far, scale = _far_decode_case(17, hd=hd, nh=nh, m=2)
+    inp["q"] = g.normal(size=(1, 1, nh, hd))
+    inp["k_chunk"], inp["v_chunk"] = g.normal(size=(1, 1, 1, hd)), g.normal(size=(1, 1, 1, hd))
+    inp["gate"] = g.normal(size=(1, 1, nh, hd))
+    far["mu"] = np.array([[[[2.0, 0.0], [0.0, -1.0]]]])
+    clipped = dict(far, rect=1)
+    zeroed = dict(far, mu=np.array([[[[2.0, 0.0], [0.0, 0.0]]]]))
+    a = oracle.attend_far(inp, clipped, scale, hpg)
+    b = oracle.attend_far(inp, zeroed, scale, hpg)
+    np.testing.assert_allclose(a, b, rtol=1e-12)
+    assert not np.allclose(oracle.attend_far(inp, far, scale, hpg), a)
