@@ -168,6 +168,40 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  *
  * Errors: SWA_E_NULL, SWA_E_SHAPE, SWA_E_ALIGN, SWA_E_WORKSPACE, SWA_E_CUDA.
  */
+/* Far field of a decode step ("o1c_msl.metal", cortiq-engine 0.8.79:
+ * o1c_tok_far, o1c_tok_merge, o1c_tok_commit; the clip of "dory_msl.metal"
+ * dory_ofar). Keys that leave the window are not dropped: every query head
+ * keeps m landmarks, each with a running max, mass and numerator of the keys
+ * evicted so far, scored against the landmark's query. A row adds to its
+ * window the far part: landmark scores s * <q, k~_a> give weights
+ * w_b = sum_a exp(fs_a - f) mu[a][b] (clipped at 0 when rect), gains
+ * gain_b = w_b exp(f + max_b - fm), far mass sum_b gain_b mass_b and far
+ * numerator sum_b gain_b num_b, joined to the near softmax under a common
+ * exponent; a negative far mass drops the far part. The row of a full window
+ * evicts its oldest key (ring slot win_head) into every landmark first.
+ * Per sequence (the pages hold one), all f32, device memory:
+ *   k_tilde [B][nk][m][hd]  landmark keys (16-byte aligned)
+ *   q_tilde [B][nh][m][hd]  landmark queries (16-byte aligned)
+ *   mu      [B][nh][m][m]   landmark weight matrix, row a, column b
+ *   mz      [B][nh][2m]     per landmark: running max (score units, -inf when
+ *                           empty), then mass; rewritten iff commit = 1
+ *   t_hat   [B][nh][m][hd]  per landmark numerator (16-byte aligned);
+ *                           rewritten iff commit = 1
+ * 1 <= m <= 32. Only decode steps (t = 1) take a far field. The evicted key
+ * must still be in the ring: do not let swa_prep write the ring in such a
+ * step (pass ring_k = ring_v = NULL there) and commit through swa_attend.
+ * meta.far_len counts the evicted keys; with far_len = 0 and no eviction the
+ * far part is empty. */
+typedef struct swa_far_args {
+  int m;                         /* landmarks per query head, 1..32          */
+  int rect;                      /* 1: clip negative landmark weights at 0   */
+  const float* k_tilde;
+  const float* q_tilde;
+  const float* mu;
+  float* mz;
+  float* t_hat;
+} swa_far_args;
+
 typedef struct swa_attend_args {
   int B, t, nh, nk, hd, cap, ns;
   float scale;                   /* score scale (e.g. 1/sqrt(hd))           */
@@ -190,6 +224,7 @@ typedef struct swa_attend_args {
   uint32_t* err;                 /* optional device error word              */
   cudaEvent_t ev_start;          /* optional                                */
   cudaEvent_t ev_stop;           /* optional                                */
+  const swa_far_args* far;       /* optional far field (t = 1), host struct */
 } swa_attend_args;
 
 /* Bytes of workspace swa_attend needs for these sizes (reads B, t, nh, nk,

@@ -117,8 +117,13 @@ def _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits=0) -> _abi.AttendArgs:
     return a
 
 
-def attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits: int = 0) -> int:
+def attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits: int = 0, far_m: int = 0) -> int:
+    """Workspace bytes of swa_attend; far_m > 0 sizes it for a far field."""
     a = _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits)
+    fa = _abi.FarArgs()
+    if far_m:
+        fa.m = int(far_m)
+        a.far = ctypes.pointer(fa)
     n = int(library().swa_attend_workspace_size(ctypes.byref(a)))
     if n == 0:
         raise SwaError(_abi.SWA_E_SHAPE, "swa_attend_workspace_size")
@@ -127,15 +132,21 @@ def attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits: int = 0) -> int
 
 def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate_scale,
            scale: float, *, out=None, workspace=None, commit: bool = False, meta_out=None,
-           num_splits: int = 0, err=None, ev_start=None, ev_stop=None, stream=None):
-    """Attention of a chunk (decode, verify or prompt); see include/swa.h."""
+           num_splits: int = 0, err=None, ev_start=None, ev_stop=None, far=None, stream=None):
+    """Attention of a chunk (decode, verify or prompt); see include/swa.h.
+
+    far: optional far field of a decode step (t = 1), a dict with m, rect and
+    the device tensors k_tilde [B][nk][m][hd], q_tilde [B][nh][m][hd],
+    mu [B][nh][m][m], mz [B][nh][2m], t_hat [B][nh][m][hd] (mz and t_hat are
+    updated in place when commit)."""
     B, t, nh, hd = q.shape
     nk = k_chunk.shape[2]
     cap = ring_k.shape[2]
     ns = sink_k.shape[2] if sink_k is not None else 0
     if out is None:
         out = torch.empty_like(q)
-    need = attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits)
+    far_m = int(far["m"]) if far is not None else 0
+    need = attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits, far_m)
     if workspace is None:
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     a = _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits)
@@ -158,6 +169,17 @@ def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate
     a.err = _ptr(err, "err", (1,), torch.int32, required=False)
     a.ev_start = ctypes.c_void_p(ev_start.cuda_event) if ev_start is not None else None
     a.ev_stop = ctypes.c_void_p(ev_stop.cuda_event) if ev_stop is not None else None
+    fa = None
+    if far is not None:
+        m = far_m
+        fa = _abi.FarArgs()
+        fa.m, fa.rect = m, 1 if far.get("rect") else 0
+        fa.k_tilde = _ptr(far["k_tilde"], "k_tilde", (B, nk, m, hd))
+        fa.q_tilde = _ptr(far["q_tilde"], "q_tilde", (B, nh, m, hd))
+        fa.mu = _ptr(far["mu"], "mu", (B, nh, m, m))
+        fa.mz = _ptr(far["mz"], "mz", (B, nh, 2 * m))
+        fa.t_hat = _ptr(far["t_hat"], "t_hat", (B, nh, m, hd))
+        a.far = ctypes.pointer(fa)
     rc = library().swa_attend(ctypes.byref(a), _stream(stream))
     _abi.check(rc, "swa_attend")
     return out
@@ -187,7 +209,7 @@ class TokenPath:
 
     def __init__(self, *, B, t, nh, nk, hd, cap, ns, window=None, q_scale, gate_scale,
                  ring_k, ring_v, sink_k, sink_v, meta, pos0, scale=None, eps=1e-6,
-                 theta=10000.0, device="cuda", num_splits=0):
+                 theta=10000.0, device="cuda", num_splits=0, far=None):
         self.B, self.t, self.nh, self.nk, self.hd, self.cap, self.ns = B, t, nh, nk, hd, cap, ns
         self.scale = float(scale) if scale is not None else hd ** -0.5
         self.eps, self.theta = float(eps), float(theta)
@@ -206,8 +228,17 @@ class TokenPath:
         self.q = torch.empty(B, t, nh, hd, **f32)
         self.k = torch.empty(B, t, nk, hd, **f32)
         self.out = torch.empty(B, t, nh, hd, **f32)
-        self.workspace = torch.empty(attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits),
-                                     device=dev, dtype=torch.uint8)
+        # far field of decode steps: landmark state on the device (mz and t_hat
+        # advance with every committed step)
+        self.far = None
+        if far is not None:
+            self.far = {"m": int(far["m"]), "rect": int(far.get("rect", 0))}
+            for key in ("k_tilde", "q_tilde", "mu", "mz", "t_hat"):
+                self.far[key] = far[key].to(**f32).contiguous()
+        self.workspace = torch.empty(
+            attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits,
+                                  self.far["m"] if self.far else 0),
+            device=dev, dtype=torch.uint8)
         self.err = torch.zeros(1, device=dev, dtype=torch.int32)
         self.in_bufs = {
             "yq": torch.empty(B, t, nh, hd, **f32), "yk": torch.empty(B, t, nk, hd, **f32),
@@ -225,14 +256,16 @@ class TokenPath:
             for name, x in (("yq", yq), ("yk", yk), ("yv", yv), ("gate", gate)):
                 self.in_bufs[name].copy_(x, non_blocking=True)
             yq, yk, yv, gate = (self.in_bufs[n] for n in ("yq", "yk", "yv", "gate"))
-        ring = self.t == 1
+        # the prep writes the ring for single rows, except with a far field:
+        # that step's eviction still reads the evicted slot, so the commit does
+        ring = self.t == 1 and self.far is None
         q, k, v = prep(yq, yk, yv, None, self.q_scale, self.eps, pos0=self.pos0, theta=self.theta,
                        ring_k=self.ring_k if ring else None, ring_v=self.ring_v if ring else None,
                        q_out=self.q, k_out=self.k, copy_v=False, stream=stream)
         attend(self.meta, q, k, v, self.ring_k, self.ring_v, self.sink_k, self.sink_v, gate,
                self.gate_scale, self.scale, out=self.out, workspace=self.workspace,
                commit=commit, meta_out=self.meta_next, num_splits=self.num_splits, err=self.err,
-               ev_start=ev_start, ev_stop=ev_stop, stream=stream)
+               ev_start=ev_start, ev_stop=ev_stop, far=self.far, stream=stream)
         if host:
             if out_host is None:
                 return self.out.to("cpu")

@@ -33,6 +33,14 @@ class PrepArgs(ctypes.Structure):
     ]
 
 
+class FarArgs(ctypes.Structure):
+    _fields_ = [
+        ("m", ctypes.c_int), ("rect", ctypes.c_int),
+        ("k_tilde", ctypes.c_void_p), ("q_tilde", ctypes.c_void_p), ("mu", ctypes.c_void_p),
+        ("mz", ctypes.c_void_p), ("t_hat", ctypes.c_void_p),
+    ]
+
+
 class AttendArgs(ctypes.Structure):
     _fields_ = [
         ("B", ctypes.c_int), ("t", ctypes.c_int), ("nh", ctypes.c_int), ("nk", ctypes.c_int),
@@ -45,6 +53,7 @@ class AttendArgs(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("commit", ctypes.c_int), ("meta_out", c_float_p), ("num_splits", ctypes.c_int),
         ("err", c_float_p), ("ev_start", ctypes.c_void_p), ("ev_stop", ctypes.c_void_p),
+        ("far", ctypes.POINTER(FarArgs)),
     ]
 
 

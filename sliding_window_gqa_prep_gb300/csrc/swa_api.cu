@@ -44,6 +44,7 @@ static int attend_shape_ok(const swa_attend_args* a) {
   if (a->nh % a->nk != 0) return 0;
   if (a->nh / a->nk > 32) return 0;
   if (a->num_splits < 0) return 0;
+  if (a->far && (a->t != 1 || a->far->m < 1 || a->far->m > 32)) return 0;
   return 1;
 }
 
@@ -66,6 +67,13 @@ static int cached_occupancy(int hd, int nq) {
 // CTAs over the SMs: it minimises (waves of resident CTAs) x (keys per CTA +
 // a fixed per-CTA cost), with the keys of a row block bounded by
 // ns + cap + rows - 1 (the window never exceeds cap).
+// Far records after the rest of the workspace: per (sequence, query head) the
+// far exponent, mass, a keep flag and the far numerator.
+static void add_far_records(const swa_attend_args* a, AttendPlan* p) {
+  p->off_far = p->ws_bytes;
+  if (a->far) p->ws_bytes += (((size_t)a->B * a->nh * (4 + a->hd) * sizeof(float)) + 255) & ~(size_t)255;
+}
+
 bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   if (!attend_shape_ok(a)) return false;
   const int hpg = a->nh / a->nk;
@@ -92,6 +100,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
     p->off_nsplit = p->off_ml + up(ml_bytes);
     p->off_meta = p->off_nsplit + up(ns_bytes);
     p->ws_bytes = p->off_meta + up((size_t)a->B * sizeof(swa_meta));
+    add_far_records(a, p);
     return true;
   }
   int rows = 32 / hpg;
@@ -135,6 +144,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   p->off_nsplit = p->off_ml + up(ml_bytes);
   p->off_meta = p->off_nsplit + up(ns_bytes);
   p->ws_bytes = p->off_meta + up((size_t)a->B * sizeof(swa_meta));
+  add_far_records(a, p);
   return true;
 }
 
@@ -226,7 +236,12 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
     return SWA_E_NULL;
   if (a->ns > 0 && (!a->sink_k || !a->sink_v)) return SWA_E_NULL;
   if (a->commit && !a->meta_out) return SWA_E_NULL;
+  if (a->far && (!a->far->k_tilde || !a->far->q_tilde || !a->far->mu || !a->far->mz || !a->far->t_hat))
+    return SWA_E_NULL;
   if (!attend_shape_ok(a)) return SWA_E_SHAPE;
+  if (a->far && (!aligned16(a->far->k_tilde) || !aligned16(a->far->q_tilde) || !aligned16(a->far->t_hat) ||
+                 (reinterpret_cast<uintptr_t>(a->far->mu) & 3u) || (reinterpret_cast<uintptr_t>(a->far->mz) & 3u)))
+    return SWA_E_ALIGN;
   if (!(a->scale == a->scale) || std::isinf(a->scale)) return SWA_E_SHAPE;
   const void* ptrs[] = {a->q, a->k_chunk, a->v_chunk, a->ring_k, a->ring_v, a->sink_k,
                         a->sink_v, a->gate, a->gate_scale, a->out};
@@ -263,7 +278,22 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   p.err = a->err;
   p.nq = plan.nq; p.rows = plan.rows; p.n_rb = plan.n_rb; p.chunk = plan.chunk;
   p.splits = plan.splits;
-  int rc = launch_attend_partial(p, stream, a->ev_start, a->ev_stop);
+  p.scale = a->scale;
+  p.far = a->far ? 1 : 0;
+  p.far_m = a->far ? a->far->m : 0;
+  p.far_rect = a->far ? (a->far->rect != 0) : 0;
+  p.k_tilde = a->far ? a->far->k_tilde : nullptr;
+  p.q_tilde = a->far ? a->far->q_tilde : nullptr;
+  p.mu = a->far ? a->far->mu : nullptr;
+  p.mz = a->far ? a->far->mz : nullptr;
+  p.t_hat = a->far ? a->far->t_hat : nullptr;
+  p.ws_far = reinterpret_cast<float*>(ws + plan.off_far);
+  int rc = SWA_OK;
+  if (p.far) {            // before the attention: it reads the evicted ring slot, which the commit overwrites
+    rc = launch_far(p, stream);
+    if (rc != SWA_OK) return rc;
+  }
+  rc = launch_attend_partial(p, stream, a->ev_start, a->ev_stop);
   if (rc != SWA_OK) return rc;
   return launch_attend_merge(p, stream);
 }

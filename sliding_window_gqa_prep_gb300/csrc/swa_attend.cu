@@ -60,6 +60,9 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
   for (int s0 = lane; s0 < nval; s0 += 32) M = fmaxf(M, p.ws_ml[(item0 + s0) * p.nq + q].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float* far_rec = p.far ? p.ws_far + ((size_t)b * p.nh + h) * (4 + HD) : nullptr;
+  const bool far_on = far_rec && far_rec[2] > 0.5f;
+  if (far_on) M = fmaxf(M, far_rec[0]);
   float4 acc[PER];
 #pragma unroll
   for (int c = 0; c < PER; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -96,6 +99,12 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
       const float4 a = s_acc[w][d4];
       t.x += a.x; t.y += a.y; t.z += a.z; t.w += a.w;
       dsum += s_den[w];
+    }
+    if (far_on) {
+      const float sf = exp2f(far_rec[0] - M);
+      const float4 a = *reinterpret_cast<const float4*>(far_rec + 4 + d4 * 4);
+      t.x += a.x * sf; t.y += a.y * sf; t.z += a.z * sf; t.w += a.w * sf;
+      dsum += far_rec[1] * sf;
     }
     *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) = gated(p, row, h, d4, HD, t, 1.0f / dsum);
   }
@@ -172,6 +181,10 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
     if (s0 + lane < nval) M = fmaxf(M, p.ws_ml[(item0 + s0 + lane) * p.nq + q].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  // the far part of a decode row joins under the common exponent (o1c_tok_merge)
+  const float* far_rec = p.far ? p.ws_far + ((size_t)b * p.nh + h) * (4 + HD) : nullptr;
+  const bool far_on = far_rec && far_rec[2] > 0.5f;
+  if (far_on) M = fmaxf(M, far_rec[0]);
   float den = 0.f;
   float4 acc[PER];
 #pragma unroll
@@ -203,6 +216,18 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  if (far_on) {
+    const float sf = exp2f(far_rec[0] - M);
+    den += far_rec[1] * sf;
+#pragma unroll
+    for (int c = 0; c < PER; ++c) {
+      const int d4 = c * 32 + lane;
+      if (d4 < D4) {
+        const float4 a = *reinterpret_cast<const float4*>(far_rec + 4 + d4 * 4);
+        acc[c].x += a.x * sf; acc[c].y += a.y * sf; acc[c].z += a.z * sf; acc[c].w += a.w * sf;
+      }
+    }
+  }
   const float inv = 1.0f / den;
 #pragma unroll
   for (int c = 0; c < PER; ++c) {

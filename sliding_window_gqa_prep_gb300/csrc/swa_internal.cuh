@@ -32,6 +32,7 @@ struct AttendPlan {
   size_t off_ml;   // byte offset of the (m, l) records
   size_t off_nsplit; // byte offset of the per-(b, rb) valid-split counts
   size_t off_meta;   // byte offset of the per-sequence copy of the meta before the chunk
+  size_t off_far;    // byte offset of the far records [B][nh] x (4 + hd) floats (far field only)
 };
 bool make_plan(const swa_attend_args* a, AttendPlan* p);
 
@@ -59,10 +60,20 @@ struct AttendParams {
   swa_meta* meta_out;
   uint32_t* err;
   int nq, rows, n_rb, chunk, splits;
+  // far field (decode rows): far == 0 means none
+  int far, far_m, far_rect;
+  const float* k_tilde;       // [B][nk][m][hd]
+  const float* q_tilde;       // [B][nh][m][hd]
+  const float* mu;            // [B][nh][m][m]
+  float* mz;                  // [B][nh][2m]
+  float* t_hat;               // [B][nh][m][hd]
+  float* ws_far;              // [B][nh] x (fm in log2 units, far mass, have, 0, numerator[hd])
+  float scale;                // score scale in natural units (the far state's units)
 };
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int launch_attend_merge(const AttendParams& p, cudaStream_t s);
+int launch_far(const AttendParams& p, cudaStream_t s);
 int launch_rollback(swa_meta* meta, const int32_t* n_back, int B, int cap, uint32_t* err,
                     cudaStream_t s);
 int attend_partial_occupancy(int hd, int nq);   // resident CTAs per SM

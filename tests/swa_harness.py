@@ -40,13 +40,23 @@ def to_dev(inp, dev="cuda"):
     return out
 
 
-def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_alias=False):
+def far_to_dev(far, dev="cuda"):
+    return {k: (v.to(dev).contiguous() if torch.is_tensor(v) else v) for k, v in far.items()}
+
+
+def far_to_np(far):
+    return {k: (v.numpy().astype(np.float64) if torch.is_tensor(v) else v) for k, v in far.items()}
+
+
+def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_alias=False, far=None):
     """rope table -> prep -> attend (+ commit) on the GPU. The prep writes the
-    ring only for t == 1 with window == cap (prep's slot map); otherwise the
-    attend's commit does."""
-    d = to_dev(inp)
+    ring only for t == 1 with window == cap (prep's slot map) and no far field;
+    otherwise the attend's commit does. far: the generator's far state (CPU);
+    the result then holds the far state after the call."""
+    d = {k: v for k, v in to_dev({k: v for k, v in inp.items() if k != "far"}).items()}
+    far_d = far_to_dev(far) if far is not None else None
     if prep_ring is None:
-        prep_ring = w.t == 1 and w.window == w.cap
+        prep_ring = w.t == 1 and w.window == w.cap and far is None
     rope = swa.rope_table(d["pos0"], w.t, w.hd, w.theta)
     ring_k, ring_v = d["ring_k"].clone(), d["ring_v"].clone()
     q, k, v = swa.prep(d["yq"], d["yk"], d["yv"], rope, d["q_scale"], w.eps, pos0=d["pos0"],
@@ -58,13 +68,15 @@ def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_ali
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = swa.attend(meta, q, k, v, ring_k, ring_v, d["sink_k"] if w.ns else None,
                      d["sink_v"] if w.ns else None, d["gate"], d["gate_scale"], w.score_scale,
-                     commit=commit, meta_out=meta_out, num_splits=num_splits, err=err)
+                     commit=commit, meta_out=meta_out, num_splits=num_splits, err=err, far=far_d)
     torch.cuda.synchronize()
     return {
         "rope": rope.cpu().numpy(), "q": q.cpu().numpy(), "k": k.cpu().numpy(),
         "v": v.cpu().numpy(), "out": out.cpu().numpy(), "ring_k": ring_k.cpu().numpy(),
         "ring_v": ring_v.cpu().numpy(), "meta_out": meta_out.cpu().numpy(),
         "err": int(err.item()),
+        "far": None if far_d is None else {k: (v.cpu().numpy() if torch.is_tensor(v) else v)
+                                          for k, v in far_d.items()},
         "ring_after_prep_k": None if ring_after_prep_k is None else ring_after_prep_k.cpu().numpy(),
     }
 

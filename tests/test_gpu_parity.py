@@ -12,8 +12,8 @@ import torch
 import oracle
 import workloads
 import sliding_window_gqa_prep_gb300 as swa
-from swa_harness import (assert_close, check_commit_placement, gpu_full_path, oracle_inputs,
-                         to_dev)
+from swa_harness import (assert_close, check_commit_placement, far_to_dev, far_to_np,
+                         gpu_full_path, oracle_inputs, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -112,6 +112,14 @@ ATTEND_CASES = [
     dict(B=2, t=33, nh=12, nk=2, hd=64, window=20, cap=20, ns=1, pos_mode="full", pos_lo=20, pos_hi=900),
     # tensor-core prompt path: empty ring, hpg 4, several key tiles
     dict(B=2, t=70, nh=8, nk=2, hd=128, window=64, cap=64, ns=0, pos_mode="prompt", pos_lo=0, pos_hi=200),
+    # every remaining attention-kernel instance: decode with 8 query vectors
+    # (hd 64 / 128 / 256), verify with 16 and 32 (hd 64) and 16 (hd 256)
+    dict(B=2, t=2, nh=8, nk=2, hd=64, window=80, cap=80, ns=2, pos_mode="full", pos_lo=80, pos_hi=900),
+    dict(B=2, t=2, nh=8, nk=2, hd=128, window=70, cap=70, ns=1, pos_mode="partial", pos_lo=1, pos_hi=70),
+    dict(B=2, t=2, nh=8, nk=2, hd=256, window=50, cap=50, ns=3, pos_mode="full", pos_lo=50, pos_hi=700),
+    dict(B=3, t=8, nh=8, nk=2, hd=64, window=120, cap=120, ns=4, pos_mode="partial", pos_lo=1, pos_hi=120),
+    dict(B=2, t=4, nh=8, nk=2, hd=64, window=90, cap=90, ns=0, pos_mode="full", pos_lo=90, pos_hi=999),
+    dict(B=2, t=4, nh=8, nk=2, hd=256, window=75, cap=75, ns=2, pos_mode="full", pos_lo=75, pos_hi=800),
     # mid-size chunks (64 <= rows x heads < 128): the 64-vector mma.sync path
     dict(B=2, t=20, nh=8, nk=2, hd=128, window=90, cap=90, ns=2, pos_mode="full", pos_lo=90, pos_hi=900),
     dict(B=2, t=12, nh=16, nk=2, hd=64, window=30, cap=30, ns=1, pos_mode="partial", pos_lo=1, pos_hi=30),
@@ -368,18 +376,121 @@ def test_rollback_after_verify_commit_equals_committing_the_accepted_prefix():
 
 
 # ---------------------------------------------------------------------------
+# far field of decode rows (o1c_tok_far, o1c_tok_merge, o1c_tok_commit)
+# ---------------------------------------------------------------------------
+def _far_case(seed, **kw):
+    base = dict(B=4, t=1, nh=8, nk=2, hd=128, window=96, cap=96, ns=3, pos_mode="partial",
+                pos_lo=40, pos_hi=96, far_m=16, seed=seed)
+    base.update(kw)
+    w = workloads.custom(**base)
+    inp = workloads.make_inputs(w)
+    # sequences 1.. are partial (no eviction); give one of them evictions behind it
+    inp["meta"][1, 2] = 7
+    inp["far"]["mz"][1, :, :w.far_m] = torch.randn(w.nh, w.far_m, generator=torch.Generator().manual_seed(seed))
+    inp["far"]["mz"][1, :, w.far_m:] = 3.0
+    return w, inp
+
+
+def _check_far_state(w, inp, res, atol=2e-5):
+    far_ref = far_to_np(inp["far"])
+    mz_ref, th_ref = oracle.far_commit(oracle_inputs(w, inp, *_gpu_prepped(res)), far_ref, w.score_scale, w.hpg)
+    got_mz, got_th = res["far"]["mz"].astype(np.float64), res["far"]["t_hat"].astype(np.float64)
+    fin = np.isfinite(mz_ref)
+    assert np.array_equal(fin, np.isfinite(got_mz))
+    assert_close(got_mz[fin], mz_ref[fin], "far max / mass", max_abs=2e-4, max_rel=1e-5)
+    assert_close(got_th, th_ref, "far numerators", max_abs=1e-3, max_rel=1e-5)
+
+
+def _gpu_prepped(res):
+    return res["q"], res["k"], res["v"]
+
+
+@pytest.mark.parametrize("rect", [0, 1])
+@pytest.mark.parametrize("splits", [0, 1, 64])
+def test_far_decode_step_matches_oracle(rect, splits):
+    w, inp = _far_case(41)
+    inp["far"]["rect"] = rect
+    inp["far"]["mu"] = inp["far"]["mu"] - 0.05       # some negative landmark weights for the clip
+    res = gpu_full_path(w, inp, commit=True, num_splits=splits, far=inp["far"])
+    assert res["err"] == 0
+    a = oracle_inputs(w, inp, *_gpu_prepped(res))
+    ref = oracle.attend_far(a, far_to_np(inp["far"]), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, "out (far field)")
+    check_commit_placement(w, inp, res)
+    _check_far_state(w, inp, res)
+
+
+def test_far_part_with_negative_mass_is_dropped_on_gpu():
+    w, inp = _far_case(43)
+    inp["far"]["mu"] = -inp["far"]["mu"].abs() - 0.1
+    res = gpu_full_path(w, inp, commit=False, far=inp["far"])
+    a = oracle_inputs(w, inp, *_gpu_prepped(res))
+    assert_close(res["out"], oracle.attend(a, w.score_scale, w.hpg), "out (far mass < 0)")
+    # without commit the far state is left as it was
+    np.testing.assert_array_equal(res["far"]["t_hat"], inp["far"]["t_hat"].numpy())
+
+
+def test_far_field_exact_over_decode_steps_with_landmarks_at_the_evicted_keys():
+    """GPU version of the Nystrom pin: the landmarks are the keys the next
+    steps evict and mu inverts their kernel matrix, so every step must equal
+    the oracle's far-field step (itself pinned to full attention over every
+    evicted key) while the far state advances through the GPU's commits."""
+    hd, nh, nk, m, W = 64, 4, 2, 4, 12
+    w = workloads.custom(B=2, t=1, nh=nh, nk=nk, hd=hd, window=W, cap=W, ns=1, pos_mode="full",
+                         pos_lo=W, pos_hi=5 * W, seed=47)
+    inp = workloads.make_inputs(w)
+    inp["meta"][:, 2] = 0                               # nothing evicted yet
+    rng = np.random.default_rng(5)
+    scale = w.score_scale
+    kt = np.zeros((w.B, nk, m, hd))
+    qt = 1.5 * rng.normal(size=(w.B, nh, m, hd))
+    mu = np.zeros((w.B, nh, m, m))
+    for b in range(w.B):
+        head0 = int(inp["meta"][b, 1])
+        for g in range(nk):
+            kt[b, g] = inp["ring_k"][b, g, [(head0 + j) % W for j in range(m)]].numpy()
+        for h in range(nh):
+            mu[b, h] = np.linalg.inv(np.exp(scale * qt[b, h] @ kt[b, h // w.hpg].T))
+    far_np = {"m": m, "rect": 0, "k_tilde": kt, "q_tilde": qt, "mu": mu,
+              "mz": np.concatenate([np.full((w.B, nh, m), -np.inf), np.zeros((w.B, nh, m))], axis=2),
+              "t_hat": np.zeros((w.B, nh, m, hd))}
+    far_d = {k: (torch.tensor(v, dtype=torch.float32).cuda() if isinstance(v, np.ndarray) else v)
+             for k, v in far_np.items()}
+    d = to_dev({k: v for k, v in inp.items() if k != "far"})
+    ring_k, ring_v, meta = d["ring_k"].clone(), d["ring_v"].clone(), d["meta"].clone()
+    g = torch.Generator().manual_seed(9)
+    for step in range(m):
+        q = torch.randn(w.B, 1, nh, hd, generator=g)
+        k = torch.randn(w.B, 1, nk, hd, generator=g)
+        v = torch.randn(w.B, 1, nk, hd, generator=g)
+        gate = torch.randn(w.B, 1, nh, hd, generator=g)
+        a = {"meta": meta.cpu().numpy().astype(np.int64), "q": q.numpy(), "k_chunk": k.numpy(),
+             "v_chunk": v.numpy(), "ring_k": ring_k.cpu().numpy(), "ring_v": ring_v.cpu().numpy(),
+             "sink_k": inp["sink_k"].numpy(), "sink_v": inp["sink_v"].numpy(), "gate": gate.numpy(),
+             "gate_scale": inp["gate_scale"].numpy()}
+        ref = oracle.attend_far(a, far_np, scale, w.hpg)
+        meta_next = torch.empty_like(meta)
+        out = swa.attend(meta, q.cuda(), k.cuda(), v.cuda(), ring_k, ring_v, d["sink_k"], d["sink_v"],
+                         gate.cuda(), d["gate_scale"], scale, commit=True, meta_out=meta_next, far=far_d)
+        assert_close(out.cpu().numpy(), ref, f"far step {step}")
+        far_np["mz"], far_np["t_hat"] = oracle.far_commit(a, far_np, scale, w.hpg)
+        meta = meta_next
+        assert int(meta[0, 2].item()) == step + 1
+
+
+# ---------------------------------------------------------------------------
 # the five named workloads at full size, in the launch configuration the bench
 # times (automatic splits): every prep output, sampled attention outputs
 # ---------------------------------------------------------------------------
 SAMPLES = {"tiny_decode": 16, "batched_decode": 24, "spec_verify": 24, "prompt_chunk": 24,
-           "long_decode": 10}
+           "long_decode": 10, "batched_decode_far": 24}
 
 
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
 def test_named_workload_full_size(name):
     w = workloads.WORKLOADS[name]
     inp = workloads.make_inputs(w)
-    res = gpu_full_path(w, inp, commit=True)
+    res = gpu_full_path(w, inp, commit=True, far=inp.get("far"))
     assert res["err"] == 0
     rope = oracle.rope_table(inp["pos0"].numpy(), w.t, w.hd, w.theta)
     q, k, v = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope,
@@ -392,7 +503,11 @@ def test_named_workload_full_size(name):
     while len(picks) < SAMPLES[name]:
         picks.append((int(rng.integers(w.B)), int(rng.integers(w.t)), int(rng.integers(w.nh))))
     got = np.stack([res["out"][b, i, h] for b, i, h in picks])
-    ref = np.stack([oracle.attend_row(b, i, h, a, w.score_scale, w.hpg) for b, i, h in picks])
+    if w.far_m:
+        far = far_to_np(inp["far"])
+        ref = np.stack([oracle.attend_far_row(b, h, a, far, w.score_scale, w.hpg) for b, i, h in picks])
+    else:
+        ref = np.stack([oracle.attend_row(b, i, h, a, w.score_scale, w.hpg) for b, i, h in picks])
     assert_close(got, ref, f"{name} sampled out")
     # every output is finite and the meta after the commit is exact for all sequences
     assert np.all(np.isfinite(res["out"]))

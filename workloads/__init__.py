@@ -42,6 +42,7 @@ class Workload:
     theta: float = 10000.0
     eps: float = 1e-6
     scale: Optional[float] = None   # None -> 1/sqrt(hd)
+    far_m: int = 0                  # landmarks of a far field (decode rows), 0 = none
 
     @property
     def hpg(self) -> int:
@@ -53,7 +54,8 @@ class Workload:
 
 
 # The five workloads of the method's token path (decode token, batched decode,
-# speculative verify, prompt chunk, long-window decode).
+# speculative verify, prompt chunk, long-window decode), and batched decode with
+# the far field of the sealed layer.
 WORKLOADS: Dict[str, Workload] = {
     "tiny_decode": Workload("tiny_decode", B=1, t=1, nh=8, nk=2, hd=64, window=32, cap=32,
                             ns=0, seed=0, pos_mode="fixed", pos_lo=100),
@@ -67,6 +69,11 @@ WORKLOADS: Dict[str, Workload] = {
     "long_decode": Workload("long_decode", B=16, t=1, nh=8, nk=2, hd=256, window=32768,
                             cap=32768, ns=8, seed=4, pos_mode="full", pos_lo=32768,
                             pos_hi=131072),
+    # batched_decode with the sealed layer's far field: 32 landmarks per query head
+    "batched_decode_far": Workload("batched_decode_far", B=64, t=1, nh=16, nk=4, hd=128,
+                                   window=4096, cap=4096, ns=4, seed=5, pos_mode="full",
+                                   pos_lo=4096, pos_hi=20000, scale=1.0 / math.sqrt(128.0),
+                                   far_m=32),
 }
 
 
@@ -133,6 +140,29 @@ def make_inputs(w: Workload, seed: Optional[int] = None, batch: Optional[int] = 
         "sink_k": torch.randn(B, nk, w.ns, hd, generator=g),
         "sink_v": torch.randn(B, nk, w.ns, hd, generator=g),
     }
+    if w.far_m:
+        # far field state (drawn after everything above): landmark keys and
+        # queries ~ N(0, 1); mu = identity + N(0, 0.02^2); per landmark a
+        # running max ~ N(0, 1), a mass ~ U(1, 50) and a numerator ~ N(0, 1).
+        # Sequences that have evicted nothing yet (far_len = 0) hold the empty
+        # state: max -inf, mass 0, numerator 0.
+        m = w.far_m
+        mx = torch.randn(B, nh, m, generator=g)
+        z = torch.rand(B, nh, m, generator=g) * 49.0 + 1.0
+        far = {
+            "m": m, "rect": 0,
+            "k_tilde": torch.randn(B, nk, m, hd, generator=g),
+            "q_tilde": torch.randn(B, nh, m, hd, generator=g),
+            "mu": torch.eye(m).expand(B, nh, m, m) + 0.02 * torch.randn(B, nh, m, m, generator=g),
+            "t_hat": torch.randn(B, nh, m, hd, generator=g),
+        }
+        empty = (meta[:, 2] == 0).view(B, 1, 1)
+        mx = torch.where(empty, torch.full_like(mx, -math.inf), mx)
+        z = torch.where(empty, torch.zeros_like(z), z)
+        far["t_hat"] = torch.where(empty.unsqueeze(-1), torch.zeros_like(far["t_hat"]), far["t_hat"])
+        far["mz"] = torch.cat([mx, z], dim=2).contiguous()
+        far["mu"] = far["mu"].contiguous()
+        out["far"] = far
     return out
 
 
