@@ -200,10 +200,14 @@ def oracle_prep_seq(w, inp, b):
     rope = oracle.rope_table(inp["pos0"].numpy()[b:b + 1], w.t, w.hd, w.theta)
     q, k, v = oracle.prep(inp["yq"].numpy()[b:b + 1], inp["yk"].numpy()[b:b + 1],
                           inp["yv"].numpy()[b:b + 1], rope, inp["q_scale"].numpy(), w.eps)
-    return {"meta": inp["meta"].numpy()[b:b + 1], "q": q, "k_chunk": k, "v_chunk": v,
-            "ring_k": inp["ring_k"].numpy()[b:b + 1], "ring_v": inp["ring_v"].numpy()[b:b + 1],
-            "sink_k": inp["sink_k"].numpy()[b:b + 1], "sink_v": inp["sink_v"].numpy()[b:b + 1],
-            "gate": inp["gate"].numpy()[b:b + 1], "gate_scale": inp["gate_scale"].numpy()}
+    a = {"meta": inp["meta"].numpy()[b:b + 1], "q": q, "k_chunk": k, "v_chunk": v,
+         "ring_k": inp["ring_k"].numpy()[b:b + 1], "ring_v": inp["ring_v"].numpy()[b:b + 1],
+         "sink_k": inp["sink_k"].numpy()[b:b + 1], "sink_v": inp["sink_v"].numpy()[b:b + 1],
+         "gate": inp["gate"].numpy()[b:b + 1], "gate_scale": inp["gate_scale"].numpy()}
+    if "far" in inp:              # the sequence's far field state
+        a["far"] = {k: (v.numpy()[b:b + 1].astype(np.float64) if torch.is_tensor(v) else v)
+                    for k, v in inp["far"].items()}
+    return a
 
 
 def oracle_unit(w, a, i, g):
@@ -211,7 +215,10 @@ def oracle_unit(w, a, i, g):
     returns the attended KV-keys of the unit."""
     import oracle
     for h in range(g * w.hpg, (g + 1) * w.hpg):
-        oracle.attend_row(0, i, h, a, w.score_scale, w.hpg)
+        if "far" in a:
+            oracle.attend_far_row(0, h, a, a["far"], w.score_scale, w.hpg)
+        else:
+            oracle.attend_row(0, i, h, a, w.score_scale, w.hpg)
     L, W = int(a["meta"][0][0]), int(a["meta"][0][3])
     return w.ns + min(W, L + i + 1)
 
@@ -297,6 +304,7 @@ def run_reference(args, w, rank):
 def workload_config(w, n):
     return {"workload": w.name, "B": w.B, "t": w.t, "nh": w.nh, "nk": w.nk, "hd": w.hd,
             "window": w.window, "cap": w.cap, "ns": w.ns, "seed": w.seed,
+            "far_landmarks": w.far_m,
             "parallelism": f"sequence shards x{n} (no collective)" if n > 1 else "1 GPU",
             "l2": "inputs larger than L2: the K/V rings read each step exceed 129 MB"
             if w.B * w.nk * w.cap * w.hd * 8 > 129e6 else
@@ -325,7 +333,8 @@ def run_gpu(args, w, rank, world, local_rank):
                        q_scale=inp["q_scale"], gate_scale=inp["gate_scale"],
                        ring_k=inp["ring_k"], ring_v=inp["ring_v"], sink_k=inp["sink_k"],
                        sink_v=inp["sink_v"], meta=inp["meta"], pos0=inp["pos0"],
-                       scale=w.score_scale, eps=w.eps, theta=w.theta, device=dev)
+                       scale=w.score_scale, eps=w.eps, theta=w.theta, device=dev,
+                       far=inp.get("far"))
     d_in = {k: inp[k].to(dev).contiguous() for k in ("yq", "yk", "yv", "gate")}
     del inp["ring_k"], inp["ring_v"]
 
