@@ -128,3 +128,39 @@ def test_rollback_rejects_bad_arguments(lib):
     assert lib.swa_rollback(FAKE, FAKE, 0, 8, None, None) == _abi.SWA_E_SHAPE
     assert lib.swa_rollback(FAKE, FAKE, 1, 0, None, None) == _abi.SWA_E_SHAPE
     assert lib.swa_rollback(FAKE + 4, FAKE, 1, 8, None, None) == _abi.SWA_E_ALIGN
+
+
+def _far(**kw):
+    f = _abi.FarArgs()
+    f.m, f.rect = 16, 0
+    for k in ("k_tilde", "q_tilde", "mu", "mz", "t_hat"):
+        setattr(f, k, FAKE)
+    for k, v in kw.items():
+        setattr(f, k, v)
+    return f
+
+
+def test_attend_rejects_bad_far_field_arguments(lib):
+    call = lambda a: lib.swa_attend(ctypes.byref(a), None)
+    for missing in ("k_tilde", "q_tilde", "mu", "mz", "t_hat"):
+        f = _far(**{missing: None})
+        assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_NULL, missing
+    f = _far()
+    assert call(_attend(t=2, far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE     # decode rows only
+    for m in (0, 33):
+        f = _far(m=m)
+        assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE, m
+    f = _far(t_hat=FAKE + 4)
+    assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_ALIGN
+    f = _far(mz=FAKE + 2)
+    assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_ALIGN
+
+
+def test_workspace_grows_by_the_far_records(lib):
+    a = _attend()
+    base = lib.swa_attend_workspace_size(ctypes.byref(a))
+    f = _far()
+    a.far = ctypes.pointer(f)
+    with_far = lib.swa_attend_workspace_size(ctypes.byref(a))
+    need = 2 * 8 * (4 + 128) * 4                        # B * nh * (4 + hd) floats
+    assert with_far - base >= need and with_far - base < need + 256
