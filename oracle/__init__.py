@@ -8,5 +8,5 @@ from .swa_oracle import (  # noqa: F401
     ring_modulus, rope_table, rotate_head, unit_head, prep, prep_ring_slot,
     prep_ring_write, row_window, row_key_list, sigmoid_gate, attend_row, attend,
     commit_slot, commit_meta, commit, rollback_meta, rollback,
-    far_evict, far_part, far_row_state, attend_far_row, attend_far, far_commit,
+    far_evict, far_evictions, far_part, far_row_state, attend_far_row, attend_far, far_commit,
 )

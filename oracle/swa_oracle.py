@@ -374,40 +374,55 @@ def far_part(q, far, b, h, g, mx2, z2, scale):
     return True, fm, far_den, gain
 
 
-def far_row_state(meta_b, far, b, h, g, inp, scale):
-    """This row's eviction against every landmark of head h: the state after
-    it (mx2, z2, t_hat2) and whether a key was evicted."""
+def far_evictions(meta_b, t, cap):
+    """The chunk rows that evict a key and the ring slot each evicts: with a
+    full window (win_len + row + 1 > W) row j evicts the oldest key still held,
+    logical key j - j0 with j0 = W - win_len, i.e. ring slot
+    (win_head + j - j0) % W (o1c_far_e). Chunks with a far field are at most W
+    rows long, so every evicted key is a ring key."""
+    W = ring_modulus(meta_b, cap)
+    j0 = W - int(meta_b[WIN_LEN])
+    head0 = int(meta_b[WIN_HEAD])
+    return [(j, (head0 + j - j0) % W) for j in range(max(j0, 0), t)]
+
+
+def far_row_state(meta_b, far, b, h, g, inp, scale, row=0):
+    """The far state of head h as row `row` of the chunk sees it: every
+    eviction of rows 0..row applied in order (far_evict per landmark), with
+    the landmark numerators t_hat * rr + e * v. Returns (evictions, mx, z,
+    t_hat) after them."""
     cap = inp["ring_k"].shape[2]
     m = far["m"]
-    W = ring_modulus(meta_b, cap)
-    evict = int(meta_b[WIN_LEN]) == W
-    mx = np.asarray(far["mz"][b, h, :m], np.float64)
-    z = np.asarray(far["mz"][b, h, m:], np.float64)
-    th = np.asarray(far["t_hat"][b, h], np.float64)
-    if not evict:
-        return False, mx.copy(), z.copy(), th.copy()
-    slot = int(meta_b[WIN_HEAD]) % W
-    k_ev = inp["ring_k"][b, g, slot]
-    v_ev = np.asarray(inp["ring_v"][b, g, slot], np.float64)
-    mx2, z2, th2 = np.zeros(m), np.zeros(m), np.zeros_like(th)
-    for a in range(m):
-        mx2[a], z2[a], rr, e = far_evict(float(mx[a]), float(z[a]), k_ev, far["q_tilde"][b, h, a], scale)
-        th2[a] = th[a] * rr + e * v_ev
-    return True, mx2, z2, th2
+    mx = np.array(far["mz"][b, h, :m], np.float64)
+    z = np.array(far["mz"][b, h, m:], np.float64)
+    th = np.array(far["t_hat"][b, h], np.float64)
+    t = inp["q"].shape[1]
+    n_ev = 0
+    for j, slot in far_evictions(meta_b, t, cap):
+        if j > row:
+            break
+        n_ev += 1
+        k_ev = inp["ring_k"][b, g, slot]
+        v_ev = np.asarray(inp["ring_v"][b, g, slot], np.float64)
+        for a in range(m):
+            mx[a], z[a], rr, e = far_evict(float(mx[a]), float(z[a]), k_ev, far["q_tilde"][b, h, a], scale)
+            th[a] = th[a] * rr + e * v_ev
+    return n_ev, mx, z, th
 
 
-def attend_far_row(b, h, inp, far, scale, hpg):
-    """Output of query head h of the decode row of sequence b with the far
-    field (o1c_tok_merge, then dory_gate): with c the larger of the near max
-    and (when the far part is kept) fm,
-    o = (sum_near exp(s - c) v + exp(fm - c) sum_b gain_b t_hat2_b)
-        / (sum_near exp(s - c) + exp(fm - c) far_den)."""
+def attend_far_row(b, h, inp, far, scale, hpg, i=0):
+    """Output of query head h of chunk row i of sequence b with the far field
+    (o1c_far / o1c_tok_far, o1c_tok_merge, then dory_gate): with c the larger
+    of the near max and (when the far part is kept) fm,
+    o = (sum_near exp(s - c) v + exp(fm - c) sum_b gain_b t_hat_b)
+        / (sum_near exp(s - c) + exp(fm - c) far_den),
+    over the far state after the evictions of rows 0..i."""
     meta_b = inp["meta"][b]
     g = h // hpg
     cap = inp["ring_k"].shape[2]
     ns = inp["sink_k"].shape[2]
-    keys = row_key_list(meta_b, 0, ns, cap)
-    q = np.asarray(inp["q"][b, 0, h], np.float64)
+    keys = row_key_list(meta_b, i, ns, cap)
+    q = np.asarray(inp["q"][b, i, h], np.float64)
     K, V = [], []
     for kind, idx in keys:
         if kind == "sink":
@@ -422,8 +437,8 @@ def attend_far_row(b, h, inp, far, scale, hpg):
     K = np.asarray(K, np.float64)
     V = np.asarray(V, np.float64)
     s = scale * (K @ q)
-    evict, mx2, z2, th2 = far_row_state(meta_b, far, b, h, g, inp, scale)
-    farl = int(meta_b[FAR_LEN]) + (1 if evict else 0)
+    n_ev, mx2, z2, th2 = far_row_state(meta_b, far, b, h, g, inp, scale, row=i)
+    farl = int(meta_b[FAR_LEN]) + n_ev
     have, fm, far_den, gain = (False, -np.inf, 0.0, None)
     if farl > 0:
         have, fm, far_den, gain = far_part(q, far, b, h, g, mx2, z2, scale)
@@ -436,33 +451,34 @@ def attend_far_row(b, h, inp, far, scale, hpg):
         num = num + sf * (gain @ th2)
         den = den + sf * far_den
     o = num / den
-    return o * sigmoid_gate(np.asarray(inp["gate"][b, 0, h], np.float64),
+    return o * sigmoid_gate(np.asarray(inp["gate"][b, i, h], np.float64),
                             np.asarray(inp["gate_scale"][h], np.float64))
 
 
 def attend_far(inp, far, scale, hpg):
-    """Every output of a decode step with the far field: out [B][1][nh][hd]."""
+    """Every output of a chunk with the far field: out [B][t][nh][hd]. Far
+    chunks are at most min(W, 32) rows (every evicted key is a ring key)."""
     B, t, nh, hd = inp["q"].shape
-    assert t == 1, "the far field is defined here for decode rows (t = 1)"
-    out = np.zeros((B, 1, nh, hd), np.float64)
+    out = np.zeros((B, t, nh, hd), np.float64)
     for b in range(B):
-        for h in range(nh):
-            out[b, 0, h] = attend_far_row(b, h, inp, far, scale, hpg)
+        for i in range(t):
+            for h in range(nh):
+                out[b, i, h] = attend_far_row(b, h, inp, far, scale, hpg, i)
     return out
 
 
 def far_commit(inp, far, scale, hpg):
-    """The far state after the decode row (o1c_tok_commit, far part): for a
-    sequence whose window was full, every landmark of every head takes the
-    evicted key into its max, mass and numerator. Returns (mz, t_hat)."""
-    B, _, nh, _ = inp["q"].shape
+    """The far state after the chunk (o1c_far_commit / o1c_tok_commit, far
+    part): every key the chunk evicts joins every landmark of every head, in
+    row order. Returns (mz, t_hat)."""
+    B, t, nh, _ = inp["q"].shape
     m = far["m"]
     mz = np.array(far["mz"], np.float64, copy=True)
     th = np.array(far["t_hat"], np.float64, copy=True)
     for b in range(B):
         for h in range(nh):
-            evict, mx2, z2, th2 = far_row_state(inp["meta"][b], far, b, h, h // hpg, inp, scale)
-            if evict:
+            n_ev, mx2, z2, th2 = far_row_state(inp["meta"][b], far, b, h, h // hpg, inp, scale, row=t - 1)
+            if n_ev:
                 mz[b, h, :m] = mx2
                 mz[b, h, m:] = z2
                 th[b, h] = th2

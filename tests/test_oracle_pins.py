@@ -545,3 +545,36 @@ def test_far_rect_clips_negative_landmark_weights():
     b = oracle.attend_far(inp, zeroed, scale, hpg)
     np.testing.assert_allclose(a, b, rtol=1e-12)
     assert not np.allclose(oracle.attend_far(inp, far, scale, hpg), a)
+
+
+@pytest.mark.parametrize("len0", [6, 3])        # full window; one that fills during the chunk
+def test_far_chunk_equals_sequential_decode_steps(len0):
+    """A t-row chunk with the far field (o1c_far_e / o1c_far: row i sees the
+    evictions of rows 0..i) equals t single-row steps each committing ring,
+    meta and far state (o1c_tok_*), row by row, and leaves the same state."""
+    hd, nh, hpg, W, t = 8, 2, 2, 6, 5
+    g, inp, far, scale = _far_decode_case(19, W=W, hd=hd, nh=nh, m=3)
+    far["mu"] = np.abs(far["mu"]) + 0.1
+    inp["meta"] = np.array([[len0, 2, 4 if len0 == W else 0, W]])
+    if len0 < W:
+        far["mz"][0, :, :3] = -np.inf
+        far["mz"][0, :, 3:] = 0.0
+    inp["q"] = g.normal(size=(1, t, nh, hd))
+    inp["k_chunk"], inp["v_chunk"] = g.normal(size=(1, t, 1, hd)), g.normal(size=(1, t, 1, hd))
+    inp["gate"] = g.normal(size=(1, t, nh, hd))
+    chunk = oracle.attend_far(inp, far, scale, hpg)
+    mz_c, th_c = oracle.far_commit(inp, far, scale, hpg)
+    rk_c, rv_c, meta_c = oracle.commit(inp["meta"], inp["ring_k"], inp["ring_v"], inp["k_chunk"], inp["v_chunk"])
+    st = dict(inp)
+    fs = dict(far)
+    for i in range(t):
+        step = dict(st, q=inp["q"][:, i:i + 1], k_chunk=inp["k_chunk"][:, i:i + 1],
+                    v_chunk=inp["v_chunk"][:, i:i + 1], gate=inp["gate"][:, i:i + 1])
+        np.testing.assert_allclose(oracle.attend_far(step, fs, scale, hpg)[:, 0], chunk[:, i], rtol=1e-10)
+        fs["mz"], fs["t_hat"] = oracle.far_commit(step, fs, scale, hpg)
+        st["ring_k"], st["ring_v"], st["meta"] = oracle.commit(step["meta"], step["ring_k"], step["ring_v"],
+                                                               step["k_chunk"], step["v_chunk"])
+    np.testing.assert_allclose(fs["mz"], mz_c, rtol=1e-12)
+    np.testing.assert_allclose(fs["t_hat"], th_c, rtol=1e-12)
+    np.testing.assert_array_equal(st["meta"], meta_c)
+    np.testing.assert_array_equal(st["ring_k"], rk_c)
