@@ -168,9 +168,9 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  *
  * Errors: SWA_E_NULL, SWA_E_SHAPE, SWA_E_ALIGN, SWA_E_WORKSPACE, SWA_E_CUDA.
  */
-/* Far field of a decode step ("o1c_msl.metal", cortiq-engine 0.8.79:
- * o1c_tok_far, o1c_tok_merge, o1c_tok_commit; the clip of "dory_msl.metal"
- * dory_ofar). Keys that leave the window are not dropped: every query head
+/* Far field of a chunk ("o1c_msl.metal", cortiq-engine 0.8.79: o1c_far_e,
+ * o1c_far, o1c_far_commit and the token path's o1c_tok_far, o1c_tok_merge,
+ * o1c_tok_commit; the clip of "dory_msl.metal" dory_ofar). Keys that leave the window are not dropped: every query head
  * keeps m landmarks, each with a running max, mass and numerator of the keys
  * evicted so far, scored against the landmark's query. A row adds to its
  * window the far part: landmark scores s * <q, k~_a> give weights
@@ -187,9 +187,12 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  *                           empty), then mass; rewritten iff commit = 1
  *   t_hat   [B][nh][m][hd]  per landmark numerator (16-byte aligned);
  *                           rewritten iff commit = 1
- * 1 <= m <= 32. Only decode steps (t = 1) take a far field. The evicted key
+ * 1 <= m <= 32. A chunk with a far field has t <= 32 and t <= cap rows;
+ * once the window is full, row j evicts the oldest key still held, and row i
+ * sees the evictions of rows 0..i (o1c_far_e / o1c_far). The evicted keys
  * must still be in the ring: do not let swa_prep write the ring in such a
  * step (pass ring_k = ring_v = NULL there) and commit through swa_attend.
+ * A sequence whose window is shorter than t sets SWA_DERR_META.
  * meta.far_len counts the evicted keys; with far_len = 0 and no eviction the
  * far part is empty. */
 typedef struct swa_far_args {
@@ -224,7 +227,7 @@ typedef struct swa_attend_args {
   uint32_t* err;                 /* optional device error word              */
   cudaEvent_t ev_start;          /* optional                                */
   cudaEvent_t ev_stop;           /* optional                                */
-  const swa_far_args* far;       /* optional far field (t = 1), host struct */
+  const swa_far_args* far;       /* optional far field (t <= 32), host struct */
 } swa_attend_args;
 
 /* Bytes of workspace swa_attend needs for these sizes (reads B, t, nh, nk,

@@ -44,7 +44,7 @@ static int attend_shape_ok(const swa_attend_args* a) {
   if (a->nh % a->nk != 0) return 0;
   if (a->nh / a->nk > 32) return 0;
   if (a->num_splits < 0) return 0;
-  if (a->far && (a->t != 1 || a->far->m < 1 || a->far->m > 32)) return 0;
+  if (a->far && (a->t > 32 || a->t > a->cap || a->far->m < 1 || a->far->m > 32)) return 0;
   return 1;
 }
 
@@ -67,11 +67,11 @@ static int cached_occupancy(int hd, int nq) {
 // CTAs over the SMs: it minimises (waves of resident CTAs) x (keys per CTA +
 // a fixed per-CTA cost), with the keys of a row block bounded by
 // ns + cap + rows - 1 (the window never exceeds cap).
-// Far records after the rest of the workspace: per (sequence, query head) the
+// Far records after the rest of the workspace: per (sequence, row, query head) the
 // far exponent, mass, a keep flag and the far numerator.
 static void add_far_records(const swa_attend_args* a, AttendPlan* p) {
   p->off_far = p->ws_bytes;
-  if (a->far) p->ws_bytes += (((size_t)a->B * a->nh * (4 + a->hd) * sizeof(float)) + 255) & ~(size_t)255;
+  if (a->far) p->ws_bytes += (((size_t)a->B * a->t * a->nh * (4 + a->hd) * sizeof(float)) + 255) & ~(size_t)255;
 }
 
 bool make_plan(const swa_attend_args* a, AttendPlan* p) {

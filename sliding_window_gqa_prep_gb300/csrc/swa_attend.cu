@@ -60,7 +60,7 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
   for (int s0 = lane; s0 < nval; s0 += 32) M = fmaxf(M, p.ws_ml[(item0 + s0) * p.nq + q].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  const float* far_rec = p.far ? p.ws_far + ((size_t)b * p.nh + h) * (4 + HD) : nullptr;
+  const float* far_rec = p.far ? p.ws_far + (((size_t)b * p.t + r) * p.nh + h) * (4 + HD) : nullptr;
   const bool far_on = far_rec && far_rec[2] > 0.5f;
   if (far_on) M = fmaxf(M, far_rec[0]);
   float4 acc[PER];
@@ -182,7 +182,7 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
   // the far part of a decode row joins under the common exponent (o1c_tok_merge)
-  const float* far_rec = p.far ? p.ws_far + ((size_t)b * p.nh + h) * (4 + HD) : nullptr;
+  const float* far_rec = p.far ? p.ws_far + (((size_t)b * p.t + r) * p.nh + h) * (4 + HD) : nullptr;
   const bool far_on = far_rec && far_rec[2] > 0.5f;
   if (far_on) M = fmaxf(M, far_rec[0]);
   float den = 0.f;

@@ -2,18 +2,20 @@
 // o1c_tok_far, the far half of o1c_tok_commit; "dory_msl.metal",
 // cortiq-engine 0.8.57: the clip of dory_ofar).
 //
-// One warp per (sequence, query head), lane a = landmark a (m <= 32):
-//  1. a full window evicts its oldest key (ring slot win_head): every landmark
-//     takes it into its running max and mass (fe = s <q~_a, k>, mx' = max,
-//     rr = exp(mx - mx'), e = exp(fe - mx'), z' = z rr + e);
-//  2. the row's far part: landmark scores fs_a = s <q, k~_a>, weights
-//     w_b = sum_a exp(fs_a - f) mu[a][b] (clipped at 0 with rect), gains
-//     gain_b = w_b exp(f + mx'_b - fm) with fm = max_b (f + mx'_b), far mass
-//     sum_b gain_b z'_b (negative: no far part);
-//  3. lanes over features: the landmarks' numerators after the eviction,
-//     t'_b = t_b rr_b + e_b v, their gain-weighted sum (the row's far
-//     numerator) and, with commit, t' and (mx', z') written back.
-// The record per (sequence, query head) — fm in log2 units, far mass, keep
+// One warp per (sequence, query head), lane a = landmark a (m <= 32), for
+// every row of the chunk (o1c_far_e, o1c_far, o1c_far_commit for chunks):
+//  1. once the window is full, row j evicts the oldest key still held (ring
+//     slot (win_head + j - j0) % W, j0 = W - win_len): every landmark scores
+//     the chunk's evicted keys (fe_j = s <q~_a, k_j>) and takes the chunk's
+//     max mx', the rescale rr = exp(mx - mx') and e_j = exp(fe_j - mx');
+//  2. row i sees the evictions of rows 0..i: landmark scores
+//     fs_a = s <q_i, k~_a>, weights w_b = sum_a exp(fs_a - f) mu[a][b]
+//     (clipped at 0 with rect), gains gain_b = w_b exp(f + mx'_b - fm),
+//     fm = max_b (f + mx'_b), far mass sum_b gain_b (z_b rr_b + sum_j e_bj)
+//     (negative: no far part), and the numerator, lanes over features,
+//     sum_b gain_b rr_b t_b + sum_j (sum_b gain_b e_bj) v_j;
+//  3. with commit, every eviction into the landmarks' numerators, max and mass.
+// The record per (sequence, row, query head) — fm in log2 units, far mass, keep
 // flag, numerator — is what the merge kernel adds to the row. The kernel runs
 // before the attention and the merge, so the evicted ring slot still holds
 // the evicted key when it is read here.
@@ -37,7 +39,7 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 template <int HD>
-__global__ void __launch_bounds__(kFarWarps * 32) far_kernel(AttendParams p) {
+__global__ void __launch_bounds__(kFarWarps * 32, 1) far_kernel(AttendParams p) {
   pdl_trigger();
   pdl_wait();
   constexpr int D4 = HD / 4;
@@ -48,139 +50,210 @@ __global__ void __launch_bounds__(kFarWarps * 32) far_kernel(AttendParams p) {
   const int b = idx / p.nh, h = idx % p.nh, g = h / p.hpg;
   const int m = p.far_m;
   const bool live = lane < m;
+  bool bad = false;
   const swa_meta meta = p.meta[b];
-  const SeqState st = sanitize_state(meta, p.cap, nullptr);
-  const bool evict = st.len0 == st.W;
+  const SeqState st = sanitize_state(meta, p.cap, &bad);
+  // rows j >= j0 = W - win_len evict logical key j - j0 (ring slot
+  // (win_head + j - j0) % W); a far chunk holds at most W rows
+  const int j0 = st.W - st.len0;
+  int n_ev = p.t - j0;
+  if (n_ev < 0) n_ev = 0;
+  if (n_ev > st.W) {
+    n_ev = st.W;
+    bad = true;
+  }
+  if (bad && lane == 0 && h == 0) set_err(p.err, SWA_DERR_META);
   const size_t ghi = (size_t)b * p.nh + h;
   const size_t kvh = (size_t)b * p.nk + g;
   float* mz = p.mz + ghi * 2 * m;
+  const float* ring_k = p.ring_k + kvh * p.cap * HD;
+  const float* ring_v = p.ring_v + kvh * p.cap * HD;
+  auto ev_slot = [&](int e) { return (st.head0 + e) % st.W; };
 
-  // 1-2. the eviction score s <q~_a, k_ev> and the landmark score
-  // s <q, k~_a> of landmark `lane`: one pass over the features with both
-  // rows' loads in flight
-  float mx = live ? mz[lane] : 0.f;
-  float z = live ? mz[m + lane] : 0.f;
-  const float* k_ev = p.ring_k + (kvh * p.cap + st.head0) * HD;
-  const float* v_ev = p.ring_v + (kvh * p.cap + st.head0) * HD;
-  const bool any_far = meta.far_len + (evict ? 1u : 0u) > 0u;
   // the lane's column of mu, fetched up front (independent loads)
+  const bool any_far = meta.far_len + (uint32_t)n_ev > 0u;
   float mu_col[32];
   {
     const float* mu = p.mu + ghi * m * m;
 #pragma unroll
     for (int a = 0; a < 32; ++a) mu_col[a] = (any_far && live && a < m) ? mu[a * m + lane] : 0.f;
   }
-  float fe_acc = 0.f, fs_acc = 0.f;
-  if (live && (evict || any_far)) {
+
+  // 1. every eviction of the chunk against landmark `lane`: scores in one
+  // pass over the features, then the chunk's max, the rescale rr and e_j
+  float mx = live ? mz[lane] : 0.f;
+  float z = live ? mz[m + lane] : 0.f;
+  float ev[32];                                         // e_j after the pass below
+#pragma unroll
+  for (int j = 0; j < 32; ++j) ev[j] = 0.f;
+  if (n_ev > 0 && live) {
     const float* qt = p.q_tilde + (ghi * m + lane) * HD;
-    const float* kt = p.k_tilde + (kvh * m + lane) * HD;
-    const float* q = p.q + ghi * HD;                    // t = 1: row 0 of sequence b
-#pragma unroll 16
-    for (int d4 = 0; d4 < HD / 4; ++d4) {
-      if (evict) {
-        const float4 x = *reinterpret_cast<const float4*>(qt + d4 * 4);
-        const float4 y = *reinterpret_cast<const float4*>(k_ev + d4 * 4);
-        fe_acc += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+#pragma unroll 4
+    for (int d4 = 0; d4 < D4; ++d4) {
+      const float4 x = *reinterpret_cast<const float4*>(qt + d4 * 4);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (j < n_ev) {
+          const float4 y = *reinterpret_cast<const float4*>(ring_k + (size_t)ev_slot(j) * HD + d4 * 4);
+          ev[j] += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+        }
       }
-      const float4 u = *reinterpret_cast<const float4*>(q + d4 * 4);
-      const float4 v = *reinterpret_cast<const float4*>(kt + d4 * 4);
-      fs_acc += u.x * v.x + u.y * v.y + u.z * v.z + u.w * v.w;
     }
   }
-  float rr = 1.f, e = 0.f;
-  if (evict && live) {                                  // the key joins landmark `lane`
-    const float fe = fe_acc * p.scale;
-    const float mx2 = fmaxf(mx, fe);
-    rr = mx2 == mx ? 1.f : expf(mx - mx2);              // an empty landmark (-inf) gives 0
-    e = expf(fe - mx2);
-    z = z * rr + e;
+  float rr = 1.f;
+  if (n_ev > 0 && live) {
+    float mx2 = mx;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < n_ev) {
+        ev[j] *= p.scale;
+        mx2 = fmaxf(mx2, ev[j]);
+      }
+    rr = mx2 == mx ? 1.f : expf(mx - mx2);             // an empty landmark (-inf) gives 0
+#pragma unroll
+    for (int j = 0; j < 32; ++j) ev[j] = j < n_ev ? expf(ev[j] - mx2) : 0.f;
     mx = mx2;
   }
+  const float z_base = z * rr;                          // mass before the chunk, rescaled
 
-  // landmark weights, gains, far mass
-  float fm = -INFINITY, far_den = 0.f, gain = 0.f;
-  bool have = false;
-  if (any_far) {
-    const float fs = live ? fs_acc * p.scale : -INFINITY;
-    const float f = warp_max(fs);
-    const float ea = live ? expf(fs - f) : 0.f;
-    float w = 0.f;
-#pragma unroll
-    for (int a = 0; a < 32; ++a) w += __shfl_sync(kFFull, ea, a) * mu_col[a];   // mu_col[a] = 0 past m
-    if (p.far_rect) w = fmaxf(w, 0.f);
-    const float fb = live ? f + mx : -INFINITY;
-    fm = warp_max(fb);
-    gain = (live && fm != -INFINITY) ? w * expf(fb - fm) : 0.f;
-    far_den = warp_sum(gain * z);
-    have = fm != -INFINITY && far_den >= 0.f;            // a NaN or negative mass drops the far part
-    if (!have) {
-      far_den = 0.f;
-      gain = 0.f;
-    }
-  }
-
-  // 3. numerators after the eviction, the row's far numerator, the write-back
-  const bool write_back = p.commit && evict;
-  float4 num[PER], vv[PER];
-#pragma unroll
-  for (int c = 0; c < PER; ++c) {
-    num[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    vv[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    const int d4 = lane + 32 * c;
-    if (evict && d4 < D4) vv[c] = *reinterpret_cast<const float4*>(v_ev + d4 * 4);
-  }
-  if (have || write_back) {
-    // landmarks 8 at a time: their numerator rows are loaded before any is used
-    for (int a0 = 0; a0 < m; a0 += 8) {
-      float4 t[8][PER];
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-#pragma unroll
-        for (int c = 0; c < PER; ++c) {
-          const int d4 = lane + 32 * c;
-          t[k][c] = (a0 + k < m && d4 < D4)
-                        ? reinterpret_cast<const float4*>(p.t_hat + (ghi * m + a0 + k) * HD)[d4]
-                        : make_float4(0.f, 0.f, 0.f, 0.f);
+  // 2. each row: landmark weights, gains, far mass, numerator
+  for (int i = 0; i < p.t; ++i) {
+    int n_i = i - j0 + 1;                               // evictions of rows 0..i
+    if (n_i < 0) n_i = 0;
+    if (n_i > n_ev) n_i = n_ev;
+    float fm = -INFINITY, far_den = 0.f, gain = 0.f;
+    bool have = false;
+    if (meta.far_len + (uint32_t)n_i > 0u) {
+      float fs = -INFINITY;
+      if (live) {
+        const float* q = p.q + (((size_t)b * p.t + i) * p.nh + h) * HD;
+        const float* kt = p.k_tilde + (kvh * m + lane) * HD;
+        float acc = 0.f;
+#pragma unroll 8
+        for (int d4 = 0; d4 < D4; ++d4) {
+          const float4 u = *reinterpret_cast<const float4*>(q + d4 * 4);
+          const float4 v = *reinterpret_cast<const float4*>(kt + d4 * 4);
+          acc += u.x * v.x + u.y * v.y + u.z * v.z + u.w * v.w;
         }
+        fs = acc * p.scale;
+      }
+      const float f = warp_max(fs);
+      const float ea = live ? expf(fs - f) : 0.f;
+      float w = 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int a = a0 + k;                            // lanes past m hold gain = rr = e = 0
-        const float ga = __shfl_sync(kFFull, gain, a & 31);
-        const float ra = __shfl_sync(kFFull, rr, a & 31);
-        const float eb = __shfl_sync(kFFull, e, a & 31);
-        if (a >= m) continue;
+      for (int a = 0; a < 32; ++a) w += __shfl_sync(kFFull, ea, a) * mu_col[a];   // mu_col[a] = 0 past m
+      if (p.far_rect) w = fmaxf(w, 0.f);
+      const float fb = live ? f + mx : -INFINITY;
+      fm = warp_max(fb);
+      gain = (live && fm != -INFINITY) ? w * expf(fb - fm) : 0.f;
+      float zi = z_base;
 #pragma unroll
-        for (int c = 0; c < PER; ++c) {
-          const int d4 = lane + 32 * c;
-          if (d4 >= D4) continue;
-          float4 u = t[k][c];
-          if (evict) {
-            u.x = u.x * ra + eb * vv[c].x;
-            u.y = u.y * ra + eb * vv[c].y;
-            u.z = u.z * ra + eb * vv[c].z;
-            u.w = u.w * ra + eb * vv[c].w;
-            if (write_back) reinterpret_cast<float4*>(p.t_hat + (ghi * m + a) * HD)[d4] = u;
+      for (int j = 0; j < 32; ++j) zi += j < n_i ? ev[j] : 0.f;
+      far_den = warp_sum(gain * zi);
+      have = fm != -INFINITY && far_den >= 0.f;          // a NaN or negative mass drops the far part
+      if (!have) {
+        far_den = 0.f;
+        gain = 0.f;
+      }
+    }
+    // numerator: sum_b gain_b (rr_b t_b + sum_{j < n_i} e_bj v_j), lanes over features
+    float4 num[PER];
+#pragma unroll
+    for (int c = 0; c < PER; ++c) num[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (have) {
+      const float grr = gain * rr;
+      for (int a0 = 0; a0 < m; a0 += 8) {
+        float4 tl[8][PER];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+#pragma unroll
+          for (int c = 0; c < PER; ++c) {
+            const int d4 = lane + 32 * c;
+            tl[k][c] = (a0 + k < m && d4 < D4)
+                           ? reinterpret_cast<const float4*>(p.t_hat + (ghi * m + a0 + k) * HD)[d4]
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          num[c].x += ga * u.x; num[c].y += ga * u.y; num[c].z += ga * u.z; num[c].w += ga * u.w;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float ga = __shfl_sync(kFFull, grr, (a0 + k) & 31);   // 0 past m
+#pragma unroll
+          for (int c = 0; c < PER; ++c) {
+            num[c].x += ga * tl[k][c].x; num[c].y += ga * tl[k][c].y;
+            num[c].z += ga * tl[k][c].z; num[c].w += ga * tl[k][c].w;
+          }
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {                   // static indices keep ev[] in registers
+        if (j < n_i) {
+          const float cf = warp_sum(gain * ev[j]);      // the evicted row's weight in this row
+          const float* vr = ring_v + (size_t)ev_slot(j) * HD;
+#pragma unroll
+          for (int c = 0; c < PER; ++c) {
+            const int d4 = lane + 32 * c;
+            if (d4 < D4) {
+              const float4 v = *reinterpret_cast<const float4*>(vr + d4 * 4);
+              num[c].x += cf * v.x; num[c].y += cf * v.y; num[c].z += cf * v.z; num[c].w += cf * v.w;
+            }
+          }
         }
       }
     }
-  }
-  float* rec = p.ws_far + ghi * (4 + HD);
+    float* rec = p.ws_far + (((size_t)b * p.t + i) * p.nh + h) * (4 + HD);
 #pragma unroll
-  for (int c = 0; c < PER; ++c) {
-    const int d4 = lane + 32 * c;
-    if (d4 < D4) *reinterpret_cast<float4*>(rec + 4 + d4 * 4) = num[c];
+    for (int c = 0; c < PER; ++c) {
+      const int d4 = lane + 32 * c;
+      if (d4 < D4) *reinterpret_cast<float4*>(rec + 4 + d4 * 4) = num[c];
+    }
+    if (lane == 0) {
+      rec[0] = have ? fm * 1.4426950408889634f : -INFINITY;  // log2 units, as the near records
+      rec[1] = far_den;
+      rec[2] = have ? 1.f : 0.f;
+      rec[3] = 0.f;
+    }
   }
-  if (lane == 0) {
-    rec[0] = have ? fm * 1.4426950408889634f : -INFINITY;  // log2 units, as the near records
-    rec[1] = far_den;
-    rec[2] = have ? 1.f : 0.f;
-    rec[3] = 0.f;
-  }
-  if (write_back && live) {
-    mz[lane] = mx;
-    mz[m + lane] = z;
+
+  // 3. the commit: every eviction of the chunk into the landmark numerators,
+  // the max and the mass (o1c_far_commit)
+  if (p.commit && n_ev > 0) {
+    for (int a = 0; a < m; ++a) {
+      const float ra = __shfl_sync(kFFull, rr, a);
+      float4* th = reinterpret_cast<float4*>(p.t_hat + (ghi * m + a) * HD);
+      float4 t[PER];
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = lane + 32 * c;
+        t[c] = d4 < D4 ? th[d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        t[c].x *= ra; t[c].y *= ra; t[c].z *= ra; t[c].w *= ra;
+      }
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {                   // static indices keep ev[] in registers
+        if (j < n_ev) {
+          const float ej = __shfl_sync(kFFull, ev[j], a);   // landmark a's e_j
+          const float* vr = ring_v + (size_t)ev_slot(j) * HD;
+#pragma unroll
+          for (int c = 0; c < PER; ++c) {
+            const int d4 = lane + 32 * c;
+            if (d4 < D4) {
+              const float4 v = *reinterpret_cast<const float4*>(vr + d4 * 4);
+              t[c].x += ej * v.x; t[c].y += ej * v.y; t[c].z += ej * v.z; t[c].w += ej * v.w;
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = lane + 32 * c;
+        if (d4 < D4) th[d4] = t[c];
+      }
+    }
+    if (live) {
+      float zf = z_base;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) zf += j < n_ev ? ev[j] : 0.f;
+      mz[lane] = mx;
+      mz[m + lane] = zf;
+    }
   }
 }
 

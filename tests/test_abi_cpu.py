@@ -146,7 +146,8 @@ def test_attend_rejects_bad_far_field_arguments(lib):
         f = _far(**{missing: None})
         assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_NULL, missing
     f = _far()
-    assert call(_attend(t=2, far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE     # decode rows only
+    assert call(_attend(t=33, far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE    # at most 32 rows
+    assert call(_attend(t=8, cap=6, far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE   # t <= cap
     for m in (0, 33):
         f = _far(m=m)
         assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE, m
@@ -162,5 +163,5 @@ def test_workspace_grows_by_the_far_records(lib):
     f = _far()
     a.far = ctypes.pointer(f)
     with_far = lib.swa_attend_workspace_size(ctypes.byref(a))
-    need = 2 * 8 * (4 + 128) * 4                        # B * nh * (4 + hd) floats
+    need = 2 * 1 * 8 * (4 + 128) * 4                    # B * t * nh * (4 + hd) floats
     assert with_far - base >= need and with_far - base < need + 256

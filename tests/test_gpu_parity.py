@@ -409,6 +409,22 @@ def _gpu_prepped(res):
 @pytest.mark.parametrize("splits", [0, 1, 64])
 def test_far_decode_step_matches_oracle(rect, splits):
     w, inp = _far_case(41)
+    _far_step_check(w, inp, rect, splits)
+
+
+@pytest.mark.parametrize("t,hd,nh,nk,W", [(4, 128, 8, 2, 96), (8, 128, 16, 4, 96), (8, 256, 8, 2, 40),
+                                          (32, 64, 8, 2, 64)])
+def test_far_chunk_matches_oracle(t, hd, nh, nk, W):
+    """Chunks with the far field (row i sees the evictions of rows 0..i):
+    verify-sized blocks on the CUDA-core kernel, a 32-row chunk of 4 heads per
+    KV head on the tcgen05 kernel; one sequence starts evicting mid-chunk."""
+    w, inp = _far_case(53 + t, t=t, hd=hd, nh=nh, nk=nk, window=W, cap=W, pos_lo=max(1, W // 2), pos_hi=W)
+    inp["meta"][2, 0] = W - 2                           # fills after two rows of the chunk
+    inp["meta"][2, 1] = 0
+    _far_step_check(w, inp, 0, 0)
+
+
+def _far_step_check(w, inp, rect, splits):
     inp["far"]["rect"] = rect
     inp["far"]["mu"] = inp["far"]["mu"] - 0.05       # some negative landmark weights for the clip
     res = gpu_full_path(w, inp, commit=True, num_splits=splits, far=inp["far"])
