@@ -216,7 +216,7 @@ def oracle_unit(w, a, i, g):
     import oracle
     for h in range(g * w.hpg, (g + 1) * w.hpg):
         if "far" in a:
-            oracle.attend_far_row(0, h, a, a["far"], w.score_scale, w.hpg)
+            oracle.attend_far_row(0, h, a, a["far"], w.score_scale, w.hpg, i)
         else:
             oracle.attend_row(0, i, h, a, w.score_scale, w.hpg)
     L, W = int(a["meta"][0][0]), int(a["meta"][0][3])

@@ -38,17 +38,20 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-template <int HD>
+template <int HD, int MAXT>
 __global__ void __launch_bounds__(kFarWarps * 32, 1) far_kernel(AttendParams p) {
   pdl_trigger();
   pdl_wait();
   constexpr int D4 = HD / 4;
   constexpr int PER = (D4 + 31) / 32;
+  constexpr int RG = MAXT < 8 ? MAXT : 8;               // rows per numerator sweep
+  extern __shared__ __align__(16) float far_smem[];     // [kFarWarps][m][HD] landmark numerators
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int idx = blockIdx.x * kFarWarps + warp;        // b * nh + h
   if (idx >= p.B * p.nh) return;
   const int b = idx / p.nh, h = idx % p.nh, g = h / p.hpg;
   const int m = p.far_m;
+  const int t = p.t;
   const bool live = lane < m;
   bool bad = false;
   const swa_meta meta = p.meta[b];
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(kFarWarps * 32, 1) far_kernel(AttendParams p) 
   // rows j >= j0 = W - win_len evict logical key j - j0 (ring slot
   // (win_head + j - j0) % W); a far chunk holds at most W rows
   const int j0 = st.W - st.len0;
-  int n_ev = p.t - j0;
+  int n_ev = t - j0;
   if (n_ev < 0) n_ev = 0;
   if (n_ev > st.W) {
     n_ev = st.W;
@@ -69,7 +72,32 @@ __global__ void __launch_bounds__(kFarWarps * 32, 1) far_kernel(AttendParams p) 
   const float* ring_k = p.ring_k + kvh * p.cap * HD;
   const float* ring_v = p.ring_v + kvh * p.cap * HD;
   auto ev_slot = [&](int e) { return (st.head0 + e) % st.W; };
+  auto n_upto = [&](int i) {                            // evictions of rows 0..i
+    int n = i - j0 + 1;
+    return n < 0 ? 0 : (n > n_ev ? n_ev : n);
+  };
 
+  // the head's landmark numerators into shared memory, once (lanes over features)
+  float* th_s = far_smem + (size_t)warp * m * HD;
+  for (int a0 = 0; a0 < m; a0 += 8) {                   // 8 rows' loads in flight before the stores
+    float4 tmp[8][PER];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = lane + 32 * c;
+        tmp[k][c] = (a0 + k < m && d4 < D4)
+                        ? reinterpret_cast<const float4*>(p.t_hat + (ghi * m + a0 + k) * HD)[d4]
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = lane + 32 * c;
+        if (a0 + k < m && d4 < D4) reinterpret_cast<float4*>(th_s + (a0 + k) * HD)[d4] = tmp[k][c];
+      }
+  }
   // the lane's column of mu, fetched up front (independent loads)
   const bool any_far = meta.far_len + (uint32_t)n_ev > 0u;
   float mu_col[32];
@@ -79,133 +107,82 @@ __global__ void __launch_bounds__(kFarWarps * 32, 1) far_kernel(AttendParams p) 
     for (int a = 0; a < 32; ++a) mu_col[a] = (any_far && live && a < m) ? mu[a * m + lane] : 0.f;
   }
 
-  // 1. every eviction of the chunk against landmark `lane`: scores in one
-  // pass over the features, then the chunk's max, the rescale rr and e_j
+  // 1. every eviction of the chunk against landmark `lane` and every row's
+  // landmark score, in one pass over the features (the lane's q~ and k~ rows
+  // are read once; the evicted keys and the rows' queries are broadcast)
   float mx = live ? mz[lane] : 0.f;
   float z = live ? mz[m + lane] : 0.f;
-  float ev[32];                                         // e_j after the pass below
+  float ev[MAXT], fs[MAXT];                             // MAXT >= t >= evictions
 #pragma unroll
-  for (int j = 0; j < 32; ++j) ev[j] = 0.f;
-  if (n_ev > 0 && live) {
+  for (int j = 0; j < MAXT; ++j) ev[j] = fs[j] = 0.f;
+  if (live && any_far) {
     const float* qt = p.q_tilde + (ghi * m + lane) * HD;
-#pragma unroll 4
+    const float* kt = p.k_tilde + (kvh * m + lane) * HD;
+    const float* qrow = p.q + ((size_t)b * t * p.nh + h) * HD;   // row i at qrow + i * nh * HD
+#pragma unroll 2
     for (int d4 = 0; d4 < D4; ++d4) {
       const float4 x = *reinterpret_cast<const float4*>(qt + d4 * 4);
+      const float4 k = *reinterpret_cast<const float4*>(kt + d4 * 4);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
+      for (int j = 0; j < MAXT; ++j) {
         if (j < n_ev) {
           const float4 y = *reinterpret_cast<const float4*>(ring_k + (size_t)ev_slot(j) * HD + d4 * 4);
           ev[j] += x.x * y.x + x.y * y.y + x.z * y.z + x.w * y.w;
+        }
+        if (j < t) {
+          const float4 u = *reinterpret_cast<const float4*>(qrow + (size_t)j * p.nh * HD + d4 * 4);
+          fs[j] += u.x * k.x + u.y * k.y + u.z * k.z + u.w * k.w;
         }
       }
     }
   }
   float rr = 1.f;
-  if (n_ev > 0 && live) {
+  if (n_ev > 0 && live) {                               // the chunk's max, rescale and e_j
     float mx2 = mx;
 #pragma unroll
-    for (int j = 0; j < 32; ++j)
+    for (int j = 0; j < MAXT; ++j)
       if (j < n_ev) {
         ev[j] *= p.scale;
         mx2 = fmaxf(mx2, ev[j]);
       }
     rr = mx2 == mx ? 1.f : expf(mx - mx2);             // an empty landmark (-inf) gives 0
 #pragma unroll
-    for (int j = 0; j < 32; ++j) ev[j] = j < n_ev ? expf(ev[j] - mx2) : 0.f;
+    for (int j = 0; j < MAXT; ++j) ev[j] = j < n_ev ? expf(ev[j] - mx2) : 0.f;
     mx = mx2;
   }
   const float z_base = z * rr;                          // mass before the chunk, rescaled
+  __syncwarp();                                         // th_s is complete
 
-  // 2. each row: landmark weights, gains, far mass, numerator
-  for (int i = 0; i < p.t; ++i) {
-    int n_i = i - j0 + 1;                               // evictions of rows 0..i
-    if (n_i < 0) n_i = 0;
-    if (n_i > n_ev) n_i = n_ev;
-    float fm = -INFINITY, far_den = 0.f, gain = 0.f;
+  // 2. each row's gains and far mass (the record's header); gn[i] = gain_i
+  float gn[MAXT];
+#pragma unroll
+  for (int i = 0; i < MAXT; ++i) {
+    gn[i] = 0.f;
+    if (i >= t) continue;
+    const int n_i = n_upto(i);
+    float fm = -INFINITY, far_den = 0.f;
     bool have = false;
     if (meta.far_len + (uint32_t)n_i > 0u) {
-      float fs = -INFINITY;
-      if (live) {
-        const float* q = p.q + (((size_t)b * p.t + i) * p.nh + h) * HD;
-        const float* kt = p.k_tilde + (kvh * m + lane) * HD;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int d4 = 0; d4 < D4; ++d4) {
-          const float4 u = *reinterpret_cast<const float4*>(q + d4 * 4);
-          const float4 v = *reinterpret_cast<const float4*>(kt + d4 * 4);
-          acc += u.x * v.x + u.y * v.y + u.z * v.z + u.w * v.w;
-        }
-        fs = acc * p.scale;
-      }
-      const float f = warp_max(fs);
-      const float ea = live ? expf(fs - f) : 0.f;
+      const float fsi = live ? fs[i] * p.scale : -INFINITY;
+      const float f = warp_max(fsi);
+      const float ea = live ? expf(fsi - f) : 0.f;
       float w = 0.f;
 #pragma unroll
       for (int a = 0; a < 32; ++a) w += __shfl_sync(kFFull, ea, a) * mu_col[a];   // mu_col[a] = 0 past m
       if (p.far_rect) w = fmaxf(w, 0.f);
       const float fb = live ? f + mx : -INFINITY;
       fm = warp_max(fb);
-      gain = (live && fm != -INFINITY) ? w * expf(fb - fm) : 0.f;
+      float gain = (live && fm != -INFINITY) ? w * expf(fb - fm) : 0.f;
       float zi = z_base;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) zi += j < n_i ? ev[j] : 0.f;
+      for (int j = 0; j < MAXT; ++j) zi += j < n_i ? ev[j] : 0.f;
       far_den = warp_sum(gain * zi);
       have = fm != -INFINITY && far_den >= 0.f;          // a NaN or negative mass drops the far part
-      if (!have) {
-        far_den = 0.f;
-        gain = 0.f;
-      }
-    }
-    // numerator: sum_b gain_b (rr_b t_b + sum_{j < n_i} e_bj v_j), lanes over features
-    float4 num[PER];
-#pragma unroll
-    for (int c = 0; c < PER; ++c) num[c] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (have) {
-      const float grr = gain * rr;
-      for (int a0 = 0; a0 < m; a0 += 8) {
-        float4 tl[8][PER];
-#pragma unroll
-        for (int k = 0; k < 8; ++k)
-#pragma unroll
-          for (int c = 0; c < PER; ++c) {
-            const int d4 = lane + 32 * c;
-            tl[k][c] = (a0 + k < m && d4 < D4)
-                           ? reinterpret_cast<const float4*>(p.t_hat + (ghi * m + a0 + k) * HD)[d4]
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float ga = __shfl_sync(kFFull, grr, (a0 + k) & 31);   // 0 past m
-#pragma unroll
-          for (int c = 0; c < PER; ++c) {
-            num[c].x += ga * tl[k][c].x; num[c].y += ga * tl[k][c].y;
-            num[c].z += ga * tl[k][c].z; num[c].w += ga * tl[k][c].w;
-          }
-        }
-      }
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {                   // static indices keep ev[] in registers
-        if (j < n_i) {
-          const float cf = warp_sum(gain * ev[j]);      // the evicted row's weight in this row
-          const float* vr = ring_v + (size_t)ev_slot(j) * HD;
-#pragma unroll
-          for (int c = 0; c < PER; ++c) {
-            const int d4 = lane + 32 * c;
-            if (d4 < D4) {
-              const float4 v = *reinterpret_cast<const float4*>(vr + d4 * 4);
-              num[c].x += cf * v.x; num[c].y += cf * v.y; num[c].z += cf * v.z; num[c].w += cf * v.w;
-            }
-          }
-        }
-      }
-    }
-    float* rec = p.ws_far + (((size_t)b * p.t + i) * p.nh + h) * (4 + HD);
-#pragma unroll
-    for (int c = 0; c < PER; ++c) {
-      const int d4 = lane + 32 * c;
-      if (d4 < D4) *reinterpret_cast<float4*>(rec + 4 + d4 * 4) = num[c];
+      if (!have) far_den = 0.f;
+      gn[i] = have ? gain : 0.f;
     }
     if (lane == 0) {
+      float* rec = p.ws_far + (((size_t)b * t + i) * p.nh + h) * (4 + HD);
       rec[0] = have ? fm * 1.4426950408889634f : -INFINITY;  // log2 units, as the near records
       rec[1] = far_den;
       rec[2] = have ? 1.f : 0.f;
@@ -213,48 +190,141 @@ __global__ void __launch_bounds__(kFarWarps * 32, 1) far_kernel(AttendParams p) 
     }
   }
 
-  // 3. the commit: every eviction of the chunk into the landmark numerators,
+  // 3. numerators, RG rows at a time, lanes over features:
+  // sum_b gain_b rr_b t_b + sum_{j < n_i} (sum_b gain_b e_bj) v_j
+  for (int i0 = 0; i0 < t; i0 += RG) {
+    float4 num[RG][PER];
+#pragma unroll
+    for (int k = 0; k < RG; ++k)
+#pragma unroll
+      for (int c = 0; c < PER; ++c) num[k][c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float grr[RG];
+#pragma unroll
+    for (int k = 0; k < RG; ++k) {
+      float v = 0.f;
+#pragma unroll
+      for (int i = 0; i < MAXT; ++i) v = i == i0 + k ? gn[i] : v;  // static register indices
+      grr[k] = v * rr;
+    }
+    for (int a = 0; a < m; ++a) {
+      float4 ta[PER];
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = lane + 32 * c;
+        ta[c] = d4 < D4 ? reinterpret_cast<const float4*>(th_s + a * HD)[d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < RG; ++k) {
+        const float ga = __shfl_sync(kFFull, grr[k], a);
+#pragma unroll
+        for (int c = 0; c < PER; ++c) {
+          num[k][c].x += ga * ta[c].x; num[k][c].y += ga * ta[c].y;
+          num[k][c].z += ga * ta[c].z; num[k][c].w += ga * ta[c].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < MAXT; ++j) {
+      if (j >= n_ev) continue;
+      float4 vj[PER];
+      const float* vr = ring_v + (size_t)ev_slot(j) * HD;
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = lane + 32 * c;
+        vj[c] = d4 < D4 ? *reinterpret_cast<const float4*>(vr + d4 * 4) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int k = 0; k < RG; ++k) {
+        const int i = i0 + k;
+        if (i >= t || j >= n_upto(i)) continue;
+        float gi = 0.f;
+#pragma unroll
+        for (int ii = 0; ii < MAXT; ++ii) gi = ii == i ? gn[ii] : gi;
+        const float cf = warp_sum(gi * ev[j]);          // the evicted row's weight in row i
+#pragma unroll
+        for (int c = 0; c < PER; ++c) {
+          num[k][c].x += cf * vj[c].x; num[k][c].y += cf * vj[c].y;
+          num[k][c].z += cf * vj[c].z; num[k][c].w += cf * vj[c].w;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < RG; ++k) {
+      const int i = i0 + k;
+      if (i >= t) continue;
+      float* rec = p.ws_far + (((size_t)b * t + i) * p.nh + h) * (4 + HD);
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = lane + 32 * c;
+        if (d4 < D4) *reinterpret_cast<float4*>(rec + 4 + d4 * 4) = num[k][c];
+      }
+    }
+  }
+
+  // 4. the commit: every eviction of the chunk into the landmark numerators,
   // the max and the mass (o1c_far_commit)
   if (p.commit && n_ev > 0) {
     for (int a = 0; a < m; ++a) {
       const float ra = __shfl_sync(kFFull, rr, a);
-      float4* th = reinterpret_cast<float4*>(p.t_hat + (ghi * m + a) * HD);
-      float4 t[PER];
+      float4 tv[PER];
 #pragma unroll
       for (int c = 0; c < PER; ++c) {
         const int d4 = lane + 32 * c;
-        t[c] = d4 < D4 ? th[d4] : make_float4(0.f, 0.f, 0.f, 0.f);
-        t[c].x *= ra; t[c].y *= ra; t[c].z *= ra; t[c].w *= ra;
+        tv[c] = d4 < D4 ? reinterpret_cast<const float4*>(th_s + a * HD)[d4] : make_float4(0.f, 0.f, 0.f, 0.f);
+        tv[c].x *= ra; tv[c].y *= ra; tv[c].z *= ra; tv[c].w *= ra;
       }
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {                   // static indices keep ev[] in registers
-        if (j < n_ev) {
-          const float ej = __shfl_sync(kFFull, ev[j], a);   // landmark a's e_j
-          const float* vr = ring_v + (size_t)ev_slot(j) * HD;
+      for (int j = 0; j < MAXT; ++j) {
+        if (j >= n_ev) continue;
+        const float ej = __shfl_sync(kFFull, ev[j], a);     // landmark a's e_j
+        const float* vr = ring_v + (size_t)ev_slot(j) * HD;
 #pragma unroll
-          for (int c = 0; c < PER; ++c) {
-            const int d4 = lane + 32 * c;
-            if (d4 < D4) {
-              const float4 v = *reinterpret_cast<const float4*>(vr + d4 * 4);
-              t[c].x += ej * v.x; t[c].y += ej * v.y; t[c].z += ej * v.z; t[c].w += ej * v.w;
-            }
+        for (int c = 0; c < PER; ++c) {
+          const int d4 = lane + 32 * c;
+          if (d4 < D4) {
+            const float4 v = *reinterpret_cast<const float4*>(vr + d4 * 4);
+            tv[c].x += ej * v.x; tv[c].y += ej * v.y; tv[c].z += ej * v.z; tv[c].w += ej * v.w;
           }
         }
       }
+      float4* th = reinterpret_cast<float4*>(p.t_hat + (ghi * m + a) * HD);
 #pragma unroll
       for (int c = 0; c < PER; ++c) {
         const int d4 = lane + 32 * c;
-        if (d4 < D4) th[d4] = t[c];
+        if (d4 < D4) th[d4] = tv[c];
       }
     }
     if (live) {
       float zf = z_base;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) zf += j < n_ev ? ev[j] : 0.f;
+      for (int j = 0; j < MAXT; ++j) zf += j < n_ev ? ev[j] : 0.f;
       mz[lane] = mx;
       mz[m + lane] = zf;
     }
   }
+}
+
+template <int HD, int MAXT>
+int run_far(const AttendParams& p, dim3 grid, dim3 block, size_t smem, cudaStream_t s) {
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(far_kernel<HD, MAXT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)(kFarWarps * 32 * HD * sizeof(float)));
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  far_kernel<HD, MAXT><<<grid, block, smem, s>>>(p);
+  return finish_launch(cudaSuccess);
+}
+
+// the row and eviction arrays are sized by the chunk: 1, 8 or 32 rows
+template <int HD>
+int run_far_t(const AttendParams& p, dim3 grid, dim3 block, size_t smem, cudaStream_t s) {
+  if (p.t == 1) return run_far<HD, 1>(p, grid, block, smem, s);
+  if (p.t <= 8) return run_far<HD, 8>(p, grid, block, smem, s);
+  return run_far<HD, 32>(p, grid, block, smem, s);
 }
 
 }  // namespace
@@ -267,13 +337,13 @@ int launch_far(const AttendParams& p, cudaStream_t s) {
   // programmatically its CTAs were resident early and the step took 237.5 us
   // instead of 210 us on batched_decode_far. It still triggers its dependents,
   // so the attention's CTAs are scheduled during its tail.
+  const size_t smem = (size_t)kFarWarps * p.far_m * p.hd * sizeof(float);
   switch (p.hd) {
-    case 64: far_kernel<64><<<grid, block, 0, s>>>(p); break;
-    case 128: far_kernel<128><<<grid, block, 0, s>>>(p); break;
-    case 256: far_kernel<256><<<grid, block, 0, s>>>(p); break;
+    case 64: return run_far_t<64>(p, grid, block, smem, s);
+    case 128: return run_far_t<128>(p, grid, block, smem, s);
+    case 256: return run_far_t<256>(p, grid, block, smem, s);
     default: return SWA_E_SHAPE;
   }
-  return finish_launch(cudaSuccess);
 }
 
 }  // namespace swa

@@ -499,7 +499,7 @@ def test_far_field_exact_over_decode_steps_with_landmarks_at_the_evicted_keys():
 # times (automatic splits): every prep output, sampled attention outputs
 # ---------------------------------------------------------------------------
 SAMPLES = {"tiny_decode": 16, "batched_decode": 24, "spec_verify": 24, "prompt_chunk": 24,
-           "long_decode": 10, "batched_decode_far": 24}
+           "long_decode": 10, "batched_decode_far": 24, "spec_verify_far": 24}
 
 
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
@@ -521,7 +521,7 @@ def test_named_workload_full_size(name):
     got = np.stack([res["out"][b, i, h] for b, i, h in picks])
     if w.far_m:
         far = far_to_np(inp["far"])
-        ref = np.stack([oracle.attend_far_row(b, h, a, far, w.score_scale, w.hpg) for b, i, h in picks])
+        ref = np.stack([oracle.attend_far_row(b, h, a, far, w.score_scale, w.hpg, i) for b, i, h in picks])
     else:
         ref = np.stack([oracle.attend_row(b, i, h, a, w.score_scale, w.hpg) for b, i, h in picks])
     assert_close(got, ref, f"{name} sampled out")

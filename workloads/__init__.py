@@ -74,6 +74,10 @@ WORKLOADS: Dict[str, Workload] = {
                                    window=4096, cap=4096, ns=4, seed=5, pos_mode="full",
                                    pos_lo=4096, pos_hi=20000, scale=1.0 / math.sqrt(128.0),
                                    far_m=32),
+    # spec_verify with the far field: 32 landmarks per query head
+    "spec_verify_far": Workload("spec_verify_far", B=128, t=8, nh=32, nk=8, hd=128, window=2048,
+                                cap=2048, ns=4, seed=6, pos_mode="partial", pos_lo=1, pos_hi=2048,
+                                far_m=32),
 }
 
 
