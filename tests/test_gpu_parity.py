@@ -424,6 +424,13 @@ def test_far_chunk_matches_oracle(t, hd, nh, nk, W):
     _far_step_check(w, inp, 0, 0)
 
 
+def test_far_decode_with_odd_landmark_count():
+    """m = 7: the per-head shared-memory sections of a CTA that serves several
+    decode heads stay aligned; heads past nh in the last CTA write nothing."""
+    w, inp = _far_case(61, nh=6, nk=2, far_m=7)
+    _far_step_check(w, inp, 1, 0)
+
+
 def _far_step_check(w, inp, rect, splits):
     inp["far"]["rect"] = rect
     inp["far"]["mu"] = inp["far"]["mu"] - 0.05       # some negative landmark weights for the clip
