@@ -377,9 +377,14 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
         *reinterpret_cast<uint4*>(vl + off) = lv4;
       }
     };
-    // tile j: K half, then (once P V of tile j - 2 has freed the set) V half
+    // tile j: K half (once S of tile j - 2 has read the set), then V half (once P V of
+    // tile j - 2 has). For j >= 3 the S wait is already met by the v_free wait of tile
+    // j - 3 (that commit follows S of tile j - 2); for j == 2 it is the only guard. S of
+    // tile j cannot commit before this iteration arrives on split_done, so the parity
+    // names S of tile j - 2 and no later phase.
     for (int j = 0; j < ntiles; ++j) {
       bool ok = mbar_wait_bounded(&land_full[j & 1], (uint32_t)((j >> 1) & 1), kWaitLimitNs);
+      if (ok && j >= 2) ok = mbar_wait_bounded(&s_full[j & 1], (uint32_t)(((j - 2) >> 1) & 1), kWaitLimitNs);
       ok = __all_sync(kTF, ok) && !*s_abort;
       if (ok) split_k(j);
       if (ok && j >= 2)
