@@ -301,6 +301,26 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def prep_bytes(w):
+    """Bytes the prep moves once per step (P1-P3): the q and k heads read and
+    written; for single rows without a far field also the v heads read and
+    the K/V rows written into the ring."""
+    q = w.B * w.t * w.nh * w.hd * 4
+    k = w.B * w.t * w.nk * w.hd * 4
+    ring = 3 * k if (w.t == 1 and not w.far_m) else 0
+    return 2 * q + 2 * k + ring
+
+
+def prep_report(w, prep_ms, peak_gbs):
+    """The prep stage timed on its own (CUDA events around its kernel)."""
+    us = statistics.median(prep_ms) * 1e3
+    b = prep_bytes(w)
+    gbs = b / (us * 1e-6) / 1e9
+    return {"us_median": us, "bytes": b, "gbs": gbs, "frac_of_hbm": gbs / peak_gbs,
+            "note": "rotation, unit heads, query scale and (single rows) the ring write; "
+                    "the RoPE angles are evaluated in the kernel (f64)"}
+
+
 def workload_config(w, n):
     return {"workload": w.name, "B": w.B, "t": w.t, "nh": w.nh, "nk": w.nk, "hd": w.hd,
             "window": w.window, "cap": w.cap, "ns": w.ns, "seed": w.seed,
@@ -367,13 +387,15 @@ def run_gpu(args, w, rank, world, local_rank):
     # the attention kernel alone: events the library records right before and
     # after it on the same stream, over the same number of steps
     kev = make_events(2 * K)
+    pev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * K)]
     barrier()
     for s in range(K):
         tp.step(d_in["yq"], d_in["yk"], d_in["yv"], d_in["gate"], ev_start=kev[2 * s],
-                ev_stop=kev[2 * s + 1])
+                ev_stop=kev[2 * s + 1], prep_events=(pev[2 * s], pev[2 * s + 1]))
     barrier()
     clk = clocks.stop() if clocks else None
     kern_ms = [kev[2 * s].elapsed_time(kev[2 * s + 1]) for s in range(K)]
+    prep_ms = [pev[2 * s].elapsed_time(pev[2 * s + 1]) for s in range(K)]
     err = int(tp.err.item())
     ms = max_over_ranks(ms, dev)
 
@@ -438,6 +460,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "kv_read_gbs_step": kv_bytes * world / step_s / 1e9,
         "kv_read_frac_of_peak_step": kv_bytes / step_s / 1e9 / peak,
         "roofline": roof,
+        "prep": prep_report(w, prep_ms, pk["hbm_gbs"]),
         "gpu_launches": launches,
         "launches_per_step": launches / K,
         "device_errors": err,

@@ -246,11 +246,13 @@ class TokenPath:
         }
 
     def step(self, yq, yk, yv, gate, *, commit: bool = True, out_host=None,
-             ev_start=None, ev_stop=None, stream=None):
+             ev_start=None, ev_stop=None, prep_events=None, stream=None):
         """One pass of the path. commit = True writes the chunk into the ring and
         the advanced meta into ``meta_next`` (the current ``meta`` is kept, so
         repeating a step repeats the same work). Host inputs are copied in and
-        the output is copied back (into ``out_host`` when given, e.g. pinned)."""
+        the output is copied back (into ``out_host`` when given, e.g. pinned).
+        ev_start / ev_stop bracket the attention kernel, prep_events (a pair of
+        torch CUDA events) the prep kernel, on the step's stream."""
         host = not yq.is_cuda
         if host:
             for name, x in (("yq", yq), ("yk", yk), ("yv", yv), ("gate", gate)):
@@ -259,9 +261,13 @@ class TokenPath:
         # the prep writes the ring for single rows, except with a far field:
         # that step's eviction still reads the evicted slot, so the commit does
         ring = self.t == 1 and self.far is None
+        if prep_events is not None:
+            prep_events[0].record(stream)
         q, k, v = prep(yq, yk, yv, None, self.q_scale, self.eps, pos0=self.pos0, theta=self.theta,
                        ring_k=self.ring_k if ring else None, ring_v=self.ring_v if ring else None,
                        q_out=self.q, k_out=self.k, copy_v=False, stream=stream)
+        if prep_events is not None:
+            prep_events[1].record(stream)
         attend(self.meta, q, k, v, self.ring_k, self.ring_v, self.sink_k, self.sink_v, gate,
                self.gate_scale, self.scale, out=self.out, workspace=self.workspace,
                commit=commit, meta_out=self.meta_next, num_splits=self.num_splits, err=self.err,
