@@ -22,19 +22,6 @@
 namespace swa {
 namespace {
 
-// Gate of one output row: o = acc * inv, times sigmoid(gate * gate_scale).
-__device__ __forceinline__ float4 gated(const AttendParams& p, size_t row, int h, int d4, int hd,
-                                        float4 acc, float inv) {
-  const float4 gt = *reinterpret_cast<const float4*>(p.gate + row * hd + d4 * 4);
-  const float4 gs = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * hd + d4 * 4);
-  float4 o;
-  o.x = acc.x * inv / (1.0f + expf(-(gt.x * gs.x)));
-  o.y = acc.y * inv / (1.0f + expf(-(gt.y * gs.y)));
-  o.z = acc.z * inv / (1.0f + expf(-(gt.z * gs.z)));
-  o.w = acc.w * inv / (1.0f + expf(-(gt.w * gs.w)));
-  return o;
-}
-
 // One output row (b, r, h) by a whole CTA of 8 warps: every warp finds the
 // max over the valid splits, warp w adds the rescaled records of splits
 // w, w + 8, ... (lanes over features), and the CTA sums the 8 partials.
@@ -45,16 +32,22 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
   __shared__ float4 s_acc[8][D4];
   __shared__ float s_den[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row = blk;                      // (b * t + r) * nh + h
-  if (row >= (size_t)p.B * p.t * p.nh) return;
-  const int h = (int)(row % p.nh);
-  const size_t br = row / p.nh;
-  const int r = (int)(br % p.t);
-  const int b = (int)(br / p.t);
+  const uint32_t row = blk;                    // (b * t + r) * nh + h (< 2^31)
+  if (row >= (uint32_t)p.B * p.t * p.nh) return;
+  const int h = (int)(row % (uint32_t)p.nh);
+  const uint32_t br = row / (uint32_t)p.nh;
+  const int r = (int)(br % (uint32_t)p.t);
+  const int b = (int)(br / (uint32_t)p.t);
   const int g = h / p.hpg;
   const int rb = r / p.rows;
   const int q = (r - rb * p.rows) * p.hpg + (h - g * p.hpg);
   const size_t item0 = (((size_t)b * p.nk + g) * p.n_rb + rb) * p.splits;
+  // the gate of the features this thread writes at the end, loaded up front
+  float4 gt = make_float4(0.f, 0.f, 0.f, 0.f), gs = gt;
+  if ((int)threadIdx.x < D4) {
+    gt = *reinterpret_cast<const float4*>(p.gate + (size_t)row * HD + threadIdx.x * 4);
+    gs = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * HD + threadIdx.x * 4);
+  }
   const int nval = p.ws_nsplit[b * p.n_rb + rb];
   float M = -INFINITY;
   for (int s0 = lane; s0 < nval; s0 += 32) M = fmaxf(M, p.ws_ml[(item0 + s0) * p.nq + q].x);
@@ -106,8 +99,138 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
       t.x += a.x * sf; t.y += a.y * sf; t.z += a.z * sf; t.w += a.w * sf;
       dsum += far_rec[1] * sf;
     }
-    *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) = gated(p, row, h, d4, HD, t, 1.0f / dsum);
+    const float inv = 1.0f / dsum;
+    float4 o;
+    o.x = t.x * inv / (1.0f + expf(-(gt.x * gs.x)));
+    o.y = t.y * inv / (1.0f + expf(-(gt.y * gs.y)));
+    o.z = t.z * inv / (1.0f + expf(-(gt.z * gs.z)));
+    o.w = t.w * inv / (1.0f + expf(-(gt.w * gs.w)));
+    *reinterpret_cast<float4*>(p.out + (size_t)row * HD + d4 * 4) = o;
   }
+}
+
+// Elementwise merge for calls with S <= 4 splits and no far field: a thread per
+// (output row, 4 features), kMergeVec of them per thread with all their loads
+// in flight at once; each thread takes the max over the row's valid splits, the
+// rescaled sums and the gate itself (the (m, l) and split-count reads of the 32
+// threads of a row are broadcasts). With one split this is bit-identical to the
+// warp path (the weight is exp2(0) = 1).
+constexpr int kMergeVec = 2;
+constexpr int kMergeFewSplits = 4;
+
+template <int HD, int S>
+__device__ __forceinline__ void merge_elementwise(const AttendParams& p, unsigned blk) {
+  // 32-bit index math: the host takes this path only when the element count fits
+  constexpr int D4 = HD / 4;
+  const uint32_t total = (uint32_t)p.B * p.t * p.nh * D4;
+  const uint32_t base = blk * blockDim.x * kMergeVec + threadIdx.x;
+  float4 gt[kMergeVec], gs[kMergeVec], a[kMergeVec][S];
+  float2 ml[kMergeVec][S];
+  int nval[kMergeVec];
+#pragma unroll
+  for (int k = 0; k < kMergeVec; ++k) {
+    const uint32_t idx = base + k * blockDim.x;
+    nval[k] = 0;
+    if (idx >= total) continue;
+    const uint32_t row = idx / D4;                   // (b * t + r) * nh + h
+    const int d4 = (int)(idx % D4);
+    const int h = (int)(row % (uint32_t)p.nh);
+    const uint32_t br = row / (uint32_t)p.nh;
+    const int r = (int)(br % (uint32_t)p.t);
+    const int b = (int)(br / (uint32_t)p.t);
+    const int g = h / p.hpg;
+    const int rb = r / p.rows;
+    const int q = (r - rb * p.rows) * p.hpg + (h - g * p.hpg);
+    const size_t item0 = (((size_t)b * p.nk + g) * p.n_rb + rb) * S;
+    nval[k] = p.ws_nsplit[b * p.n_rb + rb];
+    gt[k] = *reinterpret_cast<const float4*>(p.gate + (size_t)row * HD + d4 * 4);
+    gs[k] = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * HD + d4 * 4);
+    // every split's record is allocated: read them all, use the valid ones
+#pragma unroll
+    for (int sp = 0; sp < S; ++sp) {
+      ml[k][sp] = p.ws_ml[(item0 + sp) * p.nq + q];
+      a[k][sp] = *reinterpret_cast<const float4*>(p.ws_acc + ((item0 + sp) * p.nq + q) * (size_t)HD + d4 * 4);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kMergeVec; ++k) {
+    const uint32_t idx = base + k * blockDim.x;
+    if (idx >= total) continue;
+    float M = -INFINITY;
+#pragma unroll
+    for (int sp = 0; sp < S; ++sp)
+      if (sp < nval[k]) M = fmaxf(M, ml[k][sp].x);
+    float den = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sp = 0; sp < S; ++sp) {
+      if (sp < nval[k] && ml[k][sp].x != -INFINITY) {  // a split with no key of this row weighs 0
+        const float w = exp2f(ml[k][sp].x - M);
+        den += ml[k][sp].y * w;
+        acc.x += a[k][sp].x * w; acc.y += a[k][sp].y * w; acc.z += a[k][sp].z * w; acc.w += a[k][sp].w * w;
+      }
+    }
+    const float inv = 1.0f / den;
+    float4 o;
+    o.x = acc.x * inv / (1.0f + expf(-(gt[k].x * gs[k].x)));
+    o.y = acc.y * inv / (1.0f + expf(-(gt[k].y * gs[k].y)));
+    o.z = acc.z * inv / (1.0f + expf(-(gt[k].z * gs[k].z)));
+    o.w = acc.w * inv / (1.0f + expf(-(gt[k].w * gs[k].w)));
+    *reinterpret_cast<float4*>(p.out + (size_t)idx * 4) = o;
+  }
+}
+
+// Commit of sequence b, spread over commit_blocks CTAs (cta = index among the
+// trailing CTAs of a merge launch).
+template <int HD>
+__device__ void commit_chunk(const AttendParams& p, int cta) {
+  // ---- commit of sequence b, spread over commit_blocks CTAs: the last
+  // min(t, W) chunk rows into their ring slots (o1c_ring_commit), then the
+  // meta (o1c_meta). The ring map comes from the copy of the meta the
+  // attention kernel saved, so meta_out may alias meta.
+  const int cb = cta % p.commit_blocks;
+  const int b = cta / p.commit_blocks;
+  const swa_meta m0 = p.ws_meta[b];
+  const SeqState st = sanitize_state(m0, p.cap, nullptr);
+  const int first = max(0, p.t - st.W);      // only the last W rows survive
+  const int nrow = p.t - first;
+  const int per_row = p.nk * (HD / 4);
+  const int stride = p.commit_blocks * blockDim.x;
+  for (int idx = cb * blockDim.x + threadIdx.x; idx < nrow * per_row; idx += stride) {
+    const int j = first + idx / per_row;
+    const int g = (idx % per_row) / (HD / 4);
+    const int d4 = idx % (HD / 4);
+    int slot = (int)(((long long)st.head0 + st.len0 + j) % st.W);
+    const size_t src = (((size_t)b * p.t + j) * p.nk + g) * HD + d4 * 4;
+    const size_t dst = (((size_t)b * p.nk + g) * p.cap + slot) * HD + d4 * 4;
+    *reinterpret_cast<float4*>(p.ring_k + dst) = *reinterpret_cast<const float4*>(p.k_chunk + src);
+    *reinterpret_cast<float4*>(p.ring_v + dst) = *reinterpret_cast<const float4*>(p.v_chunk + src);
+  }
+  if (cb == 0 && threadIdx.x == 0) {
+    swa_meta m1 = m0;
+    const long long tot = (long long)st.len0 + p.t;
+    if (tot <= st.W) {
+      m1.win_len = (uint32_t)tot;
+    } else {
+      const long long ev = tot - st.W;
+      m1.win_len = (uint32_t)st.W;
+      m1.win_head = (uint32_t)((st.head0 + ev) % st.W);
+      m1.far_len = (uint32_t)(m0.far_len + (uint32_t)ev);
+    }
+    p.meta_out[b] = m1;
+  }
+}
+
+// Merge of few split records (elementwise) + gate; trailing CTAs commit the chunk.
+template <int HD, int S>
+__global__ void __launch_bounds__(256) attend_merge_few_kernel(AttendParams p, int out_blocks) {
+  pdl_trigger();
+  pdl_wait();
+  if ((int)blockIdx.x >= out_blocks) {
+    commit_chunk<HD>(p, (int)blockIdx.x - out_blocks);
+    return;
+  }
+  merge_elementwise<HD, S>(p, blockIdx.x);
 }
 
 // Merge of the split records + gate; trailing CTAs commit the chunk. With
@@ -118,41 +241,7 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
   pdl_trigger();
   pdl_wait();
   if ((int)blockIdx.x >= out_blocks) {
-    // ---- commit of sequence b, spread over commit_blocks CTAs: the last
-    // min(t, W) chunk rows into their ring slots (o1c_ring_commit), then the
-    // meta (o1c_meta). The ring map comes from the copy of the meta the
-    // attention kernel saved, so meta_out may alias meta.
-    const int cb = (blockIdx.x - out_blocks) % p.commit_blocks;
-    const int b = (blockIdx.x - out_blocks) / p.commit_blocks;
-    const swa_meta m0 = p.ws_meta[b];
-    const SeqState st = sanitize_state(m0, p.cap, nullptr);
-    const int first = max(0, p.t - st.W);      // only the last W rows survive
-    const int nrow = p.t - first;
-    const int per_row = p.nk * (HD / 4);
-    const int stride = p.commit_blocks * blockDim.x;
-    for (int idx = cb * blockDim.x + threadIdx.x; idx < nrow * per_row; idx += stride) {
-      const int j = first + idx / per_row;
-      const int g = (idx % per_row) / (HD / 4);
-      const int d4 = idx % (HD / 4);
-      int slot = (int)(((long long)st.head0 + st.len0 + j) % st.W);
-      const size_t src = (((size_t)b * p.t + j) * p.nk + g) * HD + d4 * 4;
-      const size_t dst = (((size_t)b * p.nk + g) * p.cap + slot) * HD + d4 * 4;
-      *reinterpret_cast<float4*>(p.ring_k + dst) = *reinterpret_cast<const float4*>(p.k_chunk + src);
-      *reinterpret_cast<float4*>(p.ring_v + dst) = *reinterpret_cast<const float4*>(p.v_chunk + src);
-    }
-    if (cb == 0 && threadIdx.x == 0) {
-      swa_meta m1 = m0;
-      const long long tot = (long long)st.len0 + p.t;
-      if (tot <= st.W) {
-        m1.win_len = (uint32_t)tot;
-      } else {
-        const long long ev = tot - st.W;
-        m1.win_len = (uint32_t)st.W;
-        m1.win_head = (uint32_t)((st.head0 + ev) % st.W);
-        m1.far_len = (uint32_t)(m0.far_len + (uint32_t)ev);
-      }
-      p.meta_out[b] = m1;
-    }
+    commit_chunk<HD>(p, (int)blockIdx.x - out_blocks);
     return;
   }
   if (wide) {
@@ -165,19 +254,37 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
   constexpr int D4 = HD / 4;
   constexpr int PER = (D4 + 31) / 32;          // float4 chunks per lane
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const size_t row = (size_t)blockIdx.x * (blockDim.x / 32) + warp;   // (b * t + r) * nh + h
-  if (row >= (size_t)p.B * p.t * p.nh) return;
-  const int h = (int)(row % p.nh);
-  const size_t br = row / p.nh;
-  const int r = (int)(br % p.t);
-  const int b = (int)(br / p.t);
+  const uint32_t row = blockIdx.x * (blockDim.x / 32) + warp;   // (b * t + r) * nh + h (< 2^31)
+  if (row >= (uint32_t)p.B * p.t * p.nh) return;
+  const int h = (int)(row % (uint32_t)p.nh);
+  const uint32_t br = row / (uint32_t)p.nh;
+  const int r = (int)(br % (uint32_t)p.t);
+  const int b = (int)(br / (uint32_t)p.t);
   const int g = h / p.hpg;
   const int rb = r / p.rows;
   const int q = (r - rb * p.rows) * p.hpg + (h - g * p.hpg);
   const size_t item0 = (((size_t)b * p.nk + g) * p.n_rb + rb) * p.splits;
+  // Loads that wait for nothing go out together: the gate and its scale, the
+  // valid-split count, the (m, l) of split `lane` and the numerator of split 0
+  // (every split's record is allocated, so reads past the valid splits stay in
+  // bounds; split 0 always exists, a row sees at least its own key).
+  float4 gt[PER], gs[PER], a0[PER];
+  const float* src0 = p.ws_acc + (item0 * p.nq + q) * (size_t)HD;
+#pragma unroll
+  for (int c = 0; c < PER; ++c) {
+    const int d4 = c * 32 + lane;
+    if (d4 < D4) {
+      gt[c] = *reinterpret_cast<const float4*>(p.gate + (size_t)row * HD + d4 * 4);
+      gs[c] = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * HD + d4 * 4);
+      a0[c] = *reinterpret_cast<const float4*>(src0 + d4 * 4);
+    }
+  }
   const int nval = p.ws_nsplit[b * p.n_rb + rb];
-  float M = -INFINITY;
-  for (int s0 = 0; s0 < nval; s0 += 32)
+  float2 ml0 = make_float2(-INFINITY, 0.f);
+  if (lane < p.splits) ml0 = p.ws_ml[(item0 + lane) * p.nq + q];
+  if (lane >= nval) ml0 = make_float2(-INFINITY, 0.f);
+  float M = ml0.x;
+  for (int s0 = 32; s0 < nval; s0 += 32)
     if (s0 + lane < nval) M = fmaxf(M, p.ws_ml[(item0 + s0 + lane) * p.nq + q].x);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
@@ -190,19 +297,29 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
 #pragma unroll
   for (int c = 0; c < PER; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < nval; s0 += 32) {
+    float2 ml = ml0;
+    if (s0 > 0) {
+      ml = make_float2(-INFINITY, 0.f);
+      if (s0 + lane < nval) ml = p.ws_ml[(item0 + s0 + lane) * p.nq + q];
+    }
     float w = 0.f;
-    if (s0 + lane < nval) {
-      const float2 ml = p.ws_ml[(item0 + s0 + lane) * p.nq + q];
-      if (ml.x != -INFINITY) {                 // a split with no key of this row weighs 0
-        w = exp2f(ml.x - M);
-        den += ml.y * w;
-      }
+    if (ml.x != -INFINITY) {                   // a split with no key of this row weighs 0
+      w = exp2f(ml.x - M);                     // (its numerator is 0, so 0 x it is exact)
+      den += ml.y * w;
     }
     const int cnt = min(32, nval - s0);
+    int k = 0;
+    if (s0 == 0) {
+      const float wk = __shfl_sync(0xffffffffu, w, 0);
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        acc[c].x += a0[c].x * wk; acc[c].y += a0[c].y * wk; acc[c].z += a0[c].z * wk; acc[c].w += a0[c].w * wk;
+      }
+      k = 1;
+    }
 #pragma unroll 4
-    for (int k = 0; k < cnt; ++k) {
+    for (; k < cnt; ++k) {
       const float wk = __shfl_sync(0xffffffffu, w, k);
-      if (wk == 0.f) continue;
       const float* src = p.ws_acc + ((item0 + s0 + k) * p.nq + q) * (size_t)HD;
 #pragma unroll
       for (int c = 0; c < PER; ++c) {
@@ -233,14 +350,12 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
   for (int c = 0; c < PER; ++c) {
     const int d4 = c * 32 + lane;
     if (d4 >= D4) continue;
-    const float4 gt = *reinterpret_cast<const float4*>(p.gate + row * HD + d4 * 4);
-    const float4 gs = *reinterpret_cast<const float4*>(p.gate_scale + (size_t)h * HD + d4 * 4);
     float4 o;
-    o.x = acc[c].x * inv / (1.0f + expf(-(gt.x * gs.x)));
-    o.y = acc[c].y * inv / (1.0f + expf(-(gt.y * gs.y)));
-    o.z = acc[c].z * inv / (1.0f + expf(-(gt.z * gs.z)));
-    o.w = acc[c].w * inv / (1.0f + expf(-(gt.w * gs.w)));
-    *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) = o;
+    o.x = acc[c].x * inv / (1.0f + expf(-(gt[c].x * gs[c].x)));
+    o.y = acc[c].y * inv / (1.0f + expf(-(gt[c].y * gs[c].y)));
+    o.z = acc[c].z * inv / (1.0f + expf(-(gt[c].z * gs[c].z)));
+    o.w = acc[c].w * inv / (1.0f + expf(-(gt[c].w * gs[c].w)));
+    *reinterpret_cast<float4*>(p.out + (size_t)row * HD + d4 * 4) = o;
   }
 }
 
@@ -264,9 +379,27 @@ int launch_attend_merge(const AttendParams& p, cudaStream_t s) {
   const size_t rows = (size_t)p.B * p.t * p.nh;
   const int block = 256;
   // many splits per row: a CTA per row (8 warps share the splits); else a warp per row
+  const int commit_ctas = p.commit ? p.B * p.commit_blocks : 0;
+  const size_t elems = rows * (size_t)(p.hd / 4);
+  if (!p.far && p.splits <= kMergeFewSplits && elems + (size_t)block * kMergeVec < (1ull << 32)) {
+    // few splits, no far field: elementwise
+    const size_t per_cta = (size_t)block * kMergeVec;
+    const int out_blocks = (int)((rows * (size_t)(p.hd / 4) + per_cta - 1) / per_cta);
+    const dim3 grid(out_blocks + commit_ctas);
+#define SWA_FEW(HDV, SV) case HDV * 10 + SV: \
+    return finish_launch(launch_pdl(attend_merge_few_kernel<HDV, SV>, grid, dim3(block), 0, s, p, out_blocks));
+    switch (p.hd * 10 + p.splits) {
+      SWA_FEW(64, 1) SWA_FEW(64, 2) SWA_FEW(64, 3) SWA_FEW(64, 4)
+      SWA_FEW(128, 1) SWA_FEW(128, 2) SWA_FEW(128, 3) SWA_FEW(128, 4)
+      SWA_FEW(256, 1) SWA_FEW(256, 2) SWA_FEW(256, 3) SWA_FEW(256, 4)
+      default: return SWA_E_SHAPE;
+    }
+#undef SWA_FEW
+  }
+  // many splits: a CTA per row (8 warps share the splits); else a warp per row
   const int wide = p.splits >= 16 ? 1 : 0;
   const int out_blocks = wide ? (int)rows : (int)((rows + block / 32 - 1) / (block / 32));
-  const int grid = out_blocks + (p.commit ? p.B * p.commit_blocks : 0);
+  const int grid = out_blocks + commit_ctas;
   switch (p.hd) {
     case 64: return finish_launch(launch_pdl(attend_merge_kernel<64>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
     case 128: return finish_launch(launch_pdl(attend_merge_kernel<128>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));

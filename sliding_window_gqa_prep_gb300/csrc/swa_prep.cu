@@ -8,7 +8,8 @@
 // contiguous, coalesced vectors. The sum of squares is a butterfly over the
 // warp. Every byte moves once. The row's angles, when the kernel computes
 // them, cost f64 sine/cosine evaluations, which are slow on this GPU: one CTA
-// per row evaluates them once for all of the row's heads.
+// per row evaluates them once for all of the row's heads (several rows per CTA,
+// sharing the angle work, measured slower: fewer warps in flight).
 #include "swa_internal.cuh"
 
 namespace swa {
@@ -39,11 +40,42 @@ __device__ __forceinline__ void stv(float* p, const float (&r)[P]) {
 constexpr int kPrepWarps = 8;
 constexpr int kPrepBatch = 4;      // heads a warp loads before it stores any
 
-// One head of one row: rotation, unit norm, query scale / ring write.
+// Inputs of one head: both halves of the rotated vector and, for a q head, both
+// halves of its per-feature scale, for a k head both halves of its v row.
 template <int HD>
-__device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, int lane,
+struct HeadIn {
+  float x[HD / 64], y[HD / 64], sa[HD / 64], sb[HD / 64];
+};
+
+template <int HD>
+__device__ __forceinline__ void load_head(const PrepParams& p, int row, int a, int lane, HeadIn<HD>& in) {
+  constexpr int P = HD / 64;
+  constexpr int HALF = HD / 2;
+  const int e = lane * P;
+  if (a < p.nh) {
+    const float* src = p.yq + ((size_t)row * p.nh + a) * HD;
+    ldv<P>(src + e, in.x);
+    ldv<P>(src + HALF + e, in.y);
+    ldv<P>(p.q_scale + (size_t)a * HD + e, in.sa);
+    ldv<P>(p.q_scale + (size_t)a * HD + HALF + e, in.sb);
+  } else {
+    const int kh = a - p.nh;
+    const float* src = p.yk + ((size_t)row * p.nk + kh) * HD;
+    ldv<P>(src + e, in.x);
+    ldv<P>(src + HALF + e, in.y);
+    if (p.v_out || p.ring_k) {
+      const float* vs = p.yv + ((size_t)row * p.nk + kh) * HD;
+      ldv<P>(vs + e, in.sa);
+      ldv<P>(vs + HALF + e, in.sb);
+    }
+  }
+}
+
+// One head of one row: rotation, unit norm, query scale / ring write (to `slot`).
+template <int HD>
+__device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, int lane, uint32_t slot,
                                           const float (&c)[HD / 64], const float (&s)[HD / 64],
-                                          const float (&x)[HD / 64], const float (&y)[HD / 64]) {
+                                          const HeadIn<HD>& in) {
   constexpr int P = HD / 64;
   constexpr int HALF = HD / 2;
   const int e = lane * P;
@@ -51,8 +83,8 @@ __device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, i
   float ss = 0.f;
 #pragma unroll
   for (int i = 0; i < P; ++i) {
-    u[i] = x[i] * c[i] - y[i] * s[i];
-    v[i] = y[i] * c[i] + x[i] * s[i];
+    u[i] = in.x[i] * c[i] - in.y[i] * s[i];
+    v[i] = in.y[i] * c[i] + in.x[i] * s[i];
     ss += u[i] * u[i] + v[i] * v[i];
   }
 #pragma unroll
@@ -60,13 +92,10 @@ __device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, i
   const float inv = 1.0f / sqrtf(ss + p.eps);
 
   if (a < p.nh) {
-    float sa[P], sb[P];
-    ldv<P>(p.q_scale + (size_t)a * HD + e, sa);
-    ldv<P>(p.q_scale + (size_t)a * HD + HALF + e, sb);
 #pragma unroll
     for (int i = 0; i < P; ++i) {
-      u[i] = u[i] * inv * sa[i];
-      v[i] = v[i] * inv * sb[i];
+      u[i] = u[i] * inv * in.sa[i];
+      v[i] = v[i] * inv * in.sb[i];
     }
     float* dst = p.q_out + ((size_t)row * p.nh + a) * HD;
     stv<P>(dst + e, u);
@@ -82,24 +111,18 @@ __device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, i
   float* kd = p.k_out + ((size_t)row * p.nk + kh) * HD;
   stv<P>(kd + e, u);
   stv<P>(kd + HALF + e, v);
-  if (!p.v_out && !p.ring_k) return;
-  const float* vs = p.yv + ((size_t)row * p.nk + kh) * HD;
-  float va[P], vb[P];
-  ldv<P>(vs + e, va);
-  ldv<P>(vs + HALF + e, vb);
   if (p.v_out) {
     float* vd = p.v_out + ((size_t)row * p.nk + kh) * HD;
-    stv<P>(vd + e, va);
-    stv<P>(vd + HALF + e, vb);
+    stv<P>(vd + e, in.sa);
+    stv<P>(vd + HALF + e, in.sb);
   }
   if (p.ring_k) {
-    const int b = row / p.t, j = row % p.t;
-    const uint32_t slot = (uint32_t)(((uint64_t)p.pos0[b] + (uint64_t)j) % (uint64_t)p.cap);
+    const int b = row / p.t;
     const size_t at = (((size_t)b * p.nk + kh) * p.cap + slot) * HD;
     stv<P>(p.ring_k + at + e, u);
     stv<P>(p.ring_k + at + HALF + e, v);
-    stv<P>(p.ring_v + at + e, va);
-    stv<P>(p.ring_v + at + HALF + e, vb);
+    stv<P>(p.ring_v + at + e, in.sa);
+    stv<P>(p.ring_v + at + HALF + e, in.sb);
   }
 }
 
@@ -112,16 +135,32 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
   const int row = blockIdx.x;      // b * t + j
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int b = row / p.t, j = row % p.t;
+  // heads a = warp, warp + kPrepWarps, ...: q heads first, then k heads (the
+  // head split of dory_prep); kPrepBatch heads' inputs are in flight at once.
+  // The first batch is requested before the angles are evaluated, so its load
+  // latency overlaps them.
+  const int nheads = p.nh + p.nk;
+  HeadIn<HD> in[kPrepBatch];
+  auto load_batch = [&](int a0) {
+#pragma unroll
+    for (int k = 0; k < kPrepBatch; ++k) {
+      const int a = a0 + k * kPrepWarps;
+      if (a < nheads) load_head<HD>(p, row, a, lane, in[k]);
+    }
+  };
+  load_batch(warp);
+  const bool need_pos = p.rope == nullptr || p.ring_k != nullptr;
+  const uint64_t pos = need_pos ? (uint64_t)p.pos0[b] + (uint64_t)j : 0;
+  const uint32_t slot = p.ring_k ? (uint32_t)(pos % (uint64_t)p.cap) : 0u;
   // Without a table, the row's cos/sin are computed once per CTA (the CTA
   // covers every head of the row), with the same f64 expression as
   // rope_table_kernel (bit-identical f32 values).
   __shared__ __align__(16) float s_cs[HD];
   if (p.rope == nullptr) {
-    const int b = row / p.t, j = row % p.t;
-    const double pos = (double)p.pos0[b] + (double)j;
     for (int e2 = threadIdx.x; e2 < HALF; e2 += blockDim.x) {
       double sn, cs;
-      sincos(pos * p.inv_freq[e2], &sn, &cs);
+      sincos((double)pos * p.inv_freq[e2], &sn, &cs);
       s_cs[e2] = (float)cs;
       s_cs[HALF + e2] = (float)sn;
     }
@@ -133,25 +172,12 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepParams p) {
   ldv<P>(rope + e, c);
   ldv<P>(rope + HALF + e, s);
 
-  // heads a = warp, warp + kPrepWarps, ...: q heads first, then k heads (the
-  // head split of dory_prep); kPrepBatch heads' inputs are in flight at once
-  const int nheads = p.nh + p.nk;
   for (int a0 = warp; a0 < nheads; a0 += kPrepWarps * kPrepBatch) {
-    float x[kPrepBatch][P], y[kPrepBatch][P];
+    if (a0 != warp) load_batch(a0);
 #pragma unroll
     for (int k = 0; k < kPrepBatch; ++k) {
       const int a = a0 + k * kPrepWarps;
-      if (a < nheads) {
-        const float* src = a < p.nh ? p.yq + ((size_t)row * p.nh + a) * HD
-                                    : p.yk + ((size_t)row * p.nk + (a - p.nh)) * HD;
-        ldv<P>(src + e, x[k]);
-        ldv<P>(src + HALF + e, y[k]);
-      }
-    }
-#pragma unroll
-    for (int k = 0; k < kPrepBatch; ++k) {
-      const int a = a0 + k * kPrepWarps;
-      if (a < nheads) prep_head<HD>(p, row, a, lane, c, s, x[k], y[k]);
+      if (a < nheads) prep_head<HD>(p, row, a, lane, slot, c, s, in[k]);
     }
   }
 }

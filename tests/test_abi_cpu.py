@@ -103,6 +103,7 @@ def test_attend_rejects_bad_arguments(lib):
     assert call(_attend(cap=0)) == _abi.SWA_E_SHAPE
     assert call(_attend(ns=-1)) == _abi.SWA_E_SHAPE
     assert call(_attend(scale=float("nan"))) == _abi.SWA_E_SHAPE
+    assert call(_attend(B=1 << 20, t=1024)) == _abi.SWA_E_SHAPE   # 2^33 output rows
     assert call(_attend(out=FAKE + 8)) == _abi.SWA_E_ALIGN
     assert call(_attend(workspace_bytes=16)) == _abi.SWA_E_WORKSPACE
     assert call(_attend(workspace=None)) == _abi.SWA_E_WORKSPACE

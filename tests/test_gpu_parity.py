@@ -123,6 +123,17 @@ ATTEND_CASES = [
     # mid-size chunks (64 <= rows x heads < 128): the 64-vector mma.sync path
     dict(B=2, t=20, nh=8, nk=2, hd=128, window=90, cap=90, ns=2, pos_mode="full", pos_lo=90, pos_hi=900),
     dict(B=2, t=12, nh=16, nk=2, hd=64, window=30, cap=30, ns=1, pos_mode="partial", pos_lo=1, pos_hi=30),
+    # verify blocks of 32 query vectors at hd 128 with other head groupings:
+    # hpg 2 (16 rows), a window of three 128-key spans with a ragged tail, wrapped rings
+    dict(B=2, t=16, nh=4, nk=2, hd=128, window=300, cap=300, ns=4, pos_mode="full", pos_lo=300, pos_hi=5000),
+    # hpg 8 (4 rows), a window of 129 keys
+    dict(B=2, t=4, nh=16, nk=2, hd=128, window=129, cap=129, ns=1, pos_mode="partial", pos_lo=1, pos_hi=129),
+    # hpg 16 (2 rows), one KV head, no sinks
+    dict(B=1, t=2, nh=16, nk=1, hd=128, window=512, cap=512, ns=0, pos_mode="full", pos_lo=512, pos_hi=3000),
+    # hpg 4, two row blocks (8 + 3 rows), a window shorter than the block
+    dict(B=2, t=11, nh=8, nk=2, hd=128, window=6, cap=6, ns=2, pos_mode="full", pos_lo=6, pos_hi=400),
+    # hpg 6 (5 rows = 30 of 32 query slots), prompt-style rings (some empty)
+    dict(B=3, t=5, nh=12, nk=2, hd=128, window=260, cap=260, ns=3, pos_mode="prompt", pos_lo=0, pos_hi=300),
 ]
 
 
@@ -161,6 +172,17 @@ def test_attend_only_matches_oracle_on_shared_q_k():
 def test_split_count_invariance(splits):
     w = workloads.custom(B=2, t=4, nh=8, nk=2, hd=128, window=500, cap=500, ns=4,
                          pos_mode="full", pos_lo=500, pos_hi=9000, seed=3, scale=3.0)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=False, num_splits=splits)
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, f"out (splits={splits})")
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5])
+def test_split_count_invariance_verify_block(splits):
+    """hd 128 blocks of 32 query vectors (the verify kernel) under several split counts."""
+    w = workloads.custom(B=2, t=8, nh=8, nk=2, hd=128, window=700, cap=700, ns=4,
+                         pos_mode="full", pos_lo=700, pos_hi=9000, seed=4, scale=3.0)
     inp = workloads.make_inputs(w)
     res = gpu_full_path(w, inp, commit=False, num_splits=splits)
     ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
