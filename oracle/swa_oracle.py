@@ -38,6 +38,14 @@ optional clip of "dory_msl.metal" ``dory_ofar`` (``rect``). Reading: the state
 (landmark keys and queries, the m x m matrix mu, per-landmark max / mass /
 numerator) is per sequence; the pages hold one sequence and never build it.
 
+The full-sequence attention (``flash_row``, ``flash_attention``) follows
+"egemma2_msl.metal" (cortiq-engine 0.8.17) ``eg_flash64`` / ``eg_flash_staged``:
+every row of a segment attends every row of the same segment (no window, no
+causal mask), grouped query heads, Q/K/V read in place from a packed row
+buffer; pinned against a masked dense attention over the whole buffer, closed
+forms (one key, two keys, zero query) and row-permutation / segment
+independence.
+
 Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
 (closed forms, a library attention routine on a materialised sequence,
 invariants, hand-derived integer fixtures under ``tests/golden/``) except the
@@ -483,3 +491,36 @@ def far_commit(inp, far, scale, hpg):
                 mz[b, h, m:] = z2
                 th[b, h] = th2
     return mz, th
+
+
+# ---------------------------------------------------------------------------
+# Full-sequence attention ("egemma2_msl.metal", cortiq-engine 0.8.17:
+# eg_flash64 / eg_flash_staged). Every query row of a segment attends every key
+# row of the same segment: no window, no causal mask, no sinks, no gate.
+# Grouped query heads (q head h reads K/V head h // group), scores scaled by
+# `scale`, max-subtracted softmax, value sum divided by the weight sum.
+# Q, K and V are read in place from the rows of one packed buffer qkv[T][ld]:
+# q head h at columns q_off + h*hd .. +hd, K/V head g at k_off / v_off + g*hd.
+# A segment is (first row, length). Output rows are [nq*hd], head h at h*hd.
+# ---------------------------------------------------------------------------
+def flash_row(qkv, s0, length, r, h, hd, group, q_off, k_off, v_off, scale):
+    """Output of query row s0 + r, head h: softmax over the segment's keys."""
+    g = h // group
+    q = np.asarray(qkv[s0 + r, q_off + h * hd:q_off + (h + 1) * hd], dtype=np.float64)
+    keys = np.asarray(qkv[s0:s0 + length, k_off + g * hd:k_off + (g + 1) * hd], dtype=np.float64)
+    vals = np.asarray(qkv[s0:s0 + length, v_off + g * hd:v_off + (g + 1) * hd], dtype=np.float64)
+    s = scale * (keys @ q)
+    p = np.exp(s - s.max())
+    return (p @ vals) / p.sum()
+
+
+def flash_attention(qkv, segs, hd, nq, group, q_off, k_off, v_off, scale):
+    """All segments' rows, every q head: out[T][nq*hd] (rows outside every
+    segment stay zero)."""
+    out = np.zeros((qkv.shape[0], nq * hd))
+    for s0, length in segs:
+        for r in range(int(length)):
+            for h in range(nq):
+                out[s0 + r, h * hd:(h + 1) * hd] = flash_row(qkv, int(s0), int(length), r, h, hd, group,
+                                                             q_off, k_off, v_off, scale)
+    return out

@@ -11,7 +11,10 @@ Each pin is chosen so that a plausible mistake in the oracle fails it:
     with an explicit sliding-window mask) on a materialised logical sequence;
   * invariants: softmax weights sum to 1, ring-rotation invariance, a t-row
     chunk equals t single-row steps with commits, the RoPE relative-position
-    identity.
+    identity;
+  * for the full-sequence attention: a block-diagonally masked dense attention
+    over the whole packed buffer, one-key / two-key / zero-query closed forms,
+    row permutation and segment / KV-head independence.
 """
 import json
 import math
@@ -578,3 +581,111 @@ def test_far_chunk_equals_sequential_decode_steps(len0):
     np.testing.assert_allclose(fs["t_hat"], th_c, rtol=1e-12)
     np.testing.assert_array_equal(st["meta"], meta_c)
     np.testing.assert_array_equal(st["ring_k"], rk_c)
+
+
+# ---------------------------------------------------------------------------
+# full-sequence attention (egemma2_msl.metal eg_flash64 / eg_flash_staged)
+# ---------------------------------------------------------------------------
+def _flash_case(seed, segs, hd=8, nq=4, group=2, pad=4):
+    """Packed rows [q heads | k heads | v heads | pad]: offsets not at 0 and a
+    row stride larger than the three blocks, so a slip in either shows."""
+    g = np.random.default_rng(seed)
+    nk = nq // group
+    q_off, k_off = pad, pad + nq * hd
+    v_off = k_off + nk * hd
+    ld = v_off + nk * hd + pad
+    T = max(s0 + n for s0, n in segs) + 2
+    return g.normal(size=(T, ld)), dict(hd=hd, nq=nq, group=group, q_off=q_off, k_off=k_off, v_off=v_off)
+
+
+def test_flash_matches_masked_dense_attention_over_the_whole_buffer():
+    """One dense score matrix over all T rows per head with a block-diagonal
+    segment mask (torch scaled_dot_product_attention in float64), against the
+    oracle's per-segment, per-row loops."""
+    segs = [(0, 5), (5, 1), (7, 9)]                 # row 6 belongs to no segment
+    qkv, c = _flash_case(1, segs)
+    hd, nq, group, scale = c["hd"], c["nq"], c["group"], 0.7
+    got = oracle.flash_attention(qkv, segs, scale=scale, **c)
+    T = qkv.shape[0]
+    seg_id = np.full(T, -1)
+    for k, (s0, n) in enumerate(segs):
+        seg_id[s0:s0 + n] = k
+    mask = (seg_id[:, None] == seg_id[None, :]) & (seg_id[:, None] >= 0)
+    mask[seg_id < 0, :] = True                        # rows outside segments: any finite value
+    for h in range(nq):
+        g = h // group
+        q = torch.tensor(qkv[:, c["q_off"] + h * hd:c["q_off"] + (h + 1) * hd])
+        k = torch.tensor(qkv[:, c["k_off"] + g * hd:c["k_off"] + (g + 1) * hd])
+        v = torch.tensor(qkv[:, c["v_off"] + g * hd:c["v_off"] + (g + 1) * hd])
+        ref = torch.nn.functional.scaled_dot_product_attention(
+            q[None, None], k[None, None], v[None, None], attn_mask=torch.tensor(mask)[None, None],
+            scale=scale)[0, 0].numpy()
+        for s0, n in segs:
+            np.testing.assert_allclose(got[s0:s0 + n, h * hd:(h + 1) * hd], ref[s0:s0 + n], rtol=1e-12, atol=1e-13)
+    assert not got[6].any()
+
+
+def test_flash_one_key_segment_returns_its_value_row():
+    segs = [(2, 1)]
+    qkv, c = _flash_case(2, segs)
+    got = oracle.flash_attention(qkv, segs, scale=3.0, **c)
+    for h in range(c["nq"]):
+        g = h // c["group"]
+        np.testing.assert_array_equal(got[2, h * c["hd"]:(h + 1) * c["hd"]],
+                                      qkv[2, c["v_off"] + g * c["hd"]:c["v_off"] + (g + 1) * c["hd"]])
+
+
+def test_flash_zero_query_gives_the_mean_of_the_segment_values():
+    segs = [(0, 7)]
+    qkv, c = _flash_case(3, segs)
+    qkv[:, c["q_off"]:c["q_off"] + c["nq"] * c["hd"]] = 0.0
+    got = oracle.flash_attention(qkv, segs, scale=1.0, **c)
+    for h in range(c["nq"]):
+        g = h // c["group"]
+        mean = qkv[0:7, c["v_off"] + g * c["hd"]:c["v_off"] + (g + 1) * c["hd"]].mean(axis=0)
+        np.testing.assert_allclose(got[0:7, h * c["hd"]:(h + 1) * c["hd"]], np.tile(mean, (7, 1)), rtol=1e-13)
+
+
+def test_flash_two_key_closed_form():
+    """Two keys: o = (e^{s1} v1 + e^{s2} v2) / (e^{s1} + e^{s2}), s_k = scale <q, k_k>,
+    written out by hand for one head with hd = 2 and group = 1."""
+    qkv = np.array([[1.0, 2.0, 0.5, -1.0, 3.0, 4.0],
+                    [-2.0, 0.0, 2.0, 1.0, -5.0, 6.0]])    # per row: q (2) | k (2) | v (2)
+    scale = 0.25
+    got = oracle.flash_attention(qkv, [(0, 2)], hd=2, nq=1, group=1, q_off=0, k_off=2, v_off=4, scale=scale)
+    for r in range(2):
+        q = qkv[r, 0:2]
+        s1 = scale * (q[0] * 0.5 + q[1] * -1.0)
+        s2 = scale * (q[0] * 2.0 + q[1] * 1.0)
+        e1, e2 = math.exp(s1), math.exp(s2)
+        want = [(e1 * 3.0 + e2 * -5.0) / (e1 + e2), (e1 * 4.0 + e2 * 6.0) / (e1 + e2)]
+        np.testing.assert_allclose(got[r], want, rtol=1e-14)
+
+
+def test_flash_row_permutation_permutes_the_outputs():
+    segs = [(1, 8)]
+    qkv, c = _flash_case(4, segs)
+    got = oracle.flash_attention(qkv, segs, scale=0.9, **c)
+    perm = np.random.default_rng(5).permutation(8)
+    qkv2 = qkv.copy()
+    qkv2[1:9] = qkv[1:9][perm]
+    got2 = oracle.flash_attention(qkv2, segs, scale=0.9, **c)
+    np.testing.assert_allclose(got2[1:9], got[1:9][perm], rtol=1e-12, atol=1e-14)
+
+
+def test_flash_segments_are_independent_and_heads_share_kv_by_group():
+    segs = [(0, 4), (4, 5)]
+    qkv, c = _flash_case(6, segs)
+    got = oracle.flash_attention(qkv, segs, scale=1.1, **c)
+    qkv2 = qkv.copy()
+    qkv2[4:9] = np.random.default_rng(7).normal(size=(5, qkv.shape[1]))
+    got2 = oracle.flash_attention(qkv2, segs, scale=1.1, **c)
+    np.testing.assert_array_equal(got2[0:4], got[0:4])
+    # group = 2: q heads 0 and 1 read K/V head 0; swapping the K/V of head 1
+    # changes heads 2 and 3 only
+    qkv3 = qkv.copy()
+    hd, k1 = c["hd"], c["k_off"] + c["hd"]
+    qkv3[:, k1:k1 + hd] = np.random.default_rng(8).normal(size=(qkv.shape[0], hd))
+    got3 = oracle.flash_attention(qkv3, segs, scale=1.1, **c)
+    np.testing.assert_array_equal(got3[:, 0:2 * hd], got[:, 0:2 * hd])
+    assert np.abs(got3[0:9, 2 * hd:] - got[0:9, 2 * hd:]).max() > 1e-3
