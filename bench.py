@@ -28,6 +28,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse  # noqa: E402
+import dataclasses  # noqa: E402
 import hashlib  # noqa: E402
 import json  # noqa: E402
 import re  # noqa: E402
@@ -55,7 +56,8 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=list(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=list(workloads.WORKLOADS) + list(workloads.FLASH_WORKLOADS))
     ap.add_argument("--impl", default="swa", choices=["swa", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="CPU time budget of the oracle baseline sample")
@@ -473,11 +475,226 @@ def run_gpu(args, w, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# Full-sequence attention (swa_flash): the second workload
+# ---------------------------------------------------------------------------
+FLASH_L2_FLUSH_BYTES = 256 << 20
+
+
+def flash_recorded_traffic(w):
+    """DRAM bytes per launch of swa_flash's kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(PROFILE_DIR, f"attend_prompt_tc_kernel_{w.name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    m = re.search(r"traffic_bytes_per_launch\s*[:=]\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_sha256_16\s*[:=]\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != source_hash(os.path.join(CSRC, "swa_prompt_tc.cu")):
+        return None
+    return float(m.group(1))
+
+
+def flash_config(w, n):
+    return {"workload": w.name, "segments": [list(s) for s in w.segs], "T": w.T, "nh": w.nh, "nk": w.nk,
+            "hd": w.hd, "ld": w.ld, "seed": w.seed, "scale": w.score_scale,
+            "parallelism": f"replicas x{n} (no collective)" if n > 1 else "1 GPU",
+            "l2": f"L2 flushed between timed calls (a {FLASH_L2_FLUSH_BYTES >> 20} MB write): "
+                  "the packed rows fit in L2"}
+
+
+def flash_oracle_rows(w, qkv, picks):
+    """The oracle on (segment, row, KV head) units: all query heads of the unit."""
+    import oracle
+    keys = 0
+    for (s0, n), r, g in picks:
+        for h in range(g * w.group, (g + 1) * w.group):
+            oracle.flash_row(qkv, s0, n, r, h, w.hd, w.group, w.q_off, w.k_off, w.v_off, w.score_scale)
+        keys += n
+    return keys
+
+
+def flash_units(w, count, seed):
+    rng = np.random.default_rng(seed)
+    segs = [s for s in w.segs if s[1] > 0]
+    out = []
+    for _ in range(count):
+        s0, n = segs[int(rng.integers(len(segs)))]
+        out.append(((s0, n), int(rng.integers(n)), int(rng.integers(w.nk))))
+    return out
+
+
+def flash_cpu_baseline(w, budget_s):
+    qkv = workloads.make_flash_inputs(w)["qkv"].numpy()
+    t0 = time.perf_counter()
+    keys, n = 0, 0
+    units = flash_units(w, 100000, 0)
+    while time.perf_counter() - t0 < budget_s and n < len(units):
+        keys += flash_oracle_rows(w, qkv, units[n:n + 1])
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": keys / dt, "unit": "keys/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} random (query row, KV head) units of {w.name}, all query heads of each "
+                      f"({keys} attended keys, {dt:.1f} s, numpy float64, one thread)"}
+
+
+def run_flash_reference(args, w, rank):
+    """Reference arm for the full-sequence workload: the CPU oracle as it stands,
+    each step a bounded sample of (query row, KV head) units."""
+    if rank != 0:
+        return
+    qkv = workloads.make_flash_inputs(w)["qkv"].numpy()
+    t_a = time.perf_counter()
+    flash_oracle_rows(w, qkv, flash_units(w, 1, 1))
+    t_unit = max(time.perf_counter() - t_a, 1e-5)
+    budget_per_step = 150.0 / max(1, args.steps + args.warmup)
+    per_step = int(max(1, budget_per_step / t_unit))
+    state = {"i": 0}
+
+    def step():
+        state["i"] += 1
+        return flash_oracle_rows(w, qkv, flash_units(w, per_step, state["i"]))
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    keys = 0
+    for _ in range(args.steps):
+        keys += step()
+    dt = time.perf_counter() - t0
+    value = keys / dt
+    sample = (f"per step: {per_step} random (query row, KV head) units of {w.name} with all their query "
+              f"heads; numpy float64, one thread")
+    line = {"impl": "reference", "metric": "attended keys/s", "value": value, "unit": "keys/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": flash_config(w, args.gpus),
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_flash_gpu(args, w, rank, world, local_rank):
+    """One step = one swa_flash call over the workload's packed rows (resident in
+    HBM); an L2-sized write separates the timed calls."""
+    import sliding_window_gqa_prep_gb300 as swa
+    from sliding_window_gqa_prep_gb300.dist import max_over_ranks
+
+    dev = torch.device("cuda", local_rank)
+    inp = workloads.make_flash_inputs(dataclasses.replace(w, seed=w.seed + 1000 * rank))
+    keys, useful_flop = workloads.flash_keys_and_flops(w)
+    qkv = inp["qkv"].to(dev)
+    segs = inp["segs"].to(dev)
+    out = torch.zeros(w.T, w.nh * w.hd, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    flush = torch.empty(FLASH_L2_FLUSH_BYTES // 4, device=dev)
+    kw = dict(hd=w.hd, nh=w.nh, nk=w.nk, q_off=w.q_off, k_off=w.k_off, v_off=w.v_off,
+              scale=w.score_scale, max_len=w.max_len, err=err)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        swa.flash(qkv, segs, out=out, **kw)
+    barrier()
+    K = args.steps
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
+    kev = make_events(2 * K)
+    barrier()
+    l0 = swa.launch_count()
+    for s in range(K):
+        flush.zero_()
+        swa.flash(qkv, segs, out=out, ev_start=kev[2 * s], ev_stop=kev[2 * s + 1], **kw)
+    barrier()
+    launches = swa.launch_count() - l0
+    clk = clocks.stop() if clocks else None
+    kern_ms = [kev[2 * s].elapsed_time(kev[2 * s + 1]) for s in range(K)]
+    ms = max_over_ranks(sum(kern_ms), dev)
+
+    e2e = None
+    if not args.no_e2e:
+        # the public call on host buffers: pinned rows in, output rows back, every step
+        h_qkv = inp["qkv"].pin_memory()
+        h_out = torch.empty(w.T, w.nh * w.hd).pin_memory()
+        d_qkv = torch.empty_like(qkv)
+
+        def e2e_step():
+            d_qkv.copy_(h_qkv, non_blocking=True)
+            swa.flash(d_qkv, segs, out=out, **kw)
+            h_out.copy_(out, non_blocking=True)
+
+        for _ in range(max(args.warmup, 1)):
+            e2e_step()
+        barrier()
+        t0 = time.perf_counter()
+        for _ in range(K):
+            e2e_step()
+        barrier()
+        e2e_s = max_over_ranks(time.perf_counter() - t0, dev)
+        e2e = {"value": keys * K * world / e2e_s, "unit": "keys/s",
+               "h2d_bytes_per_step": h_qkv.numel() * 4, "d2h_bytes_per_step": h_out.numel() * 4,
+               "ms_per_step": e2e_s * 1e3 / K}
+    if rank != 0:
+        return
+    pk = peaks()
+    kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
+    roof = {"bound": "tensor", "achieved": 3 * useful_flop / kern_avg_s / 1e12, "peak": pk["tf32_tflops"],
+            "unit": "TFLOP/s",
+            "peak_kind": f"{pk['kind']} bf16 x 1.1/2.25 (nominal TF32/bf16); achieved counts the 3 TF32 "
+                         "products of each multiply-add",
+            "useful_tflops": useful_flop / kern_avg_s / 1e12}
+    roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": "attend_prompt_tc_kernel (full-sequence)",
+                 "traffic": flash_recorded_traffic(w), "launch_ms_avg": kern_avg_s * 1e3})
+    line = {
+        "metric": "attended keys/s",
+        "value": keys * world / (ms / 1e3 / K),
+        "unit": "keys/s",
+        "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 (3xTF32 tensor-core products, f32 softmax)",
+        "data": "synthetic (seeded generator, shapes of the named workload)",
+        "config": flash_config(w, world),
+        "roofline": roof,
+        "gpu_launches": launches,
+        "launches_per_step": launches / K,
+        "device_errors": int(err.item()),
+        "clocks": clk,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = flash_cpu_baseline(w, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.workload in workloads.FLASH_WORKLOADS:
+        w = workloads.FLASH_WORKLOADS[args.workload]
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        if args.impl == "reference":
+            run_flash_reference(args, w, rank)
+            return
+        torch.cuda.set_device(local_rank)
+        if world > 1:
+            torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        try:
+            run_flash_gpu(args, w, rank, world, local_rank)
+        finally:
+            if world > 1:
+                torch.distributed.destroy_process_group()
+        return
     w = workloads.WORKLOADS[args.workload]
     if args.batch:
-        import dataclasses
         w = dataclasses.replace(w, B=args.batch)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

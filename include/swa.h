@@ -54,6 +54,8 @@ extern "C" {
                                 or win_head >= window (values were clamped) */
 #define SWA_DERR_TIMEOUT  2u /* a bounded wait on a copy into shared memory
                                 expired; the kernel stopped without output */
+#define SWA_DERR_SEGMENT  4u /* swa_flash: a segment reaches past row T or is
+                                longer than max_len (its rows are not written) */
 
 /* Per-sequence ring state, as the per-group meta of o1c_msl.metal:
  *   win_len  — keys held in the ring (<= window)
@@ -295,6 +297,51 @@ int swa_rollback(swa_meta* meta, const int32_t* n_back, int B, int cap, uint32_t
  */
 #define SWA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);
+
+/*
+ * swa_flash — full-sequence attention over packed q|k|v rows, the second
+ * workload beside the token path ("egemma2_msl.metal", cortiq-engine 0.8.17,
+ * kernels eg_flash64 / eg_flash_staged): every query row of a segment attends
+ * every key row of the same segment (no window, no causal mask, no sinks, no
+ * gate), q head h reads K/V head h / (nh / nk), scores are multiplied by
+ * `scale`, the softmax is max-subtracted in f32 and the value sum is divided by
+ * the weight sum. Both products run on the tensor cores as 3xTF32 (f32
+ * accuracy), with each K/V block of a KV head staged in shared memory once per
+ * 128 query vectors (the rows x query heads of that KV head).
+ *
+ *   qkv      [T][ld] f32: row r holds q head h at qkv + r*ld + q_off + h*hd and
+ *            K / V head g at k_off + g*hd / v_off + g*hd; read in place.
+ *   segs     [nseg][2] u32 on the device: first row and length of each segment.
+ *            A segment with first + length > T or length > max_len is skipped
+ *            and sets SWA_DERR_SEGMENT; empty segments are allowed. Segments
+ *            must not overlap (their outputs would race); this is not checked.
+ *   out      [T][ldo] f32: row r of a segment receives head h at
+ *            out + r*ldo + h*hd (nh * hd <= ldo); other rows are not written.
+ *   max_len  an upper bound of the segment lengths (>= 1); it sizes the grid.
+ *   ld, ldo, q_off, k_off, v_off   in floats, multiples of 4 (16-byte rows).
+ *   hd       64 or 128.  nh % nk == 0 and nh / nk <= 32.
+ *   scale    finite.
+ *   err      optional device word (SWA_DERR_SEGMENT, SWA_DERR_TIMEOUT).
+ *   ev_start, ev_stop  optional events recorded on `stream` right before and
+ *            after the attention kernel (NULL: none).
+ * The call enqueues one kernel, allocates nothing and needs no workspace.
+ * Errors: SWA_E_NULL (qkv, segs or out NULL), SWA_E_SHAPE (sizes, offsets past
+ * ld, nh * hd > ldo, nseg < 1, max_len < 1, scale not finite), SWA_E_ALIGN
+ * (pointers not 16-byte aligned, or ld / ldo / offsets not multiples of 4),
+ * SWA_E_CUDA.
+ */
+typedef struct swa_flash_args {
+  int T, nseg, hd, nh, nk;
+  int ld, q_off, k_off, v_off, ldo;
+  int max_len;
+  float scale;
+  const float* qkv;            /* [T][ld] */
+  const uint32_t* segs;        /* [nseg][2]: first row, length */
+  float* out;                  /* [T][ldo] */
+  uint32_t* err;               /* optional */
+  cudaEvent_t ev_start, ev_stop;  /* optional */
+} swa_flash_args;
+int swa_flash(const swa_flash_args* args, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

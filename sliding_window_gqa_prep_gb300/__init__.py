@@ -197,6 +197,35 @@ def rollback(meta: torch.Tensor, n_back: torch.Tensor, cap: int, err=None, strea
     return meta
 
 
+def flash(qkv: torch.Tensor, segs: torch.Tensor, *, hd: int, nh: int, nk: int, q_off: int, k_off: int,
+          v_off: int, scale: float, max_len: int, out: Optional[torch.Tensor] = None, ldo: Optional[int] = None,
+          err=None, ev_start=None, ev_stop=None, stream=None) -> torch.Tensor:
+    """Full-sequence attention over packed q|k|v rows (swa_flash): qkv [T][ld],
+    segs [nseg][2] int32 (first row, length), every row of a segment attends
+    every row of the segment. Returns out [T][ldo] (rows outside every segment
+    are left as they were; a new output starts zeroed)."""
+    if qkv.dim() != 2:
+        raise ValueError("qkv must be [T][ld]")
+    T, ld = qkv.shape
+    nseg = segs.shape[0]
+    if ldo is None:
+        ldo = nh * hd
+    if out is None:
+        out = torch.zeros(T, ldo, device=qkv.device, dtype=torch.float32)
+    a = _abi.FlashArgs()
+    a.T, a.nseg, a.hd, a.nh, a.nk = T, nseg, hd, nh, nk
+    a.ld, a.q_off, a.k_off, a.v_off, a.ldo, a.max_len = ld, q_off, k_off, v_off, ldo, int(max_len)
+    a.scale = float(scale)
+    a.qkv = _ptr(qkv, "qkv", (T, ld))
+    a.segs = _ptr(segs, "segs", (nseg, 2), torch.int32)
+    a.out = _ptr(out, "out", (T, ldo))
+    a.err = _ptr(err, "err", (1,), torch.int32, required=False)
+    a.ev_start = ctypes.c_void_p(ev_start.cuda_event) if ev_start is not None else None
+    a.ev_stop = ctypes.c_void_p(ev_stop.cuda_event) if ev_stop is not None else None
+    _abi.check(library().swa_flash(ctypes.byref(a), _stream(stream)), "swa_flash")
+    return out
+
+
 class TokenPath:
     """One batch of sequences of a sealed sliding-window layer, resident on the GPU.
 

@@ -57,6 +57,18 @@ class AttendArgs(ctypes.Structure):
     ]
 
 
+class FlashArgs(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int), ("nseg", ctypes.c_int), ("hd", ctypes.c_int), ("nh", ctypes.c_int),
+        ("nk", ctypes.c_int),
+        ("ld", ctypes.c_int), ("q_off", ctypes.c_int), ("k_off", ctypes.c_int), ("v_off", ctypes.c_int),
+        ("ldo", ctypes.c_int), ("max_len", ctypes.c_int),
+        ("scale", ctypes.c_float),
+        ("qkv", c_float_p), ("segs", ctypes.c_void_p), ("out", c_float_p), ("err", ctypes.c_void_p),
+        ("ev_start", ctypes.c_void_p), ("ev_stop", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 
 
@@ -97,6 +109,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                  ctypes.c_void_p, ctypes.c_void_p]
     lib.swa_attend.restype = ctypes.c_int
     lib.swa_attend.argtypes = [ctypes.POINTER(AttendArgs), ctypes.c_void_p]
+    lib.swa_flash.restype = ctypes.c_int
+    lib.swa_flash.argtypes = [ctypes.POINTER(FlashArgs), ctypes.c_void_p]
     _lib = lib
     return lib
 

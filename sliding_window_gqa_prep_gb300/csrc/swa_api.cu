@@ -254,7 +254,7 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return SWA_E_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return SWA_E_ALIGN;
 
-  AttendParams p;
+  AttendParams p{};
   p.B = a->B; p.t = a->t; p.nh = a->nh; p.nk = a->nk; p.hd = a->hd; p.cap = a->cap;
   p.ns = a->ns; p.hpg = a->nh / a->nk;
   p.qmul = a->scale * 1.4426950408889634f;
@@ -298,6 +298,38 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   rc = launch_attend_partial(p, stream, a->ev_start, a->ev_stop);
   if (rc != SWA_OK) return rc;
   return launch_attend_merge(p, stream);
+}
+
+int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
+  if (!a) return SWA_E_NULL;
+  if (!a->qkv || !a->segs || !a->out) return SWA_E_NULL;
+  if (a->T < 1 || a->nseg < 1 || a->nh < 1 || a->nk < 1 || a->max_len < 1 || a->max_len > a->T)
+    return SWA_E_SHAPE;
+  if (a->hd != 64 && a->hd != 128) return SWA_E_SHAPE;
+  if (a->nh % a->nk != 0 || a->nh / a->nk > 32) return SWA_E_SHAPE;
+  if (a->ld < 1 || a->ldo < 1 || a->q_off < 0 || a->k_off < 0 || a->v_off < 0) return SWA_E_SHAPE;
+  const long long qh = (long long)a->nh * a->hd, kh = (long long)a->nk * a->hd;
+  if (a->q_off + qh > a->ld || a->k_off + kh > a->ld || a->v_off + kh > a->ld || qh > a->ldo)
+    return SWA_E_SHAPE;
+  if (!(a->scale == a->scale) || std::isinf(a->scale)) return SWA_E_SHAPE;
+  const int hpg = a->nh / a->nk;
+  const int rows = 128 / hpg;                   // query vectors of a CTA: rows x hpg <= 128
+  const long long n_rb = (a->max_len + rows - 1) / rows;
+  if (n_rb > 65535 || (long long)a->nseg * a->nk > 65535) return SWA_E_SHAPE;
+  if ((a->ld | a->ldo | a->q_off | a->k_off | a->v_off) & 3) return SWA_E_ALIGN;
+  if (!aligned16(a->qkv) || !aligned16(a->out) || (reinterpret_cast<uintptr_t>(a->segs) & 3u))
+    return SWA_E_ALIGN;
+  AttendParams p{};
+  p.B = a->nseg; p.t = 0; p.nh = a->nh; p.nk = a->nk; p.hd = a->hd; p.cap = 0; p.ns = 0; p.hpg = hpg;
+  p.qmul = a->scale * 1.4426950408889634f;
+  p.scale = a->scale;
+  p.out = a->out;
+  p.err = a->err;
+  p.nq = 128; p.rows = rows; p.n_rb = (int)n_rb; p.chunk = 0; p.splits = 1;
+  p.qkv = a->qkv; p.segs = a->segs;
+  p.T = a->T; p.ld = a->ld; p.q_off = a->q_off; p.k_off = a->k_off; p.v_off = a->v_off; p.ldo = a->ldo;
+  p.max_len = a->max_len;
+  return launch_flash_tc(p, stream, a->ev_start, a->ev_stop);
 }
 
 }  // extern "C"

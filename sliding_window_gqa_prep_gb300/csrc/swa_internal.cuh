@@ -69,6 +69,11 @@ struct AttendParams {
   float* t_hat;               // [B][nh][m][hd]
   float* ws_far;              // [B][nh] x (fm in log2 units, far mass, have, 0, numerator[hd])
   float scale;                // score scale in natural units (the far state's units)
+  // full-sequence attention (swa_flash): packed q|k|v rows and segments; B is
+  // the segment count there
+  const float* qkv;
+  const uint32_t* segs;       // [B][2]: first row, length
+  int T, ld, q_off, k_off, v_off, ldo, max_len;
 };
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
@@ -84,6 +89,8 @@ int attend_decode_occupancy(int hd, int nq);
 int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // prompt-chunk kernel on tcgen05 / TMEM (128 query vectors per CTA), swa_prompt_tc.cu
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+// the same kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu
+int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // verify kernel (16 or 32 query vectors per CTA, CUDA cores), swa_verify.cu
 int launch_attend_verify(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int attend_verify_occupancy(int hd, int nq);

@@ -27,8 +27,13 @@
 // Pipelining: the hi/lo operand sets and the S accumulator are double
 // buffered, so the MMA lane issues S of tile i+1 before P V of tile i and the
 // tensor cores compute the next scores while the softmax warps work on the
-// current ones; the K half of the next split needs no wait (its buffer was
-// last read by S of tile i-1), only its V half waits for P V of tile i-1.
+// current ones; the K half of split j waits for S of tile j-2 (the last reader
+// of its buffer), the V half for P V of tile j-2.
+//
+// The same kernel with FLASH = true is swa_flash's full-sequence attention
+// ("egemma2_msl.metal", cortiq-engine 0.8.17: eg_flash64 / eg_flash_staged):
+// the keys of a row block are the rows of its segment of a packed q|k|v buffer,
+// only the segment's tail is masked, and o = O / l is written directly.
 // Every hand-off is an mbarrier; all waits are bounded (1 s) and report
 // SWA_DERR_TIMEOUT; tensor memory is released on every path.
 #include "swa_internal.cuh"
@@ -125,7 +130,11 @@ __device__ __forceinline__ uint32_t tf32_hi(float x) {
   return r;
 }
 
-template <int HD>
+// FLASH = false: a row block of the token path (sinks, ring window, chunk rows;
+// split record to the workspace). FLASH = true: a row block of one segment of
+// packed q|k|v rows attending all of the segment's rows (swa_flash); blockIdx.z
+// = segment * nk + KV head, and the normalised output is written directly.
+template <int HD, bool FLASH>
 __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
   pdl_trigger();
   pdl_wait();
@@ -151,15 +160,30 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rb = blockIdx.y, bg = blockIdx.z;
   const int b = bg / p.nk, g = bg % p.nk;
-  const SeqState st = load_state(p, b, tid == 0 && g == 0 && rb == 0);
   const int r0 = rb * p.rows;
-  const int r_last = min(r0 + p.rows, p.t) - 1;
+  SeqState st{0, 0, 0};
+  int s0 = 0, r_last, xlo = 0, n;
+  if constexpr (FLASH) {
+    // segment b: rows s0 .. s0 + len - 1 of the packed buffer; keys = its rows
+    s0 = (int)p.segs[2 * b];
+    const uint32_t len = p.segs[2 * b + 1];
+    if ((uint64_t)(uint32_t)s0 + len > (uint64_t)p.T || len > (uint32_t)p.max_len) {
+      if (tid == 0 && g == 0 && rb == 0) set_err(p.err, SWA_DERR_SEGMENT);
+      return;
+    }
+    if (r0 >= (int)len) return;
+    r_last = min(r0 + p.rows, (int)len) - 1;
+    n = (int)len;
+  } else {
+    st = load_state(p, b, tid == 0 && g == 0 && rb == 0);
+    r_last = min(r0 + p.rows, p.t) - 1;
+    const int win0 = min(st.W, st.len0 + r0 + 1);
+    xlo = st.len0 + r0 + 1 - win0;
+    n = p.ns + (st.len0 + r_last - xlo + 1);
+    if (g == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = 1;
+    if (g == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
+  }
   const int rows_eff = r_last - r0 + 1;
-  const int win0 = min(st.W, st.len0 + r0 + 1);
-  const int xlo = st.len0 + r0 + 1 - win0;
-  const int n = p.ns + (st.len0 + r_last - xlo + 1);
-  if (g == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = 1;
-  if (g == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
   const int ntiles = (n + kTN - 1) / kTN;
   const size_t kv_head = (size_t)b * p.nk + g;
 
@@ -194,7 +218,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     const bool q_ok = rr < rows_eff && q < p.rows * p.hpg;
     const int r = r0 + rr;
     {
-      const float* src = p.q + (((size_t)b * p.t + r) * p.nh + (size_t)g * p.hpg + h) * HD;
+      const float* src = FLASH ? p.qkv + (size_t)(s0 + r) * p.ld + p.q_off + ((size_t)g * p.hpg + h) * HD
+                               : p.q + (((size_t)b * p.t + r) * p.nh + (size_t)g * p.hpg + h) * HD;
       for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t hi[32], lo[32];
 #pragma unroll
@@ -239,7 +264,11 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       const float* sv = nullptr;
       if (lane < cnt) {
         const int j = j0 + lane;
-        if (j < p.ns) {
+        if constexpr (FLASH) {
+          const size_t at = (size_t)(s0 + j) * p.ld + (size_t)g * HD;
+          sk = p.qkv + at + p.k_off;
+          sv = p.qkv + at + p.v_off;
+        } else if (j < p.ns) {
           const size_t at = (kv_head * p.ns + j) * HD;
           sk = p.sink_k + at;
           sv = p.sink_v + at;
@@ -429,10 +458,12 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       uint32_t sr[32];
       tc_ld32(tmem + lane_off + ((i & 1) ? C::C_S1 : C::C_S0), sr);
       tc_wait_ld();
-      // window mask; a tile wholly inside this row's window skips it
+      // window mask; a tile wholly inside this row's window skips it (a whole
+      // segment row sees every key of its segment: only the tail is masked)
       const int j0 = i * kTN;
-      const bool inside = q_ok && cnt == kTN && j0 >= p.ns && xlo + (j0 - p.ns) >= q_lo &&
-                          xlo + (j0 + kTN - 1 - p.ns) <= q_hi;
+      const bool inside = FLASH ? q_ok && cnt == kTN
+                                : q_ok && cnt == kTN && j0 >= p.ns && xlo + (j0 - p.ns) >= q_lo &&
+                                      xlo + (j0 + kTN - 1 - p.ns) <= q_hi;
       float tmax = -INFINITY;
       float s[32];
 #pragma unroll
@@ -441,7 +472,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
         if (!inside) {
           const int j = j0 + k;
           v = q_ok && k < cnt;
-          if (v && j >= p.ns) {
+          if (!FLASH && v && j >= p.ns) {
             const int x = xlo + (j - p.ns);
             v = x >= q_lo && x <= q_hi;
           }
@@ -496,7 +527,24 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     if (!dead && !*s_abort) {
       const bool ok = __all_sync(kTF, ntiles == 0 ||
                                           mbar_wait_bounded(pv_done, (uint32_t)((ntiles - 1) & 1), kWaitLimitNs));
-      if (ok) {
+      if (ok && FLASH) {
+        // o = O / l straight to the output row of this query vector
+        tc_fence_after();
+        const float inv = 1.0f / l_run;
+        float* dst = p.out + (size_t)(s0 + r) * p.ldo + ((size_t)g * p.hpg + (q % p.hpg)) * HD;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(tmem + lane_off + C::C_O + c0, o);
+          tc_wait_ld();
+          if (q_ok) {
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+              *reinterpret_cast<float4*>(dst + c0 + k) =
+                  make_float4(__uint_as_float(o[k]) * inv, __uint_as_float(o[k + 1]) * inv,
+                              __uint_as_float(o[k + 2]) * inv, __uint_as_float(o[k + 3]) * inv);
+          }
+        }
+      } else if (ok) {
         tc_fence_after();
         const size_t item = ((size_t)bg * p.n_rb + rb) * p.splits;
         float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD;
@@ -530,10 +578,10 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   }
 }
 
-template <int HD>
+template <int HD, bool FLASH>
 int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   using C = TCfg<HD>;
-  auto kern = attend_prompt_tc_kernel<HD>;
+  auto kern = attend_prompt_tc_kernel<HD, FLASH>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -555,8 +603,16 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
 
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   switch (p.hd) {
-    case 64: return launch_tc<64>(p, s, e0, e1);
-    case 128: return launch_tc<128>(p, s, e0, e1);
+    case 64: return launch_tc<64, false>(p, s, e0, e1);
+    case 128: return launch_tc<128, false>(p, s, e0, e1);
+  }
+  return SWA_E_SHAPE;
+}
+
+int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  switch (p.hd) {
+    case 64: return launch_tc<64, true>(p, s, e0, e1);
+    case 128: return launch_tc<128, true>(p, s, e0, e1);
   }
   return SWA_E_SHAPE;
 }

@@ -166,3 +166,36 @@ def test_workspace_grows_by_the_far_records(lib):
     with_far = lib.swa_attend_workspace_size(ctypes.byref(a))
     need = 2 * 1 * 8 * (4 + 128) * 4                    # B * t * nh * (4 + hd) floats
     assert with_far - base >= need and with_far - base < need + 256
+
+
+def _flash(**kw):
+    a = _abi.FlashArgs()
+    a.T, a.nseg, a.hd, a.nh, a.nk = 100, 2, 64, 8, 4
+    a.ld, a.q_off, a.k_off, a.v_off, a.ldo, a.max_len = 1024, 0, 512, 768, 512, 60
+    a.scale = 0.125
+    for f in ("qkv", "segs", "out"):
+        setattr(a, f, FAKE)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_flash_rejects_bad_arguments(lib):
+    call = lambda a: lib.swa_flash(ctypes.byref(a), None)
+    assert lib.swa_flash(None, None) == _abi.SWA_E_NULL
+    for f in ("qkv", "segs", "out"):
+        assert call(_flash(**{f: None})) == _abi.SWA_E_NULL, f
+    assert call(_flash(hd=256)) == _abi.SWA_E_SHAPE               # tensor-core tiles: hd 64 or 128
+    assert call(_flash(nh=9)) == _abi.SWA_E_SHAPE                 # nh % nk
+    assert call(_flash(nh=132, nk=2, ld=20000, k_off=8448, v_off=8576, ldo=8448)) == _abi.SWA_E_SHAPE  # hpg 66
+    assert call(_flash(nseg=0)) == _abi.SWA_E_SHAPE
+    assert call(_flash(max_len=0)) == _abi.SWA_E_SHAPE
+    assert call(_flash(max_len=101)) == _abi.SWA_E_SHAPE          # longer than the buffer
+    assert call(_flash(v_off=800)) == _abi.SWA_E_SHAPE            # V heads past the row
+    assert call(_flash(ldo=256)) == _abi.SWA_E_SHAPE              # output row too short
+    assert call(_flash(scale=float("inf"))) == _abi.SWA_E_SHAPE
+    assert call(_flash(nseg=70000)) == _abi.SWA_E_SHAPE           # grid z = nseg * nk
+    assert call(_flash(k_off=514)) == _abi.SWA_E_ALIGN            # offsets in float4 units
+    assert call(_flash(ld=1026)) == _abi.SWA_E_ALIGN
+    assert call(_flash(qkv=FAKE + 4)) == _abi.SWA_E_ALIGN
+    assert call(_flash(segs=FAKE + 2)) == _abi.SWA_E_ALIGN

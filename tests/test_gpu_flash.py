@@ -1,0 +1,87 @@
+"""Parity of swa_flash (full-sequence attention over packed q|k|v rows, on the
+tensor cores as 3xTF32) with the CPU oracle, through the C ABI on the GPU.
+
+Floating point: max_abs <= 2e-5 and max_abs / max|oracle| <= 1e-4 per tensor.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+import sliding_window_gqa_prep_gb300 as swa
+from swa_harness import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU test collected on a machine without a GPU")
+    yield
+
+
+def _run(w, segs_dev=None, out=None, err=None):
+    inp = workloads.make_flash_inputs(w)
+    qkv = inp["qkv"].cuda()
+    segs = (segs_dev if segs_dev is not None else inp["segs"]).cuda()
+    res = swa.flash(qkv, segs, hd=w.hd, nh=w.nh, nk=w.nk, q_off=w.q_off, k_off=w.k_off, v_off=w.v_off,
+                    scale=w.score_scale, max_len=w.max_len, out=out, err=err)
+    torch.cuda.synchronize()
+    return inp, res.cpu().numpy()
+
+
+def _oracle(w, inp, segs=None):
+    return oracle.flash_attention(inp["qkv"].numpy(), segs if segs is not None else w.segs, w.hd, w.nh, w.group,
+                                  w.q_off, w.k_off, w.v_off, w.score_scale)
+
+
+FLASH_CASES = [
+    # group 1 (128 rows per CTA): a one-row segment, exactly 128 rows, ragged tails
+    dict(segs=((0, 1), (1, 37), (40, 128), (170, 300)), T=480, nh=4, nk=4, hd=64, seed=1),
+    # group 4 (32 rows per CTA), hd 128, offsets inside a padded row
+    dict(segs=((3, 200), (210, 33)), T=250, nh=8, nk=2, hd=128, seed=2, pad=8),
+    # group 6 (21 rows = 126 of 128 query slots per CTA)
+    dict(segs=((0, 90), (90, 64)), T=160, nh=12, nk=2, hd=64, seed=3, pad=4),
+    # a sharp softmax (scores of several units), exercising the lazy running max
+    dict(segs=((0, 257),), T=257, nh=2, nk=1, hd=128, seed=4, scale=0.5),
+]
+
+
+@pytest.mark.parametrize("kw", FLASH_CASES)
+def test_flash_matches_oracle(kw):
+    w = workloads.FlashWorkload("case", **kw)
+    inp, got = _run(w)
+    ref = _oracle(w, inp)
+    rows = np.concatenate([np.arange(s0, s0 + n) for s0, n in w.segs])
+    assert_close(got[rows], ref[rows], "flash out")
+    outside = np.setdiff1d(np.arange(w.T), rows)
+    assert not got[outside].any()                       # rows outside every segment untouched
+
+
+def test_flash_skips_bad_and_empty_segments_and_reports_them():
+    w = workloads.FlashWorkload("case", segs=((0, 50), (50, 0), (60, 40)), T=100, nh=4, nk=2, hd=64, seed=5)
+    bad = torch.tensor([[0, 50], [50, 0], [60, 41]], dtype=torch.int32)   # the last reaches row 101
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full((w.T, w.nh * w.hd), 7.0, device="cuda")
+    inp, got = _run(w, segs_dev=bad, out=out, err=err)
+    assert int(err.item()) & 4                             # SWA_DERR_SEGMENT
+    ref = _oracle(w, inp, segs=[(0, 50)])
+    assert_close(got[0:50], ref[0:50], "flash out")
+    assert np.all(got[50:] == 7.0)                         # the empty and the bad segment wrote nothing
+
+
+def test_flash_full_size_workload_sampled():
+    """The benchmark's workload (9801 patches, 16 heads of 64) in the launch the
+    bench times, compared with the oracle on sampled rows."""
+    w = workloads.FLASH_WORKLOADS["vision_flash"]
+    inp, got = _run(w)
+    qkv = inp["qkv"].numpy()
+    rng = np.random.default_rng(11)
+    picks = [(0, 0), (w.T - 1, w.nh - 1)] + [(int(rng.integers(w.T)), int(rng.integers(w.nh))) for _ in range(22)]
+    ref = np.stack([oracle.flash_row(qkv, 0, w.T, r, h, w.hd, w.group, w.q_off, w.k_off, w.v_off, w.score_scale)
+                    for r, h in picks])
+    gpu = np.stack([got[r, h * w.hd:(h + 1) * w.hd] for r, h in picks])
+    assert_close(gpu, ref, "flash sampled out")
+    assert np.all(np.isfinite(got))

@@ -195,3 +195,71 @@ def kv_keys_and_bytes(w: Workload, meta) -> tuple:
             keys += w.ns + min(W, L + i + 1)
         distinct += w.ns + min(L + w.t, W + w.t - 1)
     return keys * w.nk, distinct * w.nk * 2 * w.hd * 4
+
+
+# ---------------------------------------------------------------------------
+# Full-sequence attention over packed q|k|v rows (the second workload,
+# "egemma2_msl.metal" eg_flash64 / eg_flash_staged: a vision tower's patch
+# sequence with head dim 64). A row holds [pad | q heads | k heads | v heads |
+# pad]; segments are (first row, length). qkv ~ N(0, 1), drawn in one call.
+# ---------------------------------------------------------------------------
+@dataclasses.dataclass(frozen=True)
+class FlashWorkload:
+    name: str
+    segs: tuple      # ((first row, length), ...)
+    T: int           # rows of the packed buffer
+    nh: int          # query heads
+    nk: int          # KV heads
+    hd: int          # head dim
+    seed: int
+    scale: Optional[float] = None   # None -> 1/sqrt(hd)
+    pad: int = 0                     # floats before the q heads and after the v heads (multiple of 4)
+
+    @property
+    def group(self) -> int:
+        return self.nh // self.nk
+
+    @property
+    def q_off(self) -> int:
+        return self.pad
+
+    @property
+    def k_off(self) -> int:
+        return self.pad + self.nh * self.hd
+
+    @property
+    def v_off(self) -> int:
+        return self.k_off + self.nk * self.hd
+
+    @property
+    def ld(self) -> int:
+        return self.v_off + self.nk * self.hd + self.pad
+
+    @property
+    def max_len(self) -> int:
+        return max(1, max(n for _, n in self.segs))
+
+    @property
+    def score_scale(self) -> float:
+        return self.scale if self.scale is not None else 1.0 / math.sqrt(self.hd)
+
+
+# one vision-tower image: 99 x 99 = 9801 patches, 16 heads of 64
+FLASH_WORKLOADS: Dict[str, FlashWorkload] = {
+    "vision_flash": FlashWorkload("vision_flash", segs=((0, 9801),), T=9801, nh=16, nk=16, hd=64, seed=7),
+}
+
+
+def make_flash_inputs(w: FlashWorkload) -> Dict[str, torch.Tensor]:
+    g = torch.Generator().manual_seed(w.seed)
+    return {"qkv": torch.randn(w.T, w.ld, generator=g),
+            "segs": torch.tensor([list(s) for s in w.segs], dtype=torch.int32).reshape(len(w.segs), 2)}
+
+
+def flash_keys_and_flops(w: FlashWorkload) -> tuple:
+    """Attended keys of one call counted per (query row, KV head) as the token
+    path counts them (each serves nh / nk query heads), and the useful flops
+    (4 * hd per (query row, query head, key): the score and the value sum); a
+    measurement definition."""
+    pairs = sum(n * n for _, n in w.segs)
+    return pairs * w.nk, 4 * w.hd * pairs * w.nh
