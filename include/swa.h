@@ -324,11 +324,18 @@ int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);
  *   err      optional device word (SWA_DERR_SEGMENT, SWA_DERR_TIMEOUT).
  *   ev_start, ev_stop  optional events recorded on `stream` right before and
  *            after the attention kernel (NULL: none).
- * The call enqueues one kernel, allocates nothing and needs no workspace.
- * Errors: SWA_E_NULL (qkv, segs or out NULL), SWA_E_SHAPE (sizes, offsets past
- * ld, nh * hd > ldo, nseg < 1, max_len < 1, scale not finite), SWA_E_ALIGN
- * (pointers not 16-byte aligned, or ld / ldo / offsets not multiples of 4),
- * SWA_E_CUDA.
+ *   workspace, workspace_bytes  optional device scratch (256-byte aligned) of
+ *            at least swa_flash_workspace_size(args) bytes. With it, a first
+ *            kernel splits each KV head's K and V rows into TF32 hi/lo operand
+ *            blocks of 32 keys once per call (instead of once per block of
+ *            query vectors) and the attention kernel copies them in whole
+ *            blocks; without it (NULL), the attention kernel splits the rows it
+ *            stages itself. Both give bit-identical outputs.
+ * The call allocates nothing. Errors: SWA_E_NULL (qkv, segs or out NULL),
+ * SWA_E_SHAPE (sizes, offsets past ld, nh * hd > ldo, nseg < 1, max_len < 1,
+ * scale not finite), SWA_E_ALIGN (pointers not 16-byte aligned, workspace not
+ * 256-byte aligned, or ld / ldo / offsets not multiples of 4),
+ * SWA_E_WORKSPACE (a workspace smaller than needed), SWA_E_CUDA.
  */
 typedef struct swa_flash_args {
   int T, nseg, hd, nh, nk;
@@ -340,7 +347,12 @@ typedef struct swa_flash_args {
   float* out;                  /* [T][ldo] */
   uint32_t* err;               /* optional */
   cudaEvent_t ev_start, ev_stop;  /* optional */
+  void* workspace;             /* optional */
+  size_t workspace_bytes;
 } swa_flash_args;
+/* Workspace bytes of the split-once form of swa_flash: nseg * nk *
+ * ceil(max_len / 32) blocks of 4 x 32 x hd floats; 0 for unsupported sizes. */
+size_t swa_flash_workspace_size(const swa_flash_args* args);
 int swa_flash(const swa_flash_args* args, cudaStream_t stream);
 
 #ifdef __cplusplus

@@ -197,13 +197,30 @@ def rollback(meta: torch.Tensor, n_back: torch.Tensor, cap: int, err=None, strea
     return meta
 
 
+def _flash_struct(T, nseg, hd, nh, nk, ld, q_off, k_off, v_off, ldo, max_len, scale) -> _abi.FlashArgs:
+    a = _abi.FlashArgs()
+    a.T, a.nseg, a.hd, a.nh, a.nk = T, nseg, hd, nh, nk
+    a.ld, a.q_off, a.k_off, a.v_off, a.ldo, a.max_len = ld, q_off, k_off, v_off, ldo, int(max_len)
+    a.scale = float(scale)
+    return a
+
+
+def flash_workspace_size(T, nseg, hd, nh, nk, max_len) -> int:
+    """Bytes of swa_flash's split-once workspace (0 for unsupported sizes)."""
+    a = _flash_struct(T, nseg, hd, nh, nk, 3 * nh * hd, 0, nh * hd, (nh + nk) * hd, nh * hd, max_len, 1.0)
+    return int(library().swa_flash_workspace_size(ctypes.byref(a)))
+
+
 def flash(qkv: torch.Tensor, segs: torch.Tensor, *, hd: int, nh: int, nk: int, q_off: int, k_off: int,
           v_off: int, scale: float, max_len: int, out: Optional[torch.Tensor] = None, ldo: Optional[int] = None,
-          err=None, ev_start=None, ev_stop=None, stream=None) -> torch.Tensor:
+          err=None, ev_start=None, ev_stop=None, workspace: Optional[torch.Tensor] = None,
+          stream=None) -> torch.Tensor:
     """Full-sequence attention over packed q|k|v rows (swa_flash): qkv [T][ld],
     segs [nseg][2] int32 (first row, length), every row of a segment attends
     every row of the segment. Returns out [T][ldo] (rows outside every segment
-    are left as they were; a new output starts zeroed)."""
+    are left as they were; a new output starts zeroed). With `workspace` (a
+    uint8 CUDA tensor of at least flash_workspace_size bytes) each KV head's
+    K/V rows are split into TF32 operand blocks once per call."""
     if qkv.dim() != 2:
         raise ValueError("qkv must be [T][ld]")
     T, ld = qkv.shape
@@ -212,10 +229,10 @@ def flash(qkv: torch.Tensor, segs: torch.Tensor, *, hd: int, nh: int, nk: int, q
         ldo = nh * hd
     if out is None:
         out = torch.zeros(T, ldo, device=qkv.device, dtype=torch.float32)
-    a = _abi.FlashArgs()
-    a.T, a.nseg, a.hd, a.nh, a.nk = T, nseg, hd, nh, nk
-    a.ld, a.q_off, a.k_off, a.v_off, a.ldo, a.max_len = ld, q_off, k_off, v_off, ldo, int(max_len)
-    a.scale = float(scale)
+    a = _flash_struct(T, nseg, hd, nh, nk, ld, q_off, k_off, v_off, ldo, max_len, scale)
+    if workspace is not None:
+        a.workspace = _ptr(workspace, "workspace", dtype=torch.uint8)
+        a.workspace_bytes = workspace.numel()
     a.qkv = _ptr(qkv, "qkv", (T, ld))
     a.segs = _ptr(segs, "segs", (nseg, 2), torch.int32)
     a.out = _ptr(out, "out", (T, ldo))

@@ -66,6 +66,7 @@ class FlashArgs(ctypes.Structure):
         ("scale", ctypes.c_float),
         ("qkv", c_float_p), ("segs", ctypes.c_void_p), ("out", c_float_p), ("err", ctypes.c_void_p),
         ("ev_start", ctypes.c_void_p), ("ev_stop", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
 
@@ -111,6 +112,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.swa_attend.argtypes = [ctypes.POINTER(AttendArgs), ctypes.c_void_p]
     lib.swa_flash.restype = ctypes.c_int
     lib.swa_flash.argtypes = [ctypes.POINTER(FlashArgs), ctypes.c_void_p]
+    lib.swa_flash_workspace_size.restype = ctypes.c_size_t
+    lib.swa_flash_workspace_size.argtypes = [ctypes.POINTER(FlashArgs)]
     _lib = lib
     return lib
 

@@ -300,13 +300,27 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   return launch_attend_merge(p, stream);
 }
 
+static bool flash_shape_ok(const swa_flash_args* a) {
+  if (a->T < 1 || a->nseg < 1 || a->nh < 1 || a->nk < 1 || a->max_len < 1 || a->max_len > a->T) return false;
+  if (a->hd != 64 && a->hd != 128) return false;
+  return a->nh % a->nk == 0 && a->nh / a->nk <= 32;
+}
+
+// split-once operand blocks: [nseg][nk][ceil(max_len / 32)][4][32][hd] floats
+static size_t flash_ops_bytes(const swa_flash_args* a) {
+  const size_t nblk = ((size_t)a->max_len + kFlashBlockKeys - 1) / kFlashBlockKeys;
+  return (size_t)a->nseg * a->nk * nblk * 4 * kFlashBlockKeys * a->hd * sizeof(float);
+}
+
+size_t swa_flash_workspace_size(const swa_flash_args* a) {
+  if (!a || !flash_shape_ok(a)) return 0;
+  return flash_ops_bytes(a);
+}
+
 int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   if (!a) return SWA_E_NULL;
   if (!a->qkv || !a->segs || !a->out) return SWA_E_NULL;
-  if (a->T < 1 || a->nseg < 1 || a->nh < 1 || a->nk < 1 || a->max_len < 1 || a->max_len > a->T)
-    return SWA_E_SHAPE;
-  if (a->hd != 64 && a->hd != 128) return SWA_E_SHAPE;
-  if (a->nh % a->nk != 0 || a->nh / a->nk > 32) return SWA_E_SHAPE;
+  if (!flash_shape_ok(a)) return SWA_E_SHAPE;
   if (a->ld < 1 || a->ldo < 1 || a->q_off < 0 || a->k_off < 0 || a->v_off < 0) return SWA_E_SHAPE;
   const long long qh = (long long)a->nh * a->hd, kh = (long long)a->nk * a->hd;
   if (a->q_off + qh > a->ld || a->k_off + kh > a->ld || a->v_off + kh > a->ld || qh > a->ldo)
@@ -319,6 +333,10 @@ int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   if ((a->ld | a->ldo | a->q_off | a->k_off | a->v_off) & 3) return SWA_E_ALIGN;
   if (!aligned16(a->qkv) || !aligned16(a->out) || (reinterpret_cast<uintptr_t>(a->segs) & 3u))
     return SWA_E_ALIGN;
+  if (a->workspace) {
+    if (a->workspace_bytes < flash_ops_bytes(a)) return SWA_E_WORKSPACE;
+    if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return SWA_E_ALIGN;
+  }
   AttendParams p{};
   p.B = a->nseg; p.t = 0; p.nh = a->nh; p.nk = a->nk; p.hd = a->hd; p.cap = 0; p.ns = 0; p.hpg = hpg;
   p.qmul = a->scale * 1.4426950408889634f;
@@ -329,6 +347,8 @@ int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   p.qkv = a->qkv; p.segs = a->segs;
   p.T = a->T; p.ld = a->ld; p.q_off = a->q_off; p.k_off = a->k_off; p.v_off = a->v_off; p.ldo = a->ldo;
   p.max_len = a->max_len;
+  p.flash_ops = static_cast<float*>(a->workspace);
+  p.flash_nblk = (a->max_len + kFlashBlockKeys - 1) / kFlashBlockKeys;
   return launch_flash_tc(p, stream, a->ev_start, a->ev_stop);
 }
 

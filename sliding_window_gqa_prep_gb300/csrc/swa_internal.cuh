@@ -74,6 +74,8 @@ struct AttendParams {
   const float* qkv;
   const uint32_t* segs;       // [B][2]: first row, length
   int T, ld, q_off, k_off, v_off, ldo, max_len;
+  float* flash_ops;           // split-once operand blocks [B][nk][flash_nblk][4][32][hd], or null
+  int flash_nblk;             // blocks of 32 keys per (segment, KV head) in flash_ops
 };
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
@@ -89,8 +91,10 @@ int attend_decode_occupancy(int hd, int nq);
 int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // prompt-chunk kernel on tcgen05 / TMEM (128 query vectors per CTA), swa_prompt_tc.cu
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
-// the same kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu
+// the same kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu;
+// with p.flash_ops set it first splits every KV head's K/V rows into operand blocks once
 int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+constexpr int kFlashBlockKeys = 32;   // keys per split-once operand block (= the kernel's key tile)
 // verify kernel (16 or 32 query vectors per CTA, CUDA cores), swa_verify.cu
 int launch_attend_verify(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int attend_verify_occupancy(int hd, int nq);

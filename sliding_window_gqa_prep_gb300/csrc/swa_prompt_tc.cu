@@ -30,10 +30,14 @@
 // current ones; the K half of split j waits for S of tile j-2 (the last reader
 // of its buffer), the V half for P V of tile j-2.
 //
-// The same kernel with FLASH = true is swa_flash's full-sequence attention
+// The same kernel with MODE 1 or 2 is swa_flash's full-sequence attention
 // ("egemma2_msl.metal", cortiq-engine 0.8.17: eg_flash64 / eg_flash_staged):
 // the keys of a row block are the rows of its segment of a packed q|k|v buffer,
-// only the segment's tail is masked, and o = O / l is written directly.
+// only the segment's tail is masked, and o = O / l is written directly. In
+// MODE 2 flash_presplit_kernel has already split each KV head's K/V rows into
+// the four operand blocks of every 32-key tile (the split warps' output layout),
+// once per call: the producer lands them straight in the operand set (four
+// contiguous copies per tile) and the split warps sit idle.
 // Every hand-off is an mbarrier; all waits are bounded (1 s) and report
 // SWA_DERR_TIMEOUT; tensor memory is released on every path.
 #include "swa_internal.cuh"
@@ -48,8 +52,12 @@ constexpr int kSoftThreads = 128;
 constexpr unsigned kTF = 0xffffffffu;
 constexpr float kLazyMax = 8.0f;       // log2 headroom before the running max is raised
 
-template <int HD>
+template <int HD, int MODE = 0>
 struct TCfg {
+  // operand sets: two behind the split warps; with split-once blocks (MODE 2) the
+  // landing stages are unused and their room holds more sets, so the producer runs
+  // further ahead of the MMAs
+  static constexpr int NSETS = MODE != 2 ? 2 : (HD == 64 ? 4 : 3);
   // TMEM columns
   static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S0 = 2 * HD, C_S1 = 2 * HD + kTN;
   static constexpr uint32_t C_O = 2 * HD + 2 * kTN, C_PHI = 3 * HD + 2 * kTN, C_PLO = 3 * HD + 3 * kTN;
@@ -59,10 +67,10 @@ struct TCfg {
   static constexpr int LAND = kTN * HD * 4;                 // one fp32 tile of K or V
   static constexpr int OFF_LK = 0;                          // [2 stages] K landing
   static constexpr int OFF_LV = 2 * LAND;                   // [2 stages] V landing
-  static constexpr int OFF_OPS = 4 * LAND;                  // [2 sets] K_hi, K_lo, V^T_hi, V^T_lo
+  static constexpr int OFF_OPS = MODE != 2 ? 4 * LAND : 0;  // [NSETS] K_hi, K_lo, V^T_hi, V^T_lo
   static constexpr int SET = 4 * LAND;
-  static constexpr int OFF_BAR = OFF_OPS + 2 * SET;         // mbarriers
-  static constexpr int NBAR = 14;
+  static constexpr int OFF_BAR = OFF_OPS + NSETS * SET;     // mbarriers
+  static constexpr int NBAR = 16;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
@@ -130,15 +138,20 @@ __device__ __forceinline__ uint32_t tf32_hi(float x) {
   return r;
 }
 
-// FLASH = false: a row block of the token path (sinks, ring window, chunk rows;
-// split record to the workspace). FLASH = true: a row block of one segment of
-// packed q|k|v rows attending all of the segment's rows (swa_flash); blockIdx.z
-// = segment * nk + KV head, and the normalised output is written directly.
-template <int HD, bool FLASH>
+// MODE 0: a row block of the token path (sinks, ring window, chunk rows; split
+// record to the workspace). MODE 1 / 2: a row block of one segment of packed
+// q|k|v rows attending all of the segment's rows (swa_flash); blockIdx.z =
+// segment * nk + KV head, and the normalised output is written directly; MODE 2
+// takes split-once operand blocks from p.flash_ops.
+template <int HD, int MODE>
 __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
+  constexpr bool FLASH = MODE != 0;
+  constexpr bool PRESPLIT = MODE == 2;
+  constexpr int NS = TCfg<HD, MODE>::NSETS;    // operand sets: tile j uses set j % NS
+  static_assert(PRESPLIT || NS == 2, "the split warps use two operand sets");
   pdl_trigger();
   pdl_wait();
-  using C = TCfg<HD>;
+  using C = TCfg<HD, MODE>;
   extern __shared__ __align__(1024) unsigned char sm[];
   float* landK = reinterpret_cast<float*>(sm + C::OFF_LK);
   float* landV = reinterpret_cast<float*>(sm + C::OFF_LV);
@@ -147,15 +160,15 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     return reinterpret_cast<uint32_t*>(sm + C::OFF_OPS + set * C::SET + which * C::LAND);
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
-  uint64_t* land_full = bars + 0;    // [2] producer -> softmax warps (bytes)
-  uint64_t* land_empty = bars + 2;   // [2] softmax warps -> producer (4 arrivals)
-  uint64_t* split_done = bars + 4;   // [2 sets] softmax warps -> MMA (4 arrivals)
-  uint64_t* s_full = bars + 6;       // [2 S buffers] MMA commit -> softmax warps
-  uint64_t* p_ready = bars + 8;      // softmax warps -> MMA (4 arrivals)
-  uint64_t* pv_done = bars + 9;      // MMA commit -> softmax warps
-  uint64_t* v_free = bars + 10;      // [2 sets] MMA commit (P V of the set done) -> split warps
-  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + 12);
-  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + 12) + 1);
+  uint64_t* land_full = bars + 0;    // [2] producer -> split warps (bytes)
+  uint64_t* land_empty = bars + 2;   // [2] split warps -> producer (4 arrivals)
+  uint64_t* split_done = bars + 4;   // [NS sets] split warps (4 arrivals) or split-once copies -> MMA
+  uint64_t* s_full = bars + 8;       // [2 S buffers] MMA commit -> softmax warps
+  uint64_t* p_ready = bars + 10;     // softmax warps -> MMA (4 arrivals)
+  uint64_t* pv_done = bars + 11;     // MMA commit -> softmax warps
+  uint64_t* v_free = bars + 12;      // [NS sets] MMA commit (P V of the set done) -> split warps / producer
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + C::NBAR);
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + C::NBAR) + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rb = blockIdx.y, bg = blockIdx.z;
@@ -192,14 +205,15 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     mbar_init(&land_full[1], 1);
     mbar_init(&land_empty[0], 4);
     mbar_init(&land_empty[1], 4);
-    mbar_init(&split_done[0], 4);
-    mbar_init(&split_done[1], 4);
+    for (int k = 0; k < NS; ++k) {
+      // split warps' 4 arrivals, or the producer's one arrival + bytes (MODE 2)
+      mbar_init(&split_done[k], PRESPLIT ? 1 : 4);
+      mbar_init(&v_free[k], 1);
+    }
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
     mbar_init(p_ready, 4);
     mbar_init(pv_done, 1);
-    mbar_init(&v_free[0], 1);
-    mbar_init(&v_free[1], 1);
     mbar_fence_init();
     *s_abort = 0;
   }
@@ -244,7 +258,36 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   tc_fence_after();
 
   // ------------------------------------------------------------------ producer
-  if (warp == 4) {
+  if (PRESPLIT && warp == 4) {
+    // the four operand blocks of tile i into set i % NS, once P V of tile i - NS (the
+    // set's last reader; its commit follows S of tile i - NS as well) is done
+    const float* blocks = p.flash_ops + (size_t)bg * p.flash_nblk * 4 * (kTN * HD);
+    int issued = 0;
+    for (int i = 0; i < ntiles; ++i) {
+      const int set = i % NS;
+      bool ok = i < NS || mbar_wait_bounded(&v_free[set], (uint32_t)(((i - NS) / NS) & 1), kWaitLimitNs);
+      ok = __all_sync(kTF, ok);
+      if (!ok) {
+        if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
+        break;
+      }
+      if (__shfl_sync(kTF, *s_abort, 0)) break;
+      if (lane == 0) {
+        const float* src = blocks + (size_t)i * 4 * (kTN * HD);
+        mbar_arrive_expect_tx(&split_done[set], (uint32_t)(4 * C::LAND));
+        for (int which = 0; which < 4; ++which)
+          bulk_g2s(op(set, which), src + (size_t)which * (kTN * HD), (uint32_t)C::LAND, &split_done[set]);
+      }
+      __syncwarp();
+      issued = i + 1;
+    }
+    // copies still in flight after an abort land before the CTA exits (bounded; on
+    // the normal path the MMA lane has already seen them)
+    if (lane == 0)
+      for (int i = max(0, issued - NS); i < issued; ++i)
+        mbar_wait_bounded(&split_done[i % NS], (uint32_t)((i / NS) & 1), kWaitLimitNs);
+  }
+  if (!PRESPLIT && warp == 4) {
     for (int i = 0; i < ntiles; ++i) {
       const int stage = i & 1;
       const int use = i >> 1;
@@ -308,11 +351,11 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     const uint32_t id_o = tc_idesc(kTM, HD);
     // S(j) = Q_lo K_hi + Q_hi K_lo + Q_hi K_hi of tile j into S buffer j % 2
     auto issue_s = [&](int j) -> bool {
-      const int set = j & 1;
-      if (!mbar_wait_bounded(&split_done[set], (uint32_t)((j >> 1) & 1), kWaitLimitNs) || *s_abort)
+      const int set = j % NS, sb = j & 1;          // operand set, S buffer
+      if (!mbar_wait_bounded(&split_done[set], (uint32_t)((j / NS) & 1), kWaitLimitNs) || *s_abort)
         return false;
       tc_fence_after();
-      const uint32_t dcol = set ? C::C_S1 : C::C_S0;
+      const uint32_t dcol = sb ? C::C_S1 : C::C_S0;
 #pragma unroll 1
       for (int term = 0; term < 3; ++term) {
         const uint32_t qcol = term == 0 ? C::C_QLO : C::C_QHI;
@@ -322,7 +365,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
           tc_mma(tmem + dcol, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
         }
       }
-      tc_commit(&s_full[set]);
+      tc_commit(&s_full[sb]);
       return true;
     };
     bool ok = ntiles == 0 || issue_s(0);
@@ -331,7 +374,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       if (!mbar_wait_bounded(p_ready, (uint32_t)(i & 1), kWaitLimitNs) || *s_abort) { ok = false; break; }
       tc_fence_after();
       // O += P_lo V_hi + P_hi V_lo + P_hi V_hi over 32 / 8 steps of K = 8
-      const int set = i & 1;
+      const int set = i % NS;
 #pragma unroll 1
       for (int term = 0; term < 3; ++term) {
         const uint32_t pcol = term == 0 ? C::C_PLO : C::C_PHI;
@@ -351,7 +394,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   }
 
   // ------------------------------------------------------------------ split warps
-  if (warp >= 6) {
+  if (!PRESPLIT && warp >= 6) {
     const int sidx = tid - 6 * 32;                     // 0 .. 127
     // fp32 landing tile j -> TF32 hi/lo operands of set j % 2.
     // K: element (key, f) -> (key/8)*K_SBO + (f/4)*128 + (key%8)*16 + (f%4)*4 bytes. Lane t of an
@@ -578,10 +621,73 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   }
 }
 
-template <int HD, bool FLASH>
-int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+// One CTA per (segment, KV head, 32-key block): the block's K rows as TF32 hi/lo
+// in the K-major layout of the kernel's K operand ((key / 8) * K_SBO + (f / 4) *
+// 128 + (key % 8) * 16 + (f % 4) * 4 bytes) and its V rows transposed likewise
+// ((f / 8) * V_SBO + (key / 4) * 128 + (f % 8) * 16 + (key % 4) * 4); keys past
+// the segment are zeros. Same arithmetic as the split warps: bit-identical.
+template <int HD>
+__global__ void __launch_bounds__(256) flash_presplit_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
   using C = TCfg<HD>;
-  auto kern = attend_prompt_tc_kernel<HD, FLASH>;
+  constexpr int D4 = HD / 4;
+  __shared__ __align__(16) float vs[kTN][HD + 4];
+  const int blk = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.nk, g = bg % p.nk;
+  const uint32_t s0 = p.segs[2 * b], len = p.segs[2 * b + 1];
+  if ((uint64_t)s0 + len > (uint64_t)p.T || len > (uint32_t)p.max_len) return;   // the attention reports it
+  const int j0 = blk * kTN;
+  if (j0 >= (int)len) return;
+  const int cnt = min(kTN, (int)len - j0);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(p.flash_ops + ((size_t)bg * p.flash_nblk + blk) * 4 * (kTN * HD));
+  // K: thread -> (key, f4) with key % 8 fastest, so 8 threads write 128 contiguous bytes
+  for (int idx = threadIdx.x; idx < kTN * D4; idx += blockDim.x) {
+    const int key = (idx & 7) + 8 * (idx / (8 * D4)), f4 = (idx >> 3) % D4;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 w = v;
+    if (key < cnt) {
+      const size_t row = (size_t)(s0 + j0 + key) * p.ld + (size_t)g * HD + f4 * 4;
+      v = *reinterpret_cast<const float4*>(p.qkv + row + p.k_off);
+      w = *reinterpret_cast<const float4*>(p.qkv + row + p.v_off);
+    }
+    *reinterpret_cast<float4*>(&vs[key][f4 * 4]) = w;
+    const float x[4] = {v.x, v.y, v.z, v.w};
+    uint4 hv, lv;
+    uint32_t* hp = &hv.x;
+    uint32_t* lp = &lv.x;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      hp[e] = tf32_hi(x[e]);
+      lp[e] = tf32_hi(x[e] - __uint_as_float(hp[e]));
+    }
+    const int off = ((key >> 3) * (int)C::K_SBO + f4 * 128 + (key & 7) * 16) / 4;
+    *reinterpret_cast<uint4*>(dst + off) = hv;
+    *reinterpret_cast<uint4*>(dst + kTN * HD + off) = lv;
+  }
+  __syncthreads();
+  // V^T: thread -> (f, 4 keys) with f % 8 fastest
+  for (int idx = threadIdx.x; idx < HD * kTN / 4; idx += blockDim.x) {
+    const int f = idx % HD, k4 = idx / HD;
+    uint4 hv, lv;
+    uint32_t* hp = &hv.x;
+    uint32_t* lp = &lv.x;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x = vs[k4 * 4 + e][f];
+      hp[e] = tf32_hi(x);
+      lp[e] = tf32_hi(x - __uint_as_float(hp[e]));
+    }
+    const int off = ((f >> 3) * (int)C::V_SBO + k4 * 128 + (f & 7) * 16) / 4;
+    *reinterpret_cast<uint4*>(dst + 2 * kTN * HD + off) = hv;
+    *reinterpret_cast<uint4*>(dst + 3 * kTN * HD + off) = lv;
+  }
+}
+
+template <int HD, int MODE>
+int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  using C = TCfg<HD, MODE>;
+  auto kern = attend_prompt_tc_kernel<HD, MODE>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -589,6 +695,11 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
     if (e != cudaSuccess) return cuda_status(e);
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  if (MODE == 2) {
+    const dim3 pgrid((unsigned)p.flash_nblk, (unsigned)(p.B * p.nk));
+    const int rc = finish_launch(launch_pdl(flash_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p));
+    if (rc != SWA_OK) return rc;
   }
   dim3 grid(1u, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
   if (e0) cudaEventRecord(e0, s);
@@ -603,16 +714,16 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
 
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   switch (p.hd) {
-    case 64: return launch_tc<64, false>(p, s, e0, e1);
-    case 128: return launch_tc<128, false>(p, s, e0, e1);
+    case 64: return launch_tc<64, 0>(p, s, e0, e1);
+    case 128: return launch_tc<128, 0>(p, s, e0, e1);
   }
   return SWA_E_SHAPE;
 }
 
 int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   switch (p.hd) {
-    case 64: return launch_tc<64, true>(p, s, e0, e1);
-    case 128: return launch_tc<128, true>(p, s, e0, e1);
+    case 64: return p.flash_ops ? launch_tc<64, 2>(p, s, e0, e1) : launch_tc<64, 1>(p, s, e0, e1);
+    case 128: return p.flash_ops ? launch_tc<128, 2>(p, s, e0, e1) : launch_tc<128, 1>(p, s, e0, e1);
   }
   return SWA_E_SHAPE;
 }

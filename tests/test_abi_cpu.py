@@ -199,3 +199,14 @@ def test_flash_rejects_bad_arguments(lib):
     assert call(_flash(ld=1026)) == _abi.SWA_E_ALIGN
     assert call(_flash(qkv=FAKE + 4)) == _abi.SWA_E_ALIGN
     assert call(_flash(segs=FAKE + 2)) == _abi.SWA_E_ALIGN
+
+
+def test_flash_workspace_size_and_checks(lib):
+    a = _flash()
+    need = lib.swa_flash_workspace_size(ctypes.byref(a))
+    assert need == 2 * 4 * 2 * 4 * 32 * 64 * 4          # nseg * nk * ceil(60 / 32) blocks of 4 x 32 x hd floats
+    assert lib.swa_flash_workspace_size(None) == 0
+    assert lib.swa_flash_workspace_size(ctypes.byref(_flash(hd=256))) == 0
+    call = lambda a: lib.swa_flash(ctypes.byref(a), None)
+    assert call(_flash(workspace=FAKE, workspace_bytes=need - 1)) == _abi.SWA_E_WORKSPACE
+    assert call(_flash(workspace=FAKE + 16, workspace_bytes=need)) == _abi.SWA_E_ALIGN   # wants 256 B

@@ -22,12 +22,16 @@ def _gpu():
     yield
 
 
-def _run(w, segs_dev=None, out=None, err=None):
+def _run(w, segs_dev=None, out=None, err=None, split_once=False):
     inp = workloads.make_flash_inputs(w)
     qkv = inp["qkv"].cuda()
     segs = (segs_dev if segs_dev is not None else inp["segs"]).cuda()
+    ws = None
+    if split_once:
+        n = swa.flash_workspace_size(w.T, len(w.segs), w.hd, w.nh, w.nk, w.max_len)
+        ws = torch.full((n,), 0xFF, dtype=torch.uint8, device="cuda")      # NaN bit patterns
     res = swa.flash(qkv, segs, hd=w.hd, nh=w.nh, nk=w.nk, q_off=w.q_off, k_off=w.k_off, v_off=w.v_off,
-                    scale=w.score_scale, max_len=w.max_len, out=out, err=err)
+                    scale=w.score_scale, max_len=w.max_len, out=out, err=err, workspace=ws)
     torch.cuda.synchronize()
     return inp, res.cpu().numpy()
 
@@ -49,10 +53,13 @@ FLASH_CASES = [
 ]
 
 
+@pytest.mark.parametrize("split_once", [False, True])
 @pytest.mark.parametrize("kw", FLASH_CASES)
-def test_flash_matches_oracle(kw):
+def test_flash_matches_oracle(kw, split_once):
+    """Both forms: K/V split in the attention kernel, and split once per call into a
+    workspace (poisoned with NaN bit patterns first)."""
     w = workloads.FlashWorkload("case", **kw)
-    inp, got = _run(w)
+    inp, got = _run(w, split_once=split_once)
     ref = _oracle(w, inp)
     rows = np.concatenate([np.arange(s0, s0 + n) for s0, n in w.segs])
     assert_close(got[rows], ref[rows], "flash out")
@@ -60,12 +67,20 @@ def test_flash_matches_oracle(kw):
     assert not got[outside].any()                       # rows outside every segment untouched
 
 
+@pytest.mark.parametrize("kw", FLASH_CASES[:2])
+def test_flash_split_once_is_bit_identical(kw):
+    w = workloads.FlashWorkload("case", **kw)
+    _, a = _run(w)
+    _, b = _run(w, split_once=True)
+    np.testing.assert_array_equal(a, b)
+
+
 def test_flash_skips_bad_and_empty_segments_and_reports_them():
     w = workloads.FlashWorkload("case", segs=((0, 50), (50, 0), (60, 40)), T=100, nh=4, nk=2, hd=64, seed=5)
     bad = torch.tensor([[0, 50], [50, 0], [60, 41]], dtype=torch.int32)   # the last reaches row 101
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.full((w.T, w.nh * w.hd), 7.0, device="cuda")
-    inp, got = _run(w, segs_dev=bad, out=out, err=err)
+    inp, got = _run(w, segs_dev=bad, out=out, err=err, split_once=True)
     assert int(err.item()) & 4                             # SWA_DERR_SEGMENT
     ref = _oracle(w, inp, segs=[(0, 50)])
     assert_close(got[0:50], ref[0:50], "flash out")
@@ -76,7 +91,7 @@ def test_flash_full_size_workload_sampled():
     """The benchmark's workload (9801 patches, 16 heads of 64) in the launch the
     bench times, compared with the oracle on sampled rows."""
     w = workloads.FLASH_WORKLOADS["vision_flash"]
-    inp, got = _run(w)
+    inp, got = _run(w, split_once=True)
     qkv = inp["qkv"].numpy()
     rng = np.random.default_rng(11)
     picks = [(0, 0), (w.T - 1, w.nh - 1)] + [(int(rng.integers(w.T)), int(rng.integers(w.nh))) for _ in range(22)]
