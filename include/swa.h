@@ -44,7 +44,7 @@ extern "C" {
 #define SWA_E_NULL       -1  /* a required pointer is NULL */
 #define SWA_E_SHAPE      -2  /* unsupported or inconsistent sizes */
 #define SWA_E_ALIGN      -3  /* a tensor pointer is not 16-byte aligned */
-#define SWA_E_WORKSPACE  -4  /* workspace missing or smaller than swa_attend_workspace_size */
+#define SWA_E_WORKSPACE  -4  /* workspace missing or smaller than swa_attend_workspace_min */
 #define SWA_E_HAZARD     -5  /* prep ring write requested for t > 1 (see swa_prep) */
 #define SWA_E_CUDA       -6  /* a CUDA launch or query failed */
 
@@ -162,9 +162,14 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  * choose; a positive value caps the splits per (sequence, KV head, row block)
  * (results agree within f32 rounding for any split count).
  *
- * Workspace: `workspace_bytes` >= swa_attend_workspace_size(args), device
- * memory, 256-byte aligned, no initial contents needed; overlapping calls
- * must not share it. ev_start / ev_stop, when non-NULL, are recorded on the
+ * Workspace: device memory, 256-byte aligned, no initial contents needed;
+ * overlapping calls must not share it. `workspace_bytes` must be at least
+ * swa_attend_workspace_min(args). swa_attend_workspace_size(args) (larger for
+ * chunks with at least 128 query vectors per KV head) also holds, for the
+ * tensor-core prompt kernel, every KV head's sink and window keys split once
+ * into TF32 operand blocks of 32 keys, which the kernel then copies in whole
+ * blocks; with less, the kernel splits the keys it stages itself (same
+ * results within f32 rounding). ev_start / ev_stop, when non-NULL, are recorded on the
  * stream right before and after the main attention kernel (for timing it).
  * err, when non-NULL, is a device word the kernels OR SWA_DERR_* bits into.
  *
@@ -236,6 +241,8 @@ typedef struct swa_attend_args {
  * hd, cap, ns, num_splits; 0 if the sizes are invalid). Queries the current
  * device's SM count on first use. */
 size_t swa_attend_workspace_size(const swa_attend_args* args);
+/* The smallest workspace swa_attend accepts for these sizes (0 if unsupported). */
+size_t swa_attend_workspace_min(const swa_attend_args* args);
 
 int swa_attend(const swa_attend_args* args, cudaStream_t stream);
 
@@ -281,9 +288,11 @@ int swa_rollback(swa_meta* meta, const int32_t* n_back, int B, int cap, uint32_t
  * means what it means for swa_attend, and the caller still passes all inputs
  * and outputs. Nothing is allocated: no cudaMalloc, cudaFree or allocating
  * library call.
- *   - Sizes whose scratch need (swa_attend_workspace_size) exceeds
+ *   - Sizes whose scratch need (swa_attend_workspace_min) exceeds
  *     SWA_NOALLOC_SCRATCH_BYTES are refused with SWA_E_WORKSPACE before
  *     anything is enqueued; use swa_attend with your own workspace for them.
+ *     The split-once operand blocks of the tensor-core prompt kernel are used
+ *     when swa_attend_workspace_size fits the array too.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and caches it; make
  *     that first call before any stream capture.

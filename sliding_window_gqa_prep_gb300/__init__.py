@@ -130,6 +130,20 @@ def attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits: int = 0, far_m:
     return n
 
 
+def attend_workspace_min(B, t, nh, nk, hd, cap, ns, num_splits: int = 0, far_m: int = 0) -> int:
+    """The smallest workspace swa_attend accepts (without the split-once operand
+    blocks of the tensor-core prompt kernel, which attend_workspace_size includes)."""
+    a = _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits)
+    fa = _abi.FarArgs()
+    if far_m:
+        fa.m = int(far_m)
+        a.far = ctypes.pointer(fa)
+    n = int(library().swa_attend_workspace_min(ctypes.byref(a)))
+    if n == 0:
+        raise SwaError(_abi.SWA_E_SHAPE, "swa_attend_workspace_min")
+    return n
+
+
 def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate_scale,
            scale: float, *, out=None, workspace=None, commit: bool = False, meta_out=None,
            num_splits: int = 0, err=None, ev_start=None, ev_stop=None, far=None, stream=None):
@@ -146,8 +160,8 @@ def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate
     if out is None:
         out = torch.empty_like(q)
     far_m = int(far["m"]) if far is not None else 0
-    need = attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits, far_m)
     if workspace is None:
+        need = attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits, far_m)
         workspace = torch.empty(need, device=q.device, dtype=torch.uint8)
     a = _attend_struct(B, t, nh, nk, hd, cap, ns, num_splits)
     a.scale = float(scale)

@@ -105,6 +105,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.swa_prep.argtypes = [ctypes.POINTER(PrepArgs), ctypes.c_void_p]
     lib.swa_attend_workspace_size.restype = ctypes.c_size_t
     lib.swa_attend_workspace_size.argtypes = [ctypes.POINTER(AttendArgs)]
+    lib.swa_attend_workspace_min.restype = ctypes.c_size_t
+    lib.swa_attend_workspace_min.argtypes = [ctypes.POINTER(AttendArgs)]
     lib.swa_rollback.restype = ctypes.c_int
     lib.swa_rollback.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                  ctypes.c_void_p, ctypes.c_void_p]

@@ -78,6 +78,9 @@ static void add_far_records(const swa_attend_args* a, AttendPlan* p) {
 
 bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   if (!attend_shape_ok(a)) return false;
+  p->off_ops = 0;
+  p->ops_nblk = 0;
+  p->ops_nsb = 0;
   const int hpg = a->nh / a->nk;
   // Prompt-sized chunks run on tensor cores, one split per row block: blocks of
   // 128 query vectors on tcgen05 when a chunk has at least 128 query vectors
@@ -103,6 +106,16 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
     p->off_meta = p->off_nsplit + up(ns_bytes);
     p->ws_bytes = p->off_meta + up((size_t)a->B * sizeof(swa_meta));
     add_far_records(a, p);
+    p->ws_min = p->ws_bytes;
+    if (block == 128) {
+      // split-once operand blocks for the tcgen05 kernel: per (sequence, KV head) the
+      // sinks' blocks, then blocks of the logical keys 0 .. len0 + t - 1 (< cap + t)
+      p->ops_nsb = (a->ns + kOpsBlockKeys - 1) / kOpsBlockKeys;
+      const long long nlog = ((long long)a->cap + a->t + kOpsBlockKeys - 1) / kOpsBlockKeys;
+      p->ops_nblk = (int)(p->ops_nsb + nlog);
+      p->off_ops = p->ws_bytes;
+      p->ws_bytes += up((size_t)a->B * a->nk * p->ops_nblk * 4 * kOpsBlockKeys * a->hd * sizeof(float));
+    }
     return true;
   }
   int rows = 32 / hpg;
@@ -147,6 +160,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   p->off_meta = p->off_nsplit + up(ns_bytes);
   p->ws_bytes = p->off_meta + up((size_t)a->B * sizeof(swa_meta));
   add_far_records(a, p);
+  p->ws_min = p->ws_bytes;
   return true;
 }
 
@@ -231,6 +245,13 @@ size_t swa_attend_workspace_size(const swa_attend_args* a) {
   return plan.ws_bytes;
 }
 
+size_t swa_attend_workspace_min(const swa_attend_args* a) {
+  if (!a) return 0;
+  AttendPlan plan;
+  if (!make_plan(a, &plan)) return 0;
+  return plan.ws_min;
+}
+
 int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   if (!a) return SWA_E_NULL;
   if (!a->meta || !a->q || !a->k_chunk || !a->v_chunk || !a->ring_k || !a->ring_v || !a->gate ||
@@ -251,7 +272,7 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
     if (p && !aligned16(p)) return SWA_E_ALIGN;
   AttendPlan plan;
   if (!make_plan(a, &plan)) return SWA_E_SHAPE;
-  if (!a->workspace || a->workspace_bytes < plan.ws_bytes) return SWA_E_WORKSPACE;
+  if (!a->workspace || a->workspace_bytes < plan.ws_min) return SWA_E_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return SWA_E_ALIGN;
 
   AttendParams p{};
@@ -290,6 +311,11 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   p.mz = a->far ? a->far->mz : nullptr;
   p.t_hat = a->far ? a->far->t_hat : nullptr;
   p.ws_far = reinterpret_cast<float*>(ws + plan.off_far);
+  // the split-once operand blocks when the workspace holds them
+  p.ops = (plan.ops_nblk > 0 && a->workspace_bytes >= plan.ws_bytes) ? reinterpret_cast<float*>(ws + plan.off_ops)
+                                                                      : nullptr;
+  p.ops_nblk = plan.ops_nblk;
+  p.ops_nsb = plan.ops_nsb;
   int rc = SWA_OK;
   if (p.far) {            // before the attention: it reads the evicted ring slot, which the commit overwrites
     rc = launch_far(p, stream);
@@ -307,14 +333,14 @@ static bool flash_shape_ok(const swa_flash_args* a) {
 }
 
 // split-once operand blocks: [nseg][nk][ceil(max_len / 32)][4][32][hd] floats
-static size_t flash_ops_bytes(const swa_flash_args* a) {
-  const size_t nblk = ((size_t)a->max_len + kFlashBlockKeys - 1) / kFlashBlockKeys;
-  return (size_t)a->nseg * a->nk * nblk * 4 * kFlashBlockKeys * a->hd * sizeof(float);
+static size_t ops_bytes(const swa_flash_args* a) {
+  const size_t nblk = ((size_t)a->max_len + kOpsBlockKeys - 1) / kOpsBlockKeys;
+  return (size_t)a->nseg * a->nk * nblk * 4 * kOpsBlockKeys * a->hd * sizeof(float);
 }
 
 size_t swa_flash_workspace_size(const swa_flash_args* a) {
   if (!a || !flash_shape_ok(a)) return 0;
-  return flash_ops_bytes(a);
+  return ops_bytes(a);
 }
 
 int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
@@ -334,7 +360,7 @@ int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   if (!aligned16(a->qkv) || !aligned16(a->out) || (reinterpret_cast<uintptr_t>(a->segs) & 3u))
     return SWA_E_ALIGN;
   if (a->workspace) {
-    if (a->workspace_bytes < flash_ops_bytes(a)) return SWA_E_WORKSPACE;
+    if (a->workspace_bytes < ops_bytes(a)) return SWA_E_WORKSPACE;
     if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return SWA_E_ALIGN;
   }
   AttendParams p{};
@@ -347,8 +373,8 @@ int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   p.qkv = a->qkv; p.segs = a->segs;
   p.T = a->T; p.ld = a->ld; p.q_off = a->q_off; p.k_off = a->k_off; p.v_off = a->v_off; p.ldo = a->ldo;
   p.max_len = a->max_len;
-  p.flash_ops = static_cast<float*>(a->workspace);
-  p.flash_nblk = (a->max_len + kFlashBlockKeys - 1) / kFlashBlockKeys;
+  p.ops = static_cast<float*>(a->workspace);
+  p.ops_nblk = (a->max_len + kOpsBlockKeys - 1) / kOpsBlockKeys;
   return launch_flash_tc(p, stream, a->ev_start, a->ev_stop);
 }
 

@@ -33,6 +33,10 @@ struct AttendPlan {
   size_t off_nsplit; // byte offset of the per-(b, rb) valid-split counts
   size_t off_meta;   // byte offset of the per-sequence copy of the meta before the chunk
   size_t off_far;    // byte offset of the far records [B][nh] x (4 + hd) floats (far field only)
+  size_t ws_min;     // the smallest workspace swa_attend accepts (no split-once operand blocks)
+  size_t off_ops;    // byte offset of the split-once operand blocks (tensor-core prompt kernel)
+  int ops_nblk;      // their blocks per (sequence, KV head), 0 if the plan has none
+  int ops_nsb;       // sink blocks among them
 };
 bool make_plan(const swa_attend_args* a, AttendPlan* p);
 
@@ -74,8 +78,12 @@ struct AttendParams {
   const float* qkv;
   const uint32_t* segs;       // [B][2]: first row, length
   int T, ld, q_off, k_off, v_off, ldo, max_len;
-  float* flash_ops;           // split-once operand blocks [B][nk][flash_nblk][4][32][hd], or null
-  int flash_nblk;             // blocks of 32 keys per (segment, KV head) in flash_ops
+  // split-once operand blocks [B][nk][ops_nblk][4][32][hd] (TF32 K hi, K lo, V^T hi,
+  // V^T lo of 32 keys), or null: swa_flash's segment rows, or the token path's
+  // sink blocks then its logical keys 0 .. len0 + t - 1 (tensor-core prompt kernel)
+  float* ops;
+  int ops_nblk;               // blocks per (sequence or segment, KV head)
+  int ops_nsb;                // token path: sink blocks among them (ceil(ns / 32))
 };
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
@@ -92,9 +100,10 @@ int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, 
 // prompt-chunk kernel on tcgen05 / TMEM (128 query vectors per CTA), swa_prompt_tc.cu
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // the same kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu;
-// with p.flash_ops set it first splits every KV head's K/V rows into operand blocks once
+// with p.ops set it first splits every KV head's K/V rows into operand blocks once
+// (the same holds for launch_attend_prompt_tc on the token path)
 int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
-constexpr int kFlashBlockKeys = 32;   // keys per split-once operand block (= the kernel's key tile)
+constexpr int kOpsBlockKeys = 32;   // keys per split-once operand block (= the kernel's key tile)
 // verify kernel (16 or 32 query vectors per CTA, CUDA cores), swa_verify.cu
 int launch_attend_verify(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int attend_verify_occupancy(int hd, int nq);

@@ -50,8 +50,10 @@ int scratch_address(void** out) {
 extern "C" int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream) {
   if (!args) return SWA_E_NULL;
   // Sizes whose partial records would not fit the fixed scratch are refused
-  // before anything is enqueued.
-  const size_t need = swa_attend_workspace_size(args);
+  // before anything is enqueued (the split-once operand blocks of the tensor-core
+  // prompt kernel are used when they fit as well, skipped otherwise).
+  const size_t need = swa_attend_workspace_min(args);
+  if (need == 0) return SWA_E_SHAPE;
   if (need > swa::kScratchBytes) return SWA_E_WORKSPACE;
   void* scratch = nullptr;
   const int rc = swa::scratch_address(&scratch);

@@ -57,7 +57,7 @@ struct TCfg {
   // operand sets: two behind the split warps; with split-once blocks (MODE 2) the
   // landing stages are unused and their room holds more sets, so the producer runs
   // further ahead of the MMAs
-  static constexpr int NSETS = MODE != 2 ? 2 : (HD == 64 ? 4 : 3);
+  static constexpr int NSETS = MODE < 2 ? 2 : (HD == 64 ? 4 : 3);
   // TMEM columns
   static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S0 = 2 * HD, C_S1 = 2 * HD + kTN;
   static constexpr uint32_t C_O = 2 * HD + 2 * kTN, C_PHI = 3 * HD + 2 * kTN, C_PLO = 3 * HD + 3 * kTN;
@@ -67,7 +67,7 @@ struct TCfg {
   static constexpr int LAND = kTN * HD * 4;                 // one fp32 tile of K or V
   static constexpr int OFF_LK = 0;                          // [2 stages] K landing
   static constexpr int OFF_LV = 2 * LAND;                   // [2 stages] V landing
-  static constexpr int OFF_OPS = MODE != 2 ? 4 * LAND : 0;  // [NSETS] K_hi, K_lo, V^T_hi, V^T_lo
+  static constexpr int OFF_OPS = MODE < 2 ? 4 * LAND : 0;   // [NSETS] K_hi, K_lo, V^T_hi, V^T_lo
   static constexpr int SET = 4 * LAND;
   static constexpr int OFF_BAR = OFF_OPS + NSETS * SET;     // mbarriers
   static constexpr int NBAR = 16;
@@ -138,15 +138,17 @@ __device__ __forceinline__ uint32_t tf32_hi(float x) {
   return r;
 }
 
-// MODE 0: a row block of the token path (sinks, ring window, chunk rows; split
+// MODE 0 / 3: a row block of the token path (sinks, ring window, chunk rows; split
 // record to the workspace). MODE 1 / 2: a row block of one segment of packed
 // q|k|v rows attending all of the segment's rows (swa_flash); blockIdx.z =
-// segment * nk + KV head, and the normalised output is written directly; MODE 2
-// takes split-once operand blocks from p.flash_ops.
+// segment * nk + KV head, and the normalised output is written directly. MODE 2
+// and 3 take split-once operand blocks from p.ops (token path: the sinks' blocks,
+// then blocks of logical keys 32k .. 32k + 31; a row block's tiles are its sink
+// blocks and the logical blocks that hold its window).
 template <int HD, int MODE>
 __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
-  constexpr bool FLASH = MODE != 0;
-  constexpr bool PRESPLIT = MODE == 2;
+  constexpr bool FLASH = MODE == 1 || MODE == 2;
+  constexpr bool PRESPLIT = MODE >= 2;
   constexpr int NS = TCfg<HD, MODE>::NSETS;    // operand sets: tile j uses set j % NS
   static_assert(PRESPLIT || NS == 2, "the split warps use two operand sets");
   pdl_trigger();
@@ -197,7 +199,10 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     if (g == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
   }
   const int rows_eff = r_last - r0 + 1;
-  const int ntiles = (n + kTN - 1) / kTN;
+  // MODE 3 tiles: sink blocks 0 .. nsb - 1, then logical blocks kb0 .. (len0 + r_last) / 32
+  const int nsb = MODE == 3 ? p.ops_nsb : 0;
+  const int kb0 = xlo / kTN;
+  const int ntiles = MODE == 3 ? nsb + (st.len0 + r_last) / kTN - kb0 + 1 : (n + kTN - 1) / kTN;
   const size_t kv_head = (size_t)b * p.nk + g;
 
   if (tid == 0) {
@@ -261,7 +266,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   if (PRESPLIT && warp == 4) {
     // the four operand blocks of tile i into set i % NS, once P V of tile i - NS (the
     // set's last reader; its commit follows S of tile i - NS as well) is done
-    const float* blocks = p.flash_ops + (size_t)bg * p.flash_nblk * 4 * (kTN * HD);
+    const float* blocks = p.ops + (size_t)bg * p.ops_nblk * 4 * (kTN * HD);
     int issued = 0;
     for (int i = 0; i < ntiles; ++i) {
       const int set = i % NS;
@@ -273,7 +278,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       }
       if (__shfl_sync(kTF, *s_abort, 0)) break;
       if (lane == 0) {
-        const float* src = blocks + (size_t)i * 4 * (kTN * HD);
+        const int blk = (MODE == 3 && i >= nsb) ? i + kb0 : i;
+        const float* src = blocks + (size_t)blk * 4 * (kTN * HD);
         mbar_arrive_expect_tx(&split_done[set], (uint32_t)(4 * C::LAND));
         for (int which = 0; which < 4; ++which)
           bulk_g2s(op(set, which), src + (size_t)which * (kTN * HD), (uint32_t)C::LAND, &split_done[set]);
@@ -504,15 +510,26 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       // window mask; a tile wholly inside this row's window skips it (a whole
       // segment row sees every key of its segment: only the tail is masked)
       const int j0 = i * kTN;
-      const bool inside = FLASH ? q_ok && cnt == kTN
-                                : q_ok && cnt == kTN && j0 >= p.ns && xlo + (j0 - p.ns) >= q_lo &&
-                                      xlo + (j0 + kTN - 1 - p.ns) <= q_hi;
+      bool inside;
+      // MODE 3: a sink tile holds sinks j0 .. j0 + 31 (valid below ns); a logical tile
+      // holds keys x0 .. x0 + 31, each valid inside the row's window
+      const bool sink_tile = MODE == 3 && i < nsb;
+      const int x0 = (kb0 + i - nsb) * kTN;
+      if constexpr (MODE == 3) {
+        inside = sink_tile ? q_ok && p.ns - j0 >= kTN : q_ok && x0 >= q_lo && x0 + kTN - 1 <= q_hi;
+      } else {
+        inside = FLASH ? q_ok && cnt == kTN
+                       : q_ok && cnt == kTN && j0 >= p.ns && xlo + (j0 - p.ns) >= q_lo &&
+                             xlo + (j0 + kTN - 1 - p.ns) <= q_hi;
+      }
       float tmax = -INFINITY;
       float s[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         bool v = true;
-        if (!inside) {
+        if (MODE == 3 && !inside) {
+          v = q_ok && (sink_tile ? j0 + k < p.ns : (x0 + k >= q_lo && x0 + k <= q_hi));
+        } else if (!inside) {
           const int j = j0 + k;
           v = q_ok && k < cnt;
           if (!FLASH && v && j >= p.ns) {
@@ -621,35 +638,28 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   }
 }
 
-// One CTA per (segment, KV head, 32-key block): the block's K rows as TF32 hi/lo
-// in the K-major layout of the kernel's K operand ((key / 8) * K_SBO + (f / 4) *
-// 128 + (key % 8) * 16 + (f % 4) * 4 bytes) and its V rows transposed likewise
-// ((f / 8) * V_SBO + (key / 4) * 128 + (f % 8) * 16 + (key % 4) * 4); keys past
-// the segment are zeros. Same arithmetic as the split warps: bit-identical.
-template <int HD>
-__global__ void __launch_bounds__(256) flash_presplit_kernel(AttendParams p) {
-  pdl_trigger();
-  pdl_wait();
+// One 32-key block as TF32 hi/lo operands, by a CTA of 256 threads: the K rows in
+// the K-major layout of the kernel's K operand ((key / 8) * K_SBO + (f / 4) * 128 +
+// (key % 8) * 16 + (f % 4) * 4 bytes) and the V rows transposed likewise ((f / 8) *
+// V_SBO + (key / 4) * 128 + (f % 8) * 16 + (key % 4) * 4); keys whose source is
+// null are zeros. Same arithmetic as the split warps: bit-identical operands.
+// src(key, &k, &v) gives the key's K and V rows (nullptr: none).
+template <int HD, class Src>
+__device__ __forceinline__ void split_block(uint32_t* dst, Src src) {
   using C = TCfg<HD>;
   constexpr int D4 = HD / 4;
   __shared__ __align__(16) float vs[kTN][HD + 4];
-  const int blk = blockIdx.x, bg = blockIdx.y;
-  const int b = bg / p.nk, g = bg % p.nk;
-  const uint32_t s0 = p.segs[2 * b], len = p.segs[2 * b + 1];
-  if ((uint64_t)s0 + len > (uint64_t)p.T || len > (uint32_t)p.max_len) return;   // the attention reports it
-  const int j0 = blk * kTN;
-  if (j0 >= (int)len) return;
-  const int cnt = min(kTN, (int)len - j0);
-  uint32_t* dst = reinterpret_cast<uint32_t*>(p.flash_ops + ((size_t)bg * p.flash_nblk + blk) * 4 * (kTN * HD));
   // K: thread -> (key, f4) with key % 8 fastest, so 8 threads write 128 contiguous bytes
   for (int idx = threadIdx.x; idx < kTN * D4; idx += blockDim.x) {
     const int key = (idx & 7) + 8 * (idx / (8 * D4)), f4 = (idx >> 3) % D4;
+    const float* kr = nullptr;
+    const float* vr = nullptr;
+    src(key, &kr, &vr);
     float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
     float4 w = v;
-    if (key < cnt) {
-      const size_t row = (size_t)(s0 + j0 + key) * p.ld + (size_t)g * HD + f4 * 4;
-      v = *reinterpret_cast<const float4*>(p.qkv + row + p.k_off);
-      w = *reinterpret_cast<const float4*>(p.qkv + row + p.v_off);
+    if (kr) {
+      v = *reinterpret_cast<const float4*>(kr + f4 * 4);
+      w = *reinterpret_cast<const float4*>(vr + f4 * 4);
     }
     *reinterpret_cast<float4*>(&vs[key][f4 * 4]) = w;
     const float x[4] = {v.x, v.y, v.z, v.w};
@@ -684,6 +694,69 @@ __global__ void __launch_bounds__(256) flash_presplit_kernel(AttendParams p) {
   }
 }
 
+// swa_flash: one CTA per (segment, KV head, 32-key block) of the segment's rows.
+template <int HD>
+__global__ void __launch_bounds__(256) flash_presplit_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
+  const int blk = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.nk, g = bg % p.nk;
+  const uint32_t s0 = p.segs[2 * b], len = p.segs[2 * b + 1];
+  if ((uint64_t)s0 + len > (uint64_t)p.T || len > (uint32_t)p.max_len) return;   // the attention reports it
+  const int j0 = blk * kTN;
+  if (j0 >= (int)len) return;
+  const int cnt = min(kTN, (int)len - j0);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(p.ops + ((size_t)bg * p.ops_nblk + blk) * 4 * (kTN * HD));
+  split_block<HD>(dst, [&](int key, const float** kr, const float** vr) {
+    if (key < cnt) {
+      const float* row = p.qkv + (size_t)(s0 + j0 + key) * p.ld + (size_t)g * HD;
+      *kr = row + p.k_off;
+      *vr = row + p.v_off;
+    }
+  });
+}
+
+// Token path: one CTA per (sequence, KV head, block): blocks 0 .. nsb - 1 hold the
+// sinks, block nsb + k the logical keys x = 32k .. 32k + 31 below len0 + t (ring
+// slot (head0 + x) % W for x < len0, chunk row x - len0 after), read before the
+// commit rewrites the ring.
+template <int HD>
+__global__ void __launch_bounds__(256) token_presplit_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
+  const int blk = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.nk, g = bg % p.nk;
+  const SeqState st = sanitize_state(p.meta[b], p.cap, nullptr);   // the attention reports bad metas
+  const size_t kv_head = (size_t)b * p.nk + g;
+  const bool sink = blk < p.ops_nsb;
+  const int j0 = blk * kTN;                                        // first sink of a sink block
+  const int x0 = (blk - p.ops_nsb) * kTN;                          // first logical key otherwise
+  if (!sink && x0 >= st.len0 + p.t) return;                        // past every row's window
+  uint32_t* dst = reinterpret_cast<uint32_t*>(p.ops + ((size_t)bg * p.ops_nblk + blk) * 4 * (kTN * HD));
+  split_block<HD>(dst, [&](int key, const float** kr, const float** vr) {
+    if (sink) {
+      if (j0 + key < p.ns) {
+        const size_t at = (kv_head * p.ns + j0 + key) * HD;
+        *kr = p.sink_k + at;
+        *vr = p.sink_v + at;
+      }
+      return;
+    }
+    const int x = x0 + key;
+    if (x < st.len0) {
+      int slot = st.head0 + x;
+      if (slot >= st.W) slot -= st.W;
+      const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
+      *kr = p.ring_k + at;
+      *vr = p.ring_v + at;
+    } else if (x < st.len0 + p.t) {
+      const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
+      *kr = p.k_chunk + at;
+      *vr = p.v_chunk + at;
+    }
+  });
+}
+
 template <int HD, int MODE>
 int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   using C = TCfg<HD, MODE>;
@@ -696,9 +769,10 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
     if (e != cudaSuccess) return cuda_status(e);
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  if (MODE == 2) {
-    const dim3 pgrid((unsigned)p.flash_nblk, (unsigned)(p.B * p.nk));
-    const int rc = finish_launch(launch_pdl(flash_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p));
+  if (MODE >= 2) {
+    const dim3 pgrid((unsigned)p.ops_nblk, (unsigned)(p.B * p.nk));
+    const int rc = finish_launch(MODE == 2 ? launch_pdl(flash_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p)
+                                           : launch_pdl(token_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p));
     if (rc != SWA_OK) return rc;
   }
   dim3 grid(1u, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
@@ -714,16 +788,16 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
 
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   switch (p.hd) {
-    case 64: return launch_tc<64, 0>(p, s, e0, e1);
-    case 128: return launch_tc<128, 0>(p, s, e0, e1);
+    case 64: return p.ops ? launch_tc<64, 3>(p, s, e0, e1) : launch_tc<64, 0>(p, s, e0, e1);
+    case 128: return p.ops ? launch_tc<128, 3>(p, s, e0, e1) : launch_tc<128, 0>(p, s, e0, e1);
   }
   return SWA_E_SHAPE;
 }
 
 int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   switch (p.hd) {
-    case 64: return p.flash_ops ? launch_tc<64, 2>(p, s, e0, e1) : launch_tc<64, 1>(p, s, e0, e1);
-    case 128: return p.flash_ops ? launch_tc<128, 2>(p, s, e0, e1) : launch_tc<128, 1>(p, s, e0, e1);
+    case 64: return p.ops ? launch_tc<64, 2>(p, s, e0, e1) : launch_tc<64, 1>(p, s, e0, e1);
+    case 128: return p.ops ? launch_tc<128, 2>(p, s, e0, e1) : launch_tc<128, 1>(p, s, e0, e1);
   }
   return SWA_E_SHAPE;
 }

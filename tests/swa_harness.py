@@ -48,7 +48,8 @@ def far_to_np(far):
     return {k: (v.numpy().astype(np.float64) if torch.is_tensor(v) else v) for k, v in far.items()}
 
 
-def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_alias=False, far=None):
+def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_alias=False, far=None,
+                  min_workspace=False):
     """rope table -> prep -> attend (+ commit) on the GPU. The prep writes the
     ring only for t == 1 with window == cap (prep's slot map) and no far field;
     otherwise the attend's commit does. far: the generator's far state (CPU);
@@ -68,7 +69,10 @@ def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_ali
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = swa.attend(meta, q, k, v, ring_k, ring_v, d["sink_k"] if w.ns else None,
                      d["sink_v"] if w.ns else None, d["gate"], d["gate_scale"], w.score_scale,
-                     commit=commit, meta_out=meta_out, num_splits=num_splits, err=err, far=far_d)
+                     commit=commit, meta_out=meta_out, num_splits=num_splits, err=err, far=far_d,
+                     workspace=(torch.empty(swa.attend_workspace_min(w.B, w.t, w.nh, w.nk, w.hd, w.cap, w.ns,
+                                                                     num_splits, w.far_m),
+                                            dtype=torch.uint8, device="cuda") if min_workspace else None))
     torch.cuda.synchronize()
     return {
         "rope": rope.cpu().numpy(), "q": q.cpu().numpy(), "k": k.cpu().numpy(),

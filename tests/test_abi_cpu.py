@@ -158,6 +158,19 @@ def test_attend_rejects_bad_far_field_arguments(lib):
     assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_ALIGN
 
 
+def test_workspace_minimum_and_split_once_blocks(lib):
+    a = _attend()                                           # decode: no split-once blocks
+    assert lib.swa_attend_workspace_min(ctypes.byref(a)) == lib.swa_attend_workspace_size(ctypes.byref(a))
+    p = _attend(t=64, nh=8, nk=2, cap=100, ns=3)           # 256 query vectors per KV head: tcgen05
+    lo = lib.swa_attend_workspace_min(ctypes.byref(p))
+    hi = lib.swa_attend_workspace_size(ctypes.byref(p))
+    blocks = 1 + (100 + 64 + 31) // 32                      # sink block + logical blocks
+    assert hi - lo >= 2 * 2 * blocks * 4 * 32 * 128 * 4 and hi - lo < 2 * 2 * blocks * 4 * 32 * 128 * 4 + 256
+    call = lambda a: lib.swa_attend(ctypes.byref(a), None)
+    assert call(_attend(t=64, nh=8, nk=2, cap=100, ns=3, workspace_bytes=lo - 1)) == _abi.SWA_E_WORKSPACE
+    assert lib.swa_attend_workspace_min(None) == 0
+
+
 def test_workspace_grows_by_the_far_records(lib):
     a = _attend()
     base = lib.swa_attend_workspace_size(ctypes.byref(a))

@@ -150,6 +150,19 @@ def test_full_path_matches_oracle(kw, sharp):
     check_commit_placement(w, inp, res)
 
 
+@pytest.mark.parametrize("kw", [c for c in ATTEND_CASES if c["hd"] <= 128 and c["t"] * c["nh"] // c["nk"] >= 128])
+def test_tensor_core_prompt_with_the_minimum_workspace(kw):
+    """The tcgen05 prompt kernel staging and splitting K/V itself (a workspace of
+    swa_attend_workspace_min bytes, no split-once operand blocks)."""
+    w = workloads.custom(seed=5, **kw)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=True, min_workspace=True)
+    assert res["err"] == 0
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, "out")
+    check_commit_placement(w, inp, res)
+
+
 def test_attend_only_matches_oracle_on_shared_q_k():
     """Attend fed the same (generator-drawn) q and chunk k/v on both sides."""
     w = workloads.custom(B=3, t=8, nh=16, nk=4, hd=128, window=100, cap=100, ns=4,
