@@ -54,10 +54,11 @@ constexpr float kLazyMax = 8.0f;       // log2 headroom before the running max i
 
 template <int HD, int MODE = 0>
 struct TCfg {
-  // operand sets: two behind the split warps; with split-once blocks (MODE 2) the
-  // landing stages are unused and their room holds more sets, so the producer runs
-  // further ahead of the MMAs
-  static constexpr int NSETS = MODE < 2 ? 2 : (HD == 64 ? 4 : 3);
+  // operand sets behind the split warps (MODE 0 / 1)
+  static constexpr int NSETS = 2;
+  // split-once blocks (MODE 2 / 3): separate pools of K (hi, lo) and V^T (hi, lo)
+  // slots, consecutive K slots adjacent so that one S product spans two tiles
+  static constexpr int NSK = HD == 64 ? 8 : 4, NSV = HD == 64 ? 4 : 2;
   // TMEM columns
   static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S0 = 2 * HD, C_S1 = 2 * HD + kTN;
   static constexpr uint32_t C_O = 2 * HD + 2 * kTN, C_PHI = 3 * HD + 2 * kTN, C_PLO = 3 * HD + 3 * kTN;
@@ -67,10 +68,13 @@ struct TCfg {
   static constexpr int LAND = kTN * HD * 4;                 // one fp32 tile of K or V
   static constexpr int OFF_LK = 0;                          // [2 stages] K landing
   static constexpr int OFF_LV = 2 * LAND;                   // [2 stages] V landing
-  static constexpr int OFF_OPS = MODE < 2 ? 4 * LAND : 0;   // [NSETS] K_hi, K_lo, V^T_hi, V^T_lo
+  static constexpr int OFF_OPS = 4 * LAND;                  // [NSETS] K_hi, K_lo, V^T_hi, V^T_lo
   static constexpr int SET = 4 * LAND;
-  static constexpr int OFF_BAR = OFF_OPS + NSETS * SET;     // mbarriers
-  static constexpr int NBAR = 16;
+  // MODE 2 / 3 pools: K_hi [NSK], K_lo [NSK], V^T_hi [NSV], V^T_lo [NSV]
+  static constexpr int OFF_KHI = 0, OFF_KLO = NSK * LAND, OFF_VHI = 2 * NSK * LAND;
+  static constexpr int OFF_VLO = (2 * NSK + NSV) * LAND;
+  static constexpr int OFF_BAR = MODE < 2 ? OFF_OPS + NSETS * SET : 2 * (NSK + NSV) * LAND;   // mbarriers
+  static constexpr int NBAR = 32;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
@@ -149,8 +153,9 @@ template <int HD, int MODE>
 __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
   constexpr bool FLASH = MODE == 1 || MODE == 2;
   constexpr bool PRESPLIT = MODE >= 2;
-  constexpr int NS = TCfg<HD, MODE>::NSETS;    // operand sets: tile j uses set j % NS
-  static_assert(PRESPLIT || NS == 2, "the split warps use two operand sets");
+  constexpr int NS = TCfg<HD, MODE>::NSETS;    // MODE 0 / 1 operand sets: tile j uses set j % NS
+  constexpr int NSK = TCfg<HD, MODE>::NSK, NSV = TCfg<HD, MODE>::NSV;
+  static_assert(NSK % 2 == 0, "S of a tile pair spans two adjacent K slots");
   pdl_trigger();
   pdl_wait();
   using C = TCfg<HD, MODE>;
@@ -162,13 +167,21 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     return reinterpret_cast<uint32_t*>(sm + C::OFF_OPS + set * C::SET + which * C::LAND);
   };
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  // MODE 0 / 1
   uint64_t* land_full = bars + 0;    // [2] producer -> split warps (bytes)
   uint64_t* land_empty = bars + 2;   // [2] split warps -> producer (4 arrivals)
-  uint64_t* split_done = bars + 4;   // [NS sets] split warps (4 arrivals) or split-once copies -> MMA
-  uint64_t* s_full = bars + 8;       // [2 S buffers] MMA commit -> softmax warps
-  uint64_t* p_ready = bars + 10;     // softmax warps -> MMA (4 arrivals)
-  uint64_t* pv_done = bars + 11;     // MMA commit -> softmax warps
-  uint64_t* v_free = bars + 12;      // [NS sets] MMA commit (P V of the set done) -> split warps / producer
+  uint64_t* split_done = bars + 4;   // [2 sets] split warps -> MMA (4 arrivals)
+  uint64_t* v_free = bars + 12;      // [2 sets] MMA commit (P V of the set done) -> split warps
+  // MODE 2 / 3
+  uint64_t* kfull = bars + 0;        // [NSK] K copies landed (bytes)
+  uint64_t* kfree = bars + 8;        // [NSK] MMA commit: S that read the slot is done
+  uint64_t* vfull = bars + 16;       // [NSV] V copies landed (bytes)
+  uint64_t* vfree = bars + 20;       // [NSV] MMA commit: P V that read the slot is done
+  uint64_t* s_empty = bars + 25;     // softmax warps: both halves of the pair's S read (4 arrivals)
+  // both: S (MODE 0 / 1: [2 buffers]; MODE 2 / 3: one 64-column buffer per tile pair)
+  uint64_t* s_full = PRESPLIT ? bars + 24 : bars + 8;
+  uint64_t* p_ready = PRESPLIT ? bars + 26 : bars + 10;   // softmax warps -> MMA (4 arrivals)
+  uint64_t* pv_done = PRESPLIT ? bars + 27 : bars + 11;   // MMA commit -> softmax warps
   volatile int* s_abort = reinterpret_cast<volatile int*>(bars + C::NBAR);
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + C::NBAR) + 1);
 
@@ -206,17 +219,29 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   const size_t kv_head = (size_t)b * p.nk + g;
 
   if (tid == 0) {
-    mbar_init(&land_full[0], 1);
-    mbar_init(&land_full[1], 1);
-    mbar_init(&land_empty[0], 4);
-    mbar_init(&land_empty[1], 4);
-    for (int k = 0; k < NS; ++k) {
-      // split warps' 4 arrivals, or the producer's one arrival + bytes (MODE 2)
-      mbar_init(&split_done[k], PRESPLIT ? 1 : 4);
-      mbar_init(&v_free[k], 1);
+    if constexpr (PRESPLIT) {
+      for (int k = 0; k < NSK; ++k) {
+        mbar_init(&kfull[k], 1);
+        mbar_init(&kfree[k], 1);
+      }
+      for (int k = 0; k < NSV; ++k) {
+        mbar_init(&vfull[k], 1);
+        mbar_init(&vfree[k], 1);
+      }
+      mbar_init(s_full, 1);
+      mbar_init(s_empty, 4);
+    } else {
+      mbar_init(&land_full[0], 1);
+      mbar_init(&land_full[1], 1);
+      mbar_init(&land_empty[0], 4);
+      mbar_init(&land_empty[1], 4);
+      for (int k = 0; k < NS; ++k) {
+        mbar_init(&split_done[k], 4);
+        mbar_init(&v_free[k], 1);
+      }
+      mbar_init(&s_full[0], 1);
+      mbar_init(&s_full[1], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
     mbar_init(p_ready, 4);
     mbar_init(pv_done, 1);
     mbar_fence_init();
@@ -263,14 +288,21 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   tc_fence_after();
 
   // ------------------------------------------------------------------ producer
-  if (PRESPLIT && warp == 4) {
-    // the four operand blocks of tile i into set i % NS, once P V of tile i - NS (the
-    // set's last reader; its commit follows S of tile i - NS as well) is done
-    const float* blocks = p.ops + (size_t)bg * p.ops_nblk * 4 * (kTN * HD);
+  if (PRESPLIT && (warp == 4 || warp == 6)) {
+    // MODE 2 / 3 producers: warp 4 lands the K half (hi, lo) of tile i's block in K
+    // slot i % NSK once the S that last read the slot is done; warp 6 (a split warp,
+    // idle here) lands the V^T half in V slot i % NSV once its P V is done.
+    const bool kside = warp == 4;
+    const int nslot = kside ? NSK : NSV;
+    uint64_t* fullb = kside ? kfull : vfull;
+    uint64_t* freeb = kside ? kfree : vfree;
+    unsigned char* hi_pool = sm + (kside ? C::OFF_KHI : C::OFF_VHI);
+    unsigned char* lo_pool = sm + (kside ? C::OFF_KLO : C::OFF_VLO);
+    const float* blocks = p.ops + (size_t)bg * p.ops_nblk * 4 * (kTN * HD) + (kside ? 0 : 2 * kTN * HD);
     int issued = 0;
     for (int i = 0; i < ntiles; ++i) {
-      const int set = i % NS;
-      bool ok = i < NS || mbar_wait_bounded(&v_free[set], (uint32_t)(((i - NS) / NS) & 1), kWaitLimitNs);
+      const int slot = i % nslot;
+      bool ok = i < nslot || mbar_wait_bounded(&freeb[slot], (uint32_t)(((i - nslot) / nslot) & 1), kWaitLimitNs);
       ok = __all_sync(kTF, ok);
       if (!ok) {
         if (lane == 0) { *s_abort = 1; set_err(p.err, SWA_DERR_TIMEOUT); }
@@ -280,9 +312,9 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       if (lane == 0) {
         const int blk = (MODE == 3 && i >= nsb) ? i + kb0 : i;
         const float* src = blocks + (size_t)blk * 4 * (kTN * HD);
-        mbar_arrive_expect_tx(&split_done[set], (uint32_t)(4 * C::LAND));
-        for (int which = 0; which < 4; ++which)
-          bulk_g2s(op(set, which), src + (size_t)which * (kTN * HD), (uint32_t)C::LAND, &split_done[set]);
+        mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(2 * C::LAND));
+        bulk_g2s(hi_pool + (size_t)slot * C::LAND, src, (uint32_t)C::LAND, &fullb[slot]);
+        bulk_g2s(lo_pool + (size_t)slot * C::LAND, src + kTN * HD, (uint32_t)C::LAND, &fullb[slot]);
       }
       __syncwarp();
       issued = i + 1;
@@ -290,8 +322,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     // copies still in flight after an abort land before the CTA exits (bounded; on
     // the normal path the MMA lane has already seen them)
     if (lane == 0)
-      for (int i = max(0, issued - NS); i < issued; ++i)
-        mbar_wait_bounded(&split_done[i % NS], (uint32_t)((i / NS) & 1), kWaitLimitNs);
+      for (int i = max(0, issued - nslot); i < issued; ++i)
+        mbar_wait_bounded(&fullb[i % nslot], (uint32_t)((i / nslot) & 1), kWaitLimitNs);
   }
   if (!PRESPLIT && warp == 4) {
     for (int i = 0; i < ntiles; ++i) {
@@ -352,7 +384,73 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   }
 
   // ------------------------------------------------------------------ MMA issuer
-  if (warp == 5 && lane == 0) {
+  if (PRESPLIT && warp == 5 && lane == 0) {
+    // MODE 2 / 3: S of a tile pair (2p, 2p + 1) as one product of N = 64 keys (the
+    // two tiles' K slots are adjacent) into the 64-column S buffer (tile 2p in its
+    // first 32 columns); the order S(0), PV(0), S(1), PV(1), PV(2), S(2), PV(3) ...
+    // puts S of the next pair between the two P V of the current one, so it runs
+    // while the softmax warps work on the pair's second tile.
+    const uint32_t id_s = tc_idesc(kTM, 2 * kTN);
+    const uint32_t id_o = tc_idesc(kTM, HD);
+    const int npairs = (ntiles + 1) / 2;
+    auto issue_s = [&](int pr) -> bool {
+      const int t0 = 2 * pr, t1 = t0 + 1;
+      if (!mbar_wait_bounded(&kfull[t0 % NSK], (uint32_t)((t0 / NSK) & 1), kWaitLimitNs) || *s_abort)
+        return false;
+      // a missing second tile leaves columns 32..63 undefined; nothing reads them
+      if (t1 < ntiles && (!mbar_wait_bounded(&kfull[t1 % NSK], (uint32_t)((t1 / NSK) & 1), kWaitLimitNs) || *s_abort))
+        return false;
+      // the softmax warps have read both halves of the previous pair's S
+      if (pr >= 1 && (!mbar_wait_bounded(s_empty, (uint32_t)((pr - 1) & 1), kWaitLimitNs) || *s_abort))
+        return false;
+      tc_fence_after();
+      const int slot = t0 % NSK;
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t qcol = term == 0 ? C::C_QLO : C::C_QHI;
+        const uint32_t* kb =
+            reinterpret_cast<const uint32_t*>(sm + (term == 1 ? C::OFF_KLO : C::OFF_KHI) + (size_t)slot * C::LAND);
+        for (int ks = 0; ks < HD / 8; ++ks) {
+          const uint64_t bd = smem_desc(kb + ks * 64, C::K_LBO, C::K_SBO);   // 8 groups of 8 keys
+          tc_mma(tmem + C::C_S0, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
+        }
+      }
+      tc_commit(s_full);
+      tc_commit(&kfree[t0 % NSK]);
+      if (t1 < ntiles) tc_commit(&kfree[t1 % NSK]);
+      return true;
+    };
+    auto issue_pv = [&](int i) -> bool {
+      if (!mbar_wait_bounded(p_ready, (uint32_t)(i & 1), kWaitLimitNs) || *s_abort) return false;
+      if (!mbar_wait_bounded(&vfull[i % NSV], (uint32_t)((i / NSV) & 1), kWaitLimitNs) || *s_abort) return false;
+      tc_fence_after();
+      const int slot = i % NSV;
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t pcol = term == 0 ? C::C_PLO : C::C_PHI;
+        const uint32_t* vb =
+            reinterpret_cast<const uint32_t*>(sm + (term == 1 ? C::OFF_VLO : C::OFF_VHI) + (size_t)slot * C::LAND);
+        for (int ks = 0; ks < kTN / 8; ++ks) {
+          const uint64_t bd = smem_desc(vb + ks * 64, C::V_LBO, C::V_SBO);
+          tc_mma(tmem + C::C_O, tmem + pcol + ks * 8, bd, id_o, i > 0 || term > 0 || ks > 0);
+        }
+      }
+      tc_commit(pv_done);
+      tc_commit(&vfree[slot]);
+      return true;
+    };
+    bool ok = ntiles == 0 || issue_s(0);
+    for (int pr = 0; ok && pr < npairs; ++pr) {
+      ok = issue_pv(2 * pr);
+      if (ok && pr + 1 < npairs) ok = issue_s(pr + 1);
+      if (ok && 2 * pr + 1 < ntiles) ok = issue_pv(2 * pr + 1);
+    }
+    if (!ok) {
+      *s_abort = 1;
+      set_err(p.err, SWA_DERR_TIMEOUT);
+    }
+  }
+  if (!PRESPLIT && warp == 5 && lane == 0) {
     const uint32_t id_s = tc_idesc(kTM, kTN);
     const uint32_t id_o = tc_idesc(kTM, HD);
     // S(j) = Q_lo K_hi + Q_hi K_lo + Q_hi K_hi of tile j into S buffer j % 2
@@ -499,7 +597,10 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     for (int i = 0; !dead && i < ntiles; ++i) {
       if (*s_abort) { fail(); break; }
       const int cnt = min(kTN, n - i * kTN);
-      if (!__all_sync(kTF, mbar_wait_bounded(&s_full[i & 1], (uint32_t)((i >> 1) & 1), kWaitLimitNs))) {
+      // S of tile i: MODE 0 / 1 buffer i % 2; MODE 2 / 3 the pair's buffer, tile i in its
+      // half i % 2 (the same columns)
+      if (!__all_sync(kTF, mbar_wait_bounded(PRESPLIT ? s_full : &s_full[i & 1], (uint32_t)((i >> 1) & 1),
+                                             kWaitLimitNs))) {
         fail();
         break;
       }
@@ -507,6 +608,12 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       uint32_t sr[32];
       tc_ld32(tmem + lane_off + ((i & 1) ? C::C_S1 : C::C_S0), sr);
       tc_wait_ld();
+      if (PRESPLIT && ((i & 1) || i == ntiles - 1)) {
+        // both halves of the pair's S are in registers: the next pair's S may overwrite it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(s_empty);
+      }
       // window mask; a tile wholly inside this row's window skips it (a whole
       // segment row sees every key of its segment: only the tail is masked)
       const int j0 = i * kTN;
