@@ -156,6 +156,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   constexpr int NS = TCfg<HD, MODE>::NSETS;    // MODE 0 / 1 operand sets: tile j uses set j % NS
   constexpr int NSK = TCfg<HD, MODE>::NSK, NSV = TCfg<HD, MODE>::NSV;
   static_assert(NSK % 2 == 0, "S of a tile pair spans two adjacent K slots");
+  static_assert(NSK <= 8 && NSV <= 4, "the barrier block holds 8 K and 4 V slots (kfull/kfree, vfull/vfree)");
   pdl_trigger();
   pdl_wait();
   using C = TCfg<HD, MODE>;
