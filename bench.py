@@ -23,7 +23,7 @@ from __future__ import annotations
 
 import os
 
-# The CPU oracle is timed single-threaded (reported as cores = 1).
+# Each oracle worker process is single-threaded (one per host core; see oracle_pool).
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
@@ -235,27 +235,82 @@ def _units_of(w, b, seed):
     return units
 
 
-def cpu_baseline(w, budget_s):
-    """The oracle on a time-bounded sample: sequences in turn, each prepped
-    (rope table + prep of all its rows) and then attended unit by unit."""
-    inp = sample_inputs(w)
-    B = inp["meta"].shape[0]
-    t0 = time.perf_counter()
-    keys, n, seqs, b = 0, 0, 0, 0
-    while time.perf_counter() - t0 < budget_s:
-        a = oracle_prep_seq(w, inp, b % B)
-        seqs += 1
-        for i, g in _units_of(w, b % B, 0):
-            keys += oracle_unit(w, a, i, g)
-            n += 1
-            if time.perf_counter() - t0 >= budget_s:
-                break
-        b += 1
-    dt = time.perf_counter() - t0
-    return {"value": keys / dt, "unit": "keys/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} (sequence, row, KV head) units of {w.name} over {seqs} prepped sequences, "
-                      f"all query heads of each unit ({keys} attended KV-keys, {dt:.1f} s, "
-                      f"numpy float64, one thread)"}
+# The oracle runs on every host core: one single-threaded worker process per core
+# (spawn context, safe after CUDA is initialised), each holding the workload's
+# seeded sample inputs; a task is one sequence, prepped and attended unit by unit
+# (token path), or a batch of (query row, KV head) units (full-sequence attention).
+_POOL_W = None
+_POOL_INP = None
+
+
+def host_cores():
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def host_cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _pool_init(kind, name, batch):
+    global _POOL_W, _POOL_INP
+    if kind == "token":
+        w = workloads.WORKLOADS[name]
+        if batch:
+            w = dataclasses.replace(w, B=batch)
+        _POOL_W, _POOL_INP = w, sample_inputs(w)
+    else:
+        w = workloads.FLASH_WORKLOADS[name]
+        _POOL_W, _POOL_INP = w, workloads.make_flash_inputs(w)["qkv"].numpy()
+
+
+def _token_task(job):
+    """Sequence job[0] of the sample, prepped, then its first job[1] units;
+    returns (attended KV-keys, units)."""
+    b, limit, seed = job
+    w, inp = _POOL_W, _POOL_INP
+    b %= inp["meta"].shape[0]
+    a = oracle_prep_seq(w, inp, b)
+    units = _units_of(w, b, seed)[:limit]
+    return sum(oracle_unit(w, a, i, g) for i, g in units), len(units)
+
+
+def _flash_task(job):
+    count, seed = job
+    return flash_oracle_rows(_POOL_W, _POOL_INP, flash_units(_POOL_W, count, seed)), count
+
+
+def oracle_pool(kind, w, batch=None):
+    import multiprocessing as mp
+    return mp.get_context("spawn").Pool(host_cores(), initializer=_pool_init, initargs=(kind, w.name, batch))
+
+
+def cpu_baseline(w, budget_s, batch=None):
+    """The oracle on a time-bounded sample, on every host core: rounds of one task
+    per worker (a sequence of the sample, prepped, then attended unit by unit)."""
+    n = host_cores()
+    with oracle_pool("token", w, batch) as pool:
+        pool.map(_token_task, [(k, 1, 0) for k in range(n)])        # warm the workers
+        t0 = time.perf_counter()
+        keys = units = seqs = 0
+        r = 0
+        while time.perf_counter() - t0 < budget_s:
+            for k, u in pool.map(_token_task, [(r * n + k, 1 << 30, r) for k in range(n)]):
+                keys += k
+                units += u
+            seqs += n
+            r += 1
+        dt = time.perf_counter() - t0
+    return {"value": keys / dt, "unit": "keys/s", "cores": n, "kind": "oracle", "cpu": host_cpu_model(),
+            "sample": f"{units} (sequence, row, KV head) units of {w.name} over {seqs} prepped sequences, "
+                      f"all query heads of each unit ({keys} attended KV-keys, {dt:.1f} s, numpy float64, "
+                      f"{n} single-threaded worker processes, one per host core)"}
 
 
 def run_reference(args, w, rank):
@@ -263,41 +318,39 @@ def run_reference(args, w, rank):
     of the workload and attends a bounded number of its units."""
     if rank != 0:
         return
-    inp = sample_inputs(w)
-    B = inp["meta"].shape[0]
-    t_a = time.perf_counter()
-    a0 = oracle_prep_seq(w, inp, 0)
-    t_prep = time.perf_counter() - t_a
-    t_a = time.perf_counter()
-    oracle_unit(w, a0, *_units_of(w, 0, 1)[0])
-    t_unit = max(time.perf_counter() - t_a, 1e-5)
-    budget_per_step = 150.0 / max(1, args.steps + args.warmup)
-    per_step = int(max(1, min(w.t * w.nk, (budget_per_step - t_prep) / t_unit)))
-    state = {"b": 0}
+    n = host_cores()
+    with oracle_pool("token", w, args.batch) as pool:
+        # size a step: every worker preps one sequence and attends per_step of its units
+        t_a = time.perf_counter()
+        pool.map(_token_task, [(k, 1, 1) for k in range(n)])
+        t_unit = max(time.perf_counter() - t_a, 1e-4)
+        budget_per_step = 150.0 / max(1, args.steps + args.warmup)
+        per_step = int(max(1, min(w.t * w.nk, budget_per_step / t_unit)))
+        state = {"r": 0}
 
-    def step():
-        b = state["b"] % B
-        state["b"] += 1
-        a = oracle_prep_seq(w, inp, b)
-        return sum(oracle_unit(w, a, i, g) for i, g in _units_of(w, b, 1)[:per_step])
+        def step():
+            r = state["r"]
+            state["r"] += 1
+            return sum(k for k, _ in pool.map(_token_task, [(r * n + k, per_step, 1) for k in range(n)]))
 
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    keys = 0
-    for _ in range(args.steps):
-        keys += step()
-    dt = time.perf_counter() - t0
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        keys = 0
+        for _ in range(args.steps):
+            keys += step()
+        dt = time.perf_counter() - t0
     value = keys / dt
-    sample = (f"per step: rope table + prep of one sequence of {w.name} and {per_step} of its "
-              f"(row, KV head) units with all their query heads; numpy float64, one thread")
+    sample = (f"per step: on each of {n} worker processes (one per host core), the rope table and prep "
+              f"of one sequence of {w.name} and {per_step} of its (row, KV head) units with all their "
+              f"query heads; numpy float64, single-threaded workers")
     line = {"impl": "reference", "metric": "attended KV-keys/s", "value": value, "unit": "keys/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(w, args.gpus),
-            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": n, "kind": "oracle",
+                             "cpu": host_cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -471,7 +524,7 @@ def run_gpu(args, w, rank, world, local_rank):
     if e2e:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds, args.batch)
     print(json.dumps(line), flush=True)
 
 
@@ -525,17 +578,21 @@ def flash_units(w, count, seed):
 
 
 def flash_cpu_baseline(w, budget_s):
-    qkv = workloads.make_flash_inputs(w)["qkv"].numpy()
-    t0 = time.perf_counter()
-    keys, n = 0, 0
-    units = flash_units(w, 100000, 0)
-    while time.perf_counter() - t0 < budget_s and n < len(units):
-        keys += flash_oracle_rows(w, qkv, units[n:n + 1])
-        n += 1
-    dt = time.perf_counter() - t0
-    return {"value": keys / dt, "unit": "keys/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} random (query row, KV head) units of {w.name}, all query heads of each "
-                      f"({keys} attended keys, {dt:.1f} s, numpy float64, one thread)"}
+    n = host_cores()
+    with oracle_pool("flash", w) as pool:
+        pool.map(_flash_task, [(1, k) for k in range(n)])             # warm the workers
+        t0 = time.perf_counter()
+        keys = units = r = 0
+        while time.perf_counter() - t0 < budget_s:
+            for k, u in pool.map(_flash_task, [(4, 1000 + r * n + k) for k in range(n)]):
+                keys += k
+                units += u
+            r += 1
+        dt = time.perf_counter() - t0
+    return {"value": keys / dt, "unit": "keys/s", "cores": n, "kind": "oracle", "cpu": host_cpu_model(),
+            "sample": f"{units} random (query row, KV head) units of {w.name}, all query heads of each "
+                      f"({keys} attended keys, {dt:.1f} s, numpy float64, {n} single-threaded worker "
+                      f"processes, one per host core)"}
 
 
 def run_flash_reference(args, w, rank):
@@ -543,34 +600,36 @@ def run_flash_reference(args, w, rank):
     each step a bounded sample of (query row, KV head) units."""
     if rank != 0:
         return
-    qkv = workloads.make_flash_inputs(w)["qkv"].numpy()
-    t_a = time.perf_counter()
-    flash_oracle_rows(w, qkv, flash_units(w, 1, 1))
-    t_unit = max(time.perf_counter() - t_a, 1e-5)
-    budget_per_step = 150.0 / max(1, args.steps + args.warmup)
-    per_step = int(max(1, budget_per_step / t_unit))
-    state = {"i": 0}
+    n = host_cores()
+    with oracle_pool("flash", w) as pool:
+        t_a = time.perf_counter()
+        pool.map(_flash_task, [(1, k) for k in range(n)])
+        t_unit = max(time.perf_counter() - t_a, 1e-4)
+        budget_per_step = 150.0 / max(1, args.steps + args.warmup)
+        per_step = int(max(1, budget_per_step / t_unit))
+        state = {"i": 0}
 
-    def step():
-        state["i"] += 1
-        return flash_oracle_rows(w, qkv, flash_units(w, per_step, state["i"]))
+        def step():
+            state["i"] += 1
+            return sum(k for k, _ in pool.map(_flash_task, [(per_step, 100000 * state["i"] + k) for k in range(n)]))
 
-    for _ in range(args.warmup):
-        step()
-    t0 = time.perf_counter()
-    keys = 0
-    for _ in range(args.steps):
-        keys += step()
-    dt = time.perf_counter() - t0
+        for _ in range(args.warmup):
+            step()
+        t0 = time.perf_counter()
+        keys = 0
+        for _ in range(args.steps):
+            keys += step()
+        dt = time.perf_counter() - t0
     value = keys / dt
-    sample = (f"per step: {per_step} random (query row, KV head) units of {w.name} with all their query "
-              f"heads; numpy float64, one thread")
+    sample = (f"per step: on each of {n} worker processes (one per host core), {per_step} random (query row, "
+              f"KV head) units of {w.name} with all their query heads; numpy float64, single-threaded workers")
     line = {"impl": "reference", "metric": "attended keys/s", "value": value, "unit": "keys/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": dt * 1e3 / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": flash_config(w, args.gpus),
-            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "keys/s", "cores": n, "kind": "oracle", "cpu": host_cpu_model(),
+                             "sample": sample},
             "e2e": {"value": value, "unit": "keys/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
