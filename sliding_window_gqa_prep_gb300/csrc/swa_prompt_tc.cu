@@ -57,13 +57,21 @@ struct TCfg {
   // operand sets behind the split warps (MODE 0 / 1)
   static constexpr int NSETS = 2;
   // split-once blocks (MODE 2 / 3): separate pools of K (hi, lo) and V^T (hi, lo)
-  // slots, consecutive K slots adjacent so that one S product spans two tiles
+  // slots, consecutive K slots adjacent so that one S product spans G tiles
   static constexpr int NSK = HD == 64 ? 8 : 4, NSV = HD == 64 ? 4 : 2;
-  // TMEM columns
+  // MODE 2 / 3: S of G consecutive tiles is one product of N = 32 G keys (the MMA
+  // time of S follows its instruction count, not N). At hd 128 the 128 S columns
+  // leave no room for P in tensor memory: P (hi, lo) sits in shared memory and is
+  // the A operand of P V.
+  static constexpr bool PRE = MODE >= 2;
+  static constexpr int G = PRE ? (HD == 64 ? 8 : 4) : 1;
+  static constexpr bool P_SMEM = PRE && HD == 128;
+  // TMEM columns: Q_hi | Q_lo | S (MODE 0 / 1: buffers S0, S1 of 32; MODE 2 / 3: 32 G) | O | P_hi | P_lo
+  static constexpr uint32_t SCOLS = PRE ? G * kTN : 2 * kTN;
   static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S0 = 2 * HD, C_S1 = 2 * HD + kTN;
-  static constexpr uint32_t C_O = 2 * HD + 2 * kTN, C_PHI = 3 * HD + 2 * kTN, C_PLO = 3 * HD + 3 * kTN;
+  static constexpr uint32_t C_O = 2 * HD + SCOLS, C_PHI = 3 * HD + SCOLS, C_PLO = 3 * HD + SCOLS + kTN;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(3 * HD + 4 * kTN <= 512, "tensor memory budget");
+  static_assert((P_SMEM ? C_O + HD : C_PLO + kTN) <= TMEM_COLS, "tensor memory budget");
   // shared memory (bytes)
   static constexpr int LAND = kTN * HD * 4;                 // one fp32 tile of K or V
   static constexpr int OFF_LK = 0;                          // [2 stages] K landing
@@ -73,14 +81,21 @@ struct TCfg {
   // MODE 2 / 3 pools: K_hi [NSK], K_lo [NSK], V^T_hi [NSV], V^T_lo [NSV]
   static constexpr int OFF_KHI = 0, OFF_KLO = NSK * LAND, OFF_VHI = 2 * NSK * LAND;
   static constexpr int OFF_VLO = (2 * NSK + NSV) * LAND;
-  static constexpr int OFF_BAR = MODE < 2 ? OFF_OPS + NSETS * SET : 2 * (NSK + NSV) * LAND;   // mbarriers
+  // P_SMEM: P_hi, P_lo after the pools, K-major (rows = query vectors, K = keys)
+  static constexpr int OFF_PHI = 2 * (NSK + NSV) * LAND, OFF_PLO = OFF_PHI + kTM * kTN * 4;
+  static constexpr int OFF_BAR = MODE < 2 ? OFF_OPS + NSETS * SET
+                                          : 2 * (NSK + NSV) * LAND + (P_SMEM ? 2 * kTM * kTN * 4 : 0);   // mbarriers
   static constexpr int NBAR = 32;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
+  static_assert(BYTES <= 232448, "227 KB of shared memory per CTA");
   // K-major core-matrix layouts: LBO = next core matrix along K, SBO = next 8 rows
   static constexpr uint32_t K_LBO = 128, K_SBO = (HD / 4) * 128;   // K_hi: rows = keys, K = features
   static constexpr uint32_t V_LBO = 128, V_SBO = (kTN / 4) * 128;  // V^T: rows = features, K = keys
+  static constexpr uint32_t P_LBO = 128, P_SBO = (kTN / 4) * 128;  // P: rows = query vectors, K = keys
+  static_assert(!P_SMEM || (OFF_PLO + (int)(kTM / 8 * P_SBO) <= OFF_BAR && OFF_PHI % 16 == 0 && P_LBO == 128),
+                "P_hi, P_lo: 16-byte aligned, below the barriers");
 };
 
 // ---- tcgen05 / TMEM wrappers -------------------------------------------------
@@ -100,6 +115,12 @@ __device__ __forceinline__ void tc_mma(uint32_t d, uint32_t a, uint64_t bdesc, u
   asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
                :: "r"(d), "r"(a), "l"(bdesc), "r"(idesc), "r"(acc ? 1 : 0) : "memory");
+}
+// the same with A K-major in shared memory
+__device__ __forceinline__ void tc_mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+               "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+               :: "r"(d), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc ? 1 : 0) : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
@@ -155,7 +176,9 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   constexpr bool PRESPLIT = MODE >= 2;
   constexpr int NS = TCfg<HD, MODE>::NSETS;    // MODE 0 / 1 operand sets: tile j uses set j % NS
   constexpr int NSK = TCfg<HD, MODE>::NSK, NSV = TCfg<HD, MODE>::NSV;
-  static_assert(NSK % 2 == 0, "S of a tile pair spans two adjacent K slots");
+  constexpr int G = TCfg<HD, MODE>::G;
+  constexpr bool P_SMEM = TCfg<HD, MODE>::P_SMEM;
+  static_assert(NSK % G == 0, "S of a tile group spans G adjacent K slots");
   static_assert(NSK <= 8 && NSV <= 4, "the barrier block holds 8 K and 4 V slots (kfull/kfree, vfull/vfree)");
   pdl_trigger();
   pdl_wait();
@@ -178,8 +201,8 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   uint64_t* kfree = bars + 8;        // [NSK] MMA commit: S that read the slot is done
   uint64_t* vfull = bars + 16;       // [NSV] V copies landed (bytes)
   uint64_t* vfree = bars + 20;       // [NSV] MMA commit: P V that read the slot is done
-  uint64_t* s_empty = bars + 25;     // softmax warps: both halves of the pair's S read (4 arrivals)
-  // both: S (MODE 0 / 1: [2 buffers]; MODE 2 / 3: one 64-column buffer per tile pair)
+  uint64_t* s_empty = bars + 25;     // softmax warps: every tile of the group's S read (4 arrivals)
+  // both: S (MODE 0 / 1: [2 buffers]; MODE 2 / 3: one buffer of a tile group)
   uint64_t* s_full = PRESPLIT ? bars + 24 : bars + 8;
   uint64_t* p_ready = PRESPLIT ? bars + 26 : bars + 10;   // softmax warps -> MMA (4 arrivals)
   uint64_t* pv_done = PRESPLIT ? bars + 27 : bars + 11;   // MMA commit -> softmax warps
@@ -386,39 +409,39 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
 
   // ------------------------------------------------------------------ MMA issuer
   if (PRESPLIT && warp == 5 && lane == 0) {
-    // MODE 2 / 3: S of a tile pair (2p, 2p + 1) as one product of N = 64 keys (the
-    // two tiles' K slots are adjacent) into the 64-column S buffer (tile 2p in its
-    // first 32 columns); the order S(0), PV(0), S(1), PV(1), PV(2), S(2), PV(3) ...
-    // puts S of the next pair between the two P V of the current one, so it runs
-    // while the softmax warps work on the pair's second tile.
-    const uint32_t id_s = tc_idesc(kTM, 2 * kTN);
+    // MODE 2 / 3: S of a group of G tiles (their K slots are adjacent) as one product
+    // of N = 32 G keys; S of group g + 1 is issued right after P V of group g's
+    // second-to-last tile, so it runs while the softmax warps work on the last one.
+    const uint32_t id_s = tc_idesc(kTM, G * kTN);
     const uint32_t id_o = tc_idesc(kTM, HD);
-    const int npairs = (ntiles + 1) / 2;
-    auto issue_s = [&](int pr) -> bool {
-      const int t0 = 2 * pr, t1 = t0 + 1;
-      if (!mbar_wait_bounded(&kfull[t0 % NSK], (uint32_t)((t0 / NSK) & 1), kWaitLimitNs) || *s_abort)
-        return false;
-      // a missing second tile leaves columns 32..63 undefined; nothing reads them
-      if (t1 < ntiles && (!mbar_wait_bounded(&kfull[t1 % NSK], (uint32_t)((t1 / NSK) & 1), kWaitLimitNs) || *s_abort))
-        return false;
-      // the softmax warps have read both halves of the previous pair's S
-      if (pr >= 1 && (!mbar_wait_bounded(s_empty, (uint32_t)((pr - 1) & 1), kWaitLimitNs) || *s_abort))
+    const int ngroups = (ntiles + G - 1) / G;
+    auto issue_s = [&](int gr) -> bool {
+      const int t0 = G * gr;
+      // missing tiles of the last group leave their columns undefined; nothing reads them
+      for (int k = 0; k < G; ++k) {
+        const int t = t0 + k;
+        if (t < ntiles && (!mbar_wait_bounded(&kfull[t % NSK], (uint32_t)((t / NSK) & 1), kWaitLimitNs) || *s_abort))
+          return false;
+      }
+      // the softmax warps have read every tile of the previous group
+      if (gr >= 1 && (!mbar_wait_bounded(s_empty, (uint32_t)((gr - 1) & 1), kWaitLimitNs) || *s_abort))
         return false;
       tc_fence_after();
       const int slot = t0 % NSK;
+      const uint32_t dcol = C::C_S0;
 #pragma unroll 1
       for (int term = 0; term < 3; ++term) {
         const uint32_t qcol = term == 0 ? C::C_QLO : C::C_QHI;
         const uint32_t* kb =
             reinterpret_cast<const uint32_t*>(sm + (term == 1 ? C::OFF_KLO : C::OFF_KHI) + (size_t)slot * C::LAND);
         for (int ks = 0; ks < HD / 8; ++ks) {
-          const uint64_t bd = smem_desc(kb + ks * 64, C::K_LBO, C::K_SBO);   // 8 groups of 8 keys
-          tc_mma(tmem + C::C_S0, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
+          const uint64_t bd = smem_desc(kb + ks * 64, C::K_LBO, C::K_SBO);   // 4 G groups of 8 keys
+          tc_mma(tmem + dcol, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
         }
       }
       tc_commit(s_full);
-      tc_commit(&kfree[t0 % NSK]);
-      if (t1 < ntiles) tc_commit(&kfree[t1 % NSK]);
+      for (int k = 0; k < G; ++k)
+        if (t0 + k < ntiles) tc_commit(&kfree[(t0 + k) % NSK]);
       return true;
     };
     auto issue_pv = [&](int i) -> bool {
@@ -428,12 +451,21 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       const int slot = i % NSV;
 #pragma unroll 1
       for (int term = 0; term < 3; ++term) {
-        const uint32_t pcol = term == 0 ? C::C_PLO : C::C_PHI;
         const uint32_t* vb =
             reinterpret_cast<const uint32_t*>(sm + (term == 1 ? C::OFF_VLO : C::OFF_VHI) + (size_t)slot * C::LAND);
-        for (int ks = 0; ks < kTN / 8; ++ks) {
-          const uint64_t bd = smem_desc(vb + ks * 64, C::V_LBO, C::V_SBO);
-          tc_mma(tmem + C::C_O, tmem + pcol + ks * 8, bd, id_o, i > 0 || term > 0 || ks > 0);
+        if constexpr (P_SMEM) {
+          const uint32_t* pb = reinterpret_cast<const uint32_t*>(sm + (term == 0 ? C::OFF_PLO : C::OFF_PHI));
+          for (int ks = 0; ks < kTN / 8; ++ks) {
+            const uint64_t ad = smem_desc(pb + ks * 64, C::P_LBO, C::P_SBO);
+            const uint64_t bd = smem_desc(vb + ks * 64, C::V_LBO, C::V_SBO);
+            tc_mma_ss(tmem + C::C_O, ad, bd, id_o, i > 0 || term > 0 || ks > 0);
+          }
+        } else {
+          const uint32_t pcol = term == 0 ? C::C_PLO : C::C_PHI;
+          for (int ks = 0; ks < kTN / 8; ++ks) {
+            const uint64_t bd = smem_desc(vb + ks * 64, C::V_LBO, C::V_SBO);
+            tc_mma(tmem + C::C_O, tmem + pcol + ks * 8, bd, id_o, i > 0 || term > 0 || ks > 0);
+          }
         }
       }
       tc_commit(pv_done);
@@ -441,10 +473,9 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       return true;
     };
     bool ok = ntiles == 0 || issue_s(0);
-    for (int pr = 0; ok && pr < npairs; ++pr) {
-      ok = issue_pv(2 * pr);
-      if (ok && pr + 1 < npairs) ok = issue_s(pr + 1);
-      if (ok && 2 * pr + 1 < ntiles) ok = issue_pv(2 * pr + 1);
+    for (int i = 0; ok && i < ntiles; ++i) {
+      ok = issue_pv(i);
+      if (ok && i % G == G - 2 && i / G + 1 < ngroups) ok = issue_s(i / G + 1);
     }
     if (!ok) {
       *s_abort = 1;
@@ -598,19 +629,21 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     for (int i = 0; !dead && i < ntiles; ++i) {
       if (*s_abort) { fail(); break; }
       const int cnt = min(kTN, n - i * kTN);
-      // S of tile i: MODE 0 / 1 buffer i % 2; MODE 2 / 3 the pair's buffer, tile i in its
-      // half i % 2 (the same columns)
-      if (!__all_sync(kTF, mbar_wait_bounded(PRESPLIT ? s_full : &s_full[i & 1], (uint32_t)((i >> 1) & 1),
+      // S of tile i: MODE 0 / 1 buffer i % 2; MODE 2 / 3 the group's buffer, tile i in
+      // its 32 columns i % G
+      if (!__all_sync(kTF, mbar_wait_bounded(PRESPLIT ? s_full : &s_full[i & 1],
+                                             PRESPLIT ? (uint32_t)((i / G) & 1) : (uint32_t)((i >> 1) & 1),
                                              kWaitLimitNs))) {
         fail();
         break;
       }
       tc_fence_after();
       uint32_t sr[32];
-      tc_ld32(tmem + lane_off + ((i & 1) ? C::C_S1 : C::C_S0), sr);
+      tc_ld32(tmem + lane_off + (PRESPLIT ? C::C_S0 + (uint32_t)((i % G) * kTN) : ((i & 1) ? C::C_S1 : C::C_S0)),
+              sr);
       tc_wait_ld();
-      if (PRESPLIT && ((i & 1) || i == ntiles - 1)) {
-        // both halves of the pair's S are in registers: the next pair's S may overwrite it
+      if (PRESPLIT && (i % G == G - 1 || i == ntiles - 1)) {
+        // every tile of the group's S is read: S of the next group may overwrite it
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(s_empty);
@@ -673,8 +706,23 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
         break;
       }
       tc_fence_after();
-      tc_st32(tmem + lane_off + C::C_PHI, phi);
-      tc_st32(tmem + lane_off + C::C_PLO, plo);
+      if constexpr (P_SMEM) {
+        // row q of P in the K-major layout: (q / 8) * P_SBO + (k / 4) * 128 + (q % 8) * 16 +
+        // (k % 4) * 4 bytes (8 lanes write 128 contiguous bytes per store)
+        const int prow = (q >> 3) * (int)C::P_SBO + (q & 7) * 16;
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4) {
+          *reinterpret_cast<uint4*>(sm + C::OFF_PHI + prow + k4 * 128) =
+              make_uint4(phi[4 * k4], phi[4 * k4 + 1], phi[4 * k4 + 2], phi[4 * k4 + 3]);
+          *reinterpret_cast<uint4*>(sm + C::OFF_PLO + prow + k4 * 128) =
+              make_uint4(plo[4 * k4], plo[4 * k4 + 1], plo[4 * k4 + 2], plo[4 * k4 + 3]);
+        }
+        // the generic-proxy stores become visible to the MMA's (async-proxy) reads
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      } else {
+        tc_st32(tmem + lane_off + C::C_PHI, phi);
+        tc_st32(tmem + lane_off + C::C_PLO, plo);
+      }
       // rescale this row of O when its max moved (warp-uniform decision)
       if (i > 0 && __any_sync(kTF, c != 1.f)) {
         for (int c0 = 0; c0 < HD; c0 += 32) {
