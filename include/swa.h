@@ -168,12 +168,14 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  * chunks with at least 128 query vectors per KV head) also holds, for the
  * tensor-core prompt kernel, every KV head's sink and window keys split once
  * into TF32 operand blocks of 32 keys, which the kernel then copies in whole
- * blocks; with less, the kernel splits the keys it stages itself (same
+ * blocks, and the order in which its CTAs take the row blocks (longest
+ * first); with less, the kernel splits the keys it stages itself (same
  * results within f32 rounding). ev_start / ev_stop, when non-NULL, are recorded on the
  * stream right before and after the main attention kernel (for timing it).
  * err, when non-NULL, is a device word the kernels OR SWA_DERR_* bits into.
  *
- * Errors: SWA_E_NULL, SWA_E_SHAPE, SWA_E_ALIGN, SWA_E_WORKSPACE, SWA_E_CUDA.
+ * Errors: SWA_E_NULL, SWA_E_SHAPE (also B * nk > 65534, or more than 65535
+ * row blocks: grid limits), SWA_E_ALIGN, SWA_E_WORKSPACE, SWA_E_CUDA.
  */
 /* Far field of a chunk ("o1c_msl.metal", cortiq-engine 0.8.79: o1c_far_e,
  * o1c_far, o1c_far_commit and the token path's o1c_tok_far, o1c_tok_merge,

@@ -47,6 +47,8 @@ static int attend_shape_ok(const swa_attend_args* a) {
   if (a->far && (a->t > 32 || a->t > a->cap || a->far->m < 1 || a->far->m > 32)) return 0;
   // output rows are indexed in 32 bits (q alone would exceed device memory first)
   if ((long long)a->B * a->t * a->nh >= (1LL << 31)) return 0;
+  // grid y / z extents: (sequence, KV head) pairs (one more row in the split-once pass)
+  if ((long long)a->B * a->nk > 65534) return 0;
   return 1;
 }
 
@@ -79,6 +81,7 @@ static void add_far_records(const swa_attend_args* a, AttendPlan* p) {
 bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   if (!attend_shape_ok(a)) return false;
   p->off_ops = 0;
+  p->off_order = 0;
   p->ops_nblk = 0;
   p->ops_nsb = 0;
   const int hpg = a->nh / a->nk;
@@ -91,6 +94,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
     p->nq = block;
     p->rows = rows;
     p->n_rb = (a->t + rows - 1) / rows;
+    if (p->n_rb > 65535) return false;
     const long long keys_max = (long long)a->ns + a->cap + rows - 1;
     if (keys_max > (1LL << 30)) return false;
     p->keys_max = (int)keys_max;
@@ -115,6 +119,9 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
       p->ops_nblk = (int)(p->ops_nsb + nlog);
       p->off_ops = p->ws_bytes;
       p->ws_bytes += up((size_t)a->B * a->nk * p->ops_nblk * 4 * kOpsBlockKeys * a->hd * sizeof(float));
+      // the order in which the kernel's CTAs take the row blocks (longest first)
+      p->off_order = p->ws_bytes;
+      p->ws_bytes += up(p->items * sizeof(int));
     }
     return true;
   }
@@ -127,6 +134,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   p->nq = nq;
   p->rows = rows;
   p->n_rb = (a->t + rows - 1) / rows;
+  if (p->n_rb > 65535) return false;
   const long long keys_max = (long long)a->ns + a->cap + rows - 1;
   if (keys_max > (1LL << 30)) return false;
   p->keys_max = (int)keys_max;
@@ -316,6 +324,7 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
                                                                       : nullptr;
   p.ops_nblk = plan.ops_nblk;
   p.ops_nsb = plan.ops_nsb;
+  p.ws_order = p.ops ? reinterpret_cast<int*>(ws + plan.off_order) : nullptr;
   int rc = SWA_OK;
   if (p.far) {            // before the attention: it reads the evicted ring slot, which the commit overwrites
     rc = launch_far(p, stream);

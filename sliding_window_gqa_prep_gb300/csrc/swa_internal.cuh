@@ -37,6 +37,7 @@ struct AttendPlan {
   size_t off_ops;    // byte offset of the split-once operand blocks (tensor-core prompt kernel)
   int ops_nblk;      // their blocks per (sequence, KV head), 0 if the plan has none
   int ops_nsb;       // sink blocks among them
+  size_t off_order;  // byte offset of the tensor-core row-block order (with the operand blocks)
 };
 bool make_plan(const swa_attend_args* a, AttendPlan* p);
 
@@ -84,6 +85,8 @@ struct AttendParams {
   float* ops;
   int ops_nblk;               // blocks per (sequence or segment, KV head)
   int ops_nsb;                // token path: sink blocks among them (ceil(ns / 32))
+  int* ws_order;              // with ops on the token path: [B * nk * n_rb] row blocks (index
+                              // (b * nk + g) * n_rb + rb), longest first
 };
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);

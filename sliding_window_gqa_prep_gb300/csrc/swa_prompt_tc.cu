@@ -170,6 +170,14 @@ __device__ __forceinline__ uint32_t tf32_hi(float x) {
 // and 3 take split-once operand blocks from p.ops (token path: the sinks' blocks,
 // then blocks of logical keys 32k .. 32k + 31; a row block's tiles are its sink
 // blocks and the logical blocks that hold its window).
+// MODE 3 tiles of row block rb: the sink blocks, then logical blocks kb0 .. (len0 +
+// r_last) / 32, where kb0 holds the first key of the block's first row's window
+__device__ __forceinline__ int tc_row_block_tiles(const AttendParams& p, const SeqState& st, int rb) {
+  const int r0 = rb * p.rows, r_last = min(r0 + p.rows, p.t) - 1;
+  const int xlo = st.len0 + r0 + 1 - min(st.W, st.len0 + r0 + 1);
+  return p.ops_nsb + (st.len0 + r_last) / kTN - xlo / kTN + 1;
+}
+
 template <int HD, int MODE>
 __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
   constexpr bool FLASH = MODE == 1 || MODE == 2;
@@ -210,7 +218,13 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + C::NBAR) + 1);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rb = blockIdx.y, bg = blockIdx.z;
+  int rb = blockIdx.y, bg = blockIdx.z;
+  if constexpr (MODE == 3) {
+    // the row blocks run longest first, in the order the split-once pass wrote
+    const int u = p.ws_order[blockIdx.y + (size_t)p.n_rb * blockIdx.z];
+    rb = u % p.n_rb;
+    bg = u / p.n_rb;
+  }
   const int b = bg / p.nk, g = bg % p.nk;
   const int r0 = rb * p.rows;
   SeqState st{0, 0, 0};
@@ -239,7 +253,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   // MODE 3 tiles: sink blocks 0 .. nsb - 1, then logical blocks kb0 .. (len0 + r_last) / 32
   const int nsb = MODE == 3 ? p.ops_nsb : 0;
   const int kb0 = xlo / kTN;
-  const int ntiles = MODE == 3 ? nsb + (st.len0 + r_last) / kTN - kb0 + 1 : (n + kTN - 1) / kTN;
+  const int ntiles = MODE == 3 ? tc_row_block_tiles(p, st, rb) : (n + kTN - 1) / kTN;
   const size_t kv_head = (size_t)b * p.nk + g;
 
   if (tid == 0) {
@@ -872,14 +886,58 @@ __global__ void __launch_bounds__(256) flash_presplit_kernel(AttendParams p) {
   });
 }
 
+// The token path's row blocks ordered by their tile count, longest first, by one CTA
+// of 256 threads (a counting sort; equal counts in any order): the attention
+// kernel's CTA c takes row block ws_order[c], so the CTAs that start last are the
+// shortest and the SMs finish close together. Every order gives the same results.
+__device__ void order_row_blocks(const AttendParams& p) {
+  constexpr int kBins = 2048;
+  __shared__ int cnt[kBins];
+  const int U = p.B * p.nk * p.n_rb;
+  const int nb = min(kBins, p.ops_nblk + 1);   // a row block has at most ops_nblk tiles
+  auto key = [&](int u) {                       // bin nb - 1 - tiles: longest first
+    const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
+    const int tiles = min(max(tc_row_block_tiles(p, st, u % p.n_rb), 0), nb - 1);
+    return nb - 1 - tiles;
+  };
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int u = threadIdx.x; u < U; u += blockDim.x) atomicAdd(&cnt[key(u)], 1);
+  __syncthreads();
+  // exclusive prefix over the bins by warp 0: lane l sums bins l * per .. l * per + per - 1
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x, per = (nb + 31) / 32;
+    const int lo = min(lane * per, nb), hi = min(lo + per, nb);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += cnt[i];
+    int incl = sum;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      const int c = cnt[i];
+      cnt[i] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int u = threadIdx.x; u < U; u += blockDim.x) p.ws_order[atomicAdd(&cnt[key(u)], 1)] = u;
+}
+
 // Token path: one CTA per (sequence, KV head, block): blocks 0 .. nsb - 1 hold the
 // sinks, block nsb + k the logical keys x = 32k .. 32k + 31 below len0 + t (ring
 // slot (head0 + x) % W for x < len0, chunk row x - len0 after), read before the
-// commit rewrites the ring.
+// commit rewrites the ring. The extra row blockIdx.y = B * nk orders the row blocks.
 template <int HD>
 __global__ void __launch_bounds__(256) token_presplit_kernel(AttendParams p) {
   pdl_trigger();
   pdl_wait();
+  if (blockIdx.y == (unsigned)(p.B * p.nk)) {
+    if (blockIdx.x == 0) order_row_blocks(p);
+    return;
+  }
   const int blk = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.nk, g = bg % p.nk;
   const SeqState st = sanitize_state(p.meta[b], p.cap, nullptr);   // the attention reports bad metas
@@ -926,7 +984,7 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   if (MODE >= 2) {
-    const dim3 pgrid((unsigned)p.ops_nblk, (unsigned)(p.B * p.nk));
+    const dim3 pgrid((unsigned)p.ops_nblk, (unsigned)(p.B * p.nk + (MODE == 3 ? 1 : 0)));
     const int rc = finish_launch(MODE == 2 ? launch_pdl(flash_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p)
                                            : launch_pdl(token_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p));
     if (rc != SWA_OK) return rc;

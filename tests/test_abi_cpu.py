@@ -116,6 +116,18 @@ def test_workspace_size_rejects_bad_sizes(lib):
     assert lib.swa_attend_workspace_size(ctypes.byref(a)) == 0
 
 
+def test_attend_rejects_shapes_past_the_grid_limits(lib):
+    size = lambda **kw: lib.swa_attend_workspace_size(ctypes.byref(_attend(**kw)))
+    call = lambda **kw: lib.swa_attend(ctypes.byref(_attend(**kw)), None)
+    # (sequence, KV head) pairs index a grid dimension (65535), one more row for the ordering
+    assert size(B=32767, nk=2) > 0
+    assert size(B=32768, nk=2) == 0 and call(B=32768, nk=2) == _abi.SWA_E_SHAPE
+    # row blocks of 4 rows (32 query heads per KV head, 128 query vectors) index another
+    assert size(B=1, t=4 * 65535, nh=32, nk=1) > 0
+    assert size(B=1, t=4 * 65535 + 1, nh=32, nk=1) == 0
+    assert call(B=1, t=4 * 65535 + 1, nh=32, nk=1) == _abi.SWA_E_SHAPE
+
+
 def test_rope_table_rejects_bad_arguments(lib):
     assert lib.swa_rope_table(None, FAKE, 1, 1, 64, 1e4, None) == _abi.SWA_E_NULL
     assert lib.swa_rope_table(FAKE, FAKE, 1, 1, 48, 1e4, None) == _abi.SWA_E_SHAPE
@@ -165,7 +177,9 @@ def test_workspace_minimum_and_split_once_blocks(lib):
     lo = lib.swa_attend_workspace_min(ctypes.byref(p))
     hi = lib.swa_attend_workspace_size(ctypes.byref(p))
     blocks = 1 + (100 + 64 + 31) // 32                      # sink block + logical blocks
-    assert hi - lo >= 2 * 2 * blocks * 4 * 32 * 128 * 4 and hi - lo < 2 * 2 * blocks * 4 * 32 * 128 * 4 + 256
+    ops = 2 * 2 * blocks * 4 * 32 * 128 * 4                 # B * nk * blocks * (K, V) x (hi, lo) x 32 x hd
+    order = 2 * 2 * (64 // 32) * 4                          # one int per row block (32 rows of 4 heads)
+    assert hi - lo >= ops + order and hi - lo < ops + order + 2 * 256
     call = lambda a: lib.swa_attend(ctypes.byref(a), None)
     assert call(_attend(t=64, nh=8, nk=2, cap=100, ns=3, workspace_bytes=lo - 1)) == _abi.SWA_E_WORKSPACE
     assert lib.swa_attend_workspace_min(None) == 0
