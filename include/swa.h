@@ -172,6 +172,10 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  * first); with less, the kernel splits the keys it stages itself (same
  * results within f32 rounding). ev_start / ev_stop, when non-NULL, are recorded on the
  * stream right before and after the main attention kernel (for timing it).
+ * gate_ready, when non-NULL, is an event the stream waits for after the
+ * attention and before the merge, the only kernel that reads gate: a caller
+ * may still be copying the gate in (on another stream) while the attention
+ * runs, and record gate_ready after that copy.
  * err, when non-NULL, is a device word the kernels OR SWA_DERR_* bits into.
  *
  * Errors: SWA_E_NULL, SWA_E_SHAPE (also B * nk > 65534, or more than 65535
@@ -237,6 +241,7 @@ typedef struct swa_attend_args {
   cudaEvent_t ev_start;          /* optional                                */
   cudaEvent_t ev_stop;           /* optional                                */
   const swa_far_args* far;       /* optional far field (t <= 32), host struct */
+  cudaEvent_t gate_ready;        /* optional: the merge waits for it        */
 } swa_attend_args;
 
 /* Bytes of workspace swa_attend needs for these sizes (reads B, t, nh, nk,

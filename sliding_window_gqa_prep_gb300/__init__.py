@@ -146,8 +146,13 @@ def attend_workspace_min(B, t, nh, nk, hd, cap, ns, num_splits: int = 0, far_m: 
 
 def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate_scale,
            scale: float, *, out=None, workspace=None, commit: bool = False, meta_out=None,
-           num_splits: int = 0, err=None, ev_start=None, ev_stop=None, far=None, stream=None):
+           num_splits: int = 0, err=None, ev_start=None, ev_stop=None, far=None, stream=None,
+           gate_ready=None):
     """Attention of a chunk (decode, verify or prompt); see include/swa.h.
+
+    gate_ready: optional recorded torch CUDA event that the merge (the only
+    kernel that reads ``gate``) waits for, so the gate may still be copied in
+    on another stream while the attention runs.
 
     far: optional far field of a decode step (t = 1), a dict with m, rect and
     the device tensors k_tilde [B][nk][m][hd], q_tilde [B][nh][m][hd],
@@ -183,6 +188,7 @@ def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate
     a.err = _ptr(err, "err", (1,), torch.int32, required=False)
     a.ev_start = ctypes.c_void_p(ev_start.cuda_event) if ev_start is not None else None
     a.ev_stop = ctypes.c_void_p(ev_stop.cuda_event) if ev_stop is not None else None
+    a.gate_ready = ctypes.c_void_p(gate_ready.cuda_event) if gate_ready is not None else None
     fa = None
     if far is not None:
         m = far_m
@@ -306,13 +312,16 @@ class TokenPath:
         }
 
     def step(self, yq, yk, yv, gate, *, commit: bool = True, out_host=None,
-             ev_start=None, ev_stop=None, prep_events=None, stream=None):
+             ev_start=None, ev_stop=None, prep_events=None, stream=None, v_ready=None,
+             gate_ready=None):
         """One pass of the path. commit = True writes the chunk into the ring and
         the advanced meta into ``meta_next`` (the current ``meta`` is kept, so
         repeating a step repeats the same work). Host inputs are copied in and
         the output is copied back (into ``out_host`` when given, e.g. pinned).
         ev_start / ev_stop bracket the attention kernel, prep_events (a pair of
-        torch CUDA events) the prep kernel, on the step's stream."""
+        torch CUDA events) the prep kernel, on the step's stream. v_ready and
+        gate_ready are events of device inputs still being copied in: the
+        attention waits for v_ready, the merge for gate_ready."""
         host = not yq.is_cuda
         if host:
             for name, x in (("yq", yq), ("yk", yk), ("yv", yv), ("gate", gate)):
@@ -328,10 +337,13 @@ class TokenPath:
                        q_out=self.q, k_out=self.k, copy_v=False, stream=stream)
         if prep_events is not None:
             prep_events[1].record(stream)
+        if v_ready is not None:
+            (stream if stream is not None else torch.cuda.current_stream()).wait_event(v_ready)
         attend(self.meta, q, k, v, self.ring_k, self.ring_v, self.sink_k, self.sink_v, gate,
                self.gate_scale, self.scale, out=self.out, workspace=self.workspace,
                commit=commit, meta_out=self.meta_next, num_splits=self.num_splits, err=self.err,
-               ev_start=ev_start, ev_stop=ev_stop, far=self.far, stream=stream)
+               ev_start=ev_start, ev_stop=ev_stop, far=self.far, stream=stream,
+               gate_ready=gate_ready)
         if host:
             if out_host is None:
                 return self.out.to("cpu")
@@ -344,10 +356,16 @@ class TokenPath:
         """Record one host-to-host step as a CUDA graph: the copies of the
         pinned inputs ``h_in`` to the device, prep, attention, merge/gate/
         commit and the copy of the output into the pinned ``h_out``. Write a
-        step's inputs into ``h_in`` and call ``replay``."""
+        step's inputs into ``h_in`` and call ``replay``.
+
+        The inputs travel on a copy stream in the order the kernels need them
+        (yq and yk for the prep, then yv for the attention, then the gate for
+        the merge), so the later copies overlap the prep and the attention."""
         self.h_in = {n: torch.empty(tuple(b.shape), dtype=b.dtype).pin_memory()
                      for n, b in self.in_bufs.items()}
         self.h_out = torch.empty(tuple(self.out.shape), dtype=self.out.dtype).pin_memory()
+        self._copy_stream = torch.cuda.Stream()
+        self._arrived = {n: torch.cuda.Event() for n in ("qk", "v", "gate")}
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
         with torch.cuda.stream(side):           # warm-up: attributes, plans, allocations
@@ -361,10 +379,18 @@ class TokenPath:
         return g
 
     def _graph_body(self):
-        for name, buf in self.in_bufs.items():
-            buf.copy_(self.h_in[name], non_blocking=True)
-        self.step(self.in_bufs["yq"], self.in_bufs["yk"], self.in_bufs["yv"], self.in_bufs["gate"])
+        cur, cs, ev = torch.cuda.current_stream(), self._copy_stream, self._arrived
+        cs.wait_stream(cur)
+        with torch.cuda.stream(cs):
+            for name, mark in (("yq", None), ("yk", "qk"), ("yv", "v"), ("gate", "gate")):
+                self.in_bufs[name].copy_(self.h_in[name], non_blocking=True)
+                if mark:
+                    ev[mark].record(cs)
+        cur.wait_event(ev["qk"])
+        self.step(self.in_bufs["yq"], self.in_bufs["yk"], self.in_bufs["yv"], self.in_bufs["gate"],
+                  v_ready=ev["v"], gate_ready=ev["gate"])
         self.h_out.copy_(self.out, non_blocking=True)
+        cur.wait_stream(cs)
 
     def replay(self):
         """One captured step; returns the pinned host output."""

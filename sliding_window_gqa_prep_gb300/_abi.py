@@ -53,7 +53,7 @@ class AttendArgs(ctypes.Structure):
         ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
         ("commit", ctypes.c_int), ("meta_out", c_float_p), ("num_splits", ctypes.c_int),
         ("err", c_float_p), ("ev_start", ctypes.c_void_p), ("ev_stop", ctypes.c_void_p),
-        ("far", ctypes.POINTER(FarArgs)),
+        ("far", ctypes.POINTER(FarArgs)), ("gate_ready", ctypes.c_void_p),
     ]
 
 

@@ -332,6 +332,10 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   }
   rc = launch_attend_partial(p, stream, a->ev_start, a->ev_stop);
   if (rc != SWA_OK) return rc;
+  if (a->gate_ready) {    // the gate may still be arriving: only the merge reads it
+    const cudaError_t e = cudaStreamWaitEvent(stream, a->gate_ready, 0);
+    if (e != cudaSuccess) return cuda_status(e);
+  }
   return launch_attend_merge(p, stream);
 }
 

@@ -357,6 +357,28 @@ def test_token_path_captured_graph_matches_oracle_twice():
         assert_close(out.numpy(), ref, "graph replay out")
 
 
+def test_prompt_chunk_captured_graph_follows_each_steps_inputs():
+    # a tensor-core chunk (64 rows x 4 query heads per KV head): the copies of yv and
+    # the gate overlap the prep and the attention. Every window stays below W - t,
+    # so one replay's commit never lands in the next one's window.
+    w = workloads.custom(B=2, t=64, nh=8, nk=2, hd=128, window=200, cap=200, ns=3,
+                         pos_mode="prompt", pos_lo=0, pos_hi=100, seed=29)
+    inp = workloads.make_inputs(w)
+    g = torch.Generator().manual_seed(30)
+    other = dict(inp, **{k: torch.randn(inp[k].shape, generator=g) for k in ("yq", "yk", "yv", "gate")})
+    tp = swa.TokenPath(B=w.B, t=w.t, nh=w.nh, nk=w.nk, hd=w.hd, cap=w.cap, ns=w.ns,
+                       q_scale=inp["q_scale"], gate_scale=inp["gate_scale"],
+                       ring_k=inp["ring_k"], ring_v=inp["ring_v"], sink_k=inp["sink_k"],
+                       sink_v=inp["sink_v"], meta=inp["meta"], pos0=inp["pos0"])
+    tp.capture()
+    for cur in (inp, other, inp):
+        for k in ("yq", "yk", "yv", "gate"):
+            tp.h_in[k].copy_(cur[k])
+        out = tp.replay()
+        assert_close(out.numpy(), oracle.attend(oracle_inputs(w, cur), w.score_scale, w.hpg),
+                     "graph replay out")
+
+
 def test_rollback_matches_oracle_bit_for_bit():
     g = torch.Generator().manual_seed(31)
     B, cap = 300, 64
