@@ -346,7 +346,12 @@ int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);
  *            blocks of 32 keys once per call (instead of once per block of
  *            query vectors) and the attention kernel copies them in whole
  *            blocks; without it (NULL), the attention kernel splits the rows it
- *            stages itself. Both give bit-identical outputs.
+ *            stages itself. Both give bit-identical outputs, except in a split
+ *            launch tail: when the blocks of 128 query vectors (one per SM at
+ *            a time) fill at least one wave of the device's SMs and leave a
+ *            remainder of at most half a wave, and the workspace has room for
+ *            it, the last blocks run as several key ranges each whose partial
+ *            sums the last range combines (agreeing within f32 rounding).
  * The call allocates nothing. Errors: SWA_E_NULL (qkv, segs or out NULL),
  * SWA_E_SHAPE (sizes, offsets past ld, nh * hd > ldo, nseg < 1, max_len < 1,
  * scale not finite), SWA_E_ALIGN (pointers not 16-byte aligned, workspace not
@@ -367,7 +372,10 @@ typedef struct swa_flash_args {
   size_t workspace_bytes;
 } swa_flash_args;
 /* Workspace bytes of the split-once form of swa_flash: nseg * nk *
- * ceil(max_len / 32) blocks of 4 x 32 x hd floats; 0 for unsupported sizes. */
+ * ceil(max_len / 32) blocks of 4 x 32 x hd floats, plus, when the launch has a
+ * split tail on the current device, its partial records (128 x (hd + 2)
+ * floats per key range, at most one range per SM) and counters; 0 for
+ * unsupported sizes. Queries the current device's SM count on first use. */
 size_t swa_flash_workspace_size(const swa_flash_args* args);
 int swa_flash(const swa_flash_args* args, cudaStream_t stream);
 

@@ -351,9 +351,38 @@ static size_t ops_bytes(const swa_flash_args* a) {
   return (size_t)a->nseg * a->nk * nblk * 4 * kOpsBlockKeys * a->hd * sizeof(float);
 }
 
+// The tail of a flash launch. The attention runs one CTA (one row block of one
+// segment and KV head, a "unit") per SM at a time; when the units fill at least
+// one wave of SMs and leave a remainder of at most half of one, the last `tail`
+// units are cut into q = sms / tail pieces each (key ranges of the unit, combined
+// by the last piece), so that the last wave keeps every SM busy.
+struct FlashTail {
+  int tail = 0, q = 1;
+  size_t rec_bytes = 0;   // piece records [tail * q][128] x (hd + 2) floats
+  size_t bytes = 0;       // + combine counters [tail][4] ints
+};
+static FlashTail flash_tail(const swa_flash_args* a) {
+  FlashTail ft;
+  const int rows = 128 / (a->nh / a->nk);
+  const long long units = (long long)((a->max_len + rows - 1) / rows) * a->nseg * a->nk;
+  const int n = num_sms();
+  const long long sms = n > 0 ? n : 148;
+  if (units < sms) return ft;
+  const long long rem = units % sms;
+  if (rem == 0 || 2 * rem > sms) return ft;
+  const long long q = sms / rem;
+  if (units - rem + rem * q >= (1LL << 31)) return ft;
+  ft.tail = (int)rem;
+  ft.q = (int)q;
+  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  ft.rec_bytes = up((size_t)rem * q * 128 * (a->hd + 2) * sizeof(float));
+  ft.bytes = ft.rec_bytes + up((size_t)rem * 4 * sizeof(int));
+  return ft;
+}
+
 size_t swa_flash_workspace_size(const swa_flash_args* a) {
   if (!a || !flash_shape_ok(a)) return 0;
-  return ops_bytes(a);
+  return ops_bytes(a) + flash_tail(a).bytes;
 }
 
 int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
@@ -388,6 +417,18 @@ int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   p.max_len = a->max_len;
   p.ops = static_cast<float*>(a->workspace);
   p.ops_nblk = (a->max_len + kOpsBlockKeys - 1) / kOpsBlockKeys;
+  if (a->workspace) {
+    // the split tail when the workspace has room for its records
+    const FlashTail ft = flash_tail(a);
+    const size_t ob = ops_bytes(a);   // a multiple of 512 bytes
+    if (ft.tail > 0 && a->workspace_bytes >= ob + ft.bytes) {
+      unsigned char* ws = static_cast<unsigned char*>(a->workspace);
+      p.flash_tail = ft.tail;
+      p.flash_q = ft.q;
+      p.ws_rec = reinterpret_cast<float*>(ws + ob);
+      p.ws_cnt = reinterpret_cast<int*>(ws + ob + ft.rec_bytes);
+    }
+  }
   return launch_flash_tc(p, stream, a->ev_start, a->ev_stop);
 }
 

@@ -85,6 +85,9 @@ struct AttendParams {
   float* ops;
   int ops_nblk;               // blocks per (sequence or segment, KV head)
   int ops_nsb;                // token path: sink blocks among them (ceil(ns / 32))
+  int flash_tail, flash_q;    // swa_flash: the last flash_tail units run as flash_q pieces each
+  float* ws_rec;              // their records: [tail * q][128] x (O[hd], then (m, l))
+  int* ws_cnt;                // [tail][4] pieces done per unit and softmax warp
   int* ws_order;              // with ops on the token path: [B * nk * n_rb] row blocks (index
                               // (b * nk + g) * n_rb + rb), longest first
 };

@@ -225,6 +225,25 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     rb = u % p.n_rb;
     bg = u / p.n_rb;
   }
+  // MODE 2 launch tail (swa_flash): the last flash_tail units of the 1-D grid run as
+  // flash_q pieces each, piece j taking the j-th of flash_q equal runs of the
+  // unit's tiles; tail_at numbers the pieces of the tail in launch order
+  int piece = 0, npiece = 1, tail_at = 0;
+  if constexpr (MODE == 2) {
+    if (p.flash_q > 1) {
+      const long long full = (long long)p.n_rb * p.B * p.nk - p.flash_tail;
+      long long u = blockIdx.x;
+      if (u >= full) {
+        const long long pc = u - full;
+        u = full + pc / p.flash_q;
+        piece = (int)(pc % p.flash_q);
+        npiece = p.flash_q;
+        tail_at = (int)pc;
+      }
+      rb = (int)(u % p.n_rb);
+      bg = (int)(u / p.n_rb);
+    }
+  }
   const int b = bg / p.nk, g = bg % p.nk;
   const int r0 = rb * p.rows;
   SeqState st{0, 0, 0};
@@ -253,7 +272,12 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   // MODE 3 tiles: sink blocks 0 .. nsb - 1, then logical blocks kb0 .. (len0 + r_last) / 32
   const int nsb = MODE == 3 ? p.ops_nsb : 0;
   const int kb0 = xlo / kTN;
-  const int ntiles = MODE == 3 ? tc_row_block_tiles(p, st, rb) : (n + kTN - 1) / kTN;
+  // a piece takes tiles tile0 .. tile0 + ntiles - 1 of the unit's ceil(n / 32) (may be none)
+  const int nt_all = (n + kTN - 1) / kTN;
+  const int tile0 = npiece > 1 ? (int)((long long)piece * nt_all / npiece) : 0;
+  const int ntiles = MODE == 3    ? tc_row_block_tiles(p, st, rb)
+                     : npiece > 1 ? (int)((long long)(piece + 1) * nt_all / npiece) - tile0
+                                  : nt_all;
   const size_t kv_head = (size_t)b * p.nk + g;
 
   if (tid == 0) {
@@ -348,7 +372,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       }
       if (__shfl_sync(kTF, *s_abort, 0)) break;
       if (lane == 0) {
-        const int blk = (MODE == 3 && i >= nsb) ? i + kb0 : i;
+        const int blk = (MODE == 3 && i >= nsb) ? i + kb0 : i + tile0;
         const float* src = blocks + (size_t)blk * 4 * (kTN * HD);
         mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(2 * C::LAND));
         bulk_g2s(hi_pool + (size_t)slot * C::LAND, src, (uint32_t)C::LAND, &fullb[slot]);
@@ -642,7 +666,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     };
     for (int i = 0; !dead && i < ntiles; ++i) {
       if (*s_abort) { fail(); break; }
-      const int cnt = min(kTN, n - i * kTN);
+      const int cnt = min(kTN, n - (tile0 + i) * kTN);
       // S of tile i: MODE 0 / 1 buffer i % 2; MODE 2 / 3 the group's buffer, tile i in
       // its 32 columns i % G
       if (!__all_sync(kTF, mbar_wait_bounded(PRESPLIT ? s_full : &s_full[i & 1],
@@ -664,7 +688,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       }
       // window mask; a tile wholly inside this row's window skips it (a whole
       // segment row sees every key of its segment: only the tail is masked)
-      const int j0 = i * kTN;
+      const int j0 = (tile0 + i) * kTN;
       bool inside;
       // MODE 3: a sink tile holds sinks j0 .. j0 + 31 (valid below ns); a logical tile
       // holds keys x0 .. x0 + 31, each valid inside the row's window
@@ -757,7 +781,58 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     if (!dead && !*s_abort) {
       const bool ok = __all_sync(kTF, ntiles == 0 ||
                                           mbar_wait_bounded(pv_done, (uint32_t)((ntiles - 1) & 1), kWaitLimitNs));
-      if (ok && FLASH) {
+      if (ok && FLASH && npiece > 1) {
+        // a piece of a split unit: its record (O unnormalised, then m, l) to the
+        // workspace; per softmax warp (32 query vectors), the last of the unit's
+        // pieces to get there combines all of them. No wait on another CTA.
+        tc_fence_after();
+        const size_t rstride = (size_t)kTM * (HD + 2);
+        float* rec = p.ws_rec + (size_t)tail_at * rstride;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(tmem + lane_off + C::C_O + c0, o);
+          tc_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(rec + (size_t)q * HD + c0 + k) =
+                ntiles > 0 ? make_float4(__uint_as_float(o[k]), __uint_as_float(o[k + 1]),
+                                         __uint_as_float(o[k + 2]), __uint_as_float(o[k + 3]))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        reinterpret_cast<float2*>(rec + kTM * HD)[q] =
+            ntiles > 0 ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(p.ws_cnt + (size_t)(tail_at / npiece) * 4 + warp, 1) == npiece - 1;
+        if (__shfl_sync(kTF, last, 0)) {
+          __threadfence();
+          const float* rec0 = p.ws_rec + (size_t)(tail_at - piece) * rstride;
+          auto ml_of = [&](int j) { return __ldcg(reinterpret_cast<const float2*>(rec0 + j * rstride + kTM * HD) + q); };
+          float M = -INFINITY;
+          for (int j = 0; j < npiece; ++j) M = fmaxf(M, ml_of(j).x);
+          float den = 0.f;
+          for (int j = 0; j < npiece; ++j) {
+            const float2 ml = ml_of(j);
+            if (ml.x != -INFINITY) den += ml.y * exp2f(ml.x - M);   // a piece without keys weighs 0
+          }
+          const float inv = 1.0f / den;
+          if (q_ok) {
+            float* dst = p.out + (size_t)(s0 + r) * p.ldo + ((size_t)g * p.hpg + (q % p.hpg)) * HD;
+            for (int c = 0; c < HD; c += 4) {
+              float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+              for (int j = 0; j < npiece; ++j) {
+                const float2 ml = ml_of(j);
+                if (ml.x == -INFINITY) continue;
+                const float w = exp2f(ml.x - M);
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(rec0 + j * rstride + (size_t)q * HD + c));
+                acc.x += v.x * w; acc.y += v.y * w; acc.z += v.z * w; acc.w += v.w * w;
+              }
+              *reinterpret_cast<float4*>(dst + c) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+            }
+          }
+        }
+      } else if (ok && FLASH) {
         // o = O / l straight to the output row of this query vector
         tc_fence_after();
         const float inv = 1.0f / l_run;
@@ -869,6 +944,9 @@ template <int HD>
 __global__ void __launch_bounds__(256) flash_presplit_kernel(AttendParams p) {
   pdl_trigger();
   pdl_wait();
+  // the attention's combine counters of a split launch tail (4 per tail unit)
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < 4 * p.flash_tail; i += blockDim.x) p.ws_cnt[i] = 0;
   const int blk = blockIdx.x, bg = blockIdx.y;
   const int b = bg / p.nk, g = bg % p.nk;
   const uint32_t s0 = p.segs[2 * b], len = p.segs[2 * b + 1];
@@ -990,6 +1068,8 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
     if (rc != SWA_OK) return rc;
   }
   dim3 grid(1u, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
+  if (MODE == 2 && p.flash_q > 1)   // 1-D: whole units, then the tail's pieces
+    grid = dim3((unsigned)((long long)p.n_rb * p.B * p.nk - p.flash_tail + (long long)p.flash_tail * p.flash_q));
   if (e0) cudaEventRecord(e0, s);
   cudaError_t e = launch_pdl(kern, grid, dim3(kTThreads), C::BYTES, s, p);
   note_launch();

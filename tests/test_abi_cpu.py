@@ -237,3 +237,18 @@ def test_flash_workspace_size_and_checks(lib):
     call = lambda a: lib.swa_flash(ctypes.byref(a), None)
     assert call(_flash(workspace=FAKE, workspace_bytes=need - 1)) == _abi.SWA_E_WORKSPACE
     assert call(_flash(workspace=FAKE + 16, workspace_bytes=need)) == _abi.SWA_E_ALIGN   # wants 256 B
+
+
+def test_flash_workspace_holds_the_split_tail_records(lib):
+    # 154 row blocks of 128 (one head) pass one wave of SMs (148 when no GPU is
+    # visible): the size adds the tail pieces' records (128 x (hd + 2) floats each,
+    # at most one per SM) and a 256-byte block of combine counters
+    T = 128 * 154
+    a = _flash(T=T, nseg=1, nh=1, nk=1, ld=192, q_off=0, k_off=64, v_off=128, ldo=64, max_len=T)
+    need = lib.swa_flash_workspace_size(ctypes.byref(a))
+    ops = (T // 32) * 4 * 32 * 64 * 4
+    rec = 128 * (64 + 2) * 4
+    assert need > ops and (need - ops - 256) % rec == 0 and 0 < (need - ops - 256) // rec <= 152
+    # one segment of 128 rows: far from a wave, no records
+    b = _flash(T=128, nseg=1, nh=1, nk=1, ld=192, q_off=0, k_off=64, v_off=128, ldo=64, max_len=128)
+    assert lib.swa_flash_workspace_size(ctypes.byref(b)) == (128 // 32) * 4 * 32 * 64 * 4

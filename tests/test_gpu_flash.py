@@ -75,6 +75,63 @@ def test_flash_split_once_is_bit_identical(kw):
     np.testing.assert_array_equal(a, b)
 
 
+def _split_tail(w, sms):
+    """The (tail, pieces) of the launch: with at least one full wave of one-CTA-per-SM
+    units (row block x segment x KV head) and a remainder of at most half a wave,
+    the last `tail` units of the launch run as sms // tail key ranges each."""
+    n_rb = -(-w.max_len // (128 // w.group))
+    units = n_rb * len(w.segs) * w.nk
+    tail = units % sms if units >= sms else 0
+    return (tail, sms // tail) if 0 < 2 * tail <= sms else (0, 1)
+
+
+def _tail_cells(w, sms, tail):
+    """(row, head) of every output the tail units write."""
+    rows = 128 // w.group
+    n_rb = -(-w.max_len // rows)
+    units = n_rb * len(w.segs) * w.nk
+    cells = []
+    for u in range(units - tail, units):
+        rb, bg = u % n_rb, u // n_rb
+        (s0, n), g = w.segs[bg // w.nk], bg % w.nk
+        for r in range(rb * rows, min(rb * rows + rows, n)):
+            cells += [(s0 + r, h) for h in range(g * w.group, (g + 1) * w.group)]
+    return cells
+
+
+@pytest.mark.parametrize("shape", ["one_head", "empty_pieces"])
+def test_flash_split_launch_tail_matches_oracle(shape):
+    """Two units past a whole wave: each is cut into sms // 2 key ranges whose
+    records the last piece combines. "one_head": one segment of (sms + 2) row blocks
+    of 128. "empty_pieces": 32 query heads per KV head (4 rows per CTA), so the tail
+    row blocks have 10 tiles for sms // 2 pieces and most pieces hold no key."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if shape == "one_head":
+        T = 128 * (sms + 2)
+        w = workloads.FlashWorkload("case", segs=((0, T),), T=T, nh=1, nk=1, hd=64, seed=8)
+    else:
+        n1 = 4 * (sms // 2 + 1)
+        w = workloads.FlashWorkload("case", segs=((0, 200), (200, n1)), T=200 + n1, nh=32, nk=1, hd=64, seed=9)
+    tail, q = _split_tail(w, sms)
+    assert tail == 2 and q == sms // 2
+    inp, got = _run(w, split_once=True)
+    _, plain = _run(w)                                  # no workspace: never split
+    cells = _tail_cells(w, sms, tail)
+    qkv = inp["qkv"].numpy()
+    seg_of = lambda r: next((s0, n) for s0, n in w.segs if s0 <= r < s0 + n)
+    ref = np.stack([oracle.flash_row(qkv, seg_of(r)[0], seg_of(r)[1], r - seg_of(r)[0], h, w.hd, w.group,
+                                     w.q_off, w.k_off, w.v_off, w.score_scale) for r, h in cells])
+    gpu = np.stack([got[r, h * w.hd:(h + 1) * w.hd] for r, h in cells])
+    assert_close(gpu, ref, "split tail out")
+    rows = np.concatenate([np.arange(s0, s0 + n) for s0, n in w.segs])
+    assert_close(got[rows], plain[rows], "split launch vs unsplit")
+    # every other output comes from a whole unit: bit-identical to the unsplit kernel
+    mask = np.ones(got.shape, dtype=bool)
+    for r, h in cells:
+        mask[r, h * w.hd:(h + 1) * w.hd] = False
+    np.testing.assert_array_equal(got[mask], plain[mask])
+
+
 def test_flash_skips_bad_and_empty_segments_and_reports_them():
     w = workloads.FlashWorkload("case", segs=((0, 50), (50, 0), (60, 40)), T=100, nh=4, nk=2, hd=64, seed=5)
     bad = torch.tensor([[0, 50], [50, 0], [60, 41]], dtype=torch.int32)   # the last reaches row 101
