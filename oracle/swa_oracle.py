@@ -27,8 +27,10 @@ Readings where the pages are silent (each is listed in the design doc):
 * the attend reads chunk rows from the chunk buffers and ring rows only for
   logical keys older than the chunk; the chunk is committed to the ring after
   every read (o1c_ring_commit runs after the attention);
-* the far field (far_len, landmarks) is outside the path: no far terms enter
-  the denominator; far_len is only advanced by the commit, as o1c_meta does;
+* without a far field (``attend``) no far terms enter the denominator and
+  far_len is only advanced by the commit, as o1c_meta does; the far field
+  below gives a row a far part only when far_len plus its own evictions is
+  positive;
 * softmax starts from -inf and has no denominator clamp (every row attends at
   least its own key, so the sum is >= 1).
 
