@@ -341,7 +341,8 @@ int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);
  *   ev_start, ev_stop  optional events recorded on `stream` right before and
  *            after the attention kernel (NULL: none).
  *   workspace, workspace_bytes  optional device scratch (256-byte aligned) of
- *            at least swa_flash_workspace_size(args) bytes. With it, a first
+ *            at least swa_flash_workspace_size(args) bytes, no initial contents
+ *            needed, not shared by calls that overlap on the GPU. With it, a first
  *            kernel splits each KV head's K and V rows into TF32 hi/lo operand
  *            blocks of 32 keys once per call (instead of once per block of
  *            query vectors) and the attention kernel copies them in whole
