@@ -252,3 +252,26 @@ def test_flash_workspace_holds_the_split_tail_records(lib):
     # one segment of 128 rows: far from a wave, no records
     b = _flash(T=128, nseg=1, nh=1, nk=1, ld=192, q_off=0, k_off=64, v_off=128, ldo=64, max_len=128)
     assert lib.swa_flash_workspace_size(ctypes.byref(b)) == (128 // 32) * 4 * 32 * 64 * 4
+
+
+def test_flash_split_tail_rule_over_shapes(lib):
+    # the library's rule: with U units (row blocks of 128 query vectors x segments x
+    # KV heads) and S SMs (148 when no GPU is visible), U >= S and 0 < U % S <= S / 2
+    # give U % S tail units of S // (U % S) pieces, each with a 128 x (hd + 2)-float
+    # record, plus a 256-byte counter block
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
+    up = lambda x: (x + 255) // 256 * 256
+    for nseg, nh, nk, hd, max_len in [(1, 1, 1, 64, 128 * 150), (1, 16, 16, 64, 9801), (3, 8, 2, 128, 1000),
+                                      (2, 32, 1, 64, 308), (1, 4, 4, 128, 128 * 37), (5, 2, 1, 64, 128 * 31)]:
+        rows = 128 // (nh // nk)
+        units = -(-max_len // rows) * nseg * nk
+        tail = units % sms if units >= sms else 0
+        extra = 0
+        if 0 < 2 * tail <= sms:
+            extra = up(tail * (sms // tail) * 128 * (hd + 2) * 4) + up(tail * 4 * 4)
+        ld = (nh + 2 * nk) * hd
+        a = _flash(T=max_len * nseg, nseg=nseg, nh=nh, nk=nk, hd=hd, ld=ld, q_off=0, k_off=nh * hd,
+                   v_off=(nh + nk) * hd, ldo=nh * hd, max_len=max_len)
+        ops = nseg * nk * -(-max_len // 32) * 4 * 32 * hd * 4
+        assert lib.swa_flash_workspace_size(ctypes.byref(a)) == ops + extra, (nseg, nh, nk, hd, max_len)
