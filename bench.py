@@ -16,8 +16,9 @@ the algorithmic KV-read bandwidth (each distinct K/V byte of a
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
        [--impl reference]
-Under torchrun every rank runs the full workload on its own GPU (sequence
-shards, no collective on the data path) and rank 0 prints the line.
+Under torchrun the batch has world x B sequences and every rank runs its shard
+of B sequences on its own GPU (no collective on the data path; weak scaling);
+rank 0 prints the line.
 """
 from __future__ import annotations
 
@@ -101,6 +102,20 @@ def dominant_kernel(w):
     return name, os.path.join(CSRC, src)
 
 
+# the HBM figure the method's bandwidth target is stated against (GB300 HBM3e, nominal)
+NOMINAL_HBM_GBS = 8000.0
+
+
+def rank_inputs(w, rank, world):
+    """The inputs rank `rank` of `world` works on: its shard (dist.shard_sequences)
+    of one batch of world x B sequences with the workload's shapes, each sequence
+    drawn from its own generator (workloads.make_shard_inputs), so the per-GPU
+    work is the workload's B sequences at every world size (weak scaling)."""
+    from sliding_window_gqa_prep_gb300.dist import shard_sequences
+    global_b = world * w.B
+    return workloads.make_shard_inputs(w, global_b, shard_sequences(global_b, rank, world))
+
+
 def peaks():
     """Roofline denominators: measured HBM copy GB/s and bf16 TFLOP/s (or the
     fallback), the FP32 CUDA-core peak derived from unit counts and the max SM
@@ -139,20 +154,97 @@ def recorded_traffic(w):
     return float(m.group(1))
 
 
+class _Nvml:
+    """The few read-only NVML queries the clock record needs, through ctypes on
+    the driver's libnvidia-ml (no Python package required)."""
+    SM = 0x1                                   # NVML_CLOCK_SM
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        ok = False
+        try:                                   # the same GPU as the CUDA device, by UUID
+            uuid = "GPU-" + str(torch.cuda.get_device_properties(cuda_index).uuid)
+            ok = self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.h)) == 0
+        except Exception:
+            ok = False
+        if not ok:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = int(vis.split(",")[cuda_index]) if vis else cuda_index
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(idx, ctypes.byref(self.h)) != 0:
+                raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    def sample(self):
+        c = self.c
+        sm, smax, mw, rs = c.c_uint(), c.c_uint(), c.c_uint(), c.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, self.SM, c.byref(sm)) != 0:
+            return None
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, self.SM, c.byref(smax))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, c.byref(mw))
+        self.reasons_fn(self.h, c.byref(rs))
+        return (float(sm.value), float(smax.value), mw.value / 1000.0,
+                [n for bit, n in self.REASONS.items() if rs.value & bit])
+
+
 class ClockSampler:
-    """nvidia-smi clock / throttle samples during the timed region."""
+    """SM clock, power and throttle reasons sampled during the timed regions.
+
+    A background thread polls NVML every 2 ms between start() and stop() (the
+    calls are read-only and release the interpreter lock), plus one sample at
+    each mark() taken right after a timed region's work is enqueued, when the
+    GPU is certainly busy; so even a region of a few milliseconds has samples.
+    Without NVML it falls back to ``nvidia-smi -lms 100``."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, local_rank):
+        import threading
+        self.local_rank = local_rank
         vis = os.environ.get("CUDA_VISIBLE_DEVICES")
         self.index = vis.split(",")[local_rank] if vis else str(local_rank)
+        self.rows = []
+        self.lock = threading.Lock()
+        self.stop_ev = threading.Event()
+        self.thread = None
         self.proc = None
         self.file = None
+        self.source = None
+        try:
+            self.nvml = _Nvml(local_rank)
+        except (OSError, AttributeError):
+            self.nvml = None
+
+    def _poll(self):
+        while not self.stop_ev.is_set():
+            self.mark()
+            self.stop_ev.wait(0.002)
+
+    def mark(self):
+        if self.nvml is None:
+            return
+        r = self.nvml.sample()
+        if r:
+            with self.lock:
+                self.rows.append(r)
 
     def start(self):
+        import threading
+        if self.nvml is not None:
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return
         try:
+            self.source = "nvidia-smi"
             self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -160,9 +252,7 @@ class ClockSampler:
         except (OSError, ValueError):
             self.proc = None
 
-    def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+    def _smi_rows(self):
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -170,27 +260,38 @@ class ClockSampler:
             self.proc.kill()
         self.file.flush()
         self.file.seek(0)
-        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        raw = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
         self.file.close()
         os.unlink(self.file.name)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []
+        for r in raw:
             if len(r) < 9:
                 continue
             try:
-                sm.append(float(r[1]))
-                smax.append(float(r[2]))
-                power.append(float(r[3]))
+                rows.append((float(r[1]), float(r[2]), float(r[3]),
+                             [n for n, v in zip(names, r[5:9]) if v.strip().lower() == "active"]))
             except ValueError:
                 continue
-            for name, val in zip(names[1:], r[5:9]):
-                if val.strip().lower() == "active":
-                    reasons.add(name)
+        return rows
+
+    def stop(self):
+        if self.thread is not None:
+            self.stop_ev.set()
+            self.thread.join(timeout=5)
+            rows = self.rows
+        elif self.proc is not None:
+            rows = self._smi_rows()
+        else:
+            return {"sm_mhz": None, "sm_max_mhz": None, "samples": 0,
+                    "reasons": [], "source": "unavailable (no NVML, no nvidia-smi)"}
+        sm = [r[0] for r in rows]
+        reasons = sorted({n for r in rows for n in r[3]})
         return {"sm_mhz": statistics.median(sm) if sm else None,
-                "sm_max_mhz": max(smax) if smax else None,
-                "power_w_max": max(power) if power else None,
-                "samples": len(sm), "reasons": sorted(reasons)}
+                "sm_min_mhz": min(sm) if sm else None,
+                "sm_max_mhz": max(r[1] for r in rows) if rows else None,
+                "power_w_max": max(r[2] for r in rows) if rows else None,
+                "samples": len(sm), "reasons": reasons, "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -226,7 +327,8 @@ def oracle_unit(w, a, i, g):
 
 
 def sample_inputs(w, nseq=4):
-    return workloads.make_inputs(w, batch=min(w.B, nseq))
+    """The first sequences of the batch the GPU arm runs at one GPU."""
+    return workloads.make_shard_inputs(w, w.B, range(min(w.B, nseq)))
 
 
 def _units_of(w, b, seed):
@@ -390,7 +492,9 @@ def workload_config(w, n):
     return {"workload": w.name, "B": w.B, "t": w.t, "nh": w.nh, "nk": w.nk, "hd": w.hd,
             "window": w.window, "cap": w.cap, "ns": w.ns, "seed": w.seed,
             "far_landmarks": w.far_m,
-            "parallelism": f"sequence shards x{n} (no collective)" if n > 1 else "1 GPU",
+            "global_batch": n * w.B,
+            "parallelism": f"sequence shards x{n} of a {n * w.B}-sequence batch (no collective)"
+            if n > 1 else "1 GPU",
             "l2": "inputs larger than L2: the K/V rings read each step exceed 129 MB"
             if not rings_fit_l2(w) else
             f"L2 flushed between timed steps (a {L2_FLUSH_BYTES >> 20} MB write outside the timed "
@@ -413,7 +517,7 @@ def run_gpu(args, w, rank, world, local_rank):
     from sliding_window_gqa_prep_gb300.dist import max_over_ranks
 
     dev = torch.device("cuda", local_rank)
-    inp = workloads.make_inputs(w, seed=w.seed + 1000 * rank)
+    inp = rank_inputs(w, rank, world)
     keys, kv_bytes = keys_and_bytes(w, inp["meta"])
     tp = swa.TokenPath(B=w.B, t=w.t, nh=w.nh, nk=w.nk, hd=w.hd, cap=w.cap, ns=w.ns,
                        q_scale=inp["q_scale"], gate_scale=inp["gate_scale"],
@@ -454,6 +558,8 @@ def run_gpu(args, w, rank, world, local_rank):
         for s in range(K):
             tp.step(d_in["yq"], d_in["yk"], d_in["yv"], d_in["gate"])
         e1.record()
+        if clocks:
+            clocks.mark()
         barrier()
         ms = e0.elapsed_time(e1)
     else:
@@ -464,6 +570,8 @@ def run_gpu(args, w, rank, world, local_rank):
             sev[2 * s].record()
             tp.step(d_in["yq"], d_in["yk"], d_in["yv"], d_in["gate"])
             sev[2 * s + 1].record()
+        if clocks:
+            clocks.mark()
         barrier()
         ms = sum(sev[2 * s].elapsed_time(sev[2 * s + 1]) for s in range(K))
     launches = swa.launch_count() - l0
@@ -476,6 +584,8 @@ def run_gpu(args, w, rank, world, local_rank):
         cold()
         tp.step(d_in["yq"], d_in["yk"], d_in["yv"], d_in["gate"], ev_start=kev[2 * s],
                 ev_stop=kev[2 * s + 1], prep_events=(pev[2 * s], pev[2 * s + 1]))
+    if clocks:
+        clocks.mark()
     barrier()
     clk = clocks.stop() if clocks else None
     kern_ms = [kev[2 * s].elapsed_time(kev[2 * s + 1]) for s in range(K)]
@@ -543,6 +653,10 @@ def run_gpu(args, w, rank, world, local_rank):
                 "peak": pk["tf32_tflops"], "unit": "TFLOP/s",
                 "peak_kind": f"{pk['kind']} bf16 x 1.1/2.25 (nominal TF32/bf16); achieved counts the 3 TF32 products of each multiply-add",
                 "useful_tflops": useful_flop / kern_avg_s / 1e12}
+    if path == "decode":
+        roof["frac_of_nominal_8tbs"] = roof["achieved"] / NOMINAL_HBM_GBS
+    elif path == "verify":
+        roof["kv_frac_of_nominal_8tbs"] = roof["kv_gbs"] / NOMINAL_HBM_GBS
     roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": kernel_name,
                  "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
                  "launch_ms_avg": kern_avg_s * 1e3})
@@ -557,6 +671,7 @@ def run_gpu(args, w, rank, world, local_rank):
         "config": workload_config(w, world),
         "kv_read_gbs_step": kv_bytes * world / step_s / 1e9,
         "kv_read_frac_of_peak_step": kv_bytes / step_s / 1e9 / peak,
+        "kv_read_frac_of_nominal_8tbs_step": kv_bytes / step_s / 1e9 / NOMINAL_HBM_GBS,
         "roofline": roof,
         "prep": prep_report(w, prep_ms, pk["hbm_gbs"]),
         "gpu_launches": launches,
@@ -718,6 +833,8 @@ def run_flash_gpu(args, w, rank, world, local_rank):
         sev[2 * s].record()
         swa.flash(qkv, segs, out=out, ev_start=kev[2 * s], ev_stop=kev[2 * s + 1], **kw)
         sev[2 * s + 1].record()
+    if clocks:
+        clocks.mark()
     barrier()
     launches = swa.launch_count() - l0
     clk = clocks.stop() if clocks else None

@@ -301,15 +301,19 @@ int swa_rollback(swa_meta* meta, const int32_t* n_back, int B, int cap, uint32_t
  *     The split-once operand blocks of the tensor-core prompt kernel are used
  *     when swa_attend_workspace_size fits the array too.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it with the
+ *     id of the device's context; make that first call before any stream
+ *     capture. A call that finds another context current (after
+ *     cudaDeviceReset, for instance) looks the address up again, so make the
+ *     first call after a reset outside any capture as well.
  *   - All calls share the one array, which keeps the last call's contents.
  *     Nothing in it needs to start at zero (every record is written before it
  *     is read within a call), but calls that overlap on the GPU (different
  *     streams, or different host threads, without ordering between them)
  *     race on it and corrupt each other's results: order them.
- * Errors: those of swa_attend, SWA_E_WORKSPACE for oversized calls, SWA_E_CUDA
- * if the address lookup fails.
+ * Errors: those of swa_attend, in the same order (NULL pointers, sizes,
+ * alignment), then SWA_E_WORKSPACE for oversized calls and SWA_E_CUDA if the
+ * address lookup fails.
  */
 #define SWA_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
 int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);

@@ -20,7 +20,7 @@ pages of the ``cortiq-engine`` crate on docs.rs):
 * "egemma2_msl.metal" (cortiq-engine 0.8.17): ``eg_qkv_prep`` (rotate-half
   pairing of a head and the [*, hd/2] cos/sin tables).
 
-Readings where the pages are silent (each is listed in the design doc):
+Readings where the pages are silent:
 * the RoPE table holds, per row, cos of the hd/2 angles then their sines,
   angle_e = pos * theta^(-2e/hd), pos = pos0 + row (the pages consume the
   table but do not build it);

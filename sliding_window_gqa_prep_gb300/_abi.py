@@ -112,6 +112,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                  ctypes.c_void_p, ctypes.c_void_p]
     lib.swa_attend.restype = ctypes.c_int
     lib.swa_attend.argtypes = [ctypes.POINTER(AttendArgs), ctypes.c_void_p]
+    lib.swa_attend_noalloc.restype = ctypes.c_int
+    lib.swa_attend_noalloc.argtypes = [ctypes.POINTER(AttendArgs), ctypes.c_void_p]
     lib.swa_flash.restype = ctypes.c_int
     lib.swa_flash.argtypes = [ctypes.POINTER(FlashArgs), ctypes.c_void_p]
     lib.swa_flash_workspace_size.restype = ctypes.c_size_t

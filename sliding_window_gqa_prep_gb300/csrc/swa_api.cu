@@ -172,6 +172,29 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   return true;
 }
 
+// Every check of swa_attend's arguments that does not depend on the workspace,
+// in the order swa_attend applies them: NULL pointers, sizes, alignment.
+int attend_args_status(const swa_attend_args* a) {
+  if (!a) return SWA_E_NULL;
+  if (!a->meta || !a->q || !a->k_chunk || !a->v_chunk || !a->ring_k || !a->ring_v || !a->gate ||
+      !a->gate_scale || !a->out)
+    return SWA_E_NULL;
+  if (a->ns > 0 && (!a->sink_k || !a->sink_v)) return SWA_E_NULL;
+  if (a->commit && !a->meta_out) return SWA_E_NULL;
+  if (a->far && (!a->far->k_tilde || !a->far->q_tilde || !a->far->mu || !a->far->mz || !a->far->t_hat))
+    return SWA_E_NULL;
+  if (!attend_shape_ok(a)) return SWA_E_SHAPE;
+  if (a->far && (!aligned16(a->far->k_tilde) || !aligned16(a->far->q_tilde) || !aligned16(a->far->t_hat) ||
+                 (reinterpret_cast<uintptr_t>(a->far->mu) & 3u) || (reinterpret_cast<uintptr_t>(a->far->mz) & 3u)))
+    return SWA_E_ALIGN;
+  if (!(a->scale == a->scale) || std::isinf(a->scale)) return SWA_E_SHAPE;
+  const void* ptrs[] = {a->q, a->k_chunk, a->v_chunk, a->ring_k, a->ring_v, a->sink_k,
+                        a->sink_v, a->gate, a->gate_scale, a->out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return SWA_E_ALIGN;
+  return SWA_OK;
+}
+
 }  // namespace swa
 
 using namespace swa;
@@ -261,23 +284,8 @@ size_t swa_attend_workspace_min(const swa_attend_args* a) {
 }
 
 int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
-  if (!a) return SWA_E_NULL;
-  if (!a->meta || !a->q || !a->k_chunk || !a->v_chunk || !a->ring_k || !a->ring_v || !a->gate ||
-      !a->gate_scale || !a->out)
-    return SWA_E_NULL;
-  if (a->ns > 0 && (!a->sink_k || !a->sink_v)) return SWA_E_NULL;
-  if (a->commit && !a->meta_out) return SWA_E_NULL;
-  if (a->far && (!a->far->k_tilde || !a->far->q_tilde || !a->far->mu || !a->far->mz || !a->far->t_hat))
-    return SWA_E_NULL;
-  if (!attend_shape_ok(a)) return SWA_E_SHAPE;
-  if (a->far && (!aligned16(a->far->k_tilde) || !aligned16(a->far->q_tilde) || !aligned16(a->far->t_hat) ||
-                 (reinterpret_cast<uintptr_t>(a->far->mu) & 3u) || (reinterpret_cast<uintptr_t>(a->far->mz) & 3u)))
-    return SWA_E_ALIGN;
-  if (!(a->scale == a->scale) || std::isinf(a->scale)) return SWA_E_SHAPE;
-  const void* ptrs[] = {a->q, a->k_chunk, a->v_chunk, a->ring_k, a->ring_v, a->sink_k,
-                        a->sink_v, a->gate, a->gate_scale, a->out};
-  for (const void* p : ptrs)
-    if (p && !aligned16(p)) return SWA_E_ALIGN;
+  const int rc0 = attend_args_status(a);
+  if (rc0 != SWA_OK) return rc0;
   AttendPlan plan;
   if (!make_plan(a, &plan)) return SWA_E_SHAPE;
   if (!a->workspace || a->workspace_bytes < plan.ws_min) return SWA_E_WORKSPACE;

@@ -40,6 +40,8 @@ struct AttendPlan {
   size_t off_order;  // byte offset of the tensor-core row-block order (with the operand blocks)
 };
 bool make_plan(const swa_attend_args* a, AttendPlan* p);
+// swa_attend's argument checks short of the workspace (SWA_OK or the first error)
+int attend_args_status(const swa_attend_args* a);
 
 // Kernel parameters of the attention (one struct, passed by value).
 struct AttendParams {

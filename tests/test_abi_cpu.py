@@ -110,6 +110,24 @@ def test_attend_rejects_bad_arguments(lib):
     assert call(_attend(workspace=FAKE + 16)) == _abi.SWA_E_ALIGN  # workspace wants 256 B
 
 
+def test_noalloc_reports_the_errors_of_swa_attend_in_its_order(lib):
+    """swa_attend_noalloc runs swa_attend's argument checks before its own size
+    check, so a call that is wrong in several ways gets the same status from both."""
+    noalloc = lambda a: lib.swa_attend_noalloc(ctypes.byref(a), None)
+    attend = lambda a: lib.swa_attend(ctypes.byref(a), None)
+    assert lib.swa_attend_noalloc(None, None) == _abi.SWA_E_NULL
+    for kw in (dict(q=None), dict(q=None, hd=100), dict(q=None, B=256, t=8, nh=128, nk=32, cap=4096),
+               dict(sink_k=None, hd=100), dict(commit=1, nh=9), dict(hd=100), dict(nh=9),
+               dict(scale=float("inf")), dict(out=FAKE + 8), dict(out=FAKE + 8, B=256, t=8, nh=128, nk=32, cap=4096)):
+        want = attend(_attend(**kw))
+        assert want != _abi.SWA_OK
+        assert noalloc(_attend(**kw)) == want, kw
+    # valid arguments whose scratch need exceeds the fixed array: refused before any CUDA call
+    big = _attend(B=256, t=8, nh=128, nk=32, hd=128, cap=4096, ns=4)
+    assert lib.swa_attend_workspace_min(ctypes.byref(big)) > (16 << 20)
+    assert noalloc(big) == _abi.SWA_E_WORKSPACE
+
+
 def test_workspace_size_rejects_bad_sizes(lib):
     assert lib.swa_attend_workspace_size(None) == 0
     a = _attend(hd=100)

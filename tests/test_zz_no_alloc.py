@@ -59,7 +59,30 @@ CASES = [
     # verify-shaped chunk with commit: a different plan and scratch layout
     dict(B=4, t=8, nh=16, nk=4, hd=64, window=300, cap=300, ns=2, pos_mode="partial",
          pos_lo=1, pos_hi=300, seed=32),
+    # prompt chunk on the tensor-core kernel whose split-once operand blocks fit
+    # the fixed scratch as well (swa_attend_workspace_size <= 16 MiB)
+    dict(B=2, t=128, nh=8, nk=2, hd=64, window=256, cap=256, ns=4, pos_mode="full",
+         pos_lo=256, pos_hi=2000, seed=33),
+    # prompt chunk whose operand blocks do not fit: only swa_attend_workspace_min
+    # does, and the kernel stages and splits K/V itself
+    dict(B=2, t=128, nh=32, nk=8, hd=128, window=2048, cap=2048, ns=4, pos_mode="full",
+         pos_lo=2048, pos_hi=6000, seed=34),
 ]
+
+
+def _fits(kw):
+    w = workloads.custom(**kw)
+    a = _abi.AttendArgs()
+    a.B, a.t, a.nh, a.nk, a.hd, a.cap, a.ns = w.B, w.t, w.nh, w.nk, w.hd, w.cap, w.ns
+    a.scale = w.score_scale
+    lib = swa.library()
+    return (lib.swa_attend_workspace_min(ctypes.byref(a)) <= (16 << 20),
+            lib.swa_attend_workspace_size(ctypes.byref(a)) <= (16 << 20))
+
+
+def test_noalloc_prompt_cases_cover_both_scratch_layouts():
+    assert _fits(CASES[2]) == (True, True)
+    assert _fits(CASES[3]) == (True, False)
 
 
 def test_noalloc_matches_swa_attend_on_two_calls_in_a_row():
@@ -99,6 +122,10 @@ def test_noalloc_refuses_sizes_beyond_its_scratch():
     a = _abi.AttendArgs()
     a.B, a.t, a.nh, a.nk, a.hd, a.cap, a.ns = 256, 8, 128, 32, 128, 4096, 4
     a.scale = 0.1
+    # aligned stand-ins that are never dereferenced: the call is refused first
+    for f in ("meta", "q", "k_chunk", "v_chunk", "ring_k", "ring_v", "sink_k", "sink_v", "gate",
+              "gate_scale", "out"):
+        setattr(a, f, 0x10000)
     need = swa.library().swa_attend_workspace_size(ctypes.byref(a))
     assert need > (16 << 20)
     n0 = swa.launch_count()

@@ -170,6 +170,85 @@ def make_inputs(w: Workload, seed: Optional[int] = None, batch: Optional[int] = 
     return out
 
 
+def _seq_pos0(w: Workload, b: int, g: torch.Generator) -> int:
+    """pos0 of global sequence b, by the rules of make_meta."""
+    W = w.window
+    if w.pos_mode == "fixed":
+        return w.pos_lo
+    if w.pos_mode == "full":
+        return int(torch.randint(w.pos_lo, w.pos_hi, (1,), generator=g)[0])
+    if w.pos_mode == "partial":
+        if b == 0:
+            return int(torch.randint(W, 4 * W, (1,), generator=g)[0])
+        return int(torch.randint(w.pos_lo, w.pos_hi + 1, (1,), generator=g)[0])
+    if w.pos_mode == "prompt":
+        return 0 if b == 0 else int(torch.randint(w.pos_lo, w.pos_hi + 1, (1,), generator=g)[0])
+    raise ValueError(w.pos_mode)
+
+
+def make_shard_inputs(w: Workload, global_B: int, seqs, seed: Optional[int] = None) -> dict:
+    """Inputs of sequences ``seqs`` of a batch of ``global_B`` sequences with the
+    shapes of ``w``, each sequence drawn from a generator of its own, so that a
+    sequence's inputs are the same whichever shard (rank) holds it.
+
+    The shared tensors q_scale, gate_scale come from ``Generator(seed)``;
+    sequence b draws, from ``Generator(seed * 1000003 + 1 + b)``, its pos0 (the
+    rules of make_meta, by global index), then yq, yk, yv, gate, ring_k, ring_v,
+    sink_k, sink_v with the distributions of make_inputs (and the far field
+    state when ``w.far_m``). Returns the layout of make_inputs for B = len(seqs).
+    """
+    seqs = list(seqs)
+    if any(b < 0 or b >= global_B for b in seqs):
+        raise ValueError("sequence index outside the batch")
+    base = w.seed if seed is None else seed
+    g0 = torch.Generator(device="cpu")
+    g0.manual_seed(base)
+    t, nh, nk, hd, W = w.t, w.nh, w.nk, w.hd, w.window
+    q_scale = torch.rand(nh, hd, generator=g0) + 0.5
+    gate_scale = torch.randn(nh, hd, generator=g0)
+    parts = {k: [] for k in ("yq", "yk", "yv", "gate", "ring_k", "ring_v", "sink_k", "sink_v")}
+    far_parts = {k: [] for k in ("mx", "z", "k_tilde", "q_tilde", "mu", "t_hat")}
+    pos = []
+    for b in seqs:
+        g = torch.Generator(device="cpu")
+        g.manual_seed(base * 1000003 + 1 + b)
+        pos.append(_seq_pos0(w, b, g))
+        parts["yq"].append(torch.randn(1, t, nh, hd, generator=g))
+        parts["yk"].append(torch.randn(1, t, nk, hd, generator=g))
+        parts["yv"].append(torch.randn(1, t, nk, hd, generator=g))
+        parts["gate"].append(torch.randn(1, t, nh, hd, generator=g))
+        parts["ring_k"].append(torch.randn(1, nk, w.cap, hd, generator=g))
+        parts["ring_v"].append(torch.randn(1, nk, w.cap, hd, generator=g))
+        parts["sink_k"].append(torch.randn(1, nk, w.ns, hd, generator=g))
+        parts["sink_v"].append(torch.randn(1, nk, w.ns, hd, generator=g))
+        if w.far_m:
+            m = w.far_m
+            far_parts["mx"].append(torch.randn(1, nh, m, generator=g))
+            far_parts["z"].append(torch.rand(1, nh, m, generator=g) * 49.0 + 1.0)
+            far_parts["k_tilde"].append(torch.randn(1, nk, m, hd, generator=g))
+            far_parts["q_tilde"].append(torch.randn(1, nh, m, hd, generator=g))
+            far_parts["mu"].append(torch.eye(m).expand(1, nh, m, m)
+                                   + 0.02 * torch.randn(1, nh, m, m, generator=g))
+            far_parts["t_hat"].append(torch.randn(1, nh, m, hd, generator=g))
+    pos0 = torch.tensor(pos, dtype=torch.int64)
+    win_len = torch.clamp(pos0, max=W)
+    meta = torch.stack([win_len, (pos0 - win_len) % W, pos0 - win_len, torch.full_like(pos0, W)], dim=1)
+    out = {"pos0": pos0, "meta": meta, "q_scale": q_scale, "gate_scale": gate_scale}
+    for k, v in parts.items():
+        out[k] = torch.cat(v, dim=0)
+    if w.far_m:
+        B = len(seqs)
+        f = {k: torch.cat(v, dim=0) for k, v in far_parts.items()}
+        empty = (meta[:, 2] == 0).view(B, 1, 1)
+        mx = torch.where(empty, torch.full_like(f["mx"], -math.inf), f["mx"])
+        z = torch.where(empty, torch.zeros_like(f["z"]), f["z"])
+        t_hat = torch.where(empty.unsqueeze(-1), torch.zeros_like(f["t_hat"]), f["t_hat"])
+        out["far"] = {"m": w.far_m, "rect": 0, "k_tilde": f["k_tilde"], "q_tilde": f["q_tilde"],
+                      "mu": f["mu"].contiguous(), "t_hat": t_hat,
+                      "mz": torch.cat([mx, z], dim=2).contiguous()}
+    return out
+
+
 def custom(name="custom", **kw) -> Workload:
     """A workload with arbitrary shapes (parity cases, edge cases)."""
     base = dict(B=1, t=1, nh=4, nk=1, hd=64, window=16, cap=16, ns=0, seed=0,
