@@ -57,6 +57,11 @@ __device__ __forceinline__ float2 unpack2(u64 v) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
   return r;
 }
+__device__ __forceinline__ u64 mul2(u64 a, u64 b) {
+  u64 d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
 __device__ __forceinline__ float comp(const float4& v, int i) {
   return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
 }
@@ -239,16 +244,17 @@ attend_verify_kernel(AttendParams p) {
   }
   // P V lane arrangement
   const int fg = lane % C::FG, qgl = lane / C::FG;
-  u64 acc[C::QPL][C::FPL / 2];
+  // O as pairs of query vectors: acc[k2][f] = (O[q][f], O[q + 1][f]) for the
+  // lane's query vectors q = qgl * QPL + 2 k2 and its features f
+  u64 acc[C::QPL / 2][C::FPL];
 #pragma unroll
-  for (int k = 0; k < C::QPL; ++k)
+  for (int k = 0; k < C::QPL / 2; ++k)
 #pragma unroll
-    for (int d = 0; d < C::FPL / 2; ++d) acc[k][d] = 0ull;
+    for (int d = 0; d < C::FPL; ++d) acc[k][d] = 0ull;
 
-  u64* Pw = reinterpret_cast<u64*>(smem + C::OFF_P) + warp * C::KW * C::QW;
-  u64* Cw = reinterpret_cast<u64*>(smem + C::OFF_C) + warp * C::QW;
+  float* Pw = smem + C::OFF_P + warp * C::KW * C::QW;     // [KW][QW] P of the warp's keys
+  float* Cw = smem + C::OFF_C + warp * C::QW;             // [QW] rescale factors
   const u64 one2 = pack2(1.f, 1.f);
-  const u64 zero2 = 0ull;
   const bool b1 = (e & 2) != 0, b0 = (e & 1) != 0;
   // Visit order of the warp's query chunks: after the chunk-level reduction
   // rounds (lane bits 2 and 1 when QW = 16, bit 2 when QW = 8) a lane keeps
@@ -394,19 +400,16 @@ attend_verify_kernel(AttendParams p) {
     }
 #pragma unroll
     for (int j = 0; j < C::KPL; ++j) {
-      u64* dst = Pw + (size_t)(kq + 4 * j) * C::QW + e * C::QO;
+      float* dst = Pw + (size_t)(kq + 4 * j) * C::QW + e * C::QO;
       if constexpr (C::QO == 2) {
-        ulonglong2 pv;
-        pv.x = pack2(sc[j][0], sc[j][0]);
-        pv.y = pack2(sc[j][1], sc[j][1]);
-        *reinterpret_cast<ulonglong2*>(dst) = pv;
+        *reinterpret_cast<float2*>(dst) = make_float2(sc[j][0], sc[j][1]);
       } else {
-        *dst = pack2(sc[j][0], sc[j][0]);
+        *dst = sc[j][0];
       }
     }
     if (kq == 0) {
 #pragma unroll
-      for (int o = 0; o < C::QO; ++o) Cw[e * C::QO + o] = pack2(cq[o], cq[o]);
+      for (int o = 0; o < C::QO; ++o) Cw[e * C::QO + o] = cq[o];
     }
     __syncwarp();
 
@@ -415,41 +418,41 @@ attend_verify_kernel(AttendParams p) {
 #pragma unroll
     for (int o = 0; o < C::QO; ++o) moved |= cq[o] != 1.f;
     if (__any_sync(kVFull, moved)) {                // some running max moved: rescale
-      u64 cc[C::QPL];
 #pragma unroll
       for (int k2 = 0; k2 < C::QPL / 2; ++k2) {
-        const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(Cw + qgl * C::QPL + 2 * k2);
-        cc[2 * k2] = a.x;
-        cc[2 * k2 + 1] = a.y;
+        const u64 cc = *reinterpret_cast<const u64*>(Cw + qgl * C::QPL + 2 * k2);
+#pragma unroll
+        for (int d = 0; d < C::FPL; ++d) acc[k2][d] = mul2(acc[k2][d], cc);
       }
-#pragma unroll
-      for (int k = 0; k < C::QPL; ++k)
-#pragma unroll
-        for (int d = 0; d < C::FPL / 2; ++d) acc[k][d] = ffma2(acc[k][d], cc[k], zero2);
     }
     const int nkv = min(C::KW, cnt - kbase);
 #pragma unroll 2
     for (int kk = 0; kk < nkv; ++kk) {
-      u64 pk[C::QPL];
+      // P of the lane's query vectors as natural pairs (q, q + 1); V once per feature
+      u64 pk[C::QPL / 2];
 #pragma unroll
-      for (int k2 = 0; k2 < C::QPL / 2; ++k2) {
+      for (int k4 = 0; k4 < C::QPL / 4; ++k4) {
         const ulonglong2 a =
-            *reinterpret_cast<const ulonglong2*>(Pw + (size_t)kk * C::QW + qgl * C::QPL + 2 * k2);
-        pk[2 * k2] = a.x;
-        pk[2 * k2 + 1] = a.y;
+            *reinterpret_cast<const ulonglong2*>(Pw + (size_t)kk * C::QW + qgl * C::QPL + 4 * k4);
+        pk[2 * k4] = a.x;
+        pk[2 * k4 + 1] = a.y;
       }
       const float* vr = Vt + (size_t)(kbase + kk) * HD;
-      u64 vv[C::FPL / 2];
+      float vf[C::FPL];
 #pragma unroll
       for (int u = 0; u < C::FCH; ++u) {
-        const ulonglong2 a = *reinterpret_cast<const ulonglong2*>(vr + (fg + C::FG * u) * 4);
-        vv[2 * u] = a.x;
-        vv[2 * u + 1] = a.y;
+        const float4 a = *reinterpret_cast<const float4*>(vr + (fg + C::FG * u) * 4);
+        vf[4 * u] = a.x;
+        vf[4 * u + 1] = a.y;
+        vf[4 * u + 2] = a.z;
+        vf[4 * u + 3] = a.w;
       }
 #pragma unroll
-      for (int k = 0; k < C::QPL; ++k)
+      for (int d = 0; d < C::FPL; ++d) {
+        const u64 vd = pack2(vf[d], vf[d]);
 #pragma unroll
-        for (int d = 0; d < C::FPL / 2; ++d) acc[k][d] = ffma2(pk[k], vv[d], acc[k][d]);
+        for (int k2 = 0; k2 < C::QPL / 2; ++k2) acc[k2][d] = ffma2(pk[k2], vd, acc[k2][d]);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
@@ -495,13 +498,17 @@ attend_verify_kernel(AttendParams p) {
   }
   float* red = smem;                           // [kVCW][QW][HD], reuses the stage buffers
 #pragma unroll
-  for (int k = 0; k < C::QPL; ++k) {
-    float* row = red + ((size_t)warp * C::QW + qgl * C::QPL + k) * HD;
+  for (int k2 = 0; k2 < C::QPL / 2; ++k2) {
+    float* row0 = red + ((size_t)warp * C::QW + qgl * C::QPL + 2 * k2) * HD;
+    float* row1 = row0 + HD;
 #pragma unroll
     for (int u = 0; u < C::FCH; ++u) {
-      const float2 a = unpack2(acc[k][2 * u]);
-      const float2 c2 = unpack2(acc[k][2 * u + 1]);
-      *reinterpret_cast<float4*>(row + (fg + C::FG * u) * 4) = make_float4(a.x, a.y, c2.x, c2.y);
+      const float2 a0 = unpack2(acc[k2][4 * u]);
+      const float2 a1 = unpack2(acc[k2][4 * u + 1]);
+      const float2 a2 = unpack2(acc[k2][4 * u + 2]);
+      const float2 a3 = unpack2(acc[k2][4 * u + 3]);
+      *reinterpret_cast<float4*>(row0 + (fg + C::FG * u) * 4) = make_float4(a0.x, a1.x, a2.x, a3.x);
+      *reinterpret_cast<float4*>(row1 + (fg + C::FG * u) * 4) = make_float4(a0.y, a1.y, a2.y, a3.y);
     }
   }
   named_barrier(1, kVCW * 32);
