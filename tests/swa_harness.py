@@ -120,3 +120,77 @@ def check_commit_placement(w, inp, res):
                 np.testing.assert_array_equal(res["ring_v"][b, :, slot], ring0_v[b, :, slot])
         expect = oracle.commit_meta(meta[b], w.t, w.cap)
         assert res["meta_out"][b].astype(np.int64).tolist() == expect.tolist(), (b, res["meta_out"][b], expect)
+
+
+def check_commit_placement_full(w, inp, res):
+    """check_commit_placement for large batches, vectorised: the expected ring
+    is the ring before the call with chunk row j of sequence b written to the
+    oracle's slot for (b, j), rows in order (a later row that lands on the
+    same slot wins); it must equal the GPU's ring bit for bit, as must the
+    meta after the commit."""
+    meta = inp["meta"].numpy()
+    exp_k = inp["ring_k"].numpy().copy()
+    exp_v = inp["ring_v"].numpy().copy()
+    for b in range(w.B):
+        for j in range(w.t):
+            slot = oracle.commit_slot(meta[b], j, w.cap)
+            exp_k[b, :, slot] = res["k"][b, j]
+            exp_v[b, :, slot] = res["v"][b, j]
+        expect = oracle.commit_meta(meta[b], w.t, w.cap)
+        assert res["meta_out"][b].astype(np.int64).tolist() == expect.tolist(), (b, res["meta_out"][b], expect)
+    np.testing.assert_array_equal(res["ring_k"], exp_k)
+    np.testing.assert_array_equal(res["ring_v"], exp_v)
+
+
+# ---------------------------------------------------------------------------
+# The oracle over many output vectors: a pool of single-threaded worker
+# processes (spawn start, safe after CUDA is initialised), each sent the slices
+# of the sequences it computes, calling oracle.attend_row /
+# oracle.attend_far_row as they are.
+# ---------------------------------------------------------------------------
+_PER_SEQ = ("meta", "q", "k_chunk", "v_chunk", "ring_k", "ring_v", "sink_k", "sink_v", "gate")
+_FAR_PER_SEQ = ("k_tilde", "q_tilde", "mu", "mz", "t_hat")
+
+
+def _oracle_task(job):
+    sub, far, rows, scale, hpg = job
+    if far is None:
+        return np.stack([oracle.attend_row(b, i, h, sub, scale, hpg) for b, i, h in rows])
+    return np.stack([oracle.attend_far_row(b, h, sub, far, scale, hpg, i) for b, i, h in rows])
+
+
+def oracle_rows(a, rows, scale, hpg, far=None, procs=None):
+    """oracle.attend_row (or attend_far_row with `far`) for every (b, i, h) in
+    `rows`, in that order, computed by a process pool; each task holds whole
+    sequences, re-indexed from 0."""
+    import os
+    import multiprocessing as mp
+    procs = procs or max(1, min(16, os.cpu_count() or 1))
+    seqs = sorted({b for b, _, _ in rows})
+    groups = [seqs[k::procs] for k in range(procs) if seqs[k::procs]]
+    jobs, where = [], []
+    for grp in groups:
+        idx = {b: n for n, b in enumerate(grp)}
+        sub = {k: (np.ascontiguousarray(v[grp]) if k in _PER_SEQ else v) for k, v in a.items()}
+        fsub = None
+        if far is not None:
+            fsub = {k: (np.ascontiguousarray(v[grp]) if k in _FAR_PER_SEQ else v) for k, v in far.items()}
+        mine = [(n, r) for n, r in enumerate(rows) if r[0] in idx]
+        jobs.append((sub, fsub, [(idx[b], i, h) for _, (b, i, h) in mine], scale, hpg))
+        where.append([n for n, _ in mine])
+    saved = {v: os.environ.get(v) for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for v in saved:
+        os.environ[v] = "1"
+    try:
+        with mp.get_context("spawn").Pool(len(jobs)) as pool:
+            parts = pool.map(_oracle_task, jobs, chunksize=1)
+    finally:
+        for v, old in saved.items():
+            if old is None:
+                os.environ.pop(v, None)
+            else:
+                os.environ[v] = old
+    out = np.empty((len(rows), parts[0].shape[1]), np.float64)
+    for part, pos in zip(parts, where):
+        out[pos] = part
+    return out
