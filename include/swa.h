@@ -253,6 +253,85 @@ size_t swa_attend_workspace_min(const swa_attend_args* args);
 
 int swa_attend(const swa_attend_args* args, cudaStream_t stream);
 
+/*
+ * swa_decode_step — one decode token (t = 1) of every sequence in one call:
+ * the prep of swa_prep (RoPE angles from pos0 and theta in the kernel, no
+ * table) followed by swa_attend with commit = 1 ("dory_msl.metal",
+ * cortiq-engine 0.8.57, dory_prep and dory_gate; "o1c_msl.metal",
+ * cortiq-engine 0.8.79, o1c_tok_near / o1c_tok_merge / o1c_tok_commit, the
+ * page's fused token path: for one token the number of dispatches, not the
+ * arithmetic, was the layer's cost).
+ *
+ * Results are those of swa_prep(rope = NULL, ring_k = ring_v = NULL) and then
+ * swa_attend(commit = 1) on the same tensors (bit for bit with the split count
+ * the form uses: one per (sequence, KV head) in the one-kernel form, the
+ * planner's otherwise; split counts change only the f32 rounding): out[b][h] for every
+ * query head; the row's k-hat / v row written to ring slot
+ * (win_head + win_len) % W (the evicted key's slot, or the next free one); the
+ * advanced meta in meta_out. The ring is read per the meta before the call.
+ *
+ * When a KV head has at most 8 query heads, meta_out does not alias meta, and
+ * either the library's split planner gives every (sequence, KV head) a single
+ * CTA or one CTA's keys (sinks + window) hold at most 512 KB of K and V (512
+ * keys at hd 128: the launch-bound regime), the whole step is ONE kernel:
+ * the CTA of (sequence, KV head) preps that KV head's query heads and its own
+ * k / v head, attends with its own row held in shared memory, writes the gated
+ * output and commits its row (the committed slot is never a key of the row's
+ * window). Otherwise the step runs the prep kernel, the attention and the merge,
+ * with q-hat and k-hat in the workspace. swa_decode_launches tells which.
+ *
+ *   yq [B][nh][hd], yk, yv [B][nk][hd], gate [B][nh][hd]    the row's inputs
+ *   q_scale, gate_scale [nh][hd]
+ *   pos0 [B] u32 device: the row's absolute position (angles)
+ *   meta [B] device, before the step; meta_out [B] device, after it
+ *   ring_k, ring_v [B][nk][cap][hd]; sink_k, sink_v [B][nk][ns][hd] (NULL if ns = 0)
+ *   out [B][nh][hd]
+ *   workspace   swa_decode_workspace_size(args) bytes, 256-byte aligned (may be
+ *               NULL when that is 0); no initial contents; not shared by
+ *               overlapping calls
+ *   err         optional device error word (SWA_DERR_META, SWA_DERR_TIMEOUT)
+ *   ev_start / ev_stop   optional, recorded around the attention kernel (the
+ *               whole step in the one-kernel form)
+ * Errors: SWA_E_NULL, SWA_E_SHAPE, SWA_E_ALIGN, SWA_E_WORKSPACE, SWA_E_CUDA
+ * (as swa_prep and swa_attend; eps < 0, theta <= 0 or a non-finite scale are
+ * SWA_E_SHAPE).
+ */
+typedef struct swa_decode_args {
+  int B, nh, nk, hd, cap, ns;
+  float scale;                   /* score scale (e.g. 1/sqrt(hd))           */
+  float eps;                     /* added to the sum of squares             */
+  double theta;                  /* RoPE base                               */
+  const float* yq;               /* [B][nh][hd]                             */
+  const float* yk;               /* [B][nk][hd]                             */
+  const float* yv;               /* [B][nk][hd]                             */
+  const float* q_scale;          /* [nh][hd]                                */
+  const uint32_t* pos0;          /* [B]                                     */
+  const swa_meta* meta;          /* [B], state before the step              */
+  float* ring_k;                 /* [B][nk][cap][hd], read and committed    */
+  float* ring_v;                 /* [B][nk][cap][hd], read and committed    */
+  const float* sink_k;           /* [B][nk][ns][hd]; NULL allowed if ns = 0 */
+  const float* sink_v;           /* [B][nk][ns][hd]; NULL allowed if ns = 0 */
+  const float* gate;             /* [B][nh][hd]                             */
+  const float* gate_scale;       /* [nh][hd]                                */
+  float* out;                    /* [B][nh][hd]                             */
+  swa_meta* meta_out;            /* [B], state after the step               */
+  void* workspace;               /* see swa_decode_workspace_size           */
+  size_t workspace_bytes;
+  uint32_t* err;                 /* optional device error word              */
+  cudaEvent_t ev_start;          /* optional                                */
+  cudaEvent_t ev_stop;           /* optional                                */
+} swa_decode_args;
+
+/* Workspace bytes swa_decode_step needs for these sizes: 0 in the one-kernel
+ * form, else room for q-hat, k-hat and swa_attend's workspace (reads B, nh,
+ * nk, hd, cap, ns and whether meta_out aliases meta; 0 also when the sizes are
+ * invalid). */
+size_t swa_decode_workspace_size(const swa_decode_args* args);
+/* Kernels one swa_decode_step call with these arguments launches: 1 (one
+ * kernel) or 3 (prep, attention, merge); 0 if the sizes are invalid. */
+int swa_decode_launches(const swa_decode_args* args);
+int swa_decode_step(const swa_decode_args* args, cudaStream_t stream);
+
 /* Speculative rollback of the ring meta ("dory_msl.metal", cortiq-engine
  * 0.8.57, kernel dory_o1_back). After a verify step committed t draft rows
  * (swa_attend with commit = 1) and only the first a were accepted, pass

@@ -11,6 +11,8 @@ Public calls (same names as the C ABI):
   attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v,
          gate, gate_scale, scale, ...)           -> out [B][t][nh][hd]
   attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits=0)
+  decode_step(yq, yk, yv, q_scale, pos0, meta, ring_k, ring_v, sink_k, sink_v,
+              gate, gate_scale, scale, ...)      -> out [B][nh][hd] (t = 1, one call)
   TokenPath: holds a batch's ring state and runs whole steps
 Meta tensors are int32 [B][4] = (win_len, win_head, far_len, window), read by
 the kernels as uint32; pos0 tensors are int32 [B].
@@ -25,7 +27,8 @@ import torch
 from . import _abi
 from ._abi import SwaError, SWA_DERR_META, SWA_DERR_TIMEOUT  # noqa: F401
 
-__all__ = ["rope_table", "prep", "attend", "attend_workspace_size", "rollback", "launch_count",
+__all__ = ["rope_table", "prep", "attend", "attend_workspace_size", "decode_step",
+           "decode_workspace_size", "decode_launches", "rollback", "launch_count",
            "TokenPath", "SwaError", "library"]
 
 
@@ -205,6 +208,76 @@ def attend(meta, q, k_chunk, v_chunk, ring_k, ring_v, sink_k, sink_v, gate, gate
     return out
 
 
+def _decode_struct(B, nh, nk, hd, cap, ns, meta=None, meta_out=None) -> _abi.DecodeArgs:
+    a = _abi.DecodeArgs()
+    a.B, a.nh, a.nk, a.hd, a.cap, a.ns = B, nh, nk, hd, cap, ns
+    if meta is not None:
+        a.meta = meta.data_ptr()
+    if meta_out is not None:
+        a.meta_out = meta_out.data_ptr()
+    return a
+
+
+def decode_workspace_size(B, nh, nk, hd, cap, ns, *, meta=None, meta_out=None) -> int:
+    """Workspace bytes of decode_step (0 when the step runs as one kernel; that
+    form needs meta_out distinct from meta, so pass both to decide)."""
+    a = _decode_struct(B, nh, nk, hd, cap, ns, meta, meta_out)
+    return int(library().swa_decode_workspace_size(ctypes.byref(a)))
+
+
+def decode_launches(B, nh, nk, hd, cap, ns, *, meta=None, meta_out=None) -> int:
+    """Kernels one decode_step call launches: 1 (one kernel) or 3."""
+    a = _decode_struct(B, nh, nk, hd, cap, ns, meta, meta_out)
+    n = int(library().swa_decode_launches(ctypes.byref(a)))
+    if n == 0:
+        raise SwaError(_abi.SWA_E_SHAPE, "swa_decode_launches")
+    return n
+
+
+def decode_step(yq, yk, yv, q_scale, pos0, meta, ring_k, ring_v, sink_k, sink_v, gate, gate_scale,
+                scale: float, *, eps: float = 1e-6, theta: float = 10000.0, out=None, meta_out=None,
+                workspace=None, err=None, ev_start=None, ev_stop=None, stream=None):
+    """One decode token of every sequence (t = 1): prep, attention, gate and
+    commit in one call (one kernel when the plan allows it); see include/swa.h.
+    yq [B][nh][hd], yk / yv [B][nk][hd], gate [B][nh][hd]; the ring gets the
+    row's k-hat / v and meta_out the advanced meta. Returns out [B][nh][hd]."""
+    B, nh, hd = yq.shape
+    nk = yk.shape[1]
+    cap = ring_k.shape[2]
+    ns = sink_k.shape[2] if sink_k is not None else 0
+    if out is None:
+        out = torch.empty_like(yq)
+    if meta_out is None:
+        raise ValueError("meta_out is required")
+    if workspace is None:
+        need = decode_workspace_size(B, nh, nk, hd, cap, ns, meta=meta, meta_out=meta_out)
+        workspace = torch.empty(max(need, 1), device=yq.device, dtype=torch.uint8)
+    a = _decode_struct(B, nh, nk, hd, cap, ns)
+    a.scale, a.eps, a.theta = float(scale), float(eps), float(theta)
+    a.yq = _ptr(yq, "yq", (B, nh, hd))
+    a.yk = _ptr(yk, "yk", (B, nk, hd))
+    a.yv = _ptr(yv, "yv", (B, nk, hd))
+    a.q_scale = _ptr(q_scale, "q_scale", (nh, hd))
+    a.pos0 = _ptr(pos0, "pos0", (B,), torch.int32)
+    a.meta = _ptr(meta, "meta", (B, 4), torch.int32)
+    a.ring_k = _ptr(ring_k, "ring_k", (B, nk, cap, hd))
+    a.ring_v = _ptr(ring_v, "ring_v", (B, nk, cap, hd))
+    a.sink_k = _ptr(sink_k, "sink_k", (B, nk, ns, hd)) if ns else 0
+    a.sink_v = _ptr(sink_v, "sink_v", (B, nk, ns, hd)) if ns else 0
+    a.gate = _ptr(gate, "gate", (B, nh, hd))
+    a.gate_scale = _ptr(gate_scale, "gate_scale", (nh, hd))
+    a.out = _ptr(out, "out", (B, nh, hd))
+    a.meta_out = _ptr(meta_out, "meta_out", (B, 4), torch.int32)
+    a.workspace = _ptr(workspace, "workspace", None, torch.uint8)
+    a.workspace_bytes = workspace.numel()
+    a.err = _ptr(err, "err", (1,), torch.int32, required=False)
+    a.ev_start = ctypes.c_void_p(ev_start.cuda_event) if ev_start is not None else None
+    a.ev_stop = ctypes.c_void_p(ev_stop.cuda_event) if ev_stop is not None else None
+    rc = library().swa_decode_step(ctypes.byref(a), _stream(stream))
+    _abi.check(rc, "swa_decode_step")
+    return out
+
+
 def rollback(meta: torch.Tensor, n_back: torch.Tensor, cap: int, err=None, stream=None):
     """Rewind each sequence's meta (in place) by n_back[b] rejected draft
     tokens, one token at a time as dory_o1_back does. Returns meta."""
@@ -301,10 +374,16 @@ class TokenPath:
             self.far = {"m": int(far["m"]), "rect": int(far.get("rect", 0))}
             for key in ("k_tilde", "q_tilde", "mu", "mz", "t_hat"):
                 self.far[key] = far[key].to(**f32).contiguous()
-        self.workspace = torch.empty(
-            attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits,
-                                  self.far["m"] if self.far else 0),
-            device=dev, dtype=torch.uint8)
+        # single rows without a far field and with automatic splits run as
+        # decode_step (one kernel when the plan gives each (sequence, KV head) a
+        # single CTA)
+        self.decode = t == 1 and far is None and num_splits == 0
+        need = attend_workspace_size(B, t, nh, nk, hd, cap, ns, num_splits,
+                                     self.far["m"] if self.far else 0)
+        if self.decode:
+            need = max(need, decode_workspace_size(B, nh, nk, hd, cap, ns, meta=self.meta,
+                                                   meta_out=self.meta_next))
+        self.workspace = torch.empty(need, device=dev, dtype=torch.uint8)
         self.err = torch.zeros(1, device=dev, dtype=torch.int32)
         self.in_bufs = {
             "yq": torch.empty(B, t, nh, hd, **f32), "yk": torch.empty(B, t, nk, hd, **f32),
@@ -327,6 +406,29 @@ class TokenPath:
             for name, x in (("yq", yq), ("yk", yk), ("yv", yv), ("gate", gate)):
                 self.in_bufs[name].copy_(x, non_blocking=True)
             yq, yk, yv, gate = (self.in_bufs[n] for n in ("yq", "yk", "yv", "gate"))
+        if self.decode and commit:
+            # one decode token: prep, attention, gate and commit in one call
+            cur = stream if stream is not None else torch.cuda.current_stream()
+            for ev in (v_ready, gate_ready):
+                if ev is not None:
+                    cur.wait_event(ev)
+            if prep_events is not None:
+                prep_events[0].record(stream)
+                prep_events[1].record(stream)
+            B, nh, nk, hd = self.B, self.nh, self.nk, self.hd
+            decode_step(yq.view(B, nh, hd), yk.view(B, nk, hd), yv.view(B, nk, hd), self.q_scale,
+                        self.pos0, self.meta, self.ring_k, self.ring_v, self.sink_k, self.sink_v,
+                        gate.view(B, nh, hd), self.gate_scale, self.scale, eps=self.eps,
+                        theta=self.theta, out=self.out.view(B, nh, hd), meta_out=self.meta_next,
+                        workspace=self.workspace, err=self.err, ev_start=ev_start, ev_stop=ev_stop,
+                        stream=stream)
+            if host:
+                if out_host is None:
+                    return self.out.to("cpu")
+                out_host.copy_(self.out, non_blocking=True)
+                cur.synchronize()
+                return out_host
+            return self.out
         # the prep writes the ring for single rows, except with a far field:
         # that step's eviction still reads the evicted slot, so the commit does
         ring = self.t == 1 and self.far is None

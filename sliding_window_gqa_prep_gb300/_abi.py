@@ -57,6 +57,20 @@ class AttendArgs(ctypes.Structure):
     ]
 
 
+class DecodeArgs(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int), ("nh", ctypes.c_int), ("nk", ctypes.c_int), ("hd", ctypes.c_int),
+        ("cap", ctypes.c_int), ("ns", ctypes.c_int),
+        ("scale", ctypes.c_float), ("eps", ctypes.c_float), ("theta", ctypes.c_double),
+        ("yq", c_float_p), ("yk", c_float_p), ("yv", c_float_p), ("q_scale", c_float_p),
+        ("pos0", c_float_p), ("meta", c_float_p),
+        ("ring_k", c_float_p), ("ring_v", c_float_p), ("sink_k", c_float_p), ("sink_v", c_float_p),
+        ("gate", c_float_p), ("gate_scale", c_float_p), ("out", c_float_p), ("meta_out", c_float_p),
+        ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+        ("err", c_float_p), ("ev_start", ctypes.c_void_p), ("ev_stop", ctypes.c_void_p),
+    ]
+
+
 class FlashArgs(ctypes.Structure):
     _fields_ = [
         ("T", ctypes.c_int), ("nseg", ctypes.c_int), ("hd", ctypes.c_int), ("nh", ctypes.c_int),
@@ -114,6 +128,12 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.swa_attend.argtypes = [ctypes.POINTER(AttendArgs), ctypes.c_void_p]
     lib.swa_attend_noalloc.restype = ctypes.c_int
     lib.swa_attend_noalloc.argtypes = [ctypes.POINTER(AttendArgs), ctypes.c_void_p]
+    lib.swa_decode_step.restype = ctypes.c_int
+    lib.swa_decode_step.argtypes = [ctypes.POINTER(DecodeArgs), ctypes.c_void_p]
+    lib.swa_decode_workspace_size.restype = ctypes.c_size_t
+    lib.swa_decode_workspace_size.argtypes = [ctypes.POINTER(DecodeArgs)]
+    lib.swa_decode_launches.restype = ctypes.c_int
+    lib.swa_decode_launches.argtypes = [ctypes.POINTER(DecodeArgs)]
     lib.swa_flash.restype = ctypes.c_int
     lib.swa_flash.argtypes = [ctypes.POINTER(FlashArgs), ctypes.c_void_p]
     lib.swa_flash_workspace_size.restype = ctypes.c_size_t

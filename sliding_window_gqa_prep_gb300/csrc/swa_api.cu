@@ -283,15 +283,9 @@ size_t swa_attend_workspace_min(const swa_attend_args* a) {
   return plan.ws_min;
 }
 
-int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
-  const int rc0 = attend_args_status(a);
-  if (rc0 != SWA_OK) return rc0;
-  AttendPlan plan;
-  if (!make_plan(a, &plan)) return SWA_E_SHAPE;
-  if (!a->workspace || a->workspace_bytes < plan.ws_min) return SWA_E_WORKSPACE;
-  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return SWA_E_ALIGN;
-
-  AttendParams p{};
+// Kernel parameters of an attention call with plan `plan` (workspace regions
+// only when the call has a workspace).
+static void fill_attend_params(const swa_attend_args* a, const AttendPlan& plan, AttendParams& p) {
   p.B = a->B; p.t = a->t; p.nh = a->nh; p.nk = a->nk; p.hd = a->hd; p.cap = a->cap;
   p.ns = a->ns; p.hpg = a->nh / a->nk;
   p.qmul = a->scale * 1.4426950408889634f;
@@ -301,10 +295,13 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   p.sink_k = a->sink_k; p.sink_v = a->sink_v;
   p.gate = a->gate; p.gate_scale = a->gate_scale; p.out = a->out;
   char* ws = static_cast<char*>(a->workspace);
-  p.ws_acc = reinterpret_cast<float*>(ws);
-  p.ws_ml = reinterpret_cast<float2*>(ws + plan.off_ml);
-  p.ws_nsplit = reinterpret_cast<int*>(ws + plan.off_nsplit);
-  p.ws_meta = reinterpret_cast<swa_meta*>(ws + plan.off_meta);
+  if (ws) {
+    p.ws_acc = reinterpret_cast<float*>(ws);
+    p.ws_ml = reinterpret_cast<float2*>(ws + plan.off_ml);
+    p.ws_nsplit = reinterpret_cast<int*>(ws + plan.off_nsplit);
+    p.ws_meta = reinterpret_cast<swa_meta*>(ws + plan.off_meta);
+    p.ws_far = reinterpret_cast<float*>(ws + plan.off_far);
+  }
   {
     // commit CTAs per sequence: about 4 float4 pairs per thread of 256
     const long long rows = a->t < a->cap ? a->t : a->cap;
@@ -326,13 +323,23 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   p.mu = a->far ? a->far->mu : nullptr;
   p.mz = a->far ? a->far->mz : nullptr;
   p.t_hat = a->far ? a->far->t_hat : nullptr;
-  p.ws_far = reinterpret_cast<float*>(ws + plan.off_far);
   // the split-once operand blocks when the workspace holds them
-  p.ops = (plan.ops_nblk > 0 && a->workspace_bytes >= plan.ws_bytes) ? reinterpret_cast<float*>(ws + plan.off_ops)
-                                                                      : nullptr;
+  p.ops = (ws && plan.ops_nblk > 0 && a->workspace_bytes >= plan.ws_bytes)
+              ? reinterpret_cast<float*>(ws + plan.off_ops) : nullptr;
   p.ops_nblk = plan.ops_nblk;
   p.ops_nsb = plan.ops_nsb;
   p.ws_order = p.ops ? reinterpret_cast<int*>(ws + plan.off_order) : nullptr;
+}
+
+int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
+  const int rc0 = attend_args_status(a);
+  if (rc0 != SWA_OK) return rc0;
+  AttendPlan plan;
+  if (!make_plan(a, &plan)) return SWA_E_SHAPE;
+  if (!a->workspace || a->workspace_bytes < plan.ws_min) return SWA_E_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(a->workspace) & 255u) != 0) return SWA_E_ALIGN;
+  AttendParams p{};
+  fill_attend_params(a, plan, p);
   int rc = SWA_OK;
   if (p.far) {            // before the attention: it reads the evicted ring slot, which the commit overwrites
     rc = launch_far(p, stream);
@@ -345,6 +352,111 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_status(e);
   }
   return launch_attend_merge(p, stream);
+}
+
+// ---------------------------------------------------------------------------
+// swa_decode_step: prep + attend + commit of one token, one kernel when the plan
+// runs each (sequence, KV head) as a single CTA
+// ---------------------------------------------------------------------------
+static void decode_as_attend(const swa_decode_args* a, swa_attend_args* t) {
+  std::memset(t, 0, sizeof(*t));
+  t->B = a->B; t->t = 1; t->nh = a->nh; t->nk = a->nk; t->hd = a->hd; t->cap = a->cap; t->ns = a->ns;
+  t->scale = a->scale;
+  t->meta = a->meta;
+  t->ring_k = a->ring_k; t->ring_v = a->ring_v;
+  t->sink_k = a->sink_k; t->sink_v = a->sink_v;
+  t->gate = a->gate; t->gate_scale = a->gate_scale;
+  t->out = a->out;
+  t->commit = 1;
+  t->meta_out = a->meta_out;
+  t->err = a->err;
+  t->ev_start = a->ev_start; t->ev_stop = a->ev_stop;
+}
+
+static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// K/V bytes of one (sequence, KV head) up to which a decode step runs as one
+// kernel even where the split planner would cut the window: below it the CTA
+// streams its window in a few microseconds, less than the two launches saved.
+constexpr size_t kStepOneCtaBytes = 512 * 1024;
+
+// 1: one kernel (the plan then has one split per (sequence, KV head)),
+// 3: prep + attention + merge, 0: invalid sizes.
+static int decode_form(const swa_decode_args* a, AttendPlan* plan) {
+  swa_attend_args t;
+  decode_as_attend(a, &t);
+  if (a->B < 1 || a->nh < 1 || a->nk < 1 || a->cap < 1 || a->ns < 0 || !hd_ok(a->hd)) return 0;
+  if (!make_plan(&t, plan)) return 0;
+  const bool aliased = a->meta_out != nullptr && (const void*)a->meta_out == (const void*)a->meta;
+  const bool short_window = (size_t)plan->keys_max * a->hd * 8 <= kStepOneCtaBytes;
+  if (plan->nq > 8 || aliased || (plan->splits != 1 && !short_window)) return 3;
+  plan->splits = 1;
+  plan->chunk = (plan->keys_max + TK - 1) / TK * TK;
+  return 1;
+}
+
+size_t swa_decode_workspace_size(const swa_decode_args* a) {
+  if (!a) return 0;
+  AttendPlan plan;
+  const int form = decode_form(a, &plan);
+  if (form != 3) return 0;
+  return up256((size_t)a->B * a->nh * a->hd * sizeof(float)) +
+         up256((size_t)a->B * a->nk * a->hd * sizeof(float)) + plan.ws_bytes;
+}
+
+int swa_decode_launches(const swa_decode_args* a) {
+  if (!a) return 0;
+  AttendPlan plan;
+  return decode_form(a, &plan);
+}
+
+int swa_decode_step(const swa_decode_args* a, cudaStream_t stream) {
+  if (!a) return SWA_E_NULL;
+  if (!a->yq || !a->yk || !a->yv || !a->q_scale || !a->pos0 || !a->meta || !a->ring_k || !a->ring_v ||
+      !a->gate || !a->gate_scale || !a->out || !a->meta_out)
+    return SWA_E_NULL;
+  if (a->ns > 0 && (!a->sink_k || !a->sink_v)) return SWA_E_NULL;
+  swa_attend_args t;
+  decode_as_attend(a, &t);
+  if (!attend_shape_ok(&t)) return SWA_E_SHAPE;
+  if (!(a->eps >= 0.0f) || !(a->theta > 0.0) || !(a->scale == a->scale) || std::isinf(a->scale))
+    return SWA_E_SHAPE;
+  const void* ptrs[] = {a->yq, a->yk, a->yv, a->q_scale, a->ring_k, a->ring_v, a->sink_k,
+                        a->sink_v, a->gate, a->gate_scale, a->out, a->meta, a->meta_out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return SWA_E_ALIGN;
+  AttendPlan plan;
+  const int form = decode_form(a, &plan);
+  if (form == 0) return SWA_E_SHAPE;
+  double inv_freq[128];
+  fill_inv_freq(a->theta, a->hd, inv_freq);
+  if (form == 1) {
+    AttendParams p{};
+    fill_attend_params(&t, plan, p);
+    return launch_decode_step(p, inv_freq, a->yq, a->yk, a->yv, a->q_scale, a->pos0, a->eps, stream,
+                              a->ev_start, a->ev_stop);
+  }
+  // prep (q-hat, k-hat into the workspace; v read in place) + attention + merge
+  const size_t qb = up256((size_t)a->B * a->nh * a->hd * sizeof(float));
+  const size_t kb = up256((size_t)a->B * a->nk * a->hd * sizeof(float));
+  if (!a->workspace || a->workspace_bytes < qb + kb + plan.ws_min) return SWA_E_WORKSPACE;
+  if (reinterpret_cast<uintptr_t>(a->workspace) & 255u) return SWA_E_ALIGN;
+  char* ws = static_cast<char*>(a->workspace);
+  swa_prep_args pa;
+  std::memset(&pa, 0, sizeof pa);
+  pa.B = a->B; pa.t = 1; pa.nh = a->nh; pa.nk = a->nk; pa.hd = a->hd; pa.cap = a->cap; pa.eps = a->eps;
+  pa.yq = a->yq; pa.yk = a->yk; pa.yv = a->yv; pa.rope = nullptr; pa.q_scale = a->q_scale;
+  pa.pos0 = a->pos0; pa.theta = a->theta;
+  pa.q_out = reinterpret_cast<float*>(ws);
+  pa.k_out = reinterpret_cast<float*>(ws + qb);
+  int rc = swa_prep(&pa, stream);
+  if (rc != SWA_OK) return rc;
+  t.q = pa.q_out;
+  t.k_chunk = pa.k_out;
+  t.v_chunk = a->yv;
+  t.workspace = ws + qb + kb;
+  t.workspace_bytes = a->workspace_bytes - qb - kb;
+  return swa_attend(&t, stream);
 }
 
 static bool flash_shape_ok(const swa_flash_args* a) {

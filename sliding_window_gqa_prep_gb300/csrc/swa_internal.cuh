@@ -103,6 +103,11 @@ int attend_partial_occupancy(int hd, int nq);   // resident CTAs per SM
 // decode kernel (nq <= 8 query vectors per CTA), swa_decode.cu
 int launch_attend_decode(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 int attend_decode_occupancy(int hd, int nq);
+// one-launch decode step (t = 1, one split per (sequence, KV head), nq <= 8): prep,
+// attention with the row's own key from shared memory, gate and commit, swa_decode.cu
+int launch_decode_step(const AttendParams& p, const double* inv_freq, const float* yq, const float* yk,
+                       const float* yv, const float* q_scale, const uint32_t* pos0, float eps, cudaStream_t s,
+                       cudaEvent_t e0, cudaEvent_t e1);
 // prompt-chunk kernel (64 query vectors per CTA, tensor cores), swa_prompt.cu
 int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // prompt-chunk kernel on tcgen05 / TMEM (128 query vectors per CTA), swa_prompt_tc.cu
@@ -255,6 +260,26 @@ __device__ __forceinline__ SeqState load_state(const AttendParams& p, int b, boo
   const SeqState st = sanitize_state(p.meta[b], p.cap, &bad);
   if (bad && report) set_err(p.err, SWA_DERR_META);
   return st;
+}
+
+// One head of the prep ("dory_msl.metal" dory_prep) as a warp sees it: lane l
+// holds the P = hd/64 pairs (e, e + hd/2) with e in [l*P, (l+1)*P). Rotates
+// (u = x c - y s, v = y c + x s) and returns 1 / sqrt(sum over the head of
+// u^2 + v^2 + eps), summed across the warp. Shared by the prep kernel and the
+// one-launch decode step so that both produce the same bits.
+template <int P>
+__device__ __forceinline__ float rotate_unit(const float (&x)[P], const float (&y)[P], const float (&c)[P],
+                                             const float (&s)[P], float eps, float (&u)[P], float (&v)[P]) {
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < P; ++i) {
+    u[i] = x[i] * c[i] - y[i] * s[i];
+    v[i] = y[i] * c[i] + x[i] * s[i];
+    ss += u[i] * u[i] + v[i] * v[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  return 1.0f / sqrtf(ss + eps);
 }
 
 #endif  // __CUDACC__

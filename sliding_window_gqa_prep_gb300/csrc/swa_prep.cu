@@ -80,16 +80,7 @@ __device__ __forceinline__ void prep_head(const PrepParams& p, int row, int a, i
   constexpr int HALF = HD / 2;
   const int e = lane * P;
   float u[P], v[P];
-  float ss = 0.f;
-#pragma unroll
-  for (int i = 0; i < P; ++i) {
-    u[i] = in.x[i] * c[i] - in.y[i] * s[i];
-    v[i] = in.y[i] * c[i] + in.x[i] * s[i];
-    ss += u[i] * u[i] + v[i] * v[i];
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = 1.0f / sqrtf(ss + p.eps);
+  const float inv = rotate_unit<P>(in.x, in.y, c, s, p.eps, u, v);
 
   if (a < p.nh) {
 #pragma unroll

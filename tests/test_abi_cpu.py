@@ -293,3 +293,33 @@ def test_flash_split_tail_rule_over_shapes(lib):
                    v_off=(nh + nk) * hd, ldo=nh * hd, max_len=max_len)
         ops = nseg * nk * -(-max_len // 32) * 4 * 32 * hd * 4
         assert lib.swa_flash_workspace_size(ctypes.byref(a)) == ops + extra, (nseg, nh, nk, hd, max_len)
+
+
+def _decode(**kw):
+    a = _abi.DecodeArgs()
+    a.B, a.nh, a.nk, a.hd, a.cap, a.ns = 2, 8, 2, 128, 64, 2
+    a.scale, a.eps, a.theta = 0.1, 1e-6, 1e4
+    for f in ("yq", "yk", "yv", "q_scale", "pos0", "meta", "ring_k", "ring_v", "sink_k", "sink_v",
+              "gate", "gate_scale", "out", "meta_out"):
+        setattr(a, f, FAKE)
+    for k, v in kw.items():
+        setattr(a, k, v)
+    return a
+
+
+def test_decode_step_rejects_bad_arguments(lib):
+    call = lambda a: lib.swa_decode_step(ctypes.byref(a), None)
+    assert lib.swa_decode_step(None, None) == _abi.SWA_E_NULL
+    for f in ("yq", "yk", "yv", "q_scale", "pos0", "meta", "ring_k", "gate", "out", "meta_out"):
+        assert call(_decode(**{f: None})) == _abi.SWA_E_NULL, f
+    assert call(_decode(sink_k=None)) == _abi.SWA_E_NULL           # ns > 0 needs sinks
+    assert call(_decode(hd=96)) == _abi.SWA_E_SHAPE
+    assert call(_decode(nh=9)) == _abi.SWA_E_SHAPE
+    assert call(_decode(nh=66)) == _abi.SWA_E_SHAPE                 # 33 query heads per KV head
+    assert call(_decode(eps=-1.0)) == _abi.SWA_E_SHAPE
+    assert call(_decode(theta=0.0)) == _abi.SWA_E_SHAPE
+    assert call(_decode(scale=float("inf"))) == _abi.SWA_E_SHAPE
+    assert call(_decode(out=FAKE + 8)) == _abi.SWA_E_ALIGN
+    assert lib.swa_decode_workspace_size(None) == 0
+    assert lib.swa_decode_launches(None) == 0
+    assert lib.swa_decode_launches(ctypes.byref(_decode(hd=96))) == 0
