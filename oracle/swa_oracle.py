@@ -467,7 +467,8 @@ def attend_far_row(b, h, inp, far, scale, hpg, i=0):
 
 def attend_far(inp, far, scale, hpg):
     """Every output of a chunk with the far field: out [B][t][nh][hd]. Far
-    chunks are at most min(W, 32) rows (every evicted key is a ring key)."""
+    chunks are at most min(W, 64) rows ("o1c_msl.metal" sizes its far scratch
+    for OB_K = 64 rows; within W rows every evicted key is a ring key)."""
     B, t, nh, hd = inp["q"].shape
     out = np.zeros((B, t, nh, hd), np.float64)
     for b in range(B):

@@ -583,6 +583,83 @@ def test_far_chunk_equals_sequential_decode_steps(len0):
     np.testing.assert_array_equal(st["ring_k"], rk_c)
 
 
+@pytest.mark.parametrize("t,len0", [(64, 80), (48, 40)])  # OB_K = 64 rows: full window; one that fills mid-chunk
+def test_far_chunk_of_up_to_64_rows_equals_sequential_decode_steps(t, len0):
+    """The chunk length the pages size their far scratch for ("o1c_msl.metal"
+    OB_K = 64, o1c_far_e / o1c_far): a 64- or 48-row chunk with the far field
+    equals as many single-row steps, each committing ring, meta and far state,
+    row by row, and leaves the same state."""
+    hd, nh, hpg, W, m = 8, 2, 2, 80, 3
+    g, inp, far, scale = _far_decode_case(23, W=W, hd=hd, nh=nh, m=m)
+    far["mu"] = np.abs(far["mu"]) + 0.1
+    inp["meta"] = np.array([[len0, 5, 9 if len0 == W else 0, W]])
+    if len0 < W:
+        far["mz"][0, :, :m] = -np.inf
+        far["mz"][0, :, m:] = 0.0
+    inp["q"] = g.normal(size=(1, t, nh, hd))
+    inp["k_chunk"], inp["v_chunk"] = g.normal(size=(1, t, 1, hd)), g.normal(size=(1, t, 1, hd))
+    inp["gate"] = g.normal(size=(1, t, nh, hd))
+    assert len(oracle.far_evictions(inp["meta"][0], t, W)) == t - (W - len0)
+    chunk = oracle.attend_far(inp, far, scale, hpg)
+    mz_c, th_c = oracle.far_commit(inp, far, scale, hpg)
+    rk_c, rv_c, meta_c = oracle.commit(inp["meta"], inp["ring_k"], inp["ring_v"], inp["k_chunk"], inp["v_chunk"])
+    st = dict(inp)
+    fs = dict(far)
+    for i in range(t):
+        step = dict(st, q=inp["q"][:, i:i + 1], k_chunk=inp["k_chunk"][:, i:i + 1],
+                    v_chunk=inp["v_chunk"][:, i:i + 1], gate=inp["gate"][:, i:i + 1])
+        np.testing.assert_allclose(oracle.attend_far(step, fs, scale, hpg)[:, 0], chunk[:, i], rtol=1e-10)
+        fs["mz"], fs["t_hat"] = oracle.far_commit(step, fs, scale, hpg)
+        st["ring_k"], st["ring_v"], st["meta"] = oracle.commit(step["meta"], step["ring_k"], step["ring_v"],
+                                                               step["k_chunk"], step["v_chunk"])
+    np.testing.assert_allclose(fs["mz"], mz_c, rtol=1e-12)
+    np.testing.assert_allclose(fs["t_hat"], th_c, rtol=1e-12)
+    np.testing.assert_array_equal(st["meta"], meta_c)
+    np.testing.assert_array_equal(st["ring_k"], rk_c)
+
+
+def test_far_chunk_of_64_rows_is_exact_with_landmarks_at_its_evictions():
+    """Nystrom exactness over a whole 64-row chunk: a ring of 46 keys in a
+    window of 80 fills at row 34, so rows 34..63 evict the 30 oldest keys. With
+    those keys as the 30 landmarks and mu = [exp(s <q~_b, k_j>)]^-1, every row
+    equals full softmax attention over the sinks, every ring key and the
+    chunk's rows up to itself: the far field returns exactly what the window
+    dropped."""
+    hd, nh, hpg, W, t, len0, head0, m = 32, 2, 2, 80, 64, 46, 10, 30
+    g = np.random.default_rng(29)
+    ns = 2
+    ring_k, ring_v = g.normal(size=(1, 1, W, hd)), g.normal(size=(1, 1, W, hd))
+    inp = {"meta": np.array([[len0, head0, 0, W]], dtype=np.int64), "ring_k": ring_k, "ring_v": ring_v,
+           "sink_k": g.normal(size=(1, 1, ns, hd)), "sink_v": g.normal(size=(1, 1, ns, hd)),
+           "gate_scale": g.normal(size=(nh, hd)), "q": g.normal(size=(1, t, nh, hd)),
+           "k_chunk": g.normal(size=(1, t, 1, hd)), "v_chunk": g.normal(size=(1, t, 1, hd)),
+           "gate": g.normal(size=(1, t, nh, hd))}
+    scale = hd ** -0.5
+    ev = oracle.far_evictions(inp["meta"][0], t, W)
+    assert [j for j, _ in ev] == list(range(34, 64))
+    assert [slot for _, slot in ev] == [(head0 + x) % W for x in range(m)]
+    kt = np.stack([ring_k[0, 0, slot] for _, slot in ev])[None, None]
+    qt = 2.5 * g.normal(size=(1, nh, m, hd))
+    mu = np.zeros((1, nh, m, m))
+    for h in range(nh):
+        Bm = np.exp(scale * qt[0, h] @ kt[0, 0].T)
+        assert np.linalg.cond(Bm) < 1e8
+        mu[0, h] = np.linalg.inv(Bm)
+    far = {"m": m, "rect": 0, "k_tilde": kt, "q_tilde": qt, "mu": mu,
+           "mz": np.concatenate([np.full((1, nh, m), -np.inf), np.zeros((1, nh, m))], axis=2),
+           "t_hat": np.zeros((1, nh, m, hd))}
+    got = oracle.attend_far(inp, far, scale, hpg)
+    ring_keys = [(head0 + x) % W for x in range(len0)]
+    for i in range(t):
+        K = np.concatenate([inp["sink_k"][0, 0], ring_k[0, 0, ring_keys], inp["k_chunk"][0, :i + 1, 0]])
+        V = np.concatenate([inp["sink_v"][0, 0], ring_v[0, 0, ring_keys], inp["v_chunk"][0, :i + 1, 0]])
+        for h in range(nh):
+            sc = scale * (K @ inp["q"][0, i, h])
+            p = np.exp(sc - sc.max())
+            ref = (p @ V) / p.sum() * oracle.sigmoid_gate(inp["gate"][0, i, h], inp["gate_scale"][h])
+            np.testing.assert_allclose(got[0, i, h], ref, rtol=1e-7, atol=1e-9)
+
+
 # ---------------------------------------------------------------------------
 # full-sequence attention (egemma2_msl.metal eg_flash64 / eg_flash_staged)
 # ---------------------------------------------------------------------------
