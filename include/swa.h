@@ -200,7 +200,8 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  *                           empty), then mass; rewritten iff commit = 1
  *   t_hat   [B][nh][m][hd]  per landmark numerator (16-byte aligned);
  *                           rewritten iff commit = 1
- * 1 <= m <= 32. A chunk with a far field has t <= 32 and t <= cap rows;
+ * 1 <= m <= 32. A chunk with a far field has t <= 64 rows (the pages size
+ * their far scratch for OB_K = 64) and t <= cap;
  * once the window is full, row j evicts the oldest key still held, and row i
  * sees the evictions of rows 0..i (o1c_far_e / o1c_far). The evicted keys
  * must still be in the ring: do not let swa_prep write the ring in such a
@@ -240,7 +241,7 @@ typedef struct swa_attend_args {
   uint32_t* err;                 /* optional device error word              */
   cudaEvent_t ev_start;          /* optional                                */
   cudaEvent_t ev_stop;           /* optional                                */
-  const swa_far_args* far;       /* optional far field (t <= 32), host struct */
+  const swa_far_args* far;       /* optional far field (t <= 64), host struct */
   cudaEvent_t gate_ready;        /* optional: the merge waits for it        */
 } swa_attend_args;
 

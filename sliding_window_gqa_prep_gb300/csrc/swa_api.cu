@@ -44,7 +44,7 @@ static int attend_shape_ok(const swa_attend_args* a) {
   if (a->nh % a->nk != 0) return 0;
   if (a->nh / a->nk > 32) return 0;
   if (a->num_splits < 0) return 0;
-  if (a->far && (a->t > 32 || a->t > a->cap || a->far->m < 1 || a->far->m > 32)) return 0;
+  if (a->far && (a->t > 64 || a->t > a->cap || a->far->m < 1 || a->far->m > 32)) return 0;
   // output rows are indexed in 32 bits (q alone would exceed device memory first)
   if ((long long)a->B * a->t * a->nh >= (1LL << 31)) return 0;
   // grid y / z extents: (sequence, KV head) pairs (one more row in the split-once pass)

@@ -3,7 +3,8 @@
 // of o1c_tok_commit; "dory_msl.metal", cortiq-engine 0.8.57: the clip of
 // dory_ofar).
 //
-// One CTA per (sequence, query head) and one warp per chunk row; lane a is
+// One CTA per (sequence, query head), one warp per chunk row (chunks of up to
+// 64 rows, the pages' OB_K: 32 warps, two rows each past 32); lane a is
 // landmark a (m <= 32) in the scalar steps and lanes run over features in the
 // numerators:
 //  1. the head's landmark numerators go to shared memory once; once the window
@@ -29,6 +30,7 @@ namespace swa {
 namespace {
 
 constexpr unsigned kFFull = 0xffffffffu;
+constexpr int kFarRows = 64;                            // longest chunk with a far field (OB_K)
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -50,8 +52,8 @@ __global__ void __launch_bounds__(MAXW * 32) far_kernel(AttendParams p) {
   extern __shared__ __align__(16) float far_smem[];
   const int m = p.far_m, t = p.t;
   float* th_s = far_smem;                               // [m][HD]  landmark numerators before the chunk
-  float* fe_s = th_s + (size_t)m * HD;                  // [32][32] eviction scores, e_j after step 2
-  float* rr_s = fe_s + 32 * 32;                         // [32]     rescale of each landmark
+  float* fe_s = th_s + (size_t)m * HD;                  // [64][32] eviction scores, e_j after step 2
+  float* rr_s = fe_s + kFarRows * 32;                   // [32]     rescale of each landmark
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
   const int b = blockIdx.x / p.nh, h = blockIdx.x % p.nh, g = h / p.hpg;
   const bool live = lane < m;
@@ -252,7 +254,7 @@ int run_far_w(const AttendParams& p, dim3 grid, dim3 block, size_t smem, cudaStr
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64 || !attr_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(far_kernel<HD, MAXW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)((32 * HD + 32 * 32 + 32) * sizeof(float)));
+                                               (int)((32 * HD + kFarRows * 32 + 32) * sizeof(float)));
     if (e != cudaSuccess) return cuda_status(e);
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
@@ -261,6 +263,7 @@ int run_far_w(const AttendParams& p, dim3 grid, dim3 block, size_t smem, cudaStr
 }
 
 // blocks of up to 8 warps get the full register budget; longer chunks up to 32
+// warps (a warp takes rows warp and warp + 32 of a chunk longer than 32)
 template <int HD>
 int run_far(const AttendParams& p, dim3 grid, dim3 block, size_t smem, cudaStream_t s) {
   return p.t <= 8 ? run_far_w<HD, 8>(p, grid, block, smem, s) : run_far_w<HD, 32>(p, grid, block, smem, s);
@@ -270,8 +273,8 @@ int run_far(const AttendParams& p, dim3 grid, dim3 block, size_t smem, cudaStrea
 
 int launch_far(const AttendParams& p, cudaStream_t s) {
   const dim3 grid((unsigned)(p.B * p.nh));               // a CTA per (sequence, query head)
-  const dim3 block((unsigned)(32 * p.t));                // a warp per chunk row (t <= 32)
-  const size_t smem = ((size_t)p.far_m * p.hd + 32 * 32 + 32) * sizeof(float);
+  const dim3 block((unsigned)(32 * (p.t < 32 ? p.t : 32)));   // a warp per chunk row, at most 32
+  const size_t smem = ((size_t)p.far_m * p.hd + kFarRows * 32 + 32) * sizeof(float);
   // An ordinary launch (after the prep in full stream order): launched
   // programmatically, its CTAs were resident early and the step was slower
   // (237.5 vs 210 us on batched_decode_far). It still triggers its dependents,

@@ -471,11 +471,14 @@ def test_far_decode_step_matches_oracle(rect, splits):
 
 
 @pytest.mark.parametrize("t,hd,nh,nk,W", [(4, 128, 8, 2, 96), (8, 128, 16, 4, 96), (8, 256, 8, 2, 40),
-                                          (32, 64, 8, 2, 64)])
+                                          (32, 64, 8, 2, 64), (48, 128, 8, 2, 96), (64, 128, 16, 4, 80),
+                                          (48, 256, 8, 2, 64), (64, 256, 4, 2, 70)])
 def test_far_chunk_matches_oracle(t, hd, nh, nk, W):
-    """Chunks with the far field (row i sees the evictions of rows 0..i):
-    verify-sized blocks on the CUDA-core kernel, a 32-row chunk of 4 heads per
-    KV head on the tcgen05 kernel; one sequence starts evicting mid-chunk."""
+    """Chunks with the far field (row i sees the evictions of rows 0..i), up to
+    the pages' 64 rows (OB_K): verify-sized blocks on the CUDA-core kernel,
+    chunks of 4 heads per KV head on the tcgen05 kernel, hd 256 chunks of 48 and
+    64 rows on the CUDA-core kernel (two far rows per warp past 32); one
+    sequence starts evicting mid-chunk."""
     w, inp = _far_case(53 + t, t=t, hd=hd, nh=nh, nk=nk, window=W, cap=W, pos_lo=max(1, W // 2), pos_hi=W)
     inp["meta"][2, 0] = W - 2                           # fills after two rows of the chunk
     inp["meta"][2, 1] = 0
