@@ -177,7 +177,10 @@ def test_attend_rejects_bad_far_field_arguments(lib):
         f = _far(**{missing: None})
         assert call(_attend(far=ctypes.pointer(f))) == _abi.SWA_E_NULL, missing
     f = _far()
-    assert call(_attend(t=33, far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE    # at most 32 rows
+    # at most 64 rows (the pages' OB_K), even with room in the ring
+    assert call(_attend(t=65, cap=128, far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE
+    assert lib.swa_attend_workspace_size(ctypes.byref(_attend(t=65, cap=128, far=ctypes.pointer(f)))) == 0
+    assert lib.swa_attend_workspace_size(ctypes.byref(_attend(t=64, cap=128, far=ctypes.pointer(f)))) > 0
     assert call(_attend(t=8, cap=6, far=ctypes.pointer(f))) == _abi.SWA_E_SHAPE   # t <= cap
     for m in (0, 33):
         f = _far(m=m)
