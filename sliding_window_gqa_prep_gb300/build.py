@@ -21,7 +21,7 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libswa_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["swa_api.cu", "swa_prep.cu", "swa_attend.cu", "swa_decode.cu", "swa_prompt.cu", "swa_prompt_tc.cu", "swa_verify.cu", "swa_noalloc.cu", "swa_rollback.cu", "swa_far.cu"]
+SOURCES = ["swa_api.cu", "swa_prep.cu", "swa_attend.cu", "swa_decode.cu", "swa_prompt.cu", "swa_prompt_tc.cu", "swa_prompt_h16.cu", "swa_verify.cu", "swa_noalloc.cu", "swa_rollback.cu", "swa_far.cu"]
 
 
 def _nvcc() -> str:

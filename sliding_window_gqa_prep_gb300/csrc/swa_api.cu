@@ -82,6 +82,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   if (!attend_shape_ok(a)) return false;
   p->off_ops = 0;
   p->off_order = 0;
+  p->off_exp = 0;
   p->ops_nblk = 0;
   p->ops_nsb = 0;
   const int hpg = a->nh / a->nk;
@@ -117,8 +118,11 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
       p->ops_nsb = (a->ns + kOpsBlockKeys - 1) / kOpsBlockKeys;
       const long long nlog = ((long long)a->cap + a->t + kOpsBlockKeys - 1) / kOpsBlockKeys;
       p->ops_nblk = (int)(p->ops_nsb + nlog);
+      // (f16 K hi, K lo, V^T hi, V^T lo of 32 keys each) and their exponents (e_k, e_v)
       p->off_ops = p->ws_bytes;
-      p->ws_bytes += up((size_t)a->B * a->nk * p->ops_nblk * 4 * kOpsBlockKeys * a->hd * sizeof(float));
+      p->ws_bytes += up((size_t)a->B * a->nk * p->ops_nblk * 4 * kOpsBlockKeys * a->hd * 2);
+      p->off_exp = p->ws_bytes;
+      p->ws_bytes += up((size_t)a->B * a->nk * p->ops_nblk * 2 * sizeof(int));
       // the order in which the kernel's CTAs take the row blocks (longest first)
       p->off_order = p->ws_bytes;
       p->ws_bytes += up(p->items * sizeof(int));
@@ -329,6 +333,7 @@ static void fill_attend_params(const swa_attend_args* a, const AttendPlan& plan,
   p.ops_nblk = plan.ops_nblk;
   p.ops_nsb = plan.ops_nsb;
   p.ws_order = p.ops ? reinterpret_cast<int*>(ws + plan.off_order) : nullptr;
+  p.ops_exp = p.ops ? reinterpret_cast<int*>(ws + plan.off_exp) : nullptr;
 }
 
 int swa_attend(const swa_attend_args* a, cudaStream_t stream) {

@@ -365,7 +365,7 @@ int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0,
   if (p.nq <= 8) return launch_attend_decode(p, s, e0, e1);
   if (p.nq == 16 || p.nq == 32) return launch_attend_verify(p, s, e0, e1);
   if (p.nq == 64) return launch_attend_prompt(p, s, e0, e1);
-  if (p.nq == 128) return launch_attend_prompt_tc(p, s, e0, e1);
+  if (p.nq == 128) return p.ops ? launch_attend_prompt_h16(p, s, e0, e1) : launch_attend_prompt_tc(p, s, e0, e1);
   return SWA_E_SHAPE;
 }
 

@@ -38,6 +38,7 @@ struct AttendPlan {
   int ops_nblk;      // their blocks per (sequence, KV head), 0 if the plan has none
   int ops_nsb;       // sink blocks among them
   size_t off_order;  // byte offset of the tensor-core row-block order (with the operand blocks)
+  size_t off_exp;    // byte offset of the operand blocks' exponents (with the operand blocks)
 };
 bool make_plan(const swa_attend_args* a, AttendPlan* p);
 // swa_attend's argument checks short of the workspace (SWA_OK or the first error)
@@ -92,6 +93,8 @@ struct AttendParams {
   int* ws_cnt;                // [tail][4] pieces done per unit and softmax warp
   int* ws_order;              // with ops on the token path: [B * nk * n_rb] row blocks (index
                               // (b * nk + g) * n_rb + rb), longest first
+  int* ops_exp;               // token path: [B][nk][ops_nblk] x (e_k, e_v), the power-of-two
+                              // exponents of the f16 operand blocks (ops then holds f16 blocks)
 };
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
@@ -112,6 +115,9 @@ int launch_decode_step(const AttendParams& p, const double* inv_freq, const floa
 int launch_attend_prompt(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // prompt-chunk kernel on tcgen05 / TMEM (128 query vectors per CTA), swa_prompt_tc.cu
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+// prompt-chunk kernel of the token path with split-once f16 operand blocks (a workspace
+// of plan.ws_bytes): persistent, tcgen05 kind::f16, swa_prompt_h16.cu
+int launch_attend_prompt_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 // the same kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu;
 // with p.ops set it first splits every KV head's K/V rows into operand blocks once
 // (the same holds for launch_attend_prompt_tc on the token path)

@@ -1,0 +1,707 @@
+// Prompt-chunk attention of the token path on the 5th-generation tensor cores
+// (tcgen05, TMEM) with f16 hi/lo operands: the GEMM path of "o1c_msl.metal"
+// (cortiq-engine 0.8.79: o1c_gather, o1c_cols, o1c_gmax, o1c_gsoft, o1c_gadd and
+// the engine GEMMs Q K^T and P V they feed) as one persistent kernel.
+//
+// Precision. Every operand block is scaled by a power of two 2^-e so that its
+// largest magnitude lies in [2^14, 2^15), then split x = hi + lo with hi = x
+// rounded to f16 and lo = (x - hi) rounded to f16 (x - hi is exact in f32). Each
+// product is hi*hi' + hi*lo' + lo*hi' accumulated in f32 (three tcgen05.mma
+// kind::f16): 11 + 11 significand bits per operand, the same as a TF32 hi/lo
+// split, at twice the TF32 rate and half its bytes. The scales are undone
+// exactly: a score tile is multiplied by 2^(e_q + e_k) (e_q per query vector,
+// e_k per K block); P is written as p * 2^(e_v - E + 4), where e_v is the V
+// block's exponent and E a running V exponent that is raised (with O rescaled)
+// only when a block exceeds it by more than 3, so P < 2^15 and O accumulates in
+// units of 2^(E - 4). A block of zeros has e_v = -127 (its P underflows to 0).
+//
+// Work: one unit = 128 query vectors (rows x heads of one KV head) of a row
+// block against its tiles of 32 keys (sink blocks, then the logical blocks that
+// hold its window). The grid has one CTA per SM; CTA c takes the units of ranks
+// c, 2P - 1 - c, 2P + c, ... of the longest-first order (P = grid size), so the
+// SMs finish close together, and tensor memory, barriers and the pipelines stay
+// up from one unit to the next.
+//
+// CTA = 7 warps:
+//   warps 0-3  one thread per query vector = per TMEM lane: Q of each unit into
+//              TMEM, softmax of its score row, P (f16 hi | lo) written over the
+//              row's own S columns, rare O rescales, the unit's record;
+//   warp 4     K producer: per group of 4 tiles, the K halves (hi, lo) of their
+//              split-once blocks as bulk copies into one of two 4-slot halves;
+//   warp 5     one lane issues every tcgen05.mma and tcgen05.commit;
+//   warp 6     V producer: the V^T halves of each tile into one of 4 slots.
+// Tensor memory (512 columns at hd 128): Q_hi | Q_lo (f16 pairs, hd/2 columns
+// each) | S buffer 0 | S buffer 1 (128 columns = 4 tiles each) | O (hd). S of a
+// group of 4 tiles is one N = 128 product. Both S buffers are in flight: the MMA
+// lane issues S of group g + 2 once P V of group g is done, so the tensor cores
+// compute scores two groups ahead, and P V of tile j runs while the softmax warps
+// work on tile j + 1 (P lives in its tile's S columns: no P buffer to wait for).
+// Every hand-off is an mbarrier; all waits are bounded (1 s) and report
+// SWA_DERR_TIMEOUT; tensor memory is released on every path.
+#include <cuda_fp16.h>
+
+#include "swa_internal.cuh"
+#include "swa_tcgen05.cuh"
+
+namespace swa {
+namespace {
+
+constexpr int kHM = 128;               // query vectors per unit (MMA M)
+constexpr int kHN = 32;                // keys per tile
+constexpr int kHG = 4;                 // tiles per S product (N = 128)
+constexpr int kHThreads = 7 * 32;
+constexpr float kHLazyMax = 8.0f;      // log2 headroom before the running max is raised
+constexpr int kVHead = 4;              // P = p * 2^(e_v - E + kVHead)
+constexpr int kVSlack = 3;             // E is raised when e_v > E + kVSlack (P < 2^15)
+constexpr int kZeroExp = -127;         // exponent of a block of zeros
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int HD>
+struct HCfg {
+  static constexpr int LAND = kHN * HD * 2;                 // one f16 half-tile (hi or lo), bytes
+  static constexpr int NSV = 4;                             // V slots
+  // shared memory: K_hi [2 halves x 4 slots], K_lo [8], V^T_hi [4], V^T_lo [4]
+  static constexpr int OFF_KHI = 0, OFF_KLO = 8 * LAND, OFF_VHI = 16 * LAND, OFF_VLO = 16 * LAND + NSV * LAND;
+  static constexpr int OFF_BAR = 16 * LAND + 2 * NSV * LAND;
+  static constexpr int NBAR = 40;
+  static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
+  // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
+  static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
+  static_assert(BYTES <= 232448, "227 KB of shared memory per CTA");
+  // TMEM columns
+  static constexpr uint32_t C_QHI = 0, C_QLO = HD / 2, C_S0 = HD, C_S1 = HD + kHG * kHN, C_O = HD + 2 * kHG * kHN;
+  static constexpr uint32_t TMEM_COLS = 512;
+  static_assert(C_O + HD <= TMEM_COLS, "tensor memory budget");
+  // K-major core-matrix layouts (8 rows x 16 bytes): LBO = next core matrix along K, SBO = next 8 rows
+  static constexpr uint32_t K_SBO = (HD / 8) * 128;        // K: rows = keys, K = features
+  static constexpr uint32_t V_SBO = (kHN / 8) * 128;       // V^T: rows = features, K = keys
+};
+
+// barrier block
+enum : int {
+  B_KFULL = 0,     // [2] K half h landed (bytes)
+  B_KFREE = 2,     // [2] MMA commit: the S that read K half h is done
+  B_VFULL = 4,     // [4] V slot landed (bytes)
+  B_VFREE = 8,     // [4] MMA commit: the P V that read the V slot is done
+  B_SFULL = 12,    // [2] MMA commit: S of the group in buffer b is done
+  B_SFREE = 14,    // [2] MMA commit: every P V of the group in buffer b is done
+  B_PREADY = 16,   // [8] softmax warps (4 arrivals): P of tile T % 8 written (and O rescaled)
+  B_PVDONE = 24,   // [8] MMA commit: P V of tile T % 8 done
+  B_QREADY = 32,   // softmax warps (4 arrivals): Q of the next unit in TMEM
+  B_FIN = 33,      // MMA commit: every MMA issued is done
+};
+
+// tiles of row block rb: the sink blocks, then logical blocks kb0 .. (len0 + r_last) / 32,
+// where kb0 holds the first key of the block's first row's window
+__device__ __forceinline__ int h16_row_block_tiles(const AttendParams& p, const SeqState& st, int rb) {
+  const int r0 = rb * p.rows, r_last = min(r0 + p.rows, p.t) - 1;
+  const int xlo = st.len0 + r0 + 1 - min(st.W, st.len0 + r0 + 1);
+  return p.ops_nsb + (st.len0 + r_last) / kHN - xlo / kHN + 1;
+}
+
+// exact 2^k for k in [-126, 127]; 0 below (the block exponents are clamped to +-100)
+__device__ __forceinline__ float pow2i(int k) {
+  return k < -126 ? 0.f : __int_as_float((127 + min(k, 127)) << 23);
+}
+
+// exponent e with max |x| * 2^-e in [2^14, 2^15) (clamped to +-100); kZeroExp if max |x| = 0
+__device__ __forceinline__ int block_exp(float amax) {
+  return amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : kZeroExp;
+}
+
+// x = hi + lo as f16 pairs: hi = RN(x), lo = RN(x - hi); element 2c in the low half
+__device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 f = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x0 - f.x, x1 - f.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// A unit: (sequence b, KV head g, row block rb) at rank `rank` of the order
+struct Unit {
+  int b, g, bg, rb, r0, rows_eff, xlo, kb0, ntiles;
+  SeqState st;
+};
+
+// rank of this CTA's k-th unit (boustrophedon over the longest-first order)
+__device__ __forceinline__ long long unit_rank(int k) {
+  const long long P = gridDim.x;
+  return (long long)k * P + ((k & 1) ? (P - 1 - blockIdx.x) : blockIdx.x);
+}
+
+__device__ __forceinline__ Unit load_unit(const AttendParams& p, long long rank, bool report) {
+  Unit u;
+  const int id = p.ws_order[rank];
+  u.rb = id % p.n_rb;
+  u.bg = id / p.n_rb;
+  u.b = u.bg / p.nk;
+  u.g = u.bg % p.nk;
+  u.st = load_state(p, u.b, report && u.g == 0 && u.rb == 0);
+  u.r0 = u.rb * p.rows;
+  const int r_last = min(u.r0 + p.rows, p.t) - 1;
+  u.rows_eff = r_last - u.r0 + 1;
+  u.xlo = u.st.len0 + u.r0 + 1 - min(u.st.W, u.st.len0 + u.r0 + 1);
+  u.kb0 = u.xlo / kHN;
+  u.ntiles = h16_row_block_tiles(p, u.st, u.rb);
+  return u;
+}
+
+template <int HD>
+__global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendParams p) {
+  using C = HCfg<HD>;
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(1024) unsigned char sm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(bars + C::NBAR);
+  volatile uint32_t* s_tmem = reinterpret_cast<volatile uint32_t*>(reinterpret_cast<int*>(bars + C::NBAR) + 1);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long U = (long long)p.B * p.nk * p.n_rb;
+  const unsigned char* ops = reinterpret_cast<const unsigned char*>(p.ops);
+
+  if (tid == 0) {
+    for (int k = 0; k < 2; ++k) {
+      mbar_init(&bars[B_KFULL + k], 1);
+      mbar_init(&bars[B_KFREE + k], 1);
+      mbar_init(&bars[B_SFULL + k], 1);
+      mbar_init(&bars[B_SFREE + k], 1);
+    }
+    for (int k = 0; k < C::NSV; ++k) {
+      mbar_init(&bars[B_VFULL + k], 1);
+      mbar_init(&bars[B_VFREE + k], 1);
+    }
+    for (int k = 0; k < 8; ++k) {
+      mbar_init(&bars[B_PREADY + k], 4);
+      mbar_init(&bars[B_PVDONE + k], 1);
+    }
+    mbar_init(&bars[B_QREADY], 4);
+    mbar_init(&bars[B_FIN], 1);
+    mbar_fence_init();
+    *s_abort = 0;
+  }
+  if (warp == 0) tc_alloc(const_cast<uint32_t*>(s_tmem), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  auto abort_now = [&]() {
+    *s_abort = 1;
+    set_err(p.err, SWA_DERR_TIMEOUT);
+  };
+
+  // ------------------------------------------------------------------ K producer
+  if (warp == 4 && lane == 0) {
+    long long GR = 0;              // groups issued so far (this CTA)
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const long long rank = unit_rank(k);
+      if (rank >= U) break;
+      const Unit u = load_unit(p, rank, false);
+      const unsigned char* blocks = ops + (size_t)u.bg * p.ops_nblk * 4 * C::LAND;
+      for (int i0 = 0; i0 < u.ntiles; i0 += kHG, ++GR) {
+        const int h = (int)(GR & 1);
+        if (GR >= 2 && (!mbar_wait_bounded(&bars[B_KFREE + h], (uint32_t)(((GR - 2) >> 1) & 1), kWaitLimitNs) ||
+                        *s_abort)) {
+          ok = false;
+          break;
+        }
+        const int cnt = min(kHG, u.ntiles - i0);
+        mbar_arrive_expect_tx(&bars[B_KFULL + h], (uint32_t)(cnt * 2 * C::LAND));
+        for (int j = 0; j < cnt; ++j) {
+          const int i = i0 + j;
+          const int blk = i >= p.ops_nsb ? i + u.kb0 : i;
+          const unsigned char* src = blocks + (size_t)blk * 4 * C::LAND;
+          bulk_g2s(sm + C::OFF_KHI + (size_t)(h * kHG + j) * C::LAND, src, (uint32_t)C::LAND, &bars[B_KFULL + h]);
+          bulk_g2s(sm + C::OFF_KLO + (size_t)(h * kHG + j) * C::LAND, src + C::LAND, (uint32_t)C::LAND,
+                   &bars[B_KFULL + h]);
+        }
+      }
+    }
+    if (!ok) abort_now();
+    // copies still in flight land before the CTA exits (bounded; on the normal path
+    // the MMA lane has already seen them)
+    for (long long g2 = GR - 2 < 0 ? 0 : GR - 2; g2 < GR; ++g2)
+      mbar_wait_bounded(&bars[B_KFULL + (g2 & 1)], (uint32_t)((g2 >> 1) & 1), kWaitLimitNs);
+  }
+
+  // ------------------------------------------------------------------ V producer
+  if (warp == 6 && lane == 0) {
+    long long T = 0;               // tiles issued so far
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const long long rank = unit_rank(k);
+      if (rank >= U) break;
+      const Unit u = load_unit(p, rank, false);
+      const unsigned char* blocks = ops + (size_t)u.bg * p.ops_nblk * 4 * C::LAND;
+      for (int i = 0; i < u.ntiles; ++i, ++T) {
+        const int slot = (int)(T % C::NSV);
+        if (T >= C::NSV &&
+            (!mbar_wait_bounded(&bars[B_VFREE + slot], (uint32_t)(((T - C::NSV) / C::NSV) & 1), kWaitLimitNs) ||
+             *s_abort)) {
+          ok = false;
+          break;
+        }
+        const int blk = i >= p.ops_nsb ? i + u.kb0 : i;
+        const unsigned char* src = blocks + (size_t)blk * 4 * C::LAND + 2 * C::LAND;
+        mbar_arrive_expect_tx(&bars[B_VFULL + slot], (uint32_t)(2 * C::LAND));
+        bulk_g2s(sm + C::OFF_VHI + (size_t)slot * C::LAND, src, (uint32_t)C::LAND, &bars[B_VFULL + slot]);
+        bulk_g2s(sm + C::OFF_VLO + (size_t)slot * C::LAND, src + C::LAND, (uint32_t)C::LAND, &bars[B_VFULL + slot]);
+      }
+    }
+    if (!ok) abort_now();
+    for (long long t2 = T - C::NSV < 0 ? 0 : T - C::NSV; t2 < T; ++t2)
+      mbar_wait_bounded(&bars[B_VFULL + (int)(t2 % C::NSV)], (uint32_t)((t2 / C::NSV) & 1), kWaitLimitNs);
+  }
+
+  // ------------------------------------------------------------------ MMA issuer
+  if (warp == 5 && lane == 0) {
+    const uint32_t id_s = tc_idesc_f16(kHM, kHG * kHN);
+    const uint32_t id_o = tc_idesc_f16(kHM, HD);
+    long long T = 0, GR = 0;
+    bool ok = true;
+    // S of group gr (K half gr & 1 into S buffer gr & 1): Q_lo K_hi + Q_hi K_lo + Q_hi K_hi
+    auto issue_s = [&](long long gr) -> bool {
+      const int h = (int)(gr & 1);
+      if (!mbar_wait_bounded(&bars[B_KFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs) || *s_abort) return false;
+      if (gr >= 2 && (!mbar_wait_bounded(&bars[B_SFREE + h], (uint32_t)(((gr - 2) >> 1) & 1), kWaitLimitNs) ||
+                      *s_abort))
+        return false;
+      tc_fence_after();
+      const uint32_t d = tmem + (h ? C::C_S1 : C::C_S0);
+#pragma unroll 1
+      for (int term = 0; term < 3; ++term) {
+        const uint32_t qcol = term == 0 ? C::C_QLO : C::C_QHI;
+        const unsigned char* kb = sm + (term == 1 ? C::OFF_KLO : C::OFF_KHI) + (size_t)h * kHG * C::LAND;
+        for (int ks = 0; ks < HD / 16; ++ks) {
+          const uint64_t bd = smem_desc(kb + ks * 256, 128, C::K_SBO);
+          tc_mma_f16(d, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
+        }
+      }
+      tc_commit(&bars[B_SFULL + h]);
+      tc_commit(&bars[B_KFREE + h]);
+      return true;
+    };
+    for (int k = 0, un = 0; ok; ++k, ++un) {
+      const long long rank = unit_rank(k);
+      if (rank >= U) break;
+      const Unit u = load_unit(p, rank, false);
+      const int ng = (u.ntiles + kHG - 1) / kHG;
+      // Q of this unit is in tensor memory (the previous unit's S are all done)
+      if (!mbar_wait_bounded(&bars[B_QREADY], (uint32_t)(un & 1), kWaitLimitNs) || *s_abort) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (ng > 0) ok = issue_s(GR);
+      if (ok && ng > 1) ok = issue_s(GR + 1);
+      for (int i = 0; ok && i < u.ntiles; ++i) {
+        const long long t = T + i;
+        const int gi = i / kHG, h = (int)((GR + gi) & 1);
+        const int vs = (int)(t % C::NSV);
+        if (!mbar_wait_bounded(&bars[B_PREADY + (int)(t & 7)], (uint32_t)((t >> 3) & 1), kWaitLimitNs) ||
+            *s_abort || !mbar_wait_bounded(&bars[B_VFULL + vs], (uint32_t)((t / C::NSV) & 1), kWaitLimitNs) ||
+            *s_abort) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // O += P_lo V_hi + P_hi V_lo + P_hi V_hi; P of tile i: its S columns, hi | lo
+        const uint32_t pcol = (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN);
+#pragma unroll 1
+        for (int term = 0; term < 3; ++term) {
+          const uint32_t acol = pcol + (term == 0 ? kHN / 2 : 0);
+          const unsigned char* vb = sm + (term == 1 ? C::OFF_VLO : C::OFF_VHI) + (size_t)vs * C::LAND;
+          for (int ks = 0; ks < kHN / 16; ++ks) {
+            const uint64_t bd = smem_desc(vb + ks * 256, 128, C::V_SBO);
+            tc_mma_f16(tmem + C::C_O, tmem + acol + ks * 8, bd, id_o, i > 0 || term > 0 || ks > 0);
+          }
+        }
+        tc_commit(&bars[B_PVDONE + (int)(t & 7)]);
+        tc_commit(&bars[B_VFREE + vs]);
+        if (i % kHG == kHG - 1 || i == u.ntiles - 1) tc_commit(&bars[B_SFREE + h]);
+        // S of group gi + 1 once P V of group gi - 1 is done (its buffer)
+        if (i % kHG == 0 && gi >= 1 && gi + 1 < ng) ok = issue_s(GR + gi + 1);
+      }
+      T += u.ntiles;
+      GR += ng;
+    }
+    if (!ok) abort_now();
+    tc_commit(&bars[B_FIN]);
+    mbar_wait_bounded(&bars[B_FIN], 0, kWaitLimitNs);
+  }
+
+  // ------------------------------------------------------------------ softmax warps
+  if (warp < 4) {
+    const int q = tid;                                   // query vector = TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    long long T = 0, GR = 0;
+    bool dead = false;
+    auto fail = [&]() {
+      if (lane == 0) abort_now();
+      dead = true;
+    };
+    const int2* exps = reinterpret_cast<const int2*>(p.ops_exp);
+    for (int k = 0, un = 0; !dead; ++k, ++un) {
+      const long long rank = unit_rank(k);
+      if (rank >= U) break;
+      const Unit u = load_unit(p, rank, true);
+      if (__any_sync(kFull, *s_abort)) { fail(); break; }
+      const int rr = q / p.hpg, hq = q % p.hpg;
+      const bool q_ok = rr < u.rows_eff && q < p.rows * p.hpg;
+      const int r = u.r0 + rr;
+      const int q_lo = u.st.len0 + r + 1 - min(u.st.W, u.st.len0 + r + 1);
+      const int q_hi = u.st.len0 + r;
+      if (u.g == 0 && tid == 0) {
+        p.ws_nsplit[u.b * p.n_rb + u.rb] = 1;
+        if (u.rb == 0) p.ws_meta[u.b] = p.meta[u.b];
+      }
+      // ---- Q of the unit: q * qmul * 2^-e_q as f16 hi / lo pairs into TMEM
+      int e_q;
+      {
+        float x[HD];
+        const float* src = p.q + (((size_t)u.b * p.t + r) * p.nh + (size_t)u.g * p.hpg + hq) * HD;
+#pragma unroll
+        for (int c = 0; c < HD; c += 4) {
+          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (q_ok) v = *reinterpret_cast<const float4*>(src + c);
+          x[c] = v.x * p.qmul;
+          x[c + 1] = v.y * p.qmul;
+          x[c + 2] = v.z * p.qmul;
+          x[c + 3] = v.w * p.qmul;
+        }
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < HD; ++c) amax = fmaxf(amax, fabsf(x[c]));
+        e_q = amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : 0;
+        const float sq = pow2i(-e_q);
+#pragma unroll
+        for (int c0 = 0; c0 < HD; c0 += 64) {
+          uint32_t hi[32], lo[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) split_pair(x[c0 + 2 * c] * sq, x[c0 + 2 * c + 1] * sq, hi[c], lo[c]);
+          tc_st32(tmem + lane_off + C::C_QHI + c0 / 2, hi);
+          tc_st32(tmem + lane_off + C::C_QLO + c0 / 2, lo);
+        }
+        tc_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_QREADY]);
+
+      float m_run = -INFINITY, l_run = 0.f;
+      int E = kZeroExp;
+      const int nsb = p.ops_nsb;
+      const size_t exp_base = (size_t)u.bg * p.ops_nblk;
+      auto exp_of = [&](int i) -> int2 {
+        if (i >= u.ntiles) return make_int2(0, kZeroExp);
+        return __ldg(exps + exp_base + (i >= nsb ? i + u.kb0 : i));
+      };
+      int2 ex0 = exp_of(0), ex1 = exp_of(1);
+      for (int i = 0; i < u.ntiles; ++i) {
+        const long long t = T + i;
+        const int gi = i / kHG;
+        const long long gr = GR + gi;
+        const int h = (int)(gr & 1);
+        const int2 ex = ex0;
+        ex0 = ex1;
+        ex1 = exp_of(i + 2);
+        if (i % kHG == 0 &&
+            !__all_sync(kFull, mbar_wait_bounded(&bars[B_SFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs))) {
+          fail();
+          break;
+        }
+        if (__any_sync(kFull, *s_abort)) { fail(); break; }
+        tc_fence_after();
+        const uint32_t scol = (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN);
+        uint32_t sr[32];
+        tc_ld32(tmem + lane_off + scol, sr);
+        tc_wait_ld();
+        // window mask; a tile wholly inside this row's window skips it. A sink tile
+        // holds sinks j0 .. j0 + 31 (valid below ns), a logical tile keys x0 .. x0 + 31.
+        const bool sink_tile = i < nsb;
+        const int j0 = i * kHN;
+        const int x0 = (u.kb0 + i - nsb) * kHN;
+        const bool inside = sink_tile ? q_ok && p.ns - j0 >= kHN : q_ok && x0 >= q_lo && x0 + kHN - 1 <= q_hi;
+        const float f = ldexpf(1.0f, e_q + ex.x);        // undoes the Q and K block scales
+        float s[32];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          bool v = true;
+          if (!inside) v = q_ok && (sink_tile ? j0 + c < p.ns : (x0 + c >= q_lo && x0 + c <= q_hi));
+          s[c] = v ? __uint_as_float(sr[c]) * f : -INFINITY;
+          tmax = fmaxf(tmax, s[c]);
+        }
+        // The running max m_run moves only when a tile exceeds it by more than
+        // kHLazyMax (log2 units): below that p = 2^(s - m_run) <= 2^kHLazyMax, and
+        // O and l keep one common scale, so o = O / l is unchanged.
+        const bool raise = tmax > m_run + kHLazyMax;
+        const float m_new = raise ? tmax : m_run;
+        const float c1 = raise ? exp2f(m_run - m_new) : 1.f;
+        const int e_v = ex.y;
+        const int E_new = (i == 0 || e_v > E + kVSlack) ? e_v : E;
+        const float c2 = i == 0 ? 1.f : ldexpf(1.0f, E - E_new);
+        const float pscale = pow2i(e_v - E_new + kVHead);   // P = p * 2^(e_v - E + kVHead)
+        uint32_t w[32];                                      // P hi pairs | P lo pairs
+        float psum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[c] - m_new);
+          const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[c + 1] - m_new);
+          psum += p0 + p1;
+          split_pair(p0 * pscale, p1 * pscale, w[c / 2], w[16 + c / 2]);
+        }
+        l_run = l_run * c1 + psum;
+        tc_st32(tmem + lane_off + scol, w);
+        // O rescale (warp-uniform): O holds P V of tiles < i; wait for the last of them
+        const float c = c1 * c2;
+        if (i > 0 && __any_sync(kFull, c != 1.f && m_run != -INFINITY)) {
+          const long long tp = t - 1;
+          if (!__all_sync(kFull, mbar_wait_bounded(&bars[B_PVDONE + (int)(tp & 7)], (uint32_t)((tp >> 3) & 1),
+                                                   kWaitLimitNs))) {
+            fail();
+            break;
+          }
+          tc_fence_after();
+          for (int c0 = 0; c0 < HD; c0 += 32) {
+            uint32_t o[32];
+            tc_ld32(tmem + lane_off + C::C_O + c0, o);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c);
+            tc_st32(tmem + lane_off + C::C_O + c0, o);
+          }
+        }
+        m_run = m_new;
+        E = E_new;
+        tc_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars[B_PREADY + (int)(t & 7)]);
+      }
+      if (dead) break;
+      // ---- the unit's record: O * 2^(E - kVHead) (unnormalised), m, l
+      const size_t item = (size_t)u.bg * p.n_rb + u.rb;
+      float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD;
+      if (u.ntiles > 0) {
+        const long long tl = T + u.ntiles - 1;
+        if (!__all_sync(kFull, mbar_wait_bounded(&bars[B_PVDONE + (int)(tl & 7)], (uint32_t)((tl >> 3) & 1),
+                                                 kWaitLimitNs))) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const float os = ldexpf(1.0f, E - kVHead);
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t o[32];
+          tc_ld32(tmem + lane_off + C::C_O + c0, o);
+          tc_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c0 + e) =
+                make_float4(__uint_as_float(o[e]) * os, __uint_as_float(o[e + 1]) * os,
+                            __uint_as_float(o[e + 2]) * os, __uint_as_float(o[e + 3]) * os);
+        }
+      } else {
+        for (int c0 = 0; c0 < HD; c0 += 4) *reinterpret_cast<float4*>(dst + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run);
+      T += u.ntiles;
+      GR += (u.ntiles + kHG - 1) / kHG;
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  // every role has waited for what it issued (copies, MMAs) before it got here
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tc_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// The token path's row blocks ordered by their tile count, longest first, by one CTA
+// of 256 threads (a counting sort; equal counts in any order). Every order gives the
+// same results.
+__device__ void order_row_blocks_h16(const AttendParams& p) {
+  constexpr int kBins = 2048;
+  __shared__ int cnt[kBins];
+  const int U = p.B * p.nk * p.n_rb;
+  const int nb = min(kBins, p.ops_nblk + 1);   // a row block has at most ops_nblk tiles
+  auto key = [&](int u) {                       // bin nb - 1 - tiles: longest first
+    const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
+    const int tiles = min(max(h16_row_block_tiles(p, st, u % p.n_rb), 0), nb - 1);
+    return nb - 1 - tiles;
+  };
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) cnt[i] = 0;
+  __syncthreads();
+  for (int u = threadIdx.x; u < U; u += blockDim.x) atomicAdd(&cnt[key(u)], 1);
+  __syncthreads();
+  // exclusive prefix over the bins by warp 0: lane l sums bins l * per .. l * per + per - 1
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x, per = (nb + 31) / 32;
+    const int lo = min(lane * per, nb), hi = min(lo + per, nb);
+    int sum = 0;
+    for (int i = lo; i < hi; ++i) sum += cnt[i];
+    int incl = sum;
+    for (int d = 1; d < 32; d <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, d);
+      if (lane >= d) incl += v;
+    }
+    int run = incl - sum;
+    for (int i = lo; i < hi; ++i) {
+      const int c = cnt[i];
+      cnt[i] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  for (int u = threadIdx.x; u < U; u += blockDim.x) p.ws_order[atomicAdd(&cnt[key(u)], 1)] = u;
+}
+
+// Split-once operand blocks: one CTA of 256 threads per (sequence, KV head, block).
+// Blocks 0 .. nsb - 1 hold the sinks, block nsb + k the logical keys x = 32k .. 32k + 31
+// below len0 + t (ring slot (head0 + x) % W for x < len0, chunk row x - len0 after),
+// read before the commit rewrites the ring; missing keys are zeros. A block is
+// K_hi | K_lo (keys x features, K-major core matrices: (key / 8) * K_SBO + (f / 8) *
+// 128 + (key % 8) * 16 + (f % 8) * 2 bytes) | V^T_hi | V^T_lo ((f / 8) * V_SBO + (key /
+// 8) * 128 + (f % 8) * 16 + (key % 8) * 2), each f16 of 2^-e times the block's rows;
+// ops_exp holds (e_k, e_v). The extra row blockIdx.y = B * nk orders the row blocks.
+template <int HD>
+__global__ void __launch_bounds__(256) token_presplit_h16_kernel(AttendParams p) {
+  using C = HCfg<HD>;
+  pdl_trigger();
+  pdl_wait();
+  if (blockIdx.y == (unsigned)(p.B * p.nk)) {
+    if (blockIdx.x == 0) order_row_blocks_h16(p);
+    return;
+  }
+  const int blk = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.nk, g = bg % p.nk;
+  const SeqState st = sanitize_state(p.meta[b], p.cap, nullptr);   // the attention reports bad metas
+  const size_t kv_head = (size_t)b * p.nk + g;
+  const bool sink = blk < p.ops_nsb;
+  const int j0 = blk * kHN;                                        // first sink of a sink block
+  const int x0 = (blk - p.ops_nsb) * kHN;                          // first logical key otherwise
+  if (!sink && x0 >= st.len0 + p.t) return;                        // past every row's window
+  __shared__ __align__(16) float ks[kHN][HD + 4];
+  __shared__ __align__(16) float vs[kHN][HD + 4];
+  __shared__ float red[2][8];
+  constexpr int D4 = HD / 4;
+  float ak = 0.f, av = 0.f;
+  for (int idx = threadIdx.x; idx < kHN * D4; idx += blockDim.x) {
+    const int key = idx / D4, f4 = idx % D4;
+    const float* kr = nullptr;
+    const float* vr = nullptr;
+    if (sink) {
+      if (j0 + key < p.ns) {
+        const size_t at = (kv_head * p.ns + j0 + key) * HD;
+        kr = p.sink_k + at;
+        vr = p.sink_v + at;
+      }
+    } else {
+      const int x = x0 + key;
+      if (x < st.len0) {
+        int slot = st.head0 + x;
+        if (slot >= st.W) slot -= st.W;
+        const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
+        kr = p.ring_k + at;
+        vr = p.ring_v + at;
+      } else if (x < st.len0 + p.t) {
+        const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
+        kr = p.k_chunk + at;
+        vr = p.v_chunk + at;
+      }
+    }
+    float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
+    if (kr) {
+      kv = *reinterpret_cast<const float4*>(kr + f4 * 4);
+      vv = *reinterpret_cast<const float4*>(vr + f4 * 4);
+    }
+    *reinterpret_cast<float4*>(&ks[key][f4 * 4]) = kv;
+    *reinterpret_cast<float4*>(&vs[key][f4 * 4]) = vv;
+    ak = fmaxf(ak, fmaxf(fmaxf(fabsf(kv.x), fabsf(kv.y)), fmaxf(fabsf(kv.z), fabsf(kv.w))));
+    av = fmaxf(av, fmaxf(fmaxf(fabsf(vv.x), fabsf(vv.y)), fmaxf(fabsf(vv.z), fabsf(vv.w))));
+  }
+  for (int d = 16; d > 0; d >>= 1) {
+    ak = fmaxf(ak, __shfl_xor_sync(kFull, ak, d));
+    av = fmaxf(av, __shfl_xor_sync(kFull, av, d));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    red[0][threadIdx.x >> 5] = ak;
+    red[1][threadIdx.x >> 5] = av;
+  }
+  __syncthreads();
+  ak = 0.f;
+  av = 0.f;
+  for (int w = 0; w < 8; ++w) {
+    ak = fmaxf(ak, red[0][w]);
+    av = fmaxf(av, red[1][w]);
+  }
+  const int e_k = block_exp(ak), e_v = block_exp(av);
+  const float sk = pow2i(-(e_k == kZeroExp ? 0 : e_k)), sv = pow2i(-(e_v == kZeroExp ? 0 : e_v));
+  unsigned char* dst = reinterpret_cast<unsigned char*>(p.ops) + ((size_t)bg * p.ops_nblk + blk) * 4 * C::LAND;
+  if (threadIdx.x == 0) reinterpret_cast<int2*>(p.ops_exp)[(size_t)bg * p.ops_nblk + blk] = make_int2(e_k, e_v);
+  // K: thread -> (key, 8 features): one 16-byte store each of hi and lo
+  for (int idx = threadIdx.x; idx < kHN * (HD / 8); idx += blockDim.x) {
+    const int key = idx % kHN, f8 = idx / kHN;
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      split_pair(ks[key][f8 * 8 + 2 * e] * sk, ks[key][f8 * 8 + 2 * e + 1] * sk, hw[e], lw[e]);
+    const size_t off = (size_t)(key >> 3) * C::K_SBO + f8 * 128 + (key & 7) * 16;
+    *reinterpret_cast<uint4*>(dst + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(dst + C::LAND + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+  // V^T: thread -> (feature, 8 keys)
+  for (int idx = threadIdx.x; idx < HD * (kHN / 8); idx += blockDim.x) {
+    const int f = idx % HD, k8 = idx / HD;
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      split_pair(vs[k8 * 8 + 2 * e][f] * sv, vs[k8 * 8 + 2 * e + 1][f] * sv, hw[e], lw[e]);
+    const size_t off = (size_t)(f >> 3) * C::V_SBO + k8 * 128 + (f & 7) * 16;
+    *reinterpret_cast<uint4*>(dst + 2 * C::LAND + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(dst + 3 * C::LAND + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
+}
+
+template <int HD>
+int launch_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  using C = HCfg<HD>;
+  auto kern = attend_prompt_h16_kernel<HD>;
+  static bool attr_set[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_set[dev]) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::BYTES);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (dev >= 0 && dev < 64) attr_set[dev] = true;
+  }
+  const dim3 pgrid((unsigned)p.ops_nblk, (unsigned)(p.B * p.nk + 1));
+  int rc = finish_launch(launch_pdl(token_presplit_h16_kernel<HD>, pgrid, dim3(256), 0, s, p));
+  if (rc != SWA_OK) return rc;
+  const long long units = (long long)p.B * p.nk * p.n_rb;
+  const int sms = num_sms();
+  const unsigned grid = (unsigned)(units < sms ? units : (sms > 0 ? sms : 148));
+  if (e0) cudaEventRecord(e0, s);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kHThreads), C::BYTES, s, p);
+  note_launch();
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e1) cudaEventRecord(e1, s);
+  return cuda_status(e);
+}
+
+}  // namespace
+
+int launch_attend_prompt_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  switch (p.hd) {
+    case 64: return launch_h16<64>(p, s, e0, e1);
+    case 128: return launch_h16<128>(p, s, e0, e1);
+  }
+  return SWA_E_SHAPE;
+}
+
+}  // namespace swa

@@ -198,9 +198,10 @@ def test_workspace_minimum_and_split_once_blocks(lib):
     lo = lib.swa_attend_workspace_min(ctypes.byref(p))
     hi = lib.swa_attend_workspace_size(ctypes.byref(p))
     blocks = 1 + (100 + 64 + 31) // 32                      # sink block + logical blocks
-    ops = 2 * 2 * blocks * 4 * 32 * 128 * 4                 # B * nk * blocks * (K, V) x (hi, lo) x 32 x hd
+    ops = 2 * 2 * blocks * 4 * 32 * 128 * 2                 # B * nk * blocks * (K, V) x (hi, lo) x 32 x hd f16
+    exps = 2 * 2 * blocks * 8                               # (e_k, e_v) per block
     order = 2 * 2 * (64 // 32) * 4                          # one int per row block (32 rows of 4 heads)
-    assert hi - lo >= ops + order and hi - lo < ops + order + 2 * 256
+    assert hi - lo >= ops + exps + order and hi - lo < ops + exps + order + 3 * 256
     call = lambda a: lib.swa_attend(ctypes.byref(a), None)
     assert call(_attend(t=64, nh=8, nk=2, cap=100, ns=3, workspace_bytes=lo - 1)) == _abi.SWA_E_WORKSPACE
     assert lib.swa_attend_workspace_min(None) == 0
