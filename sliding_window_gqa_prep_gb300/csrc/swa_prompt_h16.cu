@@ -104,6 +104,21 @@ __device__ __forceinline__ float pow2i(int k) {
   return k < -126 ? 0.f : __int_as_float((127 + min(k, 127)) << 23);
 }
 
+// exact 2^k for k in [-252, 254] (a product of two normal powers; tiny results round to
+// subnormals or 0)
+__device__ __forceinline__ float pow2w(int k) {
+  const int a = k >> 1;
+  return pow2i(a) * pow2i(k - a);
+}
+
+// 2^x by the MUFU instruction (relative error about 2^-22; -inf -> +0, results below
+// 2^-126 flush to 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // exponent e with max |x| * 2^-e in [2^14, 2^15) (clamped to +-100); kZeroExp if max |x| = 0
 __device__ __forceinline__ int block_exp(float amax) {
   return amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : kZeroExp;
@@ -130,14 +145,16 @@ __device__ __forceinline__ long long unit_rank(int k) {
   return (long long)k * P + ((k & 1) ? (P - 1 - blockIdx.x) : blockIdx.x);
 }
 
-__device__ __forceinline__ Unit load_unit(const AttendParams& p, long long rank, bool report) {
+// the unit of row-block id `id` (index (b * nk + g) * n_rb + rb) with its sequence's meta
+__device__ __forceinline__ Unit unit_from(const AttendParams& p, int id, const swa_meta m, bool report) {
   Unit u;
-  const int id = p.ws_order[rank];
   u.rb = id % p.n_rb;
   u.bg = id / p.n_rb;
   u.b = u.bg / p.nk;
   u.g = u.bg % p.nk;
-  u.st = load_state(p, u.b, report && u.g == 0 && u.rb == 0);
+  bool bad = false;
+  u.st = sanitize_state(m, p.cap, &bad);
+  if (bad && report && u.g == 0 && u.rb == 0) set_err(p.err, SWA_DERR_META);
   u.r0 = u.rb * p.rows;
   const int r_last = min(u.r0 + p.rows, p.t) - 1;
   u.rows_eff = r_last - u.r0 + 1;
@@ -145,6 +162,11 @@ __device__ __forceinline__ Unit load_unit(const AttendParams& p, long long rank,
   u.kb0 = u.xlo / kHN;
   u.ntiles = h16_row_block_tiles(p, u.st, u.rb);
   return u;
+}
+
+__device__ __forceinline__ Unit load_unit(const AttendParams& p, long long rank, bool report) {
+  const int id = p.ws_order[rank];
+  return unit_from(p, id, p.meta[id / p.n_rb / p.nk], report);
 }
 
 template <int HD>
@@ -335,6 +357,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
   if (warp < 4) {
     const int q = tid;                                   // query vector = TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int rr = q / p.hpg, hq = q % p.hpg;
     long long T = 0, GR = 0;
     bool dead = false;
     auto fail = [&]() {
@@ -342,12 +365,55 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       dead = true;
     };
     const int2* exps = reinterpret_cast<const int2*>(p.ops_exp);
-    for (int k = 0, un = 0; !dead; ++k, ++un) {
-      const long long rank = unit_rank(k);
-      if (rank >= U) break;
-      const Unit u = load_unit(p, rank, true);
+    // Q of unit u into TMEM: q * qmul * 2^-e_q as f16 hi / lo pairs (returns e_q); the
+    // S products of the previous unit are all done when this runs
+    auto put_q = [&](const Unit& u) -> int {
+      const bool q_ok = rr < u.rows_eff && q < p.rows * p.hpg;
+      float x[HD];
+      const float* src = p.q + (((size_t)u.b * p.t + u.r0 + rr) * p.nh + (size_t)u.g * p.hpg + hq) * HD;
+#pragma unroll
+      for (int c = 0; c < HD; c += 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q_ok) v = *reinterpret_cast<const float4*>(src + c);
+        x[c] = v.x * p.qmul;
+        x[c + 1] = v.y * p.qmul;
+        x[c + 2] = v.z * p.qmul;
+        x[c + 3] = v.w * p.qmul;
+      }
+      float am[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < HD; ++c) am[c & 3] = fmaxf(am[c & 3], fabsf(x[c]));
+      const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+      const int e = amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : 0;
+      const float sq = pow2i(-e);
+#pragma unroll
+      for (int c0 = 0; c0 < HD; c0 += 64) {
+        uint32_t hi[32], lo[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) split_pair(x[c0 + 2 * c] * sq, x[c0 + 2 * c + 1] * sq, hi[c], lo[c]);
+        tc_st32(tmem + lane_off + C::C_QHI + c0 / 2, hi);
+        tc_st32(tmem + lane_off + C::C_QLO + c0 / 2, lo);
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_QREADY]);
+      return e;
+    };
+    long long rank = unit_rank(0);
+    Unit u{};
+    int e_q = 0;
+    if (rank < U) {
+      u = load_unit(p, rank, true);
+      e_q = put_q(u);
+    }
+    for (int k = 0; rank < U && !dead; ++k) {
       if (__any_sync(kFull, *s_abort)) { fail(); break; }
-      const int rr = q / p.hpg, hq = q % p.hpg;
+      // the next unit's id now, its meta after the first tile: both arrive during this unit
+      const long long nrank = unit_rank(k + 1);
+      const bool has_next = nrank < U;
+      const int nid = has_next ? p.ws_order[nrank] : 0;
+      swa_meta nmeta{};
       const bool q_ok = rr < u.rows_eff && q < p.rows * p.hpg;
       const int r = u.r0 + rr;
       const int q_lo = u.st.len0 + r + 1 - min(u.st.W, u.st.len0 + r + 1);
@@ -356,39 +422,6 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         p.ws_nsplit[u.b * p.n_rb + u.rb] = 1;
         if (u.rb == 0) p.ws_meta[u.b] = p.meta[u.b];
       }
-      // ---- Q of the unit: q * qmul * 2^-e_q as f16 hi / lo pairs into TMEM
-      int e_q;
-      {
-        float x[HD];
-        const float* src = p.q + (((size_t)u.b * p.t + r) * p.nh + (size_t)u.g * p.hpg + hq) * HD;
-#pragma unroll
-        for (int c = 0; c < HD; c += 4) {
-          float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (q_ok) v = *reinterpret_cast<const float4*>(src + c);
-          x[c] = v.x * p.qmul;
-          x[c + 1] = v.y * p.qmul;
-          x[c + 2] = v.z * p.qmul;
-          x[c + 3] = v.w * p.qmul;
-        }
-        float amax = 0.f;
-#pragma unroll
-        for (int c = 0; c < HD; ++c) amax = fmaxf(amax, fabsf(x[c]));
-        e_q = amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : 0;
-        const float sq = pow2i(-e_q);
-#pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 64) {
-          uint32_t hi[32], lo[32];
-#pragma unroll
-          for (int c = 0; c < 32; ++c) split_pair(x[c0 + 2 * c] * sq, x[c0 + 2 * c + 1] * sq, hi[c], lo[c]);
-          tc_st32(tmem + lane_off + C::C_QHI + c0 / 2, hi);
-          tc_st32(tmem + lane_off + C::C_QLO + c0 / 2, lo);
-        }
-        tc_wait_st();
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_QREADY]);
-
       float m_run = -INFINITY, l_run = 0.f;
       int E = kZeroExp;
       const int nsb = p.ops_nsb;
@@ -423,35 +456,40 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         const int j0 = i * kHN;
         const int x0 = (u.kb0 + i - nsb) * kHN;
         const bool inside = sink_tile ? q_ok && p.ns - j0 >= kHN : q_ok && x0 >= q_lo && x0 + kHN - 1 <= q_hi;
-        const float f = ldexpf(1.0f, e_q + ex.x);        // undoes the Q and K block scales
+        const float f = pow2w(e_q + ex.x);                // undoes the Q and K block scales
         float s[32];
-        float tmax = -INFINITY;
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           bool v = true;
           if (!inside) v = q_ok && (sink_tile ? j0 + c < p.ns : (x0 + c >= q_lo && x0 + c <= q_hi));
           s[c] = v ? __uint_as_float(sr[c]) * f : -INFINITY;
-          tmax = fmaxf(tmax, s[c]);
         }
+        float mx[8];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
+        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         // The running max m_run moves only when a tile exceeds it by more than
         // kHLazyMax (log2 units): below that p = 2^(s - m_run) <= 2^kHLazyMax, and
         // O and l keep one common scale, so o = O / l is unchanged.
         const bool raise = tmax > m_run + kHLazyMax;
         const float m_new = raise ? tmax : m_run;
-        const float c1 = raise ? exp2f(m_run - m_new) : 1.f;
+        const float c1 = raise ? ex2(m_run - m_new) : 1.f;
         const int e_v = ex.y;
         const int E_new = (i == 0 || e_v > E + kVSlack) ? e_v : E;
-        const float c2 = i == 0 ? 1.f : ldexpf(1.0f, E - E_new);
+        const float c2 = i == 0 ? 1.f : pow2w(max(E - E_new, -252));
         const float pscale = pow2i(e_v - E_new + kVHead);   // P = p * 2^(e_v - E + kVHead)
         uint32_t w[32];                                      // P hi pairs | P lo pairs
-        float psum = 0.f;
+        const float mref = m_new == -INFINITY ? 0.f : m_new;   // no valid key yet: every s is -inf, p = 0
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float p0 = m_new == -INFINITY ? 0.f : exp2f(s[c] - m_new);
-          const float p1 = m_new == -INFINITY ? 0.f : exp2f(s[c + 1] - m_new);
-          psum += p0 + p1;
+          const float p0 = ex2(s[c] - mref);
+          const float p1 = ex2(s[c + 1] - mref);
+          ps[(c >> 1) & 3] += p0 + p1;
           split_pair(p0 * pscale, p1 * pscale, w[c / 2], w[16 + c / 2]);
         }
+        const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         l_run = l_run * c1 + psum;
         tc_st32(tmem + lane_off + scol, w);
         // O rescale (warp-uniform): O holds P V of tiles < i; wait for the last of them
@@ -479,8 +517,17 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_PREADY + (int)(t & 7)]);
+        if (i == 0 && has_next) nmeta = p.meta[nid / p.n_rb / p.nk];
       }
       if (dead) break;
+      if (u.ntiles == 0 && has_next) nmeta = p.meta[nid / p.n_rb / p.nk];
+      // ---- the next unit's Q: its first S products run while this unit's record is written
+      Unit nu{};
+      int e_qn = 0;
+      if (has_next) {
+        nu = unit_from(p, nid, nmeta, true);
+        e_qn = put_q(nu);
+      }
       // ---- the unit's record: O * 2^(E - kVHead) (unnormalised), m, l
       const size_t item = (size_t)u.bg * p.n_rb + u.rb;
       float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD;
@@ -492,7 +539,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
           break;
         }
         tc_fence_after();
-        const float os = ldexpf(1.0f, E - kVHead);
+        const float os = pow2w(E - kVHead);
         for (int c0 = 0; c0 < HD; c0 += 32) {
           uint32_t o[32];
           tc_ld32(tmem + lane_off + C::C_O + c0, o);
@@ -509,6 +556,9 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run);
       T += u.ntiles;
       GR += (u.ntiles + kHG - 1) / kHG;
+      u = nu;
+      e_q = e_qn;
+      rank = nrank;
     }
   }
 
