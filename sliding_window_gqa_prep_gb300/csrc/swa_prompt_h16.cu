@@ -49,7 +49,7 @@ namespace {
 constexpr int kHM = 128;               // query vectors per unit (MMA M)
 constexpr int kHN = 32;                // keys per tile
 constexpr int kHG = 4;                 // tiles per S product (N = 128)
-constexpr int kHThreads = 7 * 32;
+constexpr int kHThreads = 11 * 32;
 constexpr float kHLazyMax = 8.0f;      // log2 headroom before the running max is raised
 constexpr int kVHead = 4;              // P = p * 2^(e_v - E + kVHead)
 constexpr int kVSlack = 3;             // E is raised when e_v > E + kVSlack (P < 2^15)
@@ -63,8 +63,10 @@ struct HCfg {
   // shared memory: K_hi [2 halves x 4 slots], K_lo [8], V^T_hi [4], V^T_lo [4]
   static constexpr int OFF_KHI = 0, OFF_KLO = 8 * LAND, OFF_VHI = 16 * LAND, OFF_VLO = 16 * LAND + NSV * LAND;
   static constexpr int OFF_BAR = 16 * LAND + 2 * NSV * LAND;
-  static constexpr int NBAR = 40;
-  static constexpr size_t USED = (size_t)OFF_BAR + NBAR * 8 + 16;
+  static constexpr int NBAR = 48;
+  // softmax pair exchange: [2 tile parities][2 halves][128 query vectors] floats
+  static constexpr int OFF_XCH = OFF_BAR + NBAR * 8 + 16;
+  static constexpr size_t USED = (size_t)OFF_XCH + 2 * 2 * kHM * 4;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
   static_assert(BYTES <= 232448, "227 KB of shared memory per CTA");
@@ -78,17 +80,18 @@ struct HCfg {
 };
 
 // barrier block
+// (a commit costs the issuing thread about as much as three MMAs, so each event has
+// one barrier: "S of group g done" also frees K half g % 2, "P V of tile T done" also
+// frees V slot T % 4 and, for a group's last tile, the group's S buffer)
 enum : int {
   B_KFULL = 0,     // [2] K half h landed (bytes)
-  B_KFREE = 2,     // [2] MMA commit: the S that read K half h is done
   B_VFULL = 4,     // [4] V slot landed (bytes)
-  B_VFREE = 8,     // [4] MMA commit: the P V that read the V slot is done
-  B_SFULL = 12,    // [2] MMA commit: S of the group in buffer b is done
-  B_SFREE = 14,    // [2] MMA commit: every P V of the group in buffer b is done
-  B_PREADY = 16,   // [8] softmax warps (4 arrivals): P of tile T % 8 written (and O rescaled)
-  B_PVDONE = 24,   // [8] MMA commit: P V of tile T % 8 done
+  B_SFULL = 12,    // [2] MMA commit: S of the group in buffer b is done (K half b is free)
+  B_PREADY = 16,   // [8] softmax warps (8 arrivals): P of tile T % 8 written (and O rescaled)
+  B_PVDONE = 24,   // [8] MMA commit: P V of tile T % 8 done (V slot T % 4 is free)
   B_QREADY = 32,   // softmax warps (4 arrivals): Q of the next unit in TMEM
   B_FIN = 33,      // MMA commit: every MMA issued is done
+  B_XCH = 34,      // [4 lane quarters x 2 slots] softmax pair exchange (2 arrivals)
 };
 
 // tiles of row block rb: the sink blocks, then logical blocks kb0 .. (len0 + r_last) / 32,
@@ -122,6 +125,11 @@ __device__ __forceinline__ float ex2(float x) {
 // exponent e with max |x| * 2^-e in [2^14, 2^15) (clamped to +-100); kZeroExp if max |x| = 0
 __device__ __forceinline__ int block_exp(float amax) {
   return amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : kZeroExp;
+}
+
+// bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) from global memory into L2
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
 }
 
 // x = hi + lo as f16 pairs: hi = RN(x), lo = RN(x - hi); element 2c in the low half
@@ -185,20 +193,18 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
   if (tid == 0) {
     for (int k = 0; k < 2; ++k) {
       mbar_init(&bars[B_KFULL + k], 1);
-      mbar_init(&bars[B_KFREE + k], 1);
       mbar_init(&bars[B_SFULL + k], 1);
-      mbar_init(&bars[B_SFREE + k], 1);
     }
     for (int k = 0; k < C::NSV; ++k) {
       mbar_init(&bars[B_VFULL + k], 1);
-      mbar_init(&bars[B_VFREE + k], 1);
     }
     for (int k = 0; k < 8; ++k) {
-      mbar_init(&bars[B_PREADY + k], 4);
+      mbar_init(&bars[B_PREADY + k], 8);
       mbar_init(&bars[B_PVDONE + k], 1);
     }
-    mbar_init(&bars[B_QREADY], 4);
+    mbar_init(&bars[B_QREADY], 8);
     mbar_init(&bars[B_FIN], 1);
+    for (int k = 0; k < 8; ++k) mbar_init(&bars[B_XCH + k], 2);
     mbar_fence_init();
     *s_abort = 0;
   }
@@ -213,7 +219,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
   };
 
   // ------------------------------------------------------------------ K producer
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     long long GR = 0;              // groups issued so far (this CTA)
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -221,9 +227,13 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       if (rank >= U) break;
       const Unit u = load_unit(p, rank, false);
       const unsigned char* blocks = ops + (size_t)u.bg * p.ops_nblk * 4 * C::LAND;
+      // the unit's Q rows into L2 ahead of the softmax warps (hpg heads of a row are contiguous)
+      for (int j = 0; j < u.rows_eff; ++j)
+        bulk_prefetch_l2(p.q + (((size_t)u.b * p.t + u.r0 + j) * p.nh + (size_t)u.g * p.hpg) * HD,
+                         (uint32_t)(p.hpg * HD * 4));
       for (int i0 = 0; i0 < u.ntiles; i0 += kHG, ++GR) {
         const int h = (int)(GR & 1);
-        if (GR >= 2 && (!mbar_wait_bounded(&bars[B_KFREE + h], (uint32_t)(((GR - 2) >> 1) & 1), kWaitLimitNs) ||
+        if (GR >= 2 && (!mbar_wait_bounded(&bars[B_SFULL + h], (uint32_t)(((GR - 2) >> 1) & 1), kWaitLimitNs) ||
                         *s_abort)) {
           ok = false;
           break;
@@ -248,7 +258,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
   }
 
   // ------------------------------------------------------------------ V producer
-  if (warp == 6 && lane == 0) {
+  if (warp == 10 && lane == 0) {
     long long T = 0;               // tiles issued so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
@@ -259,7 +269,8 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       for (int i = 0; i < u.ntiles; ++i, ++T) {
         const int slot = (int)(T % C::NSV);
         if (T >= C::NSV &&
-            (!mbar_wait_bounded(&bars[B_VFREE + slot], (uint32_t)(((T - C::NSV) / C::NSV) & 1), kWaitLimitNs) ||
+            (!mbar_wait_bounded(&bars[B_PVDONE + (int)((T - C::NSV) & 7)], (uint32_t)(((T - C::NSV) >> 3) & 1),
+                                kWaitLimitNs) ||
              *s_abort)) {
           ok = false;
           break;
@@ -277,18 +288,22 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
   }
 
   // ------------------------------------------------------------------ MMA issuer
-  if (warp == 5 && lane == 0) {
+  if (warp == 9 && lane == 0) {
     const uint32_t id_s = tc_idesc_f16(kHM, kHG * kHN);
     const uint32_t id_o = tc_idesc_f16(kHM, HD);
     long long T = 0, GR = 0;
+    long long last0 = 0, last1 = 0;  // last tile of the latest group in S buffer 0 / 1
     bool ok = true;
     // S of group gr (K half gr & 1 into S buffer gr & 1): Q_lo K_hi + Q_hi K_lo + Q_hi K_hi
     auto issue_s = [&](long long gr) -> bool {
       const int h = (int)(gr & 1);
       if (!mbar_wait_bounded(&bars[B_KFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs) || *s_abort) return false;
-      if (gr >= 2 && (!mbar_wait_bounded(&bars[B_SFREE + h], (uint32_t)(((gr - 2) >> 1) & 1), kWaitLimitNs) ||
-                      *s_abort))
-        return false;
+      // the buffer's previous group: every P V done (its last tile's)
+      if (gr >= 2) {
+        const long long tl = h ? last1 : last0;
+        if (!mbar_wait_bounded(&bars[B_PVDONE + (int)(tl & 7)], (uint32_t)((tl >> 3) & 1), kWaitLimitNs) || *s_abort)
+          return false;
+      }
       tc_fence_after();
       const uint32_t d = tmem + (h ? C::C_S1 : C::C_S0);
 #pragma unroll 1
@@ -301,7 +316,6 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         }
       }
       tc_commit(&bars[B_SFULL + h]);
-      tc_commit(&bars[B_KFREE + h]);
       return true;
     };
     for (int k = 0, un = 0; ok; ++k, ++un) {
@@ -328,20 +342,20 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
           break;
         }
         tc_fence_after();
-        // O += P_lo V_hi + P_hi V_lo + P_hi V_hi; P of tile i: its S columns, hi | lo
+        // O += P_lo V_hi + P_hi V_lo + P_hi V_hi; P of tile i in its S columns: for keys
+        // 0-15 and then 16-31, 8 columns of hi pairs and 8 of lo pairs
         const uint32_t pcol = (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN);
 #pragma unroll 1
         for (int term = 0; term < 3; ++term) {
-          const uint32_t acol = pcol + (term == 0 ? kHN / 2 : 0);
           const unsigned char* vb = sm + (term == 1 ? C::OFF_VLO : C::OFF_VHI) + (size_t)vs * C::LAND;
           for (int ks = 0; ks < kHN / 16; ++ks) {
             const uint64_t bd = smem_desc(vb + ks * 256, 128, C::V_SBO);
-            tc_mma_f16(tmem + C::C_O, tmem + acol + ks * 8, bd, id_o, i > 0 || term > 0 || ks > 0);
+            const uint32_t acol = pcol + ks * 16 + (term == 0 ? 8 : 0);   // keys 16 ks ..: hi | lo
+            tc_mma_f16(tmem + C::C_O, tmem + acol, bd, id_o, i > 0 || term > 0 || ks > 0);
           }
         }
         tc_commit(&bars[B_PVDONE + (int)(t & 7)]);
-        tc_commit(&bars[B_VFREE + vs]);
-        if (i % kHG == kHG - 1 || i == u.ntiles - 1) tc_commit(&bars[B_SFREE + h]);
+        if (i % kHG == kHG - 1 || i == u.ntiles - 1) (h ? last1 : last0) = t;
         // S of group gi + 1 once P V of group gi - 1 is done (its buffer)
         if (i % kHG == 0 && gi >= 1 && gi + 1 < ng) ok = issue_s(GR + gi + 1);
       }
@@ -354,25 +368,52 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
   }
 
   // ------------------------------------------------------------------ softmax warps
-  if (warp < 4) {
-    const int q = tid;                                   // query vector = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+  // Warps w and w + 4 share TMEM lanes 32 (w % 4) .. + 31 (one query vector each per
+  // lane): warp w takes keys 0-15 of every tile, features 0 .. hd/2 - 1 of Q and O,
+  // warp w + 4 the other halves. The pair exchanges row maxima (and at the end l)
+  // through shared memory with a 64-thread named barrier; both then take the same
+  // decisions (running max, V exponent, rescale) from the same values.
+  if (warp < 8) {
+    const int quarter = warp & 3, half = warp >> 2;
+    const int q = quarter * 32 + lane;                   // query vector = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int rr = q / p.hpg, hq = q % p.hpg;
+    constexpr int HH = HD / 2;                           // features per half
+    float* xch = reinterpret_cast<float*>(sm + C::OFF_XCH);
+    int xc = 0;                                          // exchanges so far (slot parity)
     long long T = 0, GR = 0;
     bool dead = false;
     auto fail = [&]() {
       if (lane == 0) abort_now();
       dead = true;
     };
+    // v to the pair's other warp and its value back (bounded wait; on a timeout the
+    // warp is marked dead and the value is its own)
+    auto swap_with_pair = [&](float v) -> float {
+      const int sl = xc & 1;
+      float* slot = xch + sl * 2 * kHM;
+      uint64_t* xb = &bars[B_XCH + quarter * 2 + sl];
+      slot[half * kHM + q] = v;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(xb);
+      const bool ok = __all_sync(kFull, mbar_wait_bounded(xb, (uint32_t)((xc >> 1) & 1), kWaitLimitNs));
+      ++xc;
+      if (!ok) {
+        fail();
+        return v;
+      }
+      return slot[(1 - half) * kHM + q];
+    };
     const int2* exps = reinterpret_cast<const int2*>(p.ops_exp);
-    // Q of unit u into TMEM: q * qmul * 2^-e_q as f16 hi / lo pairs (returns e_q); the
-    // S products of the previous unit are all done when this runs
+    // this half of Q of unit u into TMEM: q * qmul * 2^-e_q as f16 hi / lo pairs
+    // (returns e_q); the S products of the previous unit are all done when this runs
     auto put_q = [&](const Unit& u) -> int {
       const bool q_ok = rr < u.rows_eff && q < p.rows * p.hpg;
-      float x[HD];
-      const float* src = p.q + (((size_t)u.b * p.t + u.r0 + rr) * p.nh + (size_t)u.g * p.hpg + hq) * HD;
+      float x[HH];
+      const float* src =
+          p.q + (((size_t)u.b * p.t + u.r0 + rr) * p.nh + (size_t)u.g * p.hpg + hq) * HD + half * HH;
 #pragma unroll
-      for (int c = 0; c < HD; c += 4) {
+      for (int c = 0; c < HH; c += 4) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q_ok) v = *reinterpret_cast<const float4*>(src + c);
         x[c] = v.x * p.qmul;
@@ -382,17 +423,24 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       }
       float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < HD; ++c) am[c & 3] = fmaxf(am[c & 3], fabsf(x[c]));
-      const float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+      for (int c = 0; c < HH; ++c) am[c & 3] = fmaxf(am[c & 3], fabsf(x[c]));
+      float amax = fmaxf(fmaxf(am[0], am[1]), fmaxf(am[2], am[3]));
+      amax = fmaxf(amax, swap_with_pair(amax));
       const int e = amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : 0;
       const float sq = pow2i(-e);
-#pragma unroll
-      for (int c0 = 0; c0 < HD; c0 += 64) {
+      if constexpr (HH == 64) {
         uint32_t hi[32], lo[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) split_pair(x[c0 + 2 * c] * sq, x[c0 + 2 * c + 1] * sq, hi[c], lo[c]);
-        tc_st32(tmem + lane_off + C::C_QHI + c0 / 2, hi);
-        tc_st32(tmem + lane_off + C::C_QLO + c0 / 2, lo);
+        for (int c = 0; c < 32; ++c) split_pair(x[2 * c] * sq, x[2 * c + 1] * sq, hi[c], lo[c]);
+        tc_st32(tmem + lane_off + C::C_QHI + half * 32, hi);
+        tc_st32(tmem + lane_off + C::C_QLO + half * 32, lo);
+      } else {
+        static_assert(HH == 32, "hd 64 or 128");
+        uint32_t hi[16], lo[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) split_pair(x[2 * c] * sq, x[2 * c + 1] * sq, hi[c], lo[c]);
+        tc_st16(tmem + lane_off + C::C_QHI + half * 16, hi);
+        tc_st16(tmem + lane_off + C::C_QLO + half * 16, lo);
       }
       tc_wait_st();
       tc_fence_before();
@@ -407,6 +455,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       u = load_unit(p, rank, true);
       e_q = put_q(u);
     }
+    if (dead) rank = U;
     for (int k = 0; rank < U && !dead; ++k) {
       if (__any_sync(kFull, *s_abort)) { fail(); break; }
       // the next unit's id now, its meta after the first tile: both arrive during this unit
@@ -422,7 +471,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         p.ws_nsplit[u.b * p.n_rb + u.rb] = 1;
         if (u.rb == 0) p.ws_meta[u.b] = p.meta[u.b];
       }
-      float m_run = -INFINITY, l_run = 0.f;
+      float m_run = -INFINITY, l_run = 0.f;              // l_run: this half's keys
       int E = kZeroExp;
       const int nsb = p.ops_nsb;
       const size_t exp_base = (size_t)u.bg * p.ops_nblk;
@@ -446,29 +495,31 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         }
         if (__any_sync(kFull, *s_abort)) { fail(); break; }
         tc_fence_after();
-        const uint32_t scol = (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN);
-        uint32_t sr[32];
-        tc_ld32(tmem + lane_off + scol, sr);
+        // this half's 16 columns of the tile's S, later its P
+        const uint32_t scol = (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN + half * 16);
+        uint32_t sr[16];
+        tc_ld16(tmem + lane_off + scol, sr);
         tc_wait_ld();
         // window mask; a tile wholly inside this row's window skips it. A sink tile
         // holds sinks j0 .. j0 + 31 (valid below ns), a logical tile keys x0 .. x0 + 31.
         const bool sink_tile = i < nsb;
-        const int j0 = i * kHN;
-        const int x0 = (u.kb0 + i - nsb) * kHN;
-        const bool inside = sink_tile ? q_ok && p.ns - j0 >= kHN : q_ok && x0 >= q_lo && x0 + kHN - 1 <= q_hi;
+        const int j0 = i * kHN + half * 16;
+        const int x0 = (u.kb0 + i - nsb) * kHN + half * 16;
+        const bool inside = sink_tile ? q_ok && p.ns - j0 >= 16 : q_ok && x0 >= q_lo && x0 + 15 <= q_hi;
         const float f = pow2w(e_q + ex.x);                // undoes the Q and K block scales
-        float s[32];
+        float s[16];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 16; ++c) {
           bool v = true;
           if (!inside) v = q_ok && (sink_tile ? j0 + c < p.ns : (x0 + c >= q_lo && x0 + c <= q_hi));
           s[c] = v ? __uint_as_float(sr[c]) * f : -INFINITY;
         }
-        float mx[8];
+        float mx[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) mx[c] = fmaxf(fmaxf(s[c], s[c + 8]), fmaxf(s[c + 16], s[c + 24]));
-        const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 0; c < 4; ++c) mx[c] = fmaxf(fmaxf(s[c], s[c + 4]), fmaxf(s[c + 8], s[c + 12]));
+        float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        tmax = fmaxf(tmax, swap_with_pair(tmax));
+        if (dead) break;
         // The running max m_run moves only when a tile exceeds it by more than
         // kHLazyMax (log2 units): below that p = 2^(s - m_run) <= 2^kHLazyMax, and
         // O and l keep one common scale, so o = O / l is unchanged.
@@ -479,20 +530,20 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         const int E_new = (i == 0 || e_v > E + kVSlack) ? e_v : E;
         const float c2 = i == 0 ? 1.f : pow2w(max(E - E_new, -252));
         const float pscale = pow2i(e_v - E_new + kVHead);   // P = p * 2^(e_v - E + kVHead)
-        uint32_t w[32];                                      // P hi pairs | P lo pairs
+        uint32_t w[16];                                      // 8 hi pairs | 8 lo pairs
         const float mref = m_new == -INFINITY ? 0.f : m_new;   // no valid key yet: every s is -inf, p = 0
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
+        for (int c = 0; c < 16; c += 2) {
           const float p0 = ex2(s[c] - mref);
           const float p1 = ex2(s[c + 1] - mref);
           ps[(c >> 1) & 3] += p0 + p1;
-          split_pair(p0 * pscale, p1 * pscale, w[c / 2], w[16 + c / 2]);
+          split_pair(p0 * pscale, p1 * pscale, w[c / 2], w[8 + c / 2]);
         }
         const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
         l_run = l_run * c1 + psum;
-        tc_st32(tmem + lane_off + scol, w);
-        // O rescale (warp-uniform): O holds P V of tiles < i; wait for the last of them
+        tc_st16(tmem + lane_off + scol, w);
+        // O rescale (warp-uniform; the pair decides alike): O holds P V of tiles < i
         const float c = c1 * c2;
         if (i > 0 && __any_sync(kFull, c != 1.f && m_run != -INFINITY)) {
           const long long tp = t - 1;
@@ -502,7 +553,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
             break;
           }
           tc_fence_after();
-          for (int c0 = 0; c0 < HD; c0 += 32) {
+          for (int c0 = half * HH; c0 < half * HH + HH; c0 += 32) {
             uint32_t o[32];
             tc_ld32(tmem + lane_off + C::C_O + c0, o);
             tc_wait_ld();
@@ -528,9 +579,12 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         nu = unit_from(p, nid, nmeta, true);
         e_qn = put_q(nu);
       }
-      // ---- the unit's record: O * 2^(E - kVHead) (unnormalised), m, l
+      if (dead) break;
+      // ---- the unit's record: O * 2^(E - kVHead) (unnormalised), m, l (both halves' keys)
       const size_t item = (size_t)u.bg * p.n_rb + u.rb;
-      float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD;
+      float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD + half * HH;
+      const float l_other = swap_with_pair(l_run);
+      if (dead) break;
       if (u.ntiles > 0) {
         const long long tl = T + u.ntiles - 1;
         if (!__all_sync(kFull, mbar_wait_bounded(&bars[B_PVDONE + (int)(tl & 7)], (uint32_t)((tl >> 3) & 1),
@@ -540,9 +594,9 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         }
         tc_fence_after();
         const float os = pow2w(E - kVHead);
-        for (int c0 = 0; c0 < HD; c0 += 32) {
+        for (int c0 = 0; c0 < HH; c0 += 32) {
           uint32_t o[32];
-          tc_ld32(tmem + lane_off + C::C_O + c0, o);
+          tc_ld32(tmem + lane_off + C::C_O + half * HH + c0, o);
           tc_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
@@ -551,9 +605,9 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
                             __uint_as_float(o[e + 2]) * os, __uint_as_float(o[e + 3]) * os);
         }
       } else {
-        for (int c0 = 0; c0 < HD; c0 += 4) *reinterpret_cast<float4*>(dst + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int c0 = 0; c0 < HH; c0 += 4) *reinterpret_cast<float4*>(dst + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run);
+      if (half == 0) p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run + l_other);
       T += u.ntiles;
       GR += (u.ntiles + kHG - 1) / kHG;
       u = nu;
