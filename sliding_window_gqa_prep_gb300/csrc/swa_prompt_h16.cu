@@ -64,9 +64,10 @@ struct HCfg {
   static constexpr int OFF_KHI = 0, OFF_KLO = 8 * LAND, OFF_VHI = 16 * LAND, OFF_VLO = 16 * LAND + NSV * LAND;
   static constexpr int OFF_BAR = 16 * LAND + 2 * NSV * LAND;
   static constexpr int NBAR = 48;
-  // softmax pair exchange: [2 tile parities][2 halves][128 query vectors] floats
+  // softmax pair exchange: values [2 parities][256 softmax threads], flags [256]
   static constexpr int OFF_XCH = OFF_BAR + NBAR * 8 + 16;
-  static constexpr size_t USED = (size_t)OFF_XCH + 2 * 2 * kHM * 4;
+  static constexpr int OFF_XFLAG = OFF_XCH + 2 * 256 * 4;
+  static constexpr size_t USED = (size_t)OFF_XFLAG + 256 * 4;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
   static_assert(BYTES <= 232448, "227 KB of shared memory per CTA");
@@ -91,7 +92,6 @@ enum : int {
   B_PVDONE = 24,   // [8] MMA commit: P V of tile T % 8 done (V slot T % 4 is free)
   B_QREADY = 32,   // softmax warps (4 arrivals): Q of the next unit in TMEM
   B_FIN = 33,      // MMA commit: every MMA issued is done
-  B_XCH = 34,      // [4 lane quarters x 2 slots] softmax pair exchange (2 arrivals)
 };
 
 // tiles of row block rb: the sink blocks, then logical blocks kb0 .. (len0 + r_last) / 32,
@@ -204,10 +204,10 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     }
     mbar_init(&bars[B_QREADY], 8);
     mbar_init(&bars[B_FIN], 1);
-    for (int k = 0; k < 8; ++k) mbar_init(&bars[B_XCH + k], 2);
     mbar_fence_init();
     *s_abort = 0;
   }
+  if (tid < 256) reinterpret_cast<uint32_t*>(sm + C::OFF_XFLAG)[tid] = 0;
   if (warp == 0) tc_alloc(const_cast<uint32_t*>(s_tmem), C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -294,6 +294,11 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     long long T = 0, GR = 0;
     long long last0 = 0, last1 = 0;  // last tile of the latest group in S buffer 0 / 1
     bool ok = true;
+    // shared-memory descriptors as a base plus (byte offset >> 4): every operand lies in
+    // this CTA's window (< 2^18 bytes), so the 14-bit address field never carries. The
+    // issuing lane shares its scheduler with softmax warps: few instructions per MMA.
+    const uint64_t kd0 = smem_desc(sm, 128, C::K_SBO);
+    const uint64_t vd0 = smem_desc(sm, 128, C::V_SBO);
     // S of group gr (K half gr & 1 into S buffer gr & 1): Q_lo K_hi + Q_hi K_lo + Q_hi K_hi
     auto issue_s = [&](long long gr) -> bool {
       const int h = (int)(gr & 1);
@@ -306,14 +311,14 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       }
       tc_fence_after();
       const uint32_t d = tmem + (h ? C::C_S1 : C::C_S0);
-#pragma unroll 1
+      const uint64_t kd = kd0 + (uint64_t)((h * kHG * C::LAND) >> 4);
+#pragma unroll
       for (int term = 0; term < 3; ++term) {
-        const uint32_t qcol = term == 0 ? C::C_QLO : C::C_QHI;
-        const unsigned char* kb = sm + (term == 1 ? C::OFF_KLO : C::OFF_KHI) + (size_t)h * kHG * C::LAND;
-        for (int ks = 0; ks < HD / 16; ++ks) {
-          const uint64_t bd = smem_desc(kb + ks * 256, 128, C::K_SBO);
-          tc_mma_f16(d, tmem + qcol + ks * 8, bd, id_s, term > 0 || ks > 0);
-        }
+        const uint32_t qa = tmem + (term == 0 ? C::C_QLO : C::C_QHI);
+        const uint32_t kofs = term == 1 ? C::OFF_KLO : C::OFF_KHI;
+#pragma unroll
+        for (int ks = 0; ks < HD / 16; ++ks)
+          tc_mma_f16(d, qa + ks * 8, kd + ((kofs + ks * 256) >> 4), id_s, term > 0 || ks > 0);
       }
       tc_commit(&bars[B_SFULL + h]);
       return true;
@@ -344,15 +349,15 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         tc_fence_after();
         // O += P_lo V_hi + P_hi V_lo + P_hi V_hi; P of tile i in its S columns: for keys
         // 0-15 and then 16-31, 8 columns of hi pairs and 8 of lo pairs
-        const uint32_t pcol = (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN);
-#pragma unroll 1
+        const uint32_t pa = tmem + (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN);
+        const uint64_t vd = vd0 + (uint64_t)((vs * C::LAND) >> 4);
+#pragma unroll
         for (int term = 0; term < 3; ++term) {
-          const unsigned char* vb = sm + (term == 1 ? C::OFF_VLO : C::OFF_VHI) + (size_t)vs * C::LAND;
-          for (int ks = 0; ks < kHN / 16; ++ks) {
-            const uint64_t bd = smem_desc(vb + ks * 256, 128, C::V_SBO);
-            const uint32_t acol = pcol + ks * 16 + (term == 0 ? 8 : 0);   // keys 16 ks ..: hi | lo
-            tc_mma_f16(tmem + C::C_O, tmem + acol, bd, id_o, i > 0 || term > 0 || ks > 0);
-          }
+          const uint32_t vofs = term == 1 ? C::OFF_VLO : C::OFF_VHI;
+#pragma unroll
+          for (int ks = 0; ks < kHN / 16; ++ks)   // keys 16 ks ..: 8 columns of hi pairs, then 8 of lo pairs
+            tc_mma_f16(tmem + C::C_O, pa + ks * 16 + (term == 0 ? 8 : 0), vd + ((vofs + ks * 256) >> 4), id_o,
+                       i > 0 || term > 0 || ks > 0);
         }
         tc_commit(&bars[B_PVDONE + (int)(t & 7)]);
         if (i % kHG == kHG - 1 || i == u.ntiles - 1) (h ? last1 : last0) = t;
@@ -379,30 +384,35 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int rr = q / p.hpg, hq = q % p.hpg;
     constexpr int HH = HD / 2;                           // features per half
-    float* xch = reinterpret_cast<float*>(sm + C::OFF_XCH);
-    int xc = 0;                                          // exchanges so far (slot parity)
+    float* xval = reinterpret_cast<float*>(sm + C::OFF_XCH);
+    uint32_t* xflag = reinterpret_cast<uint32_t*>(sm + C::OFF_XFLAG);
+    uint32_t xseq = 0;                                   // exchanges so far
     long long T = 0, GR = 0;
     bool dead = false;
     auto fail = [&]() {
       if (lane == 0) abort_now();
       dead = true;
     };
-    // v to the pair's other warp and its value back (bounded wait; on a timeout the
-    // warp is marked dead and the value is its own)
+    // v to the thread of the same query vector in the pair's other warp (softmax thread
+    // tid ^ 128) and its value back: a value slot per parity and a sequence flag per
+    // thread (release / acquire), polled a bounded number of times; on a timeout the
+    // warp is marked dead and the value is its own
     auto swap_with_pair = [&](float v) -> float {
-      const int sl = xc & 1;
-      float* slot = xch + sl * 2 * kHM;
-      uint64_t* xb = &bars[B_XCH + quarter * 2 + sl];
-      slot[half * kHM + q] = v;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(xb);
-      const bool ok = __all_sync(kFull, mbar_wait_bounded(xb, (uint32_t)((xc >> 1) & 1), kWaitLimitNs));
-      ++xc;
-      if (!ok) {
+      ++xseq;
+      float* slot = xval + (xseq & 1) * 256;
+      slot[tid] = v;
+      asm volatile("st.release.cta.shared.u32 [%0], %1;" :: "r"(smem_u32(xflag + tid)), "r"(xseq) : "memory");
+      const uint32_t fa = smem_u32(xflag + (tid ^ 128));
+      uint32_t f = 0;
+      for (int n = 0; n < (1 << 24); ++n) {
+        asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(f) : "r"(fa) : "memory");
+        if (f >= xseq) break;
+      }
+      if (!__all_sync(kFull, f >= xseq)) {
         fail();
         return v;
       }
-      return slot[(1 - half) * kHM + q];
+      return slot[tid ^ 128];
     };
     const int2* exps = reinterpret_cast<const int2*>(p.ops_exp);
     // this half of Q of unit u into TMEM: q * qmul * 2^-e_q as f16 hi / lo pairs
@@ -506,18 +516,23 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         const int j0 = i * kHN + half * 16;
         const int x0 = (u.kb0 + i - nsb) * kHN + half * 16;
         const bool inside = sink_tile ? q_ok && p.ns - j0 >= 16 : q_ok && x0 >= q_lo && x0 + 15 <= q_hi;
-        const float f = pow2w(e_q + ex.x);                // undoes the Q and K block scales
-        float s[16];
+        // f undoes the Q and K block scales (> 0: the sum is clamped at the smallest subnormal)
+        const float f = pow2w(max(e_q + ex.x, -149));
+        float s[16];                                       // scores in block-scaled units, -inf if masked
+        if (__all_sync(kFull, inside)) {
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          bool v = true;
-          if (!inside) v = q_ok && (sink_tile ? j0 + c < p.ns : (x0 + c >= q_lo && x0 + c <= q_hi));
-          s[c] = v ? __uint_as_float(sr[c]) * f : -INFINITY;
+          for (int c = 0; c < 16; ++c) s[c] = __uint_as_float(sr[c]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            const bool v = q_ok && (sink_tile ? j0 + c < p.ns : (x0 + c >= q_lo && x0 + c <= q_hi));
+            s[c] = v ? __uint_as_float(sr[c]) : -INFINITY;
+          }
         }
         float mx[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) mx[c] = fmaxf(fmaxf(s[c], s[c + 4]), fmaxf(s[c + 8], s[c + 12]));
-        float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * f;
         tmax = fmaxf(tmax, swap_with_pair(tmax));
         if (dead) break;
         // The running max m_run moves only when a tile exceeds it by more than
@@ -529,18 +544,23 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         const int e_v = ex.y;
         const int E_new = (i == 0 || e_v > E + kVSlack) ? e_v : E;
         const float c2 = i == 0 ? 1.f : pow2w(max(E - E_new, -252));
-        const float pscale = pow2i(e_v - E_new + kVHead);   // P = p * 2^(e_v - E + kVHead)
-        uint32_t w[16];                                      // 8 hi pairs | 8 lo pairs
+        // P = p * 2^kp with kp = e_v - E + kVHead, as one exp2 of s f - (m - kp). kp is
+        // clamped at -100 (the row sum then keeps every p above 2^-26); a tile with
+        // e_v that far below E holds V values 2^-89 times the largest, whose products
+        // this scales by at most 2^27.
+        const int kp = max(e_v - E_new + kVHead, -100);
         const float mref = m_new == -INFINITY ? 0.f : m_new;   // no valid key yet: every s is -inf, p = 0
+        const float moff = mref - (float)kp;
+        uint32_t w[16];                                      // 8 hi pairs | 8 lo pairs
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int c = 0; c < 16; c += 2) {
-          const float p0 = ex2(s[c] - mref);
-          const float p1 = ex2(s[c + 1] - mref);
+          const float p0 = ex2(fmaf(s[c], f, -moff));
+          const float p1 = ex2(fmaf(s[c + 1], f, -moff));
           ps[(c >> 1) & 3] += p0 + p1;
-          split_pair(p0 * pscale, p1 * pscale, w[c / 2], w[8 + c / 2]);
+          split_pair(p0, p1, w[c / 2], w[8 + c / 2]);
         }
-        const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) * pow2i(-kp);
         l_run = l_run * c1 + psum;
         tc_st16(tmem + lane_off + scol, w);
         // O rescale (warp-uniform; the pair decides alike): O holds P V of tiles < i
