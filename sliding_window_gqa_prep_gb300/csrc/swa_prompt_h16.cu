@@ -64,10 +64,9 @@ struct HCfg {
   static constexpr int OFF_KHI = 0, OFF_KLO = 8 * LAND, OFF_VHI = 16 * LAND, OFF_VLO = 16 * LAND + NSV * LAND;
   static constexpr int OFF_BAR = 16 * LAND + 2 * NSV * LAND;
   static constexpr int NBAR = 48;
-  // softmax pair exchange: values [2 parities][256 softmax threads], flags [256]
+  // softmax pair exchange: one (sequence, value) word per softmax thread
   static constexpr int OFF_XCH = OFF_BAR + NBAR * 8 + 16;
-  static constexpr int OFF_XFLAG = OFF_XCH + 2 * 256 * 4;
-  static constexpr size_t USED = (size_t)OFF_XFLAG + 256 * 4;
+  static constexpr size_t USED = (size_t)OFF_XCH + 256 * 8;
   // at least 116 KB, so that one CTA (and one 512-column TMEM allocation) runs per SM
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
   static_assert(BYTES <= 232448, "227 KB of shared memory per CTA");
@@ -207,7 +206,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     mbar_fence_init();
     *s_abort = 0;
   }
-  if (tid < 256) reinterpret_cast<uint32_t*>(sm + C::OFF_XFLAG)[tid] = 0;
+  if (tid < 256) reinterpret_cast<unsigned long long*>(sm + C::OFF_XCH)[tid] = 0ull;
   if (warp == 0) tc_alloc(const_cast<uint32_t*>(s_tmem), C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
@@ -384,8 +383,8 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int rr = q / p.hpg, hq = q % p.hpg;
     constexpr int HH = HD / 2;                           // features per half
-    float* xval = reinterpret_cast<float*>(sm + C::OFF_XCH);
-    uint32_t* xflag = reinterpret_cast<uint32_t*>(sm + C::OFF_XFLAG);
+    const uint32_t xmine = smem_u32(sm + C::OFF_XCH + tid * 8);
+    const uint32_t xpair = smem_u32(sm + C::OFF_XCH + (tid ^ 128) * 8);
     uint32_t xseq = 0;                                   // exchanges so far
     long long T = 0, GR = 0;
     bool dead = false;
@@ -394,25 +393,28 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       dead = true;
     };
     // v to the thread of the same query vector in the pair's other warp (softmax thread
-    // tid ^ 128) and its value back: a value slot per parity and a sequence flag per
-    // thread (release / acquire), polled a bounded number of times; on a timeout the
-    // warp is marked dead and the value is its own
+    // tid ^ 128) and its value back, as one 64-bit shared word (sequence number, value)
+    // per thread: a single-copy-atomic store and polled loads, no fence (a fence would
+    // wait for this thread's global loads and stores in flight). The partner cannot be
+    // more than one exchange ahead: it waits for this thread's previous word first.
+    // Polled a bounded number of times; on a timeout the warp is marked dead.
     auto swap_with_pair = [&](float v) -> float {
       ++xseq;
-      float* slot = xval + (xseq & 1) * 256;
-      slot[tid] = v;
-      asm volatile("st.release.cta.shared.u32 [%0], %1;" :: "r"(smem_u32(xflag + tid)), "r"(xseq) : "memory");
-      const uint32_t fa = smem_u32(xflag + (tid ^ 128));
-      uint32_t f = 0;
+      const unsigned long long word = ((unsigned long long)xseq << 32) | __float_as_uint(v);
+      asm volatile("st.relaxed.cta.shared.u64 [%0], %1;" :: "r"(xmine), "l"(word) : "memory");
+      uint32_t sq = 0, val = 0;
       for (int n = 0; n < (1 << 24); ++n) {
-        asm volatile("ld.acquire.cta.shared.u32 %0, [%1];" : "=r"(f) : "r"(fa) : "memory");
-        if (f >= xseq) break;
+        unsigned long long got;
+        asm volatile("ld.relaxed.cta.shared.u64 %0, [%1];" : "=l"(got) : "r"(xpair) : "memory");
+        sq = (uint32_t)(got >> 32);
+        val = (uint32_t)got;
+        if (sq >= xseq) break;
       }
-      if (!__all_sync(kFull, f >= xseq)) {
+      if (!__all_sync(kFull, sq >= xseq)) {
         fail();
         return v;
       }
-      return slot[tid ^ 128];
+      return __uint_as_float(val);
     };
     const int2* exps = reinterpret_cast<const int2*>(p.ops_exp);
     // this half of Q of unit u into TMEM: q * qmul * 2^-e_q as f16 hi / lo pairs
@@ -458,11 +460,21 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       if (lane == 0) mbar_arrive(&bars[B_QREADY]);
       return e;
     };
+    // block exponents (e_k, e_v) of tiles base .. base + 31 of unit u, lane l holding tile
+    // base + l (loaded a window ahead, read per tile by shuffle: no global load is in
+    // flight at the per-tile hand-offs)
+    auto exp_window = [&](const Unit& u, int base) -> int2 {
+      const int i = base + lane;
+      if (i >= u.ntiles) return make_int2(0, kZeroExp);
+      return __ldg(exps + (size_t)u.bg * p.ops_nblk + (i >= p.ops_nsb ? i + u.kb0 : i));
+    };
     long long rank = unit_rank(0);
     Unit u{};
     int e_q = 0;
+    int2 exw = make_int2(0, kZeroExp);
     if (rank < U) {
       u = load_unit(p, rank, true);
+      exw = exp_window(u, 0);
       e_q = put_q(u);
     }
     if (dead) rank = U;
@@ -484,20 +496,15 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       float m_run = -INFINITY, l_run = 0.f;              // l_run: this half's keys
       int E = kZeroExp;
       const int nsb = p.ops_nsb;
-      const size_t exp_base = (size_t)u.bg * p.ops_nblk;
-      auto exp_of = [&](int i) -> int2 {
-        if (i >= u.ntiles) return make_int2(0, kZeroExp);
-        return __ldg(exps + exp_base + (i >= nsb ? i + u.kb0 : i));
-      };
-      int2 ex0 = exp_of(0), ex1 = exp_of(1);
+      int2 exn = make_int2(0, kZeroExp);
       for (int i = 0; i < u.ntiles; ++i) {
         const long long t = T + i;
         const int gi = i / kHG;
         const long long gr = GR + gi;
         const int h = (int)(gr & 1);
-        const int2 ex = ex0;
-        ex0 = ex1;
-        ex1 = exp_of(i + 2);
+        if ((i & 31) == 16) exn = exp_window(u, i + 16);
+        if ((i & 31) == 0 && i > 0) exw = exn;
+        const int2 ex = make_int2(__shfl_sync(kFull, exw.x, i & 31), __shfl_sync(kFull, exw.y, i & 31));
         if (i % kHG == 0 &&
             !__all_sync(kFull, mbar_wait_bounded(&bars[B_SFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs))) {
           fail();
@@ -595,8 +602,10 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       // ---- the next unit's Q: its first S products run while this unit's record is written
       Unit nu{};
       int e_qn = 0;
+      int2 exw_n = make_int2(0, kZeroExp);
       if (has_next) {
         nu = unit_from(p, nid, nmeta, true);
+        exw_n = exp_window(nu, 0);
         e_qn = put_q(nu);
       }
       if (dead) break;
@@ -632,6 +641,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       GR += (u.ntiles + kHG - 1) / kHG;
       u = nu;
       e_q = e_qn;
+      exw = exw_n;
       rank = nrank;
     }
   }
