@@ -22,14 +22,17 @@
 // SMs finish close together, and tensor memory, barriers and the pipelines stay
 // up from one unit to the next.
 //
-// CTA = 7 warps:
-//   warps 0-3  one thread per query vector = per TMEM lane: Q of each unit into
-//              TMEM, softmax of its score row, P (f16 hi | lo) written over the
-//              row's own S columns, rare O rescales, the unit's record;
-//   warp 4     K producer: per group of 4 tiles, the K halves (hi, lo) of their
+// CTA = 12 warps:
+//   warps 0-7  two threads per query vector = per TMEM lane (warps w and w + 4 share
+//              lanes 32 (w % 4) .. + 31, each taking half of every tile's keys and half
+//              of the features): Q of each unit into TMEM, softmax of its score row,
+//              P (f16 hi | lo) written over the row's own S columns, rare O rescales,
+//              the unit's record;
+//   warp 8     K producer: per group of 4 tiles, the K halves (hi, lo) of their
 //              split-once blocks as bulk copies into one of two 4-slot halves;
-//   warp 5     one lane issues every tcgen05.mma and tcgen05.commit;
-//   warp 6     V producer: the V^T halves of each tile into one of 4 slots.
+//   warp 9     one lane issues the P V MMAs and their commits;
+//   warp 10    V producer: the V^T halves of each tile into one of 4 slots;
+//   warp 11    one lane issues the S MMAs and their commits.
 // Tensor memory (512 columns at hd 128): Q_hi | Q_lo (f16 pairs, hd/2 columns
 // each) | S buffer 0 | S buffer 1 (128 columns = 4 tiles each) | O (hd). S of a
 // group of 4 tiles is one N = 128 product. Both S buffers are in flight: the MMA
@@ -49,7 +52,7 @@ namespace {
 constexpr int kHM = 128;               // query vectors per unit (MMA M)
 constexpr int kHN = 32;                // keys per tile
 constexpr int kHG = 4;                 // tiles per S product (N = 128)
-constexpr int kHThreads = 11 * 32;
+constexpr int kHThreads = 12 * 32;
 constexpr float kHLazyMax = 8.0f;      // log2 headroom before the running max is raised
 constexpr int kVHead = 4;              // P = p * 2^(e_v - E + kVHead)
 constexpr int kVSlack = 3;             // E is raised when e_v > E + kVSlack (P < 2^15)
@@ -90,7 +93,7 @@ enum : int {
   B_PREADY = 16,   // [8] softmax warps (8 arrivals): P of tile T % 8 written (and O rescaled)
   B_PVDONE = 24,   // [8] MMA commit: P V of tile T % 8 done (V slot T % 4 is free)
   B_QREADY = 32,   // softmax warps (4 arrivals): Q of the next unit in TMEM
-  B_FIN = 33,      // MMA commit: every MMA issued is done
+  B_FIN = 33,      // [2] MMA commits: every MMA issued by the P V / the S lane is done
 };
 
 // tiles of row block rb: the sink blocks, then logical blocks kb0 .. (len0 + r_last) / 32,
@@ -203,6 +206,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     }
     mbar_init(&bars[B_QREADY], 8);
     mbar_init(&bars[B_FIN], 1);
+    mbar_init(&bars[B_FIN + 1], 1);
     mbar_fence_init();
     *s_abort = 0;
   }
@@ -286,58 +290,77 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       mbar_wait_bounded(&bars[B_VFULL + (int)(t2 % C::NSV)], (uint32_t)((t2 / C::NSV) & 1), kWaitLimitNs);
   }
 
-  // ------------------------------------------------------------------ MMA issuer
-  if (warp == 9 && lane == 0) {
+  // ------------------------------------------------------------------ MMA issuers
+  // Two lanes issue the MMAs (an MMA costs its issuing thread about 60 cycles and a
+  // commit about 200, and the issuers share their schedulers with softmax warps): warp
+  // 11 the S products, warp 9 the P V products. They write different accumulators; S
+  // of group g waits for P V of the last tile of group g - 2 (the P it overwrites).
+  // Shared-memory descriptors are a base plus (byte offset >> 4): every operand lies in
+  // this CTA's window (< 2^18 bytes), so the 14-bit address field never carries.
+  if (warp == 11 && lane == 0) {
     const uint32_t id_s = tc_idesc_f16(kHM, kHG * kHN);
-    const uint32_t id_o = tc_idesc_f16(kHM, HD);
+    const uint64_t kd0 = smem_desc(sm, 128, C::K_SBO);
     long long T = 0, GR = 0;
     long long last0 = 0, last1 = 0;  // last tile of the latest group in S buffer 0 / 1
     bool ok = true;
-    // shared-memory descriptors as a base plus (byte offset >> 4): every operand lies in
-    // this CTA's window (< 2^18 bytes), so the 14-bit address field never carries. The
-    // issuing lane shares its scheduler with softmax warps: few instructions per MMA.
-    const uint64_t kd0 = smem_desc(sm, 128, C::K_SBO);
-    const uint64_t vd0 = smem_desc(sm, 128, C::V_SBO);
-    // S of group gr (K half gr & 1 into S buffer gr & 1): Q_lo K_hi + Q_hi K_lo + Q_hi K_hi
-    auto issue_s = [&](long long gr) -> bool {
-      const int h = (int)(gr & 1);
-      if (!mbar_wait_bounded(&bars[B_KFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs) || *s_abort) return false;
-      // the buffer's previous group: every P V done (its last tile's)
-      if (gr >= 2) {
-        const long long tl = h ? last1 : last0;
-        if (!mbar_wait_bounded(&bars[B_PVDONE + (int)(tl & 7)], (uint32_t)((tl >> 3) & 1), kWaitLimitNs) || *s_abort)
-          return false;
-      }
-      tc_fence_after();
-      const uint32_t d = tmem + (h ? C::C_S1 : C::C_S0);
-      const uint64_t kd = kd0 + (uint64_t)((h * kHG * C::LAND) >> 4);
-#pragma unroll
-      for (int term = 0; term < 3; ++term) {
-        const uint32_t qa = tmem + (term == 0 ? C::C_QLO : C::C_QHI);
-        const uint32_t kofs = term == 1 ? C::OFF_KLO : C::OFF_KHI;
-#pragma unroll
-        for (int ks = 0; ks < HD / 16; ++ks)
-          tc_mma_f16(d, qa + ks * 8, kd + ((kofs + ks * 256) >> 4), id_s, term > 0 || ks > 0);
-      }
-      tc_commit(&bars[B_SFULL + h]);
-      return true;
-    };
     for (int k = 0, un = 0; ok; ++k, ++un) {
       const long long rank = unit_rank(k);
       if (rank >= U) break;
       const Unit u = load_unit(p, rank, false);
-      const int ng = (u.ntiles + kHG - 1) / kHG;
       // Q of this unit is in tensor memory (the previous unit's S are all done)
       if (!mbar_wait_bounded(&bars[B_QREADY], (uint32_t)(un & 1), kWaitLimitNs) || *s_abort) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      if (ng > 0) ok = issue_s(GR);
-      if (ok && ng > 1) ok = issue_s(GR + 1);
+      for (int i0 = 0; ok && i0 < u.ntiles; i0 += kHG) {
+        const long long gr = GR + i0 / kHG;
+        const int h = (int)(gr & 1);
+        // S of group gr (K half h into S buffer h): Q_lo K_hi + Q_hi K_lo + Q_hi K_hi
+        if (!mbar_wait_bounded(&bars[B_KFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs) || *s_abort) {
+          ok = false;
+          break;
+        }
+        if (gr >= 2) {
+          const long long tl = h ? last1 : last0;
+          if (!mbar_wait_bounded(&bars[B_PVDONE + (int)(tl & 7)], (uint32_t)((tl >> 3) & 1), kWaitLimitNs) ||
+              *s_abort) {
+            ok = false;
+            break;
+          }
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + (h ? C::C_S1 : C::C_S0);
+        const uint64_t kd = kd0 + (uint64_t)((h * kHG * C::LAND) >> 4);
+#pragma unroll
+        for (int term = 0; term < 3; ++term) {
+          const uint32_t qa = tmem + (term == 0 ? C::C_QLO : C::C_QHI);
+          const uint32_t kofs = term == 1 ? C::OFF_KLO : C::OFF_KHI;
+#pragma unroll
+          for (int ks = 0; ks < HD / 16; ++ks)
+            tc_mma_f16(d, qa + ks * 8, kd + ((kofs + ks * 256) >> 4), id_s, term > 0 || ks > 0);
+        }
+        tc_commit(&bars[B_SFULL + h]);
+        (h ? last1 : last0) = T + min(i0 + kHG, u.ntiles) - 1;
+      }
+      T += u.ntiles;
+      GR += (u.ntiles + kHG - 1) / kHG;
+    }
+    if (!ok) abort_now();
+    tc_commit(&bars[B_FIN + 1]);
+    mbar_wait_bounded(&bars[B_FIN + 1], 0, kWaitLimitNs);
+  }
+  if (warp == 9 && lane == 0) {
+    const uint32_t id_o = tc_idesc_f16(kHM, HD);
+    const uint64_t vd0 = smem_desc(sm, 128, C::V_SBO);
+    long long T = 0, GR = 0;
+    bool ok = true;
+    for (int k = 0; ok; ++k) {
+      const long long rank = unit_rank(k);
+      if (rank >= U) break;
+      const Unit u = load_unit(p, rank, false);
       for (int i = 0; ok && i < u.ntiles; ++i) {
         const long long t = T + i;
-        const int gi = i / kHG, h = (int)((GR + gi) & 1);
+        const int h = (int)((GR + i / kHG) & 1);
         const int vs = (int)(t % C::NSV);
         if (!mbar_wait_bounded(&bars[B_PREADY + (int)(t & 7)], (uint32_t)((t >> 3) & 1), kWaitLimitNs) ||
             *s_abort || !mbar_wait_bounded(&bars[B_VFULL + vs], (uint32_t)((t / C::NSV) & 1), kWaitLimitNs) ||
@@ -354,17 +377,14 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         for (int term = 0; term < 3; ++term) {
           const uint32_t vofs = term == 1 ? C::OFF_VLO : C::OFF_VHI;
 #pragma unroll
-          for (int ks = 0; ks < kHN / 16; ++ks)   // keys 16 ks ..: 8 columns of hi pairs, then 8 of lo pairs
+          for (int ks = 0; ks < kHN / 16; ++ks)
             tc_mma_f16(tmem + C::C_O, pa + ks * 16 + (term == 0 ? 8 : 0), vd + ((vofs + ks * 256) >> 4), id_o,
                        i > 0 || term > 0 || ks > 0);
         }
         tc_commit(&bars[B_PVDONE + (int)(t & 7)]);
-        if (i % kHG == kHG - 1 || i == u.ntiles - 1) (h ? last1 : last0) = t;
-        // S of group gi + 1 once P V of group gi - 1 is done (its buffer)
-        if (i % kHG == 0 && gi >= 1 && gi + 1 < ng) ok = issue_s(GR + gi + 1);
       }
       T += u.ntiles;
-      GR += ng;
+      GR += (u.ntiles + kHG - 1) / kHG;
     }
     if (!ok) abort_now();
     tc_commit(&bars[B_FIN]);
@@ -497,105 +517,126 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       int E = kZeroExp;
       const int nsb = p.ops_nsb;
       int2 exn = make_int2(0, kZeroExp);
-      for (int i = 0; i < u.ntiles; ++i) {
-        const long long t = T + i;
-        const int gi = i / kHG;
-        const long long gr = GR + gi;
+      // one group of (up to) 4 tiles per step: one S wait, one row maximum over the
+      // group (one pair exchange), one running-max / V-exponent decision and at most one
+      // O rescale; then P of each tile and its hand-off to the MMA lane
+      for (int i0 = 0; i0 < u.ntiles; i0 += kHG) {
+        const long long gr = GR + i0 / kHG;
         const int h = (int)(gr & 1);
-        if ((i & 31) == 16) exn = exp_window(u, i + 16);
-        if ((i & 31) == 0 && i > 0) exw = exn;
-        const int2 ex = make_int2(__shfl_sync(kFull, exw.x, i & 31), __shfl_sync(kFull, exw.y, i & 31));
-        if (i % kHG == 0 &&
-            !__all_sync(kFull, mbar_wait_bounded(&bars[B_SFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs))) {
+        const int cnt = min(kHG, u.ntiles - i0);
+        if ((i0 & 31) == 16) exn = exp_window(u, i0 + 16);
+        if ((i0 & 31) == 0 && i0 > 0) exw = exn;
+        if (!__all_sync(kFull, mbar_wait_bounded(&bars[B_SFULL + h], (uint32_t)((gr >> 1) & 1), kWaitLimitNs))) {
           fail();
           break;
         }
         if (__any_sync(kFull, *s_abort)) { fail(); break; }
         tc_fence_after();
-        // this half's 16 columns of the tile's S, later its P
-        const uint32_t scol = (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN + half * 16);
-        uint32_t sr[16];
-        tc_ld16(tmem + lane_off + scol, sr);
+        // this half's 16 columns of each tile's S, later its P (a missing tile's are unused)
+        const uint32_t gcol = (h ? C::C_S1 : C::C_S0) + (uint32_t)(half * 16);
+        uint32_t sr[kHG][16];
+#pragma unroll
+        for (int j = 0; j < kHG; ++j) tc_ld16(tmem + lane_off + gcol + j * kHN, sr[j]);
         tc_wait_ld();
-        // window mask; a tile wholly inside this row's window skips it. A sink tile
-        // holds sinks j0 .. j0 + 31 (valid below ns), a logical tile keys x0 .. x0 + 31.
-        const bool sink_tile = i < nsb;
-        const int j0 = i * kHN + half * 16;
-        const int x0 = (u.kb0 + i - nsb) * kHN + half * 16;
-        const bool inside = sink_tile ? q_ok && p.ns - j0 >= 16 : q_ok && x0 >= q_lo && x0 + 15 <= q_hi;
-        // f undoes the Q and K block scales (> 0: the sum is clamped at the smallest subnormal)
-        const float f = pow2w(max(e_q + ex.x, -149));
-        float s[16];                                       // scores in block-scaled units, -inf if masked
-        if (__all_sync(kFull, inside)) {
+        int ev[kHG];
+        float f[kHG];
+        float gmax = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 16; ++c) s[c] = __uint_as_float(sr[c]);
-        } else {
+        for (int j = 0; j < kHG; ++j) {
+          const int i = i0 + j;
+          const int ek = __shfl_sync(kFull, exw.x, i & 31);
+          ev[j] = __shfl_sync(kFull, exw.y, i & 31);
+          // f undoes the Q and K block scales (> 0: the sum is clamped at the smallest subnormal)
+          f[j] = pow2w(max(e_q + ek, -149));
+          // window mask; a tile wholly inside this row's window skips it. A sink tile
+          // holds sinks j0 .. j0 + 31 (valid below ns), a logical tile keys x0 .. x0 + 31.
+          const bool sink_tile = i < nsb;
+          const int j0 = i * kHN + half * 16;
+          const int x0 = (u.kb0 + i - nsb) * kHN + half * 16;
+          const bool inside =
+              j < cnt && (sink_tile ? q_ok && p.ns - j0 >= 16 : q_ok && x0 >= q_lo && x0 + 15 <= q_hi);
+          if (!__all_sync(kFull, inside)) {
 #pragma unroll
-          for (int c = 0; c < 16; ++c) {
-            const bool v = q_ok && (sink_tile ? j0 + c < p.ns : (x0 + c >= q_lo && x0 + c <= q_hi));
-            s[c] = v ? __uint_as_float(sr[c]) : -INFINITY;
+            for (int c = 0; c < 16; ++c) {
+              const bool v = j < cnt && q_ok && (sink_tile ? j0 + c < p.ns : (x0 + c >= q_lo && x0 + c <= q_hi));
+              if (!v) sr[j][c] = __float_as_uint(-INFINITY);
+            }
           }
-        }
-        float mx[4];
+          float mx[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) mx[c] = fmaxf(fmaxf(s[c], s[c + 4]), fmaxf(s[c + 8], s[c + 12]));
-        float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * f;
-        tmax = fmaxf(tmax, swap_with_pair(tmax));
+          for (int c = 0; c < 4; ++c)
+            mx[c] = fmaxf(fmaxf(__uint_as_float(sr[j][c]), __uint_as_float(sr[j][c + 4])),
+                          fmaxf(__uint_as_float(sr[j][c + 8]), __uint_as_float(sr[j][c + 12])));
+          gmax = fmaxf(gmax, fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * f[j]);
+        }
+        gmax = fmaxf(gmax, swap_with_pair(gmax));
         if (dead) break;
-        // The running max m_run moves only when a tile exceeds it by more than
+        // The running max m_run moves only when the group exceeds it by more than
         // kHLazyMax (log2 units): below that p = 2^(s - m_run) <= 2^kHLazyMax, and
         // O and l keep one common scale, so o = O / l is unchanged.
-        const bool raise = tmax > m_run + kHLazyMax;
-        const float m_new = raise ? tmax : m_run;
+        const bool raise = gmax > m_run + kHLazyMax;
+        const float m_new = raise ? gmax : m_run;
         const float c1 = raise ? ex2(m_run - m_new) : 1.f;
-        const int e_v = ex.y;
-        const int E_new = (i == 0 || e_v > E + kVSlack) ? e_v : E;
-        const float c2 = i == 0 ? 1.f : pow2w(max(E - E_new, -252));
-        // P = p * 2^kp with kp = e_v - E + kVHead, as one exp2 of s f - (m - kp). kp is
-        // clamped at -100 (the row sum then keeps every p above 2^-26); a tile with
-        // e_v that far below E holds V values 2^-89 times the largest, whose products
-        // this scales by at most 2^27.
-        const int kp = max(e_v - E_new + kVHead, -100);
-        const float mref = m_new == -INFINITY ? 0.f : m_new;   // no valid key yet: every s is -inf, p = 0
-        const float moff = mref - (float)kp;
-        uint32_t w[16];                                      // 8 hi pairs | 8 lo pairs
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        // the V exponent after this group's tiles (every e_v <= E_new + kVSlack)
+        int E_new = E;
 #pragma unroll
-        for (int c = 0; c < 16; c += 2) {
-          const float p0 = ex2(fmaf(s[c], f, -moff));
-          const float p1 = ex2(fmaf(s[c + 1], f, -moff));
-          ps[(c >> 1) & 3] += p0 + p1;
-          split_pair(p0, p1, w[c / 2], w[8 + c / 2]);
-        }
-        const float psum = ((ps[0] + ps[1]) + (ps[2] + ps[3])) * pow2i(-kp);
-        l_run = l_run * c1 + psum;
-        tc_st16(tmem + lane_off + scol, w);
-        // O rescale (warp-uniform; the pair decides alike): O holds P V of tiles < i
+        for (int j = 0; j < kHG; ++j)
+          if (j < cnt && (i0 + j == 0 || ev[j] > E_new + kVSlack)) E_new = ev[j];
+        const float c2 = i0 == 0 ? 1.f : pow2w(max(E - E_new, -252));
+        // O rescale (warp-uniform; the pair decides alike): O holds P V of the tiles
+        // before this group, all done first; none of this group's P is handed off yet
         const float c = c1 * c2;
-        if (i > 0 && __any_sync(kFull, c != 1.f && m_run != -INFINITY)) {
-          const long long tp = t - 1;
+        if (i0 > 0 && __any_sync(kFull, c != 1.f && m_run != -INFINITY)) {
+          const long long tp = T + i0 - 1;
           if (!__all_sync(kFull, mbar_wait_bounded(&bars[B_PVDONE + (int)(tp & 7)], (uint32_t)((tp >> 3) & 1),
                                                    kWaitLimitNs))) {
             fail();
             break;
           }
           tc_fence_after();
-          for (int c0 = half * HH; c0 < half * HH + HH; c0 += 32) {
-            uint32_t o[32];
-            tc_ld32(tmem + lane_off + C::C_O + c0, o);
+#pragma unroll 1
+          for (int c0 = half * HH; c0 < half * HH + HH; c0 += 16) {
+            uint32_t o[16];
+            tc_ld16(tmem + lane_off + C::C_O + c0, o);
             tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c);
-            tc_st32(tmem + lane_off + C::C_O + c0, o);
+            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c);
+            tc_st16(tmem + lane_off + C::C_O + c0, o);
           }
         }
+        const float mref = m_new == -INFINITY ? 0.f : m_new;   // no valid key yet: every s is -inf, p = 0
+        float lsum = 0.f;
+#pragma unroll
+        for (int j = 0; j < kHG; ++j) {
+          if (j < cnt) {
+            const long long t = T + i0 + j;
+            // P = p * 2^kp with kp = e_v - E + kVHead, as one exp2 of s f - (m - kp). kp
+            // is clamped at -100 (the row sum then keeps every p above 2^-26); a tile
+            // with e_v that far below E holds V values 2^-89 times the largest, whose
+            // products this scales by at most 2^27.
+            const int kp = max(ev[j] - E_new + kVHead, -100);
+            const float moff = mref - (float)kp;
+            uint32_t w[16];                                      // 8 hi pairs | 8 lo pairs
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int c = 0; c < 16; c += 2) {
+              const float p0 = ex2(fmaf(__uint_as_float(sr[j][c]), f[j], -moff));
+              const float p1 = ex2(fmaf(__uint_as_float(sr[j][c + 1]), f[j], -moff));
+              ps[(c >> 1) & 3] += p0 + p1;
+              split_pair(p0, p1, w[c / 2], w[8 + c / 2]);
+            }
+            lsum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) * pow2i(-kp);
+            tc_st16(tmem + lane_off + gcol + j * kHN, w);
+            tc_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_PREADY + (int)(t & 7)]);
+          }
+        }
+        l_run = l_run * c1 + lsum;
         m_run = m_new;
         E = E_new;
-        tc_wait_st();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bars[B_PREADY + (int)(t & 7)]);
-        if (i == 0 && has_next) nmeta = p.meta[nid / p.n_rb / p.nk];
+        if (i0 == 0 && has_next) nmeta = p.meta[nid / p.n_rb / p.nk];
       }
       if (dead) break;
       if (u.ntiles == 0 && has_next) nmeta = p.meta[nid / p.n_rb / p.nk];
