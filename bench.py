@@ -96,9 +96,9 @@ def dominant_kernel(w):
     """The attention kernel a workload runs and its source file."""
     path = attention_path(w)
     name = {"decode": "attend_decode_kernel", "verify": "attend_verify_kernel",
-            "prompt": "attend_prompt_kernel", "prompt_tc": "attend_prompt_tc_kernel"}[path]
+            "prompt": "attend_prompt_kernel", "prompt_tc": "attend_prompt_h16_kernel"}[path]
     src = {"decode": "swa_decode.cu", "verify": "swa_verify.cu", "prompt": "swa_prompt.cu",
-           "prompt_tc": "swa_prompt_tc.cu"}[path]
+           "prompt_tc": "swa_prompt_h16.cu"}[path]
     return name, os.path.join(CSRC, src)
 
 
@@ -662,9 +662,11 @@ def run_gpu(args, w, rank, world, local_rank):
                 "peak_kind": "derived: 152 SMs x 128 FP32 FMA/clk x 2 x max SM clock",
                 "kv_gbs": kv_bytes / kern_avg_s / 1e9, "kv_frac_of_hbm": kv_bytes / kern_avg_s / 1e9 / peak}
     else:
+        # f16 hi/lo operands: three kind::f16 products per multiply-add, at the bf16 rate
         roof = {"bound": "tensor", "achieved": 3 * useful_flop / kern_avg_s / 1e12,
-                "peak": pk["tf32_tflops"], "unit": "TFLOP/s",
-                "peak_kind": f"{pk['kind']} bf16 x 1.1/2.25 (nominal TF32/bf16); achieved counts the 3 TF32 products of each multiply-add",
+                "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                "peak_kind": f"{pk['kind']} bf16 (the f16 rate); achieved counts the 3 f16 products of each "
+                             "multiply-add",
                 "useful_tflops": useful_flop / kern_avg_s / 1e12}
     if path == "decode":
         roof["frac_of_nominal_8tbs"] = roof["achieved"] / NOMINAL_HBM_GBS

@@ -167,10 +167,11 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  * swa_attend_workspace_min(args). swa_attend_workspace_size(args) (larger for
  * chunks with at least 128 query vectors per KV head) also holds, for the
  * tensor-core prompt kernel, every KV head's sink and window keys split once
- * into TF32 operand blocks of 32 keys, which the kernel then copies in whole
- * blocks, and the order in which its CTAs take the row blocks (longest
- * first); with less, the kernel splits the keys it stages itself (same
- * results within f32 rounding). ev_start / ev_stop, when non-NULL, are recorded on the
+ * into operand blocks of 32 keys (f16 hi/lo pairs under a power-of-two scale per
+ * block, with the blocks' exponents), which the kernel then copies in whole
+ * blocks, and the order in which its CTAs take the row blocks (longest first);
+ * with less, a TF32 kernel splits the keys it stages itself (same results within
+ * f32 rounding). ev_start / ev_stop, when non-NULL, are recorded on the
  * stream right before and after the main attention kernel (for timing it).
  * gate_ready, when non-NULL, is an event the stream waits for after the
  * attention and before the merge, the only kernel that reads gate: a caller
