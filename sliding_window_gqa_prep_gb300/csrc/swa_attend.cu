@@ -101,10 +101,10 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
     }
     const float inv = 1.0f / dsum;
     float4 o;
-    o.x = t.x * inv / (1.0f + expf(-(gt.x * gs.x)));
-    o.y = t.y * inv / (1.0f + expf(-(gt.y * gs.y)));
-    o.z = t.z * inv / (1.0f + expf(-(gt.z * gs.z)));
-    o.w = t.w * inv / (1.0f + expf(-(gt.w * gs.w)));
+    o.x = gated(t.x, inv, gt.x, gs.x);
+    o.y = gated(t.y, inv, gt.y, gs.y);
+    o.z = gated(t.z, inv, gt.z, gs.z);
+    o.w = gated(t.w, inv, gt.w, gs.w);
     *reinterpret_cast<float4*>(p.out + (size_t)row * HD + d4 * 4) = o;
   }
 }
@@ -172,10 +172,10 @@ __device__ __forceinline__ void merge_elementwise(const AttendParams& p, unsigne
     }
     const float inv = 1.0f / den;
     float4 o;
-    o.x = acc.x * inv / (1.0f + expf(-(gt[k].x * gs[k].x)));
-    o.y = acc.y * inv / (1.0f + expf(-(gt[k].y * gs[k].y)));
-    o.z = acc.z * inv / (1.0f + expf(-(gt[k].z * gs[k].z)));
-    o.w = acc.w * inv / (1.0f + expf(-(gt[k].w * gs[k].w)));
+    o.x = gated(acc.x, inv, gt[k].x, gs[k].x);
+    o.y = gated(acc.y, inv, gt[k].y, gs[k].y);
+    o.z = gated(acc.z, inv, gt[k].z, gs[k].z);
+    o.w = gated(acc.w, inv, gt[k].w, gs[k].w);
     *reinterpret_cast<float4*>(p.out + (size_t)idx * 4) = o;
   }
 }
@@ -351,10 +351,10 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
     const int d4 = c * 32 + lane;
     if (d4 >= D4) continue;
     float4 o;
-    o.x = acc[c].x * inv / (1.0f + expf(-(gt[c].x * gs[c].x)));
-    o.y = acc[c].y * inv / (1.0f + expf(-(gt[c].y * gs[c].y)));
-    o.z = acc[c].z * inv / (1.0f + expf(-(gt[c].z * gs[c].z)));
-    o.w = acc[c].w * inv / (1.0f + expf(-(gt[c].w * gs[c].w)));
+    o.x = gated(acc[c].x, inv, gt[c].x, gs[c].x);
+    o.y = gated(acc[c].y, inv, gt[c].y, gs[c].y);
+    o.z = gated(acc[c].z, inv, gt[c].z, gs[c].z);
+    o.w = gated(acc[c].w, inv, gt[c].w, gs[c].w);
     *reinterpret_cast<float4*>(p.out + (size_t)row * HD + d4 * 4) = o;
   }
 }

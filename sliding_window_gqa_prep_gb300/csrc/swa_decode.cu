@@ -801,10 +801,10 @@ __device__ __forceinline__ void step_body(const AttendParams& p, const StepExtra
     const float4 gs = *reinterpret_cast<const float4*>(s_gs + q * HD + d4 * 4);
     const float inv = 1.0f / L;
     float4 o;
-    o.x = sum.x * inv / (1.0f + expf(-(gt.x * gs.x)));
-    o.y = sum.y * inv / (1.0f + expf(-(gt.y * gs.y)));
-    o.z = sum.z * inv / (1.0f + expf(-(gt.z * gs.z)));
-    o.w = sum.w * inv / (1.0f + expf(-(gt.w * gs.w)));
+    o.x = gated(sum.x, inv, gt.x, gs.x);
+    o.y = gated(sum.y, inv, gt.y, gs.y);
+    o.z = gated(sum.z, inv, gt.z, gs.z);
+    o.w = gated(sum.w, inv, gt.w, gs.w);
     *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) = o;
   }
   const int slot = (int)(((long long)st.head0 + st.len0) % st.W);

@@ -300,6 +300,16 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s per bounded wait
 // soon as all of its own CTAs have started. Without a programmatic dependency
 // (an ordinary launch, another preceding operation) both are no-ops.
 #ifdef __CUDACC__
+// The output gate: o * inv * sigma(g * s) with sigma(x) = 1 / (1 + e^-x) from the MUFU
+// exp2 and reciprocal (relative error about 2^-21; x -> -inf gives 0, x -> inf 1). Every
+// kernel that applies the gate uses this one function, so their results agree bit for bit.
+__device__ __forceinline__ float gated(float o, float inv, float g, float s) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"((g * s) * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return (o * inv) * r;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 #endif
