@@ -1,7 +1,6 @@
-// Device helpers of the f16 hi/lo tensor-core attention kernels (the prompt kernel
-// on split-once operand blocks and the staged kernel that splits its tiles itself):
-// power-of-two block scales, f16 hi/lo pairs, the row-block units a persistent CTA
-// walks and their longest-first order.
+// Device helpers of the f16 hi/lo tensor-core attention kernel on split-once operand
+// blocks: power-of-two block scales, f16 hi/lo pairs, the row-block units a persistent
+// CTA walks and their longest-first order.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -19,15 +18,11 @@ constexpr int kVSlack = 3;             // E is raised when e_v > E + kVSlack (P 
 constexpr int kZeroExp = -127;         // exponent of a block of zeros
 constexpr unsigned kFull = 0xffffffffu;
 
-// Tiles of row block rb. Split-once blocks (STAGED false): the sink blocks, then logical
-// blocks kb0 .. (len0 + r_last) / 32, where kb0 holds the first key of the block's first
-// row's window. Staged keys (STAGED true): the block's key list (its ns sinks, then the
-// logical keys xlo .. len0 + r_last of its rows' windows) cut into tiles of 32.
-template <bool STAGED>
+// Tiles of row block rb: the sink blocks, then logical blocks kb0 .. (len0 + r_last) / 32,
+// where kb0 holds the first key of the block's first row's window
 __device__ __forceinline__ int row_block_tiles(const AttendParams& p, const SeqState& st, int rb) {
   const int r0 = rb * p.rows, r_last = min(r0 + p.rows, p.t) - 1;
   const int xlo = st.len0 + r0 + 1 - min(st.W, st.len0 + r0 + 1);
-  if (STAGED) return (p.ns + st.len0 + r_last - xlo + 1 + kHN - 1) / kHN;
   return p.ops_nsb + (st.len0 + r_last) / kHN - xlo / kHN + 1;
 }
 
@@ -83,7 +78,6 @@ __device__ __forceinline__ long long unit_rank(int k) {
 }
 
 // the unit of row-block id `id` (index (b * nk + g) * n_rb + rb) with its sequence's meta
-template <bool STAGED = false>
 __device__ __forceinline__ Unit unit_from(const AttendParams& p, int id, const swa_meta m, bool report) {
   Unit u;
   u.rb = id % p.n_rb;
@@ -98,29 +92,26 @@ __device__ __forceinline__ Unit unit_from(const AttendParams& p, int id, const s
   u.rows_eff = r_last - u.r0 + 1;
   u.xlo = u.st.len0 + u.r0 + 1 - min(u.st.W, u.st.len0 + u.r0 + 1);
   u.kb0 = u.xlo / kHN;
-  u.ntiles = row_block_tiles<STAGED>(p, u.st, u.rb);
+  u.ntiles = row_block_tiles(p, u.st, u.rb);
   return u;
 }
 
-template <bool STAGED = false>
 __device__ __forceinline__ Unit load_unit(const AttendParams& p, long long rank, bool report) {
   const int id = p.ws_order[rank];
-  return unit_from<STAGED>(p, id, p.meta[id / p.n_rb / p.nk], report);
+  return unit_from(p, id, p.meta[id / p.n_rb / p.nk], report);
 }
 
 // The token path's row blocks ordered by their tile count, longest first, by one CTA
 // of 256 threads (a counting sort; equal counts in any order). Every order gives the
 // same results.
-template <bool STAGED = false>
 __device__ void order_row_blocks_h16(const AttendParams& p) {
   constexpr int kBins = 2048;
   __shared__ int cnt[kBins];
   const int U = p.B * p.nk * p.n_rb;
-  // a row block has at most ops_nblk tiles (split-once blocks) or chunk / 32 + 1 (staged)
-  const int nb = min(kBins, (STAGED ? p.chunk / kHN : p.ops_nblk) + 1);
+  const int nb = min(kBins, p.ops_nblk + 1);   // a row block has at most ops_nblk tiles
   auto key = [&](int u) {                       // bin nb - 1 - tiles: longest first
     const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
-    const int tiles = min(max(row_block_tiles<STAGED>(p, st, u % p.n_rb), 0), nb - 1);
+    const int tiles = min(max(row_block_tiles(p, st, u % p.n_rb), 0), nb - 1);
     return nb - 1 - tiles;
   };
   for (int i = threadIdx.x; i < nb; i += blockDim.x) cnt[i] = 0;
