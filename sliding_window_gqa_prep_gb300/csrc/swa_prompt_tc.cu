@@ -1,7 +1,10 @@
-// Prompt-chunk attention on the 5th-generation tensor cores (tcgen05, TMEM):
-// the GEMM path of "o1c_msl.metal" (cortiq-engine 0.8.79: o1c_gather, o1c_cols,
-// o1c_gmax, o1c_gsoft, o1c_gadd and the engine GEMMs Q K^T and P V they feed)
-// as one flash-style kernel per block of 128 query vectors.
+// Prompt-chunk attention on the 5th-generation tensor cores (tcgen05, TMEM) with
+// TF32 hi/lo operands that the kernel stages and splits itself: the GEMM path of
+// "o1c_msl.metal" (cortiq-engine 0.8.79: o1c_gather, o1c_cols, o1c_gmax, o1c_gsoft,
+// o1c_gadd and the engine GEMMs Q K^T and P V they feed) as one flash-style kernel
+// per block of 128 query vectors. The token path takes it for prompt chunks given
+// the minimum workspace (with room for split-once operand blocks the persistent f16
+// kernel of swa_prompt_h16.cu runs instead); swa_flash takes it always (below).
 //
 // Precision: every operand is split a = a_hi + a_lo with a_hi = a rounded to
 // TF32 and a_lo = (a - a_hi) rounded to TF32; each product is
@@ -57,17 +60,17 @@ template <int HD, int MODE = 0>
 struct TCfg {
   // operand sets behind the split warps (MODE 0 / 1)
   static constexpr int NSETS = 2;
-  // split-once blocks (MODE 2 / 3): separate pools of K (hi, lo) and V^T (hi, lo)
+  // split-once blocks (MODE 2): separate pools of K (hi, lo) and V^T (hi, lo)
   // slots, consecutive K slots adjacent so that one S product spans G tiles
   static constexpr int NSK = HD == 64 ? 8 : 4, NSV = HD == 64 ? 4 : 2;
-  // MODE 2 / 3: S of G consecutive tiles is one product of N = 32 G keys (the MMA
+  // MODE 2: S of G consecutive tiles is one product of N = 32 G keys (the MMA
   // time of S follows its instruction count, not N). At hd 128 the 128 S columns
   // leave no room for P in tensor memory: P (hi, lo) sits in shared memory and is
   // the A operand of P V.
   static constexpr bool PRE = MODE >= 2;
   static constexpr int G = PRE ? (HD == 64 ? 8 : 4) : 1;
   static constexpr bool P_SMEM = PRE && HD == 128;
-  // TMEM columns: Q_hi | Q_lo | S (MODE 0 / 1: buffers S0, S1 of 32; MODE 2 / 3: 32 G) | O | P_hi | P_lo
+  // TMEM columns: Q_hi | Q_lo | S (MODE 0 / 1: buffers S0, S1 of 32; MODE 2: 32 G) | O | P_hi | P_lo
   static constexpr uint32_t SCOLS = PRE ? G * kTN : 2 * kTN;
   static constexpr uint32_t C_QHI = 0, C_QLO = HD, C_S0 = 2 * HD, C_S1 = 2 * HD + kTN;
   static constexpr uint32_t C_O = 2 * HD + SCOLS, C_PHI = 3 * HD + SCOLS, C_PLO = 3 * HD + SCOLS + kTN;
@@ -79,7 +82,7 @@ struct TCfg {
   static constexpr int OFF_LV = 2 * LAND;                   // [2 stages] V landing
   static constexpr int OFF_OPS = 4 * LAND;                  // [NSETS] K_hi, K_lo, V^T_hi, V^T_lo
   static constexpr int SET = 4 * LAND;
-  // MODE 2 / 3 pools: K_hi [NSK], K_lo [NSK], V^T_hi [NSV], V^T_lo [NSV]
+  // MODE 2 pools: K_hi [NSK], K_lo [NSK], V^T_hi [NSV], V^T_lo [NSV]
   static constexpr int OFF_KHI = 0, OFF_KLO = NSK * LAND, OFF_VHI = 2 * NSK * LAND;
   static constexpr int OFF_VLO = (2 * NSK + NSV) * LAND;
   // P_SMEM: P_hi, P_lo after the pools, K-major (rows = query vectors, K = keys)
@@ -105,20 +108,11 @@ __device__ __forceinline__ uint32_t tf32_hi(float x) {
   return r;
 }
 
-// MODE 0 / 3: a row block of the token path (sinks, ring window, chunk rows; split
+// MODE 0: a row block of the token path (sinks, ring window, chunk rows; split
 // record to the workspace). MODE 1 / 2: a row block of one segment of packed
 // q|k|v rows attending all of the segment's rows (swa_flash); blockIdx.z =
 // segment * nk + KV head, and the normalised output is written directly. MODE 2
-// and 3 take split-once operand blocks from p.ops (token path: the sinks' blocks,
-// then blocks of logical keys 32k .. 32k + 31; a row block's tiles are its sink
-// blocks and the logical blocks that hold its window).
-// MODE 3 tiles of row block rb: the sink blocks, then logical blocks kb0 .. (len0 +
-// r_last) / 32, where kb0 holds the first key of the block's first row's window
-__device__ __forceinline__ int tc_row_block_tiles(const AttendParams& p, const SeqState& st, int rb) {
-  const int r0 = rb * p.rows, r_last = min(r0 + p.rows, p.t) - 1;
-  const int xlo = st.len0 + r0 + 1 - min(st.W, st.len0 + r0 + 1);
-  return p.ops_nsb + (st.len0 + r_last) / kTN - xlo / kTN + 1;
-}
+// takes split-once operand blocks of the segment's rows from p.ops.
 
 template <int HD, int MODE>
 __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendParams p) {
@@ -146,13 +140,13 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
   uint64_t* land_empty = bars + 2;   // [2] split warps -> producer (4 arrivals)
   uint64_t* split_done = bars + 4;   // [2 sets] split warps -> MMA (4 arrivals)
   uint64_t* v_free = bars + 12;      // [2 sets] MMA commit (P V of the set done) -> split warps
-  // MODE 2 / 3
+  // MODE 2
   uint64_t* kfull = bars + 0;        // [NSK] K copies landed (bytes)
   uint64_t* kfree = bars + 8;        // [NSK] MMA commit: S that read the slot is done
   uint64_t* vfull = bars + 16;       // [NSV] V copies landed (bytes)
   uint64_t* vfree = bars + 20;       // [NSV] MMA commit: P V that read the slot is done
   uint64_t* s_empty = bars + 25;     // softmax warps: every tile of the group's S read (4 arrivals)
-  // both: S (MODE 0 / 1: [2 buffers]; MODE 2 / 3: one buffer of a tile group)
+  // both: S (MODE 0 / 1: [2 buffers]; MODE 2: one buffer of a tile group)
   uint64_t* s_full = PRESPLIT ? bars + 24 : bars + 8;
   uint64_t* p_ready = PRESPLIT ? bars + 26 : bars + 10;   // softmax warps -> MMA (4 arrivals)
   uint64_t* pv_done = PRESPLIT ? bars + 27 : bars + 11;   // MMA commit -> softmax warps
@@ -161,12 +155,6 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   int rb = blockIdx.y, bg = blockIdx.z;
-  if constexpr (MODE == 3) {
-    // the row blocks run longest first, in the order the split-once pass wrote
-    const int u = p.ws_order[blockIdx.y + (size_t)p.n_rb * blockIdx.z];
-    rb = u % p.n_rb;
-    bg = u / p.n_rb;
-  }
   // MODE 2 launch tail (swa_flash): the last flash_tail units of the 1-D grid run as
   // flash_q pieces each, piece j taking the j-th of flash_q equal runs of the
   // unit's tiles; tail_at numbers the pieces of the tail in launch order
@@ -211,15 +199,10 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     if (g == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
   }
   const int rows_eff = r_last - r0 + 1;
-  // MODE 3 tiles: sink blocks 0 .. nsb - 1, then logical blocks kb0 .. (len0 + r_last) / 32
-  const int nsb = MODE == 3 ? p.ops_nsb : 0;
-  const int kb0 = xlo / kTN;
   // a piece takes tiles tile0 .. tile0 + ntiles - 1 of the unit's ceil(n / 32) (may be none)
   const int nt_all = (n + kTN - 1) / kTN;
   const int tile0 = npiece > 1 ? (int)((long long)piece * nt_all / npiece) : 0;
-  const int ntiles = MODE == 3    ? tc_row_block_tiles(p, st, rb)
-                     : npiece > 1 ? (int)((long long)(piece + 1) * nt_all / npiece) - tile0
-                                  : nt_all;
+  const int ntiles = npiece > 1 ? (int)((long long)(piece + 1) * nt_all / npiece) - tile0 : nt_all;
   const size_t kv_head = (size_t)b * p.nk + g;
 
   if (tid == 0) {
@@ -293,7 +276,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
 
   // ------------------------------------------------------------------ producer
   if (PRESPLIT && (warp == 4 || warp == 6)) {
-    // MODE 2 / 3 producers: warp 4 lands the K half (hi, lo) of tile i's block in K
+    // MODE 2 producers: warp 4 lands the K half (hi, lo) of tile i's block in K
     // slot i % NSK once the S that last read the slot is done; warp 6 (a split warp,
     // idle here) lands the V^T half in V slot i % NSV once its P V is done.
     const bool kside = warp == 4;
@@ -314,7 +297,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       }
       if (__shfl_sync(kTF, *s_abort, 0)) break;
       if (lane == 0) {
-        const int blk = (MODE == 3 && i >= nsb) ? i + kb0 : i + tile0;
+        const int blk = i + tile0;
         const float* src = blocks + (size_t)blk * 4 * (kTN * HD);
         mbar_arrive_expect_tx(&fullb[slot], (uint32_t)(2 * C::LAND));
         bulk_g2s(hi_pool + (size_t)slot * C::LAND, src, (uint32_t)C::LAND, &fullb[slot]);
@@ -389,7 +372,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
 
   // ------------------------------------------------------------------ MMA issuer
   if (PRESPLIT && warp == 5 && lane == 0) {
-    // MODE 2 / 3: S of a group of G tiles (their K slots are adjacent) as one product
+    // MODE 2: S of a group of G tiles (their K slots are adjacent) as one product
     // of N = 32 G keys; S of group g + 1 is issued right after P V of group g's
     // second-to-last tile, so it runs while the softmax warps work on the last one.
     const uint32_t id_s = tc_idesc(kTM, G * kTN);
@@ -609,7 +592,7 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
     for (int i = 0; !dead && i < ntiles; ++i) {
       if (*s_abort) { fail(); break; }
       const int cnt = min(kTN, n - (tile0 + i) * kTN);
-      // S of tile i: MODE 0 / 1 buffer i % 2; MODE 2 / 3 the group's buffer, tile i in
+      // S of tile i: MODE 0 / 1 buffer i % 2; MODE 2 the group's buffer, tile i in
       // its 32 columns i % G
       if (!__all_sync(kTF, mbar_wait_bounded(PRESPLIT ? s_full : &s_full[i & 1],
                                              PRESPLIT ? (uint32_t)((i / G) & 1) : (uint32_t)((i >> 1) & 1),
@@ -631,26 +614,15 @@ __global__ void __launch_bounds__(kTThreads, 1) attend_prompt_tc_kernel(AttendPa
       // window mask; a tile wholly inside this row's window skips it (a whole
       // segment row sees every key of its segment: only the tail is masked)
       const int j0 = (tile0 + i) * kTN;
-      bool inside;
-      // MODE 3: a sink tile holds sinks j0 .. j0 + 31 (valid below ns); a logical tile
-      // holds keys x0 .. x0 + 31, each valid inside the row's window
-      const bool sink_tile = MODE == 3 && i < nsb;
-      const int x0 = (kb0 + i - nsb) * kTN;
-      if constexpr (MODE == 3) {
-        inside = sink_tile ? q_ok && p.ns - j0 >= kTN : q_ok && x0 >= q_lo && x0 + kTN - 1 <= q_hi;
-      } else {
-        inside = FLASH ? q_ok && cnt == kTN
-                       : q_ok && cnt == kTN && j0 >= p.ns && xlo + (j0 - p.ns) >= q_lo &&
-                             xlo + (j0 + kTN - 1 - p.ns) <= q_hi;
-      }
+      const bool inside = FLASH ? q_ok && cnt == kTN
+                                : q_ok && cnt == kTN && j0 >= p.ns && xlo + (j0 - p.ns) >= q_lo &&
+                                      xlo + (j0 + kTN - 1 - p.ns) <= q_hi;
       float tmax = -INFINITY;
       float s[32];
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         bool v = true;
-        if (MODE == 3 && !inside) {
-          v = q_ok && (sink_tile ? j0 + k < p.ns : (x0 + k >= q_lo && x0 + k <= q_hi));
-        } else if (!inside) {
+        if (!inside) {
           const int j = j0 + k;
           v = q_ok && k < cnt;
           if (!FLASH && v && j >= p.ns) {
@@ -906,91 +878,6 @@ __global__ void __launch_bounds__(256) flash_presplit_kernel(AttendParams p) {
   });
 }
 
-// The token path's row blocks ordered by their tile count, longest first, by one CTA
-// of 256 threads (a counting sort; equal counts in any order): the attention
-// kernel's CTA c takes row block ws_order[c], so the CTAs that start last are the
-// shortest and the SMs finish close together. Every order gives the same results.
-__device__ void order_row_blocks(const AttendParams& p) {
-  constexpr int kBins = 2048;
-  __shared__ int cnt[kBins];
-  const int U = p.B * p.nk * p.n_rb;
-  const int nb = min(kBins, p.ops_nblk + 1);   // a row block has at most ops_nblk tiles
-  auto key = [&](int u) {                       // bin nb - 1 - tiles: longest first
-    const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
-    const int tiles = min(max(tc_row_block_tiles(p, st, u % p.n_rb), 0), nb - 1);
-    return nb - 1 - tiles;
-  };
-  for (int i = threadIdx.x; i < nb; i += blockDim.x) cnt[i] = 0;
-  __syncthreads();
-  for (int u = threadIdx.x; u < U; u += blockDim.x) atomicAdd(&cnt[key(u)], 1);
-  __syncthreads();
-  // exclusive prefix over the bins by warp 0: lane l sums bins l * per .. l * per + per - 1
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x, per = (nb + 31) / 32;
-    const int lo = min(lane * per, nb), hi = min(lo + per, nb);
-    int sum = 0;
-    for (int i = lo; i < hi; ++i) sum += cnt[i];
-    int incl = sum;
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, d);
-      if (lane >= d) incl += v;
-    }
-    int run = incl - sum;
-    for (int i = lo; i < hi; ++i) {
-      const int c = cnt[i];
-      cnt[i] = run;
-      run += c;
-    }
-  }
-  __syncthreads();
-  for (int u = threadIdx.x; u < U; u += blockDim.x) p.ws_order[atomicAdd(&cnt[key(u)], 1)] = u;
-}
-
-// Token path: one CTA per (sequence, KV head, block): blocks 0 .. nsb - 1 hold the
-// sinks, block nsb + k the logical keys x = 32k .. 32k + 31 below len0 + t (ring
-// slot (head0 + x) % W for x < len0, chunk row x - len0 after), read before the
-// commit rewrites the ring. The extra row blockIdx.y = B * nk orders the row blocks.
-template <int HD>
-__global__ void __launch_bounds__(256) token_presplit_kernel(AttendParams p) {
-  pdl_trigger();
-  pdl_wait();
-  if (blockIdx.y == (unsigned)(p.B * p.nk)) {
-    if (blockIdx.x == 0) order_row_blocks(p);
-    return;
-  }
-  const int blk = blockIdx.x, bg = blockIdx.y;
-  const int b = bg / p.nk, g = bg % p.nk;
-  const SeqState st = sanitize_state(p.meta[b], p.cap, nullptr);   // the attention reports bad metas
-  const size_t kv_head = (size_t)b * p.nk + g;
-  const bool sink = blk < p.ops_nsb;
-  const int j0 = blk * kTN;                                        // first sink of a sink block
-  const int x0 = (blk - p.ops_nsb) * kTN;                          // first logical key otherwise
-  if (!sink && x0 >= st.len0 + p.t) return;                        // past every row's window
-  uint32_t* dst = reinterpret_cast<uint32_t*>(p.ops + ((size_t)bg * p.ops_nblk + blk) * 4 * (kTN * HD));
-  split_block<HD>(dst, [&](int key, const float** kr, const float** vr) {
-    if (sink) {
-      if (j0 + key < p.ns) {
-        const size_t at = (kv_head * p.ns + j0 + key) * HD;
-        *kr = p.sink_k + at;
-        *vr = p.sink_v + at;
-      }
-      return;
-    }
-    const int x = x0 + key;
-    if (x < st.len0) {
-      int slot = st.head0 + x;
-      if (slot >= st.W) slot -= st.W;
-      const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
-      *kr = p.ring_k + at;
-      *vr = p.ring_v + at;
-    } else if (x < st.len0 + p.t) {
-      const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
-      *kr = p.k_chunk + at;
-      *vr = p.v_chunk + at;
-    }
-  });
-}
-
 template <int HD, int MODE>
 int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   using C = TCfg<HD, MODE>;
@@ -1003,10 +890,9 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
     if (e != cudaSuccess) return cuda_status(e);
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
-  if (MODE >= 2) {
-    const dim3 pgrid((unsigned)p.ops_nblk, (unsigned)(p.B * p.nk + (MODE == 3 ? 1 : 0)));
-    const int rc = finish_launch(MODE == 2 ? launch_pdl(flash_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p)
-                                           : launch_pdl(token_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p));
+  if (MODE == 2) {
+    const dim3 pgrid((unsigned)p.ops_nblk, (unsigned)(p.B * p.nk));
+    const int rc = finish_launch(launch_pdl(flash_presplit_kernel<HD>, pgrid, dim3(256), 0, s, p));
     if (rc != SWA_OK) return rc;
   }
   dim3 grid(1u, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
@@ -1024,8 +910,8 @@ int launch_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t
 
 int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   switch (p.hd) {
-    case 64: return p.ops ? launch_tc<64, 3>(p, s, e0, e1) : launch_tc<64, 0>(p, s, e0, e1);
-    case 128: return p.ops ? launch_tc<128, 3>(p, s, e0, e1) : launch_tc<128, 0>(p, s, e0, e1);
+    case 64: return launch_tc<64, 0>(p, s, e0, e1);
+    case 128: return launch_tc<128, 0>(p, s, e0, e1);
   }
   return SWA_E_SHAPE;
 }
