@@ -710,13 +710,13 @@ def run_gpu(args, w, rank, world, local_rank):
 def flash_recorded_traffic(w):
     """DRAM bytes per launch of swa_flash's kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
-    path = os.path.join(PROFILE_DIR, f"attend_prompt_tc_kernel_{w.name}.md")
+    path = os.path.join(PROFILE_DIR, f"attend_prompt_h16_kernel_{w.name}.md")
     if not os.path.exists(path):
         return None
     text = open(path).read()
     m = re.search(r"traffic_bytes_per_launch\s*[:=]\s*([0-9.eE+]+)", text)
     h = re.search(r"kernel_source_sha256_16\s*[:=]\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != source_hash(os.path.join(CSRC, "swa_prompt_tc.cu")):
+    if not m or not h or h.group(1) != source_hash(os.path.join(CSRC, "swa_prompt_h16.cu")):
         return None
     return float(m.group(1))
 
@@ -821,7 +821,7 @@ def run_flash_gpu(args, w, rank, world, local_rank):
     out = torch.zeros(w.T, w.nh * w.hd, device=dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, device=dev)
-    # the split-once form: each KV head's K/V split into TF32 operand blocks once per call
+    # the split-once form: each KV head's K/V split into f16 hi/lo operand blocks once per call
     ws = torch.empty(swa.flash_workspace_size(w.T, len(w.segs), w.hd, w.nh, w.nk, w.max_len),
                      dtype=torch.uint8, device=dev)
     kw = dict(hd=w.hd, nh=w.nh, nk=w.nk, q_off=w.q_off, k_off=w.k_off, v_off=w.v_off,
@@ -884,23 +884,23 @@ def run_flash_gpu(args, w, rank, world, local_rank):
         return
     pk = peaks()
     kern_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
-    roof = {"bound": "tensor", "achieved": 3 * useful_flop / kern_avg_s / 1e12, "peak": pk["tf32_tflops"],
+    roof = {"bound": "tensor", "achieved": 3 * useful_flop / kern_avg_s / 1e12, "peak": pk["bf16_tflops"],
             "unit": "TFLOP/s",
-            "peak_kind": f"{pk['kind']} bf16 x 1.1/2.25 (nominal TF32/bf16); achieved counts the 3 TF32 "
-                         "products of each multiply-add",
+            "peak_kind": f"{pk['kind']} bf16 (the f16 rate); achieved counts the 3 f16 products of each "
+                         "multiply-add",
             "useful_tflops": useful_flop / kern_avg_s / 1e12}
-    roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": "attend_prompt_tc_kernel (full-sequence)",
+    roof.update({"frac": roof["achieved"] / roof["peak"], "kernel": "attend_prompt_h16_kernel (full-sequence)",
                  "traffic": flash_recorded_traffic(w), "launch_ms_avg": kern_avg_s * 1e3})
     line = {
         "metric": "attended keys/s",
         "value": keys * world / (ms / 1e3 / K),
-        "step": "one swa_flash call: the split-once kernel (K/V into TF32 operand blocks) and the "
-                "attention kernel, L2 flushed before it",
+        "step": "one swa_flash call: the split-once kernel (K/V into f16 hi/lo operand blocks) and the "
+                "persistent attention kernel, L2 flushed before it",
         "unit": "keys/s",
         "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms / K,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32 (3xTF32 tensor-core products, f32 softmax)",
+        "dtype": "f32 (f16 hi/lo tensor-core products under power-of-two block scales, f32 softmax)",
         "data": "synthetic (seeded generator, shapes of the named workload)",
         "config": flash_config(w, world),
         "roofline": roof,

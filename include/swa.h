@@ -406,8 +406,9 @@ int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);
  * every key row of the same segment (no window, no causal mask, no sinks, no
  * gate), q head h reads K/V head h / (nh / nk), scores are multiplied by
  * `scale`, the softmax is max-subtracted in f32 and the value sum is divided by
- * the weight sum. Both products run on the tensor cores as 3xTF32 (f32
- * accuracy), with each K/V block of a KV head staged in shared memory once per
+ * the weight sum. Both products run on the tensor cores with f32 accuracy (f16
+ * hi/lo operands under power-of-two block scales with a workspace, 3xTF32
+ * without), with each K/V block of a KV head staged in shared memory once per
  * 128 query vectors (the rows x query heads of that KV head).
  *
  *   qkv      [T][ld] f32: row r holds q head h at qkv + r*ld + q_off + h*hd and
@@ -428,19 +429,20 @@ int swa_attend_noalloc(const swa_attend_args* args, cudaStream_t stream);
  *   workspace, workspace_bytes  optional device scratch (256-byte aligned) of
  *            at least swa_flash_workspace_size(args) bytes, no initial contents
  *            needed, not shared by calls that overlap on the GPU. With it, a first
- *            kernel splits each KV head's K and V rows into TF32 hi/lo operand
- *            blocks of 32 keys once per call (instead of once per block of
- *            query vectors) and the attention kernel copies them in whole
- *            blocks; without it (NULL), the attention kernel splits the rows it
- *            stages itself. Both give bit-identical outputs, except in a split
- *            launch tail: when the blocks of 128 query vectors (one per SM at
- *            a time) fill at least one wave of the device's SMs and leave a
- *            remainder of at most half a wave, and the workspace has room for
- *            it, the last blocks run as several key ranges each whose partial
- *            sums the last range combines (agreeing within f32 rounding).
+ *            kernel splits each KV head's K and V rows into f16 hi/lo operand
+ *            blocks of 32 keys (each block scaled by a power of two) once per
+ *            call and orders the blocks of 128 query vectors longest first; one
+ *            persistent CTA per SM then walks them, copying operand blocks whole.
+ *            When those blocks leave a last round of at most half the SMs, and
+ *            the workspace has room for it, the last (shortest) blocks run as
+ *            several key ranges each whose partial sums the last range combines.
+ *            Without a workspace (NULL), one CTA per block of query vectors
+ *            splits the rows it stages into TF32 hi/lo itself. Both forms are
+ *            deterministic and agree within f32 rounding.
  * The call allocates nothing. Errors: SWA_E_NULL (qkv, segs or out NULL),
  * SWA_E_SHAPE (sizes, offsets past ld, nh * hd > ldo, nseg < 1, max_len < 1,
- * scale not finite), SWA_E_ALIGN (pointers not 16-byte aligned, workspace not
+ * scale not finite, nseg * nk > 65534, more than 65535 blocks of query vectors
+ * per segment and KV head, or 2^31 of them in all), SWA_E_ALIGN (pointers not 16-byte aligned, workspace not
  * 256-byte aligned, or ld / ldo / offsets not multiples of 4),
  * SWA_E_WORKSPACE (a workspace smaller than needed), SWA_E_CUDA.
  */
@@ -458,10 +460,12 @@ typedef struct swa_flash_args {
   size_t workspace_bytes;
 } swa_flash_args;
 /* Workspace bytes of the split-once form of swa_flash: nseg * nk *
- * ceil(max_len / 32) blocks of 4 x 32 x hd floats, plus, when the launch has a
- * split tail on the current device, its partial records (128 x (hd + 2)
- * floats per key range, at most one range per SM) and counters; 0 for
- * unsupported sizes. Queries the current device's SM count on first use. */
+ * ceil(max_len / 32) blocks of 4 x 32 x hd halves and their two exponents, an
+ * int per block of query vectors (the order), plus, when the launch has a split
+ * tail on the current device, its partial records (128 x (hd + 4) floats per
+ * key range, at most one range per SM) and counters; each part rounded up to
+ * 256 bytes; 0 for unsupported sizes. Queries the current device's SM count on
+ * first use. */
 size_t swa_flash_workspace_size(const swa_flash_args* args);
 int swa_flash(const swa_flash_args* args, cudaStream_t stream);
 

@@ -313,7 +313,9 @@ def flash(qkv: torch.Tensor, segs: torch.Tensor, *, hd: int, nh: int, nk: int, q
     every row of the segment. Returns out [T][ldo] (rows outside every segment
     are left as they were; a new output starts zeroed). With `workspace` (a
     uint8 CUDA tensor of at least flash_workspace_size bytes) each KV head's
-    K/V rows are split into TF32 operand blocks once per call."""
+    K/V rows are split into f16 hi/lo operand blocks once per call and a
+    persistent kernel attends them; without it the kernel splits its own tiles
+    (TF32)."""
     if qkv.dim() != 2:
         raise ValueError("qkv must be [T][ld]")
     T, ld = qkv.shape

@@ -470,11 +470,25 @@ static bool flash_shape_ok(const swa_flash_args* a) {
   return a->nh % a->nk == 0 && a->nh / a->nk <= 32;
 }
 
-// split-once operand blocks: [nseg][nk][ceil(max_len / 32)][4][32][hd] floats
-static size_t ops_bytes(const swa_flash_args* a) {
+// The split-once workspace of swa_flash: f16 operand blocks [nseg][nk][ceil(max_len /
+// 32)] of 4 x 32 x hd halves (K hi, K lo, V^T hi, V^T lo), their exponents (2 ints a
+// block), the unit order (an int per unit), then, optionally, the launch tail's records
+// and counters. Each part starts on a 256-byte boundary.
+struct FlashWs {
+  size_t off_exp = 0, off_order = 0, bytes = 0;
+};
+static FlashWs flash_ws(const swa_flash_args* a) {
+  FlashWs f;
   const size_t nblk = ((size_t)a->max_len + kOpsBlockKeys - 1) / kOpsBlockKeys;
-  return (size_t)a->nseg * a->nk * nblk * 4 * kOpsBlockKeys * a->hd * sizeof(float);
+  const size_t nbg = (size_t)a->nseg * a->nk;
+  const size_t rows = 128 / (a->nh / a->nk);
+  const size_t n_rb = (a->max_len + rows - 1) / rows;
+  f.off_exp = nbg * nblk * 4 * kOpsBlockKeys * a->hd * 2;   // a multiple of 256 bytes
+  f.off_order = f.off_exp + up256(nbg * nblk * 2 * sizeof(int));
+  f.bytes = f.off_order + up256(nbg * n_rb * sizeof(int));
+  return f;
 }
+static size_t ops_bytes(const swa_flash_args* a) { return flash_ws(a).bytes; }
 
 // The tail of a flash launch. The attention runs one CTA (one row block of one
 // segment and KV head, a "unit") per SM at a time; when the units fill at least
@@ -483,8 +497,8 @@ static size_t ops_bytes(const swa_flash_args* a) {
 // by the last piece), so that the last wave keeps every SM busy.
 struct FlashTail {
   int tail = 0, q = 1;
-  size_t rec_bytes = 0;   // piece records [tail * q][128] x (hd + 2) floats
-  size_t bytes = 0;       // + combine counters [tail][4] ints
+  size_t rec_bytes = 0;   // piece records [tail * q] x (128 x hd, then 2 x 128 x 2) floats
+  size_t bytes = 0;       // + combine counters [tail][8] ints
 };
 static FlashTail flash_tail(const swa_flash_args* a) {
   FlashTail ft;
@@ -499,9 +513,8 @@ static FlashTail flash_tail(const swa_flash_args* a) {
   if (units - rem + rem * q >= (1LL << 31)) return ft;
   ft.tail = (int)rem;
   ft.q = (int)q;
-  auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  ft.rec_bytes = up((size_t)rem * q * 128 * (a->hd + 2) * sizeof(float));
-  ft.bytes = ft.rec_bytes + up((size_t)rem * 4 * sizeof(int));
+  ft.rec_bytes = up256((size_t)rem * q * 128 * (a->hd + 4) * sizeof(float));
+  ft.bytes = ft.rec_bytes + up256((size_t)rem * 8 * sizeof(int));
   return ft;
 }
 
@@ -522,7 +535,9 @@ int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   const int hpg = a->nh / a->nk;
   const int rows = 128 / hpg;                   // query vectors of a CTA: rows x hpg <= 128
   const long long n_rb = (a->max_len + rows - 1) / rows;
-  if (n_rb > 65535 || (long long)a->nseg * a->nk > 65535) return SWA_E_SHAPE;
+  // grids: (n_rb, nseg * nk) CTAs, or (blocks, nseg * nk + 1) and one per SM over the units
+  if (n_rb > 65535 || (long long)a->nseg * a->nk > 65534 || n_rb * a->nseg * a->nk >= (1LL << 31))
+    return SWA_E_SHAPE;
   if ((a->ld | a->ldo | a->q_off | a->k_off | a->v_off) & 3) return SWA_E_ALIGN;
   if (!aligned16(a->qkv) || !aligned16(a->out) || (reinterpret_cast<uintptr_t>(a->segs) & 3u))
     return SWA_E_ALIGN;
@@ -540,21 +555,23 @@ int swa_flash(const swa_flash_args* a, cudaStream_t stream) {
   p.qkv = a->qkv; p.segs = a->segs;
   p.T = a->T; p.ld = a->ld; p.q_off = a->q_off; p.k_off = a->k_off; p.v_off = a->v_off; p.ldo = a->ldo;
   p.max_len = a->max_len;
-  p.ops = static_cast<float*>(a->workspace);
   p.ops_nblk = (a->max_len + kOpsBlockKeys - 1) / kOpsBlockKeys;
-  if (a->workspace) {
-    // the split tail when the workspace has room for its records
-    const FlashTail ft = flash_tail(a);
-    const size_t ob = ops_bytes(a);   // a multiple of 512 bytes
-    if (ft.tail > 0 && a->workspace_bytes >= ob + ft.bytes) {
-      unsigned char* ws = static_cast<unsigned char*>(a->workspace);
-      p.flash_tail = ft.tail;
-      p.flash_q = ft.q;
-      p.ws_rec = reinterpret_cast<float*>(ws + ob);
-      p.ws_cnt = reinterpret_cast<int*>(ws + ob + ft.rec_bytes);
-    }
+  p.ops_nsb = 0;
+  if (!a->workspace) return launch_flash_tc(p, stream, a->ev_start, a->ev_stop);   // TF32, in-kernel split
+  // f16 split-once blocks; the split tail when the workspace has room for its records
+  unsigned char* ws = static_cast<unsigned char*>(a->workspace);
+  const FlashWs fw = flash_ws(a);
+  p.ops = reinterpret_cast<float*>(ws);
+  p.ops_exp = reinterpret_cast<int*>(ws + fw.off_exp);
+  p.ws_order = reinterpret_cast<int*>(ws + fw.off_order);
+  const FlashTail ft = flash_tail(a);
+  if (ft.tail > 0 && a->workspace_bytes >= fw.bytes + ft.bytes) {
+    p.flash_tail = ft.tail;
+    p.flash_q = ft.q;
+    p.ws_rec = reinterpret_cast<float*>(ws + fw.bytes);
+    p.ws_cnt = reinterpret_cast<int*>(ws + fw.bytes + ft.rec_bytes);
   }
-  return launch_flash_tc(p, stream, a->ev_start, a->ev_stop);
+  return launch_flash_h16(p, stream, a->ev_start, a->ev_stop);
 }
 
 }  // extern "C"

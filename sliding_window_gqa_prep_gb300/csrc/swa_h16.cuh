@@ -1,6 +1,7 @@
 // Device helpers of the f16 hi/lo tensor-core attention kernel on split-once operand
 // blocks: power-of-two block scales, f16 hi/lo pairs, the row-block units a persistent
-// CTA walks and their longest-first order.
+// CTA walks (token-path row blocks, or row blocks of full-sequence segments and pieces
+// of them) and their longest-first order.
 #pragma once
 #include <cuda_fp16.h>
 
@@ -65,21 +66,89 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
-// A unit: (sequence b, KV head g, row block rb) at rank `rank` of the order
+// A unit: (sequence or segment b, KV head g, row block rb), or one piece of it. Its
+// tiles are operand blocks i >= ops_nsb ? kb0 + i : i (i < ntiles) of (b, g).
 struct Unit {
   int b, g, bg, rb, r0, rows_eff, xlo, kb0, ntiles;
-  SeqState st;
+  SeqState st;                   // token path: the sequence's ring state
+  int s0, len;                   // full-sequence segments: first row and length
+  int piece, npiece, tail_at;    // piece `piece` of npiece; tail_at: its number in the launch tail
 };
 
-// rank of this CTA's k-th unit (boustrophedon over the longest-first order)
+// rank of this CTA's k-th item (boustrophedon over the longest-first order)
 __device__ __forceinline__ long long unit_rank(int k) {
   const long long P = gridDim.x;
   return (long long)k * P + ((k & 1) ? (P - 1 - blockIdx.x) : blockIdx.x);
 }
 
+// An item: a whole unit (the unit of rank urank in the order) or a piece of one. The
+// units of ranks U - flash_tail .. U - 1 (the shortest) run as flash_q pieces each,
+// piece j taking the j-th of flash_q equal runs of the unit's tiles, so that the last
+// round of the persistent CTAs is spread over the whole grid.
+struct ItemRef {
+  long long urank;
+  int piece, npiece, tail_at;
+};
+
+// this CTA's k-th item; false past the last one
+__device__ __forceinline__ bool item_of(const AttendParams& p, long long U, int k, ItemRef& it) {
+  const long long r = unit_rank(k);
+  const long long full = U - p.flash_tail;
+  if (r < full) {
+    it = ItemRef{r, 0, 1, 0};
+    return true;
+  }
+  const long long pc = r - full;
+  if (pc >= (long long)p.flash_tail * p.flash_q) return false;
+  it = ItemRef{full + pc / p.flash_q, (int)(pc % p.flash_q), p.flash_q, (int)pc};
+  return true;
+}
+
+// segment (first row s0, length len) of unit id as (s0, length), the length 0 for a
+// segment past row T or longer than max_len (reported once, by the segment's first
+// unit, when `report`)
+__device__ __forceinline__ int2 flash_segment_check(const AttendParams& p, int id, uint32_t s0, uint32_t len,
+                                                    bool report) {
+  if ((uint64_t)s0 + len > (uint64_t)p.T || len > (uint32_t)p.max_len) {
+    if (report && id % (p.n_rb * p.nk) == 0) set_err(p.err, SWA_DERR_SEGMENT);
+    return make_int2(0, 0);
+  }
+  return make_int2((int)s0, (int)len);
+}
+__device__ __forceinline__ int2 flash_segment(const AttendParams& p, int id, bool report) {
+  const int b = id / p.n_rb / p.nk;
+  return flash_segment_check(p, id, p.segs[2 * b], p.segs[2 * b + 1], report);
+}
+
+// tiles of a full-sequence unit: every key block of its segment, 0 for a row block
+// past the segment's end
+__device__ __forceinline__ int flash_unit_tiles(const AttendParams& p, int rb, int len) {
+  return rb * p.rows < len ? (len + kHN - 1) / kHN : 0;
+}
+
+// the full-sequence unit of id `id` ((segment * nk + g) * n_rb + rb), piece it.piece
+__device__ __forceinline__ Unit flash_unit_from(const AttendParams& p, int id, int2 seg, const ItemRef& it) {
+  Unit u{};
+  u.rb = id % p.n_rb;
+  u.bg = id / p.n_rb;
+  u.b = u.bg / p.nk;
+  u.g = u.bg % p.nk;
+  u.s0 = seg.x;
+  u.len = seg.y;
+  u.r0 = u.rb * p.rows;
+  u.rows_eff = max(0, min(u.r0 + p.rows, u.len) - u.r0);
+  const int n = flash_unit_tiles(p, u.rb, u.len);
+  u.piece = it.piece;
+  u.npiece = it.npiece;
+  u.tail_at = it.tail_at;
+  u.kb0 = (int)((long long)n * it.piece / it.npiece);
+  u.ntiles = (int)((long long)n * (it.piece + 1) / it.npiece) - u.kb0;
+  return u;
+}
+
 // the unit of row-block id `id` (index (b * nk + g) * n_rb + rb) with its sequence's meta
 __device__ __forceinline__ Unit unit_from(const AttendParams& p, int id, const swa_meta m, bool report) {
-  Unit u;
+  Unit u{};
   u.rb = id % p.n_rb;
   u.bg = id / p.n_rb;
   u.b = u.bg / p.nk;
@@ -93,34 +162,43 @@ __device__ __forceinline__ Unit unit_from(const AttendParams& p, int id, const s
   u.xlo = u.st.len0 + u.r0 + 1 - min(u.st.W, u.st.len0 + u.r0 + 1);
   u.kb0 = u.xlo / kHN;
   u.ntiles = row_block_tiles(p, u.st, u.rb);
+  u.npiece = 1;
   return u;
 }
 
-__device__ __forceinline__ Unit load_unit(const AttendParams& p, long long rank, bool report) {
-  const int id = p.ws_order[rank];
-  return unit_from(p, id, p.meta[id / p.n_rb / p.nk], report);
+// this CTA's k-th item as a unit (token-path row block, or full-sequence unit or piece);
+// false past the last item
+template <bool FLASH>
+__device__ __forceinline__ bool unit_at(const AttendParams& p, long long U, int k, bool report, Unit& u) {
+  ItemRef it;
+  if (!item_of(p, U, k, it)) return false;
+  const int id = p.ws_order[it.urank];
+  if constexpr (FLASH)
+    u = flash_unit_from(p, id, flash_segment(p, id, report), it);
+  else
+    u = unit_from(p, id, p.meta[id / p.n_rb / p.nk], report);
+  return true;
 }
 
-// The token path's row blocks ordered by their tile count, longest first, by one CTA
-// of 256 threads (a counting sort; equal counts in any order). Every order gives the
-// same results.
-__device__ void order_row_blocks_h16(const AttendParams& p) {
+// Units 0 .. U - 1 ordered by tile count, longest first, equal counts by index (a
+// stable counting sort by one CTA of 256 threads), into order[0 .. U - 1]; tiles(u) is
+// clamped to [0, nb - 1]. The order is the same on every call.
+template <class Tiles>
+__device__ void order_units_h16(int U, int nb, int* order, Tiles tiles) {
   constexpr int kBins = 2048;
   __shared__ int cnt[kBins];
-  const int U = p.B * p.nk * p.n_rb;
-  const int nb = min(kBins, p.ops_nblk + 1);   // a row block has at most ops_nblk tiles
+  nb = max(1, min(kBins, nb));
   auto key = [&](int u) {                       // bin nb - 1 - tiles: longest first
-    const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
-    const int tiles = min(max(row_block_tiles(p, st, u % p.n_rb), 0), nb - 1);
-    return nb - 1 - tiles;
+    return nb - 1 - min(max(tiles(u), 0), nb - 1);
   };
   for (int i = threadIdx.x; i < nb; i += blockDim.x) cnt[i] = 0;
   __syncthreads();
   for (int u = threadIdx.x; u < U; u += blockDim.x) atomicAdd(&cnt[key(u)], 1);
   __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   // exclusive prefix over the bins by warp 0: lane l sums bins l * per .. l * per + per - 1
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x, per = (nb + 31) / 32;
+  if (warp == 0) {
+    const int per = (nb + 31) / 32;
     const int lo = min(lane * per, nb), hi = min(lo + per, nb);
     int sum = 0;
     for (int i = lo; i < hi; ++i) sum += cnt[i];
@@ -137,7 +215,38 @@ __device__ void order_row_blocks_h16(const AttendParams& p) {
     }
   }
   __syncthreads();
-  for (int u = threadIdx.x; u < U; u += blockDim.x) p.ws_order[atomicAdd(&cnt[key(u)], 1)] = u;
+  // stable scatter: blockDim.x units at a time in index order, one warp after another;
+  // within a warp the lanes of one bin take consecutive places in lane order
+  for (int c0 = 0; c0 < U; c0 += blockDim.x) {
+    const int u = c0 + threadIdx.x;
+    const int k = u < U ? key(u) : -1;
+    const unsigned peers = __match_any_sync(kFull, k);
+    const int before = __popc(peers & ((1u << lane) - 1u));
+    for (int w = 0; w < nw; ++w) {
+      if (warp == w) {
+        const int pos = u < U ? cnt[k] + before : 0;
+        __syncwarp();
+        if (u < U && before == 0) cnt[k] += __popc(peers);
+        if (u < U) order[pos] = u;
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// The token path's row blocks, longest first
+__device__ void order_row_blocks_h16(const AttendParams& p) {
+  order_units_h16(p.B * p.nk * p.n_rb, p.ops_nblk + 1, p.ws_order, [&](int u) {
+    const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
+    return row_block_tiles(p, st, u % p.n_rb);
+  });
+}
+
+// The full-sequence units, longest first (units of longer segments first)
+__device__ void order_flash_units_h16(const AttendParams& p) {
+  order_units_h16(p.B * p.nk * p.n_rb, p.ops_nblk + 1, p.ws_order, [&](int u) {
+    return flash_unit_tiles(p, u % p.n_rb, flash_segment(p, u, false).y);
+  });
 }
 
 }  // namespace h16

@@ -82,19 +82,20 @@ struct AttendParams {
   const float* qkv;
   const uint32_t* segs;       // [B][2]: first row, length
   int T, ld, q_off, k_off, v_off, ldo, max_len;
-  // split-once operand blocks [B][nk][ops_nblk][4][32][hd] (TF32 K hi, K lo, V^T hi,
-  // V^T lo of 32 keys), or null: swa_flash's segment rows, or the token path's
-  // sink blocks then its logical keys 0 .. len0 + t - 1 (tensor-core prompt kernel)
+  // split-once operand blocks [B][nk][ops_nblk] of 32 keys (K hi, K lo, V^T hi, V^T lo;
+  // f16 with ops_exp, TF32 without), or null: swa_flash's segment rows, or the token
+  // path's sink blocks then its logical keys 0 .. len0 + t - 1 (tensor-core prompt kernels)
   float* ops;
   int ops_nblk;               // blocks per (sequence or segment, KV head)
   int ops_nsb;                // token path: sink blocks among them (ceil(ns / 32))
   int flash_tail, flash_q;    // swa_flash: the last flash_tail units run as flash_q pieces each
-  float* ws_rec;              // their records: [tail * q][128] x (O[hd], then (m, l))
-  int* ws_cnt;                // [tail][4] pieces done per unit and softmax warp
-  int* ws_order;              // with ops on the token path: [B * nk * n_rb] row blocks (index
-                              // (b * nk + g) * n_rb + rb), longest first
-  int* ops_exp;               // token path: [B][nk][ops_nblk] x (e_k, e_v), the power-of-two
-                              // exponents of the f16 operand blocks (ops then holds f16 blocks)
+  float* ws_rec;              // their records: [tail * q][128] x (O[hd], then (m, l)) (TF32
+                              // kernel), [tail * q] x (O[128][hd], then [2][128] (m, l)) (f16)
+  int* ws_cnt;                // [tail][4] (TF32) or [tail][8] (f16) pieces done per unit and softmax warp
+  int* ws_order;              // with f16 ops: [B * nk * n_rb] units (index (b * nk + g) * n_rb + rb),
+                              // longest first
+  int* ops_exp;               // [B][nk][ops_nblk] x (e_k, e_v), the power-of-two exponents of
+                              // the f16 operand blocks (ops then holds f16 blocks)
 };
 
 int launch_attend_partial(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
@@ -118,7 +119,10 @@ int launch_attend_prompt_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e
 // prompt-chunk kernel of the token path with split-once f16 operand blocks (a workspace
 // of plan.ws_bytes): persistent, tcgen05 kind::f16, swa_prompt_h16.cu
 int launch_attend_prompt_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
-// the same kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu;
+// the same kernel over whole segments of packed q|k|v rows (swa_flash, p.ops with f16
+// blocks, p.ops_exp, p.ws_order), swa_prompt_h16.cu
+int launch_flash_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
+// the TF32 kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu;
 // with p.ops set it first splits every KV head's K/V rows into operand blocks once
 // (the same holds for launch_attend_prompt_tc on the token path)
 int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);

@@ -22,6 +22,14 @@
 // SMs finish close together, and tensor memory, barriers and the pipelines stay
 // up from one unit to the next.
 //
+// With FLASH the same kernel is swa_flash's full-sequence attention
+// ("egemma2_msl.metal", cortiq-engine 0.8.17: eg_flash64 / eg_flash_staged): a
+// unit is a row block of one segment of packed q|k|v rows, its tiles are every
+// key block of the segment (only the segment's tail is masked), and o = O / l is
+// written straight to the output. When the units leave a short last round, the
+// shortest of them run as pieces (runs of their tiles) whose records the last
+// piece to finish combines.
+//
 // CTA = 12 warps:
 //   warps 0-7  two threads per query vector = per TMEM lane (warps w and w + 4 share
 //              lanes 32 (w % 4) .. + 31, each taking half of every tile's keys and half
@@ -91,7 +99,7 @@ enum : int {
   B_FIN = 33,      // [2] MMA commits: every MMA issued by the P V / the S lane is done
 };
 
-template <int HD>
+template <int HD, bool FLASH>
 __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendParams p) {
   using C = HCfg<HD>;
   pdl_trigger();
@@ -138,13 +146,13 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     long long GR = 0;              // groups issued so far (this CTA)
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const long long rank = unit_rank(k);
-      if (rank >= U) break;
-      const Unit u = load_unit(p, rank, false);
+      Unit u;
+      if (!unit_at<FLASH>(p, U, k, false, u)) break;
       const unsigned char* blocks = ops + (size_t)u.bg * p.ops_nblk * 4 * C::LAND;
       // the unit's Q rows into L2 ahead of the softmax warps (hpg heads of a row are contiguous)
       for (int j = 0; j < u.rows_eff; ++j)
-        bulk_prefetch_l2(p.q + (((size_t)u.b * p.t + u.r0 + j) * p.nh + (size_t)u.g * p.hpg) * HD,
+        bulk_prefetch_l2(FLASH ? p.qkv + (size_t)(u.s0 + u.r0 + j) * p.ld + p.q_off + (size_t)u.g * p.hpg * HD
+                               : p.q + (((size_t)u.b * p.t + u.r0 + j) * p.nh + (size_t)u.g * p.hpg) * HD,
                          (uint32_t)(p.hpg * HD * 4));
       for (int i0 = 0; i0 < u.ntiles; i0 += kHG, ++GR) {
         const int h = (int)(GR & 1);
@@ -177,9 +185,8 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     long long T = 0;               // tiles issued so far
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const long long rank = unit_rank(k);
-      if (rank >= U) break;
-      const Unit u = load_unit(p, rank, false);
+      Unit u;
+      if (!unit_at<FLASH>(p, U, k, false, u)) break;
       const unsigned char* blocks = ops + (size_t)u.bg * p.ops_nblk * 4 * C::LAND;
       for (int i = 0; i < u.ntiles; ++i, ++T) {
         const int slot = (int)(T % C::NSV);
@@ -216,9 +223,8 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     long long last0 = 0, last1 = 0;  // last tile of the latest group in S buffer 0 / 1
     bool ok = true;
     for (int k = 0, un = 0; ok; ++k, ++un) {
-      const long long rank = unit_rank(k);
-      if (rank >= U) break;
-      const Unit u = load_unit(p, rank, false);
+      Unit u;
+      if (!unit_at<FLASH>(p, U, k, false, u)) break;
       // Q of this unit is in tensor memory (the previous unit's S are all done)
       if (!mbar_wait_bounded(&bars[B_QREADY], (uint32_t)(un & 1), kWaitLimitNs) || *s_abort) {
         ok = false;
@@ -267,9 +273,8 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     long long T = 0, GR = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
-      const long long rank = unit_rank(k);
-      if (rank >= U) break;
-      const Unit u = load_unit(p, rank, false);
+      Unit u;
+      if (!unit_at<FLASH>(p, U, k, false, u)) break;
       for (int i = 0; ok && i < u.ntiles; ++i) {
         const long long t = T + i;
         const int h = (int)((GR + i / kHG) & 1);
@@ -355,7 +360,9 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       const bool q_ok = rr < u.rows_eff && q < p.rows * p.hpg;
       float x[HH];
       const float* src =
-          p.q + (((size_t)u.b * p.t + u.r0 + rr) * p.nh + (size_t)u.g * p.hpg + hq) * HD + half * HH;
+          (FLASH ? p.qkv + (size_t)(u.s0 + u.r0 + rr) * p.ld + p.q_off + ((size_t)u.g * p.hpg + hq) * HD
+                 : p.q + (((size_t)u.b * p.t + u.r0 + rr) * p.nh + (size_t)u.g * p.hpg + hq) * HD) +
+          half * HH;
 #pragma unroll
       for (int c = 0; c < HH; c += 4) {
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -400,30 +407,62 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       if (i >= u.ntiles) return make_int2(0, kZeroExp);
       return __ldg(exps + (size_t)u.bg * p.ops_nblk + (i >= p.ops_nsb ? i + u.kb0 : i));
     };
-    long long rank = unit_rank(0);
+    // this half of O times s into dst[0 .. HH - 1] (zeros for a unit without tiles);
+    // `store` false: tensor memory is read (warp-collective) but nothing is written
+    auto store_o = [&](float* dst, bool have_o, float s, bool store) {
+      for (int c0 = 0; c0 < HH; c0 += 32) {
+        uint32_t o[32];
+        if (have_o) {
+          tc_ld32(tmem + lane_off + C::C_O + half * HH + c0, o);
+          tc_wait_ld();
+        }
+        if (store) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            *reinterpret_cast<float4*>(dst + c0 + e) =
+                have_o ? make_float4(__uint_as_float(o[e]) * s, __uint_as_float(o[e + 1]) * s,
+                                     __uint_as_float(o[e + 2]) * s, __uint_as_float(o[e + 3]) * s)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    };
     Unit u{};
     int e_q = 0;
     int2 exw = make_int2(0, kZeroExp);
-    if (rank < U) {
-      u = load_unit(p, rank, true);
+    bool have = unit_at<FLASH>(p, U, 0, true, u);
+    if (have) {
       exw = exp_window(u, 0);
       e_q = put_q(u);
     }
-    if (dead) rank = U;
-    for (int k = 0; rank < U && !dead; ++k) {
+    for (int k = 0; have && !dead; ++k) {
       if (__any_sync(kFull, *s_abort)) { fail(); break; }
-      // the next unit's id now, its meta after the first tile: both arrive during this unit
-      const long long nrank = unit_rank(k + 1);
-      const bool has_next = nrank < U;
-      const int nid = has_next ? p.ws_order[nrank] : 0;
+      // the next item's unit id now, its meta (its segment) after the first tile: both
+      // arrive during this unit
+      ItemRef nit{};
+      const bool has_next = item_of(p, U, k + 1, nit);
+      const int nid = has_next ? p.ws_order[nit.urank] : 0;
       swa_meta nmeta{};
+      uint32_t nseg0 = 0, nseg1 = 0;
+      auto load_next = [&]() {
+        if constexpr (FLASH) {
+          const int b = nid / p.n_rb / p.nk;
+          nseg0 = p.segs[2 * b];
+          nseg1 = p.segs[2 * b + 1];
+        } else {
+          nmeta = p.meta[nid / p.n_rb / p.nk];
+        }
+      };
       const bool q_ok = rr < u.rows_eff && q < p.rows * p.hpg;
       const int r = u.r0 + rr;
-      const int q_lo = u.st.len0 + r + 1 - min(u.st.W, u.st.len0 + r + 1);
-      const int q_hi = u.st.len0 + r;
-      if (u.g == 0 && tid == 0) {
-        p.ws_nsplit[u.b * p.n_rb + u.rb] = 1;
-        if (u.rb == 0) p.ws_meta[u.b] = p.meta[u.b];
+      // this row's keys x: q_lo <= x <= q_hi (its window; for FLASH its whole segment)
+      int q_lo = 0, q_hi = u.len - 1;
+      if constexpr (!FLASH) {
+        q_lo = u.st.len0 + r + 1 - min(u.st.W, u.st.len0 + r + 1);
+        q_hi = u.st.len0 + r;
+        if (u.g == 0 && tid == 0) {
+          p.ws_nsplit[u.b * p.n_rb + u.rb] = 1;
+          if (u.rb == 0) p.ws_meta[u.b] = p.meta[u.b];
+        }
       }
       float m_run = -INFINITY, l_run = 0.f;              // l_run: this half's keys
       int E = kZeroExp;
@@ -548,23 +587,23 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         l_run = l_run * c1 + lsum;
         m_run = m_new;
         E = E_new;
-        if (i0 == 0 && has_next) nmeta = p.meta[nid / p.n_rb / p.nk];
+        if (i0 == 0 && has_next) load_next();
       }
       if (dead) break;
-      if (u.ntiles == 0 && has_next) nmeta = p.meta[nid / p.n_rb / p.nk];
-      // ---- the next unit's Q: its first S products run while this unit's record is written
+      if (u.ntiles == 0 && has_next) load_next();
+      // ---- the next unit's Q: its first S products run while this unit's output is written
       Unit nu{};
       int e_qn = 0;
       int2 exw_n = make_int2(0, kZeroExp);
       if (has_next) {
-        nu = unit_from(p, nid, nmeta, true);
+        if constexpr (FLASH)
+          nu = flash_unit_from(p, nid, flash_segment_check(p, nid, nseg0, nseg1, true), nit);
+        else
+          nu = unit_from(p, nid, nmeta, true);
         exw_n = exp_window(nu, 0);
         e_qn = put_q(nu);
       }
       if (dead) break;
-      // ---- the unit's record: O * 2^(E - kVHead) (unnormalised), m, l (both halves' keys)
-      const size_t item = (size_t)u.bg * p.n_rb + u.rb;
-      float* dst = p.ws_acc + (item * (size_t)p.nq + q) * HD + half * HH;
       const float l_other = swap_with_pair(l_run);
       if (dead) break;
       if (u.ntiles > 0) {
@@ -575,27 +614,73 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
           break;
         }
         tc_fence_after();
-        const float os = pow2w(E - kVHead);
-        for (int c0 = 0; c0 < HH; c0 += 32) {
-          uint32_t o[32];
-          tc_ld32(tmem + lane_off + C::C_O + half * HH + c0, o);
-          tc_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c0 + e) =
-                make_float4(__uint_as_float(o[e]) * os, __uint_as_float(o[e + 1]) * os,
-                            __uint_as_float(o[e + 2]) * os, __uint_as_float(o[e + 3]) * os);
-        }
-      } else {
-        for (int c0 = 0; c0 < HH; c0 += 4) *reinterpret_cast<float4*>(dst + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
-      if (half == 0) p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run + l_other);
+      const float os = pow2w(E - kVHead);                 // O is in units of 2^(E - kVHead)
+      if constexpr (!FLASH) {
+        // ---- the unit's record: O * 2^(E - kVHead) (unnormalised), m, l (both halves' keys)
+        const size_t item = (size_t)u.bg * p.n_rb + u.rb;
+        store_o(p.ws_acc + (item * (size_t)p.nq + q) * HD + half * HH, u.ntiles > 0, os, true);
+        if (half == 0) p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run + l_other);
+      } else {
+        float* dst = p.out + (size_t)(u.s0 + r) * p.ldo + ((size_t)u.g * p.hpg + hq) * HD + half * HH;
+        if (u.npiece == 1) {
+          // ---- o = O / l straight to the output row (a row block past its segment's end
+          // has no tiles and no rows)
+          if (u.ntiles > 0) store_o(dst, true, os / (l_run + l_other), q_ok);
+        } else {
+          // ---- a piece: its record (O, then (m, l) per half) and, by the last piece of
+          // the unit to get here (per softmax warp: its 32 query vectors and half of the
+          // features), the combination of all of them. No wait on another CTA.
+          const size_t rstride = (size_t)kHM * (HD + 4);
+          float* rec = p.ws_rec + (size_t)u.tail_at * rstride;
+          store_o(rec + (size_t)q * HD + half * HH, u.ntiles > 0, os, true);
+          reinterpret_cast<float2*>(rec + (size_t)kHM * HD)[half * kHM + q] =
+              u.ntiles > 0 ? make_float2(m_run, l_run + l_other) : make_float2(-INFINITY, 0.f);
+          __threadfence();
+          __syncwarp();
+          int last = 0;
+          if (lane == 0)
+            last = atomicAdd(p.ws_cnt + (size_t)(u.tail_at / u.npiece) * 8 + warp, 1) == u.npiece - 1;
+          if (__shfl_sync(kFull, last, 0)) {
+            __threadfence();
+            const float* rec0 = p.ws_rec + (size_t)(u.tail_at - u.piece) * rstride;
+            auto ml_of = [&](int j) {
+              return __ldcg(reinterpret_cast<const float2*>(rec0 + j * rstride + (size_t)kHM * HD) + half * kHM + q);
+            };
+            float M = -INFINITY;
+            for (int j = 0; j < u.npiece; ++j) M = fmaxf(M, ml_of(j).x);
+            float den = 0.f;
+            for (int j = 0; j < u.npiece; ++j) {
+              const float2 ml = ml_of(j);
+              if (ml.x != -INFINITY) den += ml.y * exp2f(ml.x - M);   // a piece without keys weighs 0
+            }
+            if (q_ok) {
+              const float inv = 1.0f / den;
+              for (int c = 0; c < HH; c += 4) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < u.npiece; ++j) {
+                  const float2 ml = ml_of(j);
+                  if (ml.x == -INFINITY) continue;
+                  const float w = exp2f(ml.x - M);
+                  const float4 v =
+                      __ldcg(reinterpret_cast<const float4*>(rec0 + j * rstride + (size_t)q * HD + half * HH + c));
+                  acc.x += v.x * w;
+                  acc.y += v.y * w;
+                  acc.z += v.z * w;
+                  acc.w += v.w * w;
+                }
+                *reinterpret_cast<float4*>(dst + c) = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+              }
+            }
+          }
+        }
+      }
       T += u.ntiles;
       GR += (u.ntiles + kHG - 1) / kHG;
       u = nu;
       e_q = e_qn;
       exw = exw_n;
-      rank = nrank;
+      have = has_next;
     }
   }
 
@@ -609,31 +694,15 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
   }
 }
 
-// Split-once operand blocks: one CTA of 256 threads per (sequence, KV head, block).
-// Blocks 0 .. nsb - 1 hold the sinks, block nsb + k the logical keys x = 32k .. 32k + 31
-// below len0 + t (ring slot (head0 + x) % W for x < len0, chunk row x - len0 after),
-// read before the commit rewrites the ring; missing keys are zeros. A block is
-// K_hi | K_lo (keys x features, K-major core matrices: (key / 8) * K_SBO + (f / 8) *
-// 128 + (key % 8) * 16 + (f % 8) * 2 bytes) | V^T_hi | V^T_lo ((f / 8) * V_SBO + (key /
-// 8) * 128 + (f % 8) * 16 + (key % 8) * 2), each f16 of 2^-e times the block's rows;
-// ops_exp holds (e_k, e_v). The extra row blockIdx.y = B * nk orders the row blocks.
-template <int HD>
-__global__ void __launch_bounds__(256) token_presplit_h16_kernel(AttendParams p) {
+// One split-once operand block of 32 keys by a CTA of 256 threads: K_hi | K_lo (keys x
+// features, K-major core matrices: (key / 8) * K_SBO + (f / 8) * 128 + (key % 8) * 16 +
+// (f % 8) * 2 bytes) | V^T_hi | V^T_lo ((f / 8) * V_SBO + (key / 8) * 128 + (f % 8) * 16
+// + (key % 8) * 2), each f16 of 2^-e times the block's rows, into block blk of (sequence
+// or segment, KV head) bg; ops_exp gets (e_k, e_v). fetch(key, kr, vr) points kr / vr at
+// the key's K and V rows, or leaves them null for a missing key (zeros).
+template <int HD, class Fetch>
+__device__ __forceinline__ void split_block_h16(const AttendParams& p, int bg, int blk, Fetch fetch) {
   using C = HCfg<HD>;
-  pdl_trigger();
-  pdl_wait();
-  if (blockIdx.y == (unsigned)(p.B * p.nk)) {
-    if (blockIdx.x == 0) order_row_blocks_h16(p);
-    return;
-  }
-  const int blk = blockIdx.x, bg = blockIdx.y;
-  const int b = bg / p.nk, g = bg % p.nk;
-  const SeqState st = sanitize_state(p.meta[b], p.cap, nullptr);   // the attention reports bad metas
-  const size_t kv_head = (size_t)b * p.nk + g;
-  const bool sink = blk < p.ops_nsb;
-  const int j0 = blk * kHN;                                        // first sink of a sink block
-  const int x0 = (blk - p.ops_nsb) * kHN;                          // first logical key otherwise
-  if (!sink && x0 >= st.len0 + p.t) return;                        // past every row's window
   __shared__ __align__(16) float ks[kHN][HD + 4];
   __shared__ __align__(16) float vs[kHN][HD + 4];
   __shared__ float red[2][8];
@@ -643,26 +712,7 @@ __global__ void __launch_bounds__(256) token_presplit_h16_kernel(AttendParams p)
     const int key = idx / D4, f4 = idx % D4;
     const float* kr = nullptr;
     const float* vr = nullptr;
-    if (sink) {
-      if (j0 + key < p.ns) {
-        const size_t at = (kv_head * p.ns + j0 + key) * HD;
-        kr = p.sink_k + at;
-        vr = p.sink_v + at;
-      }
-    } else {
-      const int x = x0 + key;
-      if (x < st.len0) {
-        int slot = st.head0 + x;
-        if (slot >= st.W) slot -= st.W;
-        const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
-        kr = p.ring_k + at;
-        vr = p.ring_v + at;
-      } else if (x < st.len0 + p.t) {
-        const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
-        kr = p.k_chunk + at;
-        vr = p.v_chunk + at;
-      }
-    }
+    fetch(key, kr, vr);
     float4 kv = make_float4(0.f, 0.f, 0.f, 0.f), vv = kv;
     if (kr) {
       kv = *reinterpret_cast<const float4*>(kr + f4 * 4);
@@ -716,10 +766,84 @@ __global__ void __launch_bounds__(256) token_presplit_h16_kernel(AttendParams p)
   }
 }
 
+// Token path: one CTA per (sequence, KV head, block). Blocks 0 .. nsb - 1 hold the
+// sinks, block nsb + k the logical keys x = 32k .. 32k + 31 below len0 + t (ring slot
+// (head0 + x) % W for x < len0, chunk row x - len0 after), read before the commit
+// rewrites the ring; missing keys are zeros. The extra row blockIdx.y = B * nk orders
+// the row blocks.
 template <int HD>
+__global__ void __launch_bounds__(256) token_presplit_h16_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
+  if (blockIdx.y == (unsigned)(p.B * p.nk)) {
+    if (blockIdx.x == 0) order_row_blocks_h16(p);
+    return;
+  }
+  const int blk = blockIdx.x, bg = blockIdx.y;
+  const int b = bg / p.nk, g = bg % p.nk;
+  const SeqState st = sanitize_state(p.meta[b], p.cap, nullptr);   // the attention reports bad metas
+  const size_t kv_head = (size_t)b * p.nk + g;
+  const bool sink = blk < p.ops_nsb;
+  const int j0 = blk * kHN;                                        // first sink of a sink block
+  const int x0 = (blk - p.ops_nsb) * kHN;                          // first logical key otherwise
+  if (!sink && x0 >= st.len0 + p.t) return;                        // past every row's window
+  split_block_h16<HD>(p, bg, blk, [&](int key, const float*& kr, const float*& vr) {
+    if (sink) {
+      if (j0 + key < p.ns) {
+        const size_t at = (kv_head * p.ns + j0 + key) * HD;
+        kr = p.sink_k + at;
+        vr = p.sink_v + at;
+      }
+    } else {
+      const int x = x0 + key;
+      if (x < st.len0) {
+        int slot = st.head0 + x;
+        if (slot >= st.W) slot -= st.W;
+        const size_t at = (kv_head * p.cap + (size_t)slot) * HD;
+        kr = p.ring_k + at;
+        vr = p.ring_v + at;
+      } else if (x < st.len0 + p.t) {
+        const size_t at = (((size_t)b * p.t + (x - st.len0)) * p.nk + g) * HD;
+        kr = p.k_chunk + at;
+        vr = p.v_chunk + at;
+      }
+    }
+  });
+}
+
+// swa_flash: one CTA per (segment, KV head, block): block k holds the segment's rows
+// 32k .. 32k + 31 (zeros past its end). The extra row blockIdx.y = nseg * nk orders the
+// units and clears the combine counters of the launch tail.
+template <int HD>
+__global__ void __launch_bounds__(256) flash_presplit_h16_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
+  if (blockIdx.y == (unsigned)(p.B * p.nk)) {
+    if (blockIdx.x == 0) {
+      for (int i = threadIdx.x; i < 8 * p.flash_tail; i += blockDim.x) p.ws_cnt[i] = 0;
+      order_flash_units_h16(p);
+    }
+    return;
+  }
+  const int blk = blockIdx.x, bg = blockIdx.y;
+  const int g = bg % p.nk;
+  const int2 seg = flash_segment(p, bg * p.n_rb, false);           // the attention reports bad segments
+  const int j0 = blk * kHN;
+  if (j0 >= seg.y) return;
+  const int cnt = min(kHN, seg.y - j0);
+  split_block_h16<HD>(p, bg, blk, [&](int key, const float*& kr, const float*& vr) {
+    if (key < cnt) {
+      const float* row = p.qkv + (size_t)(seg.x + j0 + key) * p.ld + (size_t)g * HD;
+      kr = row + p.k_off;
+      vr = row + p.v_off;
+    }
+  });
+}
+
+template <int HD, bool FLASH>
 int launch_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   using C = HCfg<HD>;
-  auto kern = attend_prompt_h16_kernel<HD>;
+  auto kern = attend_prompt_h16_kernel<HD, FLASH>;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
@@ -729,11 +853,13 @@ int launch_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   const dim3 pgrid((unsigned)p.ops_nblk, (unsigned)(p.B * p.nk + 1));
-  int rc = finish_launch(launch_pdl(token_presplit_h16_kernel<HD>, pgrid, dim3(256), 0, s, p));
+  int rc = finish_launch(FLASH ? launch_pdl(flash_presplit_h16_kernel<HD>, pgrid, dim3(256), 0, s, p)
+                               : launch_pdl(token_presplit_h16_kernel<HD>, pgrid, dim3(256), 0, s, p));
   if (rc != SWA_OK) return rc;
-  const long long units = (long long)p.B * p.nk * p.n_rb;
+  // items: whole units, then the launch tail's pieces; one persistent CTA per SM
+  const long long items = (long long)p.B * p.nk * p.n_rb - p.flash_tail + (long long)p.flash_tail * p.flash_q;
   const int sms = num_sms();
-  const unsigned grid = (unsigned)(units < sms ? units : (sms > 0 ? sms : 148));
+  const unsigned grid = (unsigned)(items < sms ? items : (sms > 0 ? sms : 148));
   if (e0) cudaEventRecord(e0, s);
   cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kHThreads), C::BYTES, s, p);
   note_launch();
@@ -746,8 +872,16 @@ int launch_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_
 
 int launch_attend_prompt_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   switch (p.hd) {
-    case 64: return launch_h16<64>(p, s, e0, e1);
-    case 128: return launch_h16<128>(p, s, e0, e1);
+    case 64: return launch_h16<64, false>(p, s, e0, e1);
+    case 128: return launch_h16<128, false>(p, s, e0, e1);
+  }
+  return SWA_E_SHAPE;
+}
+
+int launch_flash_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
+  switch (p.hd) {
+    case 64: return launch_h16<64, true>(p, s, e0, e1);
+    case 128: return launch_h16<128, true>(p, s, e0, e1);
   }
   return SWA_E_SHAPE;
 }

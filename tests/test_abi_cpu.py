@@ -250,10 +250,24 @@ def test_flash_rejects_bad_arguments(lib):
     assert call(_flash(segs=FAKE + 2)) == _abi.SWA_E_ALIGN
 
 
+def _up(x):
+    return (x + 255) // 256 * 256
+
+
+def _flash_ops_bytes(nseg, nh, nk, hd, max_len):
+    """The split-once part of the flash workspace: f16 blocks of 4 x 32 x hd halves,
+    two exponent ints per block, one order int per unit (row block of 128 // group
+    rows), each part rounded up to 256 bytes."""
+    nblk = -(-max_len // 32)
+    units = nseg * nk * -(-max_len // (128 // (nh // nk)))
+    return nseg * nk * nblk * 4 * 32 * hd * 2 + _up(nseg * nk * nblk * 8) + _up(units * 4)
+
+
 def test_flash_workspace_size_and_checks(lib):
     a = _flash()
     need = lib.swa_flash_workspace_size(ctypes.byref(a))
-    assert need == 2 * 4 * 2 * 4 * 32 * 64 * 4          # nseg * nk * ceil(60 / 32) blocks of 4 x 32 x hd floats
+    assert need == 2 * 4 * 2 * 4 * 32 * 64 * 2 + 256 + 256   # 16 blocks of 4 x 32 x hd halves, exponents, order
+    assert need == _flash_ops_bytes(2, 8, 4, 64, 60)
     assert lib.swa_flash_workspace_size(None) == 0
     assert lib.swa_flash_workspace_size(ctypes.byref(_flash(hd=256))) == 0
     call = lambda a: lib.swa_flash(ctypes.byref(a), None)
@@ -263,24 +277,24 @@ def test_flash_workspace_size_and_checks(lib):
 
 def test_flash_workspace_holds_the_split_tail_records(lib):
     # 154 row blocks of 128 (one head) pass one wave of SMs (148 when no GPU is
-    # visible): the size adds the tail pieces' records (128 x (hd + 2) floats each,
+    # visible): the size adds the tail pieces' records (128 x (hd + 4) floats each,
     # at most one per SM) and a 256-byte block of combine counters
     T = 128 * 154
     a = _flash(T=T, nseg=1, nh=1, nk=1, ld=192, q_off=0, k_off=64, v_off=128, ldo=64, max_len=T)
     need = lib.swa_flash_workspace_size(ctypes.byref(a))
-    ops = (T // 32) * 4 * 32 * 64 * 4
-    rec = 128 * (64 + 2) * 4
+    ops = _flash_ops_bytes(1, 1, 1, 64, T)
+    rec = 128 * (64 + 4) * 4
     assert need > ops and (need - ops - 256) % rec == 0 and 0 < (need - ops - 256) // rec <= 152
     # one segment of 128 rows: far from a wave, no records
     b = _flash(T=128, nseg=1, nh=1, nk=1, ld=192, q_off=0, k_off=64, v_off=128, ldo=64, max_len=128)
-    assert lib.swa_flash_workspace_size(ctypes.byref(b)) == (128 // 32) * 4 * 32 * 64 * 4
+    assert lib.swa_flash_workspace_size(ctypes.byref(b)) == _flash_ops_bytes(1, 1, 1, 64, 128)
 
 
 def test_flash_split_tail_rule_over_shapes(lib):
     # the library's rule: with U units (row blocks of 128 query vectors x segments x
     # KV heads) and S SMs (148 when no GPU is visible), U >= S and 0 < U % S <= S / 2
-    # give U % S tail units of S // (U % S) pieces, each with a 128 x (hd + 2)-float
-    # record, plus a 256-byte counter block
+    # give U % S tail units of S // (U % S) pieces, each with a 128 x (hd + 4)-float
+    # record, plus 8 counters per tail unit
     import torch
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else 148
     up = lambda x: (x + 255) // 256 * 256
@@ -291,11 +305,11 @@ def test_flash_split_tail_rule_over_shapes(lib):
         tail = units % sms if units >= sms else 0
         extra = 0
         if 0 < 2 * tail <= sms:
-            extra = up(tail * (sms // tail) * 128 * (hd + 2) * 4) + up(tail * 4 * 4)
+            extra = up(tail * (sms // tail) * 128 * (hd + 4) * 4) + up(tail * 8 * 4)
         ld = (nh + 2 * nk) * hd
         a = _flash(T=max_len * nseg, nseg=nseg, nh=nh, nk=nk, hd=hd, ld=ld, q_off=0, k_off=nh * hd,
                    v_off=(nh + nk) * hd, ldo=nh * hd, max_len=max_len)
-        ops = nseg * nk * -(-max_len // 32) * 4 * 32 * hd * 4
+        ops = _flash_ops_bytes(nseg, nh, nk, hd, max_len)
         assert lib.swa_flash_workspace_size(ctypes.byref(a)) == ops + extra, (nseg, nh, nk, hd, max_len)
 
 
