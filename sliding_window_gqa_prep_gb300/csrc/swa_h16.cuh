@@ -90,16 +90,17 @@ struct ItemRef {
   int piece, npiece, tail_at;
 };
 
-// this CTA's k-th item; false past the last one
+// this CTA's k-th item; false past the last one (the token path has no pieces)
+template <bool FLASH>
 __device__ __forceinline__ bool item_of(const AttendParams& p, long long U, int k, ItemRef& it) {
   const long long r = unit_rank(k);
-  const long long full = U - p.flash_tail;
+  const long long full = FLASH ? U - p.flash_tail : U;
   if (r < full) {
     it = ItemRef{r, 0, 1, 0};
     return true;
   }
   const long long pc = r - full;
-  if (pc >= (long long)p.flash_tail * p.flash_q) return false;
+  if (!FLASH || pc >= (long long)p.flash_tail * p.flash_q) return false;
   it = ItemRef{full + pc / p.flash_q, (int)(pc % p.flash_q), p.flash_q, (int)pc};
   return true;
 }
@@ -171,7 +172,7 @@ __device__ __forceinline__ Unit unit_from(const AttendParams& p, int id, const s
 template <bool FLASH>
 __device__ __forceinline__ bool unit_at(const AttendParams& p, long long U, int k, bool report, Unit& u) {
   ItemRef it;
-  if (!item_of(p, U, k, it)) return false;
+  if (!item_of<FLASH>(p, U, k, it)) return false;
   const int id = p.ws_order[it.urank];
   if constexpr (FLASH)
     u = flash_unit_from(p, id, flash_segment(p, id, report), it);

@@ -89,9 +89,8 @@ struct AttendParams {
   int ops_nblk;               // blocks per (sequence or segment, KV head)
   int ops_nsb;                // token path: sink blocks among them (ceil(ns / 32))
   int flash_tail, flash_q;    // swa_flash: the last flash_tail units run as flash_q pieces each
-  float* ws_rec;              // their records: [tail * q][128] x (O[hd], then (m, l)) (TF32
-                              // kernel), [tail * q] x (O[128][hd], then [2][128] (m, l)) (f16)
-  int* ws_cnt;                // [tail][4] (TF32) or [tail][8] (f16) pieces done per unit and softmax warp
+  float* ws_rec;              // their records: [tail * q] x (O[128][hd], then [2][128] (m, l))
+  int* ws_cnt;                // [tail][8] pieces done per unit and softmax warp
   int* ws_order;              // with f16 ops: [B * nk * n_rb] units (index (b * nk + g) * n_rb + rb),
                               // longest first
   int* ops_exp;               // [B][nk][ops_nblk] x (e_k, e_v), the power-of-two exponents of
@@ -122,9 +121,8 @@ int launch_attend_prompt_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t 
 // the same kernel over whole segments of packed q|k|v rows (swa_flash, p.ops with f16
 // blocks, p.ops_exp, p.ws_order), swa_prompt_h16.cu
 int launch_flash_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
-// the TF32 kernel over whole segments of packed q|k|v rows (swa_flash), swa_prompt_tc.cu;
-// with p.ops set it first splits every KV head's K/V rows into operand blocks once
-// (the same holds for launch_attend_prompt_tc on the token path)
+// the TF32 kernel over whole segments of packed q|k|v rows (swa_flash without a
+// workspace: each CTA splits the rows it stages), swa_prompt_tc.cu
 int launch_flash_tc(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1);
 constexpr int kOpsBlockKeys = 32;   // keys per split-once operand block (= the kernel's key tile)
 // verify kernel (16 or 32 query vectors per CTA, CUDA cores), swa_verify.cu

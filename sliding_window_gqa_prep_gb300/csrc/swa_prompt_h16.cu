@@ -410,20 +410,21 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     // this half of O times s into dst[0 .. HH - 1] (zeros for a unit without tiles);
     // `store` false: tensor memory is read (warp-collective) but nothing is written
     auto store_o = [&](float* dst, bool have_o, float s, bool store) {
-      for (int c0 = 0; c0 < HH; c0 += 32) {
-        uint32_t o[32];
-        if (have_o) {
+      if (have_o) {
+        for (int c0 = 0; c0 < HH; c0 += 32) {
+          uint32_t o[32];
           tc_ld32(tmem + lane_off + C::C_O + half * HH + c0, o);
           tc_wait_ld();
-        }
-        if (store) {
+          if (store) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(dst + c0 + e) =
-                have_o ? make_float4(__uint_as_float(o[e]) * s, __uint_as_float(o[e + 1]) * s,
-                                     __uint_as_float(o[e + 2]) * s, __uint_as_float(o[e + 3]) * s)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(dst + c0 + e) =
+                  make_float4(__uint_as_float(o[e]) * s, __uint_as_float(o[e + 1]) * s,
+                              __uint_as_float(o[e + 2]) * s, __uint_as_float(o[e + 3]) * s);
+          }
         }
+      } else if (store) {
+        for (int c0 = 0; c0 < HH; c0 += 4) *reinterpret_cast<float4*>(dst + c0) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
     };
     Unit u{};
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       // the next item's unit id now, its meta (its segment) after the first tile: both
       // arrive during this unit
       ItemRef nit{};
-      const bool has_next = item_of(p, U, k + 1, nit);
+      const bool has_next = item_of<FLASH>(p, U, k + 1, nit);
       const int nid = has_next ? p.ws_order[nit.urank] : 0;
       swa_meta nmeta{};
       uint32_t nseg0 = 0, nseg1 = 0;
