@@ -66,6 +66,36 @@ __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uin
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// packed pairs of f32 (element 0 in the low half) and their f32x2 arithmetic
+using u64 = unsigned long long;
+__device__ __forceinline__ u64 pack2(float lo, float hi) {
+  u64 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float2 unpack2(u64 v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ u64 fma2(u64 a, u64 b, u64 c) {
+  u64 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
+// split_pair of a packed pair, the remainder x - hi as one packed fma by -1 (exact, as
+// the subtraction)
+__device__ __forceinline__ void split_pair2(u64 x, uint32_t& hi, uint32_t& lo) {
+  const float2 v = unpack2(x);
+  const __half2 h = __floats2half2_rn(v.x, v.y);
+  const float2 f = __half22float2(h);
+  const float2 d = unpack2(fma2(pack2(f.x, f.y), pack2(-1.f, -1.f), x));
+  const __half2 l = __floats2half2_rn(d.x, d.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // A unit: (sequence or segment b, KV head g, row block rb), or one piece of it. Its
 // tiles are operand blocks i >= ops_nsb ? kb0 + i : i (i < ntiles) of (b, g).
 struct Unit {

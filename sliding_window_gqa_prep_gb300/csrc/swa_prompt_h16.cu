@@ -569,15 +569,19 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
             const int kp = max(ev[j] - E_new + kVHead, -100);
             const float moff = mref - (float)kp;
             uint32_t w[16];                                      // 8 hi pairs | 8 lo pairs
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            // two scores per packed f32x2 instruction: the scale FMA, the row sum and the
+            // lo remainder p - hi (an exact fma by -1)
+            const u64 f2 = pack2(f[j], f[j]), m2 = pack2(-moff, -moff);
+            u64 ps2[2] = {0ull, 0ull};
 #pragma unroll
             for (int c = 0; c < 16; c += 2) {
-              const float p0 = ex2(fmaf(__uint_as_float(sr[j][c]), f[j], -moff));
-              const float p1 = ex2(fmaf(__uint_as_float(sr[j][c + 1]), f[j], -moff));
-              ps[(c >> 1) & 3] += p0 + p1;
-              split_pair(p0, p1, w[c / 2], w[8 + c / 2]);
+              const float2 x = unpack2(fma2(pack2(__uint_as_float(sr[j][c]), __uint_as_float(sr[j][c + 1])), f2, m2));
+              const u64 pp = pack2(ex2(x.x), ex2(x.y));
+              ps2[(c >> 1) & 1] = fma2(pp, pack2(1.f, 1.f), ps2[(c >> 1) & 1]);
+              split_pair2(pp, w[c / 2], w[8 + c / 2]);
             }
-            lsum += ((ps[0] + ps[1]) + (ps[2] + ps[3])) * pow2i(-kp);
+            const float2 sa = unpack2(ps2[0]), sb = unpack2(ps2[1]);
+            lsum += ((sa.x + sa.y) + (sb.x + sb.y)) * pow2i(-kp);
             tc_st16(tmem + lane_off + gcol + j * kHN, w);
             tc_wait_st();
             tc_fence_before();
