@@ -30,7 +30,7 @@
 // shortest of them run as pieces (runs of their tiles) whose records the last
 // piece to finish combines.
 //
-// CTA = 12 warps:
+// CTA = 12 warps (13 at hd 64):
 //   warps 0-7  two threads per query vector = per TMEM lane (warps w and w + 4 share
 //              lanes 32 (w % 4) .. + 31, each taking half of every tile's keys and half
 //              of the features): Q of each unit into TMEM, softmax of its score row,
@@ -40,9 +40,12 @@
 //              split-once blocks as bulk copies into one of two 4-slot halves;
 //   warp 9     one lane issues the P V MMAs and their commits;
 //   warp 10    V producer: the V^T halves of each tile into one of 4 slots;
-//   warp 11    one lane issues the S MMAs and their commits.
+//   warp 11    one lane issues the S MMAs and their commits;
+//   warp 12    (hd 64) one lane issues the P V MMAs of the odd tiles of each unit into a
+//              second O accumulator (warp 9 takes the even ones); the epilogue adds them.
 // Tensor memory (512 columns at hd 128): Q_hi | Q_lo (f16 pairs, hd/2 columns
-// each) | S buffer 0 | S buffer 1 (128 columns = 4 tiles each) | O (hd). S of a
+// each) | S buffer 0 | S buffer 1 (128 columns = 4 tiles each) | O (hd; at hd 64 two
+// of them). S of a
 // group of 4 tiles is one N = 128 product. Both S buffers are in flight: the MMA
 // lane issues S of group g + 2 once P V of group g is done, so the tensor cores
 // compute scores two groups ahead, and P V of tile j runs while the softmax warps
@@ -60,7 +63,6 @@ namespace {
 
 using namespace h16;
 
-constexpr int kHThreads = 12 * 32;
 
 template <int HD>
 struct HCfg {
@@ -77,9 +79,14 @@ struct HCfg {
   static constexpr size_t BYTES = USED > 118784 ? USED : 118784;
   static_assert(BYTES <= 232448, "227 KB of shared memory per CTA");
   // TMEM columns
+  // O accumulators: at hd 64 two (tiles of even / odd index within the unit, each issued
+  // by its own P V lane: an N = 64 product costs the issuing thread as much as one of
+  // N = 128, so one lane could not keep up), summed in the epilogue; at hd 128 one
+  static constexpr int NO = HD == 64 ? 2 : 1;
+  static constexpr int THREADS = (12 + NO - 1) * 32;       // warp 12: the second P V lane
   static constexpr uint32_t C_QHI = 0, C_QLO = HD / 2, C_S0 = HD, C_S1 = HD + kHG * kHN, C_O = HD + 2 * kHG * kHN;
   static constexpr uint32_t TMEM_COLS = 512;
-  static_assert(C_O + HD <= TMEM_COLS, "tensor memory budget");
+  static_assert(C_O + NO * HD <= TMEM_COLS, "tensor memory budget");
   // K-major core-matrix layouts (8 rows x 16 bytes): LBO = next core matrix along K, SBO = next 8 rows
   static constexpr uint32_t K_SBO = (HD / 8) * 128;        // K: rows = keys, K = features
   static constexpr uint32_t V_SBO = (kHN / 8) * 128;       // V^T: rows = features, K = keys
@@ -96,11 +103,11 @@ enum : int {
   B_PREADY = 16,   // [8] softmax warps (8 arrivals): P of tile T % 8 written (and O rescaled)
   B_PVDONE = 24,   // [8] MMA commit: P V of tile T % 8 done (V slot T % 4 is free)
   B_QREADY = 32,   // softmax warps (4 arrivals): Q of the next unit in TMEM
-  B_FIN = 33,      // [2] MMA commits: every MMA issued by the P V / the S lane is done
+  B_FIN = 33,      // [3] MMA commits: every MMA issued by the P V lane / the S lane / the second P V lane is done
 };
 
 template <int HD, bool FLASH>
-__global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendParams p) {
+__global__ void __launch_bounds__(HCfg<HD>::THREADS, 1) attend_prompt_h16_kernel(AttendParams p) {
   using C = HCfg<HD>;
   pdl_trigger();
   pdl_wait();
@@ -127,6 +134,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     mbar_init(&bars[B_QREADY], 8);
     mbar_init(&bars[B_FIN], 1);
     mbar_init(&bars[B_FIN + 1], 1);
+    mbar_init(&bars[B_FIN + 2], 1);
     mbar_fence_init();
     *s_abort = 0;
   }
@@ -220,7 +228,10 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     const uint32_t id_s = tc_idesc_f16(kHM, kHG * kHN);
     const uint64_t kd0 = smem_desc(sm, 128, C::K_SBO);
     long long T = 0, GR = 0;
-    long long last0 = 0, last1 = 0;  // last tile of the latest group in S buffer 0 / 1
+    // the latest group in S buffer 0 / 1: its last tile, and the last tile of the other
+    // P V lane in it (the same tile with one lane or a one-tile group); each lane's
+    // commits are in order, so these two cover every P V that reads the buffer's P
+    long long last0 = 0, last1 = 0, prev0 = 0, prev1 = 0;
     bool ok = true;
     for (int k = 0, un = 0; ok; ++k, ++un) {
       Unit u;
@@ -239,8 +250,9 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
           break;
         }
         if (gr >= 2) {
-          const long long tl = h ? last1 : last0;
+          const long long tl = h ? last1 : last0, tp = h ? prev1 : prev0;
           if (!mbar_wait_bounded(&bars[B_PVDONE + (int)(tl & 7)], (uint32_t)((tl >> 3) & 1), kWaitLimitNs) ||
+              !mbar_wait_bounded(&bars[B_PVDONE + (int)(tp & 7)], (uint32_t)((tp >> 3) & 1), kWaitLimitNs) ||
               *s_abort) {
             ok = false;
             break;
@@ -258,7 +270,9 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
             tc_mma_f16(d, qa + ks * 8, kd + ((kofs + ks * 256) >> 4), id_s, term > 0 || ks > 0);
         }
         tc_commit(&bars[B_SFULL + h]);
-        (h ? last1 : last0) = T + min(i0 + kHG, u.ntiles) - 1;
+        const long long tlast = T + min(i0 + kHG, u.ntiles) - 1;
+        (h ? last1 : last0) = tlast;
+        (h ? prev1 : prev0) = C::NO == 2 && min(kHG, u.ntiles - i0) >= 2 ? tlast - 1 : tlast;
       }
       T += u.ntiles;
       GR += (u.ntiles + kHG - 1) / kHG;
@@ -267,15 +281,19 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     tc_commit(&bars[B_FIN + 1]);
     mbar_wait_bounded(&bars[B_FIN + 1], 0, kWaitLimitNs);
   }
-  if (warp == 9 && lane == 0) {
+  // P V lanes: warp 9 (and at hd 64 warp 12) issue the P V products of the unit's tiles
+  // i = lane k, k + NO, ... into accumulator O_k
+  if ((warp == 9 || (C::NO == 2 && warp == 12)) && lane == 0) {
+    const int kl = warp == 9 ? 0 : 1;
     const uint32_t id_o = tc_idesc_f16(kHM, HD);
     const uint64_t vd0 = smem_desc(sm, 128, C::V_SBO);
+    const uint32_t od = tmem + C::C_O + (uint32_t)(kl * HD);
     long long T = 0, GR = 0;
     bool ok = true;
     for (int k = 0; ok; ++k) {
       Unit u;
       if (!unit_at<FLASH>(p, U, k, false, u)) break;
-      for (int i = 0; ok && i < u.ntiles; ++i) {
+      for (int i = kl; ok && i < u.ntiles; i += C::NO) {
         const long long t = T + i;
         const int h = (int)((GR + i / kHG) & 1);
         const int vs = (int)(t % C::NSV);
@@ -286,7 +304,7 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
           break;
         }
         tc_fence_after();
-        // O += P_lo V_hi + P_hi V_lo + P_hi V_hi; P of tile i in its S columns: for keys
+        // O_k += P_lo V_hi + P_hi V_lo + P_hi V_hi; P of tile i in its S columns: for keys
         // 0-15 and then 16-31, 8 columns of hi pairs and 8 of lo pairs
         const uint32_t pa = tmem + (h ? C::C_S1 : C::C_S0) + (uint32_t)((i % kHG) * kHN);
         const uint64_t vd = vd0 + (uint64_t)((vs * C::LAND) >> 4);
@@ -295,8 +313,8 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
           const uint32_t vofs = term == 1 ? C::OFF_VLO : C::OFF_VHI;
 #pragma unroll
           for (int ks = 0; ks < kHN / 16; ++ks)
-            tc_mma_f16(tmem + C::C_O, pa + ks * 16 + (term == 0 ? 8 : 0), vd + ((vofs + ks * 256) >> 4), id_o,
-                       i > 0 || term > 0 || ks > 0);
+            tc_mma_f16(od, pa + ks * 16 + (term == 0 ? 8 : 0), vd + ((vofs + ks * 256) >> 4), id_o,
+                       i >= C::NO || term > 0 || ks > 0);
         }
         tc_commit(&bars[B_PVDONE + (int)(t & 7)]);
       }
@@ -304,8 +322,9 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       GR += (u.ntiles + kHG - 1) / kHG;
     }
     if (!ok) abort_now();
-    tc_commit(&bars[B_FIN]);
-    mbar_wait_bounded(&bars[B_FIN], 0, kWaitLimitNs);
+    uint64_t* fin = &bars[kl == 0 ? B_FIN : B_FIN + 2];
+    tc_commit(fin);
+    mbar_wait_bounded(fin, 0, kWaitLimitNs);
   }
 
   // ------------------------------------------------------------------ softmax warps
@@ -409,12 +428,22 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
     };
     // this half of O times s into dst[0 .. HH - 1] (zeros for a unit without tiles);
     // `store` false: tensor memory is read (warp-collective) but nothing is written
-    auto store_o = [&](float* dst, bool have_o, float s, bool store) {
+    auto store_o = [&](float* dst, bool have_o, float s, bool store, bool n_o1) {
       if (have_o) {
         for (int c0 = 0; c0 < HH; c0 += 32) {
           uint32_t o[32];
           tc_ld32(tmem + lane_off + C::C_O + half * HH + c0, o);
-          tc_wait_ld();
+          if constexpr (C::NO == 2) {
+            // O = O_0 + O_1 (O_1 holds tiles 1, 3, ...: nothing with a single tile)
+            uint32_t o1[32];
+            tc_ld32(tmem + lane_off + C::C_O + HD + half * HH + c0, o1);
+            tc_wait_ld();
+            if (n_o1)
+#pragma unroll
+              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) + __uint_as_float(o1[e]));
+          } else {
+            tc_wait_ld();
+          }
           if (store) {
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
@@ -539,21 +568,26 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
         // before this group, all done first; none of this group's P is handed off yet
         const float c = c1 * c2;
         if (i0 > 0 && __any_sync(kFull, c != 1.f && m_run != -INFINITY)) {
-          const long long tp = T + i0 - 1;
+          // the last tile of each P V lane (i0 >= 4: both lanes have one)
+          const long long tp = T + i0 - 1, tq = T + i0 - C::NO;
           if (!__all_sync(kFull, mbar_wait_bounded(&bars[B_PVDONE + (int)(tp & 7)], (uint32_t)((tp >> 3) & 1),
-                                                   kWaitLimitNs))) {
+                                                   kWaitLimitNs) &&
+                                     mbar_wait_bounded(&bars[B_PVDONE + (int)(tq & 7)], (uint32_t)((tq >> 3) & 1),
+                                                       kWaitLimitNs))) {
             fail();
             break;
           }
           tc_fence_after();
+          for (int ko = 0; ko < C::NO; ++ko) {
 #pragma unroll 1
-          for (int c0 = half * HH; c0 < half * HH + HH; c0 += 16) {
-            uint32_t o[16];
-            tc_ld16(tmem + lane_off + C::C_O + c0, o);
-            tc_wait_ld();
+            for (int c0 = ko * HD + half * HH; c0 < ko * HD + half * HH + HH; c0 += 16) {
+              uint32_t o[16];
+              tc_ld16(tmem + lane_off + C::C_O + c0, o);
+              tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c);
-            tc_st16(tmem + lane_off + C::C_O + c0, o);
+              for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * c);
+              tc_st16(tmem + lane_off + C::C_O + c0, o);
+            }
           }
         }
         const float mref = m_new == -INFINITY ? 0.f : m_new;   // no valid key yet: every s is -inf, p = 0
@@ -612,9 +646,12 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       const float l_other = swap_with_pair(l_run);
       if (dead) break;
       if (u.ntiles > 0) {
-        const long long tl = T + u.ntiles - 1;
+        // the last tile of each P V lane that has one
+        const long long tl = T + u.ntiles - 1, tm = T + max(u.ntiles - C::NO, 0);
         if (!__all_sync(kFull, mbar_wait_bounded(&bars[B_PVDONE + (int)(tl & 7)], (uint32_t)((tl >> 3) & 1),
-                                                 kWaitLimitNs))) {
+                                                 kWaitLimitNs) &&
+                                   mbar_wait_bounded(&bars[B_PVDONE + (int)(tm & 7)], (uint32_t)((tm >> 3) & 1),
+                                                     kWaitLimitNs))) {
           fail();
           break;
         }
@@ -624,21 +661,21 @@ __global__ void __launch_bounds__(kHThreads, 1) attend_prompt_h16_kernel(AttendP
       if constexpr (!FLASH) {
         // ---- the unit's record: O * 2^(E - kVHead) (unnormalised), m, l (both halves' keys)
         const size_t item = (size_t)u.bg * p.n_rb + u.rb;
-        store_o(p.ws_acc + (item * (size_t)p.nq + q) * HD + half * HH, u.ntiles > 0, os, true);
+        store_o(p.ws_acc + (item * (size_t)p.nq + q) * HD + half * HH, u.ntiles > 0, os, true, u.ntiles > 1);
         if (half == 0) p.ws_ml[item * p.nq + q] = make_float2(m_run, l_run + l_other);
       } else {
         float* dst = p.out + (size_t)(u.s0 + r) * p.ldo + ((size_t)u.g * p.hpg + hq) * HD + half * HH;
         if (u.npiece == 1) {
           // ---- o = O / l straight to the output row (a row block past its segment's end
           // has no tiles and no rows)
-          if (u.ntiles > 0) store_o(dst, true, os / (l_run + l_other), q_ok);
+          if (u.ntiles > 0) store_o(dst, true, os / (l_run + l_other), q_ok, u.ntiles > 1);
         } else {
           // ---- a piece: its record (O, then (m, l) per half) and, by the last piece of
           // the unit to get here (per softmax warp: its 32 query vectors and half of the
           // features), the combination of all of them. No wait on another CTA.
           const size_t rstride = (size_t)kHM * (HD + 4);
           float* rec = p.ws_rec + (size_t)u.tail_at * rstride;
-          store_o(rec + (size_t)q * HD + half * HH, u.ntiles > 0, os, true);
+          store_o(rec + (size_t)q * HD + half * HH, u.ntiles > 0, os, true, u.ntiles > 1);
           reinterpret_cast<float2*>(rec + (size_t)kHM * HD)[half * kHM + q] =
               u.ntiles > 0 ? make_float2(m_run, l_run + l_other) : make_float2(-INFINITY, 0.f);
           __threadfence();
@@ -866,7 +903,7 @@ int launch_h16(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_
   const int sms = num_sms();
   const unsigned grid = (unsigned)(items < sms ? items : (sms > 0 ? sms : 148));
   if (e0) cudaEventRecord(e0, s);
-  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(kHThreads), C::BYTES, s, p);
+  cudaError_t e = launch_pdl(kern, dim3(grid), dim3(C::THREADS), C::BYTES, s, p);
   note_launch();
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e1) cudaEventRecord(e1, s);
