@@ -3,8 +3,8 @@ and against swa_prep + swa_attend with commit on the same tensors (the same
 bits: output, ring and meta; the one-kernel form attends each (sequence, KV
 head) as one split, so it is compared with swa_attend at one split). The
 one-kernel form is taken for at most 8 query heads per KV head, meta_out not
-aliasing meta, and short windows or a one-split plan; the other calls run prep,
-attention and merge."""
+aliasing meta, and short windows, a one-split plan or (sequence, KV head) pairs
+that fill the device's SMs; the other calls run prep, attention and merge."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +12,7 @@ import torch
 import oracle
 import workloads
 import sliding_window_gqa_prep_gb300 as swa
-from swa_harness import assert_close, oracle_inputs, to_dev
+from swa_harness import assert_close, oracle_inputs, oracle_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -159,3 +159,64 @@ def test_decode_steps_in_sequence_equal_a_chunk():
             slot = oracle.commit_slot(meta0[b], j, w.cap)
             assert_close(ring_k[b, :, slot].cpu().numpy(), k[b, j], f"ring k row {j}")
             np.testing.assert_array_equal(ring_v[b, :, slot].cpu().numpy(), inp["yv"].numpy()[b, j])
+
+
+def _check_step(w, inp, d, launches, rows=None):
+    """The step against the oracle (every output vector, or `rows`), and against
+    swa_prep + swa_attend on the same tensors: the same bits for the output, the
+    ring and the meta."""
+    res = _gpu_step(w, d)
+    assert res["err"] == 0 and res["launches"] == launches
+    rope = oracle.rope_table(inp["pos0"].numpy(), 1, w.hd, w.theta)
+    q, k, v = oracle.prep(inp["yq"].numpy(), inp["yk"].numpy(), inp["yv"].numpy(), rope,
+                          inp["q_scale"].numpy(), w.eps)
+    rows = rows or [(b, 0, h) for b in range(w.B) for h in range(w.nh)]
+    ref = oracle_rows(oracle_inputs(w, inp, q, k, v), rows, w.score_scale, w.hpg)
+    out = res["out"].cpu().numpy()
+    assert_close(np.stack([out[b, h] for b, _, h in rows]), ref, f"{w.name}: {len(rows)} output vectors")
+    two = _reference_path(w, d, num_splits=1 if launches == 1 else 0)
+    assert torch.equal(res["out"], two["out"])
+    assert torch.equal(res["ring_k"], two["ring_k"]) and torch.equal(res["ring_v"], two["ring_v"])
+    assert torch.equal(res["meta_out"], two["meta_out"])
+    meta = inp["meta"].numpy()
+    for b in range(w.B):
+        assert res["meta_out"][b].cpu().numpy().astype(np.int64).tolist() == \
+            oracle.commit_meta(meta[b], 1, w.cap).tolist()
+    return res, k
+
+
+def test_decode_step_one_kernel_when_the_pairs_fill_the_sms():
+    """A window of 602 keys at hd 128 (616 KB of K and V per (sequence, KV head),
+    beyond the short-window rule) over at least one (sequence, KV head) per SM: one
+    kernel, one CTA per pair streaming its whole window."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    nk = 2
+    B = -(-sms // nk)
+    w = workloads.custom(B=B, t=1, nh=8, nk=nk, hd=128, window=600, cap=600, ns=2, pos_mode="full",
+                         pos_lo=600, pos_hi=9000, seed=44)
+    inp = workloads.make_inputs(w)
+    d = to_dev(inp)
+    assert swa.decode_launches(w.B, w.nh, w.nk, w.hd, w.cap, w.ns, meta=d["meta"],
+                               meta_out=torch.empty_like(d["meta"])) == 1
+    res, k = _check_step(w, inp, d, 1)
+    # the committed slot of every sequence holds its row's k-hat (within tolerance) and v
+    ring_k, ring_v = res["ring_k"].cpu().numpy(), res["ring_v"].cpu().numpy()
+    meta = inp["meta"].numpy()
+    for b in range(w.B):
+        slot = oracle.commit_slot(meta[b], 0, w.cap)
+        assert_close(ring_k[b, :, slot], k[b, 0], "committed k-hat")
+        np.testing.assert_array_equal(ring_v[b, :, slot], inp["yv"].numpy()[b, 0])
+
+
+@pytest.mark.parametrize("name", ["tiny_decode", "batched_decode", "long_decode"])
+def test_decode_step_full_size(name):
+    """The decode workloads at full size through swa_decode_step, the call the
+    benchmark times: every output vector against the oracle, and output, ring and
+    meta bit for bit against swa_prep + swa_attend."""
+    w = workloads.WORKLOADS[name]
+    inp = workloads.make_inputs(w)
+    d = to_dev({k: v for k, v in inp.items() if k != "far"})
+    launches = swa.decode_launches(w.B, w.nh, w.nk, w.hd, w.cap, w.ns, meta=d["meta"],
+                                   meta_out=torch.empty_like(d["meta"]))
+    assert launches in (1, 3)
+    _check_step(w, inp, d, launches)
