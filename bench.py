@@ -139,10 +139,12 @@ def source_hash(path):
         return hashlib.sha256(f.read()).hexdigest()[:16]
 
 
-def recorded_traffic(w):
-    """DRAM bytes per launch of the workload's attention kernel from the
-    committed ncu summary, if it was taken on the current kernel source."""
-    kernel, src = dominant_kernel(w)
+def recorded_traffic(w, kernel=None):
+    """DRAM bytes per launch of the workload's attention kernel (or `kernel`, a
+    kernel of the same source file) from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    name, src = dominant_kernel(w)
+    kernel = kernel or name
     path = os.path.join(PROFILE_DIR, f"{kernel}_{w.name}.md")
     if not os.path.exists(path):
         return None
@@ -650,7 +652,8 @@ def run_gpu(args, w, rank, world, local_rank):
     traffic = recorded_traffic(w)
     kernel_name = dominant_kernel(w)[0]
     if one_kernel:              # the whole step is one kernel: prep, attention, gate, commit
-        kernel_name, traffic = "decode_step_kernel", None
+        kernel_name = "decode_step_kernel"
+        traffic = recorded_traffic(w, kernel_name)
     path = attention_path(w)
     useful_flop = keys * w.hpg * w.hd * 4          # Q K^T and P V, 2 flop per multiply-add
     if path == "decode":
