@@ -52,11 +52,6 @@ __device__ __forceinline__ int block_exp(float amax) {
   return amax > 0.f ? max(-100, min(100, ilogbf(amax) - 14)) : kZeroExp;
 }
 
-// bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) from global memory into L2
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
-}
-
 // x = hi + lo as f16 pairs: hi = RN(x), lo = RN(x - hi); element 2c in the low half
 __device__ __forceinline__ void split_pair(float x0, float x1, uint32_t& hi, uint32_t& lo) {
   const __half2 h = __floats2half2_rn(x0, x1);

@@ -206,6 +206,11 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) from global memory into L2
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(src), "r"(bytes) : "memory");
+}
+
 // Bulk copy (TMA, non-tensor) of `bytes` (multiple of 16, both addresses
 // 16-byte aligned) from global memory into this CTA's shared memory; the
 // transaction count of `bar` is decremented by `bytes` when it lands.
