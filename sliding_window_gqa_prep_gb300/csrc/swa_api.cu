@@ -85,6 +85,7 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   p->off_exp = 0;
   p->ops_nblk = 0;
   p->ops_nsb = 0;
+  p->ordered = 0;
   const int hpg = a->nh / a->nk;
   // Prompt-sized chunks run on tensor cores, one split per row block: blocks of
   // 128 query vectors on tcgen05 when a chunk has at least 128 query vectors
@@ -145,7 +146,18 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   const int max_splits = (int)((keys_max + TK - 1) / TK);
   const long long units = (long long)a->B * a->nk * p->n_rb;
   int best_s = 1;
-  if (a->num_splits > 0) {
+  // Verify blocks (16 / 32 query vectors) of one row block per (sequence, KV head),
+  // far more of them than resident CTAs: one split each, taken longest first (the
+  // longest-processing-time rule balances the SMs without splitting), so that the
+  // attention kernel can finish them itself: no records, no merge.
+  const int sms_now = num_sms();
+  const long long slots_now =
+      (long long)(sms_now > 0 ? sms_now : 148) * cached_occupancy(a->hd, nq);
+  const bool ordered = (nq == 16 || nq == 32) && a->num_splits == 0 && !a->far && p->n_rb == 1 &&
+                       sms_now > 0 && units >= 2 * slots_now;
+  if (ordered) {
+    best_s = 1;
+  } else if (a->num_splits > 0) {
     best_s = a->num_splits < max_splits ? a->num_splits : max_splits;
   } else {
     // About 8 waves of resident CTAs (a short tail and enough key streams in
@@ -172,6 +184,11 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   p->off_meta = p->off_nsplit + up(ns_bytes);
   p->ws_bytes = p->off_meta + up((size_t)a->B * sizeof(swa_meta));
   add_far_records(a, p);
+  if (ordered) {
+    p->ordered = 1;
+    p->off_order = p->ws_bytes;
+    p->ws_bytes += up((size_t)units * sizeof(int));
+  }
   p->ws_min = p->ws_bytes;
   return true;
 }
@@ -334,6 +351,13 @@ static void fill_attend_params(const swa_attend_args* a, const AttendPlan& plan,
   p.ops_nsb = plan.ops_nsb;
   p.ws_order = p.ops ? reinterpret_cast<int*>(ws + plan.off_order) : nullptr;
   p.ops_exp = p.ops ? reinterpret_cast<int*>(ws + plan.off_exp) : nullptr;
+  if (ws && plan.ordered) {
+    // ordered verify blocks; the kernel finishes them itself unless the commit's meta
+    // aliases the meta other CTAs still read, or the gate may still be arriving
+    p.ws_order = reinterpret_cast<int*>(ws + plan.off_order);
+    const bool aliased = a->commit && (const void*)a->meta_out == (const void*)a->meta;
+    p.fused = !aliased && !a->gate_ready ? 1 : 0;
+  }
 }
 
 int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
@@ -352,6 +376,7 @@ int swa_attend(const swa_attend_args* a, cudaStream_t stream) {
   }
   rc = launch_attend_partial(p, stream, a->ev_start, a->ev_stop);
   if (rc != SWA_OK) return rc;
+  if (p.fused) return SWA_OK;   // the attention kernel wrote out and committed
   if (a->gate_ready) {    // the gate may still be arriving: only the merge reads it
     const cudaError_t e = cudaStreamWaitEvent(stream, a->gate_ready, 0);
     if (e != cudaSuccess) return cuda_status(e);

@@ -206,19 +206,7 @@ __device__ void commit_chunk(const AttendParams& p, int cta) {
     *reinterpret_cast<float4*>(p.ring_k + dst) = *reinterpret_cast<const float4*>(p.k_chunk + src);
     *reinterpret_cast<float4*>(p.ring_v + dst) = *reinterpret_cast<const float4*>(p.v_chunk + src);
   }
-  if (cb == 0 && threadIdx.x == 0) {
-    swa_meta m1 = m0;
-    const long long tot = (long long)st.len0 + p.t;
-    if (tot <= st.W) {
-      m1.win_len = (uint32_t)tot;
-    } else {
-      const long long ev = tot - st.W;
-      m1.win_len = (uint32_t)st.W;
-      m1.win_head = (uint32_t)((st.head0 + ev) % st.W);
-      m1.far_len = (uint32_t)(m0.far_len + (uint32_t)ev);
-    }
-    p.meta_out[b] = m1;
-  }
+  if (cb == 0 && threadIdx.x == 0) p.meta_out[b] = advance_meta(m0, st, p.t);
 }
 
 // Merge of few split records (elementwise) + gate; trailing CTAs commit the chunk.

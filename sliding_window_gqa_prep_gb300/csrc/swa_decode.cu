@@ -813,18 +813,7 @@ __device__ __forceinline__ void step_body(const AttendParams& p, const StepExtra
     *reinterpret_cast<float4*>(p.ring_k + dst + d4 * 4) = *reinterpret_cast<const float4*>(own_k + d4 * 4);
     *reinterpret_cast<float4*>(p.ring_v + dst + d4 * 4) = *reinterpret_cast<const float4*>(own_v + d4 * 4);
   }
-  if (g == 0 && tid == 0) {
-    const swa_meta m0 = p.meta[b];
-    swa_meta m1 = m0;
-    if (st.len0 + 1 <= st.W) {
-      m1.win_len = (uint32_t)(st.len0 + 1);
-    } else {
-      m1.win_len = (uint32_t)st.W;
-      m1.win_head = (uint32_t)((st.head0 + 1) % st.W);
-      m1.far_len = m0.far_len + 1u;
-    }
-    p.meta_out[b] = m1;
-  }
+  if (g == 0 && tid == 0) p.meta_out[b] = advance_meta(p.meta[b], st, 1);
 }
 
 template <int HD, int NQ>

@@ -261,7 +261,7 @@ __device__ void order_units_h16(int U, int nb, int* order, Tiles tiles) {
 }
 
 // The token path's row blocks, longest first
-__device__ void order_row_blocks_h16(const AttendParams& p) {
+__device__ inline void order_row_blocks_h16(const AttendParams& p) {
   order_units_h16(p.B * p.nk * p.n_rb, p.ops_nblk + 1, p.ws_order, [&](int u) {
     const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
     return row_block_tiles(p, st, u % p.n_rb);
@@ -269,7 +269,7 @@ __device__ void order_row_blocks_h16(const AttendParams& p) {
 }
 
 // The full-sequence units, longest first (units of longer segments first)
-__device__ void order_flash_units_h16(const AttendParams& p) {
+__device__ inline void order_flash_units_h16(const AttendParams& p) {
   order_units_h16(p.B * p.nk * p.n_rb, p.ops_nblk + 1, p.ws_order, [&](int u) {
     return flash_unit_tiles(p, u % p.n_rb, flash_segment(p, u, false).y);
   });

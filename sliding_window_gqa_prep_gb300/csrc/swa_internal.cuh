@@ -37,8 +37,9 @@ struct AttendPlan {
   size_t off_ops;    // byte offset of the split-once operand blocks (tensor-core prompt kernel)
   int ops_nblk;      // their blocks per (sequence, KV head), 0 if the plan has none
   int ops_nsb;       // sink blocks among them
-  size_t off_order;  // byte offset of the tensor-core row-block order (with the operand blocks)
+  size_t off_order;  // byte offset of the row-block order (tensor-core blocks, or ordered verify)
   size_t off_exp;    // byte offset of the operand blocks' exponents (with the operand blocks)
+  int ordered;       // verify blocks: one split each, CTAs take them longest first (off_order)
 };
 bool make_plan(const swa_attend_args* a, AttendPlan* p);
 // swa_attend's argument checks short of the workspace (SWA_OK or the first error)
@@ -91,8 +92,10 @@ struct AttendParams {
   int flash_tail, flash_q;    // swa_flash: the last flash_tail units run as flash_q pieces each
   float* ws_rec;              // their records: [tail * q] x (O[128][hd], then [2][128] (m, l))
   int* ws_cnt;                // [tail][8] pieces done per unit and softmax warp
-  int* ws_order;              // with f16 ops: [B * nk * n_rb] units (index (b * nk + g) * n_rb + rb),
-                              // longest first
+  int* ws_order;              // with f16 ops, or ordered verify blocks: [B * nk * n_rb] units (index
+                              // (b * nk + g) * n_rb + rb), longest first
+  int fused;                  // ordered verify blocks: the attention kernel also normalises, gates,
+                              // writes out and commits (no records, no merge)
   int* ops_exp;               // [B][nk][ops_nblk] x (e_k, e_v), the power-of-two exponents of
                               // the f16 operand blocks (ops then holds f16 blocks)
 };
@@ -266,6 +269,23 @@ __device__ __forceinline__ SeqState sanitize_state(const swa_meta m, int cap, bo
   if (head0 >= W) { head0 %= W; bad = true; }
   if (bad_out) *bad_out = bad;
   return {W, len0, head0};
+}
+
+// The meta after a commit of t rows ("o1c_msl.metal", o1c_meta): the window grows
+// to at most W; past it the head advances by the evicted rows and far_len counts
+// them.
+__device__ __forceinline__ swa_meta advance_meta(const swa_meta m0, const SeqState& st, int t) {
+  swa_meta m1 = m0;
+  const long long tot = (long long)st.len0 + t;
+  if (tot <= st.W) {
+    m1.win_len = (uint32_t)tot;
+  } else {
+    const long long ev = tot - st.W;
+    m1.win_len = (uint32_t)st.W;
+    m1.win_head = (uint32_t)((st.head0 + ev) % st.W);
+    m1.far_len = (uint32_t)(m0.far_len + (uint32_t)ev);
+  }
+  return m1;
 }
 
 __device__ __forceinline__ SeqState load_state(const AttendParams& p, int b, bool report) {

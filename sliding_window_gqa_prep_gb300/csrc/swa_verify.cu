@@ -32,6 +32,7 @@
 //    per-warp shared slice as (p, p) pairs, and each lane accumulates an
 //    8 x FPL tile of the numerator in registers.
 #include "swa_internal.cuh"
+#include "swa_h16.cuh"
 
 namespace swa {
 namespace {
@@ -112,7 +113,13 @@ attend_verify_kernel(AttendParams p) {
 
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const int s = blockIdx.x, rb = blockIdx.y, bg = blockIdx.z;
+  int s = blockIdx.x, rb = blockIdx.y, bg = blockIdx.z;
+  if (p.ws_order) {           // ordered blocks: one split each, a 1-D grid over the order
+    const int u = p.ws_order[blockIdx.x];
+    s = 0;
+    rb = u % p.n_rb;
+    bg = u / p.n_rb;
+  }
   const int b = bg / p.nk, g = bg % p.nk;
 
   const SeqState st = load_state(p, b, tid == 0 && g == 0 && rb == 0 && s == 0);
@@ -122,8 +129,10 @@ attend_verify_kernel(AttendParams p) {
   const int win0 = min(st.W, st.len0 + r0 + 1);
   const int xlo = st.len0 + r0 + 1 - win0;       // first logical key of the block
   const int n = p.ns + (st.len0 + r_last - xlo + 1);
-  if (g == 0 && s == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = (n + p.chunk - 1) / p.chunk;
-  if (g == 0 && s == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
+  if (!p.fused) {
+    if (g == 0 && s == 0 && tid == 0) p.ws_nsplit[b * p.n_rb + rb] = (n + p.chunk - 1) / p.chunk;
+    if (g == 0 && s == 0 && rb == 0 && tid == 0) p.ws_meta[b] = p.meta[b];
+  }
   const int jb = s * p.chunk;
   if (jb >= n) return;
   const int je = min(n, jb + p.chunk);
@@ -513,6 +522,57 @@ attend_verify_kernel(AttendParams p) {
   }
   named_barrier(1, kVCW * 32);
 
+  if (p.fused) {
+    // ---- the block's rows finished here (the only split of a (sequence, KV head)):
+    // o = O / l, gated, to the output (what the merge computes for one split, bit for
+    // bit); then this KV head's chunk rows committed to its ring, which no other CTA
+    // reads, and the sequence's meta by the CTA of KV head 0 (meta_out is not meta)
+    for (int idx = tid; idx < NQ * HD / 4; idx += kVCW * 32) {
+      const int q = idx / (HD / 4), d4 = idx % (HD / 4);
+      const int rr = q / p.hpg, h = q % p.hpg;
+      if (rr >= rows_eff || q >= p.rows * p.hpg) continue;
+      const int qg = q / C::QW, ql = q % C::QW;
+      float M = -INFINITY;
+#pragma unroll
+      for (int kg = 0; kg < C::KG; ++kg) M = fmaxf(M, MLs[((qg + C::QG * kg) * C::QW + ql) * 2]);
+      float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+      float L = 0.f;
+      if (M != -INFINITY) {
+#pragma unroll
+        for (int kg = 0; kg < C::KG; ++kg) {
+          const int w = qg + C::QG * kg;
+          const float mw = MLs[(w * C::QW + ql) * 2];
+          if (mw == -INFINITY) continue;
+          const float f = exp2f(mw - M);
+          L += MLs[(w * C::QW + ql) * 2 + 1] * f;
+          const float4 a = *reinterpret_cast<const float4*>(red + ((size_t)w * C::QW + ql) * HD + d4 * 4);
+          sum.x += a.x * f; sum.y += a.y * f; sum.z += a.z * f; sum.w += a.w * f;
+        }
+      }
+      const size_t row = ((size_t)b * p.t + r0 + rr) * p.nh + (size_t)g * p.hpg + h;
+      const float4 gt = *reinterpret_cast<const float4*>(p.gate + row * HD + d4 * 4);
+      const float4 gs = *reinterpret_cast<const float4*>(p.gate_scale + ((size_t)g * p.hpg + h) * HD + d4 * 4);
+      const float inv = 1.0f / L;
+      *reinterpret_cast<float4*>(p.out + row * HD + d4 * 4) =
+          make_float4(gated(sum.x, inv, gt.x, gs.x), gated(sum.y, inv, gt.y, gs.y), gated(sum.z, inv, gt.z, gs.z),
+                      gated(sum.w, inv, gt.w, gs.w));
+    }
+    if (p.commit) {
+      const int first = max(0, p.t - st.W);        // only the last W rows survive
+      const int nrow = p.t - first;
+      for (int idx = tid; idx < nrow * (HD / 4); idx += kVCW * 32) {
+        const int j = first + idx / (HD / 4), d4 = idx % (HD / 4);
+        const int slot = (int)(((long long)st.head0 + st.len0 + j) % st.W);
+        const size_t src = (((size_t)b * p.t + j) * p.nk + g) * HD + d4 * 4;
+        const size_t dst = (kv_head * p.cap + (size_t)slot) * HD + d4 * 4;
+        *reinterpret_cast<float4*>(p.ring_k + dst) = *reinterpret_cast<const float4*>(p.k_chunk + src);
+        *reinterpret_cast<float4*>(p.ring_v + dst) = *reinterpret_cast<const float4*>(p.v_chunk + src);
+      }
+      if (g == 0 && tid == 0) p.meta_out[b] = advance_meta(p.meta[b], st, p.t);
+    }
+    return;
+  }
+
   const size_t item = (((size_t)bg * p.n_rb + rb) * p.splits + s);
   float* wacc = p.ws_acc + item * (size_t)p.nq * HD;
   for (int idx = tid; idx < NQ * HD / 4; idx += kVCW * 32) {
@@ -553,6 +613,19 @@ attend_verify_kernel(AttendParams p) {
   }
 }
 
+// The order of ordered verify blocks: (sequence, KV head, row block) units by key
+// tile count, longest first, by one CTA of 256 threads.
+__global__ void __launch_bounds__(256) order_verify_kernel(AttendParams p) {
+  pdl_trigger();
+  pdl_wait();
+  h16::order_units_h16(p.B * p.nk * p.n_rb, p.chunk / TK + 1, p.ws_order, [&](int u) {
+    const SeqState st = sanitize_state(p.meta[u / p.n_rb / p.nk], p.cap, nullptr);
+    const int r0 = (u % p.n_rb) * p.rows, r_last = min(r0 + p.rows, p.t) - 1;
+    const int xlo = st.len0 + r0 + 1 - min(st.W, st.len0 + r0 + 1);
+    return (p.ns + (st.len0 + r_last - xlo + 1) + TK - 1) / TK;
+  });
+}
+
 template <int HD, int NQ>
 int launch_v(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t e1) {
   using C = VCfg<HD, NQ>;
@@ -566,6 +639,11 @@ int launch_v(const AttendParams& p, cudaStream_t s, cudaEvent_t e0, cudaEvent_t 
     if (dev >= 0 && dev < 64) attr_set[dev] = true;
   }
   dim3 grid((unsigned)p.splits, (unsigned)p.n_rb, (unsigned)(p.B * p.nk));
+  if (p.ws_order) {
+    const int rc = finish_launch(launch_pdl(order_verify_kernel, dim3(1), dim3(256), 0, s, p));
+    if (rc != SWA_OK) return rc;
+    grid = dim3((unsigned)(p.B * p.nk * p.n_rb));
+  }
   if (e0) cudaEventRecord(e0, s);
   cudaError_t e = launch_pdl(kern, grid, dim3(kVThreads), C::BYTES, s, p);
   note_launch();

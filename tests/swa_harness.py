@@ -65,6 +65,7 @@ def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_ali
                        ring_v=ring_v if prep_ring else None)
     ring_after_prep_k = ring_k.clone() if prep_ring else None
     meta = d["meta"].clone()
+    n_launch = swa.launch_count()
     meta_out = meta if meta_alias else torch.full_like(meta, -1)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = swa.attend(meta, q, k, v, ring_k, ring_v, d["sink_k"] if w.ns else None,
@@ -76,6 +77,7 @@ def gpu_full_path(w, inp, *, commit=True, num_splits=0, prep_ring=None, meta_ali
     torch.cuda.synchronize()
     return {
         "rope": rope.cpu().numpy(), "q": q.cpu().numpy(), "k": k.cpu().numpy(),
+        "attend_launches": swa.launch_count() - n_launch,
         "v": v.cpu().numpy(), "out": out.cpu().numpy(), "ring_k": ring_k.cpu().numpy(),
         "ring_v": ring_v.cpu().numpy(), "meta_out": meta_out.cpu().numpy(),
         "err": int(err.item()),

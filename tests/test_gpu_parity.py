@@ -164,6 +164,25 @@ def test_tensor_core_prompt_with_the_minimum_workspace(kw):
     check_commit_placement(w, inp, res)
 
 
+@pytest.mark.parametrize("meta_alias", [False, True])
+def test_ordered_verify_blocks_finish_in_the_attention_kernel(meta_alias):
+    """Far more verify blocks (16 query vectors, one row block per (sequence, KV
+    head)) than resident CTAs: one split each, taken longest first from an order a
+    one-CTA kernel sorts; the attention kernel itself normalises, gates, writes the
+    output and commits (two launches). With meta_out aliasing meta it writes records
+    and the merge commits (three launches). Every output row against the oracle;
+    ring and meta exact."""
+    w = workloads.custom(B=600, t=4, nh=8, nk=2, hd=128, window=64, cap=64, ns=2, pos_mode="partial",
+                         pos_lo=1, pos_hi=64, seed=47)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=True, meta_alias=meta_alias)
+    assert res["err"] == 0
+    assert res["attend_launches"] == (3 if meta_alias else 2)
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, "out")
+    check_commit_placement(w, inp, res)
+
+
 def test_attend_only_matches_oracle_on_shared_q_k():
     """Attend fed the same (generator-drawn) q and chunk k/v on both sides."""
     w = workloads.custom(B=3, t=8, nh=16, nk=4, hd=128, window=100, cap=100, ns=4,
