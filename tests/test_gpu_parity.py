@@ -183,6 +183,22 @@ def test_ordered_verify_blocks_finish_in_the_attention_kernel(meta_alias):
     check_commit_placement(w, inp, res)
 
 
+def test_ordered_verify_blocks_kernel_finish_equals_the_merge():
+    """The block finished in the attention kernel and the same block written as a
+    record and finished by the merge (meta_out aliasing meta) give the same bits:
+    for one split the merge's weight is exp2(0) = 1."""
+    w = workloads.custom(B=600, t=4, nh=8, nk=2, hd=128, window=64, cap=64, ns=2, pos_mode="partial",
+                         pos_lo=1, pos_hi=64, seed=48)
+    inp = workloads.make_inputs(w)
+    a = gpu_full_path(w, inp, commit=True)
+    b = gpu_full_path(w, inp, commit=True, meta_alias=True)
+    assert a["attend_launches"] == 2 and b["attend_launches"] == 3
+    np.testing.assert_array_equal(a["out"], b["out"])
+    np.testing.assert_array_equal(a["ring_k"], b["ring_k"])
+    np.testing.assert_array_equal(a["ring_v"], b["ring_v"])
+    np.testing.assert_array_equal(a["meta_out"], b["meta_out"])
+
+
 def test_attend_only_matches_oracle_on_shared_q_k():
     """Attend fed the same (generator-drawn) q and chunk k/v on both sides."""
     w = workloads.custom(B=3, t=8, nh=16, nk=4, hd=128, window=100, cap=100, ns=4,
