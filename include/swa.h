@@ -160,7 +160,14 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  * (max, sum, numerator) records in `workspace`, reduced by a second kernel
  * that also applies the gate and the commit. num_splits = 0 lets the library
  * choose; a positive value caps the splits per (sequence, KV head, row block)
- * (results agree within f32 rounding for any split count).
+ * (results agree within f32 rounding for any split count). Calls of 16 or 32
+ * query vectors per (sequence, KV head) (one row block each, e.g. speculative
+ * verify) with at least twice as many of them as the attention kernel has
+ * resident CTAs on the device, and num_splits = 0, run one split each, taken
+ * longest first (a one-CTA kernel sorts them first; the order is in the
+ * workspace); unless meta_out aliases meta or gate_ready is set, the attention
+ * kernel then gates, writes and commits them itself and no second kernel runs
+ * (the same bits as through the second kernel).
  *
  * Workspace: device memory, 256-byte aligned, no initial contents needed;
  * overlapping calls must not share it. `workspace_bytes` must be at least
@@ -174,7 +181,7 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  * f32 rounding). ev_start / ev_stop, when non-NULL, are recorded on the
  * stream right before and after the main attention kernel (for timing it).
  * gate_ready, when non-NULL, is an event the stream waits for after the
- * attention and before the merge, the only kernel that reads gate: a caller
+ * attention and before the merge, then the only kernel that reads gate: a caller
  * may still be copying the gate in (on another stream) while the attention
  * runs, and record gate_ready after that copy.
  * err, when non-NULL, is a device word the kernels OR SWA_DERR_* bits into.

@@ -29,8 +29,13 @@
 //    Transposed shuffles over the 8 chunk lanes leave each lane the full
 //    scores of QW / 8 query vectors for its keys.
 //  - P V: lane = (query group of 8, feature group); P is handed over through a
-//    per-warp shared slice as (p, p) pairs, and each lane accumulates an
-//    8 x FPL tile of the numerator in registers.
+//    per-warp shared slice as plain floats read as natural pairs of query
+//    vectors, V is duplicated in a register, and each lane accumulates an
+//    8 x FPL tile of the numerator as pairs (O[q][f], O[q + 1][f]).
+//  - Ordered blocks (p.ws_order): one split per block and a 1-D grid over the
+//    order order_verify_kernel writes (longest first); with p.fused the CTA, the
+//    only reader of its KV head's ring, normalises, gates and writes its rows and
+//    commits its KV head's chunk rows (and, for KV head 0, the meta) itself.
 #include "swa_internal.cuh"
 #include "swa_h16.cuh"
 
