@@ -281,9 +281,8 @@ int swa_attend(const swa_attend_args* args, cudaStream_t stream);
  *
  * When a KV head has at most 8 query heads, meta_out does not alias meta, and
  * either the library's split planner gives every (sequence, KV head) a single
- * CTA, or one CTA's keys (sinks + window) hold at most 512 KB of K and V (512
- * keys at hd 128: the launch-bound regime), or the B x nk (sequence, KV head)
- * pairs are at least as many as the device's SMs, the whole step is ONE kernel:
+ * CTA or one CTA's keys (sinks + window) hold at most 512 KB of K and V (512
+ * keys at hd 128: the launch-bound regime), the whole step is ONE kernel:
  * the CTA of (sequence, KV head) preps that KV head's query heads and its own
  * k / v head, attends with its own row held in shared memory, writes the gated
  * output and commits its row (the committed slot is never a key of the row's

@@ -411,10 +411,7 @@ static size_t up256(size_t x) { return (x + 255) & ~(size_t)255; }
 constexpr size_t kStepOneCtaBytes = 512 * 1024;
 
 // 1: one kernel (the plan then has one split per (sequence, KV head)),
-// 3: prep + attention + merge, 0: invalid sizes. Long windows also take one
-// kernel when the (sequence, KV head) pairs alone fill the device's SMs: one CTA
-// per pair then streams its whole window at about the split kernel's rate, and the
-// prep and merge launches disappear (64 x 4 pairs of 4100 keys: 185 -> 181 us a step).
+// 3: prep + attention + merge, 0: invalid sizes.
 static int decode_form(const swa_decode_args* a, AttendPlan* plan) {
   swa_attend_args t;
   decode_as_attend(a, &t);
@@ -422,9 +419,7 @@ static int decode_form(const swa_decode_args* a, AttendPlan* plan) {
   if (!make_plan(&t, plan)) return 0;
   const bool aliased = a->meta_out != nullptr && (const void*)a->meta_out == (const void*)a->meta;
   const bool short_window = (size_t)plan->keys_max * a->hd * 8 <= kStepOneCtaBytes;
-  const int sms = num_sms();
-  const bool fills = sms > 0 && (long long)a->B * a->nk >= sms;
-  if (plan->nq > 8 || aliased || (plan->splits != 1 && !short_window && !fills)) return 3;
+  if (plan->nq > 8 || aliased || (plan->splits != 1 && !short_window)) return 3;
   plan->splits = 1;
   plan->chunk = (plan->keys_max + TK - 1) / TK * TK;
   return 1;

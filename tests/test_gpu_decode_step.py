@@ -3,8 +3,8 @@ and against swa_prep + swa_attend with commit on the same tensors (the same
 bits: output, ring and meta; the one-kernel form attends each (sequence, KV
 head) as one split, so it is compared with swa_attend at one split). The
 one-kernel form is taken for at most 8 query heads per KV head, meta_out not
-aliasing meta, and short windows, a one-split plan or (sequence, KV head) pairs
-that fill the device's SMs; the other calls run prep, attention and merge."""
+aliasing meta, and short windows or a one-split plan; the other calls run prep,
+attention and merge."""
 import numpy as np
 import pytest
 import torch
@@ -183,29 +183,6 @@ def _check_step(w, inp, d, launches, rows=None):
         assert res["meta_out"][b].cpu().numpy().astype(np.int64).tolist() == \
             oracle.commit_meta(meta[b], 1, w.cap).tolist()
     return res, k
-
-
-def test_decode_step_one_kernel_when_the_pairs_fill_the_sms():
-    """A window of 602 keys at hd 128 (616 KB of K and V per (sequence, KV head),
-    beyond the short-window rule) over at least one (sequence, KV head) per SM: one
-    kernel, one CTA per pair streaming its whole window."""
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    nk = 2
-    B = -(-sms // nk)
-    w = workloads.custom(B=B, t=1, nh=8, nk=nk, hd=128, window=600, cap=600, ns=2, pos_mode="full",
-                         pos_lo=600, pos_hi=9000, seed=44)
-    inp = workloads.make_inputs(w)
-    d = to_dev(inp)
-    assert swa.decode_launches(w.B, w.nh, w.nk, w.hd, w.cap, w.ns, meta=d["meta"],
-                               meta_out=torch.empty_like(d["meta"])) == 1
-    res, k = _check_step(w, inp, d, 1)
-    # the committed slot of every sequence holds its row's k-hat (within tolerance) and v
-    ring_k, ring_v = res["ring_k"].cpu().numpy(), res["ring_v"].cpu().numpy()
-    meta = inp["meta"].numpy()
-    for b in range(w.B):
-        slot = oracle.commit_slot(meta[b], 0, w.cap)
-        assert_close(ring_k[b, :, slot], k[b, 0], "committed k-hat")
-        np.testing.assert_array_equal(ring_v[b, :, slot], inp["yv"].numpy()[b, 0])
 
 
 @pytest.mark.parametrize("name", ["tiny_decode", "batched_decode", "long_decode"])

@@ -183,6 +183,17 @@ def test_ordered_verify_blocks_finish_in_the_attention_kernel(meta_alias):
     check_commit_placement(w, inp, res)
 
 
+def test_ordered_verify_blocks_without_commit_leave_ring_and_meta_alone():
+    w = workloads.custom(B=600, t=4, nh=8, nk=2, hd=128, window=64, cap=64, ns=2, pos_mode="full",
+                         pos_lo=64, pos_hi=900, seed=49)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=False)
+    assert res["err"] == 0 and res["attend_launches"] == 2
+    assert_close(res["out"], oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg), "out")
+    np.testing.assert_array_equal(res["ring_k"], inp["ring_k"].numpy())
+    np.testing.assert_array_equal(res["ring_v"], inp["ring_v"].numpy())
+
+
 def test_ordered_verify_blocks_kernel_finish_equals_the_merge():
     """The block finished in the attention kernel and the same block written as a
     record and finished by the merge (meta_out aliasing meta) give the same bits:
