@@ -398,10 +398,10 @@ attend_verify_kernel(AttendParams p) {
       const float m_new = fmaxf(m[o], tmax);
       float c = 1.f, lsum = 0.f;
       if (m_new != -INFINITY) {
-        c = exp2f(m[o] - m_new);
+        c = h16::ex2(m[o] - m_new);
 #pragma unroll
         for (int j = 0; j < C::KPL; ++j) {
-          sc[j][o] = exp2f(sc[j][o] - m_new);
+          sc[j][o] = h16::ex2(sc[j][o] - m_new);
           lsum += sc[j][o];
         }
       } else {
@@ -440,8 +440,7 @@ attend_verify_kernel(AttendParams p) {
       }
     }
     const int nkv = min(C::KW, cnt - kbase);
-#pragma unroll 2
-    for (int kk = 0; kk < nkv; ++kk) {
+    auto pv_key = [&](int kk) {
       // P of the lane's query vectors as natural pairs (q, q + 1); V once per feature
       u64 pk[C::QPL / 2];
 #pragma unroll
@@ -467,6 +466,15 @@ attend_verify_kernel(AttendParams p) {
 #pragma unroll
         for (int k2 = 0; k2 < C::QPL / 2; ++k2) acc[k2][d] = ffma2(pk[k2], vd, acc[k2][d]);
       }
+    };
+    // A full share of keys runs fully unrolled: every P and V load can be hoisted
+    // ahead of the products (5 % of the kernel against two keys a trip)
+    if (nkv == C::KW) {
+#pragma unroll
+      for (int kk = 0; kk < C::KW; ++kk) pv_key(kk);
+    } else {
+#pragma unroll 2
+      for (int kk = 0; kk < nkv; ++kk) pv_key(kk);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);
