@@ -28,10 +28,12 @@
 //    vectors, so one packed FMA updates the scores of two query vectors.
 //    Transposed shuffles over the 8 chunk lanes leave each lane the full
 //    scores of QW / 8 query vectors for its keys.
-//  - P V: lane = (query group of 8, feature group); P is handed over through a
-//    per-warp shared slice as plain floats read as natural pairs of query
-//    vectors, V is duplicated in a register, and each lane accumulates an
-//    8 x FPL tile of the numerator as pairs (O[q][f], O[q + 1][f]).
+//  - P V: lane = (query group, feature group): all 16 query vectors of the
+//    warp and 4 features at hd 128 (8 x 4 at hd 64, 8 x 8 at hd 256); P is
+//    handed over through a per-warp shared slice as plain floats read as
+//    natural pairs of query vectors, V is duplicated in a register (one pair
+//    feeds QPL / 2 packed FMAs), and each lane accumulates its QPL x FPL tile
+//    of the numerator as pairs (O[q][f], O[q + 1][f]).
 //  - Ordered blocks (p.ws_order): one split per block and a 1-D grid over the
 //    order order_verify_kernel writes (longest first); with p.fused the CTA, the
 //    only reader of its KV head's ring, normalises, gates and writes its rows and
@@ -81,7 +83,9 @@ struct VCfg {
   static constexpr int KPL = KW / 4;              // keys per lane in the scores
   static constexpr int CH = HD / 32;              // float4 chunks per lane in the scores
   static constexpr int QO = QW / 8;               // query vectors a lane owns after the reduction
-  static constexpr int FG = QW == 16 ? 16 : 32;   // feature lanes in P V
+  // feature lanes in P V: 32 (every lane takes all QW query vectors) unless a
+  // lane would hold fewer than 4 features
+  static constexpr int FG = QW == 16 && HD == 64 ? 16 : 32;
   static constexpr int QGL = 32 / FG;             // query lanes in P V
   static constexpr int QPL = QW / QGL;            // query vectors per lane in P V
   static constexpr int FPL = HD / FG;             // features per lane in P V
@@ -98,7 +102,7 @@ struct VCfg {
   static constexpr size_t BYTES = (size_t)FLOATS * 4 + 2 * STAGES * sizeof(uint64_t);
   static constexpr int MIN_BLOCKS = HD == 256 ? 1 : 2;
   static_assert(NQ == 16 || NQ == 32, "16 or 32 query vectors");
-  static_assert(QG * KG == kVCW && KPL >= 1 && QPL == 8 && FCH >= 1, "warp arrangement");
+  static_assert(QG * KG == kVCW && KPL >= 1 && (QPL == 8 || QPL == 16) && FCH >= 1, "warp arrangement");
   static_assert(kVCW * QW * HD <= 2 * STAGES * TK * HD, "warp states fit the stage buffers");
 };
 
