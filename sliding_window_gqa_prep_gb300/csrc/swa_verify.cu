@@ -1,7 +1,8 @@
 // Attention of a row block with 16 or 32 query vectors (speculative verify
 // and other short chunks) on CUDA cores: o1c_score / o1c_soft / o1c_sum of
 // "o1c_msl.metal" (cortiq-engine 0.8.79) for several rows at once, as one
-// warp-specialised split-KV kernel writing the shared partial-record format.
+// split-KV kernel writing the shared partial-record format (or, for ordered
+// single-split blocks, the finished rows).
 //
 // With 32 query vectors per key the path does 16 flops per K/V byte, so the
 // FP32 FMA pipe, not HBM, bounds it, and the design is about feeding that
