@@ -165,9 +165,10 @@ int swa_prep(const swa_prep_args* args, cudaStream_t stream);
  * verify) with at least twice as many of them as the attention kernel has
  * resident CTAs on the device, and num_splits = 0, run one split each, taken
  * longest first (a one-CTA kernel sorts them first; the order is in the
- * workspace); unless meta_out aliases meta or gate_ready is set, the attention
- * kernel then gates, writes and commits them itself and no second kernel runs
- * (the same bits as through the second kernel).
+ * workspace); unless meta_out aliases meta, gate_ready is set or a far field is
+ * given (its part joins in the second kernel), the attention kernel then gates,
+ * writes and commits them itself and no second kernel runs (the same bits as
+ * through the second kernel).
  *
  * Workspace: device memory, 256-byte aligned, no initial contents needed;
  * overlapping calls must not share it. `workspace_bytes` must be at least

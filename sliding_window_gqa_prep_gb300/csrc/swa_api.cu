@@ -149,11 +149,12 @@ bool make_plan(const swa_attend_args* a, AttendPlan* p) {
   // Verify blocks (16 / 32 query vectors) of one row block per (sequence, KV head),
   // far more of them than resident CTAs: one split each, taken longest first (the
   // longest-processing-time rule balances the SMs without splitting), so that the
-  // attention kernel can finish them itself: no records, no merge.
+  // attention kernel can finish them itself: no records, no merge (with a far field
+  // the single-split records still go to the merge, which joins the far part).
   const int sms_now = num_sms();
   const long long slots_now =
       (long long)(sms_now > 0 ? sms_now : 148) * cached_occupancy(a->hd, nq);
-  const bool ordered = (nq == 16 || nq == 32) && a->num_splits == 0 && !a->far && p->n_rb == 1 &&
+  const bool ordered = (nq == 16 || nq == 32) && a->num_splits == 0 && p->n_rb == 1 &&
                        sms_now > 0 && units >= 2 * slots_now;
   if (ordered) {
     best_s = 1;
@@ -353,10 +354,11 @@ static void fill_attend_params(const swa_attend_args* a, const AttendPlan& plan,
   p.ops_exp = p.ops ? reinterpret_cast<int*>(ws + plan.off_exp) : nullptr;
   if (ws && plan.ordered) {
     // ordered verify blocks; the kernel finishes them itself unless the commit's meta
-    // aliases the meta other CTAs still read, or the gate may still be arriving
+    // aliases the meta other CTAs still read, the gate may still be arriving, or a far
+    // field joins the rows in the merge
     p.ws_order = reinterpret_cast<int*>(ws + plan.off_order);
     const bool aliased = a->commit && (const void*)a->meta_out == (const void*)a->meta;
-    p.fused = !aliased && !a->gate_ready ? 1 : 0;
+    p.fused = !aliased && !a->gate_ready && !a->far ? 1 : 0;
   }
 }
 

@@ -531,6 +531,24 @@ def test_far_chunk_matches_oracle(t, hd, nh, nk, W):
     _far_step_check(w, inp, 0, 0)
 
 
+def test_ordered_verify_blocks_with_a_far_field():
+    """Far more verify blocks (32 query vectors) than resident CTAs with a far
+    field: one split each, taken longest first; the blocks write records and the
+    merge joins the far part, gates and commits (far kernel, order, attention,
+    merge: four launches). Every output row against the oracle; ring, meta and
+    far state after the commit."""
+    w, inp = _far_case(71, B=600, t=8)
+    inp["meta"][2, 0] = w.window - 2                    # fills after two rows of the chunk
+    inp["meta"][2, 1] = 0
+    inp["far"]["mu"] = inp["far"]["mu"] - 0.05
+    res = gpu_full_path(w, inp, commit=True, far=inp["far"])
+    assert res["err"] == 0 and res["attend_launches"] == 4
+    a = oracle_inputs(w, inp, *_gpu_prepped(res))
+    assert_close(res["out"], oracle.attend_far(a, far_to_np(inp["far"]), w.score_scale, w.hpg), "out (far field)")
+    check_commit_placement(w, inp, res)
+    _check_far_state(w, inp, res)
+
+
 def test_far_decode_with_odd_landmark_count():
     """m = 7: the per-head shared-memory sections of a CTA that serves several
     decode heads stay aligned; heads past nh in the last CTA write nothing."""
