@@ -183,6 +183,21 @@ def test_ordered_verify_blocks_finish_in_the_attention_kernel(meta_alias):
     check_commit_placement(w, inp, res)
 
 
+@pytest.mark.parametrize("hd,t,B", [(64, 8, 320), (256, 4, 160), (256, 8, 160)])
+def test_ordered_verify_blocks_at_other_head_dims(hd, t, B):
+    """The ordered blocks finished in the attention kernel at hd 64 (32 query
+    vectors) and hd 256 (16 and 32; one CTA per SM, so fewer blocks suffice):
+    every output row against the oracle, ring and meta exact."""
+    w = workloads.custom(B=B, t=t, nh=8, nk=2, hd=hd, window=48, cap=48, ns=3, pos_mode="partial",
+                         pos_lo=1, pos_hi=48, seed=60 + hd + t)
+    inp = workloads.make_inputs(w)
+    res = gpu_full_path(w, inp, commit=True)
+    assert res["err"] == 0 and res["attend_launches"] == 2
+    ref = oracle.attend(oracle_inputs(w, inp), w.score_scale, w.hpg)
+    assert_close(res["out"], ref, "out")
+    check_commit_placement(w, inp, res)
+
+
 def test_ordered_verify_blocks_without_commit_leave_ring_and_meta_alone():
     w = workloads.custom(B=600, t=4, nh=8, nk=2, hd=128, window=64, cap=64, ns=2, pos_mode="full",
                          pos_lo=64, pos_hi=900, seed=49)
