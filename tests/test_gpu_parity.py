@@ -441,6 +441,30 @@ def test_prompt_chunk_captured_graph_follows_each_steps_inputs():
                      "graph replay out")
 
 
+def test_ordered_verify_blocks_in_a_captured_graph_with_the_gate_arriving_late():
+    """Ordered verify blocks inside the captured host-to-host step: the gate is still
+    being copied in while the attention runs, so the blocks write records and the
+    merge (which waits for the gate) finishes them. Two replays with different inputs;
+    every window stays below W - t, so a replay's commit never lands in the next one's
+    window."""
+    w = workloads.custom(B=600, t=4, nh=8, nk=2, hd=128, window=64, cap=64, ns=2,
+                         pos_mode="prompt", pos_lo=1, pos_hi=60, seed=33)   # sequence 0: empty ring
+    inp = workloads.make_inputs(w)
+    g = torch.Generator().manual_seed(34)
+    other = dict(inp, **{k: torch.randn(inp[k].shape, generator=g) for k in ("yq", "yk", "yv", "gate")})
+    tp = swa.TokenPath(B=w.B, t=w.t, nh=w.nh, nk=w.nk, hd=w.hd, cap=w.cap, ns=w.ns,
+                       q_scale=inp["q_scale"], gate_scale=inp["gate_scale"],
+                       ring_k=inp["ring_k"], ring_v=inp["ring_v"], sink_k=inp["sink_k"],
+                       sink_v=inp["sink_v"], meta=inp["meta"], pos0=inp["pos0"])
+    tp.capture()
+    for cur in (inp, other):
+        for k in ("yq", "yk", "yv", "gate"):
+            tp.h_in[k].copy_(cur[k])
+        out = tp.replay()
+        assert_close(out.numpy(), oracle.attend(oracle_inputs(w, cur), w.score_scale, w.hpg),
+                     "graph replay out")
+
+
 def test_rollback_matches_oracle_bit_for_bit():
     g = torch.Generator().manual_seed(31)
     B, cap = 300, 64
