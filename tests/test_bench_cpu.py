@@ -23,3 +23,30 @@ def test_l2_regime_follows_the_ring_size():
         assert ("flushed" in note) == (rings <= 129e6), name
         assert ("larger than L2" in note) == (rings > 129e6), name
     assert "flushed" in bench.flash_config(workloads.FLASH_WORKLOADS["vision_flash"], 1)["l2"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) on the smallest
+    workload: one JSON line with the contract's keys, its own cpu_baseline and an e2e
+    block with no copies."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny_decode",
+                          "--steps", "1", "--warmup", "1"], cwd=root, capture_output=True, text=True,
+                         timeout=600, check=True).stdout
+    lines = [l for l in out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["config"]["workload"] == "tiny_decode" and d["steps"] == 1 and d["warmup"] == 1
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    e2e = d["e2e"]
+    assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
+    assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
