@@ -305,16 +305,30 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
       }
       k = 1;
     }
-#pragma unroll 4
-    for (; k < cnt; ++k) {
-      const float wk = __shfl_sync(0xffffffffu, w, k);
-      const float* src = p.ws_acc + ((item0 + s0 + k) * p.nq + q) * (size_t)HD;
+    // up to 16 splits' numerators in flight at once (a runtime trip count let the
+    // compiler keep only a few loads ahead)
+    constexpr int KB = 16;
+    for (; k < cnt; k += KB) {
+      float4 ak[KB][PER];
 #pragma unroll
-      for (int c = 0; c < PER; ++c) {
-        const int d4 = c * 32 + lane;
-        if (d4 < D4) {
-          const float4 a = *reinterpret_cast<const float4*>(src + d4 * 4);
-          acc[c].x += a.x * wk; acc[c].y += a.y * wk; acc[c].z += a.z * wk; acc[c].w += a.w * wk;
+      for (int kk = 0; kk < KB; ++kk) {
+        const float* src = p.ws_acc + ((item0 + s0 + k + kk) * p.nq + q) * (size_t)HD;
+#pragma unroll
+        for (int c = 0; c < PER; ++c) {
+          const int d4 = c * 32 + lane;
+          ak[kk][c] = (k + kk < cnt && d4 < D4) ? *reinterpret_cast<const float4*>(src + d4 * 4)
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < KB; ++kk) {
+        const float wk = __shfl_sync(0xffffffffu, w, (k + kk) & 31);
+        if (k + kk < cnt) {
+#pragma unroll
+          for (int c = 0; c < PER; ++c) {
+            acc[c].x += ak[kk][c].x * wk; acc[c].y += ak[kk][c].y * wk;
+            acc[c].z += ak[kk][c].z * wk; acc[c].w += ak[kk][c].w * wk;
+          }
         }
       }
     }
