@@ -60,19 +60,34 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
 #pragma unroll
   for (int c = 0; c < PER; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-#pragma unroll 4
-  for (int sp = warp; sp < nval; sp += 8) {
-    const float2 ml = p.ws_ml[(item0 + sp) * p.nq + q];
-    if (ml.x == -INFINITY) continue;            // a split with no key of this row weighs 0
-    const float w = exp2f(ml.x - M);
-    den += ml.y * w;
-    const float* src = p.ws_acc + ((item0 + sp) * p.nq + q) * (size_t)HD;
+  // each warp's splits warp, warp + 8, ... eight at a time with every load in flight
+  // (the same order of additions as one at a time)
+  constexpr int KW = 8;
+  for (int sp0 = warp; sp0 < nval; sp0 += 8 * KW) {
+    float2 mlk[KW];
+    float4 ak[KW][PER];
 #pragma unroll
-    for (int c = 0; c < PER; ++c) {
-      const int d4 = c * 32 + lane;
-      if (d4 < D4) {
-        const float4 a = *reinterpret_cast<const float4*>(src + d4 * 4);
-        acc[c].x += a.x * w; acc[c].y += a.y * w; acc[c].z += a.z * w; acc[c].w += a.w * w;
+    for (int kk = 0; kk < KW; ++kk) {
+      const int sp = sp0 + 8 * kk;
+      const bool ok = sp < nval;
+      mlk[kk] = ok ? p.ws_ml[(item0 + sp) * p.nq + q] : make_float2(-INFINITY, 0.f);
+      const float* src = p.ws_acc + ((item0 + sp) * p.nq + q) * (size_t)HD;
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        const int d4 = c * 32 + lane;
+        ak[kk][c] = (ok && d4 < D4) ? *reinterpret_cast<const float4*>(src + d4 * 4)
+                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+#pragma unroll
+    for (int kk = 0; kk < KW; ++kk) {
+      if (mlk[kk].x == -INFINITY) continue;      // a split with no key of this row weighs 0
+      const float w = exp2f(mlk[kk].x - M);
+      den += mlk[kk].y * w;
+#pragma unroll
+      for (int c = 0; c < PER; ++c) {
+        acc[c].x += ak[kk][c].x * w; acc[c].y += ak[kk][c].y * w; acc[c].z += ak[kk][c].z * w;
+        acc[c].w += ak[kk][c].w * w;
       }
     }
   }
