@@ -25,7 +25,7 @@ namespace {
 // One output row (b, r, h) by a whole CTA of 8 warps: every warp finds the
 // max over the valid splits, warp w adds the rescaled records of splits
 // w, w + 8, ... (lanes over features), and the CTA sums the 8 partials.
-template <int HD>
+template <int HD, bool BATCH>
 __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
   constexpr int D4 = HD / 4;
   constexpr int PER = (D4 + 31) / 32;
@@ -60,36 +60,55 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
 #pragma unroll
   for (int c = 0; c < PER; ++c) acc[c] = make_float4(0.f, 0.f, 0.f, 0.f);
   float den = 0.f;
-  // each warp's splits warp, warp + 8, ... eight at a time with every load in flight
-  // (the same order of additions as one at a time)
-  constexpr int KW = 8;
-  for (int sp0 = warp; sp0 < nval; sp0 += 8 * KW) {
-    float2 mlk[KW];
-    float4 ak[KW][PER];
+  if constexpr (BATCH) {
+    // each warp's splits warp, warp + 8, ... eight at a time with every load in flight
+    // (the same order of additions as one at a time)
+    constexpr int KW = 8;
+    for (int sp0 = warp; sp0 < nval; sp0 += 8 * KW) {
+      float2 mlk[KW];
+      float4 ak[KW][PER];
 #pragma unroll
-    for (int kk = 0; kk < KW; ++kk) {
-      const int sp = sp0 + 8 * kk;
-      const bool ok = sp < nval;
-      mlk[kk] = ok ? p.ws_ml[(item0 + sp) * p.nq + q] : make_float2(-INFINITY, 0.f);
+      for (int kk = 0; kk < KW; ++kk) {
+        const int sp = sp0 + 8 * kk;
+        const bool ok = sp < nval;
+        mlk[kk] = ok ? p.ws_ml[(item0 + sp) * p.nq + q] : make_float2(-INFINITY, 0.f);
+        const float* src = p.ws_acc + ((item0 + sp) * p.nq + q) * (size_t)HD;
+#pragma unroll
+        for (int c = 0; c < PER; ++c) {
+          const int d4 = c * 32 + lane;
+          ak[kk][c] = (ok && d4 < D4) ? *reinterpret_cast<const float4*>(src + d4 * 4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < KW; ++kk) {
+        if (mlk[kk].x == -INFINITY) continue;      // a split with no key of this row weighs 0
+        const float w = exp2f(mlk[kk].x - M);
+        den += mlk[kk].y * w;
+#pragma unroll
+        for (int c = 0; c < PER; ++c) {
+          acc[c].x += ak[kk][c].x * w; acc[c].y += ak[kk][c].y * w; acc[c].z += ak[kk][c].z * w;
+          acc[c].w += ak[kk][c].w * w;
+        }
+      }
+    }
+  } else {
+#pragma unroll 4
+    for (int sp = warp; sp < nval; sp += 8) {
+      const float2 ml = p.ws_ml[(item0 + sp) * p.nq + q];
+      if (ml.x == -INFINITY) continue;            // a split with no key of this row weighs 0
+      const float w = exp2f(ml.x - M);
+      den += ml.y * w;
       const float* src = p.ws_acc + ((item0 + sp) * p.nq + q) * (size_t)HD;
 #pragma unroll
       for (int c = 0; c < PER; ++c) {
         const int d4 = c * 32 + lane;
-        ak[kk][c] = (ok && d4 < D4) ? *reinterpret_cast<const float4*>(src + d4 * 4)
-                                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (d4 < D4) {
+          const float4 a = *reinterpret_cast<const float4*>(src + d4 * 4);
+          acc[c].x += a.x * w; acc[c].y += a.y * w; acc[c].z += a.z * w; acc[c].w += a.w * w;
+        }
       }
-    }
-#pragma unroll
-    for (int kk = 0; kk < KW; ++kk) {
-      if (mlk[kk].x == -INFINITY) continue;      // a split with no key of this row weighs 0
-      const float w = exp2f(mlk[kk].x - M);
-      den += mlk[kk].y * w;
-#pragma unroll
-      for (int c = 0; c < PER; ++c) {
-        acc[c].x += ak[kk][c].x * w; acc[c].y += ak[kk][c].y * w; acc[c].z += ak[kk][c].z * w;
-        acc[c].w += ak[kk][c].w * w;
-      }
-    }
+  }
   }
 #pragma unroll
   for (int c = 0; c < PER; ++c) {
@@ -239,7 +258,10 @@ __global__ void __launch_bounds__(256) attend_merge_few_kernel(AttendParams p, i
 // Merge of the split records + gate; trailing CTAs commit the chunk. With
 // `wide`, one CTA per output row whose 8 warps share the splits (calls with
 // many splits per row); otherwise one warp per output row.
-template <int HD>
+// BATCH: the splits' numerators are loaded many at a time (calls with more than
+// kMergeFewSplits splits, which have few rows); without it the kernel keeps far
+// fewer registers, so that calls with many rows keep more CTAs resident.
+template <int HD, bool BATCH>
 __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int out_blocks, int wide) {
   pdl_trigger();
   pdl_wait();
@@ -248,7 +270,7 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
     return;
   }
   if (wide) {
-    merge_row_wide<HD>(p, blockIdx.x);
+    merge_row_wide<HD, BATCH>(p, blockIdx.x);
     return;
   }
   // ---- one warp per output row (b, r, h): lane s of each group of 32 splits
@@ -320,32 +342,48 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
       }
       k = 1;
     }
-    // up to 16 splits' numerators in flight at once (a runtime trip count let the
-    // compiler keep only a few loads ahead)
-    constexpr int KB = 16;
-    for (; k < cnt; k += KB) {
-      float4 ak[KB][PER];
+    if constexpr (BATCH) {
+      // up to 16 splits' numerators in flight at once (a runtime trip count let the
+      // compiler keep only a few loads ahead)
+      constexpr int KB = 16;
+      for (; k < cnt; k += KB) {
+        float4 ak[KB][PER];
 #pragma unroll
-      for (int kk = 0; kk < KB; ++kk) {
-        const float* src = p.ws_acc + ((item0 + s0 + k + kk) * p.nq + q) * (size_t)HD;
-#pragma unroll
-        for (int c = 0; c < PER; ++c) {
-          const int d4 = c * 32 + lane;
-          ak[kk][c] = (k + kk < cnt && d4 < D4) ? *reinterpret_cast<const float4*>(src + d4 * 4)
-                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-#pragma unroll
-      for (int kk = 0; kk < KB; ++kk) {
-        const float wk = __shfl_sync(0xffffffffu, w, (k + kk) & 31);
-        if (k + kk < cnt) {
+        for (int kk = 0; kk < KB; ++kk) {
+          const float* src = p.ws_acc + ((item0 + s0 + k + kk) * p.nq + q) * (size_t)HD;
 #pragma unroll
           for (int c = 0; c < PER; ++c) {
-            acc[c].x += ak[kk][c].x * wk; acc[c].y += ak[kk][c].y * wk;
-            acc[c].z += ak[kk][c].z * wk; acc[c].w += ak[kk][c].w * wk;
+            const int d4 = c * 32 + lane;
+            ak[kk][c] = (k + kk < cnt && d4 < D4) ? *reinterpret_cast<const float4*>(src + d4 * 4)
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+          const float wk = __shfl_sync(0xffffffffu, w, (k + kk) & 31);
+          if (k + kk < cnt) {
+#pragma unroll
+            for (int c = 0; c < PER; ++c) {
+              acc[c].x += ak[kk][c].x * wk; acc[c].y += ak[kk][c].y * wk;
+              acc[c].z += ak[kk][c].z * wk; acc[c].w += ak[kk][c].w * wk;
+            }
           }
         }
       }
+    } else {
+#pragma unroll 4
+      for (; k < cnt; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        const float* src = p.ws_acc + ((item0 + s0 + k) * p.nq + q) * (size_t)HD;
+#pragma unroll
+        for (int c = 0; c < PER; ++c) {
+          const int d4 = c * 32 + lane;
+          if (d4 < D4) {
+            const float4 a = *reinterpret_cast<const float4*>(src + d4 * 4);
+            acc[c].x += a.x * wk; acc[c].y += a.y * wk; acc[c].z += a.z * wk; acc[c].w += a.w * wk;
+          }
+        }
+    }
     }
   }
 #pragma unroll
@@ -417,12 +455,15 @@ int launch_attend_merge(const AttendParams& p, cudaStream_t s) {
   const int wide = p.splits >= 16 ? 1 : 0;
   const int out_blocks = wide ? (int)rows : (int)((rows + block / 32 - 1) / (block / 32));
   const int grid = out_blocks + commit_ctas;
+  const bool batch = p.splits > kMergeFewSplits;
+#define SWA_MERGE(HDV) case HDV: \
+    return finish_launch(batch ? launch_pdl(attend_merge_kernel<HDV, true>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide) \
+                               : launch_pdl(attend_merge_kernel<HDV, false>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
   switch (p.hd) {
-    case 64: return finish_launch(launch_pdl(attend_merge_kernel<64>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
-    case 128: return finish_launch(launch_pdl(attend_merge_kernel<128>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
-    case 256: return finish_launch(launch_pdl(attend_merge_kernel<256>, dim3(grid), dim3(block), 0, s, p, out_blocks, wide));
+    SWA_MERGE(64) SWA_MERGE(128) SWA_MERGE(256)
     default: return SWA_E_SHAPE;
   }
+#undef SWA_MERGE
 }
 
 }  // namespace swa
