@@ -108,7 +108,7 @@ __device__ void merge_row_wide(const AttendParams& p, unsigned blk) {
           acc[c].x += a.x * w; acc[c].y += a.y * w; acc[c].z += a.z * w; acc[c].w += a.w * w;
         }
       }
-  }
+    }
   }
 #pragma unroll
   for (int c = 0; c < PER; ++c) {
@@ -383,7 +383,7 @@ __global__ void __launch_bounds__(256) attend_merge_kernel(AttendParams p, int o
             acc[c].x += a.x * wk; acc[c].y += a.y * wk; acc[c].z += a.z * wk; acc[c].w += a.w * wk;
           }
         }
-    }
+      }
     }
   }
 #pragma unroll
